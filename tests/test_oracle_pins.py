@@ -1,0 +1,370 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each building block is checked against a library routine (PyTorch / NumPy in
+fp64), a closed form, or a worked example derived by hand
+(tests/golden/hand_examples.json); the composed model is checked against an
+fp64 PyTorch composition of library routines (rms_norm,
+scaled_dot_product_attention with grouped-query heads, silu, matmul) with
+RoPE written as complex multiplication; and the batching semantics are
+checked by the invariants the pages state for the path (batched == solo,
+segmented == per-sequence, no cross-segment leakage).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+import synth
+from synth.recipes import ModelShape, TINY
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "hand_examples.json")))
+
+
+def bf16_bits(x):
+    return torch.tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def f32(bits):
+    return synth.bf16_to_f32(np.asarray(bits, dtype=np.uint16))
+
+
+# ---- bf16 rounding -------------------------------------------------------------------
+def test_bf16_round_matches_torch():
+    rng = np.random.default_rng(0)
+    x = np.concatenate([rng.standard_normal(5000).astype(np.float32) * 3,
+                        np.array([0.0, -0.0, 1.0, 1.00390625, 1.01171875, 65504.0, 1e-40, -2.5e-39],
+                                 dtype=np.float32)])
+    # exact ties: 1 + 2^-8 (tie, even -> 1.0) and 1 + 3*2^-8 (tie, odd -> up)
+    ours = oracle.bf16_round(x)
+    assert np.array_equal(ours, bf16_bits(x))
+
+
+# ---- RMSNorm ----------------------------------------------------------------------------
+def test_rmsnorm_matches_library():
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal(257).astype(np.float32) * 2
+    g = bf16_bits(1 + 0.1 * rng.standard_normal(257))
+    got = oracle.rmsnorm(x, g, 1e-6)
+    ref = F.rms_norm(torch.tensor(x, dtype=torch.float64), (257,),
+                     weight=torch.tensor(f32(g), dtype=torch.float64), eps=1e-6).numpy()
+    np.testing.assert_allclose(got, ref, rtol=2e-7, atol=1e-7)
+
+
+def test_rmsnorm_hand_example_and_constant_input():
+    ex = GOLD["rmsnorm_3_4"]
+    got = oracle.rmsnorm(np.array(ex["x"], np.float32), bf16_bits(ex["gain"]), ex["eps"])
+    np.testing.assert_allclose(got, ex["out"], rtol=1e-7)
+    # constant input c gives sign(c) * g * |c| / sqrt(c^2 + eps)
+    c, eps = -0.75, 1e-5
+    got = oracle.rmsnorm(np.full(64, c, np.float32), bf16_bits(np.full(64, 1.5)), eps)
+    np.testing.assert_allclose(got, np.full(64, -1.5 * 0.75 / math.sqrt(0.5625 + eps)), rtol=1e-7)
+
+
+# ---- RoPE -------------------------------------------------------------------------------
+def rope_complex(v, pos, theta):
+    """RoPE as complex multiplication: z_i = v[i] + 1j*v[i+hd/2] times exp(1j*pos*theta^(-2i/hd))."""
+    hd = v.size
+    half = hd // 2
+    z = v[:half].astype(np.float64) + 1j * v[half:].astype(np.float64)
+    w = np.exp(1j * pos * theta ** (-2.0 * np.arange(half) / hd))
+    r = z * w
+    return np.concatenate([r.real, r.imag])
+
+
+def test_rope_hand_example():
+    ex = GOLD["rope_quarter_turn"]
+    got = oracle.rope(np.array(ex["x"], np.float32), ex["pos"], ex["theta"])
+    np.testing.assert_allclose(got, ex["out"], atol=1e-7)
+
+
+@pytest.mark.parametrize("hd,theta", [(64, 1e4), (128, 1e6)])
+def test_rope_properties(hd, theta):
+    rng = np.random.default_rng(hd)
+    q = rng.standard_normal(hd).astype(np.float32)
+    k = rng.standard_normal(hd).astype(np.float32)
+    # identity at position 0
+    assert np.array_equal(oracle.rope(q, 0, theta), q)
+    for pos in (1, 7, 511, 16383):
+        r = oracle.rope(q, pos, theta)
+        # complex-multiplication form (pairs i, i+hd/2; positive rotation)
+        np.testing.assert_allclose(r, rope_complex(q, pos, theta), atol=3e-6)
+        # each pair keeps its norm
+        half = hd // 2
+        np.testing.assert_allclose(np.hypot(r[:half], r[half:]), np.hypot(q[:half], q[half:]),
+                                   rtol=1e-6)
+    # q(p) . k(p') depends only on p - p'
+    d1 = float(np.dot(oracle.rope(q, 100, theta).astype(np.float64), oracle.rope(k, 90, theta)))
+    d2 = float(np.dot(oracle.rope(q, 1010, theta).astype(np.float64), oracle.rope(k, 1000, theta)))
+    assert abs(d1 - d2) < 1e-4 * max(1.0, abs(d1))
+
+
+# ---- attention ----------------------------------------------------------------------------
+def test_attention_hand_example():
+    ex = GOLD["attention_two_keys"]
+    got = oracle.attention(np.array(ex["q"], np.float32), bf16_bits(ex["k"]), bf16_bits(ex["v"]))
+    np.testing.assert_allclose(got, ex["out"], rtol=1e-6)
+
+
+@pytest.mark.parametrize("hd,n", [(4, 1), (4, 5), (8, 3), (64, 37), (128, 300)])
+def test_attention_matches_library(hd, n):
+    rng = np.random.default_rng(hd * 1000 + n)
+    q = (rng.standard_normal(hd) * 1.3).astype(np.float32)
+    kb = bf16_bits(rng.standard_normal((n, hd)) * 1.3)
+    vb = bf16_bits(rng.standard_normal((n, hd)))
+    got = oracle.attention(q, kb, vb)
+    t = lambda a: torch.tensor(a, dtype=torch.float64)[None, None]
+    ref = F.scaled_dot_product_attention(t(q[None]), t(f32(kb)), t(f32(vb)))[0, 0, 0].numpy()
+    np.testing.assert_allclose(got, ref, rtol=1e-6, atol=1e-7)
+
+
+def test_attention_special_cases():
+    rng = np.random.default_rng(3)
+    vb = bf16_bits(rng.standard_normal((6, 8)))
+    kb = bf16_bits(rng.standard_normal((6, 8)))
+    # a single key returns its value exactly
+    np.testing.assert_array_equal(oracle.attention(rng.standard_normal(8).astype(np.float32), kb[:1], vb[:1]), f32(vb[0]))
+    # q = 0 gives the mean of the values
+    np.testing.assert_allclose(oracle.attention(np.zeros(8, np.float32), kb, vb),
+                               f32(vb).astype(np.float64).mean(0), rtol=1e-6, atol=1e-7)
+
+
+# ---- SiLU, argmax ----------------------------------------------------------------------------
+def test_silu_matches_library():
+    for z in (-30.0, -2.5, -1e-3, 0.0, 0.7, 4.0, 30.0):
+        assert abs(oracle.silu(z) - F.silu(torch.tensor(z, dtype=torch.float64)).item()) < 1e-15
+
+
+def test_argmax_lowest_index_on_ties():
+    lg = np.array([0.1, 0.7, -3, 0.7, 0.2, 0.7], np.float32)
+    assert oracle.argmax(lg) == 1
+    rng = np.random.default_rng(5)
+    for _ in range(20):
+        lg = np.round(rng.standard_normal(1000), 1).astype(np.float32)  # many ties
+        assert oracle.argmax(lg) == int(np.argmax(lg))  # numpy returns the first maximum
+
+
+# ---- projections --------------------------------------------------------------------------
+@pytest.mark.parametrize("fmt", ["bf16", "affine4"])
+def test_linear_matches_matmul(fmt):
+    s = ModelShape("lin", 1, 128, 2, 2, 64, 192, 10, 1e-6, 1e4, weight_format=fmt)
+    rng = np.random.default_rng(7)
+    wb = bf16_bits(rng.standard_normal((96, 192)) * 0.02)
+    lin = oracle.LinearW(wb, fmt, 64)
+    m = oracle.OracleModel.__new__(oracle.OracleModel)
+    m.shape = s
+    m.cfg = oracle.Config(1, 128, 2, 2, 64, 192, 10, 1e-6, 1e4, 0 if fmt == "bf16" else 1, 64)
+    x = rng.standard_normal((5, 192)).astype(np.float32)
+    y = m.linear(lin, x)
+    W = f32(wb).astype(np.float64) if fmt == "bf16" else oracle.dequantize_affine4(
+        lin.packed, lin.scales, lin.biases, 64)
+    np.testing.assert_allclose(y, x.astype(np.float64) @ W.T, rtol=1e-6, atol=1e-6)
+
+
+# ---- 4-bit affine quantiser ---------------------------------------------------------------------
+def test_affine4_hand_example():
+    ex = GOLD["affine4_group"]
+    w = np.array([-0.5 + i / 64 if i < 16 else 0.25 for i in range(64)], np.float32)
+    wb = bf16_bits(w)[None, :]
+    packed, scales, biases = oracle.quantize_affine4(wb, 64)
+    assert f32(scales)[0, 0] == ex["scale_bf16_value"]
+    assert f32(biases)[0, 0] == ex["bias_value"]
+    codes = [(int(packed[0, i // 8]) >> (4 * (i % 8))) & 0xF for i in range(64)]
+    assert codes[0] == ex["code_0"] and codes[8] == ex["code_8"] and codes[16] == ex["code_16"]
+    assert int(packed[0, 2]) == ex["word_2"]
+
+
+def test_affine4_round_trip_bound():
+    rng = np.random.default_rng(11)
+    wb = bf16_bits(rng.standard_normal((64, 256)) * 0.02)
+    packed, scales, biases = oracle.quantize_affine4(wb, 64)
+    deq = oracle.dequantize_affine4(packed, scales, biases, 64)
+    w = f32(wb).astype(np.float64)
+    sc = np.repeat(f32(scales).astype(np.float64), 64, axis=1)
+    # |dequant - w| <= scale/2, plus the slack from rounding scale to bf16 (<= 15 * 2^-9 * scale)
+    assert np.all(np.abs(deq - w) <= sc * (0.5 + 15 * 2.0 ** -9) + 1e-12)
+    codes = np.stack([(packed >> np.uint32(4 * k)) & np.uint32(0xF) for k in range(8)], -1).reshape(64, 256)
+    g = w.reshape(64, 4, 64)
+    cg = codes.reshape(64, 4, 64)
+    # each group's minimum maps to 0 and its maximum to 15
+    assert np.all(cg[np.arange(64)[:, None], np.arange(4)[None], g.argmin(-1)] == 0)
+    assert np.all(cg[np.arange(64)[:, None], np.arange(4)[None], g.argmax(-1)] == 15)
+
+
+# ---- the composed model against an fp64 PyTorch composition of library routines -------------
+PIN_SHAPE = ModelShape("pin-gqa", 2, 128, 4, 2, 32, 256, 300, 1e-6, 1e4, gain_sigma=0.1)
+
+
+def torch_reference_logits(m: oracle.OracleModel, tokens):
+    """fp64 PyTorch forward of one sequence, all positions; K/V rounded to bf16 as cached."""
+    s = m.shape
+    dt = torch.float64
+
+    def W(lin):
+        if lin.w is not None:
+            return torch.tensor(f32(lin.w), dtype=dt)
+        return torch.tensor(oracle.dequantize_affine4(lin.packed, lin.scales, lin.biases, s.group_size), dtype=dt)
+
+    def g(bits):
+        return torch.tensor(f32(bits), dtype=dt)
+
+    def rope(t, pos):  # t: [T, H, hd]
+        half = s.head_dim // 2
+        z = torch.complex(t[..., :half], t[..., half:])
+        ang = pos[:, None, None] * s.rope_theta ** (-2.0 * torch.arange(half, dtype=dt) / s.head_dim)
+        r = z * torch.polar(torch.ones_like(ang), ang)
+        return torch.cat([r.real, r.imag], -1)
+
+    T = len(tokens)
+    pos = torch.arange(T, dtype=dt)
+    x = torch.tensor(f32(m.embed[np.asarray(tokens)]), dtype=dt)
+    for L in m.layers:
+        h = F.rms_norm(x, (s.d_model,), weight=g(L["attn_norm"]), eps=s.rms_eps)
+        q = rope((h @ W(L["wq"]).T).view(T, s.n_heads, s.head_dim), pos)
+        k = rope((h @ W(L["wk"]).T).view(T, s.n_kv_heads, s.head_dim), pos)
+        v = (h @ W(L["wv"]).T).view(T, s.n_kv_heads, s.head_dim)
+        k = k.float().to(torch.bfloat16).to(dt)
+        v = v.float().to(torch.bfloat16).to(dt)
+        o = F.scaled_dot_product_attention(q.transpose(0, 1)[None], k.transpose(0, 1)[None],
+                                           v.transpose(0, 1)[None], is_causal=True,
+                                           enable_gqa=True)[0].transpose(0, 1).reshape(T, -1)
+        x = x + o @ W(L["wo"]).T
+        h = F.rms_norm(x, (s.d_model,), weight=g(L["ffn_norm"]), eps=s.rms_eps)
+        x = x + (F.silu(h @ W(L["wg"]).T) * (h @ W(L["wu"]).T)) @ W(L["wd"]).T
+    h = F.rms_norm(x, (s.d_model,), weight=g(m.final_norm), eps=s.rms_eps)
+    return (h @ W(m.lm_head).T).numpy()
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "affine4"])
+def test_model_matches_torch_composition(fmt):
+    from dataclasses import replace
+    m = oracle.OracleModel(replace(PIN_SHAPE, weight_format=fmt))
+    toks = synth.tokens(23, 9, synth.stream_tokens(0), PIN_SHAPE.vocab)
+    ref = torch_reference_logits(m, toks)
+    # every position's logits: prefill of the first p+1 tokens, last logits
+    cache = oracle.KVCache(m.shape, 32)
+    got_last = oracle.prefill_sequence(m, cache, toks)
+    np.testing.assert_allclose(got_last, ref[-1], atol=2e-5)
+    # token by token through decode steps
+    c2 = oracle.KVCache(m.shape, 32)
+    for p, t in enumerate(toks):
+        lg = oracle.decode_step_batch(m, [c2], [t])[0]
+        np.testing.assert_allclose(lg, ref[p], atol=2e-5)
+
+
+# ---- batching invariants (the pages' parity gates) ----------------------------------------------
+@pytest.fixture(scope="module")
+def pin_model():
+    return oracle.OracleModel(PIN_SHAPE)
+
+
+def _prefilled(m, lens, cap=48, seed=4):
+    caches, toks = [], []
+    for r, n in enumerate(lens):
+        t = synth.tokens(n, seed, synth.stream_tokens(r), m.shape.vocab)
+        c = oracle.KVCache(m.shape, cap)
+        oracle.prefill_sequence(m, c, t)
+        caches.append(c)
+        toks.append(t)
+    return caches, toks
+
+
+def _clone(c):
+    d = oracle.KVCache(c.shape, c.capacity)
+    d.k[...] = c.k
+    d.v[...] = c.v
+    d.len = c.len
+    return d
+
+
+def test_batched_decode_equals_solo(pin_model):
+    caches, _ = _prefilled(pin_model, [3, 11, 7])
+    solo = [_clone(c) for c in caches]
+    last = [5, 17, 250]
+    lg = oracle.decode_step_batch(pin_model, caches, last)
+    for b in range(3):
+        lb = oracle.decode_step_batch(pin_model, [solo[b]], [last[b]])[0]
+        assert np.array_equal(lg[b], lb)
+        assert np.array_equal(caches[b].k, solo[b].k) and np.array_equal(caches[b].v, solo[b].v)
+        assert caches[b].len == solo[b].len
+
+
+def test_segmented_equals_per_sequence(pin_model):
+    lens = [5, 17, 1, 9]
+    toks = [synth.tokens(n, 6, synth.stream_tokens(r), PIN_SHAPE.vocab) for r, n in enumerate(lens)]
+    seg = [oracle.KVCache(PIN_SHAPE, 32) for _ in lens]
+    lg = oracle.prefill_segmented(pin_model, seg, lens, np.concatenate(toks))
+    for r, n in enumerate(lens):
+        c = oracle.KVCache(PIN_SHAPE, 32)
+        ls = oracle.prefill_sequence(pin_model, c, toks[r])
+        assert np.array_equal(lg[r], ls)
+        assert np.array_equal(seg[r].k, c.k) and np.array_equal(seg[r].v, c.v) and seg[r].len == n
+
+
+def test_no_cross_row_leakage(pin_model):
+    caches, _ = _prefilled(pin_model, [6, 6, 6])
+    other = [_clone(c) for c in caches]
+    other[1].k[:, :, :6] ^= np.uint16(0x0040)  # perturb every cached K value of row 1
+    last = [1, 2, 3]
+    a = oracle.decode_step_batch(pin_model, caches, last)
+    b = oracle.decode_step_batch(pin_model, other, last)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[2], b[2])
+    assert not np.array_equal(a[1], b[1])
+    # segmented prefill: a different token in segment 1 changes no other segment
+    lens = [4, 4, 4]
+    t = synth.tokens(12, 8, synth.stream_tokens(0), PIN_SHAPE.vocab)
+    t2 = t.copy()
+    t2[5] = (t2[5] + 1) % PIN_SHAPE.vocab
+    l1 = oracle.prefill_segmented(pin_model, [oracle.KVCache(PIN_SHAPE, 8) for _ in lens], lens, t)
+    l2 = oracle.prefill_segmented(pin_model, [oracle.KVCache(PIN_SHAPE, 8) for _ in lens], lens, t2)
+    assert np.array_equal(l1[0], l2[0]) and np.array_equal(l1[2], l2[2])
+    assert not np.array_equal(l1[1], l2[1])
+
+
+def test_prefill_then_decode_equals_longer_prefill(pin_model):
+    t = synth.tokens(13, 12, synth.stream_tokens(0), PIN_SHAPE.vocab)
+    c = oracle.KVCache(PIN_SHAPE, 16)
+    oracle.prefill_sequence(pin_model, c, t[:12])
+    lg = oracle.decode_step_batch(pin_model, [c], [t[12]])[0]
+    c2 = oracle.KVCache(PIN_SHAPE, 16)
+    ref = oracle.prefill_sequence(pin_model, c2, t)
+    np.testing.assert_allclose(lg, ref, atol=1e-6)
+
+
+def test_row_permutation(pin_model):
+    caches, _ = _prefilled(pin_model, [2, 9, 4, 7])
+    perm = [2, 0, 3, 1]
+    last = np.array([10, 20, 30, 40])
+    pc = [_clone(caches[i]) for i in perm]
+    a = oracle.decode_step_batch(pin_model, caches, last)
+    b = oracle.decode_step_batch(pin_model, pc, last[perm])
+    assert np.array_equal(a[perm], b)
+
+
+def test_rejects_bad_token_lists(pin_model):
+    c = oracle.KVCache(PIN_SHAPE, 4)
+    with pytest.raises(ValueError):  # token id out of range
+        oracle.decode_step_batch(pin_model, [c], [PIN_SHAPE.vocab])
+    with pytest.raises(ValueError):  # capacity exceeded
+        oracle.prefill_sequence(pin_model, c, np.zeros(5, np.int32))
+
+
+# ---- the seeded generator -------------------------------------------------------------------------
+def test_synth_deterministic_and_normal():
+    a = synth.normal_bf16(200000, 0, 77, sigma=1.0)
+    b = synth.normal_bf16(200000, 0, 77, sigma=1.0)
+    assert np.array_equal(a, b)
+    x = f32(a).astype(np.float64)
+    assert abs(x.mean()) < 0.01 and abs(x.std() - 1.0) < 0.01
+    # sub-range fills agree with the whole (counter based)
+    c = synth.normal_bf16(1000, 0, 77, first=5000, sigma=1.0)
+    assert np.array_equal(c, a[5000:6000])
+    t = synth.tokens(100000, 0, 3, 1024)
+    assert t.min() >= 0 and t.max() < 1024 and abs(t.mean() - 511.5) < 5
+    k1 = synth.kv(0, 0, 2, 4, 9, 64, 0, 0.32)
+    k2 = synth.kv(0, 0, 2, 4, 5, 64, 0, 0.32)
+    assert np.array_equal(k1[:, :, :5], k2)  # KV draws do not depend on the context length
