@@ -1,0 +1,299 @@
+// basic.cu -- the step's small kernels: embedding, RMSNorm, RoPE tables, RoPE + KV append,
+// plain per-token attention, greedy argmax, row gather and the 4-bit quantiser.
+#include <math.h>
+
+#include "kernels.h"
+
+// ---- embedding: x[i] = E[token[i]] (fp32); out-of-range ids set the error word ------------
+__global__ void k_embed(const int32_t* tokens, int d, int vocab, const uint16_t* table, float* x,
+                        int* err) {
+  int i = blockIdx.x;
+  int t = tokens[i];
+  float* xr = x + (size_t)i * d;
+  if (t < 0 || t >= vocab) {
+    if (threadIdx.x == 0) set_device_error(err, CBT_DEV_TOKEN_RANGE, i);
+    for (int j = threadIdx.x; j < d; j += blockDim.x) xr[j] = 0.f;
+    return;
+  }
+  const uint16_t* er = table + (size_t)t * d;
+  for (int j = threadIdx.x; j < d; j += blockDim.x) xr[j] = bf16_to_f32(er[j]);
+}
+
+void launch_embed(const int32_t* tokens, int n, const uint16_t* table, int d, int vocab, float* x,
+                  int* err, cudaStream_t s) {
+  if (n <= 0) return;
+  count_launch();
+  k_embed<<<n, 256, 0, s>>>(tokens, d, vocab, table, x, err);
+}
+
+// ---- RMSNorm: h = x / sqrt(mean(x^2) + eps) * g -----------------------------------------
+__global__ void k_rmsnorm(const float* x, const uint16_t* gain, int d, float eps, float* h) {
+  __shared__ float red[32];
+  const float* xr = x + (size_t)blockIdx.x * d;
+  float ss = 0.f;
+  for (int j = threadIdx.x; j < d; j += blockDim.x) ss = fmaf(xr[j], xr[j], ss);
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+    v = warp_sum(v);
+    if (threadIdx.x == 0) red[0] = v;
+  }
+  __syncthreads();
+  float r = rsqrtf(red[0] / (float)d + eps);
+  float* hr = h + (size_t)blockIdx.x * d;
+  for (int j = threadIdx.x; j < d; j += blockDim.x) hr[j] = xr[j] * r * bf16_to_f32(gain[j]);
+}
+
+void launch_rmsnorm(const float* x, const uint16_t* gain, int n, int d, float eps, float* h,
+                    cudaStream_t s) {
+  if (n <= 0) return;
+  count_launch();
+  k_rmsnorm<<<n, 256, 0, s>>>(x, gain, d, eps, h);
+}
+
+// ---- RoPE angles once per call: cos/sin of pos * theta^(-2i/hd), evaluated in double -------
+__global__ void k_rope_table(const QueryRow* rows, int n, int half, int head_dim, double theta,
+                             float* cosv, float* sinv) {
+  int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= n * half) return;
+  int t = idx / half, i = idx % half;
+  double freq = pow(theta, -2.0 * (double)i / (double)head_dim);
+  double ang = (double)rows[t].pos * freq;
+  double sv, cv;
+  sincos(ang, &sv, &cv);
+  cosv[idx] = (float)cv;
+  sinv[idx] = (float)sv;
+}
+
+void launch_rope_table(const QueryRow* rows, int n, int head_dim, double theta, float* cosv,
+                       float* sinv, cudaStream_t s) {
+  int half = head_dim / 2;
+  int tot = n * half;
+  if (tot <= 0) return;
+  count_launch();
+  k_rope_table<<<(tot + 255) / 256, 256, 0, s>>>(rows, n, half, head_dim, theta, cosv, sinv);
+}
+
+// ---- RoPE q, k in place at the token's position; append k, v to its own slab at pos ------
+__global__ void k_rope_append(float* qkv, const QueryRow* rows, int layer, int n_heads,
+                              int n_kv_heads, int head_dim, const float* cosv, const float* sinv,
+                              uint16_t* arena) {
+  int t = blockIdx.x;
+  int half = head_dim / 2;
+  int qd = n_heads * head_dim, kvd = n_kv_heads * head_dim;
+  float* row = qkv + (size_t)t * (qd + 2 * kvd);
+  const float* cr = cosv + (size_t)t * half;
+  const float* sr = sinv + (size_t)t * half;
+  QueryRow r = rows[t];
+  int pairs = (n_heads + n_kv_heads) * half;
+  for (int p = threadIdx.x; p < pairs; p += blockDim.x) {
+    int h = p / half, i = p % half;
+    float* v = row + (size_t)h * head_dim;  // q heads then k heads are contiguous
+    float a = v[i], b = v[i + half], c = cr[i], s = sr[i];
+    float ra = a * c - b * s;
+    float rb = a * s + b * c;
+    v[i] = ra;
+    v[i + half] = rb;
+    if (h >= n_heads) {
+      uint16_t* kd = arena + kv_offset(r, layer, 0, h - n_heads, n_kv_heads, head_dim);
+      kd[i] = f32_to_bf16(ra);
+      kd[i + half] = f32_to_bf16(rb);
+    }
+  }
+  const float* vv = row + qd + kvd;
+  for (int e = threadIdx.x; e < kvd; e += blockDim.x) {
+    int g = e / head_dim, j = e % head_dim;
+    arena[kv_offset(r, layer, 1, g, n_kv_heads, head_dim) + j] = f32_to_bf16(vv[e]);
+  }
+}
+
+void launch_rope_append(float* qkv, const QueryRow* rows, int n, int layer, int n_heads,
+                        int n_kv_heads, int head_dim, const float* cosv, const float* sinv,
+                        uint16_t* arena, cudaStream_t s) {
+  if (n <= 0) return;
+  count_launch();
+  k_rope_append<<<n, 256, 0, s>>>(qkv, rows, layer, n_heads, n_kv_heads, head_dim, cosv, sinv,
+                                  arena);
+}
+
+// ---- plain attention: one block per (token, q head), keys [0, pos] of its own slab -------
+__global__ void k_attention_naive(const float* qkv, const QueryRow* rows, int layer, int n_heads,
+                                  int n_kv_heads, int head_dim, const uint16_t* arena, float* o) {
+  extern __shared__ float sm[];
+  __shared__ float red[32];
+  int t = blockIdx.x, hq = blockIdx.y;
+  int qd = n_heads * head_dim, kvd = n_kv_heads * head_dim;
+  int g = hq / (n_heads / n_kv_heads);
+  QueryRow r = rows[t];
+  int nk = r.pos + 1;
+  float* qs = sm;              // head_dim
+  float* sc = sm + head_dim;   // nk scores
+  const float* q = qkv + (size_t)t * (qd + 2 * kvd) + (size_t)hq * head_dim;
+  for (int j = threadIdx.x; j < head_dim; j += blockDim.x) qs[j] = q[j];
+  __syncthreads();
+  QueryRow r0 = r;
+  r0.pos = 0;
+  const uint16_t* K = arena + kv_offset(r0, layer, 0, g, n_kv_heads, head_dim);
+  const uint16_t* V = arena + kv_offset(r0, layer, 1, g, n_kv_heads, head_dim);
+  float scale = rsqrtf((float)head_dim);
+  float mx = -INFINITY;
+  for (int k = threadIdx.x; k < nk; k += blockDim.x) {
+    const uint4* kr = reinterpret_cast<const uint4*>(K + (size_t)k * head_dim);
+    float dot = 0.f;
+    for (int c = 0; c < head_dim / 8; ++c) {
+      uint4 w = kr[c];
+      const float* qq = qs + c * 8;
+      dot = fmaf(qq[0], bf16_lo(w.x), dot); dot = fmaf(qq[1], bf16_hi(w.x), dot);
+      dot = fmaf(qq[2], bf16_lo(w.y), dot); dot = fmaf(qq[3], bf16_hi(w.y), dot);
+      dot = fmaf(qq[4], bf16_lo(w.z), dot); dot = fmaf(qq[5], bf16_hi(w.z), dot);
+      dot = fmaf(qq[6], bf16_lo(w.w), dot); dot = fmaf(qq[7], bf16_hi(w.w), dot);
+    }
+    float sv = dot * scale;
+    sc[k] = sv;
+    mx = fmaxf(mx, sv);
+  }
+  mx = warp_max(mx);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : -INFINITY;
+    v = warp_max(v);
+    if (threadIdx.x == 0) red[0] = v;
+  }
+  __syncthreads();
+  mx = red[0];
+  __syncthreads();
+  float z = 0.f;
+  for (int k = threadIdx.x; k < nk; k += blockDim.x) {
+    float p = expf(sc[k] - mx);
+    sc[k] = p;
+    z += p;
+  }
+  z = warp_sum(z);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = z;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+    v = warp_sum(v);
+    if (threadIdx.x == 0) red[0] = v;
+  }
+  __syncthreads();
+  float inv = 1.f / red[0];
+  float* orow = o + (size_t)t * qd + (size_t)hq * head_dim;
+  for (int j = threadIdx.x; j < head_dim; j += blockDim.x) {
+    float acc = 0.f;
+    for (int k = 0; k < nk; ++k) acc = fmaf(sc[k], bf16_to_f32(V[(size_t)k * head_dim + j]), acc);
+    orow[j] = acc * inv;
+  }
+}
+
+void launch_attention_naive(const float* qkv, const QueryRow* rows, int n, int layer, int n_heads,
+                            int n_kv_heads, int head_dim, int max_keys, const uint16_t* arena,
+                            float* o, cudaStream_t s) {
+  if (n <= 0) return;
+  size_t smem = sizeof(float) * (size_t)(head_dim + max_keys);
+  if (smem > 48 * 1024)
+    cudaFuncSetAttribute(k_attention_naive, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  count_launch();
+  k_attention_naive<<<dim3(n, n_heads), 128, smem, s>>>(qkv, rows, layer, n_heads, n_kv_heads,
+                                                         head_dim, arena, o);
+}
+
+// ---- greedy argmax, lowest index among equal maxima ----------------------------------------
+__global__ void k_argmax(const float* logits, int vocab, int32_t* out) {
+  __shared__ float bv[32];
+  __shared__ int bi[32];
+  const float* r = logits + (size_t)blockIdx.x * vocab;
+  float best = -INFINITY;
+  int idx = 0x7fffffff;
+  for (int i = threadIdx.x; i < vocab; i += blockDim.x) {
+    float v = r[i];
+    if (v > best) { best = v; idx = i; }  // strided scan: earlier index kept on ties
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    float ov = __shfl_xor_sync(0xffffffffu, best, off);
+    int oi = __shfl_xor_sync(0xffffffffu, idx, off);
+    if (ov > best || (ov == best && oi < idx)) { best = ov; idx = oi; }
+  }
+  if ((threadIdx.x & 31) == 0) { bv[threadIdx.x >> 5] = best; bi[threadIdx.x >> 5] = idx; }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    int nw = blockDim.x >> 5;
+    best = threadIdx.x < nw ? bv[threadIdx.x] : -INFINITY;
+    idx = threadIdx.x < nw ? bi[threadIdx.x] : 0x7fffffff;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      float ov = __shfl_xor_sync(0xffffffffu, best, off);
+      int oi = __shfl_xor_sync(0xffffffffu, idx, off);
+      if (ov > best || (ov == best && oi < idx)) { best = ov; idx = oi; }
+    }
+    if (threadIdx.x == 0) out[blockIdx.x] = idx == 0x7fffffff ? 0 : idx;
+  }
+}
+
+void launch_argmax(const float* logits, int n, int vocab, int32_t* out, cudaStream_t s) {
+  if (n <= 0) return;
+  count_launch();
+  k_argmax<<<n, 512, 0, s>>>(logits, vocab, out);
+}
+
+__global__ void k_gather_rows(const float* src, const int32_t* idx, int d, float* dst) {
+  const float* sr = src + (size_t)idx[blockIdx.x] * d;
+  float* dr = dst + (size_t)blockIdx.x * d;
+  for (int j = threadIdx.x; j < d; j += blockDim.x) dr[j] = sr[j];
+}
+
+void launch_gather_rows(const float* src, const int32_t* idx, int n, int d, float* dst,
+                        cudaStream_t s) {
+  if (n <= 0) return;
+  count_launch();
+  k_gather_rows<<<n, 256, 0, s>>>(src, idx, d, dst);
+}
+
+// ---- MLX-style 4-bit affine quantisation, one thread per (row, group) ----------------------
+__global__ void k_quantize_affine4(const uint16_t* w, int rows, int cols, int group,
+                                   uint32_t* packed, uint16_t* scales, uint16_t* biases) {
+  long long gid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  int ng = cols / group;
+  if (gid >= (long long)rows * ng) return;
+  int r = (int)(gid / ng), g = (int)(gid % ng);
+  const uint16_t* src = w + (size_t)r * cols + (size_t)g * group;
+  float mn = bf16_to_f32(src[0]), mx = mn;
+  for (int i = 1; i < group; ++i) {
+    float x = bf16_to_f32(src[i]);
+    mn = fminf(mn, x);
+    mx = fmaxf(mx, x);
+  }
+  // (mx - mn) is exact in double; divide, round to float, then to bf16
+  uint16_t sb = f32_to_bf16((float)(((double)mx - (double)mn) / 15.0));
+  uint16_t bb = f32_to_bf16(mn);
+  double sc = bf16_to_f32(sb), bi = bf16_to_f32(bb);
+  scales[gid] = sb;
+  biases[gid] = bb;
+  uint32_t* dst = packed + (size_t)r * (cols / 8) + (size_t)g * (group / 8);
+  for (int j = 0; j < group / 8; ++j) {
+    uint32_t word = 0;
+    for (int k = 0; k < 8; ++k) {
+      double x = bf16_to_f32(src[8 * j + k]);
+      int q = 0;
+      if (sc != 0.0) {
+        double t = rint((x - bi) / sc);
+        q = t < 0.0 ? 0 : (t > 15.0 ? 15 : (int)t);
+      }
+      word |= (uint32_t)q << (4 * k);
+    }
+    dst[j] = word;
+  }
+}
+
+void launch_quantize_affine4(const uint16_t* w, int rows, int cols, int group, uint32_t* packed,
+                             uint16_t* scales, uint16_t* biases, cudaStream_t s) {
+  long long n = (long long)rows * (cols / group);
+  if (n <= 0) return;
+  count_launch();
+  k_quantize_affine4<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(w, rows, cols, group, packed,
+                                                                 scales, biases);
+}

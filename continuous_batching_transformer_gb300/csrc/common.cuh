@@ -1,0 +1,58 @@
+// common.cuh -- small device helpers shared by the engine's kernels.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "cbt.h"
+
+#define CBT_HD __host__ __device__ __forceinline__
+#define CBT_D __device__ __forceinline__
+
+// bf16 bits <-> fp32.  Widening is exact; narrowing rounds to nearest even.
+CBT_D float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+CBT_D float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+CBT_D float bf16_to_f32(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
+CBT_D uint16_t f32_to_bf16(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7F800000u) == 0x7F800000u) return (uint16_t)((u >> 16) | ((u & 0x7FFFFFu) ? 0x40u : 0u));
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+// Where a decode row or a prefill token reads and writes its KV: the slab's element offset
+// in the arena, the token's position and the slab's capacity.  Slab layout (bf16):
+// [layer][K|V][kv head][position][head_dim].
+struct QueryRow {
+  long long base;  // element offset of the slab in the arena
+  int pos;         // position of this token in its slab
+  int cap;         // slab capacity (positions)
+};
+
+CBT_D long long kv_offset(const QueryRow& r, int layer, int kv, int head, int n_kv_heads,
+                          int head_dim) {
+  return r.base + ((((long long)layer * 2 + kv) * n_kv_heads + head) * r.cap + r.pos) * head_dim;
+}
+
+// Device error word: the first error wins (code, info).
+CBT_D void set_device_error(int* err, int code, int info) {
+  if (atomicCAS(err, 0, code) == 0) err[1] = info;
+}
+
+CBT_D float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+CBT_D float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Epilogues of a projection y = x W^T.
+enum Epilogue : int {
+  EPI_STORE = 0,   // out[n][m] = y
+  EPI_ADD = 1,     // out[n][m] += y (residual)
+  EPI_SWIGLU = 2,  // W = [gate; up] (2F rows): out[n][j] = silu(y_gate[j]) * y_up[j], j < F
+};

@@ -1,0 +1,463 @@
+// engine.cu -- the C ABI: engine state, the slab allocator and the step orchestration.
+//
+// Host side only.  One engine drives one model on one stream.  Slabs are extents of the
+// caller's KV arena handed out by a first-fit allocator with coalescing; each carries its
+// capacity and current position (the host mirror of t_s, bumped as steps are queued).
+// A decode step or a prefill call writes a small per-token row table (slab offset, position,
+// capacity) to the device and then queues the whole forward pass on the engine stream.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <map>
+#include <new>
+#include <unordered_map>
+#include <unordered_set>
+#include <vector>
+
+#include "cbt.h"
+#include "kernels.h"
+
+static std::atomic<long long> g_launches{0};
+long long kernel_launch_count() { return g_launches.load(); }
+void count_launch(int n) { g_launches += n; }
+
+namespace {
+
+constexpr size_t kSlabAlign = 4096;
+
+struct Slab {
+  size_t offset;  // bytes into the arena
+  size_t bytes;
+  int cap;
+  int pos;
+};
+
+template <class T>
+cudaError_t dmalloc(T** p, size_t count, size_t* total) {
+  size_t bytes = sizeof(T) * (count > 0 ? count : 1);
+  bytes = (bytes + 255) & ~size_t(255);
+  *total += bytes;
+  return cudaMalloc(reinterpret_cast<void**>(p), bytes);
+}
+
+}  // namespace
+
+struct cbt_engine {
+  cbt_model_config cfg;
+  std::vector<cbt_layer_weights> layers;
+  cbt_weights w;
+  cbt_engine_params p;
+  cudaStream_t stream = nullptr;
+
+  // allocator
+  std::map<size_t, size_t> free_ext;  // offset -> bytes
+  std::unordered_map<int, Slab> slabs;
+  int next_id = 1;
+  size_t in_use = 0;
+
+  // device scratch
+  int tmax = 0;
+  float *x = nullptr, *h = nullptr, *qkv = nullptr, *o = nullptr, *act = nullptr;
+  float *part = nullptr, *xg = nullptr, *logits = nullptr, *cosv = nullptr, *sinv = nullptr;
+  int32_t *next_tok = nullptr, *last_idx = nullptr;
+  QueryRow* rows = nullptr;
+  int* err = nullptr;
+  size_t part_floats = 0;
+  size_t scratch_bytes = 0;
+
+  std::vector<QueryRow> hrows;
+  std::vector<int32_t> hidx;
+  int64_t steps = 0, prefill_tokens = 0;
+
+  int qd() const { return cfg.n_heads * cfg.head_dim; }
+  int kvd() const { return cfg.n_kv_heads * cfg.head_dim; }
+};
+
+extern "C" const char* cbt_status_str(cbt_status s) {
+  switch (s) {
+    case CBT_OK: return "ok";
+    case CBT_ERR_INVALID: return "invalid argument or configuration";
+    case CBT_ERR_NULL: return "required pointer is NULL";
+    case CBT_ERR_BAD_SLAB: return "unknown or freed slab id";
+    case CBT_ERR_DUP_SLAB: return "slab id repeated in one call";
+    case CBT_ERR_BATCH: return "batch larger than max_batch";
+    case CBT_ERR_CAPACITY: return "slab capacity exceeded";
+    case CBT_ERR_POOL_EXHAUSTED: return "KV arena has no free extent large enough";
+    case CBT_ERR_TOKENS: return "prefill tokens above max_prefill_tokens";
+    case CBT_ERR_CUDA: return "CUDA runtime error";
+    case CBT_ERR_DEVICE: return "device error word set";
+    case CBT_ERR_UNSUPPORTED: return "shape not supported";
+    default: return "unknown status";
+  }
+}
+
+static void free_scratch(cbt_engine* e) {
+  void* ptrs[] = {e->x, e->h, e->qkv, e->o, e->act, e->part, e->xg, e->logits, e->cosv,
+                  e->sinv, e->next_tok, e->last_idx, e->rows, e->err};
+  for (void* q : ptrs)
+    if (q) cudaFree(q);
+}
+
+static bool linear_ok(const cbt_linear& l, int fmt) {
+  if (!l.w) return false;
+  if (fmt == CBT_WEIGHTS_AFFINE4 && (!l.scales || !l.biases)) return false;
+  return true;
+}
+
+extern "C" size_t cbt_slab_bytes(const cbt_model_config* c, int32_t cap) {
+  if (!c || cap <= 0) return 0;
+  size_t b = (size_t)c->n_layers * 2 * c->n_kv_heads * (size_t)cap * c->head_dim * 2;
+  return (b + kSlabAlign - 1) & ~(kSlabAlign - 1);
+}
+
+extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_weights* w,
+                                        const cbt_engine_params* p, cbt_engine** out) {
+  if (!out) return CBT_ERR_NULL;
+  *out = nullptr;
+  if (!cfg || !w || !p || !w->layers || !w->embed || !w->final_norm || !p->kv_arena)
+    return CBT_ERR_NULL;
+  const cbt_model_config& c = *cfg;
+  if (c.n_layers <= 0 || c.d_model <= 0 || c.n_heads <= 0 || c.n_kv_heads <= 0 || c.d_ff <= 0 ||
+      c.vocab <= 0 || c.n_heads % c.n_kv_heads != 0 || !(c.rms_eps >= 0.f) || !(c.rope_theta > 0))
+    return CBT_ERR_INVALID;
+  if (c.weight_format != CBT_WEIGHTS_BF16 && c.weight_format != CBT_WEIGHTS_AFFINE4)
+    return CBT_ERR_INVALID;
+  if (c.weight_format == CBT_WEIGHTS_AFFINE4 && c.group_size != 64) return CBT_ERR_UNSUPPORTED;
+  if (c.head_dim != 64 && c.head_dim != 128) return CBT_ERR_UNSUPPORTED;
+  const int qd = c.n_heads * c.head_dim;
+  if (c.d_model % 256 || qd % 256 || c.d_ff % 256) return CBT_ERR_UNSUPPORTED;
+  if (p->max_batch <= 0 || p->max_prefill_tokens <= 0 || p->kv_arena_bytes < kSlabAlign ||
+      (reinterpret_cast<uintptr_t>(p->kv_arena) & 255))
+    return CBT_ERR_INVALID;
+  if (!linear_ok(w->lm_head, c.weight_format)) return CBT_ERR_NULL;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const cbt_layer_weights& L = w->layers[l];
+    if (!linear_ok(L.wqkv, c.weight_format) || !linear_ok(L.wo, c.weight_format) ||
+        !linear_ok(L.wgu, c.weight_format) || !linear_ok(L.wd, c.weight_format) || !L.attn_norm ||
+        !L.ffn_norm)
+      return CBT_ERR_NULL;
+  }
+
+  cbt_engine* e = new (std::nothrow) cbt_engine();
+  if (!e) return CBT_ERR_INVALID;
+  e->cfg = c;
+  e->layers.assign(w->layers, w->layers + c.n_layers);
+  e->w = *w;
+  e->w.layers = e->layers.data();
+  e->p = *p;
+  e->stream = static_cast<cudaStream_t>(p->stream);
+  e->free_ext[0] = p->kv_arena_bytes & ~(kSlabAlign - 1);
+
+  const int T = std::max(p->max_batch, p->max_prefill_tokens);
+  e->tmax = T;
+  const int kvd = c.n_kv_heads * c.head_dim;
+  const int nqkv = qd + 2 * kvd;
+  const int Mmax = std::max({nqkv, c.d_model, 2 * c.d_ff, c.vocab});
+  int smax = 1;
+  for (int K : {c.d_model, qd, c.d_ff}) {
+    int ks = K % 1024 == 0 ? 1024 : (K % 512 == 0 ? 512 : 256);
+    smax = std::max(smax, K / ks);
+  }
+  e->part_floats = (size_t)smax * std::min(T, 32) * Mmax;
+  size_t tot = 0;
+  cudaError_t rc = cudaSuccess;
+  auto chk = [&](cudaError_t r) { if (rc == cudaSuccess) rc = r; };
+  chk(dmalloc(&e->x, (size_t)T * c.d_model, &tot));
+  chk(dmalloc(&e->h, (size_t)T * std::max(c.d_model, qd), &tot));
+  chk(dmalloc(&e->qkv, (size_t)T * nqkv, &tot));
+  chk(dmalloc(&e->o, (size_t)T * qd, &tot));
+  chk(dmalloc(&e->act, (size_t)T * c.d_ff, &tot));
+  chk(dmalloc(&e->part, e->part_floats, &tot));
+  chk(dmalloc(&e->xg, (size_t)p->max_batch * c.d_model * 2, &tot));
+  chk(dmalloc(&e->logits, (size_t)p->max_batch * c.vocab, &tot));
+  chk(dmalloc(&e->cosv, (size_t)T * c.head_dim / 2, &tot));
+  chk(dmalloc(&e->sinv, (size_t)T * c.head_dim / 2, &tot));
+  chk(dmalloc(&e->next_tok, (size_t)p->max_batch, &tot));
+  chk(dmalloc(&e->last_idx, (size_t)p->max_batch, &tot));
+  chk(dmalloc(&e->rows, (size_t)T, &tot));
+  chk(dmalloc(&e->err, 2, &tot));
+  if (rc == cudaSuccess) rc = cudaMemsetAsync(e->err, 0, 2 * sizeof(int), e->stream);
+  if (rc == cudaSuccess) rc = cudaStreamSynchronize(e->stream);
+  if (rc != cudaSuccess) {
+    free_scratch(e);
+    delete e;
+    return CBT_ERR_CUDA;
+  }
+  e->scratch_bytes = tot;
+  e->hrows.resize(T);
+  e->hidx.resize(p->max_batch);
+  *out = e;
+  return CBT_OK;
+}
+
+extern "C" cbt_status cbt_engine_destroy(cbt_engine* e) {
+  if (!e) return CBT_ERR_NULL;
+  cudaError_t rc = cudaStreamSynchronize(e->stream);
+  free_scratch(e);
+  delete e;
+  return rc == cudaSuccess ? CBT_OK : CBT_ERR_CUDA;
+}
+
+// ---- slab allocator ---------------------------------------------------------------------
+extern "C" cbt_status cbt_kv_slab_alloc(cbt_engine* e, int32_t cap, int32_t* id) {
+  if (!e || !id) return CBT_ERR_NULL;
+  if (cap <= 0) return CBT_ERR_INVALID;
+  size_t need = cbt_slab_bytes(&e->cfg, cap);
+  for (auto it = e->free_ext.begin(); it != e->free_ext.end(); ++it) {
+    if (it->second >= need) {
+      size_t off = it->first, rest = it->second - need;
+      e->free_ext.erase(it);
+      if (rest) e->free_ext[off + need] = rest;
+      int sid = e->next_id++;
+      e->slabs[sid] = Slab{off, need, cap, 0};
+      e->in_use += need;
+      *id = sid;
+      return CBT_OK;
+    }
+  }
+  return CBT_ERR_POOL_EXHAUSTED;
+}
+
+extern "C" cbt_status cbt_kv_slab_free(cbt_engine* e, int32_t id) {
+  if (!e) return CBT_ERR_NULL;
+  auto it = e->slabs.find(id);
+  if (it == e->slabs.end()) return CBT_ERR_BAD_SLAB;
+  size_t off = it->second.offset, bytes = it->second.bytes;
+  e->in_use -= bytes;
+  e->slabs.erase(it);
+  auto nx = e->free_ext.lower_bound(off);
+  if (nx != e->free_ext.end() && off + bytes == nx->first) {  // merge with the next extent
+    bytes += nx->second;
+    nx = e->free_ext.erase(nx);
+  }
+  if (nx != e->free_ext.begin()) {  // merge with the previous extent
+    auto pv = std::prev(nx);
+    if (pv->first + pv->second == off) {
+      pv->second += bytes;
+      return CBT_OK;
+    }
+  }
+  e->free_ext[off] = bytes;
+  return CBT_OK;
+}
+
+extern "C" cbt_status cbt_retire(cbt_engine* e, const int32_t* ids, int32_t n) {
+  if (!e) return CBT_ERR_NULL;
+  if (n < 0) return CBT_ERR_INVALID;
+  if (n > 0 && !ids) return CBT_ERR_NULL;
+  std::unordered_set<int> seen;
+  for (int i = 0; i < n; ++i) {
+    if (!e->slabs.count(ids[i])) return CBT_ERR_BAD_SLAB;
+    if (!seen.insert(ids[i]).second) return CBT_ERR_DUP_SLAB;
+  }
+  for (int i = 0; i < n; ++i) cbt_kv_slab_free(e, ids[i]);
+  return CBT_OK;
+}
+
+extern "C" cbt_status cbt_kv_slab_position(cbt_engine* e, int32_t id, int32_t* pos) {
+  if (!e || !pos) return CBT_ERR_NULL;
+  auto it = e->slabs.find(id);
+  if (it == e->slabs.end()) return CBT_ERR_BAD_SLAB;
+  *pos = it->second.pos;
+  return CBT_OK;
+}
+
+static cbt_status slab_copy(cbt_engine* e, int32_t id, void* k, void* v, int32_t n, int32_t on_host,
+                            bool to_slab) {
+  if (!e || !k || !v) return CBT_ERR_NULL;
+  auto it = e->slabs.find(id);
+  if (it == e->slabs.end()) return CBT_ERR_BAD_SLAB;
+  Slab& s = it->second;
+  if (n < 0) return CBT_ERR_INVALID;
+  if (n > s.cap || (!to_slab && n > s.pos)) return CBT_ERR_CAPACITY;
+  const cbt_model_config& c = e->cfg;
+  const size_t row = (size_t)c.head_dim * 2;
+  char* arena = static_cast<char*>(e->p.kv_arena) + s.offset;
+  cudaMemcpyKind kind = on_host ? (to_slab ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToHost)
+                                : cudaMemcpyDeviceToDevice;
+  cudaError_t rc = cudaSuccess;
+  for (int l = 0; l < c.n_layers && rc == cudaSuccess && n > 0; ++l) {
+    for (int kv = 0; kv < 2 && rc == cudaSuccess; ++kv) {
+      char* user = static_cast<char*>(kv == 0 ? k : v) + (size_t)l * c.n_kv_heads * n * row;
+      char* slab = arena + ((size_t)l * 2 + kv) * c.n_kv_heads * (size_t)s.cap * row;
+      size_t upitch = (size_t)n * row, spitch = (size_t)s.cap * row;
+      if (to_slab)
+        rc = cudaMemcpy2DAsync(slab, spitch, user, upitch, upitch, c.n_kv_heads, kind, e->stream);
+      else
+        rc = cudaMemcpy2DAsync(user, upitch, slab, spitch, upitch, c.n_kv_heads, kind, e->stream);
+    }
+  }
+  if (rc == cudaSuccess && on_host && !to_slab) rc = cudaStreamSynchronize(e->stream);
+  if (rc != cudaSuccess) return CBT_ERR_CUDA;
+  if (to_slab) s.pos = n;
+  return CBT_OK;
+}
+
+extern "C" cbt_status cbt_kv_slab_import(cbt_engine* e, int32_t id, const void* k, const void* v,
+                                         int32_t n, int32_t on_host) {
+  return slab_copy(e, id, const_cast<void*>(k), const_cast<void*>(v), n, on_host, true);
+}
+
+extern "C" cbt_status cbt_kv_slab_export(cbt_engine* e, int32_t id, void* k, void* v, int32_t n,
+                                         int32_t on_host) {
+  return slab_copy(e, id, k, v, n, on_host, false);
+}
+
+// ---- the forward pass over n tokens whose rows are already on the device ----------------
+static LinearW lw(const cbt_linear& l, int fmt) {
+  return LinearW{l.w, static_cast<const uint16_t*>(l.scales),
+                 static_cast<const uint16_t*>(l.biases), fmt};
+}
+
+// n tokens (decode rows or packed prefill tokens); n_out rows get logits: all n when
+// gather == false, else the n_out rows listed in e->last_idx
+static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_keys, bool gather,
+                           int n_out, float* logits, int32_t* next) {
+  const cbt_model_config& c = e->cfg;
+  cudaStream_t s = e->stream;
+  const int d = c.d_model, qd = e->qd(), kvd = e->kvd(), F = c.d_ff;
+  const int fmt = c.weight_format;
+  uint16_t* arena = static_cast<uint16_t*>(e->p.kv_arena);
+  launch_embed(tokens, n, static_cast<const uint16_t*>(e->w.embed), d, c.vocab, e->x, e->err, s);
+  launch_rope_table(e->rows, n, c.head_dim, c.rope_theta, e->cosv, e->sinv, s);
+  for (int l = 0; l < c.n_layers; ++l) {
+    const cbt_layer_weights& L = e->layers[l];
+    launch_rmsnorm(e->x, static_cast<const uint16_t*>(L.attn_norm), n, d, c.rms_eps, e->h, s);
+    launch_linear(e->h, n, d, lw(L.wqkv, fmt), qd + 2 * kvd, EPI_STORE, e->qkv, e->part,
+                  e->part_floats, s);
+    launch_rope_append(e->qkv, e->rows, n, l, c.n_heads, c.n_kv_heads, c.head_dim, e->cosv,
+                       e->sinv, arena, s);
+    launch_attention_naive(e->qkv, e->rows, n, l, c.n_heads, c.n_kv_heads, c.head_dim, max_keys,
+                           arena, e->o, s);
+    launch_linear(e->o, n, qd, lw(L.wo, fmt), d, EPI_ADD, e->x, e->part, e->part_floats, s);
+    launch_rmsnorm(e->x, static_cast<const uint16_t*>(L.ffn_norm), n, d, c.rms_eps, e->h, s);
+    launch_linear(e->h, n, d, lw(L.wgu, fmt), 2 * F, EPI_SWIGLU, e->act, e->part, e->part_floats,
+                  s);
+    launch_linear(e->act, n, F, lw(L.wd, fmt), d, EPI_ADD, e->x, e->part, e->part_floats, s);
+  }
+  const float* xf = e->x;
+  if (gather) {
+    launch_gather_rows(e->x, e->last_idx, n_out, d, e->xg, s);
+    xf = e->xg;
+  }
+  float* hf = e->xg + (size_t)e->p.max_batch * d;
+  launch_rmsnorm(xf, static_cast<const uint16_t*>(e->w.final_norm), n_out, d, c.rms_eps, hf, s);
+  float* lg = logits ? logits : e->logits;
+  launch_linear(hf, n_out, d, lw(e->w.lm_head, fmt), c.vocab, EPI_STORE, lg, e->part,
+                e->part_floats, s);
+  launch_argmax(lg, n_out, c.vocab, next ? next : e->next_tok, s);
+  return cudaGetLastError();
+}
+
+extern "C" cbt_status cbt_decode_step_batch(cbt_engine* e, const int32_t* ids, int32_t B,
+                                            const int32_t* last_tokens, float* logits,
+                                            int32_t* next_tokens) {
+  if (!e) return CBT_ERR_NULL;
+  if (B < 0) return CBT_ERR_INVALID;
+  if (B == 0) return CBT_OK;
+  if (!ids || !last_tokens) return CBT_ERR_NULL;
+  if (B > e->p.max_batch) return CBT_ERR_BATCH;
+  std::unordered_set<int> seen;
+  int max_keys = 0;
+  for (int b = 0; b < B; ++b) {
+    auto it = e->slabs.find(ids[b]);
+    if (it == e->slabs.end()) return CBT_ERR_BAD_SLAB;
+    if (!seen.insert(ids[b]).second) return CBT_ERR_DUP_SLAB;
+    const Slab& sl = it->second;
+    if (sl.pos + 1 > sl.cap) return CBT_ERR_CAPACITY;
+    e->hrows[b] = QueryRow{(long long)(sl.offset / 2), sl.pos, sl.cap};
+    max_keys = std::max(max_keys, sl.pos + 1);
+  }
+  cudaError_t rc = cudaMemcpyAsync(e->rows, e->hrows.data(), sizeof(QueryRow) * B,
+                                   cudaMemcpyHostToDevice, e->stream);
+  if (rc == cudaSuccess) rc = forward(e, B, last_tokens, max_keys, false, B, logits, next_tokens);
+  if (rc != cudaSuccess) return CBT_ERR_CUDA;
+  for (int b = 0; b < B; ++b) e->slabs[ids[b]].pos += 1;
+  e->steps += 1;
+  return CBT_OK;
+}
+
+extern "C" cbt_status cbt_prefill_segmented(cbt_engine* e, const int32_t* ids,
+                                            const int32_t* lens, int32_t K, const int32_t* tokens,
+                                            float* logits, int32_t* next_tokens) {
+  if (!e) return CBT_ERR_NULL;
+  if (K < 0) return CBT_ERR_INVALID;
+  if (K == 0) return CBT_OK;
+  if (!ids || !lens || !tokens) return CBT_ERR_NULL;
+  if (K > e->p.max_batch) return CBT_ERR_BATCH;
+  std::unordered_set<int> seen;
+  long long T = 0;
+  int max_keys = 0;
+  for (int s = 0; s < K; ++s) {
+    auto it = e->slabs.find(ids[s]);
+    if (it == e->slabs.end()) return CBT_ERR_BAD_SLAB;
+    if (!seen.insert(ids[s]).second) return CBT_ERR_DUP_SLAB;
+    if (lens[s] <= 0) return CBT_ERR_INVALID;
+    const Slab& sl = it->second;
+    if ((long long)sl.pos + lens[s] > sl.cap) return CBT_ERR_CAPACITY;
+    T += lens[s];
+    max_keys = std::max(max_keys, sl.pos + lens[s]);
+  }
+  if (T > e->p.max_prefill_tokens) return CBT_ERR_TOKENS;
+  int g = 0;
+  for (int s = 0; s < K; ++s) {
+    const Slab& sl = e->slabs[ids[s]];
+    for (int j = 0; j < lens[s]; ++j, ++g)
+      e->hrows[g] = QueryRow{(long long)(sl.offset / 2), sl.pos + j, sl.cap};
+    e->hidx[s] = g - 1;
+  }
+  cudaError_t rc = cudaMemcpyAsync(e->rows, e->hrows.data(), sizeof(QueryRow) * T,
+                                   cudaMemcpyHostToDevice, e->stream);
+  if (rc == cudaSuccess)
+    rc = cudaMemcpyAsync(e->last_idx, e->hidx.data(), sizeof(int32_t) * K, cudaMemcpyHostToDevice,
+                         e->stream);
+  if (rc == cudaSuccess)
+    rc = forward(e, (int)T, tokens, max_keys, true, K, logits, next_tokens);
+  if (rc != cudaSuccess) return CBT_ERR_CUDA;
+  for (int s = 0; s < K; ++s) e->slabs[ids[s]].pos += lens[s];
+  e->prefill_tokens += T;
+  return CBT_OK;
+}
+
+extern "C" cbt_status cbt_last_device_error(cbt_engine* e, int32_t* code, int32_t* info) {
+  if (!e || !code || !info) return CBT_ERR_NULL;
+  int h[2] = {0, 0};
+  cudaError_t rc = cudaStreamSynchronize(e->stream);
+  if (rc == cudaSuccess) rc = cudaMemcpy(h, e->err, sizeof(h), cudaMemcpyDeviceToHost);
+  if (rc == cudaSuccess) rc = cudaMemset(e->err, 0, sizeof(h));
+  if (rc != cudaSuccess) return CBT_ERR_CUDA;
+  *code = h[0];
+  *info = h[1];
+  return CBT_OK;
+}
+
+extern "C" cbt_status cbt_engine_stats(cbt_engine* e, cbt_stats* out) {
+  if (!e || !out) return CBT_ERR_NULL;
+  out->live_slabs = (int32_t)e->slabs.size();
+  out->max_batch = e->p.max_batch;
+  out->slab_bytes_in_use = (int64_t)e->in_use;
+  out->arena_bytes = (int64_t)(e->p.kv_arena_bytes & ~(kSlabAlign - 1));
+  size_t big = 0;
+  for (auto& kv : e->free_ext) big = std::max(big, kv.second);
+  out->largest_free_bytes = (int64_t)big;
+  out->scratch_bytes = (int64_t)e->scratch_bytes;
+  out->decode_steps = e->steps;
+  out->prefill_tokens = e->prefill_tokens;
+  return CBT_OK;
+}
+
+extern "C" int64_t cbt_kernel_launches(cbt_engine* e) {
+  (void)e;
+  return kernel_launch_count();
+}
+
+extern "C" cbt_status cbt_quantize_affine4(const void* w, int32_t rows, int32_t cols, int32_t group,
+                                           void* packed, void* scales, void* biases, void* stream) {
+  if (!w || !packed || !scales || !biases) return CBT_ERR_NULL;
+  if (rows <= 0 || cols <= 0 || group <= 0 || group % 8 || cols % group) return CBT_ERR_INVALID;
+  launch_quantize_affine4(static_cast<const uint16_t*>(w), rows, cols, group,
+                          static_cast<uint32_t*>(packed), static_cast<uint16_t*>(scales),
+                          static_cast<uint16_t*>(biases), static_cast<cudaStream_t>(stream));
+  return cudaGetLastError() == cudaSuccess ? CBT_OK : CBT_ERR_CUDA;
+}

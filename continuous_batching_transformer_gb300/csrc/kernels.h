@@ -1,0 +1,46 @@
+// kernels.h -- launchers of the engine's CUDA kernels (host side).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+// kernel launches queued through the launchers below (for launch accounting)
+long long kernel_launch_count();
+void count_launch(int n = 1);
+
+struct LinearW {
+  const void* w;       // bf16 [M][K] or uint32 [M][K/8]
+  const uint16_t* scales;  // affine4 only: bf16 [M][K/64]
+  const uint16_t* biases;
+  int fmt;             // CBT_WEIGHTS_BF16 / CBT_WEIGHTS_AFFINE4
+};
+
+// embed + token range check
+void launch_embed(const int32_t* tokens, int n, const uint16_t* table, int d, int vocab, float* x,
+                  int* err, cudaStream_t s);
+// RMSNorm rows of x into h
+void launch_rmsnorm(const float* x, const uint16_t* gain, int n, int d, float eps, float* h,
+                    cudaStream_t s);
+// per-token RoPE cos/sin for the positions in rows (fp32 [n][hd/2] each), in double
+void launch_rope_table(const QueryRow* rows, int n, int head_dim, double theta, float* cosv,
+                       float* sinv, cudaStream_t s);
+// RoPE q and k in place at each token's position; append k, v (bf16) to its slab
+void launch_rope_append(float* qkv, const QueryRow* rows, int n, int layer, int n_heads,
+                        int n_kv_heads, int head_dim, const float* cosv, const float* sinv,
+                        uint16_t* arena, cudaStream_t s);
+// softmax attention of each token over [0, pos] of its own slab
+void launch_attention_naive(const float* qkv, const QueryRow* rows, int n, int layer, int n_heads,
+                            int n_kv_heads, int head_dim, int max_keys, const uint16_t* arena,
+                            float* o, cudaStream_t s);
+// projection y = x W^T with an epilogue; picks the skinny or the tiled kernel
+void launch_linear(const float* x, int n, int K, const LinearW& W, int M, Epilogue epi, float* out,
+                   float* partials, size_t partial_floats, cudaStream_t s);
+// greedy argmax per row, lowest index on ties
+void launch_argmax(const float* logits, int n, int vocab, int32_t* out, cudaStream_t s);
+// gather rows idx[i] of src [*, d] into dst [i, d]
+void launch_gather_rows(const float* src, const int32_t* idx, int n, int d, float* dst,
+                        cudaStream_t s);
+// 4-bit affine quantisation of a bf16 matrix
+void launch_quantize_affine4(const uint16_t* w, int rows, int cols, int group, uint32_t* packed,
+                             uint16_t* scales, uint16_t* biases, cudaStream_t s);

@@ -1,0 +1,230 @@
+/*
+ * cbt.h -- C ABI of the continuous-batching decode engine (libcbt.so).
+ *
+ * One GB300, one process.  The library runs a pre-norm decoder transformer
+ * (RMSNorm, grouped-query attention with RoPE, SwiGLU FFN) over many live
+ * sequences at once:
+ *
+ *   - cbt_decode_step_batch(seq_ids, last_tokens) -> logits[B]: one token per
+ *     live sequence.  Every projection (QKV, O, gate/up, down, lm_head) runs
+ *     once over all B rows, so each weight is read from HBM once per step; the
+ *     amortisation law on the gnosis page ("The throughput law": sharedCost =
+ *     w + L*a against naiveCost = L*(w + a)).  Attention is per sequence: row
+ *     s reads its own KV slab over positions [0, t_s], applies RoPE at t_s,
+ *     appends its new K/V at t_s and t_s is bumped (gnosis page,
+ *     "decode_step_batch -- paint-by-numbers", Delta 1..3).
+ *   - cbt_prefill_segmented(seq_ids, seg_lens, tokens): K prompts packed in one
+ *     pass; the projections run once over all sum(seg_lens) tokens and
+ *     attention is block-diagonal causal, token g of a segment starting at
+ *     seg_start attending to [seg_start, g] only (gnosis page, "REVISED: the
+ *     hard kernel already exists -- forward_batch_segmented").  Returns the
+ *     logits of each segment's last token only (mlx-bun batching design,
+ *     section 4.2: slice the last position before the head).
+ *   - slabs: one KV slab per live sequence, allocated from a caller-provided
+ *     device arena and freed on retire (gnosis page, "1. Native station:
+ *     per-sequence KV + a batched decode step": an N-slot KV arena keyed by a
+ *     sequence id, prefillSeq / freeSeq).
+ *   - greedy sampling: argmax over each row's logits, the lowest vocabulary id
+ *     winning ties (mlx-bun batching design, section 4.4 "Vectorized
+ *     homogeneous sampling", and its campaign note on tied candidate scores).
+ *
+ * Conventions for every call:
+ *   - Return value: CBT_OK (0) or a negative cbt_status; cbt_status_str()
+ *     names it.  Errors the host can see (bad or duplicate slab id, batch
+ *     above max_batch, capacity overflow, pool exhausted, null pointers,
+ *     sizes out of range) are reported BEFORE any work is queued and leave
+ *     the engine unchanged.
+ *   - Work is queued asynchronously on the engine's CUDA stream.  Errors only
+ *     the device can see (a token id >= vocab) set a device error word that
+ *     cbt_last_device_error() reads; the offending row's outputs are then
+ *     unspecified, other rows are unaffected, and nothing traps.
+ *   - Ownership: the caller owns and frees the weights, the KV arena, token
+ *     and logits buffers; the engine borrows them for its lifetime and never
+ *     frees them.  The engine owns its scratch memory, which it allocates in
+ *     cbt_engine_create and frees in cbt_engine_destroy.
+ *   - An engine is not thread safe: one host thread at a time.
+ */
+#ifndef CBT_H
+#define CBT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t cbt_status;
+#define CBT_OK 0
+#define CBT_ERR_INVALID -1        /* a size or config field out of range */
+#define CBT_ERR_NULL -2           /* a required pointer is NULL */
+#define CBT_ERR_BAD_SLAB -3       /* slab id unknown or already freed */
+#define CBT_ERR_DUP_SLAB -4       /* the same slab id twice in one call */
+#define CBT_ERR_BATCH -5          /* B > max_batch or K > max_batch */
+#define CBT_ERR_CAPACITY -6       /* a slab would grow past its capacity */
+#define CBT_ERR_POOL_EXHAUSTED -7 /* no free extent large enough in the KV arena */
+#define CBT_ERR_TOKENS -8         /* sum of seg_lens above max_prefill_tokens */
+#define CBT_ERR_CUDA -9           /* a CUDA runtime call failed */
+#define CBT_ERR_DEVICE -10        /* the device error word was set (see below) */
+#define CBT_ERR_UNSUPPORTED -11   /* shape not supported by the kernels */
+
+/* device error word codes, as returned by cbt_last_device_error in *code */
+#define CBT_DEV_OK 0
+#define CBT_DEV_TOKEN_RANGE 1 /* a token id outside [0, vocab) */
+
+#define CBT_WEIGHTS_BF16 0    /* bf16, row-major [out][in] */
+#define CBT_WEIGHTS_AFFINE4 1 /* 4-bit affine, see cbt_linear */
+
+typedef struct {
+  int32_t n_layers;
+  int32_t d_model;
+  int32_t n_heads;    /* query heads */
+  int32_t n_kv_heads; /* key/value heads; q head j reads kv head j / (n_heads / n_kv_heads) */
+  int32_t head_dim;   /* must be 64 or 128 */
+  int32_t d_ff;       /* SwiGLU hidden size */
+  int32_t vocab;
+  float rms_eps;
+  double rope_theta; /* RoPE rotate-half form, pair (i, i + head_dim/2) turned by
+                        pos * rope_theta^(-2i/head_dim) */
+  int32_t weight_format; /* CBT_WEIGHTS_BF16 or CBT_WEIGHTS_AFFINE4 */
+  int32_t group_size;    /* CBT_WEIGHTS_AFFINE4 only: must be 64 */
+} cbt_model_config;
+
+/* One projection W [out][in] (y = x W^T), device pointers.
+ * BF16:    w = bf16 [out][in] row-major; scales = biases = NULL.
+ * AFFINE4: w = uint32 [out][in/8], element 8j+k of a row in bits 4k..4k+3 of word j;
+ *          scales, biases = bf16 [out][in/group]; the weight is scale*q + bias of its
+ *          group (MLX-style affine quantisation; cbt_quantize_affine4 produces it). */
+typedef struct {
+  const void* w;
+  const void* scales;
+  const void* biases;
+} cbt_linear;
+
+typedef struct {
+  cbt_linear wqkv;       /* [(n_heads + 2 n_kv_heads) * head_dim][d_model]: q rows, k rows, v rows */
+  cbt_linear wo;         /* [d_model][n_heads * head_dim] */
+  cbt_linear wgu;        /* [2 d_ff][d_model]: gate rows [0, d_ff), up rows [d_ff, 2 d_ff) */
+  cbt_linear wd;         /* [d_model][d_ff] */
+  const void* attn_norm; /* bf16 [d_model] RMSNorm gain before attention */
+  const void* ffn_norm;  /* bf16 [d_model] RMSNorm gain before the FFN */
+} cbt_layer_weights;
+
+typedef struct {
+  const void* embed;                /* bf16 [vocab][d_model] (never quantised) */
+  cbt_linear lm_head;               /* [vocab][d_model] */
+  const void* final_norm;           /* bf16 [d_model] */
+  const cbt_layer_weights* layers;  /* host array [n_layers]; copied by cbt_engine_create */
+} cbt_weights;
+
+typedef struct {
+  void* kv_arena;            /* device memory for all KV slabs, 256-byte aligned, borrowed */
+  size_t kv_arena_bytes;
+  int32_t max_batch;         /* most rows per decode step and most segments per prefill */
+  int32_t max_prefill_tokens;/* most tokens (sum of seg_lens) per prefill call */
+  void* stream;              /* cudaStream_t all work is queued on; NULL = legacy default */
+} cbt_engine_params;
+
+typedef struct {
+  int32_t live_slabs;
+  int32_t max_batch;
+  int64_t slab_bytes_in_use;  /* bytes of the arena held by live slabs */
+  int64_t arena_bytes;
+  int64_t largest_free_bytes; /* largest single free extent */
+  int64_t scratch_bytes;      /* device scratch the engine allocated */
+  int64_t decode_steps;       /* decode steps queued so far */
+  int64_t prefill_tokens;     /* prefill tokens queued so far */
+} cbt_stats;
+
+typedef struct cbt_engine cbt_engine;
+
+const char* cbt_status_str(cbt_status s);
+
+/* Create an engine over the caller's weights and KV arena.  Copies the config, the weight
+ * pointer tables and the params; allocates device scratch sized for max_batch rows and
+ * max_prefill_tokens tokens.  On failure *out is NULL and nothing is allocated. */
+cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_weights* weights,
+                             const cbt_engine_params* params, cbt_engine** out);
+
+/* Synchronise the engine's stream and free everything the engine allocated. */
+cbt_status cbt_engine_destroy(cbt_engine* e);
+
+/* Bytes one slab of `capacity_tokens` positions takes in the arena:
+ * n_layers * 2 (K, V) * n_kv_heads * capacity * head_dim * 2 bytes, rounded up to 4 KiB.
+ * Slab layout (bf16): [layer][K|V][kv head][position][head_dim]. */
+size_t cbt_slab_bytes(const cbt_model_config* cfg, int32_t capacity_tokens);
+
+/* Reserve a slab for one sequence (host-side first-fit allocator over the arena, no
+ * device work).  The slab starts empty (position 0).  The slab id is the sequence id
+ * every later call uses. */
+cbt_status cbt_kv_slab_alloc(cbt_engine* e, int32_t capacity_tokens, int32_t* slab_id);
+
+/* Return a slab to the arena (host-side bookkeeping only).  Work already queued on the
+ * engine stream that uses the slab still runs before any later work on that stream can
+ * reuse its extent, so a slab may be freed right after the step that last used it. */
+cbt_status cbt_kv_slab_free(cbt_engine* e, int32_t slab_id);
+
+/* retire: free the slabs of finished sequences (EOS or length limit), n ids. */
+cbt_status cbt_retire(cbt_engine* e, const int32_t* slab_ids, int32_t n);
+
+/* Current position (tokens held) of a slab. */
+cbt_status cbt_kv_slab_position(cbt_engine* e, int32_t slab_id, int32_t* pos);
+
+/* Save/restore a sequence's state.  import copies n_tokens positions of K and V into the
+ * slab (positions [0, n_tokens)) and sets its position to n_tokens; export copies
+ * positions [0, n_tokens) out.  k and v are bf16 [n_layers][n_kv_heads][n_tokens][head_dim],
+ * on the host (on_host != 0) or on the device.  Queued on the engine stream. */
+cbt_status cbt_kv_slab_import(cbt_engine* e, int32_t slab_id, const void* k, const void* v,
+                              int32_t n_tokens, int32_t on_host);
+cbt_status cbt_kv_slab_export(cbt_engine* e, int32_t slab_id, void* k, void* v,
+                              int32_t n_tokens, int32_t on_host);
+
+/* Segmented prefill of K prompts (forward_batch_segmented).
+ *   slab_ids  host int32 [K], distinct live slabs.  Segment s's tokens go to positions
+ *             [p_s, p_s + seg_lens[s]) of its slab, p_s being the slab's current position
+ *             (0 for a fresh slab: positions are segment-local from 0); each token attends
+ *             to positions [0, its own] of its own slab only.
+ *   seg_lens  host int32 [K], each >= 1, sum <= max_prefill_tokens, p_s + seg_lens[s] <=
+ *             capacity.
+ *   tokens    device int32 [sum seg_lens], the segments back to back.
+ *   logits    device float [K][vocab]: logits of each segment's last token; NULL allowed.
+ *   next_tokens device int32 [K]: greedy argmax of those logits; NULL allowed.
+ * Afterwards each slab's position is p_s + seg_lens[s]. */
+cbt_status cbt_prefill_segmented(cbt_engine* e, const int32_t* slab_ids, const int32_t* seg_lens,
+                                 int32_t K, const int32_t* tokens, float* logits,
+                                 int32_t* next_tokens);
+
+/* One continuous-batching decode step (decode_step_batch).
+ *   slab_ids    host int32 [B], distinct live slabs; row b is the sequence of slab_ids[b].
+ *   last_tokens device int32 [B]: the token each row feeds (may be the previous step's
+ *               next_tokens buffer, so greedy decode needs no host round trip).
+ *   logits      device float [B][vocab] or NULL.
+ *   next_tokens device int32 [B] or NULL: greedy argmax of each row, lowest id on ties.
+ * Row b's token is placed at position t_b (the slab's current position, which must be
+ * below its capacity), attends to [0, t_b] of its own slab, and t_b becomes t_b + 1.
+ * B == 0 is a no-op. */
+cbt_status cbt_decode_step_batch(cbt_engine* e, const int32_t* slab_ids, int32_t B,
+                                 const int32_t* last_tokens, float* logits, int32_t* next_tokens);
+
+/* Synchronise the engine's stream, then read and clear the device error word.
+ * *code = CBT_DEV_OK or a CBT_DEV_* code, *info = the offending row or token index.
+ * Returns CBT_OK, or CBT_ERR_CUDA if the stream reported an error. */
+cbt_status cbt_last_device_error(cbt_engine* e, int32_t* code, int32_t* info);
+
+cbt_status cbt_engine_stats(cbt_engine* e, cbt_stats* out);
+
+/* Number of kernel launches the engine queued so far (for launch accounting). */
+int64_t cbt_kernel_launches(cbt_engine* e);
+
+/* MLX-style 4-bit affine quantisation of a bf16 matrix on the device, groups of `group`
+ * (64) along each row: scale = bf16((max - min) / 15), bias = bf16(min),
+ * q = clamp(rint((w - bias) / scale), 0, 15) (ties to even; 0 when scale == 0), packed
+ * as in cbt_linear.  w: device bf16 [rows][cols]; packed: device uint32 [rows][cols/8];
+ * scales, biases: device bf16 [rows][cols/group].  cols % group == 0.  Queued on `stream`. */
+cbt_status cbt_quantize_affine4(const void* w, int32_t rows, int32_t cols, int32_t group,
+                                void* packed, void* scales, void* biases, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -136,6 +136,8 @@ int orc_quantize_affine4(const uint16_t* w, int rows, int cols, int group, uint3
                          uint16_t* scales, uint16_t* biases) {
   if (group <= 0 || cols % group != 0 || group % 8 != 0) return ORC_EINVAL;
   int ng = cols / group;
+  /* rows are independent: the loop over them may run in any order */
+#pragma omp parallel for schedule(static)
   for (int r = 0; r < rows; ++r) {
     for (int g = 0; g < ng; ++g) {
       const uint16_t* src = w + (size_t)r * cols + (size_t)g * group;

@@ -1,0 +1,110 @@
+"""GPU parity on the tiny decoder (2 layers, d_model 256, 4 heads, vocab 1024), through the C
+ABI, against the CPU oracle: segmented prefill of prompts {5, 17, 32, 9}, then 16 greedy
+decode steps, logits element by element (bf16 tolerance 2e-2) and greedy tokens."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from continuous_batching_transformer_gb300.model import DeviceWeights, Engine
+from synth.recipes import TINY, TINY_RUN, ModelShape
+from tests.gpu_harness import TOL, check_logits, ensure_built, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def setup():
+    ensure_built()
+    dev = torch.device("cuda:0")
+    w = DeviceWeights(TINY, dev)
+    om = oracle.OracleModel(TINY)
+    return dev, w, om
+
+
+def run_tiny(dev, w, om, use_register: bool):
+    lens = [int(n) for n in TINY_RUN.context_lengths()]
+    toks = np.concatenate([TINY_RUN.row_tokens(r, n) for r, n in enumerate(lens)])
+    eng = Engine(w, arena_bytes=32 << 20, max_batch=8, max_prefill_tokens=128)
+    cap = 64
+    slabs = [eng.kv_slab_alloc(cap) for _ in lens]
+    B = len(lens)
+    logits = torch.empty((B, TINY.vocab), dtype=torch.float32, device=dev)
+    nxt = torch.empty(B, dtype=torch.int32, device=dev)
+    eng.prefill_segmented(slabs, lens, to_dev(toks, dev), logits, nxt)
+    caches = [oracle.KVCache(TINY, cap) for _ in lens]
+    ref = oracle.prefill_segmented(om, caches, lens, toks)
+    errs = [check_logits(logits.cpu().numpy(), ref, TOL["bf16"], "prefill")]
+    assert [eng.position(s) for s in slabs] == lens
+    feed = np.array([oracle.argmax(r) for r in ref], dtype=np.int32)
+    gpu_tokens, ref_tokens = [nxt.cpu().numpy().copy()], [feed.copy()]
+    for step in range(TINY_RUN.steps):
+        if use_register:
+            last = nxt.clone()  # device-side feed, no host round trip
+        else:
+            last = to_dev(feed, dev)  # teacher-forced on the oracle's tokens
+        eng.decode_step_batch(slabs, last, logits, nxt)
+        ref = oracle.decode_step_batch(om, caches, feed if not use_register else last.cpu().numpy())
+        errs.append(check_logits(logits.cpu().numpy(), ref, TOL["bf16"], f"decode step {step}"))
+        feed = np.array([oracle.argmax(r) for r in ref], dtype=np.int32)
+        gpu_tokens.append(nxt.cpu().numpy().copy())
+        ref_tokens.append(feed.copy())
+    assert [eng.position(s) for s in slabs] == [n + TINY_RUN.steps for n in lens]
+    # the slabs hold the same K/V the oracle cached (bf16 values, up to one rounding step)
+    for r, sl in enumerate(slabs):
+        n = lens[r] + TINY_RUN.steps
+        k = torch.empty((TINY.n_layers, TINY.n_kv_heads, n, TINY.head_dim), dtype=torch.bfloat16)
+        v = torch.empty_like(k)
+        eng.export_kv(sl, k, v, n)
+        ck = torch.from_numpy(caches[r].k[:, :, :n].view(np.int16)).view(torch.bfloat16)
+        cv = torch.from_numpy(caches[r].v[:, :, :n].view(np.int16)).view(torch.bfloat16)
+        torch.testing.assert_close(k.float(), ck.float(), atol=4e-3, rtol=1e-2)
+        torch.testing.assert_close(v.float(), cv.float(), atol=4e-3, rtol=1e-2)
+    assert eng.device_error() == (0, 0)
+    eng.close()
+    return errs, np.array(gpu_tokens), np.array(ref_tokens)
+
+
+def test_tiny_teacher_forced(setup):
+    dev, w, om = setup
+    errs, g, r = run_tiny(dev, w, om, use_register=False)
+    print(f"tiny: max |logit - oracle| over prefill + 16 steps = {max(errs):.3e}")
+
+
+def test_tiny_device_register_feed(setup):
+    """Greedy decode fed from the device next-token buffer: the oracle follows the GPU's
+    tokens, and every GPU token must be the oracle's argmax (or tied within tolerance)."""
+    dev, w, om = setup
+    errs, g, r = run_tiny(dev, w, om, use_register=True)
+    assert max(errs) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "affine4"])
+def test_gqa_shape_parity(fmt):
+    """Grouped-query heads (4 q heads over 2 kv heads), non-unit norm gains, head_dim 128 and
+    both weight formats; prompts straddle several GEMM tiles (tiled and skinny paths)."""
+    ensure_built()
+    from dataclasses import replace
+    shape = ModelShape("gqa-check", 2, 512, 4, 2, 128, 1024, 2048, 1e-5, 1e6, gain_sigma=0.1,
+                       weight_format=fmt)
+    dev = torch.device("cuda:0")
+    w = DeviceWeights(shape, dev)
+    om = oracle.OracleModel(shape)
+    lens = [40, 1, 77, 33, 9]
+    toks = np.concatenate([np.asarray(np.random.default_rng(r).integers(0, shape.vocab, n), np.int32)
+                           for r, n in enumerate(lens)])
+    eng = Engine(w, arena_bytes=64 << 20, max_batch=8, max_prefill_tokens=256)
+    slabs = [eng.kv_slab_alloc(96) for _ in lens]
+    caches = [oracle.KVCache(shape, 96) for _ in lens]
+    logits = torch.empty((len(lens), shape.vocab), dtype=torch.float32, device=dev)
+    nxt = torch.empty(len(lens), dtype=torch.int32, device=dev)
+    eng.prefill_segmented(slabs, lens, to_dev(toks, dev), logits, nxt)
+    ref = oracle.prefill_segmented(om, caches, lens, toks)
+    check_logits(logits.cpu().numpy(), ref, TOL[fmt], f"{fmt} prefill")
+    feed = np.array([oracle.argmax(r) for r in ref], dtype=np.int32)
+    for step in range(3):
+        eng.decode_step_batch(slabs, to_dev(feed, dev), logits, nxt)
+        ref = oracle.decode_step_batch(om, caches, feed)
+        check_logits(logits.cpu().numpy(), ref, TOL[fmt], f"{fmt} decode {step}")
+        feed = np.array([oracle.argmax(r) for r in ref], dtype=np.int32)
+    eng.close()
