@@ -1,0 +1,349 @@
+#!/usr/bin/env python
+"""Aggregate greedy decode throughput of decode_step_batch on the 7B-shaped decoder.
+
+Default workload: 32 layers, d_model 4096, 32 q / 8 kv heads (head_dim 128), SwiGLU 14336,
+vocab 32000, bf16 seeded N(0, 0.02) weights; B = 8 persistent KV slabs whose context lengths
+are uniform in [512, 4096] (seeded synthetic KV); greedy decode, each step feeding the
+previous step's device-side next tokens.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+--impl reference times the CPU oracle on the same workload (a bounded sample of steps).
+Multi-GPU runs are independent replicas (one engine and weight copy per GPU, rows never
+exchange data); value = all ranks' tokens / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "aggregate decode tok/s at B=1..32 (7B-shape) + % of HBM roofline per step"
+NOMINAL_HBM_GBS = 8000.0
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        return None
+
+
+def workload_by_name(name: str):
+    from synth.recipes import DECODE_7B_B8, LONG_7B_B32, decode_7b_fixed
+    if name == "7b-bf16-b8":
+        return DECODE_7B_B8
+    if name == "7b-bf16-b32-long":
+        return LONG_7B_B32
+    if name.startswith("7b-bf16-b") and name.endswith("-ctx2048"):
+        return decode_7b_fixed(int(name[len("7b-bf16-b"):-len("-ctx2048")]), 2048, "bf16")
+    if name.startswith("7b-affine4-b") and name.endswith("-ctx2048"):
+        return decode_7b_fixed(int(name[len("7b-affine4-b"):-len("-ctx2048")]), 2048, "affine4")
+    raise SystemExit(f"unknown workload {name}")
+
+
+def step_bytes(shape, ctx_lens) -> float:
+    """Algorithmic HBM bytes of one decode step: every linear weight once, each row's live KV
+    (positions 0..t_b after the append) once, the appended K/V, the logits written."""
+    kv_tok = shape.kv_bytes_per_token()
+    return float(shape.weight_bytes_per_step() + sum((int(c) + 1) * kv_tok for c in ctx_lens)
+                 + len(ctx_lens) * (kv_tok + 4 * shape.vocab))
+
+
+# ---- clocks sampled during the timed region ---------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.tmp = tempfile.NamedTemporaryFile(prefix="clocks", suffix=".csv", delete=False)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if gpu_id:
+            cmd += ["-i", gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.close()
+        rows = list(csv.reader(io.StringIO(open(self.tmp.name).read())))
+        os.unlink(self.tmp.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---- the GPU arm ------------------------------------------------------------------------------
+def setup_decode(wl, device, extra_positions: int):
+    """Engine + slabs for a decode workload: synthetic KV of each row loaded into its slab,
+    each row's next token ready on the device."""
+    import numpy as np
+    import torch
+
+    from continuous_batching_transformer_gb300 import binding as B
+    from continuous_batching_transformer_gb300.model import DeviceWeights, Engine
+
+    shape = wl.shape
+    ctx = [int(c) for c in wl.context_lengths()]
+    caps = [c + extra_positions for c in ctx]
+    w = DeviceWeights(shape, device)
+    arena = sum(B.slab_bytes(w.cfg, c) for c in caps)
+    eng = Engine(w, arena_bytes=arena, max_batch=len(ctx), max_prefill_tokens=len(ctx))
+    slabs = []
+    for r, (c, cap) in enumerate(zip(ctx, caps)):
+        s = eng.kv_slab_alloc(cap)
+        eng.fill_synthetic_kv(s, r, c, wl.seed)
+        slabs.append(s)
+    first = np.array([wl.row_tokens(r, c + 1)[c] for r, c in enumerate(ctx)], dtype=np.int32)
+    tok = torch.from_numpy(first).to(device)
+    return w, eng, slabs, ctx, tok
+
+
+def gpu_arm(args, rank: int, world: int):
+    import torch
+
+    import continuous_batching_transformer_gb300 as cbt
+    from continuous_batching_transformer_gb300 import binding as B
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    if rank == 0 or not os.path.exists(cbt._build.LIB):
+        cbt.build()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+        dist.barrier()
+    wl = workload_by_name(args.workload)
+    K, W = args.steps, args.warmup
+    w, eng, slabs, ctx, tok0 = setup_decode(wl, device, extra_positions=3 * (K + W) + 8)
+    Bsz = len(slabs)
+    V = wl.shape.vocab
+    stream = eng.stream
+    bufs = [tok0.clone(), torch.empty_like(tok0)]
+    logits = torch.empty((Bsz, V), dtype=torch.float32, device=device)
+
+    def step(i):
+        eng.decode_step_batch(slabs, bufs[i % 2], logits, bufs[(i + 1) % 2])
+
+    for i in range(W):
+        step(i)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gpu_uuid = None
+    try:
+        gpu_uuid = str(torch.cuda.get_device_properties(device).uuid)
+        if not gpu_uuid.startswith("GPU-"):
+            gpu_uuid = "GPU-" + gpu_uuid
+    except Exception:
+        pass
+    clocks = ClockSampler(gpu_uuid) if rank == 0 else None
+    B.engine_set_timing(eng.handle, 1 << B.KCLASS_PROJ)
+    launches0 = B.kernel_launches(eng.handle)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(W, W + K):
+            step(i)
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    launches = B.kernel_launches(eng.handle) - launches0
+    ms = ev0.elapsed_time(ev1)
+    clk = clocks.stop() if clocks else None
+    proj_ms, proj_n, proj_bytes = B.engine_timing(eng.handle, B.KCLASS_PROJ)
+    B.engine_set_timing(eng.handle, 0)
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if dist:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    code, info = eng.device_error()
+    if code != 0:
+        raise SystemExit(f"device error word set: code {code} info {info}")
+
+    # end to end through the public API with host buffers: tokens in from pinned host memory,
+    # next tokens back to the host, every step
+    h_tok = torch.empty(Bsz, dtype=torch.int32, pin_memory=True)
+    h_out = torch.empty(Bsz, dtype=torch.int32, pin_memory=True)
+    h_tok.copy_(bufs[(W + K) % 2].cpu())
+    d_tok = torch.empty_like(tok0)
+    d_out = torch.empty_like(tok0)
+    for i in range(3):
+        d_tok.copy_(h_tok, non_blocking=True)
+        eng.decode_step_batch(slabs, d_tok, None, d_out)
+        h_out.copy_(d_out, non_blocking=True)
+        stream.synchronize()
+        h_tok.copy_(h_out)
+    if dist:
+        dist.barrier()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            d_tok.copy_(h_tok, non_blocking=True)
+            eng.decode_step_batch(slabs, d_tok, None, d_out)
+            h_out.copy_(d_out, non_blocking=True)
+            stream.synchronize()
+            h_tok.copy_(h_out)
+    e2e_s = time.perf_counter() - t0
+    t = torch.tensor([e2e_s], dtype=torch.float64, device=device)
+    if dist:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    e2e_s = float(t.item())
+
+    result = None
+    if rank == 0:
+        peaks = measured_peaks()
+        hbm_peak = peaks["hbm_gbs"] if peaks else 6800.0
+        peak_src = "of measured" if peaks else "of fallback"
+        ctx_mean = [c + W + K / 2.0 for c in ctx]  # mean live context over the timed steps
+        sb = step_bytes(wl.shape, ctx_mean)
+        step_s = ms_max / K / 1e3
+        achieved = proj_bytes / (proj_ms / 1e3) / 1e9 if proj_ms > 0 else None
+        result = {
+            "metric": METRIC,
+            "value": Bsz * K * world / (ms_max / 1e3),
+            "unit": "tok/s",
+            "n_gpus": world,
+            "steps": K,
+            "warmup": W,
+            "ms_per_step": ms_max / K,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16" if wl.shape.weight_format == "bf16" else "affine4-w/bf16",
+            "data": "synthetic (seeded N(0,0.02) weights, seeded KV slabs and tokens)",
+            "config": {"workload": wl.name, "model": wl.shape.name, "batch_per_gpu": Bsz,
+                       "ctx_lengths": ctx, "parallelism": f"replicas x{world}" if world > 1 else "1 gpu",
+                       "l2": "inputs larger than L2 (weights alone are %.1f GB per step)"
+                             % (wl.shape.weight_bytes_per_step() / 1e9)},
+            "step_roofline": {"algorithmic_bytes_per_step": sb,
+                              "achieved_gbs": sb / step_s / 1e9,
+                              "frac_of_8TBps": sb / step_s / 1e9 / NOMINAL_HBM_GBS,
+                              "frac_of_measured_hbm": sb / step_s / 1e9 / hbm_peak},
+            "roofline": {"kernel": "projection kernels (QKV, O, gate/up+SwiGLU, down, lm_head)",
+                         "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
+                         "peak_source": peak_src, "unit": "GB/s",
+                         "frac": achieved / hbm_peak if achieved else None,
+                         "share_of_step": proj_ms / ms if ms > 0 else None,
+                         "launch_groups": proj_n, "traffic": None},
+            "e2e": {"value": Bsz * K * world / e2e_s, "unit": "tok/s",
+                    "h2d_bytes_per_step": 4 * Bsz, "d2h_bytes_per_step": 4 * Bsz},
+            "gpu_launches": int(launches),
+            "clocks": clk,
+        }
+    eng.close()
+    if dist:
+        dist.destroy_process_group()
+    return result
+
+
+# ---- the oracle (CPU) ----------------------------------------------------------------------------
+def oracle_decode_sample(wl, max_steps: int, budget_s: float):
+    """Time the oracle's batched decode step on the same workload: all rows, weights streamed
+    once per step, for up to max_steps steps or until budget_s has passed."""
+    import numpy as np
+
+    import oracle
+    m = oracle.OracleModel(wl.shape)
+    ctx = [int(c) for c in wl.context_lengths()]
+    caches = []
+    for r, c in enumerate(ctx):
+        kc = oracle.KVCache(wl.shape, c + max_steps + 2)
+        kc.fill_synthetic(r, c, wl.seed)
+        caches.append(kc)
+    feed = np.array([wl.row_tokens(r, c + 1)[c] for r, c in enumerate(ctx)], dtype=np.int32)
+    done, t_total = 0, 0.0
+    while done < max_steps and (done == 0 or t_total < budget_s):
+        t0 = time.perf_counter()
+        lg = oracle.decode_step_batch(m, caches, feed)
+        t_total += time.perf_counter() - t0
+        feed = lg.argmax(axis=1).astype(np.int32)
+        done += 1
+    return {"value": len(ctx) * done / t_total, "unit": "tok/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{done} decode step(s) of all {len(ctx)} rows of {wl.name} "
+                      f"(full 32-layer model, {t_total:.1f} s of CPU time)"}, done, t_total
+
+
+def reference_arm(args, rank: int):
+    if rank != 0:
+        return None
+    wl = workload_by_name(args.workload)
+    cb, done, t_total = oracle_decode_sample(wl, max_steps=max(1, args.steps),
+                                             budget_s=args.reference_budget)
+    return {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "tok/s",
+            "n_gpus": 0, "steps": done, "warmup": 0, "ms_per_step": 1e3 * t_total / done,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": wl.name, "model": wl.shape.name,
+                                            "batch_per_gpu": len(wl.context_lengths())},
+            "cpu_baseline": cb,
+            "e2e": {"value": cb["value"], "unit": "tok/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=128)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="7b-bf16-b8")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--reference-budget", type=float, default=60.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        res = reference_arm(args, rank)
+    else:
+        res = gpu_arm(args, rank, world)
+        if rank == 0 and not args.no_cpu_baseline:
+            wl = workload_by_name(args.workload)
+            cb, _, _ = oracle_decode_sample(wl, max_steps=2, budget_s=15.0)
+            res["cpu_baseline"] = cb
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -29,7 +29,9 @@ EXPORTS = ["cbt_status_str", "cbt_engine_create", "cbt_engine_destroy", "cbt_sla
            "cbt_kv_slab_alloc", "cbt_kv_slab_free", "cbt_retire", "cbt_kv_slab_position",
            "cbt_kv_slab_import", "cbt_kv_slab_export", "cbt_prefill_segmented",
            "cbt_decode_step_batch", "cbt_last_device_error", "cbt_engine_stats",
-           "cbt_kernel_launches", "cbt_quantize_affine4"]
+           "cbt_kernel_launches", "cbt_quantize_affine4", "cbt_engine_set_timing",
+           "cbt_engine_timing"]
+KCLASS_PROJ, KCLASS_ATTN, KCLASS_OTHER = 0, 1, 2
 
 
 class CbtError(RuntimeError):
@@ -107,6 +109,9 @@ def lib():
         L.cbt_kernel_launches.restype = ctypes.c_int64
         L.cbt_quantize_affine4.argtypes = [c_void, c_int32, c_int32, c_int32, c_void, c_void,
                                            c_void, c_void]
+        L.cbt_engine_set_timing.argtypes = [c_void, c_int32]
+        L.cbt_engine_timing.argtypes = [c_void, c_int32, P(ctypes.c_double), P(ctypes.c_int64),
+                                        P(ctypes.c_double)]
         for name in EXPORTS:
             if name not in ("cbt_status_str", "cbt_slab_bytes", "cbt_kernel_launches"):
                 getattr(L, name).restype = c_int32
@@ -209,6 +214,18 @@ def engine_stats(e: int) -> Stats:
 
 def kernel_launches(e: int | None = None) -> int:
     return lib().cbt_kernel_launches(e)
+
+
+def engine_set_timing(e: int, class_mask: int) -> None:
+    _check(lib().cbt_engine_set_timing(e, class_mask), "cbt_engine_set_timing")
+
+
+def engine_timing(e: int, kclass: int):
+    """(total device ms, intervals, algorithmic bytes) of one kernel class."""
+    ms, n, by = ctypes.c_double(), ctypes.c_int64(), ctypes.c_double()
+    _check(lib().cbt_engine_timing(e, kclass, ctypes.byref(ms), ctypes.byref(n), ctypes.byref(by)),
+           "cbt_engine_timing")
+    return ms.value, n.value, by.value
 
 
 def quantize_affine4(w_ptr: int, rows: int, cols: int, group: int, packed_ptr: int,

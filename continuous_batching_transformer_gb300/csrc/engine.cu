@@ -70,6 +70,17 @@ struct cbt_engine {
   std::vector<int32_t> hidx;
   int64_t steps = 0, prefill_tokens = 0;
 
+  // measurement: event pairs around launch groups of selected kernel classes
+  struct TimeRec {
+    int cls;
+    cudaEvent_t a, b;
+    double bytes;
+  };
+  int timing_mask = 0;
+  std::vector<cudaEvent_t> ev_pool;
+  size_t ev_used = 0;
+  std::vector<TimeRec> recs;
+
   int qd() const { return cfg.n_heads * cfg.head_dim; }
   int kvd() const { return cfg.n_kv_heads * cfg.head_dim; }
 };
@@ -195,6 +206,7 @@ extern "C" cbt_status cbt_engine_destroy(cbt_engine* e) {
   if (!e) return CBT_ERR_NULL;
   cudaError_t rc = cudaStreamSynchronize(e->stream);
   free_scratch(e);
+  for (cudaEvent_t ev : e->ev_pool) cudaEventDestroy(ev);
   delete e;
   return rc == cudaSuccess ? CBT_OK : CBT_ERR_CUDA;
 }
@@ -304,6 +316,67 @@ extern "C" cbt_status cbt_kv_slab_export(cbt_engine* e, int32_t id, void* k, voi
   return slab_copy(e, id, k, v, n, on_host, false);
 }
 
+// ---- measurement ------------------------------------------------------------------------
+static cudaEvent_t next_event(cbt_engine* e) {
+  if (e->ev_used == e->ev_pool.size()) {
+    cudaEvent_t ev;
+    if (cudaEventCreate(&ev) != cudaSuccess) return nullptr;
+    e->ev_pool.push_back(ev);
+  }
+  return e->ev_pool[e->ev_used++];
+}
+
+// open an interval for class cls if it is being timed; returns the record index or -1
+static int tbegin(cbt_engine* e, int cls) {
+  if (!(e->timing_mask & (1 << cls))) return -1;
+  cudaEvent_t a = next_event(e), b = next_event(e);
+  if (!a || !b) return -1;
+  cudaEventRecord(a, e->stream);
+  e->recs.push_back({cls, a, b, 0.0});
+  return (int)e->recs.size() - 1;
+}
+
+static void tend(cbt_engine* e, int rec, double bytes) {
+  if (rec < 0) return;
+  cudaEventRecord(e->recs[rec].b, e->stream);
+  e->recs[rec].bytes = bytes;
+}
+
+extern "C" cbt_status cbt_engine_set_timing(cbt_engine* e, int32_t mask) {
+  if (!e) return CBT_ERR_NULL;
+  if (cudaStreamSynchronize(e->stream) != cudaSuccess) return CBT_ERR_CUDA;
+  e->timing_mask = mask;
+  e->recs.clear();
+  e->ev_used = 0;
+  return CBT_OK;
+}
+
+extern "C" cbt_status cbt_engine_timing(cbt_engine* e, int32_t cls, double* ms, int64_t* n,
+                                        double* bytes) {
+  if (!e || !ms || !n || !bytes) return CBT_ERR_NULL;
+  if (cls < 0 || cls >= CBT_NUM_KCLASSES) return CBT_ERR_INVALID;
+  if (cudaStreamSynchronize(e->stream) != cudaSuccess) return CBT_ERR_CUDA;
+  double t = 0.0, by = 0.0;
+  int64_t cnt = 0;
+  for (const auto& r : e->recs) {
+    if (r.cls != cls) continue;
+    float f = 0.f;
+    if (cudaEventElapsedTime(&f, r.a, r.b) != cudaSuccess) return CBT_ERR_CUDA;
+    t += f;
+    by += r.bytes;
+    ++cnt;
+  }
+  *ms = t;
+  *n = cnt;
+  *bytes = by;
+  return CBT_OK;
+}
+
+static double weight_bytes(const cbt_model_config& c, long long M, long long K) {
+  if (c.weight_format == CBT_WEIGHTS_BF16) return 2.0 * M * K;
+  return 0.5 * M * K + 4.0 * M * (K / c.group_size);  // codes + bf16 scale and bias
+}
+
 // ---- the forward pass over n tokens whose rows are already on the device ----------------
 static LinearW lw(const cbt_linear& l, int fmt) {
   return LinearW{l.w, static_cast<const uint16_t*>(l.scales),
@@ -312,41 +385,67 @@ static LinearW lw(const cbt_linear& l, int fmt) {
 
 // n tokens (decode rows or packed prefill tokens); n_out rows get logits: all n when
 // gather == false, else the n_out rows listed in e->last_idx
-static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_keys, bool gather,
-                           int n_out, float* logits, int32_t* next) {
+// One projection y = x W^T over n rows, timed as class PROJ; algorithmic bytes: the weights
+// once, x in, y out (read and written again for a residual add).
+static void projection(cbt_engine* e, const float* x, int n, int K, const cbt_linear& W, int M,
+                       Epilogue epi, float* out) {
+  const cbt_model_config& c = e->cfg;
+  const int Mo = epi == EPI_SWIGLU ? M / 2 : M;
+  int t = tbegin(e, CBT_KCLASS_PROJ);
+  launch_linear(x, n, K, lw(W, c.weight_format), M, epi, out, e->part, e->part_floats, e->stream);
+  tend(e, t, weight_bytes(c, M, K) + 4.0 * n * K + 4.0 * n * Mo * (epi == EPI_ADD ? 2 : 1));
+}
+
+// n tokens (decode rows or packed prefill tokens); n_out rows get logits: all n when
+// gather == false, else the n_out rows listed in e->last_idx.  total_keys = sum over the
+// tokens of (pos + 1), the KV positions attention reads per layer and kv head.
+static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_keys,
+                           long long total_keys, bool gather, int n_out, float* logits,
+                           int32_t* next) {
   const cbt_model_config& c = e->cfg;
   cudaStream_t s = e->stream;
   const int d = c.d_model, qd = e->qd(), kvd = e->kvd(), F = c.d_ff;
-  const int fmt = c.weight_format;
   uint16_t* arena = static_cast<uint16_t*>(e->p.kv_arena);
+  const double attn_bytes = 2.0 * 2.0 * kvd * (double)total_keys  // K and V read (bf16)
+                            + 4.0 * n * (qd + 2 * kvd)              // q, k, v in
+                            + 2.0 * 2.0 * n * kvd + 4.0 * n * qd;   // K/V appended, o out
+  int t = tbegin(e, CBT_KCLASS_OTHER);
   launch_embed(tokens, n, static_cast<const uint16_t*>(e->w.embed), d, c.vocab, e->x, e->err, s);
   launch_rope_table(e->rows, n, c.head_dim, c.rope_theta, e->cosv, e->sinv, s);
+  tend(e, t, 2.0 * n * d + 4.0 * n * d);
   for (int l = 0; l < c.n_layers; ++l) {
     const cbt_layer_weights& L = e->layers[l];
+    t = tbegin(e, CBT_KCLASS_OTHER);
     launch_rmsnorm(e->x, static_cast<const uint16_t*>(L.attn_norm), n, d, c.rms_eps, e->h, s);
-    launch_linear(e->h, n, d, lw(L.wqkv, fmt), qd + 2 * kvd, EPI_STORE, e->qkv, e->part,
-                  e->part_floats, s);
+    tend(e, t, 8.0 * n * d);
+    projection(e, e->h, n, d, L.wqkv, qd + 2 * kvd, EPI_STORE, e->qkv);
+    t = tbegin(e, CBT_KCLASS_ATTN);
     launch_rope_append(e->qkv, e->rows, n, l, c.n_heads, c.n_kv_heads, c.head_dim, e->cosv,
                        e->sinv, arena, s);
     launch_attention_naive(e->qkv, e->rows, n, l, c.n_heads, c.n_kv_heads, c.head_dim, max_keys,
                            arena, e->o, s);
-    launch_linear(e->o, n, qd, lw(L.wo, fmt), d, EPI_ADD, e->x, e->part, e->part_floats, s);
+    tend(e, t, attn_bytes);
+    projection(e, e->o, n, qd, L.wo, d, EPI_ADD, e->x);
+    t = tbegin(e, CBT_KCLASS_OTHER);
     launch_rmsnorm(e->x, static_cast<const uint16_t*>(L.ffn_norm), n, d, c.rms_eps, e->h, s);
-    launch_linear(e->h, n, d, lw(L.wgu, fmt), 2 * F, EPI_SWIGLU, e->act, e->part, e->part_floats,
-                  s);
-    launch_linear(e->act, n, F, lw(L.wd, fmt), d, EPI_ADD, e->x, e->part, e->part_floats, s);
+    tend(e, t, 8.0 * n * d);
+    projection(e, e->h, n, d, L.wgu, 2 * F, EPI_SWIGLU, e->act);
+    projection(e, e->act, n, F, L.wd, d, EPI_ADD, e->x);
   }
   const float* xf = e->x;
+  float* hf = e->xg + (size_t)e->p.max_batch * d;
+  t = tbegin(e, CBT_KCLASS_OTHER);
   if (gather) {
     launch_gather_rows(e->x, e->last_idx, n_out, d, e->xg, s);
     xf = e->xg;
   }
-  float* hf = e->xg + (size_t)e->p.max_batch * d;
   launch_rmsnorm(xf, static_cast<const uint16_t*>(e->w.final_norm), n_out, d, c.rms_eps, hf, s);
+  tend(e, t, 8.0 * n_out * d);
   float* lg = logits ? logits : e->logits;
-  launch_linear(hf, n_out, d, lw(e->w.lm_head, fmt), c.vocab, EPI_STORE, lg, e->part,
-                e->part_floats, s);
+  projection(e, hf, n_out, d, e->w.lm_head, c.vocab, EPI_STORE, lg);
+  t = tbegin(e, CBT_KCLASS_OTHER);
   launch_argmax(lg, n_out, c.vocab, next ? next : e->next_tok, s);
+  tend(e, t, 4.0 * n_out * c.vocab);
   return cudaGetLastError();
 }
 
@@ -360,6 +459,7 @@ extern "C" cbt_status cbt_decode_step_batch(cbt_engine* e, const int32_t* ids, i
   if (B > e->p.max_batch) return CBT_ERR_BATCH;
   std::unordered_set<int> seen;
   int max_keys = 0;
+  long long total_keys = 0;
   for (int b = 0; b < B; ++b) {
     auto it = e->slabs.find(ids[b]);
     if (it == e->slabs.end()) return CBT_ERR_BAD_SLAB;
@@ -368,10 +468,11 @@ extern "C" cbt_status cbt_decode_step_batch(cbt_engine* e, const int32_t* ids, i
     if (sl.pos + 1 > sl.cap) return CBT_ERR_CAPACITY;
     e->hrows[b] = QueryRow{(long long)(sl.offset / 2), sl.pos, sl.cap};
     max_keys = std::max(max_keys, sl.pos + 1);
+    total_keys += sl.pos + 1;
   }
   cudaError_t rc = cudaMemcpyAsync(e->rows, e->hrows.data(), sizeof(QueryRow) * B,
                                    cudaMemcpyHostToDevice, e->stream);
-  if (rc == cudaSuccess) rc = forward(e, B, last_tokens, max_keys, false, B, logits, next_tokens);
+  if (rc == cudaSuccess) rc = forward(e, B, last_tokens, max_keys, total_keys, false, B, logits, next_tokens);
   if (rc != cudaSuccess) return CBT_ERR_CUDA;
   for (int b = 0; b < B; ++b) e->slabs[ids[b]].pos += 1;
   e->steps += 1;
@@ -387,7 +488,7 @@ extern "C" cbt_status cbt_prefill_segmented(cbt_engine* e, const int32_t* ids,
   if (!ids || !lens || !tokens) return CBT_ERR_NULL;
   if (K > e->p.max_batch) return CBT_ERR_BATCH;
   std::unordered_set<int> seen;
-  long long T = 0;
+  long long T = 0, total_keys = 0;
   int max_keys = 0;
   for (int s = 0; s < K; ++s) {
     auto it = e->slabs.find(ids[s]);
@@ -398,6 +499,7 @@ extern "C" cbt_status cbt_prefill_segmented(cbt_engine* e, const int32_t* ids,
     if ((long long)sl.pos + lens[s] > sl.cap) return CBT_ERR_CAPACITY;
     T += lens[s];
     max_keys = std::max(max_keys, sl.pos + lens[s]);
+    total_keys += (long long)lens[s] * sl.pos + (long long)lens[s] * (lens[s] + 1) / 2;
   }
   if (T > e->p.max_prefill_tokens) return CBT_ERR_TOKENS;
   int g = 0;
@@ -413,7 +515,7 @@ extern "C" cbt_status cbt_prefill_segmented(cbt_engine* e, const int32_t* ids,
     rc = cudaMemcpyAsync(e->last_idx, e->hidx.data(), sizeof(int32_t) * K, cudaMemcpyHostToDevice,
                          e->stream);
   if (rc == cudaSuccess)
-    rc = forward(e, (int)T, tokens, max_keys, true, K, logits, next_tokens);
+    rc = forward(e, (int)T, tokens, max_keys, total_keys, true, K, logits, next_tokens);
   if (rc != cudaSuccess) return CBT_ERR_CUDA;
   for (int s = 0; s < K; ++s) e->slabs[ids[s]].pos += lens[s];
   e->prefill_tokens += T;

@@ -213,8 +213,26 @@ cbt_status cbt_last_device_error(cbt_engine* e, int32_t* code, int32_t* info);
 
 cbt_status cbt_engine_stats(cbt_engine* e, cbt_stats* out);
 
-/* Number of kernel launches the engine queued so far (for launch accounting). */
+/* Number of kernel launches the library queued so far, all engines together (for launch
+ * accounting; e may be NULL). */
 int64_t cbt_kernel_launches(cbt_engine* e);
+
+/* Measurement.  Kernel classes: */
+#define CBT_KCLASS_PROJ 0  /* projections QKV, O, gate/up (+SwiGLU), down, lm_head: weight streaming */
+#define CBT_KCLASS_ATTN 1  /* RoPE + KV append and attention over the slabs */
+#define CBT_KCLASS_OTHER 2 /* embedding, norms, RoPE tables, argmax, gathers */
+#define CBT_NUM_KCLASSES 3
+
+/* Bracket every launch group of the classes in class_mask (bit k = class k) with CUDA
+ * events on the engine stream, from now on; 0 turns it off.  Clears earlier records.
+ * Events only mark the stream between kernels; they change no result. */
+cbt_status cbt_engine_set_timing(cbt_engine* e, int32_t class_mask);
+
+/* Synchronise the stream and sum the records of one class since cbt_engine_set_timing:
+ * total device milliseconds, number of bracketed intervals, and the algorithmic bytes those
+ * intervals moved (each weight once, activations in and out, each live KV position once). */
+cbt_status cbt_engine_timing(cbt_engine* e, int32_t kclass, double* total_ms, int64_t* intervals,
+                             double* algorithmic_bytes);
 
 /* MLX-style 4-bit affine quantisation of a bf16 matrix on the device, groups of `group`
  * (64) along each row: scale = bf16((max - min) / 15), bias = bf16(min),
