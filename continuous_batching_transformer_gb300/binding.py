@@ -20,7 +20,9 @@ OK = 0
 STATUS = {0: "CBT_OK", -1: "CBT_ERR_INVALID", -2: "CBT_ERR_NULL", -3: "CBT_ERR_BAD_SLAB",
           -4: "CBT_ERR_DUP_SLAB", -5: "CBT_ERR_BATCH", -6: "CBT_ERR_CAPACITY",
           -7: "CBT_ERR_POOL_EXHAUSTED", -8: "CBT_ERR_TOKENS", -9: "CBT_ERR_CUDA",
-          -10: "CBT_ERR_DEVICE", -11: "CBT_ERR_UNSUPPORTED"}
+          -10: "CBT_ERR_DEVICE", -11: "CBT_ERR_UNSUPPORTED", -12: "CBT_ERR_LIMIT"}
+NOALLOC_MAX_ROWS = 32
+NOALLOC_SCRATCH_BYTES = 20 << 20
 WEIGHTS_BF16, WEIGHTS_AFFINE4 = 0, 1
 DEV_OK, DEV_TOKEN_RANGE = 0, 1
 
@@ -30,7 +32,7 @@ EXPORTS = ["cbt_status_str", "cbt_engine_create", "cbt_engine_destroy", "cbt_sla
            "cbt_kv_slab_import", "cbt_kv_slab_export", "cbt_prefill_segmented",
            "cbt_decode_step_batch", "cbt_last_device_error", "cbt_engine_stats",
            "cbt_kernel_launches", "cbt_quantize_affine4", "cbt_engine_set_timing",
-           "cbt_engine_timing"]
+           "cbt_engine_timing", "cbt_greedy_head_noalloc"]
 KCLASS_PROJ, KCLASS_ATTN, KCLASS_OTHER = 0, 1, 2
 
 
@@ -109,6 +111,8 @@ def lib():
         L.cbt_kernel_launches.restype = ctypes.c_int64
         L.cbt_quantize_affine4.argtypes = [c_void, c_int32, c_int32, c_int32, c_void, c_void,
                                            c_void, c_void]
+        L.cbt_greedy_head_noalloc.argtypes = [P(ModelConfig), c_void, c_int32, c_void, P(Linear),
+                                              c_void, c_void, c_void]
         L.cbt_engine_set_timing.argtypes = [c_void, c_int32]
         L.cbt_engine_timing.argtypes = [c_void, c_int32, P(ctypes.c_double), P(ctypes.c_int64),
                                         P(ctypes.c_double)]
@@ -214,6 +218,16 @@ def engine_stats(e: int) -> Stats:
 
 def kernel_launches(e: int | None = None) -> int:
     return lib().cbt_kernel_launches(e)
+
+
+def greedy_head_noalloc(cfg: ModelConfig, hidden_ptr: int, n: int, final_norm_ptr: int,
+                        lm_head: Linear, logits_ptr: int, next_ptr: int | None,
+                        stream: int = 0) -> None:
+    """Final RMSNorm + lm_head + greedy argmax on caller-owned hidden states, using only the
+    library's fixed device scratch (no allocation; see include/cbt.h)."""
+    _check(lib().cbt_greedy_head_noalloc(ctypes.byref(cfg), hidden_ptr, n, final_norm_ptr,
+                                         ctypes.byref(lm_head), logits_ptr, next_ptr, stream),
+           "cbt_greedy_head_noalloc")
 
 
 def engine_set_timing(e: int, class_mask: int) -> None:

@@ -99,6 +99,7 @@ extern "C" const char* cbt_status_str(cbt_status s) {
     case CBT_ERR_CUDA: return "CUDA runtime error";
     case CBT_ERR_DEVICE: return "device error word set";
     case CBT_ERR_UNSUPPORTED: return "shape not supported";
+    case CBT_ERR_LIMIT: return "size above the fixed no-allocation scratch";
     default: return "unknown status";
   }
 }

@@ -67,6 +67,7 @@ typedef int32_t cbt_status;
 #define CBT_ERR_CUDA -9           /* a CUDA runtime call failed */
 #define CBT_ERR_DEVICE -10        /* the device error word was set (see below) */
 #define CBT_ERR_UNSUPPORTED -11   /* shape not supported by the kernels */
+#define CBT_ERR_LIMIT -12         /* size above the fixed scratch of cbt_greedy_head_noalloc */
 
 /* device error word codes, as returned by cbt_last_device_error in *code */
 #define CBT_DEV_OK 0
@@ -241,6 +242,40 @@ cbt_status cbt_engine_timing(cbt_engine* e, int32_t kclass, double* total_ms, in
  * scales, biases: device bf16 [rows][cols/group].  cols % group == 0.  Queued on `stream`. */
 cbt_status cbt_quantize_affine4(const void* w, int32_t rows, int32_t cols, int32_t group,
                                 void* packed, void* scales, void* biases, void* stream);
+
+/* ---- Greedy head without any allocation --------------------------------------------------
+ * The pages have no counterpart to this call; it exists for callers that cannot allocate
+ * device memory: code running where cudaMalloc is forbidden or unsafe (inside another
+ * framework's memory pool or allocator hooks, a real-time loop that must not block on the
+ * allocator, an embedding runtime that hands over pre-planned buffers only).  It runs the
+ * last stage of a decode step on hidden states the caller already has:
+ *   logits[r] = RMSNorm(hidden[r], final_norm, cfg->rms_eps) lm_head^T,
+ *   next_tokens[r] = argmax(logits[r]) (lowest id on ties),
+ * the same kernels decode_step_batch ends with, but its scratch (the normalised rows and
+ * the split-K partial sums of the projection) lives in one fixed array in the library's
+ * device memory, CBT_NOALLOC_SCRATCH_BYTES large.  Every GPU that loads the library holds
+ * that array until the process exits.
+ *   cfg          model config (d_model, vocab, rms_eps, weight_format, group_size are used)
+ *   hidden       device float [n][d_model], the residual stream after the last layer
+ *   n            rows, 0 <= n <= CBT_NOALLOC_MAX_ROWS (0 is a no-op)
+ *   final_norm   device bf16 [d_model]
+ *   lm_head      projection [vocab][d_model] as in cbt_linear (device pointers)
+ *   logits       device float [n][vocab], written
+ *   next_tokens  device int32 [n], written; may be NULL
+ *   stream       cudaStream_t to queue on (NULL = legacy default stream)
+ * Returns CBT_ERR_LIMIT, before queuing anything, when n > CBT_NOALLOC_MAX_ROWS or when
+ * n*d_model + (d_model/slice)*n*vocab floats (slice = 1024, 512 or 256, the largest that
+ * divides d_model) exceed the fixed scratch.  It calls no cudaMalloc, cudaFree or any
+ * allocating library routine.  The first call on each device looks up the array's device
+ * address (cudaGetSymbolAddress, with that device current); make that first call before
+ * any stream capture.  All calls share the one array and it keeps the last call's
+ * contents, so calls that overlap on the GPU (different streams, or threads) race: queue
+ * them on one stream, or order them with events. */
+#define CBT_NOALLOC_MAX_ROWS 32
+#define CBT_NOALLOC_SCRATCH_BYTES (20u << 20)
+cbt_status cbt_greedy_head_noalloc(const cbt_model_config* cfg, const float* hidden, int32_t n,
+                                   const void* final_norm, const cbt_linear* lm_head,
+                                   float* logits, int32_t* next_tokens, void* stream);
 
 #ifdef __cplusplus
 }
