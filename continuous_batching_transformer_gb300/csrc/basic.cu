@@ -53,6 +53,52 @@ void launch_rmsnorm(const float* x, const uint16_t* gain, int n, int d, float ep
   k_rmsnorm<<<n, 256, 0, s>>>(x, gain, d, eps, h);
 }
 
+// bf16 operand of a tensor-core projection: hi = bf16(v), and lo = bf16(v - hi) in rows
+// shifted by lo_rows when lo_rows > 0 (hi + lo carries about 16 significant bits)
+CBT_D void store_act(uint16_t* act, int row, int K, int k, int lo_rows, float v) {
+  const uint16_t hi = f32_to_bf16(v);
+  act[(size_t)row * K + k] = hi;
+  if (lo_rows > 0) act[(size_t)(lo_rows + row) * K + k] = f32_to_bf16(v - bf16_to_f32(hi));
+}
+
+__global__ void k_rmsnorm_act(const float* x, const uint16_t* gain, int d, float eps,
+                              uint16_t* act, int lo_rows) {
+  __shared__ float red[32];
+  const float* xr = x + (size_t)blockIdx.x * d;
+  float ss = 0.f;
+  for (int j = threadIdx.x; j < d; j += blockDim.x) ss = fmaf(xr[j], xr[j], ss);
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+    v = warp_sum(v);
+    if (threadIdx.x == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float r = rsqrtf(red[0] / (float)d + eps);
+  for (int j = threadIdx.x; j < d; j += blockDim.x)
+    store_act(act, blockIdx.x, d, j, lo_rows, xr[j] * r * bf16_to_f32(gain[j]));
+}
+
+void launch_rmsnorm_act(const float* x, const uint16_t* gain, int n, int d, float eps,
+                        uint16_t* act, int lo_rows, cudaStream_t s) {
+  if (n <= 0) return;
+  count_launch();
+  k_rmsnorm_act<<<n, 256, 0, s>>>(x, gain, d, eps, act, lo_rows);
+}
+
+__global__ void k_f32_to_act(const float* src, int K, uint16_t* act, int lo_rows) {
+  const float* sr = src + (size_t)blockIdx.x * K;
+  for (int k = threadIdx.x; k < K; k += blockDim.x) store_act(act, blockIdx.x, K, k, lo_rows, sr[k]);
+}
+
+void launch_f32_to_act(const float* src, int n, int K, uint16_t* act, int lo_rows, cudaStream_t s) {
+  if (n <= 0) return;
+  count_launch();
+  k_f32_to_act<<<n, 256, 0, s>>>(src, K, act, lo_rows);
+}
+
 // ---- RoPE angles once per call: cos/sin of pos * theta^(-2i/hd), evaluated in double -------
 __global__ void k_rope_table(const QueryRow* rows, int n, int half, int head_dim, double theta,
                              float* cosv, float* sinv) {

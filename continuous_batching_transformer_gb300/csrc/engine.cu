@@ -70,6 +70,22 @@ struct cbt_engine {
   std::vector<int32_t> hidx;
   int64_t steps = 0, prefill_tokens = 0;
 
+  // tensor-core path (bf16 weights): TMA descriptors of every weight matrix (64x64 boxes),
+  // bf16 operand buffers of the projections and the stream-K scratch
+  bool use_tc = false;
+  int num_sms = 0;
+  struct LayerMaps {
+    CUtensorMap qkv, o, gu, d;
+  };
+  std::vector<LayerMaps> wmaps;
+  CUtensorMap lm_map;
+  int act_rows = 0;
+  uint16_t *act_h = nullptr, *act_o = nullptr, *act_u = nullptr;
+  std::map<std::pair<const void*, int>, CUtensorMap> xmaps;  // (operand buffer, N tile)
+  float* tc_part = nullptr;
+  size_t tc_part_floats = 0;
+  int* tc_cnt = nullptr;
+
   // measurement: event pairs around launch groups of selected kernel classes
   struct TimeRec {
     int cls;
@@ -105,8 +121,10 @@ extern "C" const char* cbt_status_str(cbt_status s) {
 }
 
 static void free_scratch(cbt_engine* e) {
-  void* ptrs[] = {e->x, e->h, e->qkv, e->o, e->act, e->part, e->xg, e->logits, e->cosv,
-                  e->sinv, e->next_tok, e->last_idx, e->rows, e->err};
+  void* ptrs[] = {e->x,       e->h,        e->qkv,  e->o,     e->act,    e->part,
+                  e->xg,      e->logits,   e->cosv, e->sinv,  e->next_tok, e->last_idx,
+                  e->rows,    e->err,      e->act_h, e->act_o, e->act_u,  e->tc_part,
+                  e->tc_cnt};
   for (void* q : ptrs)
     if (q) cudaFree(q);
 }
@@ -190,11 +208,46 @@ extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_w
   chk(dmalloc(&e->rows, (size_t)T, &tot));
   chk(dmalloc(&e->err, 2, &tot));
   if (rc == cudaSuccess) rc = cudaMemsetAsync(e->err, 0, 2 * sizeof(int), e->stream);
+  bool maps_ok = true;
+  if (rc == cudaSuccess && c.weight_format == CBT_WEIGHTS_BF16) {
+    // tensor-core path: weight descriptors, bf16 operand buffers, stream-K scratch
+    int dev = 0;
+    chk(cudaGetDevice(&dev));
+    chk(cudaDeviceGetAttribute(&e->num_sms, cudaDevAttrMultiProcessorCount, dev));
+    e->act_rows = std::max(64, T);
+    chk(dmalloc(&e->act_h, (size_t)e->act_rows * std::max(c.d_model, qd), &tot));
+    chk(dmalloc(&e->act_o, (size_t)e->act_rows * qd, &tot));
+    chk(dmalloc(&e->act_u, (size_t)e->act_rows * c.d_ff, &tot));
+    e->tc_part_floats = (size_t)4 << 20;
+    chk(dmalloc(&e->tc_part, e->tc_part_floats, &tot));
+    const int max_tiles = std::max({(nqkv + 127) / 128, (c.d_model + 127) / 128, c.d_ff / 64,
+                                    (c.vocab + 127) / 128});
+    chk(dmalloc(&e->tc_cnt, (size_t)max_tiles, &tot));
+    if (rc == cudaSuccess) rc = cudaMemsetAsync(e->tc_cnt, 0, sizeof(int) * max_tiles, e->stream);
+    if (rc == cudaSuccess) {
+      const size_t arows = e->act_rows;
+      for (uint16_t* a : {e->act_h, e->act_o, e->act_u}) {
+        size_t cols = a == e->act_u ? c.d_ff : (a == e->act_o ? qd : std::max(c.d_model, qd));
+        rc = cudaMemsetAsync(a, 0, arows * cols * 2, e->stream);
+        if (rc != cudaSuccess) break;
+      }
+    }
+    e->wmaps.resize(c.n_layers);
+    for (int l = 0; l < c.n_layers && maps_ok; ++l) {
+      const cbt_layer_weights& L = w->layers[l];
+      maps_ok = make_tmap_bf16(&e->wmaps[l].qkv, L.wqkv.w, c.d_model, nqkv, 64, 64) &&
+                make_tmap_bf16(&e->wmaps[l].o, L.wo.w, qd, c.d_model, 64, 64) &&
+                make_tmap_bf16(&e->wmaps[l].gu, L.wgu.w, c.d_model, 2 * c.d_ff, 64, 64) &&
+                make_tmap_bf16(&e->wmaps[l].d, L.wd.w, c.d_ff, c.d_model, 64, 64);
+    }
+    maps_ok = maps_ok && make_tmap_bf16(&e->lm_map, w->lm_head.w, c.d_model, c.vocab, 64, 64);
+    e->use_tc = maps_ok && c.d_ff % 64 == 0;
+  }
   if (rc == cudaSuccess) rc = cudaStreamSynchronize(e->stream);
-  if (rc != cudaSuccess) {
+  if (rc != cudaSuccess || !maps_ok) {
     free_scratch(e);
     delete e;
-    return CBT_ERR_CUDA;
+    return rc != cudaSuccess ? CBT_ERR_CUDA : CBT_ERR_UNSUPPORTED;
   }
   e->scratch_bytes = tot;
   e->hrows.resize(T);
@@ -397,6 +450,49 @@ static void projection(cbt_engine* e, const float* x, int n, int K, const cbt_li
   tend(e, t, weight_bytes(c, M, K) + 4.0 * n * K + 4.0 * n * Mo * (epi == EPI_ADD ? 2 : 1));
 }
 
+// Tensor-core path.  Up to 32 rows go through the projections as bf16 hi/lo pairs (lo parts
+// at row BN/2 of the operand buffer); more rows as plain bf16.
+static int tc_lo_rows(int n) { return n <= 32 ? tc_split_bn(n) / 2 : 0; }
+
+static const CUtensorMap* xmap(cbt_engine* e, const uint16_t* buf, int K, int BN) {
+  auto key = std::make_pair(static_cast<const void*>(buf), BN);
+  auto it = e->xmaps.find(key);
+  if (it != e->xmaps.end()) return &it->second;
+  CUtensorMap m;
+  if (!make_tmap_bf16(&m, buf, K, e->act_rows, 64, BN)) return nullptr;
+  return &(e->xmaps[key] = m);
+}
+
+// y = x W^T over n rows on the tensor cores, operand x in the bf16 buffer xbuf [rows][K];
+// timed as class PROJ with the same algorithmic bytes as the CUDA-core path
+static bool tc_projection(cbt_engine* e, const CUtensorMap& wmap, const uint16_t* xbuf, int n,
+                          int K, int M, Epilogue epi, float* out, int ldo, uint16_t* act_out,
+                          int act_ld) {
+  const bool split = n <= 32;
+  const int BN = split ? tc_split_bn(n) : tc_plain_bn(n);
+  const CUtensorMap* xm = xmap(e, xbuf, K, BN);
+  if (!xm) return false;
+  TcParams p{};
+  p.M = M;
+  p.K = K;
+  p.F = epi == EPI_SWIGLU ? M / 2 : 0;
+  p.n_act = n;
+  p.epi = epi;
+  p.out = out;
+  p.ldo = ldo;
+  p.act = act_out;
+  p.act_ld = act_ld;
+  p.act_lo = split ? BN / 2 : 0;
+  p.part = e->tc_part;
+  p.cnt = e->tc_cnt;
+  p.err = e->err;
+  const int Mo = epi == EPI_SWIGLU ? M / 2 : M;
+  int t = tbegin(e, CBT_KCLASS_PROJ);
+  bool ok = launch_tc_linear(wmap, *xm, p, split, BN, e->num_sms, e->tc_part_floats, e->stream);
+  tend(e, t, weight_bytes(e->cfg, M, K) + 4.0 * n * K + 4.0 * n * Mo * (epi == EPI_ADD ? 2 : 1));
+  return ok;
+}
+
 // n tokens (decode rows or packed prefill tokens); n_out rows get logits: all n when
 // gather == false, else the n_out rows listed in e->last_idx.  total_keys = sum over the
 // tokens of (pos + 1), the KV positions attention reads per layer and kv head.
@@ -410,29 +506,51 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
   const double attn_bytes = 2.0 * 2.0 * kvd * (double)total_keys  // K and V read (bf16)
                             + 4.0 * n * (qd + 2 * kvd)              // q, k, v in
                             + 2.0 * 2.0 * n * kvd + 4.0 * n * qd;   // K/V appended, o out
+  const bool tcp = e->use_tc;
+  const int lo = tc_lo_rows(n), lo_out = tc_lo_rows(n_out);
+  bool ok = true;
   int t = tbegin(e, CBT_KCLASS_OTHER);
   launch_embed(tokens, n, static_cast<const uint16_t*>(e->w.embed), d, c.vocab, e->x, e->err, s);
   launch_rope_table(e->rows, n, c.head_dim, c.rope_theta, e->cosv, e->sinv, s);
   tend(e, t, 2.0 * n * d + 4.0 * n * d);
-  for (int l = 0; l < c.n_layers; ++l) {
+  for (int l = 0; l < c.n_layers && ok; ++l) {
     const cbt_layer_weights& L = e->layers[l];
+    const uint16_t* an = static_cast<const uint16_t*>(L.attn_norm);
+    const uint16_t* fn = static_cast<const uint16_t*>(L.ffn_norm);
     t = tbegin(e, CBT_KCLASS_OTHER);
-    launch_rmsnorm(e->x, static_cast<const uint16_t*>(L.attn_norm), n, d, c.rms_eps, e->h, s);
+    if (tcp) launch_rmsnorm_act(e->x, an, n, d, c.rms_eps, e->act_h, lo, s);
+    else launch_rmsnorm(e->x, an, n, d, c.rms_eps, e->h, s);
     tend(e, t, 8.0 * n * d);
-    projection(e, e->h, n, d, L.wqkv, qd + 2 * kvd, EPI_STORE, e->qkv);
+    if (tcp)
+      ok &= tc_projection(e, e->wmaps[l].qkv, e->act_h, n, d, qd + 2 * kvd, EPI_STORE, e->qkv,
+                          qd + 2 * kvd, nullptr, 0);
+    else
+      projection(e, e->h, n, d, L.wqkv, qd + 2 * kvd, EPI_STORE, e->qkv);
     t = tbegin(e, CBT_KCLASS_ATTN);
     launch_rope_append(e->qkv, e->rows, n, l, c.n_heads, c.n_kv_heads, c.head_dim, e->cosv,
                        e->sinv, arena, s);
     launch_attention_naive(e->qkv, e->rows, n, l, c.n_heads, c.n_kv_heads, c.head_dim, max_keys,
                            arena, e->o, s);
+    if (tcp) launch_f32_to_act(e->o, n, qd, e->act_o, lo, s);
     tend(e, t, attn_bytes);
-    projection(e, e->o, n, qd, L.wo, d, EPI_ADD, e->x);
+    if (tcp)
+      ok &= tc_projection(e, e->wmaps[l].o, e->act_o, n, qd, d, EPI_ADD, e->x, d, nullptr, 0);
+    else
+      projection(e, e->o, n, qd, L.wo, d, EPI_ADD, e->x);
     t = tbegin(e, CBT_KCLASS_OTHER);
-    launch_rmsnorm(e->x, static_cast<const uint16_t*>(L.ffn_norm), n, d, c.rms_eps, e->h, s);
+    if (tcp) launch_rmsnorm_act(e->x, fn, n, d, c.rms_eps, e->act_h, lo, s);
+    else launch_rmsnorm(e->x, fn, n, d, c.rms_eps, e->h, s);
     tend(e, t, 8.0 * n * d);
-    projection(e, e->h, n, d, L.wgu, 2 * F, EPI_SWIGLU, e->act);
-    projection(e, e->act, n, F, L.wd, d, EPI_ADD, e->x);
+    if (tcp) {
+      ok &= tc_projection(e, e->wmaps[l].gu, e->act_h, n, d, 2 * F, EPI_SWIGLU, nullptr, 0,
+                          e->act_u, F);
+      ok &= tc_projection(e, e->wmaps[l].d, e->act_u, n, F, d, EPI_ADD, e->x, d, nullptr, 0);
+    } else {
+      projection(e, e->h, n, d, L.wgu, 2 * F, EPI_SWIGLU, e->act);
+      projection(e, e->act, n, F, L.wd, d, EPI_ADD, e->x);
+    }
   }
+  if (!ok) return cudaErrorNotSupported;
   const float* xf = e->x;
   float* hf = e->xg + (size_t)e->p.max_batch * d;
   t = tbegin(e, CBT_KCLASS_OTHER);
@@ -440,10 +558,17 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
     launch_gather_rows(e->x, e->last_idx, n_out, d, e->xg, s);
     xf = e->xg;
   }
-  launch_rmsnorm(xf, static_cast<const uint16_t*>(e->w.final_norm), n_out, d, c.rms_eps, hf, s);
+  const uint16_t* gn = static_cast<const uint16_t*>(e->w.final_norm);
+  if (tcp) launch_rmsnorm_act(xf, gn, n_out, d, c.rms_eps, e->act_h, lo_out, s);
+  else launch_rmsnorm(xf, gn, n_out, d, c.rms_eps, hf, s);
   tend(e, t, 8.0 * n_out * d);
   float* lg = logits ? logits : e->logits;
-  projection(e, hf, n_out, d, e->w.lm_head, c.vocab, EPI_STORE, lg);
+  if (tcp) {
+    if (!tc_projection(e, e->lm_map, e->act_h, n_out, d, c.vocab, EPI_STORE, lg, c.vocab, nullptr, 0))
+      return cudaErrorNotSupported;
+  } else {
+    projection(e, hf, n_out, d, e->w.lm_head, c.vocab, EPI_STORE, lg);
+  }
   t = tbegin(e, CBT_KCLASS_OTHER);
   launch_argmax(lg, n_out, c.vocab, next ? next : e->next_tok, s);
   tend(e, t, 4.0 * n_out * c.vocab);
@@ -474,7 +599,7 @@ extern "C" cbt_status cbt_decode_step_batch(cbt_engine* e, const int32_t* ids, i
   cudaError_t rc = cudaMemcpyAsync(e->rows, e->hrows.data(), sizeof(QueryRow) * B,
                                    cudaMemcpyHostToDevice, e->stream);
   if (rc == cudaSuccess) rc = forward(e, B, last_tokens, max_keys, total_keys, false, B, logits, next_tokens);
-  if (rc != cudaSuccess) return CBT_ERR_CUDA;
+  if (rc != cudaSuccess) return rc == cudaErrorNotSupported ? CBT_ERR_UNSUPPORTED : CBT_ERR_CUDA;
   for (int b = 0; b < B; ++b) e->slabs[ids[b]].pos += 1;
   e->steps += 1;
   return CBT_OK;
@@ -517,7 +642,7 @@ extern "C" cbt_status cbt_prefill_segmented(cbt_engine* e, const int32_t* ids,
                          e->stream);
   if (rc == cudaSuccess)
     rc = forward(e, (int)T, tokens, max_keys, total_keys, true, K, logits, next_tokens);
-  if (rc != cudaSuccess) return CBT_ERR_CUDA;
+  if (rc != cudaSuccess) return rc == cudaErrorNotSupported ? CBT_ERR_UNSUPPORTED : CBT_ERR_CUDA;
   for (int s = 0; s < K; ++s) e->slabs[ids[s]].pos += lens[s];
   e->prefill_tokens += T;
   return CBT_OK;

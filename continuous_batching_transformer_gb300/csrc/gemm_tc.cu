@@ -1,0 +1,425 @@
+// gemm_tc.cu -- projections y = x W^T on the 5th-generation tensor cores (sm_103a).
+//
+// Swap-AB: the weight rows are the MMA's M side (128 per tile), the activation rows its N
+// side, so a decode step with B rows is one 128 x N x 64 MMA chain per weight tile and every
+// weight byte crosses HBM once.  Per CTA: one TMA producer thread streams 128x64 bf16 weight
+// tiles and Nx64 activation tiles into a ring of 128-byte-swizzled shared-memory stages;
+// one thread issues tcgen05.mma into a double-buffered TMEM accumulator; four epilogue warps
+// read the accumulator back (tcgen05.ld) and apply the epilogue (store, residual add, or
+// SwiGLU into the next projection's bf16 operand).
+//
+// Decode (SPLIT): activations enter as bf16 hi/lo pairs (x = hi + lo), rows [0, BN/2) hi and
+// [BN/2, BN) lo, summed in the epilogue -- fp32-grade operands at no cost, since the N side
+// is padded anyway.  Work is split stream-K: the (row block, k-step) units are divided evenly
+// over the grid, so every CTA streams the same number of weight bytes; a row block cut
+// between CTAs is finished by whichever CTA completes it last, summing the partial sums in
+// a fixed order, so results do not depend on timing.
+// Prefill (!SPLIT): plain bf16 activations, N tiles of up to 256 tokens, whole tiles per CTA.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "kernels.h"
+#include "tc_common.cuh"
+
+namespace {
+
+constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA (+TMEM alloc), warps 2..5 epilogue
+constexpr int kABytes = 128 * 128;  // 128 rows x 64 bf16
+
+struct Sched {
+  long long u, u1;
+  int t;
+  __device__ void init(const TcParams& p) {
+    if (p.streamk) {
+      u = (long long)blockIdx.x * p.U / gridDim.x;
+      u1 = (long long)(blockIdx.x + 1) * p.U / gridDim.x;
+    } else {
+      t = blockIdx.x;
+    }
+  }
+  __device__ bool next(const TcParams& p, int& tile, int& kb, int& ke) {
+    if (p.streamk) {
+      if (u >= u1) return false;
+      tile = (int)(u / p.KS);
+      kb = (int)(u % p.KS);
+      long long rem = u1 - u;
+      ke = (int)((long long)p.KS < kb + rem ? (long long)p.KS : kb + rem);
+      u += ke - kb;
+      return true;
+    }
+    if (t >= p.RB * p.NT) return false;
+    tile = t;
+    kb = 0;
+    ke = p.KS;
+    t += gridDim.x;
+    return true;
+  }
+};
+
+// CTA whose stream-K range holds unit u (ranges are [c*U/G, (c+1)*U/G))
+__host__ __device__ inline int cta_of_unit(long long U, long long G, long long u) {
+  long long c = u * G / U;
+  while (c + 1 < G && (c + 1) * U / G <= u) ++c;
+  while (c > 0 && c * U / G > u) --c;
+  return (int)c;
+}
+
+__device__ __forceinline__ void report_timeout(const TcParams& p, volatile int* abort, int role) {
+  *abort = 1;
+  if (atomicCAS(p.err, 0, CBT_DEV_TIMEOUT) == 0) p.err[1] = role;
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  for (uint32_t i = 0; i < tc::kSpinLimit; ++i) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    if ((i & 1023) == 1023 && *abort) return false;
+    if (i > 256) __nanosleep(32);
+  }
+  return false;
+}
+
+// Final epilogue of `cnt` columns (tokens tok0 .. tok0+cnt-1) of tile row r of row block rb.
+__device__ __forceinline__ void finish(const TcParams& p, int rb, int r, const float* vals,
+                                       int tok0, int cnt, float* swx) {
+  if (p.epi != EPI_SWIGLU) {
+    const int m = rb * 128 + r;
+    if (m < p.M) {
+      for (int j = 0; j < cnt; ++j) {
+        const int t = tok0 + j;
+        if (t < p.n_act) {
+          float* o = p.out + (size_t)t * p.ldo + m;
+          if (p.epi == EPI_ADD) *o += vals[j];
+          else *o = vals[j];
+        }
+      }
+    }
+    return;
+  }
+  // SwiGLU: tile rows 0..63 are gate rows, 64..127 the up rows of the same 64 features
+  tc::named_bar_sync(1, 128);
+  if (r >= 64)
+    for (int j = 0; j < cnt; ++j) swx[(r - 64) * 33 + j] = vals[j];
+  tc::named_bar_sync(1, 128);
+  if (r < 64) {
+    const int f = rb * 64 + r;
+    if (f < p.F) {
+      for (int j = 0; j < cnt; ++j) {
+        const int t = tok0 + j;
+        if (t < p.n_act) {
+          const float g = vals[j], u = swx[r * 33 + j];
+          const float a = g / (1.f + expf(-g)) * u;
+          const uint16_t hi = f32_to_bf16(a);
+          p.act[(size_t)t * p.act_ld + f] = hi;
+          if (p.act_lo) p.act[(size_t)(p.act_lo + t) * p.act_ld + f] = f32_to_bf16(a - bf16_to_f32(hi));
+        }
+      }
+    }
+  }
+}
+
+template <int BN, int STAGES, bool SPLIT>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_tc_linear(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tx,
+                const TcParams p) {
+  constexpr int kXBytes = BN * 128;
+  constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
+  constexpr uint32_t kIdesc = tc::idesc_bf16(128, BN);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sX = smem + STAGES * kABytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sX + STAGES * kXBytes);
+  uint64_t* empty = full + STAGES;
+  uint64_t* accf = empty + STAGES;
+  uint64_t* acce = accf + 2;
+  uint64_t* done = acce + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* sflag = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [0] last, [1] abort
+  float* swx = reinterpret_cast<float*>(smem + STAGES * (kABytes + kXBytes) + 512);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(&accf[a], 1);
+      tc::mbar_init(&acce[a], 4);
+    }
+    tc::mbar_init(done, 1);
+    sflag[0] = 0;
+    sflag[1] = 0;
+    tc::mbar_fence_init();
+    tc::tma_prefetch_desc(&tw);
+    tc::tma_prefetch_desc(&tx);
+  }
+  if (warp == 1) tc::tmem_alloc(tmem_slot, kTmemCols);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  Sched sch;
+  sch.init(p);
+  int tile, kb, ke;
+  if (warp == 0) {
+    if (lane == 0) {  // ---- TMA producer
+      const uint64_t pol_w = tc::policy_evict_first(), pol_x = tc::policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      while (ok && sch.next(p, tile, kb, ke)) {
+        const int rb = tile / p.NT, nt = tile % p.NT;
+        const int y0 = p.epi == EPI_SWIGLU ? rb * 64 : rb * 128;
+        const int y1 = p.epi == EPI_SWIGLU ? p.F + rb * 64 : rb * 128 + 64;
+        for (int k = kb; k < ke; ++k) {
+          if (!wait_or_abort(&empty[stage], phase ^ 1, sflag + 1)) {
+            report_timeout(p, sflag + 1, 1);
+            ok = false;
+            break;
+          }
+          tc::mbar_expect_tx(&full[stage], kABytes + kXBytes);
+          tc::tma_load_2d(sA + stage * kABytes, &tw, &full[stage], k * 64, y0, pol_w);
+          tc::tma_load_2d(sA + stage * kABytes + 8192, &tw, &full[stage], k * 64, y1, pol_w);
+          tc::tma_load_2d(sX + stage * kXBytes, &tx, &full[stage], k * 64, nt * BN, pol_x);
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // never leave with copies in flight: wait for the last loads issued to each stage
+      for (int i = 0; i < STAGES && i < issued; ++i) {
+        if (--stage < 0) {
+          stage = STAGES - 1;
+          phase ^= 1;
+        }
+        tc::mbar_wait(&full[stage], phase);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // ---- MMA issuer
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      while (ok && sch.next(p, tile, kb, ke)) {
+        if (!wait_or_abort(&acce[acc], acc_phase ^ 1, sflag + 1)) {
+          report_timeout(p, sflag + 1, 2);
+          break;
+        }
+        tc::tc_fence_after();
+        const uint32_t d = tmem + acc * BN;
+        for (int k = kb; k < ke; ++k) {
+          if (!wait_or_abort(&full[stage], phase, sflag + 1)) {
+            report_timeout(p, sflag + 1, 3);
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sA + stage * kABytes));
+          const uint64_t xd = tc::sdesc_sw128(tc::smem_u32(sX + stage * kXBytes));
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc::mma_bf16(d, ad + 2 * kk, xd + 2 * kk, kIdesc, (k > kb || kk > 0) ? 1u : 0u);
+          tc::mma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc::mma_commit(&accf[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      // all MMAs of this thread complete before TMEM is released
+      tc::mma_commit(done);
+      tc::mbar_wait(done, 0);
+    }
+  } else {  // ---- epilogue warps 2..5
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int r = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    while (sch.next(p, tile, kb, ke)) {
+      if (!wait_or_abort(&accf[acc], acc_phase, sflag + 1)) {
+        report_timeout(p, sflag + 1, 4);
+        break;
+      }
+      tc::tc_fence_after();
+      const int rb = tile / p.NT, nt = tile % p.NT;
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      if (SPLIT) {
+        constexpr int H = BN / 2;
+        uint32_t raw[BN];
+#pragma unroll
+        for (int c = 0; c < BN / 16; ++c) tc::tmem_ld16(taddr + 16 * c, raw + 16 * c);
+        tc::tmem_ld_wait();
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&acce[acc]);
+        float vals[H];
+#pragma unroll
+        for (int n = 0; n < H; ++n) vals[n] = __uint_as_float(raw[n]) + __uint_as_float(raw[n + H]);
+        if (kb == 0 && ke == p.KS) {
+          finish(p, rb, r, vals, 0, H, swx);
+        } else {
+          const int first = cta_of_unit(p.U, gridDim.x, (long long)tile * p.KS);
+          const int slot = blockIdx.x - first;
+          float* pp = p.part + ((size_t)tile * p.slots + slot) * H * 128;
+#pragma unroll
+          for (int n = 0; n < H; ++n)
+            if (n < p.n_act) pp[n * 128 + r] = vals[n];
+          __threadfence();
+          tc::named_bar_sync(1, 128);
+          if (threadIdx.x == 64) {
+            const int old = atomicAdd(p.cnt + tile, ke - kb);
+            sflag[0] = (old + (ke - kb) == p.KS) ? 1 : 0;
+          }
+          tc::named_bar_sync(1, 128);
+          if (sflag[0]) {
+            __threadfence();
+            const int last = cta_of_unit(p.U, gridDim.x, (long long)tile * p.KS + p.KS - 1);
+            float sum[H];
+#pragma unroll
+            for (int n = 0; n < H; ++n) sum[n] = 0.f;
+            for (int s = 0; s <= last - first; ++s) {
+              const float* ps = p.part + ((size_t)tile * p.slots + s) * H * 128;
+#pragma unroll
+              for (int n = 0; n < H; ++n)
+                if (n < p.n_act) sum[n] += __ldcg(ps + n * 128 + r);
+            }
+            finish(p, rb, r, sum, 0, H, swx);
+            if (threadIdx.x == 64) p.cnt[tile] = 0;
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t raw[32];
+          tc::tmem_ld16(taddr + c0, raw);
+          tc::tmem_ld16(taddr + c0 + 16, raw + 16);
+          tc::tmem_ld_wait();
+          float vals[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) vals[j] = __uint_as_float(raw[j]);
+          finish(p, rb, r, vals, nt * BN + c0, 32, swx);
+        }
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&acce[acc]);
+      }
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int BN, int STAGES, bool SPLIT>
+cudaError_t launch_inst(const CUtensorMap& tw, const CUtensorMap& tx, const TcParams& p, int grid,
+                        cudaStream_t s) {
+  constexpr size_t smem = 1024 + STAGES * (kABytes + BN * 128) + 512 + 64 * 33 * 4;
+  static_assert(smem <= 227 * 1024, "shared memory budget");
+  auto kern = k_tc_linear<BN, STAGES, SPLIT>;
+  cudaError_t rc = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (rc != cudaSuccess) return rc;
+  count_launch();
+  kern<<<grid, kThreads, smem, s>>>(tw, tx, p);
+  return cudaGetLastError();
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+}  // namespace
+
+bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                    uint32_t box_inner, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn || !base || (reinterpret_cast<uintptr_t>(base) & 15) || (inner * 2) % 16) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int tc_split_bn(int n) { return n <= 8 ? 16 : (n <= 16 ? 32 : 64); }
+int tc_plain_bn(int n) { return n <= 64 ? 64 : (n <= 128 ? 128 : 256); }
+
+// Plan and launch one projection.  p carries shapes, epilogue and outputs; this fills the
+// schedule.  Returns false if the shape is outside what the kernel supports.
+bool launch_tc_linear(const CUtensorMap& tw, const CUtensorMap& tx, TcParams p, bool split, int BN,
+                      int num_sms, size_t part_floats, cudaStream_t s) {
+  if (p.K % 64 || p.K <= 0 || p.n_act <= 0) return false;
+  if (p.epi == EPI_SWIGLU && (p.F % 64 || p.M != 2 * p.F)) return false;
+  p.RB = p.epi == EPI_SWIGLU ? p.F / 64 : (p.M + 127) / 128;
+  p.KS = p.K / 64;
+  if (split) {
+    if (2 * p.n_act > BN) return false;
+    p.NT = 1;
+    p.streamk = 1;
+    p.U = (long long)p.RB * p.KS;
+    int G = (int)std::min<long long>(num_sms, p.U);
+    // partial slots per tile: most CTAs whose ranges meet one tile
+    for (;;) {
+      int slots = 1;
+      for (int t = 0; t < p.RB; ++t) {
+        int f = cta_of_unit(p.U, G, (long long)t * p.KS);
+        int l = cta_of_unit(p.U, G, (long long)t * p.KS + p.KS - 1);
+        slots = std::max(slots, l - f + 1);
+      }
+      if ((size_t)p.RB * slots * (BN / 2) * 128 <= part_floats || G == 1) {
+        p.slots = slots;
+        break;
+      }
+      G = std::max(1, G / 2);
+    }
+    if ((size_t)p.RB * p.slots * (BN / 2) * 128 > part_floats) return false;
+    cudaError_t rc;
+    if (BN == 16) rc = launch_inst<16, 8, true>(tw, tx, p, G, s);
+    else if (BN == 32) rc = launch_inst<32, 8, true>(tw, tx, p, G, s);
+    else if (BN == 64) rc = launch_inst<64, 8, true>(tw, tx, p, G, s);
+    else return false;
+    return rc == cudaSuccess;
+  }
+  p.NT = (p.n_act + BN - 1) / BN;
+  p.streamk = 0;
+  p.U = (long long)p.RB * p.NT * p.KS;
+  p.slots = 0;
+  const int tiles = p.RB * p.NT;
+  const int G = std::min(tiles, num_sms);
+  cudaError_t rc;
+  if (BN == 64) rc = launch_inst<64, 8, false>(tw, tx, p, G, s);
+  else if (BN == 128) rc = launch_inst<128, 6, false>(tw, tx, p, G, s);
+  else if (BN == 256) rc = launch_inst<256, 4, false>(tw, tx, p, G, s);
+  else return false;
+  return rc == cudaSuccess;
+}

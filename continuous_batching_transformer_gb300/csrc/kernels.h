@@ -1,5 +1,6 @@
 // kernels.h -- launchers of the engine's CUDA kernels (host side).
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -15,6 +16,42 @@ struct LinearW {
   const uint16_t* biases;
   int fmt;             // CBT_WEIGHTS_BF16 / CBT_WEIGHTS_AFFINE4
 };
+
+// ---- tensor-core projections (gemm_tc.cu) --------------------------------------------------
+struct TcParams {
+  int M, K;          // W is [M][K] bf16; for EPI_SWIGLU M = 2F (gate rows, then up rows)
+  int F;             // EPI_SWIGLU: features per output row
+  int n_act;         // activation rows (decode rows or prefill tokens)
+  int epi;           // Epilogue
+  float* out;        // EPI_STORE / EPI_ADD: fp32 [n_act][ldo]
+  int ldo;
+  uint16_t* act;     // EPI_SWIGLU: bf16 operand of the next projection, [rows][act_ld]
+  int act_ld;
+  int act_lo;        // row offset of the lo parts (0: plain bf16, no lo part)
+  // schedule, filled by launch_tc_linear
+  int RB, NT, KS;
+  long long U;
+  int streamk, slots;
+  float* part;       // stream-K partial sums
+  int* cnt;          // per-tile completion counters, zero between launches
+  int* err;          // device error word
+};
+
+
+bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                    uint32_t box_inner, uint32_t box_rows);
+// N tile for hi/lo (split) activations of n rows, and for plain bf16 activations
+int tc_split_bn(int n);
+int tc_plain_bn(int n);
+bool launch_tc_linear(const CUtensorMap& tw, const CUtensorMap& tx, TcParams p, bool split,
+                      int BN, int num_sms, size_t part_floats, cudaStream_t s);
+
+// RMSNorm rows of x into a bf16 operand: hi parts at rows [0, n), lo parts at rows
+// [lo_rows, lo_rows + n) when lo_rows > 0
+void launch_rmsnorm_act(const float* x, const uint16_t* gain, int n, int d, float eps,
+                        uint16_t* act, int lo_rows, cudaStream_t s);
+// fp32 rows into a bf16 operand (hi/lo as above)
+void launch_f32_to_act(const float* src, int n, int K, uint16_t* act, int lo_rows, cudaStream_t s);
 
 // embed + token range check
 void launch_embed(const int32_t* tokens, int n, const uint16_t* table, int d, int vocab, float* x,

@@ -72,6 +72,7 @@ typedef int32_t cbt_status;
 /* device error word codes, as returned by cbt_last_device_error in *code */
 #define CBT_DEV_OK 0
 #define CBT_DEV_TOKEN_RANGE 1 /* a token id outside [0, vocab) */
+#define CBT_DEV_TIMEOUT 2     /* a kernel's bounded wait ran out; it stopped early (info: role) */
 
 #define CBT_WEIGHTS_BF16 0    /* bf16, row-major [out][in] */
 #define CBT_WEIGHTS_AFFINE4 1 /* 4-bit affine, see cbt_linear */
