@@ -1,0 +1,354 @@
+// attn_tc.cu -- decode attention on the 5th-generation tensor cores (sm_103a).
+//
+// Split-K flash decoding over each row's own slab: a work item is (row b, kv head g, a run of
+// 128-key sub-chunks).  All q heads of the kv head's group are processed together, so the
+// group's K/V is read from HBM once.  For each sub-chunk:
+//   S^T[key][j] = K[key] . Q[j]   tcgen05.mma, M = 128 keys, N = 16 (q rows: 8 hi + 8 lo parts)
+//   softmax on S^T: one thread per key (TMEM lane = key), running max/sum per head
+//   O^T[d][j]  = V^T[d] . P[j]    tcgen05.mma, M = 128 dims, N = 16 (p rows: 8 hi + 8 lo)
+// and O is accumulated in registers (one thread per dim) with the running-max rescale.
+// K and V^T tiles come from two arena-wide TMA tensor maps (K rows of head_dim, V rows of 64
+// keys) into a 3-stage ring filled by a producer warp; Q and P are written by the threads in
+// the 128-byte swizzle the MMA descriptors expect.  Items run on a persistent grid.  Each
+// item leaves unnormalised partial outputs with their (max, sum); attn_merge combines them.
+#include "kernels.h"
+#include "tc_common.cuh"
+
+namespace {
+
+constexpr int kSub = 128;        // keys per sub-chunk (MMA M)
+constexpr int kStages = 3;
+constexpr int kBox = 16384;      // one 128 x 128-byte TMA box
+constexpr int kCompute = 128;    // threads of warps 0..3; warp 4 is the TMA producer
+
+// byte offset of bf16 element (row, col) in a K-major tile of 128-byte rows, 128B-swizzled,
+// whose 64-column groups are `group_stride` bytes apart
+__device__ __forceinline__ uint32_t sw128_off(int row, int col, int group_stride) {
+  const int g = col >> 6, c = col & 63;
+  return (uint32_t)(g * group_stride + row * 128 + ((((c >> 3) ^ (row & 7))) << 4) + (c & 7) * 2);
+}
+
+__device__ __forceinline__ void st_bf16(uint8_t* base, uint32_t off, uint16_t v) {
+  *reinterpret_cast<uint16_t*>(base + off) = v;
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// barrier over `n` threads that also returns whether `pred` held in any of them, so that a
+// failed (timed-out) wait makes every participant leave together
+__device__ __forceinline__ bool bar_any(int id, int n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+template <int HD>
+__global__ void __launch_bounds__(160, 1)
+    k_attn_decode(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                  const float* __restrict__ qkv, const QueryRow* __restrict__ rows,
+                  const AttnItem* __restrict__ items, int n_items, int layer, int n_heads,
+                  int n_kv_heads, float* __restrict__ part_o, float2* __restrict__ part_ml,
+                  int* err) {
+  constexpr int nKh = HD / 64;                 // K boxes (64 dims each) per sub-chunk
+  constexpr int kStageBytes = (nKh + 2) * kBox;  // K boxes + two V^T boxes
+  constexpr uint32_t kIdesc = tc::idesc_bf16(128, 16);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* stages = smem;
+  uint8_t* sQ = smem + kStages * kStageBytes;   // [16 rows][HD], nKh groups of 2 KB
+  uint8_t* sP = sQ + nKh * 2048;                // [16 rows][128 keys], 2 groups of 2 KB
+  uint64_t* full = reinterpret_cast<uint64_t*>(sP + 2 * 2048);
+  uint64_t* empty = full + kStages;
+  uint64_t* bar_s = empty + kStages;
+  uint64_t* bar_o = bar_s + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_o + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* red = reinterpret_cast<float*>(tmem_slot + 4);  // [4 warps][8 heads]
+  float* red2 = red + 32;                                // [4 warps][8 heads]
+  float* m_run = red2 + 32;                              // [8]
+  float* l_run = m_run + 8;
+  float* scl = l_run + 8;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = n_heads / n_kv_heads;
+  const int qd = n_heads * HD, kvd = n_kv_heads * HD;
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    tc::mbar_init(bar_s, 1);
+    tc::mbar_init(bar_o, 1);
+    *abort_flag = 0;
+    tc::mbar_fence_init();
+    tc::tma_prefetch_desc(&tk);
+    tc::tma_prefetch_desc(&tv);
+  }
+  if (warp == 0) tc::tmem_alloc(tmem_slot, 32);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;  // columns 0..15: S^T, 16..31: O^T
+
+  if (warp == 4) {
+    // ---- TMA producer: K boxes and V^T boxes of every sub-chunk of this CTA's items
+    if (lane == 0) {
+      const uint64_t pol = tc::policy_evict_first();
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        const AttnItem w = items[it];
+        const QueryRow r = rows[w.b];
+        const long long krow = kv_block(r, layer, 0, w.g, n_kv_heads, HD) / HD;
+        const long long vrow = kv_block(r, layer, 1, w.g, n_kv_heads, HD) / 64;
+        for (int sub = w.s0; sub < w.s1; ++sub) {
+          if (!tc::mbar_wait(&empty[stage], phase ^ 1)) {
+            *abort_flag = 1;
+            if (atomicCAS(err, 0, CBT_DEV_TIMEOUT) == 0) err[1] = 11;
+            ok = false;
+            break;
+          }
+          // K: 128 keys x HD dims; V^T: two boxes of HD rows x 64 keys
+          tc::mbar_expect_tx(&full[stage], (uint32_t)(kSub * HD * 2 + 2 * HD * 128));
+          uint8_t* st = stages + stage * kStageBytes;
+#pragma unroll
+          for (int h = 0; h < nKh; ++h)
+            tc::tma_load_2d(st + h * kBox, &tk, &full[stage], h * 64, (int)(krow + sub * kSub), pol);
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            tc::tma_load_2d(st + (nKh + j) * kBox, &tv, &full[stage], 0,
+                            (int)(vrow + (long long)(2 * sub + j) * HD), pol);
+          ++issued;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      for (int i = 0; i < kStages && i < issued; ++i) {  // no copies in flight at exit
+        if (--stage < 0) {
+          stage = kStages - 1;
+          phase ^= 1;
+        }
+        tc::mbar_wait(&full[stage], phase);
+      }
+    }
+  } else {
+    // ---- compute warps: MMA issue (thread 0), softmax (thread = key), accumulate (thread = dim)
+    const float qscale = rsqrtf((float)HD);
+    int stage = 0;
+    uint32_t phase = 0, cnt = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      const AttnItem w = items[it];
+      const QueryRow r = rows[w.b];
+      const int n = r.pos + 1;
+      // Q operand: rows 0..G-1 hi parts, 8..8+G-1 lo parts of the group's (rotated) q rows
+      const float* qrow = qkv + (size_t)w.b * (qd + 2 * kvd) + (size_t)w.g * G * HD;
+      for (int i = tid; i < 8 * HD; i += kCompute) {
+        const int h = i / HD, d = i % HD;
+        uint16_t hi = 0, lo = 0;
+        if (h < G) {
+          const float v = qrow[h * HD + d] * qscale;
+          hi = f32_to_bf16(v);
+          lo = f32_to_bf16(v - bf16_to_f32(hi));
+        }
+        st_bf16(sQ, sw128_off(h, d, 2048), hi);
+        st_bf16(sQ, sw128_off(8 + h, d, 2048), lo);
+      }
+      if (tid < 8) {
+        m_run[tid] = -INFINITY;
+        l_run[tid] = 0.f;
+      }
+      float oacc[8];
+#pragma unroll
+      for (int h = 0; h < 8; ++h) oacc[h] = 0.f;
+      fence_proxy_async();
+      tc::named_bar_sync(1, kCompute);
+
+      for (int sub = w.s0; sub < w.s1; ++sub, ++cnt) {
+        uint8_t* st = stages + stage * kStageBytes;
+        if (tid == 0) {
+          if (!tc::mbar_wait(&full[stage], phase)) {
+            *abort_flag = 1;
+            if (atomicCAS(err, 0, CBT_DEV_TIMEOUT) == 0) err[1] = 12;
+          } else {
+            tc::tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < HD / 16; ++kk) {
+              const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(st + (kk >> 2) * kBox)) + 2 * (kk & 3);
+              const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sQ + (kk >> 2) * 2048)) + 2 * (kk & 3);
+              tc::mma_bf16(tmem, ad, bd, kIdesc, kk > 0 ? 1u : 0u);
+            }
+            tc::mma_commit(bar_s);
+          }
+        }
+        tc::named_bar_sync(1, kCompute);
+        const bool bad_s = *abort_flag || !tc::mbar_wait(bar_s, cnt & 1);
+        if (bar_any(2, kCompute, bad_s)) {
+          ok = false;
+          break;
+        }
+        tc::tc_fence_after();
+        // scores of this thread's key: S^T lane = key, columns j (hi) + 8 + j (lo)
+        uint32_t raw[16];
+        tc::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16), raw);
+        tc::tmem_ld_wait();
+        const int key = sub * kSub + tid;
+        const bool valid = key < n;
+        float s[8];
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+          s[h] = valid ? __uint_as_float(raw[h]) + __uint_as_float(raw[8 + h]) : -INFINITY;
+          const float mx = warp_max(s[h]);
+          if (lane == 0) red[warp * 8 + h] = mx;
+        }
+        tc::named_bar_sync(1, kCompute);
+        if (tid < 8) {
+          const float mloc = fmaxf(fmaxf(red[tid], red[8 + tid]), fmaxf(red[16 + tid], red[24 + tid]));
+          const float mo = m_run[tid];
+          const float mn = fmaxf(mo, mloc);
+          scl[tid] = mo == -INFINITY ? 0.f : __expf(mo - mn);
+          m_run[tid] = mn;
+        }
+        tc::named_bar_sync(1, kCompute);
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+          const float p = (valid && h < G) ? __expf(s[h] - m_run[h]) : 0.f;
+          const uint16_t hi = f32_to_bf16(p);
+          st_bf16(sP, sw128_off(h, tid, 2048), hi);
+          st_bf16(sP, sw128_off(8 + h, tid, 2048), f32_to_bf16(p - bf16_to_f32(hi)));
+          const float ps = warp_sum(p);
+          if (lane == 0) red2[warp * 8 + h] = ps;
+        }
+        if (!valid) {  // this key's V^T column may hold stale values: make it zero
+          uint8_t* vt = st + nKh * kBox + (tid >> 6) * kBox;
+          for (int d = 0; d < HD; ++d) st_bf16(vt, sw128_off(d, tid & 63, 0), 0);
+        }
+        fence_proxy_async();
+        tc::tc_fence_before();
+        tc::named_bar_sync(1, kCompute);
+        if (tid < 8)
+          l_run[tid] = l_run[tid] * scl[tid] + red2[tid] + red2[8 + tid] + red2[16 + tid] + red2[24 + tid];
+        if (tid == 0) {
+          tc::tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kSub / 16; ++kk) {
+            const uint64_t ad =
+                tc::sdesc_sw128(tc::smem_u32(st + (nKh + (kk >> 2)) * kBox)) + 2 * (kk & 3);
+            const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sP + (kk >> 2) * 2048)) + 2 * (kk & 3);
+            tc::mma_bf16(tmem + 16, ad, bd, kIdesc, kk > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(bar_o);
+          tc::mma_commit(&empty[stage]);  // the stage is free once both MMAs have read it
+        }
+        const bool bad_o = !tc::mbar_wait(bar_o, cnt & 1);
+        if (bad_o && atomicCAS(err, 0, CBT_DEV_TIMEOUT) == 0) err[1] = 13;
+        if (bar_any(2, kCompute, bad_o)) {
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        tc::tc_fence_after();
+        tc::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + 16, raw);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int h = 0; h < 8; ++h)
+          oacc[h] = oacc[h] * scl[h] + __uint_as_float(raw[h]) + __uint_as_float(raw[8 + h]);
+        tc::tc_fence_before();
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+      // partial output of this item, relative to m_run
+      if (tid < HD) {
+        for (int h = 0; h < G; ++h) part_o[((size_t)it * G + h) * HD + tid] = oacc[h];
+      }
+      if (tid < G) part_ml[(size_t)it * G + tid] = make_float2(m_run[tid], l_run[tid]);
+      tc::named_bar_sync(1, kCompute);
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 32);
+  }
+}
+
+// Combine the partials of each (row, q head): o = sum_i o_i e^(m_i - M) / sum_i l_i e^(m_i - M)
+// and write it as the bf16 (hi/lo) operand of the output projection.
+__global__ void k_attn_merge(const float* __restrict__ part_o, const float2* __restrict__ part_ml,
+                             const int* __restrict__ item_base, const int* __restrict__ item_count,
+                             int n_heads, int n_kv_heads, int head_dim, uint16_t* act, int lo_rows) {
+  const int b = blockIdx.y, hq = blockIdx.x;
+  const int G = n_heads / n_kv_heads, g = hq / G, h = hq % G;
+  const int cnt = item_count[b];
+  const int first = item_base[b] + g * cnt;
+  float M = -INFINITY;
+  for (int i = 0; i < cnt; ++i) M = fmaxf(M, part_ml[(size_t)(first + i) * G + h].x);
+  float L = 0.f;
+  for (int i = 0; i < cnt; ++i) {
+    const float2 ml = part_ml[(size_t)(first + i) * G + h];
+    L += ml.y * __expf(ml.x - M);
+  }
+  const float invL = 1.f / L;
+  const int K = n_heads * head_dim;
+  for (int d = threadIdx.x; d < head_dim; d += blockDim.x) {
+    float o = 0.f;
+    for (int i = 0; i < cnt; ++i) {
+      const float wgt = __expf(part_ml[(size_t)(first + i) * G + h].x - M);
+      o += part_o[((size_t)(first + i) * G + h) * head_dim + d] * wgt;
+    }
+    o *= invL;
+    const uint16_t hi = f32_to_bf16(o);
+    act[(size_t)b * K + hq * head_dim + d] = hi;
+    if (lo_rows > 0) act[(size_t)(lo_rows + b) * K + hq * head_dim + d] = f32_to_bf16(o - bf16_to_f32(hi));
+  }
+}
+
+template <int HD>
+cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const AttnDecodeArgs& a,
+                          int grid, cudaStream_t s) {
+  constexpr int nKh = HD / 64;
+  constexpr size_t smem = 1024 + kStages * (nKh + 2) * kBox + nKh * 2048 + 2 * 2048 + 1024;
+  static_assert(smem <= 227 * 1024, "shared memory budget");
+  cudaError_t rc = cudaFuncSetAttribute(k_attn_decode<HD>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (rc != cudaSuccess) return rc;
+  count_launch();
+  k_attn_decode<HD><<<grid, 160, smem, s>>>(tk, tv, a.qkv, a.rows, a.items, a.n_items, a.layer,
+                                            a.n_heads, a.n_kv_heads, a.part_o, a.part_ml, a.err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool launch_attn_decode_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnDecodeArgs& a,
+                           int num_sms, cudaStream_t s) {
+  if (a.n_items <= 0) return true;
+  if (a.n_heads % a.n_kv_heads || a.n_heads / a.n_kv_heads > 8) return false;
+  const int grid = a.n_items < num_sms ? a.n_items : num_sms;
+  cudaError_t rc;
+  if (a.head_dim == 128) rc = launch_decode<128>(tk, tv, a, grid, s);
+  else if (a.head_dim == 64) rc = launch_decode<64>(tk, tv, a, grid, s);
+  else return false;
+  if (rc != cudaSuccess) return false;
+  count_launch();
+  k_attn_merge<<<dim3(a.n_heads, a.B), 128, 0, s>>>(a.part_o, a.part_ml, a.item_base, a.item_count,
+                                                    a.n_heads, a.n_kv_heads, a.head_dim, a.act,
+                                                    a.act_lo);
+  return cudaGetLastError() == cudaSuccess;
+}

@@ -2,6 +2,8 @@
 // plain per-token attention, greedy argmax, row gather and the 4-bit quantiser.
 #include <math.h>
 
+#include <algorithm>
+
 #include "kernels.h"
 
 // ---- embedding: x[i] = E[token[i]] (fp32); out-of-range ids set the error word ------------
@@ -143,7 +145,7 @@ __global__ void k_rope_append(float* qkv, const QueryRow* rows, int layer, int n
     v[i] = ra;
     v[i + half] = rb;
     if (h >= n_heads) {
-      uint16_t* kd = arena + kv_offset(r, layer, 0, h - n_heads, n_kv_heads, head_dim);
+      uint16_t* kd = arena + k_index(r, layer, h - n_heads, r.pos, 0, n_kv_heads, head_dim);
       kd[i] = f32_to_bf16(ra);
       kd[i + half] = f32_to_bf16(rb);
     }
@@ -151,7 +153,7 @@ __global__ void k_rope_append(float* qkv, const QueryRow* rows, int layer, int n
   const float* vv = row + qd + kvd;
   for (int e = threadIdx.x; e < kvd; e += blockDim.x) {
     int g = e / head_dim, j = e % head_dim;
-    arena[kv_offset(r, layer, 1, g, n_kv_heads, head_dim) + j] = f32_to_bf16(vv[e]);
+    arena[v_index(r, layer, g, r.pos, j, n_kv_heads, head_dim)] = f32_to_bf16(vv[e]);
   }
 }
 
@@ -162,6 +164,31 @@ void launch_rope_append(float* qkv, const QueryRow* rows, int n, int layer, int 
   count_launch();
   k_rope_append<<<n, 256, 0, s>>>(qkv, rows, layer, n_heads, n_kv_heads, head_dim, cosv, sinv,
                                   arena);
+}
+
+// ---- V of one layer between the plain [kv head][position][head_dim] layout and a slab ------
+// (to_slab: plain -> slab, else slab -> plain); positions [0, n)
+__global__ void k_v_convert(uint16_t* plain, uint16_t* arena, QueryRow r, int layer,
+                            int n_kv_heads, int n, int head_dim, int to_slab) {
+  long long tot = (long long)n_kv_heads * n * head_dim;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < tot;
+       i += (long long)gridDim.x * blockDim.x) {
+    int d = (int)(i % head_dim);
+    long long rest = i / head_dim;
+    int t = (int)(rest % n), g = (int)(rest / n);
+    long long at = v_index(r, layer, g, t, d, n_kv_heads, head_dim);
+    if (to_slab) arena[at] = plain[i];
+    else plain[i] = arena[at];
+  }
+}
+
+void launch_v_convert(uint16_t* plain, uint16_t* arena, const QueryRow& r, int layer,
+                      int n_kv_heads, int n, int head_dim, bool to_slab, cudaStream_t s) {
+  long long tot = (long long)n_kv_heads * n * head_dim;
+  if (tot <= 0) return;
+  int grid = (int)std::min<long long>((tot + 255) / 256, 4096);
+  count_launch();
+  k_v_convert<<<grid, 256, 0, s>>>(plain, arena, r, layer, n_kv_heads, n, head_dim, to_slab ? 1 : 0);
 }
 
 // ---- plain attention: one block per (token, q head), keys [0, pos] of its own slab -------
@@ -179,10 +206,8 @@ __global__ void k_attention_naive(const float* qkv, const QueryRow* rows, int la
   const float* q = qkv + (size_t)t * (qd + 2 * kvd) + (size_t)hq * head_dim;
   for (int j = threadIdx.x; j < head_dim; j += blockDim.x) qs[j] = q[j];
   __syncthreads();
-  QueryRow r0 = r;
-  r0.pos = 0;
-  const uint16_t* K = arena + kv_offset(r0, layer, 0, g, n_kv_heads, head_dim);
-  const uint16_t* V = arena + kv_offset(r0, layer, 1, g, n_kv_heads, head_dim);
+  const uint16_t* K = arena + kv_block(r, layer, 0, g, n_kv_heads, head_dim);
+  const uint16_t* V = arena + kv_block(r, layer, 1, g, n_kv_heads, head_dim);
   float scale = rsqrtf((float)head_dim);
   float mx = -INFINITY;
   for (int k = threadIdx.x; k < nk; k += blockDim.x) {
@@ -230,7 +255,8 @@ __global__ void k_attention_naive(const float* qkv, const QueryRow* rows, int la
   float* orow = o + (size_t)t * qd + (size_t)hq * head_dim;
   for (int j = threadIdx.x; j < head_dim; j += blockDim.x) {
     float acc = 0.f;
-    for (int k = 0; k < nk; ++k) acc = fmaf(sc[k], bf16_to_f32(V[(size_t)k * head_dim + j]), acc);
+    for (int k = 0; k < nk; ++k)
+      acc = fmaf(sc[k], bf16_to_f32(V[((size_t)(k >> 6) * head_dim + j) * 64 + (k & 63)]), acc);
     orow[j] = acc * inv;
   }
 }

@@ -20,18 +20,36 @@ CBT_D uint16_t f32_to_bf16(float f) {
 }
 
 // Where a decode row or a prefill token reads and writes its KV: the slab's element offset
-// in the arena, the token's position and the slab's capacity.  Slab layout (bf16):
-// [layer][K|V][kv head][position][head_dim].
+// in the arena, the token's position and the slab's capacity (a multiple of 64).
+// Slab layout (bf16): [layer][K|V][kv head] blocks of cap * head_dim elements; inside a K
+// block key t, dim d sits at t*head_dim + d (one row per key); inside a V block the keys are
+// grouped by 64 and transposed: key t, dim d sits at ((t/64)*head_dim + d)*64 + t%64, so a
+// 64-key group is a [head_dim][64] tile.  Both attention contractions then read K-major
+// tiles: Q.K^T with the keys' dims contiguous, P.V with the 64 keys of a dim contiguous.
 struct QueryRow {
   long long base;  // element offset of the slab in the arena
   int pos;         // position of this token in its slab
-  int cap;         // slab capacity (positions)
+  int cap;         // slab capacity (positions), a multiple of 64
 };
 
-CBT_D long long kv_offset(const QueryRow& r, int layer, int kv, int head, int n_kv_heads,
+CBT_HD long long kv_block(const QueryRow& r, int layer, int kv, int head, int n_kv_heads,
                           int head_dim) {
-  return r.base + ((((long long)layer * 2 + kv) * n_kv_heads + head) * r.cap + r.pos) * head_dim;
+  return r.base + (((long long)layer * 2 + kv) * n_kv_heads + head) * (long long)r.cap * head_dim;
 }
+CBT_HD long long k_index(const QueryRow& r, int layer, int head, int key, int d, int n_kv_heads,
+                         int head_dim) {
+  return kv_block(r, layer, 0, head, n_kv_heads, head_dim) + (long long)key * head_dim + d;
+}
+CBT_HD long long v_index(const QueryRow& r, int layer, int head, int key, int d, int n_kv_heads,
+                         int head_dim) {
+  return kv_block(r, layer, 1, head, n_kv_heads, head_dim) +
+         ((long long)(key >> 6) * head_dim + d) * 64 + (key & 63);
+}
+
+// One unit of decode attention: kv head g of row b over 128-key sub-chunks [s0, s1)
+struct AttnItem {
+  int b, g, s0, s1;
+};
 
 // Device error word: the first error wins (code, info).
 CBT_D void set_device_error(int* err, int code, int info) {

@@ -29,8 +29,9 @@ constexpr size_t kSlabAlign = 4096;
 struct Slab {
   size_t offset;  // bytes into the arena
   size_t bytes;
-  int cap;
+  int cap;        // positions the caller asked for (the limit of pos)
   int pos;
+  int lcap;       // cap rounded up to 64: the layout's capacity
 };
 
 template <class T>
@@ -85,6 +86,20 @@ struct cbt_engine {
   float* tc_part = nullptr;
   size_t tc_part_floats = 0;
   int* tc_cnt = nullptr;
+  // tensor-core decode attention: TMA descriptors over the whole KV arena, the per-step work
+  // list and the split-K partials (grown on demand)
+  CUtensorMap kv_kmap, kv_vmap;
+  std::vector<AttnItem> hitems;
+  std::vector<int> hitem_base, hitem_count;
+  AttnItem* items = nullptr;
+  int* item_meta = nullptr;  // [max_batch] bases, then [max_batch] counts
+  size_t items_cap = 0;
+  float* att_o = nullptr;
+  float2* att_ml = nullptr;
+  size_t att_items_cap = 0;
+  // staging buffer for host-side import/export of V
+  uint16_t* stage = nullptr;
+  size_t stage_elems = 0;
 
   // measurement: event pairs around launch groups of selected kernel classes
   struct TimeRec {
@@ -124,7 +139,7 @@ static void free_scratch(cbt_engine* e) {
   void* ptrs[] = {e->x,       e->h,        e->qkv,  e->o,     e->act,    e->part,
                   e->xg,      e->logits,   e->cosv, e->sinv,  e->next_tok, e->last_idx,
                   e->rows,    e->err,      e->act_h, e->act_o, e->act_u,  e->tc_part,
-                  e->tc_cnt};
+                  e->tc_cnt,  e->items,    e->item_meta, e->att_o, e->att_ml, e->stage};
   for (void* q : ptrs)
     if (q) cudaFree(q);
 }
@@ -135,9 +150,12 @@ static bool linear_ok(const cbt_linear& l, int fmt) {
   return true;
 }
 
+// slab capacities are whole 64-key groups (the V layout transposes groups of 64 keys)
+static int round_cap(int cap) { return (cap + 63) & ~63; }
+
 extern "C" size_t cbt_slab_bytes(const cbt_model_config* c, int32_t cap) {
   if (!c || cap <= 0) return 0;
-  size_t b = (size_t)c->n_layers * 2 * c->n_kv_heads * (size_t)cap * c->head_dim * 2;
+  size_t b = (size_t)c->n_layers * 2 * c->n_kv_heads * (size_t)round_cap(cap) * c->head_dim * 2;
   return (b + kSlabAlign - 1) & ~(kSlabAlign - 1);
 }
 
@@ -241,6 +259,17 @@ extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_w
                 make_tmap_bf16(&e->wmaps[l].d, L.wd.w, c.d_ff, c.d_model, 64, 64);
     }
     maps_ok = maps_ok && make_tmap_bf16(&e->lm_map, w->lm_head.w, c.d_model, c.vocab, 64, 64);
+    // the whole arena seen as K rows (head_dim wide) and as V^T rows (64 keys wide)
+    const uint64_t arena_elems = p->kv_arena_bytes / 2;
+    maps_ok = maps_ok && arena_elems / 64 < (1ull << 31) &&
+              make_tmap_bf16(&e->kv_kmap, p->kv_arena, c.head_dim, arena_elems / c.head_dim, 64,
+                             128) &&
+              make_tmap_bf16(&e->kv_vmap, p->kv_arena, 64, arena_elems / 64, 64, c.head_dim);
+    if (rc == cudaSuccess) {
+      e->hitem_base.resize(p->max_batch);
+      e->hitem_count.resize(p->max_batch);
+      chk(dmalloc(&e->item_meta, (size_t)2 * p->max_batch, &tot));
+    }
     e->use_tc = maps_ok && c.d_ff % 64 == 0;
   }
   if (rc == cudaSuccess) rc = cudaStreamSynchronize(e->stream);
@@ -276,7 +305,7 @@ extern "C" cbt_status cbt_kv_slab_alloc(cbt_engine* e, int32_t cap, int32_t* id)
       e->free_ext.erase(it);
       if (rest) e->free_ext[off + need] = rest;
       int sid = e->next_id++;
-      e->slabs[sid] = Slab{off, need, cap, 0};
+      e->slabs[sid] = Slab{off, need, cap, 0, round_cap(cap)};
       e->in_use += need;
       *id = sid;
       return CBT_OK;
@@ -343,16 +372,38 @@ static cbt_status slab_copy(cbt_engine* e, int32_t id, void* k, void* v, int32_t
   cudaMemcpyKind kind = on_host ? (to_slab ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToHost)
                                 : cudaMemcpyDeviceToDevice;
   cudaError_t rc = cudaSuccess;
+  const size_t layer_elems = (size_t)c.n_kv_heads * n * c.head_dim;
+  if (on_host && n > 0 && e->stage_elems < layer_elems) {  // staging for the V transposition
+    rc = cudaStreamSynchronize(e->stream);
+    if (e->stage) cudaFree(e->stage);
+    e->stage = nullptr;
+    e->stage_elems = 0;
+    if (rc == cudaSuccess) rc = cudaMalloc(reinterpret_cast<void**>(&e->stage), layer_elems * 2);
+    if (rc != cudaSuccess) return CBT_ERR_CUDA;
+    e->stage_elems = layer_elems;
+  }
+  const QueryRow qr{(long long)(s.offset / 2), 0, s.lcap};
   for (int l = 0; l < c.n_layers && rc == cudaSuccess && n > 0; ++l) {
-    for (int kv = 0; kv < 2 && rc == cudaSuccess; ++kv) {
-      char* user = static_cast<char*>(kv == 0 ? k : v) + (size_t)l * c.n_kv_heads * n * row;
-      char* slab = arena + ((size_t)l * 2 + kv) * c.n_kv_heads * (size_t)s.cap * row;
-      size_t upitch = (size_t)n * row, spitch = (size_t)s.cap * row;
-      if (to_slab)
-        rc = cudaMemcpy2DAsync(slab, spitch, user, upitch, upitch, c.n_kv_heads, kind, e->stream);
-      else
-        rc = cudaMemcpy2DAsync(user, upitch, slab, spitch, upitch, c.n_kv_heads, kind, e->stream);
-    }
+    // K: the slab's K block holds rows [0, n) of head_dim elements per kv head
+    char* user = static_cast<char*>(k) + (size_t)l * c.n_kv_heads * n * row;
+    char* slab = arena + ((size_t)l * 2) * c.n_kv_heads * (size_t)s.lcap * row;
+    size_t upitch = (size_t)n * row, spitch = (size_t)s.lcap * row;
+    if (to_slab)
+      rc = cudaMemcpy2DAsync(slab, spitch, user, upitch, upitch, c.n_kv_heads, kind, e->stream);
+    else
+      rc = cudaMemcpy2DAsync(user, upitch, slab, spitch, upitch, c.n_kv_heads, kind, e->stream);
+    if (rc != cudaSuccess) break;
+    // V: transposed 64-key groups in the slab, converted on the device
+    uint16_t* vu = static_cast<uint16_t*>(v) + (size_t)l * layer_elems;
+    uint16_t* plain = on_host ? e->stage : vu;
+    if (on_host && to_slab)
+      rc = cudaMemcpyAsync(plain, vu, layer_elems * 2, cudaMemcpyHostToDevice, e->stream);
+    if (rc != cudaSuccess) break;
+    launch_v_convert(plain, static_cast<uint16_t*>(e->p.kv_arena), qr, l, c.n_kv_heads, n,
+                     c.head_dim, to_slab, e->stream);
+    rc = cudaGetLastError();
+    if (rc == cudaSuccess && on_host && !to_slab)
+      rc = cudaMemcpyAsync(vu, plain, layer_elems * 2, cudaMemcpyDeviceToHost, e->stream);
   }
   if (rc == cudaSuccess && on_host && !to_slab) rc = cudaStreamSynchronize(e->stream);
   if (rc != cudaSuccess) return CBT_ERR_CUDA;
@@ -529,9 +580,30 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
     t = tbegin(e, CBT_KCLASS_ATTN);
     launch_rope_append(e->qkv, e->rows, n, l, c.n_heads, c.n_kv_heads, c.head_dim, e->cosv,
                        e->sinv, arena, s);
-    launch_attention_naive(e->qkv, e->rows, n, l, c.n_heads, c.n_kv_heads, c.head_dim, max_keys,
-                           arena, e->o, s);
-    if (tcp) launch_f32_to_act(e->o, n, qd, e->act_o, lo, s);
+    if (tcp && !gather) {  // decode: split-K flash decoding on the tensor cores
+      AttnDecodeArgs a{};
+      a.qkv = e->qkv;
+      a.rows = e->rows;
+      a.items = e->items;
+      a.n_items = (int)e->hitems.size();
+      a.item_base = e->item_meta;
+      a.item_count = e->item_meta + e->p.max_batch;
+      a.B = n;
+      a.layer = l;
+      a.n_heads = c.n_heads;
+      a.n_kv_heads = c.n_kv_heads;
+      a.head_dim = c.head_dim;
+      a.part_o = e->att_o;
+      a.part_ml = e->att_ml;
+      a.act = e->act_o;
+      a.act_lo = lo;
+      a.err = e->err;
+      ok &= launch_attn_decode_tc(e->kv_kmap, e->kv_vmap, a, e->num_sms, s);
+    } else {
+      launch_attention_naive(e->qkv, e->rows, n, l, c.n_heads, c.n_kv_heads, c.head_dim, max_keys,
+                             arena, e->o, s);
+      if (tcp) launch_f32_to_act(e->o, n, qd, e->act_o, lo, s);
+    }
     tend(e, t, attn_bytes);
     if (tcp)
       ok &= tc_projection(e, e->wmaps[l].o, e->act_o, n, qd, d, EPI_ADD, e->x, d, nullptr, 0);
@@ -575,6 +647,53 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
   return cudaGetLastError();
 }
 
+// Work list of the tensor-core decode attention for the rows in e->hrows[0..B): per row and kv
+// head, runs of kSubsPerItem 128-key sub-chunks over positions [0, pos].  Grows the item and
+// partial buffers when needed and copies the list to the device on the engine stream.
+static constexpr int kSubsPerItem = 2;
+
+static cudaError_t plan_decode_attention(cbt_engine* e, int B) {
+  const int Hkv = e->cfg.n_kv_heads, G = e->cfg.n_heads / Hkv, hd = e->cfg.head_dim;
+  e->hitems.clear();
+  for (int b = 0; b < B; ++b) {
+    const int nsub = (e->hrows[b].pos + 1 + 127) / 128;
+    const int splits = (nsub + kSubsPerItem - 1) / kSubsPerItem;
+    e->hitem_base[b] = (int)e->hitems.size();
+    e->hitem_count[b] = splits;
+    for (int g = 0; g < Hkv; ++g)
+      for (int sp = 0; sp < splits; ++sp)
+        e->hitems.push_back(AttnItem{b, g, sp * kSubsPerItem,
+                                     std::min(nsub, (sp + 1) * kSubsPerItem)});
+  }
+  const size_t n = e->hitems.size();
+  cudaError_t rc = cudaSuccess;
+  if (n > e->att_items_cap) {
+    size_t cap = std::max(n, e->att_items_cap * 2);
+    rc = cudaStreamSynchronize(e->stream);
+    cudaFree(e->items);
+    cudaFree(e->att_o);
+    cudaFree(e->att_ml);
+    e->items = nullptr;
+    e->att_o = nullptr;
+    e->att_ml = nullptr;
+    e->att_items_cap = 0;
+    if (rc == cudaSuccess) rc = cudaMalloc(reinterpret_cast<void**>(&e->items), cap * sizeof(AttnItem));
+    if (rc == cudaSuccess) rc = cudaMalloc(reinterpret_cast<void**>(&e->att_o), cap * G * hd * sizeof(float));
+    if (rc == cudaSuccess) rc = cudaMalloc(reinterpret_cast<void**>(&e->att_ml), cap * G * sizeof(float2));
+    if (rc != cudaSuccess) return rc;
+    e->att_items_cap = cap;
+  }
+  rc = cudaMemcpyAsync(e->items, e->hitems.data(), n * sizeof(AttnItem), cudaMemcpyHostToDevice,
+                       e->stream);
+  if (rc == cudaSuccess)
+    rc = cudaMemcpyAsync(e->item_meta, e->hitem_base.data(), B * sizeof(int),
+                         cudaMemcpyHostToDevice, e->stream);
+  if (rc == cudaSuccess)
+    rc = cudaMemcpyAsync(e->item_meta + e->p.max_batch, e->hitem_count.data(), B * sizeof(int),
+                         cudaMemcpyHostToDevice, e->stream);
+  return rc;
+}
+
 extern "C" cbt_status cbt_decode_step_batch(cbt_engine* e, const int32_t* ids, int32_t B,
                                             const int32_t* last_tokens, float* logits,
                                             int32_t* next_tokens) {
@@ -592,12 +711,13 @@ extern "C" cbt_status cbt_decode_step_batch(cbt_engine* e, const int32_t* ids, i
     if (!seen.insert(ids[b]).second) return CBT_ERR_DUP_SLAB;
     const Slab& sl = it->second;
     if (sl.pos + 1 > sl.cap) return CBT_ERR_CAPACITY;
-    e->hrows[b] = QueryRow{(long long)(sl.offset / 2), sl.pos, sl.cap};
+    e->hrows[b] = QueryRow{(long long)(sl.offset / 2), sl.pos, sl.lcap};
     max_keys = std::max(max_keys, sl.pos + 1);
     total_keys += sl.pos + 1;
   }
   cudaError_t rc = cudaMemcpyAsync(e->rows, e->hrows.data(), sizeof(QueryRow) * B,
                                    cudaMemcpyHostToDevice, e->stream);
+  if (rc == cudaSuccess && e->use_tc) rc = plan_decode_attention(e, B);
   if (rc == cudaSuccess) rc = forward(e, B, last_tokens, max_keys, total_keys, false, B, logits, next_tokens);
   if (rc != cudaSuccess) return rc == cudaErrorNotSupported ? CBT_ERR_UNSUPPORTED : CBT_ERR_CUDA;
   for (int b = 0; b < B; ++b) e->slabs[ids[b]].pos += 1;
@@ -632,7 +752,7 @@ extern "C" cbt_status cbt_prefill_segmented(cbt_engine* e, const int32_t* ids,
   for (int s = 0; s < K; ++s) {
     const Slab& sl = e->slabs[ids[s]];
     for (int j = 0; j < lens[s]; ++j, ++g)
-      e->hrows[g] = QueryRow{(long long)(sl.offset / 2), sl.pos + j, sl.cap};
+      e->hrows[g] = QueryRow{(long long)(sl.offset / 2), sl.pos + j, sl.lcap};
     e->hidx[s] = g - 1;
   }
   cudaError_t rc = cudaMemcpyAsync(e->rows, e->hrows.data(), sizeof(QueryRow) * T,

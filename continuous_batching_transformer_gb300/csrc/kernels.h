@@ -46,6 +46,28 @@ int tc_plain_bn(int n);
 bool launch_tc_linear(const CUtensorMap& tw, const CUtensorMap& tx, TcParams p, bool split,
                       int BN, int num_sms, size_t part_floats, cudaStream_t s);
 
+// ---- tensor-core decode attention (attn_tc.cu) ------------------------------------------------
+struct AttnDecodeArgs {
+  const float* qkv;          // [B][q|k|v] fp32, q and k already rotated
+  const QueryRow* rows;      // [B]
+  const AttnItem* items;     // work items, grouped by row: row b's items start at item_base[b],
+  int n_items;               //   kv head g's splits at item_base[b] + g * item_count[b]
+  const int* item_base;      // [B]
+  const int* item_count;     // [B] splits per (row, kv head)
+  int B, layer, n_heads, n_kv_heads, head_dim;
+  float* part_o;             // [n_items][G][head_dim] partial outputs
+  float2* part_ml;           // [n_items][G] (running max, running sum)
+  uint16_t* act;             // attention output as the O projection's bf16 operand
+  int act_lo;                // lo rows offset (0: plain bf16)
+  int* err;
+};
+// tk: the KV arena as [rows][head_dim] bf16, box {64, 128}; tv: as [rows][64], box {64, head_dim}
+bool launch_attn_decode_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnDecodeArgs& a,
+                           int num_sms, cudaStream_t s);
+// V of one layer between a plain [kv head][position][head_dim] buffer and a slab
+void launch_v_convert(uint16_t* plain, uint16_t* arena, const QueryRow& r, int layer,
+                      int n_kv_heads, int n, int head_dim, bool to_slab, cudaStream_t s);
+
 // RMSNorm rows of x into a bf16 operand: hi parts at rows [0, n), lo parts at rows
 // [lo_rows, lo_rows + n) when lo_rows > 0
 void launch_rmsnorm_act(const float* x, const uint16_t* gain, int n, int d, float eps,

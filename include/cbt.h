@@ -151,9 +151,12 @@ cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_weights* wei
 /* Synchronise the engine's stream and free everything the engine allocated. */
 cbt_status cbt_engine_destroy(cbt_engine* e);
 
-/* Bytes one slab of `capacity_tokens` positions takes in the arena:
- * n_layers * 2 (K, V) * n_kv_heads * capacity * head_dim * 2 bytes, rounded up to 4 KiB.
- * Slab layout (bf16): [layer][K|V][kv head][position][head_dim]. */
+/* Bytes one slab of `capacity_tokens` positions takes in the arena: the capacity rounded up
+ * to a multiple of 64 (C), times n_layers * 2 (K, V) * n_kv_heads * head_dim * 2 bytes,
+ * rounded up to 4 KiB.  Slab layout (bf16): [layer][K|V][kv head] blocks of C * head_dim
+ * elements; a K block is [position][head_dim]; a V block is [position / 64][head_dim][64]
+ * (each group of 64 positions transposed), so both attention contractions read K-major
+ * tiles.  Import and export use the plain layout described at cbt_kv_slab_import. */
 size_t cbt_slab_bytes(const cbt_model_config* cfg, int32_t capacity_tokens);
 
 /* Reserve a slab for one sequence (host-side first-fit allocator over the arena, no

@@ -71,12 +71,15 @@ def test_create_rejects_null_and_bad_config(lib):
 
 def test_slab_bytes(lib):
     cfg = B.ModelConfig(32, 4096, 32, 8, 128, 14336, 32000, 1e-5, 1e6, 0, 64)
-    # 32 layers x (K, V) x 8 heads x 128 dims x 2 bytes = 131072 bytes per position
-    assert B.slab_bytes(cfg, 1) == 131072
+    # 32 layers x (K, V) x 8 heads x 128 dims x 2 bytes = 131072 bytes per position, and a
+    # slab holds whole groups of 64 positions (V is stored as transposed 64-key groups)
+    assert B.slab_bytes(cfg, 64) == 64 * 131072
+    assert B.slab_bytes(cfg, 1) == 64 * 131072
     assert B.slab_bytes(cfg, 2048) == 2048 * 131072
+    assert B.slab_bytes(cfg, 2049) == 2112 * 131072
     tiny = B.ModelConfig(2, 256, 4, 4, 64, 1024, 1024, 1e-6, 1e4, 0, 64)
-    assert B.slab_bytes(tiny, 2) == 4096  # 2048 bytes per position
-    assert B.slab_bytes(tiny, 3) == 8192  # 6144 bytes rounded up to 4 KiB
+    assert B.slab_bytes(tiny, 2) == 64 * 2048  # 2048 bytes per position
+    assert B.slab_bytes(tiny, 65) == 128 * 2048
     assert B.slab_bytes(tiny, 0) == 0
 
 

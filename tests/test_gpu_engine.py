@@ -19,7 +19,7 @@ def weights():
     return DeviceWeights(TINY, torch.device("cuda:0"))
 
 
-def small_engine(weights, arena_positions=256, max_batch=4):
+def small_engine(weights, arena_positions=512, max_batch=4):
     return Engine(weights, arena_bytes=B.slab_bytes(weights.cfg, arena_positions), max_batch=max_batch,
                   max_prefill_tokens=64)
 
@@ -33,22 +33,25 @@ def status_of(fn, *a):
 
 
 def test_allocator_first_fit_and_coalescing(weights):
-    eng = small_engine(weights, arena_positions=64)
+    """First fit with coalescing; capacities are whole 64-position groups."""
+    eng = small_engine(weights, arena_positions=256)
     arena = eng.stats().arena_bytes
-    a = eng.kv_slab_alloc(16)
-    b = eng.kv_slab_alloc(16)
-    c = eng.kv_slab_alloc(16)
+    assert arena == B.slab_bytes(weights.cfg, 256)
+    a = eng.kv_slab_alloc(64)
+    b = eng.kv_slab_alloc(40)  # rounds up to 64 positions
+    c = eng.kv_slab_alloc(64)
     st = eng.stats()
-    assert st.live_slabs == 3 and st.slab_bytes_in_use == 3 * B.slab_bytes(weights.cfg, 16)
+    assert st.live_slabs == 3 and st.slab_bytes_in_use == 3 * B.slab_bytes(weights.cfg, 64)
     eng.kv_slab_free(b)
-    d = eng.kv_slab_alloc(16)  # first fit: reuses b's extent
+    d = eng.kv_slab_alloc(64)  # first fit: reuses b's extent
+    assert status_of(eng.kv_slab_alloc, 128) == -7  # only 64 positions left at the end
     eng.kv_slab_free(a)
     eng.kv_slab_free(c)
     eng.kv_slab_free(d)
     st = eng.stats()
     assert st.live_slabs == 0 and st.slab_bytes_in_use == 0 and st.largest_free_bytes == arena
-    big = eng.kv_slab_alloc(60)  # after coalescing the whole arena is one extent again
-    assert status_of(eng.kv_slab_alloc, 16) == -7  # pool exhausted
+    big = eng.kv_slab_alloc(250)  # after coalescing the whole arena is one extent again
+    assert status_of(eng.kv_slab_alloc, 1) == -7  # pool exhausted
     eng.kv_slab_free(big)
     eng.close()
 
