@@ -40,7 +40,32 @@ def measured_peaks():
         return None
 
 
-def workload_by_name(name: str):
+def measured_traffic(kind: str):
+    """DRAM bytes (read + write) of one launch of the kernel, from the ncu capture summarised in
+    profiles/traffic.json -- or None when the kernel's source changed since that capture."""
+    import hashlib
+    try:
+        info = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))[kind]
+        src = open(os.path.join(ROOT, info["source"]), "rb").read()
+        if hashlib.sha256(src).hexdigest() != info["sha256"]:
+            return None
+        return info["dram_bytes_per_launch"]
+    except Exception:
+        return None
+
+
+def workload_by_name(name: str, layers: int | None = None):
+    """A named decode workload; `layers` keeps every shape but the depth (used only to profile
+    single kernels on a small device footprint; the JSON line then names the reduced model)."""
+    wl = _workload_by_name(name)
+    if layers:
+        from dataclasses import replace
+        shape = replace(wl.shape, n_layers=layers, name=f"{wl.shape.name}-{layers}-layers")
+        wl = replace(wl, shape=shape, name=f"{wl.name}-{layers}-layers")
+    return wl
+
+
+def _workload_by_name(name: str):
     from synth.recipes import DECODE_7B_B8, LONG_7B_B32, decode_7b_fixed
     if name == "7b-bf16-b8":
         return DECODE_7B_B8
@@ -150,7 +175,7 @@ def gpu_arm(args, rank: int, world: int):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
         dist.barrier()
-    wl = workload_by_name(args.workload)
+    wl = workload_by_name(args.workload, args.layers)
     K, W = args.steps, args.warmup
     w, eng, slabs, ctx, tok0 = setup_decode(wl, device, extra_positions=3 * (K + W) + 8)
     Bsz = len(slabs)
@@ -174,7 +199,6 @@ def gpu_arm(args, rank: int, world: int):
     except Exception:
         pass
     clocks = ClockSampler(gpu_uuid) if rank == 0 else None
-    B.engine_set_timing(eng.handle, 1 << B.KCLASS_PROJ)
     launches0 = B.kernel_launches(eng.handle)
     if dist:
         dist.barrier()
@@ -190,7 +214,15 @@ def gpu_arm(args, rank: int, world: int):
     launches = B.kernel_launches(eng.handle) - launches0
     ms = ev0.elapsed_time(ev1)
     clk = clocks.stop() if clocks else None
+    # Kernel rooflines: the same steps again with CUDA events around every projection and
+    # every attention launch group (the engine then launches kernel by kernel instead of
+    # replaying its captured step; the kernels and their work are the same).
+    KT = max(4, min(K, 16))
+    B.engine_set_timing(eng.handle, (1 << B.KCLASS_PROJ) | (1 << B.KCLASS_ATTN))
+    for i in range(W + K, W + K + KT):
+        step(i)
     proj_ms, proj_n, proj_bytes = B.engine_timing(eng.handle, B.KCLASS_PROJ)
+    attn_ms, attn_n, attn_bytes = B.engine_timing(eng.handle, B.KCLASS_ATTN)
     B.engine_set_timing(eng.handle, 0)
     t = torch.tensor([ms], dtype=torch.float64, device=device)
     if dist:
@@ -204,7 +236,7 @@ def gpu_arm(args, rank: int, world: int):
     # next tokens back to the host, every step
     h_tok = torch.empty(Bsz, dtype=torch.int32, pin_memory=True)
     h_out = torch.empty(Bsz, dtype=torch.int32, pin_memory=True)
-    h_tok.copy_(bufs[(W + K) % 2].cpu())
+    h_tok.copy_(bufs[(W + K + KT) % 2].cpu())
     d_tok = torch.empty_like(tok0)
     d_out = torch.empty_like(tok0)
     for i in range(3):
@@ -238,6 +270,8 @@ def gpu_arm(args, rank: int, world: int):
         sb = step_bytes(wl.shape, ctx_mean)
         step_s = ms_max / K / 1e3
         achieved = proj_bytes / (proj_ms / 1e3) / 1e9 if proj_ms > 0 else None
+        attn_gbs = attn_bytes / (attn_ms / 1e3) / 1e9 if attn_ms > 0 else None
+        kt_ms = ms / K * KT  # the timed region's duration for KT steps
         result = {
             "metric": METRIC,
             "value": Bsz * K * world / (ms_max / 1e3),
@@ -263,8 +297,14 @@ def gpu_arm(args, rank: int, world: int):
                          "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
                          "peak_source": peak_src, "unit": "GB/s",
                          "frac": achieved / hbm_peak if achieved else None,
-                         "share_of_step": proj_ms / ms if ms > 0 else None,
-                         "launch_groups": proj_n, "traffic": None},
+                         "share_of_step": proj_ms / kt_ms if kt_ms > 0 else None,
+                         "launch_groups": proj_n, "timed_steps": KT,
+                         "traffic": measured_traffic("projection")},
+            "attention_roofline": {"kernel": "RoPE + KV append + split-K decode attention + merge",
+                                   "bound": "hbm", "achieved": attn_gbs, "peak": hbm_peak,
+                                   "unit": "GB/s",
+                                   "frac": attn_gbs / hbm_peak if attn_gbs else None,
+                                   "share_of_step": attn_ms / kt_ms if kt_ms > 0 else None},
             "e2e": {"value": Bsz * K * world / e2e_s, "unit": "tok/s",
                     "h2d_bytes_per_step": 4 * Bsz, "d2h_bytes_per_step": 4 * Bsz},
             "gpu_launches": int(launches),
@@ -307,7 +347,7 @@ def oracle_decode_sample(wl, max_steps: int, budget_s: float):
 def reference_arm(args, rank: int):
     if rank != 0:
         return None
-    wl = workload_by_name(args.workload)
+    wl = workload_by_name(args.workload, args.layers)
     cb, done, t_total = oracle_decode_sample(wl, max_steps=max(1, args.steps),
                                              budget_s=args.reference_budget)
     return {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "tok/s",
@@ -329,6 +369,8 @@ def main():
     ap.add_argument("--workload", default="7b-bf16-b8")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--reference-budget", type=float, default=60.0)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="profiling aid: same shapes, fewer layers (small device footprint)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     rank = int(os.environ.get("RANK", "0"))
@@ -338,7 +380,7 @@ def main():
     else:
         res = gpu_arm(args, rank, world)
         if rank == 0 and not args.no_cpu_baseline:
-            wl = workload_by_name(args.workload)
+            wl = workload_by_name(args.workload, args.layers)
             cb, _, _ = oracle_decode_sample(wl, max_steps=2, budget_s=15.0)
             res["cpu_baseline"] = cb
     if rank == 0 and res is not None:

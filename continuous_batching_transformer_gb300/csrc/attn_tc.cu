@@ -53,7 +53,7 @@ template <int HD>
 __global__ void __launch_bounds__(160, 1)
     k_attn_decode(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                   const float* __restrict__ qkv, const QueryRow* __restrict__ rows,
-                  const AttnItem* __restrict__ items, int n_items, int layer, int n_heads,
+                  const AttnItem* __restrict__ items, const int* __restrict__ n_items_dev, int layer, int n_heads,
                   int n_kv_heads, float* __restrict__ part_o, float2* __restrict__ part_ml,
                   int* err) {
   constexpr int nKh = HD / 64;                 // K boxes (64 dims each) per sub-chunk
@@ -97,6 +97,9 @@ __global__ void __launch_bounds__(160, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;  // columns 0..15: S^T, 16..31: O^T
+  pdl_wait();  // q and the K/V appended at t_s come from the previous kernel
+  pdl_launch();
+  const int n_items = *n_items_dev;
 
   if (warp == 4) {
     // ---- TMA producer: K boxes and V^T boxes of every sub-chunk of this CTA's items
@@ -293,6 +296,8 @@ __global__ void __launch_bounds__(160, 1)
 __global__ void k_attn_merge(const float* __restrict__ part_o, const float2* __restrict__ part_ml,
                              const int* __restrict__ item_base, const int* __restrict__ item_count,
                              int n_heads, int n_kv_heads, int head_dim, uint16_t* act, int lo_rows) {
+  pdl_wait();
+  pdl_launch();
   const int b = blockIdx.y, hq = blockIdx.x;
   const int G = n_heads / n_kv_heads, g = hq / G, h = hq % G;
   const int cnt = item_count[b];
@@ -328,27 +333,23 @@ cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const At
   cudaError_t rc = cudaFuncSetAttribute(k_attn_decode<HD>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (rc != cudaSuccess) return rc;
-  count_launch();
-  k_attn_decode<HD><<<grid, 160, smem, s>>>(tk, tv, a.qkv, a.rows, a.items, a.n_items, a.layer,
-                                            a.n_heads, a.n_kv_heads, a.part_o, a.part_ml, a.err);
-  return cudaGetLastError();
+  return launch_pdl(k_attn_decode<HD>, dim3(grid), dim3(160), smem, s, tk, tv, a.qkv, a.rows,
+                    a.items, a.n_items, a.layer, a.n_heads, a.n_kv_heads, a.part_o, a.part_ml,
+                    a.err);
 }
 
 }  // namespace
 
 bool launch_attn_decode_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnDecodeArgs& a,
                            int num_sms, cudaStream_t s) {
-  if (a.n_items <= 0) return true;
   if (a.n_heads % a.n_kv_heads || a.n_heads / a.n_kv_heads > 8) return false;
-  const int grid = a.n_items < num_sms ? a.n_items : num_sms;
+  const int grid = num_sms;  // persistent; the item count is read on the device
   cudaError_t rc;
   if (a.head_dim == 128) rc = launch_decode<128>(tk, tv, a, grid, s);
   else if (a.head_dim == 64) rc = launch_decode<64>(tk, tv, a, grid, s);
   else return false;
   if (rc != cudaSuccess) return false;
-  count_launch();
-  k_attn_merge<<<dim3(a.n_heads, a.B), 128, 0, s>>>(a.part_o, a.part_ml, a.item_base, a.item_count,
-                                                    a.n_heads, a.n_kv_heads, a.head_dim, a.act,
-                                                    a.act_lo);
-  return cudaGetLastError() == cudaSuccess;
+  rc = launch_pdl(k_attn_merge, dim3(a.n_heads, a.B), dim3(128), 0, s, a.part_o, a.part_ml,
+                  a.item_base, a.item_count, a.n_heads, a.n_kv_heads, a.head_dim, a.act, a.act_lo);
+  return rc == cudaSuccess;
 }

@@ -9,6 +9,8 @@
 // ---- embedding: x[i] = E[token[i]] (fp32); out-of-range ids set the error word ------------
 __global__ void k_embed(const int32_t* tokens, int d, int vocab, const uint16_t* table, float* x,
                         int* err) {
+  pdl_wait();
+  pdl_launch();
   int i = blockIdx.x;
   int t = tokens[i];
   float* xr = x + (size_t)i * d;
@@ -24,12 +26,13 @@ __global__ void k_embed(const int32_t* tokens, int d, int vocab, const uint16_t*
 void launch_embed(const int32_t* tokens, int n, const uint16_t* table, int d, int vocab, float* x,
                   int* err, cudaStream_t s) {
   if (n <= 0) return;
-  count_launch();
-  k_embed<<<n, 256, 0, s>>>(tokens, d, vocab, table, x, err);
+  launch_pdl(k_embed, dim3(n), dim3(256), 0, s, tokens, d, vocab, table, x, err);
 }
 
 // ---- RMSNorm: h = x / sqrt(mean(x^2) + eps) * g -----------------------------------------
 __global__ void k_rmsnorm(const float* x, const uint16_t* gain, int d, float eps, float* h) {
+  pdl_wait();
+  pdl_launch();
   __shared__ float red[32];
   const float* xr = x + (size_t)blockIdx.x * d;
   float ss = 0.f;
@@ -51,8 +54,7 @@ __global__ void k_rmsnorm(const float* x, const uint16_t* gain, int d, float eps
 void launch_rmsnorm(const float* x, const uint16_t* gain, int n, int d, float eps, float* h,
                     cudaStream_t s) {
   if (n <= 0) return;
-  count_launch();
-  k_rmsnorm<<<n, 256, 0, s>>>(x, gain, d, eps, h);
+  launch_pdl(k_rmsnorm, dim3(n), dim3(256), 0, s, x, gain, d, eps, h);
 }
 
 // bf16 operand of a tensor-core projection: hi = bf16(v), and lo = bf16(v - hi) in rows
@@ -65,6 +67,8 @@ CBT_D void store_act(uint16_t* act, int row, int K, int k, int lo_rows, float v)
 
 __global__ void k_rmsnorm_act(const float* x, const uint16_t* gain, int d, float eps,
                               uint16_t* act, int lo_rows) {
+  pdl_wait();
+  pdl_launch();
   __shared__ float red[32];
   const float* xr = x + (size_t)blockIdx.x * d;
   float ss = 0.f;
@@ -86,24 +90,26 @@ __global__ void k_rmsnorm_act(const float* x, const uint16_t* gain, int d, float
 void launch_rmsnorm_act(const float* x, const uint16_t* gain, int n, int d, float eps,
                         uint16_t* act, int lo_rows, cudaStream_t s) {
   if (n <= 0) return;
-  count_launch();
-  k_rmsnorm_act<<<n, 256, 0, s>>>(x, gain, d, eps, act, lo_rows);
+  launch_pdl(k_rmsnorm_act, dim3(n), dim3(256), 0, s, x, gain, d, eps, act, lo_rows);
 }
 
 __global__ void k_f32_to_act(const float* src, int K, uint16_t* act, int lo_rows) {
+  pdl_wait();
+  pdl_launch();
   const float* sr = src + (size_t)blockIdx.x * K;
   for (int k = threadIdx.x; k < K; k += blockDim.x) store_act(act, blockIdx.x, K, k, lo_rows, sr[k]);
 }
 
 void launch_f32_to_act(const float* src, int n, int K, uint16_t* act, int lo_rows, cudaStream_t s) {
   if (n <= 0) return;
-  count_launch();
-  k_f32_to_act<<<n, 256, 0, s>>>(src, K, act, lo_rows);
+  launch_pdl(k_f32_to_act, dim3(n), dim3(256), 0, s, src, K, act, lo_rows);
 }
 
 // ---- RoPE angles once per call: cos/sin of pos * theta^(-2i/hd), evaluated in double -------
 __global__ void k_rope_table(const QueryRow* rows, int n, int half, int head_dim, double theta,
                              float* cosv, float* sinv) {
+  pdl_wait();
+  pdl_launch();
   int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= n * half) return;
   int t = idx / half, i = idx % half;
@@ -120,14 +126,15 @@ void launch_rope_table(const QueryRow* rows, int n, int head_dim, double theta, 
   int half = head_dim / 2;
   int tot = n * half;
   if (tot <= 0) return;
-  count_launch();
-  k_rope_table<<<(tot + 255) / 256, 256, 0, s>>>(rows, n, half, head_dim, theta, cosv, sinv);
+  launch_pdl(k_rope_table, dim3((tot + 255) / 256), dim3(256), 0, s, rows, n, half, head_dim, theta, cosv, sinv);
 }
 
 // ---- RoPE q, k in place at the token's position; append k, v to its own slab at pos ------
 __global__ void k_rope_append(float* qkv, const QueryRow* rows, int layer, int n_heads,
                               int n_kv_heads, int head_dim, const float* cosv, const float* sinv,
                               uint16_t* arena) {
+  pdl_wait();
+  pdl_launch();
   int t = blockIdx.x;
   int half = head_dim / 2;
   int qd = n_heads * head_dim, kvd = n_kv_heads * head_dim;
@@ -161,8 +168,7 @@ void launch_rope_append(float* qkv, const QueryRow* rows, int n, int layer, int 
                         int n_kv_heads, int head_dim, const float* cosv, const float* sinv,
                         uint16_t* arena, cudaStream_t s) {
   if (n <= 0) return;
-  count_launch();
-  k_rope_append<<<n, 256, 0, s>>>(qkv, rows, layer, n_heads, n_kv_heads, head_dim, cosv, sinv,
+  launch_pdl(k_rope_append, dim3(n), dim3(256), 0, s, qkv, rows, layer, n_heads, n_kv_heads, head_dim, cosv, sinv,
                                   arena);
 }
 
@@ -170,6 +176,8 @@ void launch_rope_append(float* qkv, const QueryRow* rows, int n, int layer, int 
 // (to_slab: plain -> slab, else slab -> plain); positions [0, n)
 __global__ void k_v_convert(uint16_t* plain, uint16_t* arena, QueryRow r, int layer,
                             int n_kv_heads, int n, int head_dim, int to_slab) {
+  pdl_wait();
+  pdl_launch();
   long long tot = (long long)n_kv_heads * n * head_dim;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < tot;
        i += (long long)gridDim.x * blockDim.x) {
@@ -187,13 +195,14 @@ void launch_v_convert(uint16_t* plain, uint16_t* arena, const QueryRow& r, int l
   long long tot = (long long)n_kv_heads * n * head_dim;
   if (tot <= 0) return;
   int grid = (int)std::min<long long>((tot + 255) / 256, 4096);
-  count_launch();
-  k_v_convert<<<grid, 256, 0, s>>>(plain, arena, r, layer, n_kv_heads, n, head_dim, to_slab ? 1 : 0);
+  launch_pdl(k_v_convert, dim3(grid), dim3(256), 0, s, plain, arena, r, layer, n_kv_heads, n, head_dim, to_slab ? 1 : 0);
 }
 
 // ---- plain attention: one block per (token, q head), keys [0, pos] of its own slab -------
 __global__ void k_attention_naive(const float* qkv, const QueryRow* rows, int layer, int n_heads,
                                   int n_kv_heads, int head_dim, const uint16_t* arena, float* o) {
+  pdl_wait();
+  pdl_launch();
   extern __shared__ float sm[];
   __shared__ float red[32];
   int t = blockIdx.x, hq = blockIdx.y;
@@ -268,13 +277,14 @@ void launch_attention_naive(const float* qkv, const QueryRow* rows, int n, int l
   size_t smem = sizeof(float) * (size_t)(head_dim + max_keys);
   if (smem > 48 * 1024)
     cudaFuncSetAttribute(k_attention_naive, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  count_launch();
-  k_attention_naive<<<dim3(n, n_heads), 128, smem, s>>>(qkv, rows, layer, n_heads, n_kv_heads,
+  launch_pdl(k_attention_naive, dim3(dim3(n, n_heads)), dim3(128), smem, s, qkv, rows, layer, n_heads, n_kv_heads,
                                                          head_dim, arena, o);
 }
 
 // ---- greedy argmax, lowest index among equal maxima ----------------------------------------
 __global__ void k_argmax(const float* logits, int vocab, int32_t* out) {
+  pdl_wait();
+  pdl_launch();
   __shared__ float bv[32];
   __shared__ int bi[32];
   const float* r = logits + (size_t)blockIdx.x * vocab;
@@ -308,11 +318,12 @@ __global__ void k_argmax(const float* logits, int vocab, int32_t* out) {
 
 void launch_argmax(const float* logits, int n, int vocab, int32_t* out, cudaStream_t s) {
   if (n <= 0) return;
-  count_launch();
-  k_argmax<<<n, 512, 0, s>>>(logits, vocab, out);
+  launch_pdl(k_argmax, dim3(n), dim3(512), 0, s, logits, vocab, out);
 }
 
 __global__ void k_gather_rows(const float* src, const int32_t* idx, int d, float* dst) {
+  pdl_wait();
+  pdl_launch();
   const float* sr = src + (size_t)idx[blockIdx.x] * d;
   float* dr = dst + (size_t)blockIdx.x * d;
   for (int j = threadIdx.x; j < d; j += blockDim.x) dr[j] = sr[j];
@@ -321,13 +332,14 @@ __global__ void k_gather_rows(const float* src, const int32_t* idx, int d, float
 void launch_gather_rows(const float* src, const int32_t* idx, int n, int d, float* dst,
                         cudaStream_t s) {
   if (n <= 0) return;
-  count_launch();
-  k_gather_rows<<<n, 256, 0, s>>>(src, idx, d, dst);
+  launch_pdl(k_gather_rows, dim3(n), dim3(256), 0, s, src, idx, d, dst);
 }
 
 // ---- MLX-style 4-bit affine quantisation, one thread per (row, group) ----------------------
 __global__ void k_quantize_affine4(const uint16_t* w, int rows, int cols, int group,
                                    uint32_t* packed, uint16_t* scales, uint16_t* biases) {
+  pdl_wait();
+  pdl_launch();
   long long gid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   int ng = cols / group;
   if (gid >= (long long)rows * ng) return;
@@ -365,7 +377,6 @@ void launch_quantize_affine4(const uint16_t* w, int rows, int cols, int group, u
                              uint16_t* scales, uint16_t* biases, cudaStream_t s) {
   long long n = (long long)rows * (cols / group);
   if (n <= 0) return;
-  count_launch();
-  k_quantize_affine4<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(w, rows, cols, group, packed,
+  launch_pdl(k_quantize_affine4, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, w, rows, cols, group, packed,
                                                                  scales, biases);
 }

@@ -68,6 +68,13 @@ CBT_D float warp_max(float v) {
   return v;
 }
 
+// Programmatic dependent launch: every kernel of a step is launched so that it may start
+// while its predecessor drains; it must call pdl_wait() before touching memory the
+// predecessor writes (or reads: buffers are reused), and calls pdl_launch() to let its own
+// successor start early.  Without the launch attribute both are no-ops.
+CBT_D void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+CBT_D void pdl_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Epilogues of a projection y = x W^T.
 enum Epilogue : int {
   EPI_STORE = 0,   // out[n][m] = y

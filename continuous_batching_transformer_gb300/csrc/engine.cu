@@ -13,6 +13,7 @@
 #include <new>
 #include <unordered_map>
 #include <unordered_set>
+#include <tuple>
 #include <vector>
 
 #include "cbt.h"
@@ -92,14 +93,17 @@ struct cbt_engine {
   std::vector<AttnItem> hitems;
   std::vector<int> hitem_base, hitem_count;
   AttnItem* items = nullptr;
-  int* item_meta = nullptr;  // [max_batch] bases, then [max_batch] counts
+  int* item_meta = nullptr;  // [max_batch] bases, [max_batch] counts, then the item total
   size_t items_cap = 0;
   float* att_o = nullptr;
   float2* att_ml = nullptr;
   size_t att_items_cap = 0;
+  int item_total = 0;
   // staging buffer for host-side import/export of V
   uint16_t* stage = nullptr;
   size_t stage_elems = 0;
+  // captured decode steps, keyed by (B, last_tokens, logits, next_tokens)
+  std::map<std::tuple<int, const void*, const void*, const void*>, cudaGraphExec_t> graphs;
 
   // measurement: event pairs around launch groups of selected kernel classes
   struct TimeRec {
@@ -268,7 +272,7 @@ extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_w
     if (rc == cudaSuccess) {
       e->hitem_base.resize(p->max_batch);
       e->hitem_count.resize(p->max_batch);
-      chk(dmalloc(&e->item_meta, (size_t)2 * p->max_batch, &tot));
+      chk(dmalloc(&e->item_meta, (size_t)2 * p->max_batch + 1, &tot));
     }
     e->use_tc = maps_ok && c.d_ff % 64 == 0;
   }
@@ -290,6 +294,7 @@ extern "C" cbt_status cbt_engine_destroy(cbt_engine* e) {
   cudaError_t rc = cudaStreamSynchronize(e->stream);
   free_scratch(e);
   for (cudaEvent_t ev : e->ev_pool) cudaEventDestroy(ev);
+  for (auto& kv : e->graphs) cudaGraphExecDestroy(kv.second);
   delete e;
   return rc == cudaSuccess ? CBT_OK : CBT_ERR_CUDA;
 }
@@ -585,7 +590,7 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
       a.qkv = e->qkv;
       a.rows = e->rows;
       a.items = e->items;
-      a.n_items = (int)e->hitems.size();
+      a.n_items = e->item_meta + 2 * e->p.max_batch;
       a.item_base = e->item_meta;
       a.item_count = e->item_meta + e->p.max_batch;
       a.B = n;
@@ -647,6 +652,8 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
   return cudaGetLastError();
 }
 
+static void drop_graphs(cbt_engine* e);
+
 // Work list of the tensor-core decode attention for the rows in e->hrows[0..B): per row and kv
 // head, runs of kSubsPerItem 128-key sub-chunks over positions [0, pos].  Grows the item and
 // partial buffers when needed and copies the list to the device on the engine stream.
@@ -670,6 +677,7 @@ static cudaError_t plan_decode_attention(cbt_engine* e, int B) {
   if (n > e->att_items_cap) {
     size_t cap = std::max(n, e->att_items_cap * 2);
     rc = cudaStreamSynchronize(e->stream);
+    drop_graphs(e);  // captured steps hold the old buffer addresses
     cudaFree(e->items);
     cudaFree(e->att_o);
     cudaFree(e->att_ml);
@@ -685,13 +693,52 @@ static cudaError_t plan_decode_attention(cbt_engine* e, int B) {
   }
   rc = cudaMemcpyAsync(e->items, e->hitems.data(), n * sizeof(AttnItem), cudaMemcpyHostToDevice,
                        e->stream);
+  e->item_total = (int)n;
   if (rc == cudaSuccess)
     rc = cudaMemcpyAsync(e->item_meta, e->hitem_base.data(), B * sizeof(int),
                          cudaMemcpyHostToDevice, e->stream);
   if (rc == cudaSuccess)
     rc = cudaMemcpyAsync(e->item_meta + e->p.max_batch, e->hitem_count.data(), B * sizeof(int),
                          cudaMemcpyHostToDevice, e->stream);
+  if (rc == cudaSuccess)
+    rc = cudaMemcpyAsync(e->item_meta + 2 * e->p.max_batch, &e->item_total, sizeof(int),
+                         cudaMemcpyHostToDevice, e->stream);
   return rc;
+}
+
+// The decode step as a CUDA graph, captured once per (B, token/logits/next buffers) and
+// replayed: ~300 kernel launches become one graph launch, and the kernels' programmatic
+// dependencies let each one's prologue overlap its predecessor's tail.  Every per-step input
+// (row table, attention work list and its length) lives in device buffers written before the
+// launch, so a captured graph stays valid while those buffers keep their addresses.
+static void drop_graphs(cbt_engine* e) {
+  for (auto& kv : e->graphs) cudaGraphExecDestroy(kv.second);
+  e->graphs.clear();
+}
+
+static cudaError_t run_decode_graph(cbt_engine* e, int B, const int32_t* tokens, int max_keys,
+                                    long long total_keys, float* logits, int32_t* next) {
+  auto key = std::make_tuple(B, static_cast<const void*>(tokens), static_cast<const void*>(logits),
+                             static_cast<const void*>(next));
+  auto it = e->graphs.find(key);
+  if (it == e->graphs.end()) {
+    if (e->graphs.size() >= 16) drop_graphs(e);
+    cudaGraph_t g = nullptr;
+    cudaError_t rc = cudaStreamBeginCapture(e->stream, cudaStreamCaptureModeThreadLocal);
+    if (rc != cudaSuccess) return rc;
+    cudaError_t frc = forward(e, B, tokens, max_keys, total_keys, false, B, logits, next);
+    rc = cudaStreamEndCapture(e->stream, &g);
+    if (frc != cudaSuccess || rc != cudaSuccess) {
+      if (g) cudaGraphDestroy(g);
+      return frc != cudaSuccess ? frc : rc;
+    }
+    cudaGraphExec_t ex = nullptr;
+    rc = cudaGraphInstantiate(&ex, g, 0);
+    cudaGraphDestroy(g);
+    if (rc != cudaSuccess) return rc;
+    it = e->graphs.emplace(key, ex).first;
+  }
+  return cudaGraphLaunch(it->second, e->stream);
 }
 
 extern "C" cbt_status cbt_decode_step_batch(cbt_engine* e, const int32_t* ids, int32_t B,
@@ -718,7 +765,12 @@ extern "C" cbt_status cbt_decode_step_batch(cbt_engine* e, const int32_t* ids, i
   cudaError_t rc = cudaMemcpyAsync(e->rows, e->hrows.data(), sizeof(QueryRow) * B,
                                    cudaMemcpyHostToDevice, e->stream);
   if (rc == cudaSuccess && e->use_tc) rc = plan_decode_attention(e, B);
-  if (rc == cudaSuccess) rc = forward(e, B, last_tokens, max_keys, total_keys, false, B, logits, next_tokens);
+  if (rc == cudaSuccess) {
+    if (e->use_tc && e->timing_mask == 0 && e->stream != nullptr)
+      rc = run_decode_graph(e, B, last_tokens, max_keys, total_keys, logits, next_tokens);
+    else
+      rc = forward(e, B, last_tokens, max_keys, total_keys, false, B, logits, next_tokens);
+  }
   if (rc != cudaSuccess) return rc == cudaErrorNotSupported ? CBT_ERR_UNSUPPORTED : CBT_ERR_CUDA;
   for (int b = 0; b < B; ++b) e->slabs[ids[b]].pos += 1;
   e->steps += 1;

@@ -35,6 +35,8 @@ template <int NB, bool Q4>
 __global__ void __launch_bounds__(GEMV_THREADS) gemv_splitk(const float* __restrict__ x, int n,
                                                             int K, LinearW W, int M, int Ks,
                                                             float* __restrict__ part) {
+  pdl_wait();
+  pdl_launch();
   extern __shared__ float xs[];  // [NB][Ks]
   const int k0 = blockIdx.y * Ks;
   for (int i = threadIdx.x; i < n * Ks; i += blockDim.x) {
@@ -89,6 +91,8 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_splitk(const float* __restr
 
 __global__ void splitk_reduce(const float* __restrict__ part, int S, int n, int M, int epi,
                               float* __restrict__ out) {
+  pdl_wait();
+  pdl_launch();
   const int Mo = epi == EPI_SWIGLU ? M / 2 : M;
   long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   if (idx >= (long long)n * Mo) return;
@@ -112,6 +116,8 @@ constexpr int TT = 64, TM = 64, TK = 16;
 template <bool Q4, int EPI>
 __global__ void __launch_bounds__(256) gemm_tiled(const float* __restrict__ x, int n, int K,
                                                   LinearW W, int M, float* __restrict__ out) {
+  pdl_wait();
+  pdl_launch();
   // SWIGLU: columns j of the tile are gate row j and up row j + M/2
   __shared__ float xs[TK][TT + 4];
   __shared__ float ws[TK][TM + 4];
@@ -196,12 +202,10 @@ void run_gemv(const float* x, int n, int K, const LinearW& W, int M, int Ks, flo
   size_t smem = sizeof(float) * (size_t)NB * Ks;
   if (W.fmt == CBT_WEIGHTS_BF16) {
     cudaFuncSetAttribute(gemv_splitk<NB, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    count_launch();
-    gemv_splitk<NB, false><<<grid, GEMV_THREADS, smem, s>>>(x, n, K, W, M, Ks, part);
+    launch_pdl((gemv_splitk<NB, false>), dim3(grid), dim3(GEMV_THREADS), smem, s, x, n, K, W, M, Ks, part);
   } else {
     cudaFuncSetAttribute(gemv_splitk<NB, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    count_launch();
-    gemv_splitk<NB, true><<<grid, GEMV_THREADS, smem, s>>>(x, n, K, W, M, Ks, part);
+    launch_pdl((gemv_splitk<NB, true>), dim3(grid), dim3(GEMV_THREADS), smem, s, x, n, K, W, M, Ks, part);
   }
 }
 
@@ -209,11 +213,10 @@ template <int EPI>
 void run_tiled(const float* x, int n, int K, const LinearW& W, int M, float* out, cudaStream_t s) {
   int Mo = EPI == EPI_SWIGLU ? M / 2 : M;
   dim3 grid((Mo + TM - 1) / TM, (n + TT - 1) / TT);
-  count_launch();
   if (W.fmt == CBT_WEIGHTS_BF16)
-    gemm_tiled<false, EPI><<<grid, 256, 0, s>>>(x, n, K, W, M, out);
+    launch_pdl((gemm_tiled<false, EPI>), dim3(grid), dim3(256), 0, s, x, n, K, W, M, out);
   else
-    gemm_tiled<true, EPI><<<grid, 256, 0, s>>>(x, n, K, W, M, out);
+    launch_pdl((gemm_tiled<true, EPI>), dim3(grid), dim3(256), 0, s, x, n, K, W, M, out);
 }
 
 }  // namespace
@@ -228,8 +231,7 @@ void launch_linear(const float* x, int n, int K, const LinearW& W, int M, Epilog
     else run_gemv<32>(x, n, K, W, M, Ks, partials, s);
     int Mo = epi == EPI_SWIGLU ? M / 2 : M;
     long long tot = (long long)n * Mo;
-    count_launch();
-    splitk_reduce<<<(unsigned)((tot + 255) / 256), 256, 0, s>>>(partials, K / Ks, n, M, epi, out);
+    launch_pdl(splitk_reduce, dim3((unsigned)((tot + 255) / 256)), dim3(256), 0, s, partials, K / Ks, n, M, epi, out);
     return;
   }
   if (epi == EPI_STORE) run_tiled<EPI_STORE>(x, n, K, W, M, out, s);

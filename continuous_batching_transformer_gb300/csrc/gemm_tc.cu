@@ -162,6 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  pdl_launch();
   Sched sch;
   sch.init(p);
   int tile, kb, ke;
@@ -172,6 +173,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       long long issued = 0;
       bool ok = true;
+      // The weights never depend on the previous kernel: the first STAGES weight tiles are
+      // requested before waiting for it; their activation tiles follow once it has finished.
+      int pend_k[STAGES], pend_nt[STAGES], pend_st[STAGES];
+      int npend = 0;
+      bool dep_done = false;
+      auto flush_pending = [&]() {
+        pdl_wait();
+        dep_done = true;
+        for (int i = 0; i < npend; ++i)
+          tc::tma_load_2d(sX + pend_st[i] * kXBytes, &tx, &full[pend_st[i]], pend_k[i] * 64,
+                          pend_nt[i] * BN, pol_x);
+        npend = 0;
+      };
       while (ok && sch.next(p, tile, kb, ke)) {
         const int rb = tile / p.NT, nt = tile % p.NT;
         const int y0 = p.epi == EPI_SWIGLU ? rb * 64 : rb * 128;
@@ -185,7 +199,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mbar_expect_tx(&full[stage], kABytes + kXBytes);
           tc::tma_load_2d(sA + stage * kABytes, &tw, &full[stage], k * 64, y0, pol_w);
           tc::tma_load_2d(sA + stage * kABytes + 8192, &tw, &full[stage], k * 64, y1, pol_w);
-          tc::tma_load_2d(sX + stage * kXBytes, &tx, &full[stage], k * 64, nt * BN, pol_x);
+          if (dep_done) {
+            tc::tma_load_2d(sX + stage * kXBytes, &tx, &full[stage], k * 64, nt * BN, pol_x);
+          } else {
+            pend_k[npend] = k;
+            pend_nt[npend] = nt;
+            pend_st[npend] = stage;
+            if (++npend == STAGES) flush_pending();
+          }
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -193,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      if (!dep_done) flush_pending();
       // never leave with copies in flight: wait for the last loads issued to each stage
       for (int i = 0; i < STAGES && i < issued; ++i) {
         if (--stage < 0) {
@@ -244,6 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_wait(done, 0);
     }
   } else {  // ---- epilogue warps 2..5
+    pdl_wait();  // outputs and the stream-K scratch are shared with the previous kernel
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;
     int acc = 0;
@@ -338,9 +361,7 @@ cudaError_t launch_inst(const CUtensorMap& tw, const CUtensorMap& tx, const TcPa
   auto kern = k_tc_linear<BN, STAGES, SPLIT>;
   cudaError_t rc = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (rc != cudaSuccess) return rc;
-  count_launch();
-  kern<<<grid, kThreads, smem, s>>>(tw, tx, p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, tw, tx, p);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

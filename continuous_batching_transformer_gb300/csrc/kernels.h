@@ -6,9 +6,29 @@
 
 #include "common.cuh"
 
+#include <utility>
+
 // kernel launches queued through the launchers below (for launch accounting)
 long long kernel_launch_count();
 void count_launch(int n = 1);
+
+// Launch with programmatic stream serialization (see pdl_wait / pdl_launch in common.cuh)
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  count_launch();
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 struct LinearW {
   const void* w;       // bf16 [M][K] or uint32 [M][K/8]
@@ -51,7 +71,8 @@ struct AttnDecodeArgs {
   const float* qkv;          // [B][q|k|v] fp32, q and k already rotated
   const QueryRow* rows;      // [B]
   const AttnItem* items;     // work items, grouped by row: row b's items start at item_base[b],
-  int n_items;               //   kv head g's splits at item_base[b] + g * item_count[b]
+  const int* n_items;        //   kv head g's splits at item_base[b] + g * item_count[b]
+                             //   (count on the device, so a captured step stays valid)
   const int* item_base;      // [B]
   const int* item_count;     // [B] splits per (row, kv head)
   int B, layer, n_heads, n_kv_heads, head_dim;
