@@ -7,26 +7,22 @@
 //   softmax on S^T: one thread per key (TMEM lane = key), running max/sum per head
 //   O^T[d][j]  = V^T[d] . P[j]    tcgen05.mma, M = 128 dims, N = 16 (p rows: 8 hi + 8 lo)
 // and O is accumulated in registers (one thread per dim) with the running-max rescale.
-// K and V^T tiles come from two arena-wide TMA tensor maps (K rows of head_dim, V rows of 64
-// keys) into a 3-stage ring filled by a producer warp; Q and P are written by the threads in
-// the 128-byte swizzle the MMA descriptors expect.  Items run on a persistent grid.  Each
-// item leaves unnormalised partial outputs with their (max, sum); attn_merge combines them.
+// A producer warp loads K and V^T tiles through two arena-wide TMA tensor maps (K rows of
+// head_dim, V rows of 64 keys) and the group's Q operand, which the RoPE kernel already laid
+// out as the swizzled hi/lo image the MMA reads, with a 1-D bulk copy.  K and V have their own
+// buffers and barriers, so the next K tile streams in while this sub-chunk's softmax and P.V
+// run.  Three CTAs share an SM so their latency chains overlap; items run on a persistent
+// grid.  Each item leaves unnormalised partial outputs with their (max, sum); attn_merge
+// combines them.
 #include "kernels.h"
 #include "tc_common.cuh"
 
 namespace {
 
-constexpr int kSub = 128;        // keys per sub-chunk (MMA M)
-constexpr int kStages = 3;
-constexpr int kBox = 16384;      // one 128 x 128-byte TMA box
-constexpr int kCompute = 128;    // threads of warps 0..3; warp 4 is the TMA producer
-
-// byte offset of bf16 element (row, col) in a K-major tile of 128-byte rows, 128B-swizzled,
-// whose 64-column groups are `group_stride` bytes apart
-__device__ __forceinline__ uint32_t sw128_off(int row, int col, int group_stride) {
-  const int g = col >> 6, c = col & 63;
-  return (uint32_t)(g * group_stride + row * 128 + ((((c >> 3) ^ (row & 7))) << 4) + (c & 7) * 2);
-}
+constexpr int kSub = 128;      // keys per sub-chunk (MMA M)
+constexpr int kBox = 16384;    // one 128 x 128-byte tile
+constexpr int kCompute = 128;  // threads of warps 0..3; warp 4 is the producer
+constexpr int kCtasPerSm = 3;
 
 __device__ __forceinline__ void st_bf16(uint8_t* base, uint32_t off, uint16_t v) {
   *reinterpret_cast<uint16_t*>(base + off) = v;
@@ -49,27 +45,35 @@ __device__ __forceinline__ bool bar_any(int id, int n, bool pred) {
   return r != 0;
 }
 
+__device__ __forceinline__ void flag_timeout(int* err, volatile int* abort_flag, int where) {
+  *abort_flag = 1;
+  if (atomicCAS(err, 0, CBT_DEV_TIMEOUT) == 0) err[1] = where;
+}
+
 template <int HD>
-__global__ void __launch_bounds__(160, 1)
+__global__ void __launch_bounds__(160, kCtasPerSm)
     k_attn_decode(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
-                  const float* __restrict__ qkv, const QueryRow* __restrict__ rows,
-                  const AttnItem* __restrict__ items, const int* __restrict__ n_items_dev, int layer, int n_heads,
-                  int n_kv_heads, float* __restrict__ part_o, float2* __restrict__ part_ml,
-                  int* err) {
-  constexpr int nKh = HD / 64;                 // K boxes (64 dims each) per sub-chunk
-  constexpr int kStageBytes = (nKh + 2) * kBox;  // K boxes + two V^T boxes
+                  const uint8_t* __restrict__ qtile, const QueryRow* __restrict__ rows,
+                  const AttnItem* __restrict__ items, const int* __restrict__ n_items_dev,
+                  int layer, int n_kv_heads, int G, float* __restrict__ part_o,
+                  float2* __restrict__ part_ml, int* err) {
+  constexpr int nKh = HD / 64;                          // K boxes (64 dims each)
+  constexpr uint32_t kQBytes = 16 * HD * 2;             // Q operand image
+  constexpr uint32_t kKBytes = kSub * HD * 2;           // K tile
+  constexpr uint32_t kVBytes = 2 * HD * 128;            // V^T tile: two boxes of HD rows x 64 keys
   constexpr uint32_t kIdesc = tc::idesc_bf16(128, 16);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* stages = smem;
-  uint8_t* sQ = smem + kStages * kStageBytes;   // [16 rows][HD], nKh groups of 2 KB
-  uint8_t* sP = sQ + nKh * 2048;                // [16 rows][128 keys], 2 groups of 2 KB
-  uint64_t* full = reinterpret_cast<uint64_t*>(sP + 2 * 2048);
-  uint64_t* empty = full + kStages;
-  uint64_t* bar_s = empty + kStages;
-  uint64_t* bar_o = bar_s + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_o + 1);
+  uint8_t* sK = smem;                       // nKh boxes
+  uint8_t* sV = sK + nKh * kBox;            // 2 boxes (HD rows used of each 128)
+  uint8_t* sQ = sV + 2 * kBox;              // [16 rows][HD]: nKh groups of 2 KB
+  uint8_t* sP = sQ + nKh * 2048;            // [16 rows][128 keys]: 2 groups of 2 KB
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * 2048);
+  uint64_t *kfull = bars, *vfull = bars + 1, *qfull = bars + 2;
+  uint64_t *kempty = bars + 3, *vempty = bars + 4, *qempty = bars + 5;
+  uint64_t *bar_s = bars + 6, *bar_o = bars + 7;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* red = reinterpret_cast<float*>(tmem_slot + 4);  // [4 warps][8 heads]
   float* red2 = red + 32;                                // [4 warps][8 heads]
@@ -78,15 +82,8 @@ __global__ void __launch_bounds__(160, 1)
   float* scl = l_run + 8;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int G = n_heads / n_kv_heads;
-  const int qd = n_heads * HD, kvd = n_kv_heads * HD;
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      tc::mbar_init(&full[s], 1);
-      tc::mbar_init(&empty[s], 1);
-    }
-    tc::mbar_init(bar_s, 1);
-    tc::mbar_init(bar_o, 1);
+    for (int i = 0; i < 8; ++i) tc::mbar_init(&bars[i], 1);
     *abort_flag = 0;
     tc::mbar_fence_init();
     tc::tma_prefetch_desc(&tk);
@@ -97,78 +94,64 @@ __global__ void __launch_bounds__(160, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;  // columns 0..15: S^T, 16..31: O^T
-  pdl_wait();  // q and the K/V appended at t_s come from the previous kernel
+  pdl_wait();  // the Q operand and the K/V appended at t_s come from the previous kernel
   pdl_launch();
   const int n_items = *n_items_dev;
 
   if (warp == 4) {
-    // ---- TMA producer: K boxes and V^T boxes of every sub-chunk of this CTA's items
+    // ---- producer: per item the Q image, per sub-chunk a K tile and a V^T tile
     if (lane == 0) {
       const uint64_t pol = tc::policy_evict_first();
-      int stage = 0;
-      uint32_t phase = 0;
-      long long issued = 0;
+      uint32_t qn = 0, kn = 0, vn = 0;
       bool ok = true;
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
         const AttnItem w = items[it];
         const QueryRow r = rows[w.b];
         const long long krow = kv_block(r, layer, 0, w.g, n_kv_heads, HD) / HD;
         const long long vrow = kv_block(r, layer, 1, w.g, n_kv_heads, HD) / 64;
+        if (!tc::mbar_wait(qempty, (qn & 1) ^ 1)) {
+          flag_timeout(err, abort_flag, 21);
+          break;
+        }
+        tc::mbar_expect_tx(qfull, kQBytes);
+        tc::bulk_load(sQ, qtile + ((size_t)w.b * n_kv_heads + w.g) * kQBytes, kQBytes, qfull);
+        ++qn;
         for (int sub = w.s0; sub < w.s1; ++sub) {
-          if (!tc::mbar_wait(&empty[stage], phase ^ 1)) {
-            *abort_flag = 1;
-            if (atomicCAS(err, 0, CBT_DEV_TIMEOUT) == 0) err[1] = 11;
+          if (!tc::mbar_wait(kempty, (kn & 1) ^ 1)) {
+            flag_timeout(err, abort_flag, 22);
             ok = false;
             break;
           }
-          // K: 128 keys x HD dims; V^T: two boxes of HD rows x 64 keys
-          tc::mbar_expect_tx(&full[stage], (uint32_t)(kSub * HD * 2 + 2 * HD * 128));
-          uint8_t* st = stages + stage * kStageBytes;
+          tc::mbar_expect_tx(kfull, kKBytes);
 #pragma unroll
           for (int h = 0; h < nKh; ++h)
-            tc::tma_load_2d(st + h * kBox, &tk, &full[stage], h * 64, (int)(krow + sub * kSub), pol);
+            tc::tma_load_2d(sK + h * kBox, &tk, kfull, h * 64, (int)(krow + sub * kSub), pol);
+          ++kn;
+          if (!tc::mbar_wait(vempty, (vn & 1) ^ 1)) {
+            flag_timeout(err, abort_flag, 23);
+            ok = false;
+            break;
+          }
+          tc::mbar_expect_tx(vfull, kVBytes);
 #pragma unroll
           for (int j = 0; j < 2; ++j)
-            tc::tma_load_2d(st + (nKh + j) * kBox, &tv, &full[stage], 0,
-                            (int)(vrow + (long long)(2 * sub + j) * HD), pol);
-          ++issued;
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1;
-          }
+            tc::tma_load_2d(sV + j * kBox, &tv, vfull, 0, (int)(vrow + (long long)(2 * sub + j) * HD),
+                            pol);
+          ++vn;
         }
       }
-      for (int i = 0; i < kStages && i < issued; ++i) {  // no copies in flight at exit
-        if (--stage < 0) {
-          stage = kStages - 1;
-          phase ^= 1;
-        }
-        tc::mbar_wait(&full[stage], phase);
-      }
+      // no copies in flight at exit: the last Q, K and V loads have landed
+      if (qn) tc::mbar_wait(qfull, (qn - 1) & 1);
+      if (kn) tc::mbar_wait(kfull, (kn - 1) & 1);
+      if (vn) tc::mbar_wait(vfull, (vn - 1) & 1);
     }
   } else {
     // ---- compute warps: MMA issue (thread 0), softmax (thread = key), accumulate (thread = dim)
-    const float qscale = rsqrtf((float)HD);
-    int stage = 0;
-    uint32_t phase = 0, cnt = 0;
+    uint32_t qn = 0, kn = 0, vn = 0, sn = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
       const AttnItem w = items[it];
-      const QueryRow r = rows[w.b];
-      const int n = r.pos + 1;
-      // Q operand: rows 0..G-1 hi parts, 8..8+G-1 lo parts of the group's (rotated) q rows
-      const float* qrow = qkv + (size_t)w.b * (qd + 2 * kvd) + (size_t)w.g * G * HD;
-      for (int i = tid; i < 8 * HD; i += kCompute) {
-        const int h = i / HD, d = i % HD;
-        uint16_t hi = 0, lo = 0;
-        if (h < G) {
-          const float v = qrow[h * HD + d] * qscale;
-          hi = f32_to_bf16(v);
-          lo = f32_to_bf16(v - bf16_to_f32(hi));
-        }
-        st_bf16(sQ, sw128_off(h, d, 2048), hi);
-        st_bf16(sQ, sw128_off(8 + h, d, 2048), lo);
-      }
+      const int n = rows[w.b].pos + 1;
       if (tid < 8) {
         m_run[tid] = -INFINITY;
         l_run[tid] = 0.f;
@@ -176,28 +159,30 @@ __global__ void __launch_bounds__(160, 1)
       float oacc[8];
 #pragma unroll
       for (int h = 0; h < 8; ++h) oacc[h] = 0.f;
-      fence_proxy_async();
       tc::named_bar_sync(1, kCompute);
 
-      for (int sub = w.s0; sub < w.s1; ++sub, ++cnt) {
-        uint8_t* st = stages + stage * kStageBytes;
+      for (int sub = w.s0; sub < w.s1; ++sub, ++sn) {
         if (tid == 0) {
-          if (!tc::mbar_wait(&full[stage], phase)) {
-            *abort_flag = 1;
-            if (atomicCAS(err, 0, CBT_DEV_TIMEOUT) == 0) err[1] = 12;
+          bool good = true;
+          if (sub == w.s0) good = tc::mbar_wait(qfull, qn & 1);
+          good = good && tc::mbar_wait(kfull, kn & 1);
+          if (!good) {
+            flag_timeout(err, abort_flag, 24);
           } else {
             tc::tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk) {
-              const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(st + (kk >> 2) * kBox)) + 2 * (kk & 3);
+              const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sK + (kk >> 2) * kBox)) + 2 * (kk & 3);
               const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sQ + (kk >> 2) * 2048)) + 2 * (kk & 3);
               tc::mma_bf16(tmem, ad, bd, kIdesc, kk > 0 ? 1u : 0u);
             }
             tc::mma_commit(bar_s);
+            tc::mma_commit(kempty);                 // K buffer free once the MMA has read it
+            if (sub == w.s1 - 1) tc::mma_commit(qempty);  // and the Q image after the last one
           }
         }
-        tc::named_bar_sync(1, kCompute);
-        const bool bad_s = *abort_flag || !tc::mbar_wait(bar_s, cnt & 1);
+        ++kn;
+        const bool bad_s = *abort_flag || !tc::mbar_wait(bar_s, sn & 1);
         if (bar_any(2, kCompute, bad_s)) {
           ok = false;
           break;
@@ -229,14 +214,24 @@ __global__ void __launch_bounds__(160, 1)
         for (int h = 0; h < 8; ++h) {
           const float p = (valid && h < G) ? __expf(s[h] - m_run[h]) : 0.f;
           const uint16_t hi = f32_to_bf16(p);
-          st_bf16(sP, sw128_off(h, tid, 2048), hi);
-          st_bf16(sP, sw128_off(8 + h, tid, 2048), f32_to_bf16(p - bf16_to_f32(hi)));
+          st_bf16(sP, sw128_offset(h, tid, 2048), hi);
+          st_bf16(sP, sw128_offset(8 + h, tid, 2048), f32_to_bf16(p - bf16_to_f32(hi)));
           const float ps = warp_sum(p);
           if (lane == 0) red2[warp * 8 + h] = ps;
         }
-        if (!valid) {  // this key's V^T column may hold stale values: make it zero
-          uint8_t* vt = st + nKh * kBox + (tid >> 6) * kBox;
-          for (int d = 0; d < HD; ++d) st_bf16(vt, sw128_off(d, tid & 63, 0), 0);
+        if (sub * kSub + kSub > n) {
+          // keys past t_s: their V^T columns may hold stale values, so once V has landed
+          // those columns are set to zero (P is zero there too)
+          const bool bad_v = !tc::mbar_wait(vfull, vn & 1);
+          if (bar_any(2, kCompute, bad_v)) {
+            flag_timeout(err, abort_flag, 25);
+            ok = false;
+            break;
+          }
+          if (!valid) {
+            uint8_t* vt = sV + (tid >> 6) * kBox;
+            for (int d = 0; d < HD; ++d) st_bf16(vt, sw128_offset(d, tid & 63, 0), 0);
+          }
         }
         fence_proxy_async();
         tc::tc_fence_before();
@@ -244,21 +239,23 @@ __global__ void __launch_bounds__(160, 1)
         if (tid < 8)
           l_run[tid] = l_run[tid] * scl[tid] + red2[tid] + red2[8 + tid] + red2[16 + tid] + red2[24 + tid];
         if (tid == 0) {
-          tc::tc_fence_after();
+          if (!tc::mbar_wait(vfull, vn & 1)) {
+            flag_timeout(err, abort_flag, 26);
+          } else {
+            tc::tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < kSub / 16; ++kk) {
-            const uint64_t ad =
-                tc::sdesc_sw128(tc::smem_u32(st + (nKh + (kk >> 2)) * kBox)) + 2 * (kk & 3);
-            const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sP + (kk >> 2) * 2048)) + 2 * (kk & 3);
-            tc::mma_bf16(tmem + 16, ad, bd, kIdesc, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < kSub / 16; ++kk) {
+              const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sV + (kk >> 2) * kBox)) + 2 * (kk & 3);
+              const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sP + (kk >> 2) * 2048)) + 2 * (kk & 3);
+              tc::mma_bf16(tmem + 16, ad, bd, kIdesc, kk > 0 ? 1u : 0u);
+            }
+            tc::mma_commit(bar_o);
+            tc::mma_commit(vempty);
           }
-          tc::mma_commit(bar_o);
-          tc::mma_commit(&empty[stage]);  // the stage is free once both MMAs have read it
         }
-        const bool bad_o = !tc::mbar_wait(bar_o, cnt & 1);
-        if (bad_o && atomicCAS(err, 0, CBT_DEV_TIMEOUT) == 0) err[1] = 13;
+        ++vn;
+        const bool bad_o = *abort_flag || !tc::mbar_wait(bar_o, sn & 1);
         if (bar_any(2, kCompute, bad_o)) {
-          *abort_flag = 1;
           ok = false;
           break;
         }
@@ -269,11 +266,8 @@ __global__ void __launch_bounds__(160, 1)
         for (int h = 0; h < 8; ++h)
           oacc[h] = oacc[h] * scl[h] + __uint_as_float(raw[h]) + __uint_as_float(raw[8 + h]);
         tc::tc_fence_before();
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1;
-        }
       }
+      ++qn;
       if (!ok) break;
       // partial output of this item, relative to m_run
       if (tid < HD) {
@@ -328,14 +322,14 @@ template <int HD>
 cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const AttnDecodeArgs& a,
                           int grid, cudaStream_t s) {
   constexpr int nKh = HD / 64;
-  constexpr size_t smem = 1024 + kStages * (nKh + 2) * kBox + nKh * 2048 + 2 * 2048 + 1024;
-  static_assert(smem <= 227 * 1024, "shared memory budget");
+  constexpr size_t smem = 1024 + (nKh + 2) * kBox + nKh * 2048 + 2 * 2048 + 512;
+  static_assert(smem * kCtasPerSm <= 228 * 1024, "shared memory budget");
   cudaError_t rc = cudaFuncSetAttribute(k_attn_decode<HD>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (rc != cudaSuccess) return rc;
-  return launch_pdl(k_attn_decode<HD>, dim3(grid), dim3(160), smem, s, tk, tv, a.qkv, a.rows,
-                    a.items, a.n_items, a.layer, a.n_heads, a.n_kv_heads, a.part_o, a.part_ml,
-                    a.err);
+  return launch_pdl(k_attn_decode<HD>, dim3(grid), dim3(160), smem, s, tk, tv, a.qtile, a.rows,
+                    a.items, a.n_items, a.layer, a.n_kv_heads, a.n_heads / a.n_kv_heads, a.part_o,
+                    a.part_ml, a.err);
 }
 
 }  // namespace
@@ -343,7 +337,7 @@ cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const At
 bool launch_attn_decode_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnDecodeArgs& a,
                            int num_sms, cudaStream_t s) {
   if (a.n_heads % a.n_kv_heads || a.n_heads / a.n_kv_heads > 8) return false;
-  const int grid = num_sms;  // persistent; the item count is read on the device
+  const int grid = kCtasPerSm * num_sms;  // persistent; the item count is read on the device
   cudaError_t rc;
   if (a.head_dim == 128) rc = launch_decode<128>(tk, tv, a, grid, s);
   else if (a.head_dim == 64) rc = launch_decode<64>(tk, tv, a, grid, s);

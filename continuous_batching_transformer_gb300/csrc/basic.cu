@@ -132,7 +132,7 @@ void launch_rope_table(const QueryRow* rows, int n, int head_dim, double theta, 
 // ---- RoPE q, k in place at the token's position; append k, v to its own slab at pos ------
 __global__ void k_rope_append(float* qkv, const QueryRow* rows, int layer, int n_heads,
                               int n_kv_heads, int head_dim, const float* cosv, const float* sinv,
-                              uint16_t* arena) {
+                              uint16_t* arena, uint8_t* qtile) {
   pdl_wait();
   pdl_launch();
   int t = blockIdx.x;
@@ -155,6 +155,21 @@ __global__ void k_rope_append(float* qkv, const QueryRow* rows, int layer, int n
       uint16_t* kd = arena + k_index(r, layer, h - n_heads, r.pos, 0, n_kv_heads, head_dim);
       kd[i] = f32_to_bf16(ra);
       kd[i + half] = f32_to_bf16(rb);
+    } else if (qtile) {
+      // the decode attention's Q operand of this row and kv head: [16 rows][head_dim] bf16 in
+      // the MMA's swizzled layout; row j < G holds the hi part of q head g*G + j scaled by
+      // 1/sqrt(head_dim), row 8 + j its lo part (rows beyond stay zero)
+      const int G = n_heads / n_kv_heads, g = h / G, j = h % G;
+      uint8_t* tile = qtile + ((size_t)t * n_kv_heads + g) * (16 * head_dim * 2);
+      const float qs = rsqrtf((float)head_dim);
+      const float vals[2] = {ra * qs, rb * qs};
+      const int cols[2] = {i, i + half};
+      for (int u = 0; u < 2; ++u) {
+        const uint16_t hi = f32_to_bf16(vals[u]);
+        const uint16_t lo = f32_to_bf16(vals[u] - bf16_to_f32(hi));
+        *reinterpret_cast<uint16_t*>(tile + sw128_offset(j, cols[u], 2048)) = hi;
+        *reinterpret_cast<uint16_t*>(tile + sw128_offset(8 + j, cols[u], 2048)) = lo;
+      }
     }
   }
   const float* vv = row + qd + kvd;
@@ -166,10 +181,10 @@ __global__ void k_rope_append(float* qkv, const QueryRow* rows, int layer, int n
 
 void launch_rope_append(float* qkv, const QueryRow* rows, int n, int layer, int n_heads,
                         int n_kv_heads, int head_dim, const float* cosv, const float* sinv,
-                        uint16_t* arena, cudaStream_t s) {
+                        uint16_t* arena, uint8_t* qtile, cudaStream_t s) {
   if (n <= 0) return;
-  launch_pdl(k_rope_append, dim3(n), dim3(256), 0, s, qkv, rows, layer, n_heads, n_kv_heads, head_dim, cosv, sinv,
-                                  arena);
+  launch_pdl(k_rope_append, dim3(n), dim3(256), 0, s, qkv, rows, layer, n_heads, n_kv_heads,
+             head_dim, cosv, sinv, arena, qtile);
 }
 
 // ---- V of one layer between the plain [kv head][position][head_dim] layout and a slab ------

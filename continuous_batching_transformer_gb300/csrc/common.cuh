@@ -46,6 +46,14 @@ CBT_HD long long v_index(const QueryRow& r, int layer, int head, int key, int d,
          ((long long)(key >> 6) * head_dim + d) * 64 + (key & 63);
 }
 
+// Byte offset of bf16 element (row, col) in a K-major operand tile of 128-byte rows stored in
+// the 128-byte swizzle (16-byte chunk index XOR row % 8), the layout TMA writes and tcgen05
+// descriptors read; 64-column groups of the tile are `group_stride` bytes apart.
+CBT_HD uint32_t sw128_offset(int row, int col, int group_stride) {
+  const int g = col >> 6, c = col & 63;
+  return (uint32_t)(g * group_stride + row * 128 + (((c >> 3) ^ (row & 7)) << 4) + (c & 7) * 2);
+}
+
 // One unit of decode attention: kv head g of row b over 128-key sub-chunks [s0, s1)
 struct AttnItem {
   int b, g, s0, s1;

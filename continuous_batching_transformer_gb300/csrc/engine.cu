@@ -99,6 +99,7 @@ struct cbt_engine {
   float2* att_ml = nullptr;
   size_t att_items_cap = 0;
   int item_total = 0;
+  uint8_t* qtile = nullptr;  // [max_batch][Hkv] Q operand images of the decode attention
   // staging buffer for host-side import/export of V
   uint16_t* stage = nullptr;
   size_t stage_elems = 0;
@@ -143,7 +144,8 @@ static void free_scratch(cbt_engine* e) {
   void* ptrs[] = {e->x,       e->h,        e->qkv,  e->o,     e->act,    e->part,
                   e->xg,      e->logits,   e->cosv, e->sinv,  e->next_tok, e->last_idx,
                   e->rows,    e->err,      e->act_h, e->act_o, e->act_u,  e->tc_part,
-                  e->tc_cnt,  e->items,    e->item_meta, e->att_o, e->att_ml, e->stage};
+                  e->tc_cnt,  e->items,    e->item_meta, e->att_o, e->att_ml, e->stage,
+                  e->qtile};
   for (void* q : ptrs)
     if (q) cudaFree(q);
 }
@@ -273,6 +275,9 @@ extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_w
       e->hitem_base.resize(p->max_batch);
       e->hitem_count.resize(p->max_batch);
       chk(dmalloc(&e->item_meta, (size_t)2 * p->max_batch + 1, &tot));
+      const size_t qbytes = (size_t)p->max_batch * c.n_kv_heads * 16 * c.head_dim * 2;
+      chk(dmalloc(&e->qtile, qbytes, &tot));
+      if (rc == cudaSuccess) rc = cudaMemsetAsync(e->qtile, 0, qbytes, e->stream);
     }
     e->use_tc = maps_ok && c.d_ff % 64 == 0;
   }
@@ -584,10 +589,10 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
       projection(e, e->h, n, d, L.wqkv, qd + 2 * kvd, EPI_STORE, e->qkv);
     t = tbegin(e, CBT_KCLASS_ATTN);
     launch_rope_append(e->qkv, e->rows, n, l, c.n_heads, c.n_kv_heads, c.head_dim, e->cosv,
-                       e->sinv, arena, s);
+                       e->sinv, arena, (tcp && !gather) ? e->qtile : nullptr, s);
     if (tcp && !gather) {  // decode: split-K flash decoding on the tensor cores
       AttnDecodeArgs a{};
-      a.qkv = e->qkv;
+      a.qtile = e->qtile;
       a.rows = e->rows;
       a.items = e->items;
       a.n_items = e->item_meta + 2 * e->p.max_batch;

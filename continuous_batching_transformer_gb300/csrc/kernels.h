@@ -68,7 +68,7 @@ bool launch_tc_linear(const CUtensorMap& tw, const CUtensorMap& tx, TcParams p, 
 
 // ---- tensor-core decode attention (attn_tc.cu) ------------------------------------------------
 struct AttnDecodeArgs {
-  const float* qkv;          // [B][q|k|v] fp32, q and k already rotated
+  const uint8_t* qtile;      // [B][Hkv] Q operand images written by the RoPE kernel
   const QueryRow* rows;      // [B]
   const AttnItem* items;     // work items, grouped by row: row b's items start at item_base[b],
   const int* n_items;        //   kv head g's splits at item_base[b] + g * item_count[b]
@@ -105,10 +105,11 @@ void launch_rmsnorm(const float* x, const uint16_t* gain, int n, int d, float ep
 // per-token RoPE cos/sin for the positions in rows (fp32 [n][hd/2] each), in double
 void launch_rope_table(const QueryRow* rows, int n, int head_dim, double theta, float* cosv,
                        float* sinv, cudaStream_t s);
-// RoPE q and k in place at each token's position; append k, v (bf16) to its slab
+// RoPE q and k in place at each token's position; append k, v (bf16) to its slab; with
+// qtile, also write each row's Q operand images for the decode attention ([n][Hkv][16][hd])
 void launch_rope_append(float* qkv, const QueryRow* rows, int n, int layer, int n_heads,
                         int n_kv_heads, int head_dim, const float* cosv, const float* sinv,
-                        uint16_t* arena, cudaStream_t s);
+                        uint16_t* arena, uint8_t* qtile, cudaStream_t s);
 // softmax attention of each token over [0, pos] of its own slab
 void launch_attention_naive(const float* qkv, const QueryRow* rows, int n, int layer, int n_heads,
                             int n_kv_heads, int head_dim, int max_keys, const uint16_t* arena,

@@ -72,6 +72,15 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uin
       : "memory");
 }
 
+// 1-D bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) into shared memory
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // ---- tcgen05 --------------------------------------------------------------------------------
 // whole warp: allocate ncols (power of two >= 32) TMEM columns, address written to smem
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
