@@ -7,26 +7,50 @@
 #include "kernels.h"
 
 // ---- embedding: x[i] = E[token[i]] (fp32); out-of-range ids set the error word ------------
+// With ss, also what the first RMSNorm needs when it is folded into the QKV projection: the
+// row's sums of squares over each 128-element tile, ss[tile * ss_ld + i], and the operand
+// x * gain as bf16 hi (row i of act) and lo (row lo_rows + i) parts.
 __global__ void k_embed(const int32_t* tokens, int d, int vocab, const uint16_t* table, float* x,
-                        int* err) {
+                        int* err, float* ss, int ss_ld, const uint16_t* gain, uint16_t* act,
+                        int lo_rows) {
   pdl_wait();
   pdl_launch();
   int i = blockIdx.x;
   int t = tokens[i];
   float* xr = x + (size_t)i * d;
-  if (t < 0 || t >= vocab) {
-    if (threadIdx.x == 0) set_device_error(err, CBT_DEV_TOKEN_RANGE, i);
-    for (int j = threadIdx.x; j < d; j += blockDim.x) xr[j] = 0.f;
-    return;
+  const bool bad = t < 0 || t >= vocab;
+  if (bad && threadIdx.x == 0) set_device_error(err, CBT_DEV_TOKEN_RANGE, i);
+  const uint16_t* er = table + (size_t)(bad ? 0 : t) * d;
+  for (int j = threadIdx.x; j < d; j += blockDim.x) {
+    const float v = bad ? 0.f : bf16_to_f32(er[j]);
+    xr[j] = v;
+    if (act) {
+      const float a = v * bf16_to_f32(gain[j]);
+      const uint16_t hi = f32_to_bf16(a);
+      act[(size_t)i * d + j] = hi;
+      if (lo_rows > 0) act[(size_t)(lo_rows + i) * d + j] = f32_to_bf16(a - bf16_to_f32(hi));
+    }
   }
-  const uint16_t* er = table + (size_t)t * d;
-  for (int j = threadIdx.x; j < d; j += blockDim.x) xr[j] = bf16_to_f32(er[j]);
+  if (ss) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    for (int tile = warp; tile * 128 < d; tile += nw) {
+      float s = 0.f;
+      for (int j = tile * 128 + lane; j < d && j < tile * 128 + 128; j += 32) {
+        const float v = bad ? 0.f : bf16_to_f32(er[j]);
+        s = fmaf(v, v, s);
+      }
+      s = warp_sum(s);
+      if (lane == 0) ss[(size_t)tile * ss_ld + i] = s;
+    }
+  }
 }
 
 void launch_embed(const int32_t* tokens, int n, const uint16_t* table, int d, int vocab, float* x,
-                  int* err, cudaStream_t s) {
+                  int* err, float* ss, int ss_ld, const uint16_t* gain, uint16_t* act,
+                  int lo_rows, cudaStream_t s) {
   if (n <= 0) return;
-  launch_pdl(k_embed, dim3(n), dim3(256), 0, s, tokens, d, vocab, table, x, err);
+  launch_pdl(k_embed, dim3(n), dim3(256), 0, s, tokens, d, vocab, table, x, err, ss, ss_ld, gain,
+             act, lo_rows);
 }
 
 // ---- RMSNorm: h = x / sqrt(mean(x^2) + eps) * g -----------------------------------------

@@ -100,6 +100,8 @@ struct cbt_engine {
   size_t att_items_cap = 0;
   int item_total = 0;
   uint8_t* qtile = nullptr;  // [max_batch][Hkv] Q operand images of the decode attention
+  float* ss = nullptr;       // [d/128][ss_ld] per-tile sums of squares of the residual rows
+  int ss_ld = 0;
   // staging buffer for host-side import/export of V
   uint16_t* stage = nullptr;
   size_t stage_elems = 0;
@@ -145,7 +147,7 @@ static void free_scratch(cbt_engine* e) {
                   e->xg,      e->logits,   e->cosv, e->sinv,  e->next_tok, e->last_idx,
                   e->rows,    e->err,      e->act_h, e->act_o, e->act_u,  e->tc_part,
                   e->tc_cnt,  e->items,    e->item_meta, e->att_o, e->att_ml, e->stage,
-                  e->qtile};
+                  e->qtile,   e->ss};
   for (void* q : ptrs)
     if (q) cudaFree(q);
 }
@@ -278,6 +280,8 @@ extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_w
       const size_t qbytes = (size_t)p->max_batch * c.n_kv_heads * 16 * c.head_dim * 2;
       chk(dmalloc(&e->qtile, qbytes, &tot));
       if (rc == cudaSuccess) rc = cudaMemsetAsync(e->qtile, 0, qbytes, e->stream);
+      e->ss_ld = std::max(32, p->max_batch);
+      chk(dmalloc(&e->ss, (size_t)((c.d_model + 127) / 128) * e->ss_ld, &tot));
     }
     e->use_tc = maps_ok && c.d_ff % 64 == 0;
   }
@@ -524,16 +528,30 @@ static const CUtensorMap* xmap(cbt_engine* e, const uint16_t* buf, int K, int BN
   return &(e->xmaps[key] = m);
 }
 
-// y = x W^T over n rows on the tensor cores, operand x in the bf16 buffer xbuf [rows][K];
-// timed as class PROJ with the same algorithmic bytes as the CUDA-core path
+// y = x W^T over n rows on the tensor cores, operand x in the bf16 buffer xbuf [rows][K].
+// norm_in: the operand is x * g and each column is scaled by its RMSNorm factor, from the
+// sums of squares in e->ss.  next_gain (EPI_ADD): also write the updated rows' sums of squares
+// to e->ss and x * next_gain into e->act_h, the operand of the projection that follows.
 static bool tc_projection(cbt_engine* e, const CUtensorMap& wmap, const uint16_t* xbuf, int n,
                           int K, int M, Epilogue epi, float* out, int ldo, uint16_t* act_out,
-                          int act_ld) {
+                          int act_ld, bool norm_in = false, const uint16_t* next_gain = nullptr) {
   const bool split = n <= 32;
   const int BN = split ? tc_split_bn(n) : tc_plain_bn(n);
   const CUtensorMap* xm = xmap(e, xbuf, K, BN);
   if (!xm) return false;
   TcParams p{};
+  p.ss_ld = e->ss_ld;
+  if (norm_in) {
+    p.ss_in = e->ss;
+    p.ss_tiles = (e->cfg.d_model + 127) / 128;
+    p.eps = e->cfg.rms_eps;
+  }
+  if (next_gain) {
+    p.ss_out = e->ss;
+    p.next_gain = next_gain;
+    p.next_act = e->act_h;
+    p.next_lo = split ? BN / 2 : 0;
+  }
   p.M = M;
   p.K = K;
   p.F = epi == EPI_SWIGLU ? M / 2 : 0;
@@ -568,23 +586,31 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
                             + 4.0 * n * (qd + 2 * kvd)              // q, k, v in
                             + 2.0 * 2.0 * n * kvd + 4.0 * n * qd;   // K/V appended, o out
   const bool tcp = e->use_tc;
+  // decode on the tensor cores folds every RMSNorm into the projection that consumes it:
+  // the residual-add epilogues and the embedding leave per-tile sums of squares in e->ss
+  const bool fused = tcp && !gather && n <= 32;
   const int lo = tc_lo_rows(n), lo_out = tc_lo_rows(n_out);
   bool ok = true;
   int t = tbegin(e, CBT_KCLASS_OTHER);
-  launch_embed(tokens, n, static_cast<const uint16_t*>(e->w.embed), d, c.vocab, e->x, e->err, s);
+  launch_embed(tokens, n, static_cast<const uint16_t*>(e->w.embed), d, c.vocab, e->x, e->err,
+               fused ? e->ss : nullptr, e->ss_ld,
+               static_cast<const uint16_t*>(e->layers[0].attn_norm), fused ? e->act_h : nullptr,
+               lo, s);
   launch_rope_table(e->rows, n, c.head_dim, c.rope_theta, e->cosv, e->sinv, s);
   tend(e, t, 2.0 * n * d + 4.0 * n * d);
   for (int l = 0; l < c.n_layers && ok; ++l) {
     const cbt_layer_weights& L = e->layers[l];
     const uint16_t* an = static_cast<const uint16_t*>(L.attn_norm);
     const uint16_t* fn = static_cast<const uint16_t*>(L.ffn_norm);
-    t = tbegin(e, CBT_KCLASS_OTHER);
-    if (tcp) launch_rmsnorm_act(e->x, an, n, d, c.rms_eps, e->act_h, lo, s);
-    else launch_rmsnorm(e->x, an, n, d, c.rms_eps, e->h, s);
-    tend(e, t, 8.0 * n * d);
+    if (!fused) {
+      t = tbegin(e, CBT_KCLASS_OTHER);
+      if (tcp) launch_rmsnorm_act(e->x, an, n, d, c.rms_eps, e->act_h, lo, s);
+      else launch_rmsnorm(e->x, an, n, d, c.rms_eps, e->h, s);
+      tend(e, t, 8.0 * n * d);
+    }
     if (tcp)
       ok &= tc_projection(e, e->wmaps[l].qkv, e->act_h, n, d, qd + 2 * kvd, EPI_STORE, e->qkv,
-                          qd + 2 * kvd, nullptr, 0);
+                          qd + 2 * kvd, nullptr, 0, fused);
     else
       projection(e, e->h, n, d, L.wqkv, qd + 2 * kvd, EPI_STORE, e->qkv);
     t = tbegin(e, CBT_KCLASS_ATTN);
@@ -616,17 +642,25 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
     }
     tend(e, t, attn_bytes);
     if (tcp)
-      ok &= tc_projection(e, e->wmaps[l].o, e->act_o, n, qd, d, EPI_ADD, e->x, d, nullptr, 0);
+      ok &= tc_projection(e, e->wmaps[l].o, e->act_o, n, qd, d, EPI_ADD, e->x, d, nullptr, 0,
+                          false, fused ? fn : nullptr);
     else
       projection(e, e->o, n, qd, L.wo, d, EPI_ADD, e->x);
-    t = tbegin(e, CBT_KCLASS_OTHER);
-    if (tcp) launch_rmsnorm_act(e->x, fn, n, d, c.rms_eps, e->act_h, lo, s);
-    else launch_rmsnorm(e->x, fn, n, d, c.rms_eps, e->h, s);
-    tend(e, t, 8.0 * n * d);
+    if (!fused) {
+      t = tbegin(e, CBT_KCLASS_OTHER);
+      if (tcp) launch_rmsnorm_act(e->x, fn, n, d, c.rms_eps, e->act_h, lo, s);
+      else launch_rmsnorm(e->x, fn, n, d, c.rms_eps, e->h, s);
+      tend(e, t, 8.0 * n * d);
+    }
     if (tcp) {
       ok &= tc_projection(e, e->wmaps[l].gu, e->act_h, n, d, 2 * F, EPI_SWIGLU, nullptr, 0,
-                          e->act_u, F);
-      ok &= tc_projection(e, e->wmaps[l].d, e->act_u, n, F, d, EPI_ADD, e->x, d, nullptr, 0);
+                          e->act_u, F, fused);
+      // the down projection's epilogue prepares the next layer's (or the final) RMSNorm
+      const uint16_t* next_g = l + 1 < c.n_layers
+                                   ? static_cast<const uint16_t*>(e->layers[l + 1].attn_norm)
+                                   : static_cast<const uint16_t*>(e->w.final_norm);
+      ok &= tc_projection(e, e->wmaps[l].d, e->act_u, n, F, d, EPI_ADD, e->x, d, nullptr, 0,
+                          false, fused ? next_g : nullptr);
     } else {
       projection(e, e->h, n, d, L.wgu, 2 * F, EPI_SWIGLU, e->act);
       projection(e, e->act, n, F, L.wd, d, EPI_ADD, e->x);
@@ -635,18 +669,21 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
   if (!ok) return cudaErrorNotSupported;
   const float* xf = e->x;
   float* hf = e->xg + (size_t)e->p.max_batch * d;
-  t = tbegin(e, CBT_KCLASS_OTHER);
-  if (gather) {
-    launch_gather_rows(e->x, e->last_idx, n_out, d, e->xg, s);
-    xf = e->xg;
-  }
   const uint16_t* gn = static_cast<const uint16_t*>(e->w.final_norm);
-  if (tcp) launch_rmsnorm_act(xf, gn, n_out, d, c.rms_eps, e->act_h, lo_out, s);
-  else launch_rmsnorm(xf, gn, n_out, d, c.rms_eps, hf, s);
-  tend(e, t, 8.0 * n_out * d);
+  if (!fused) {
+    t = tbegin(e, CBT_KCLASS_OTHER);
+    if (gather) {
+      launch_gather_rows(e->x, e->last_idx, n_out, d, e->xg, s);
+      xf = e->xg;
+    }
+    if (tcp) launch_rmsnorm_act(xf, gn, n_out, d, c.rms_eps, e->act_h, lo_out, s);
+    else launch_rmsnorm(xf, gn, n_out, d, c.rms_eps, hf, s);
+    tend(e, t, 8.0 * n_out * d);
+  }
   float* lg = logits ? logits : e->logits;
   if (tcp) {
-    if (!tc_projection(e, e->lm_map, e->act_h, n_out, d, c.vocab, EPI_STORE, lg, c.vocab, nullptr, 0))
+    if (!tc_projection(e, e->lm_map, e->act_h, n_out, d, c.vocab, EPI_STORE, lg, c.vocab, nullptr,
+                       0, fused))
       return cudaErrorNotSupported;
   } else {
     projection(e, hf, n_out, d, e->w.lm_head, c.vocab, EPI_STORE, lg);

@@ -14,6 +14,11 @@
 // over the grid, so every CTA streams the same number of weight bytes; a row block cut
 // between CTAs is finished by whichever CTA completes it last, summing the partial sums in
 // a fixed order, so results do not depend on timing.
+//
+// RMSNorm without a kernel of its own (decode): RMSNorm(x) W^T = rsqrt(mean(x^2) + eps) *
+// ((x * g) W^T), so the residual-add epilogue that produces x also writes x * g (the next
+// projection's operand, hi/lo) and x's sums of squares over its 128-row tile; the consuming
+// projection scales each accumulated column by the row's rsqrt(mean(x^2) + eps).
 // Prefill (!SPLIT): plain bf16 activations, N tiles of up to 256 tokens, whole tiles per CTA.
 #include <cudaTypedefs.h>
 
@@ -24,7 +29,7 @@
 
 namespace {
 
-constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA (+TMEM alloc), warps 2..5 epilogue
+constexpr int kThreads = 192;       // warp 0 TMA, warp 1 MMA (+TMEM alloc), warps 2..5 epilogue
 constexpr int kABytes = 128 * 128;  // 128 rows x 64 bf16
 
 struct Sched {
@@ -79,20 +84,45 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   return false;
 }
 
-// Final epilogue of `cnt` columns (tokens tok0 .. tok0+cnt-1) of tile row r of row block rb.
-__device__ __forceinline__ void finish(const TcParams& p, int rb, int r, const float* vals,
-                                       int tok0, int cnt, float* swx) {
+// Final epilogue of `cnt` (<= 32) columns (tokens tok0 .. tok0+cnt-1) of tile row r of row
+// block rb.  All 128 epilogue threads call it together.  rinv (when p.ss_in) holds each
+// column's RMSNorm factor.
+__device__ __forceinline__ void finish(const TcParams& p, int rb, int r, float* vals, int tok0,
+                                       int cnt, float* swx, const float* rinv) {
+  if (p.ss_in)
+    for (int j = 0; j < cnt; ++j) vals[j] *= rinv[j];
   if (p.epi != EPI_SWIGLU) {
     const int m = rb * 128 + r;
-    if (m < p.M) {
-      for (int j = 0; j < cnt; ++j) {
-        const int t = tok0 + j;
-        if (t < p.n_act) {
-          float* o = p.out + (size_t)t * p.ldo + m;
-          if (p.epi == EPI_ADD) *o += vals[j];
-          else *o = vals[j];
+    float sq[32];
+    for (int j = 0; j < cnt; ++j) {
+      const int t = tok0 + j;
+      sq[j] = 0.f;
+      if (m < p.M && t < p.n_act) {
+        float* o = p.out + (size_t)t * p.ldo + m;
+        float v = vals[j];
+        if (p.epi == EPI_ADD) v += *o;
+        *o = v;
+        sq[j] = v * v;
+        if (p.next_act) {  // the next projection's operand x * g, as hi/lo parts
+          const float a = v * bf16_to_f32(p.next_gain[m]);
+          const uint16_t hi = f32_to_bf16(a);
+          p.next_act[(size_t)t * p.ldo + m] = hi;
+          if (p.next_lo)
+            p.next_act[(size_t)(p.next_lo + t) * p.ldo + m] = f32_to_bf16(a - bf16_to_f32(hi));
         }
       }
+    }
+    if (p.ss_out) {
+      // sums of squares of the updated rows over this tile's 128 rows, for the next RMSNorm
+      const int w = r >> 5, lane = r & 31;
+      for (int j = 0; j < cnt; ++j) {
+        const float s = warp_sum(sq[j]);
+        if (lane == 0) swx[w * 32 + j] = s;
+      }
+      tc::named_bar_sync(1, 128);
+      if (r < cnt && tok0 + r < p.n_act)
+        p.ss_out[(size_t)rb * p.ss_ld + tok0 + r] = swx[r] + swx[32 + r] + swx[64 + r] + swx[96 + r];
+      tc::named_bar_sync(1, 128);
     }
     return;
   }
@@ -138,6 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* sflag = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [0] last, [1] abort
   float* swx = reinterpret_cast<float*>(smem + STAGES * (kABytes + kXBytes) + 512);
+  float* rinv = swx + 64 * 33;  // [32] RMSNorm factor of each decode column
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -269,6 +300,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_wait();  // outputs and the stream-K scratch are shared with the previous kernel
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;
+    if (SPLIT && p.ss_in) {  // RMSNorm factor of each decode row, from the per-tile sums
+      if (r < p.n_act) {
+        float s = 0.f;
+        for (int t = 0; t < p.ss_tiles; ++t) s += p.ss_in[(size_t)t * p.ss_ld + r];
+        rinv[r] = rsqrtf(s / (float)p.K + p.eps);
+      }
+      tc::named_bar_sync(1, 128);
+    }
     int acc = 0;
     uint32_t acc_phase = 0;
     while (sch.next(p, tile, kb, ke)) {
@@ -292,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int n = 0; n < H; ++n) vals[n] = __uint_as_float(raw[n]) + __uint_as_float(raw[n + H]);
         if (kb == 0 && ke == p.KS) {
-          finish(p, rb, r, vals, 0, H, swx);
+          finish(p, rb, r, vals, 0, H, swx, rinv);
         } else {
           const int first = cta_of_unit(p.U, gridDim.x, (long long)tile * p.KS);
           const int slot = blockIdx.x - first;
@@ -319,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int n = 0; n < H; ++n)
                 if (n < p.n_act) sum[n] += __ldcg(ps + n * 128 + r);
             }
-            finish(p, rb, r, sum, 0, H, swx);
+            finish(p, rb, r, sum, 0, H, swx, rinv);
             if (threadIdx.x == 64) p.cnt[tile] = 0;
           }
         }
@@ -333,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float vals[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) vals[j] = __uint_as_float(raw[j]);
-          finish(p, rb, r, vals, nt * BN + c0, 32, swx);
+          finish(p, rb, r, vals, nt * BN + c0, 32, swx, rinv);
         }
         tc::tc_fence_before();
         __syncwarp();
@@ -356,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int BN, int STAGES, bool SPLIT>
 cudaError_t launch_inst(const CUtensorMap& tw, const CUtensorMap& tx, const TcParams& p, int grid,
                         cudaStream_t s) {
-  constexpr size_t smem = 1024 + STAGES * (kABytes + BN * 128) + 512 + 64 * 33 * 4;
+  constexpr size_t smem = 1024 + STAGES * (kABytes + BN * 128) + 512 + 64 * 33 * 4 + 256;
   static_assert(smem <= 227 * 1024, "shared memory budget");
   auto kern = k_tc_linear<BN, STAGES, SPLIT>;
   cudaError_t rc = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -401,6 +440,7 @@ bool launch_tc_linear(const CUtensorMap& tw, const CUtensorMap& tx, TcParams p, 
                       int num_sms, size_t part_floats, cudaStream_t s) {
   if (p.K % 64 || p.K <= 0 || p.n_act <= 0) return false;
   if (p.epi == EPI_SWIGLU && (p.F % 64 || p.M != 2 * p.F)) return false;
+  if (!split && p.ss_in) return false;  // the per-column RMSNorm factors exist for decode rows only
   p.RB = p.epi == EPI_SWIGLU ? p.F / 64 : (p.M + 127) / 128;
   p.KS = p.K / 64;
   if (split) {

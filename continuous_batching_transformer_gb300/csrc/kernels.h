@@ -55,6 +55,18 @@ struct TcParams {
   float* part;       // stream-K partial sums
   int* cnt;          // per-tile completion counters, zero between launches
   int* err;          // device error word
+  // RMSNorm folded into the projections (decode rows only).  Consumer side: the operand is
+  // x * g, and column b of the result is scaled by rsqrt(sum_t ss_in[t][b] / K + eps).
+  const float* ss_in;     // [ss_tiles][ss_ld] sums of squares of x over 128-element tiles
+  int ss_tiles, ss_ld;
+  float eps;
+  // Producer side (EPI_ADD): also write the updated rows' sums of squares per 128-row tile
+  // ([RB][ss_ld]) and the next projection's operand x * next_gain as bf16 (hi at row t of
+  // next_act, lo at row next_lo + t when next_lo > 0; row stride ldo)
+  float* ss_out;
+  const uint16_t* next_gain;
+  uint16_t* next_act;
+  int next_lo;
 };
 
 
@@ -98,7 +110,8 @@ void launch_f32_to_act(const float* src, int n, int K, uint16_t* act, int lo_row
 
 // embed + token range check
 void launch_embed(const int32_t* tokens, int n, const uint16_t* table, int d, int vocab, float* x,
-                  int* err, cudaStream_t s);
+                  int* err, float* ss, int ss_ld, const uint16_t* gain, uint16_t* act,
+                  int lo_rows, cudaStream_t s);
 // RMSNorm rows of x into h
 void launch_rmsnorm(const float* x, const uint16_t* gain, int n, int d, float eps, float* h,
                     cudaStream_t s);
