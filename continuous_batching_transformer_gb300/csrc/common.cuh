@@ -88,4 +88,5 @@ enum Epilogue : int {
   EPI_STORE = 0,   // out[n][m] = y
   EPI_ADD = 1,     // out[n][m] += y (residual)
   EPI_SWIGLU = 2,  // W = [gate; up] (2F rows): out[n][j] = silu(y_gate[j]) * y_up[j], j < F
+  EPI_QKV = 3,     // W = [Wq; Wk; Wv]: RoPE, KV append and the attention's Q operand (decode)
 };

@@ -534,7 +534,8 @@ static const CUtensorMap* xmap(cbt_engine* e, const uint16_t* buf, int K, int BN
 // to e->ss and x * next_gain into e->act_h, the operand of the projection that follows.
 static bool tc_projection(cbt_engine* e, const CUtensorMap& wmap, const uint16_t* xbuf, int n,
                           int K, int M, Epilogue epi, float* out, int ldo, uint16_t* act_out,
-                          int act_ld, bool norm_in = false, const uint16_t* next_gain = nullptr) {
+                          int act_ld, bool norm_in = false, const uint16_t* next_gain = nullptr,
+                          int layer = 0) {
   const bool split = n <= 32;
   const int BN = split ? tc_split_bn(n) : tc_plain_bn(n);
   const CUtensorMap* xm = xmap(e, xbuf, K, BN);
@@ -545,6 +546,17 @@ static bool tc_projection(cbt_engine* e, const CUtensorMap& wmap, const uint16_t
     p.ss_in = e->ss;
     p.ss_tiles = (e->cfg.d_model + 127) / 128;
     p.eps = e->cfg.rms_eps;
+  }
+  if (epi == EPI_QKV) {  // RoPE + KV append + the attention's Q operand, in the epilogue
+    p.rows = e->rows;
+    p.layer = layer;
+    p.n_heads = e->cfg.n_heads;
+    p.n_kv_heads = e->cfg.n_kv_heads;
+    p.head_dim = e->cfg.head_dim;
+    p.cosv = e->cosv;
+    p.sinv = e->sinv;
+    p.arena = static_cast<uint16_t*>(e->p.kv_arena);
+    p.qtile = e->qtile;
   }
   if (next_gain) {
     p.ss_out = e->ss;
@@ -608,14 +620,18 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
       else launch_rmsnorm(e->x, an, n, d, c.rms_eps, e->h, s);
       tend(e, t, 8.0 * n * d);
     }
+    // decode on the tensor cores rotates q and k, appends K/V and lays out the attention's Q
+    // operand in the QKV projection's epilogue; otherwise a separate kernel does it
     if (tcp)
-      ok &= tc_projection(e, e->wmaps[l].qkv, e->act_h, n, d, qd + 2 * kvd, EPI_STORE, e->qkv,
-                          qd + 2 * kvd, nullptr, 0, fused);
+      ok &= tc_projection(e, e->wmaps[l].qkv, e->act_h, n, d, qd + 2 * kvd,
+                          fused ? EPI_QKV : EPI_STORE, e->qkv, qd + 2 * kvd, nullptr, 0, fused,
+                          nullptr, l);
     else
       projection(e, e->h, n, d, L.wqkv, qd + 2 * kvd, EPI_STORE, e->qkv);
     t = tbegin(e, CBT_KCLASS_ATTN);
-    launch_rope_append(e->qkv, e->rows, n, l, c.n_heads, c.n_kv_heads, c.head_dim, e->cosv,
-                       e->sinv, arena, (tcp && !gather) ? e->qtile : nullptr, s);
+    if (!fused)
+      launch_rope_append(e->qkv, e->rows, n, l, c.n_heads, c.n_kv_heads, c.head_dim, e->cosv,
+                         e->sinv, arena, (tcp && !gather) ? e->qtile : nullptr, s);
     if (tcp && !gather) {  // decode: split-K flash decoding on the tensor cores
       AttnDecodeArgs a{};
       a.qtile = e->qtile;

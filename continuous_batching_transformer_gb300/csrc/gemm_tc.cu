@@ -91,6 +91,43 @@ __device__ __forceinline__ void finish(const TcParams& p, int rb, int r, float* 
                                        int cnt, float* swx, const float* rinv) {
   if (p.ss_in)
     for (int j = 0; j < cnt; ++j) vals[j] *= rinv[j];
+  if (p.epi == EPI_QKV) {
+    // Row r of the tile is dim i of head `head` of q|k|v (heads are head_dim-aligned in the
+    // tile); its RoPE partner is dim i ^ half of the same head, held by tile row r ^ half.
+    const int hd = p.head_dim, half = hd >> 1;
+    const int row = rb * 128 + r, head = row / hd, i = row % hd;
+    tc::named_bar_sync(1, 128);
+    for (int j = 0; j < cnt; ++j) swx[r * 33 + j] = vals[j];
+    tc::named_bar_sync(1, 128);
+    const int pr = r ^ half;
+    const int G = p.n_heads / p.n_kv_heads;
+    for (int j = 0; j < cnt && j < p.n_act && row < p.M; ++j) {
+      const QueryRow qr = p.rows[j];
+      float v = vals[j];
+      if (head < p.n_heads + p.n_kv_heads) {  // q and k turn by pos * theta^(-2(i%half)/hd)
+        const float c = p.cosv[j * half + (i & (half - 1))];
+        const float s = p.sinv[j * half + (i & (half - 1))];
+        const float w = swx[pr * 33 + j];
+        v = i < half ? v * c - w * s : w * s + v * c;
+      }
+      if (head < p.n_heads) {
+        // Q operand image of row j, kv head head / G: hi part in tile row head % G, lo part
+        // in row 8 + head % G, scaled by 1/sqrt(head_dim)
+        uint8_t* tile = p.qtile + ((size_t)j * p.n_kv_heads + head / G) * (16 * hd * 2);
+        const float qv = v * rsqrtf((float)hd);
+        const uint16_t hi = f32_to_bf16(qv);
+        *reinterpret_cast<uint16_t*>(tile + sw128_offset(head % G, i, 2048)) = hi;
+        *reinterpret_cast<uint16_t*>(tile + sw128_offset(8 + head % G, i, 2048)) =
+            f32_to_bf16(qv - bf16_to_f32(hi));
+      } else if (head < p.n_heads + p.n_kv_heads) {
+        p.arena[k_index(qr, p.layer, head - p.n_heads, qr.pos, i, p.n_kv_heads, hd)] = f32_to_bf16(v);
+      } else {
+        p.arena[v_index(qr, p.layer, head - p.n_heads - p.n_kv_heads, qr.pos, i, p.n_kv_heads, hd)] =
+            f32_to_bf16(v);
+      }
+    }
+    return;
+  }
   if (p.epi != EPI_SWIGLU) {
     const int m = rb * 128 + r;
     float sq[32];
@@ -168,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* sflag = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [0] last, [1] abort
   float* swx = reinterpret_cast<float*>(smem + STAGES * (kABytes + kXBytes) + 512);
-  float* rinv = swx + 64 * 33;  // [32] RMSNorm factor of each decode column
+  float* rinv = swx + 128 * 33;  // [32] RMSNorm factor of each decode column
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -395,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int BN, int STAGES, bool SPLIT>
 cudaError_t launch_inst(const CUtensorMap& tw, const CUtensorMap& tx, const TcParams& p, int grid,
                         cudaStream_t s) {
-  constexpr size_t smem = 1024 + STAGES * (kABytes + BN * 128) + 512 + 64 * 33 * 4 + 256;
+  constexpr size_t smem = 1024 + STAGES * (kABytes + BN * 128) + 512 + 128 * 33 * 4 + 256;
   static_assert(smem <= 227 * 1024, "shared memory budget");
   auto kern = k_tc_linear<BN, STAGES, SPLIT>;
   cudaError_t rc = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

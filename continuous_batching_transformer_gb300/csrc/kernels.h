@@ -67,6 +67,14 @@ struct TcParams {
   const uint16_t* next_gain;
   uint16_t* next_act;
   int next_lo;
+  // EPI_QKV (decode rows): RoPE of q and k at each row's own position, the new K/V appended
+  // to the row's slab, q written as the decode attention's operand image (qtile)
+  const QueryRow* rows;
+  int layer, n_heads, n_kv_heads, head_dim;
+  const float* cosv;  // [n_act][head_dim / 2]
+  const float* sinv;
+  uint16_t* arena;
+  uint8_t* qtile;
 };
 
 
