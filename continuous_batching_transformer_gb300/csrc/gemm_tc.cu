@@ -31,6 +31,9 @@ namespace {
 
 constexpr int kThreads = 192;       // warp 0 TMA, warp 1 MMA (+TMEM alloc), warps 2..5 epilogue
 constexpr int kABytes = 128 * 128;  // 128 rows x 64 bf16
+// Decode stages: 8 x (16 KB of weights + the operand tile) keeps 128 KB of weights in flight
+// per SM (5 stages, which would let a second CTA share the SM, measured slower).
+constexpr int kSplitStages = 8;
 
 struct Sched {
   long long u, u1;
@@ -502,9 +505,9 @@ bool launch_tc_linear(const CUtensorMap& tw, const CUtensorMap& tx, TcParams p, 
     }
     if ((size_t)p.RB * p.slots * (BN / 2) * 128 > part_floats) return false;
     cudaError_t rc;
-    if (BN == 16) rc = launch_inst<16, 8, true>(tw, tx, p, G, s);
-    else if (BN == 32) rc = launch_inst<32, 8, true>(tw, tx, p, G, s);
-    else if (BN == 64) rc = launch_inst<64, 8, true>(tw, tx, p, G, s);
+    if (BN == 16) rc = launch_inst<16, kSplitStages, true>(tw, tx, p, G, s);
+    else if (BN == 32) rc = launch_inst<32, kSplitStages, true>(tw, tx, p, G, s);
+    else if (BN == 64) rc = launch_inst<64, kSplitStages, true>(tw, tx, p, G, s);
     else return false;
     return rc == cudaSuccess;
   }
