@@ -87,31 +87,56 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   return false;
 }
 
-// Final epilogue of `cnt` (<= 32) columns (tokens tok0 .. tok0+cnt-1) of tile row r of row
+// Residual values out[tok0 + j][m] of tile row r for an EPI_ADD epilogue, all loads issued
+// before any is used (the epilogue's latency is a chain of global round trips otherwise)
+template <int CNT>
+__device__ __forceinline__ void load_residual(const TcParams& p, int rb, int r, int tok0,
+                                              float* res) {
+  const int m = rb * 128 + r;
+#pragma unroll
+  for (int j = 0; j < CNT; ++j) {
+    const int t = tok0 + j;
+    res[j] = (p.epi == EPI_ADD && m < p.M && t < p.n_act) ? __ldcg(p.out + (size_t)t * p.ldo + m)
+                                                          : 0.f;
+  }
+}
+
+// Final epilogue of CNT (<= 32) columns (tokens tok0 .. tok0+CNT-1) of tile row r of row
 // block rb.  All 128 epilogue threads call it together.  rinv (when p.ss_in) holds each
-// column's RMSNorm factor.
+// column's RMSNorm factor; res the residual values from load_residual (EPI_ADD).
+template <int CNT>
 __device__ __forceinline__ void finish(const TcParams& p, int rb, int r, float* vals, int tok0,
-                                       int cnt, float* swx, const float* rinv) {
-  if (p.ss_in)
-    for (int j = 0; j < cnt; ++j) vals[j] *= rinv[j];
+                                       float* swx, const float* rinv, const float* res) {
+  if (p.ss_in) {
+#pragma unroll
+    for (int j = 0; j < CNT; ++j) vals[j] *= rinv[j];
+  }
   if (p.epi == EPI_QKV) {
     // Row r of the tile is dim i of head `head` of q|k|v (heads are head_dim-aligned in the
     // tile); its RoPE partner is dim i ^ half of the same head, held by tile row r ^ half.
     const int hd = p.head_dim, half = hd >> 1;
     const int row = rb * 128 + r, head = row / hd, i = row % hd;
+    const bool rope = head < p.n_heads + p.n_kv_heads;
+    float cs[CNT], sn[CNT];
+#pragma unroll
+    for (int j = 0; j < CNT; ++j) {
+      const bool ok = rope && j < p.n_act;
+      cs[j] = ok ? __ldg(p.cosv + j * half + (i & (half - 1))) : 1.f;
+      sn[j] = ok ? __ldg(p.sinv + j * half + (i & (half - 1))) : 0.f;
+    }
     tc::named_bar_sync(1, 128);
-    for (int j = 0; j < cnt; ++j) swx[r * 33 + j] = vals[j];
+#pragma unroll
+    for (int j = 0; j < CNT; ++j) swx[r * (CNT + 1) + j] = vals[j];
     tc::named_bar_sync(1, 128);
     const int pr = r ^ half;
     const int G = p.n_heads / p.n_kv_heads;
-    for (int j = 0; j < cnt && j < p.n_act && row < p.M; ++j) {
-      const QueryRow qr = p.rows[j];
+#pragma unroll
+    for (int j = 0; j < CNT; ++j) {
+      if (j >= p.n_act || row >= p.M) break;
       float v = vals[j];
-      if (head < p.n_heads + p.n_kv_heads) {  // q and k turn by pos * theta^(-2(i%half)/hd)
-        const float c = p.cosv[j * half + (i & (half - 1))];
-        const float s = p.sinv[j * half + (i & (half - 1))];
-        const float w = swx[pr * 33 + j];
-        v = i < half ? v * c - w * s : w * s + v * c;
+      if (rope) {  // q and k turn by pos * theta^(-2(i%half)/hd)
+        const float w = swx[pr * (CNT + 1) + j];
+        v = i < half ? v * cs[j] - w * sn[j] : w * sn[j] + v * cs[j];
       }
       if (head < p.n_heads) {
         // Q operand image of row j, kv head head / G: hi part in tile row head % G, lo part
@@ -122,29 +147,32 @@ __device__ __forceinline__ void finish(const TcParams& p, int rb, int r, float* 
         *reinterpret_cast<uint16_t*>(tile + sw128_offset(head % G, i, 2048)) = hi;
         *reinterpret_cast<uint16_t*>(tile + sw128_offset(8 + head % G, i, 2048)) =
             f32_to_bf16(qv - bf16_to_f32(hi));
-      } else if (head < p.n_heads + p.n_kv_heads) {
-        p.arena[k_index(qr, p.layer, head - p.n_heads, qr.pos, i, p.n_kv_heads, hd)] = f32_to_bf16(v);
       } else {
-        p.arena[v_index(qr, p.layer, head - p.n_heads - p.n_kv_heads, qr.pos, i, p.n_kv_heads, hd)] =
-            f32_to_bf16(v);
+        const QueryRow qr = p.rows[j];
+        if (head < p.n_heads + p.n_kv_heads)
+          p.arena[k_index(qr, p.layer, head - p.n_heads, qr.pos, i, p.n_kv_heads, hd)] =
+              f32_to_bf16(v);
+        else
+          p.arena[v_index(qr, p.layer, head - p.n_heads - p.n_kv_heads, qr.pos, i, p.n_kv_heads,
+                          hd)] = f32_to_bf16(v);
       }
     }
     return;
   }
   if (p.epi != EPI_SWIGLU) {
     const int m = rb * 128 + r;
-    float sq[32];
-    for (int j = 0; j < cnt; ++j) {
+    const float gn = (p.next_act && m < p.M) ? bf16_to_f32(p.next_gain[m]) : 0.f;
+    float sq[CNT];
+#pragma unroll
+    for (int j = 0; j < CNT; ++j) {
       const int t = tok0 + j;
       sq[j] = 0.f;
       if (m < p.M && t < p.n_act) {
-        float* o = p.out + (size_t)t * p.ldo + m;
-        float v = vals[j];
-        if (p.epi == EPI_ADD) v += *o;
-        *o = v;
+        const float v = p.epi == EPI_ADD ? vals[j] + res[j] : vals[j];
+        p.out[(size_t)t * p.ldo + m] = v;
         sq[j] = v * v;
         if (p.next_act) {  // the next projection's operand x * g, as hi/lo parts
-          const float a = v * bf16_to_f32(p.next_gain[m]);
+          const float a = v * gn;
           const uint16_t hi = f32_to_bf16(a);
           p.next_act[(size_t)t * p.ldo + m] = hi;
           if (p.next_lo)
@@ -155,12 +183,13 @@ __device__ __forceinline__ void finish(const TcParams& p, int rb, int r, float* 
     if (p.ss_out) {
       // sums of squares of the updated rows over this tile's 128 rows, for the next RMSNorm
       const int w = r >> 5, lane = r & 31;
-      for (int j = 0; j < cnt; ++j) {
+#pragma unroll
+      for (int j = 0; j < CNT; ++j) {
         const float s = warp_sum(sq[j]);
         if (lane == 0) swx[w * 32 + j] = s;
       }
       tc::named_bar_sync(1, 128);
-      if (r < cnt && tok0 + r < p.n_act)
+      if (r < CNT && tok0 + r < p.n_act)
         p.ss_out[(size_t)rb * p.ss_ld + tok0 + r] = swx[r] + swx[32 + r] + swx[64 + r] + swx[96 + r];
       tc::named_bar_sync(1, 128);
     }
@@ -168,16 +197,19 @@ __device__ __forceinline__ void finish(const TcParams& p, int rb, int r, float* 
   }
   // SwiGLU: tile rows 0..63 are gate rows, 64..127 the up rows of the same 64 features
   tc::named_bar_sync(1, 128);
-  if (r >= 64)
-    for (int j = 0; j < cnt; ++j) swx[(r - 64) * 33 + j] = vals[j];
+  if (r >= 64) {
+#pragma unroll
+    for (int j = 0; j < CNT; ++j) swx[(r - 64) * (CNT + 1) + j] = vals[j];
+  }
   tc::named_bar_sync(1, 128);
   if (r < 64) {
     const int f = rb * 64 + r;
     if (f < p.F) {
-      for (int j = 0; j < cnt; ++j) {
+#pragma unroll
+      for (int j = 0; j < CNT; ++j) {
         const int t = tok0 + j;
         if (t < p.n_act) {
-          const float g = vals[j], u = swx[r * 33 + j];
+          const float g = vals[j], u = swx[r * (CNT + 1) + j];
           const float a = g / (1.f + expf(-g)) * u;
           const uint16_t hi = f32_to_bf16(a);
           p.act[(size_t)t * p.act_ld + f] = hi;
@@ -371,7 +403,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int n = 0; n < H; ++n) vals[n] = __uint_as_float(raw[n]) + __uint_as_float(raw[n + H]);
         if (kb == 0 && ke == p.KS) {
-          finish(p, rb, r, vals, 0, H, swx, rinv);
+          float res[H];
+          load_residual<H>(p, rb, r, 0, res);
+          finish<H>(p, rb, r, vals, 0, swx, rinv, res);
         } else {
           const int first = cta_of_unit(p.U, gridDim.x, (long long)tile * p.KS);
           const int slot = blockIdx.x - first;
@@ -389,16 +423,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (sflag[0]) {
             __threadfence();
             const int last = cta_of_unit(p.U, gridDim.x, (long long)tile * p.KS + p.KS - 1);
-            float sum[H];
+            float res[H], sum[H];
+            load_residual<H>(p, rb, r, 0, res);
 #pragma unroll
             for (int n = 0; n < H; ++n) sum[n] = 0.f;
-            for (int s = 0; s <= last - first; ++s) {
-              const float* ps = p.part + ((size_t)tile * p.slots + s) * H * 128;
+            // partial slots in order (a fixed summation order keeps results reproducible),
+            // the loads of kChunk slots in flight together
+            constexpr int kChunk = H <= 16 ? 4 : 2;
+            const int nslots = last - first + 1;
+            for (int s0 = 0; s0 < nslots; s0 += kChunk) {
+              float ld[kChunk][H];
 #pragma unroll
-              for (int n = 0; n < H; ++n)
-                if (n < p.n_act) sum[n] += __ldcg(ps + n * 128 + r);
+              for (int i = 0; i < kChunk; ++i) {
+                const float* ps = p.part + ((size_t)tile * p.slots + s0 + i) * H * 128;
+#pragma unroll
+                for (int n = 0; n < H; ++n)
+                  ld[i][n] = (s0 + i < nslots && n < p.n_act) ? __ldcg(ps + n * 128 + r) : 0.f;
+              }
+#pragma unroll
+              for (int i = 0; i < kChunk; ++i)
+                if (s0 + i < nslots) {
+#pragma unroll
+                  for (int n = 0; n < H; ++n) sum[n] += ld[i][n];
+                }
             }
-            finish(p, rb, r, sum, 0, H, swx, rinv);
+            finish<H>(p, rb, r, sum, 0, swx, rinv, res);
             if (threadIdx.x == 64) p.cnt[tile] = 0;
           }
         }
@@ -409,10 +458,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tmem_ld16(taddr + c0, raw);
           tc::tmem_ld16(taddr + c0 + 16, raw + 16);
           tc::tmem_ld_wait();
-          float vals[32];
+          float vals[32], res[32];
+          load_residual<32>(p, rb, r, nt * BN + c0, res);
 #pragma unroll
           for (int j = 0; j < 32; ++j) vals[j] = __uint_as_float(raw[j]);
-          finish(p, rb, r, vals, nt * BN + c0, 32, swx, rinv);
+          finish<32>(p, rb, r, vals, nt * BN + c0, swx, rinv, res);
         }
         tc::tc_fence_before();
         __syncwarp();
