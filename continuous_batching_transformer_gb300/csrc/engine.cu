@@ -579,7 +579,11 @@ static bool tc_projection(cbt_engine* e, const CUtensorMap& wmap, const uint16_t
   p.err = e->err;
   const int Mo = epi == EPI_SWIGLU ? M / 2 : M;
   int t = tbegin(e, CBT_KCLASS_PROJ);
-  bool ok = launch_tc_linear(wmap, *xm, p, split, BN, e->num_sms, e->tc_part_floats, e->stream);
+  // decode rows: cluster split-K (partial sums meet in distributed shared memory); prefill
+  // tokens: whole tiles per CTA
+  bool ok = split ? launch_tc_csk(wmap, *xm, p, BN, e->num_sms, e->stream)
+                  : launch_tc_linear(wmap, *xm, p, split, BN, e->num_sms, e->tc_part_floats,
+                                     e->stream);
   tend(e, t, weight_bytes(e->cfg, M, K) + 4.0 * n * K + 4.0 * n * Mo * (epi == EPI_ADD ? 2 : 1));
   return ok;
 }

@@ -1,0 +1,487 @@
+// gemm_csk.cu -- decode projections y = x W^T with cluster split-K on the 5th-generation tensor
+// cores (sm_103a).
+//
+// Decode streams every weight once per step, so a projection is an HBM-bound stream split over
+// all SMs.  With a few 128-row weight tiles per matrix (32 for a 4096-row output) the K
+// dimension has to be split too, and the partial sums of a tile meet somewhere.  Through global
+// memory that hand-off is slow on a streaming SM: a store, or any release fence, waits behind
+// the ~128 KB of weight tiles the SM keeps in flight (microseconds).  Here the CTAs that split a
+// tile form a thread-block cluster and hand their partial sums to the tile's owner through
+// distributed shared memory: each sender writes its 128 rows x N/2 fp32 sums into the owner's
+// inbox with st.async, which signals the owner's mbarrier with the byte count; the owner adds
+// the partials in rank order (a fixed order, so results do not depend on timing) and runs the
+// epilogue.  No partial sum touches global memory and no fence is executed.
+//
+// Layout of the work: tile t of the matrix belongs to cluster t % NC (clusters take tiles
+// cid, cid + NC, ...), rank r of the cluster streams k-blocks [r*KS/C, (r+1)*KS/C) of each of
+// its cluster's tiles, and tile j of a cluster (in that order) is owned by rank j % C.  Per CTA
+// the pipeline is the one of gemm_tc.cu: a TMA producer warp (weights requested before the
+// previous kernel finishes, operand tiles after), an MMA warp (swap-AB: 128 weight rows x N
+// operand rows, bf16 hi/lo operand parts, fp32 accumulators in TMEM), four epilogue warps.
+#include <algorithm>
+#include <map>
+#include <tuple>
+
+#include "kernels.h"
+#include "tc_common.cuh"
+#include "tc_epilogue.cuh"
+
+namespace {
+
+using tcepi::finish;
+using tcepi::load_residual;
+
+constexpr int kThreads = 192;       // warp 0 TMA, warp 1 MMA (+TMEM alloc), warps 2..5 epilogue
+constexpr int kABytes = 128 * 128;  // 128 rows x 64 bf16
+constexpr int kMaxStages = 8;
+constexpr int kMaxSlots = 4;        // tiles one CTA owns in a launch
+constexpr int kSmemBudget = 227 * 1024;
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// address of the same shared-memory location in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t peer_addr(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// 16 bytes into a peer's shared memory; completes `bytes` on the peer's mbarrier
+__device__ __forceinline__ void st_async_f4(uint32_t raddr, float a, float b, float c, float d,
+                                            uint32_t rbar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+          raddr),
+      "f"(a), "f"(b), "f"(c), "f"(d), "r"(rbar)
+      : "memory");
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  for (uint32_t i = 0; i < tc::kSpinLimit; ++i) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    if ((i & 1023) == 1023 && *abort) return false;
+    if (i > 256) __nanosleep(32);
+  }
+  return false;
+}
+
+__device__ __forceinline__ void report_timeout(const TcParams& p, volatile int* abort, int role) {
+  *abort = 1;
+  if (atomicCAS(p.err, 0, CBT_DEV_TIMEOUT) == 0) p.err[1] = 200 + role;
+}
+
+struct Smem {
+  uint8_t *a, *x;
+  float *inbox, *swx, *rinv;
+  uint64_t *full, *empty, *accf, *acce, *done, *inbox_full;
+  uint32_t* tmem_slot;
+  volatile int* sflag;
+};
+
+template <int BN>
+__host__ __device__ constexpr size_t inbox_floats(int C, int slots) {
+  return (size_t)slots * C * 128 * (BN / 2);
+}
+
+template <int BN>
+__host__ __device__ size_t csk_smem_bytes(const CskPlan& q) {
+  return 1024 + (size_t)q.stages * (kABytes + BN * 128) + inbox_floats<BN>(q.C, q.slots) * 4 +
+         (128 * 33 + 32) * 4 + 512;
+}
+
+template <int BN>
+__device__ __forceinline__ Smem carve(uint8_t* smem, const CskPlan& q) {
+  Smem s;
+  s.a = smem;
+  s.x = s.a + q.stages * kABytes;
+  s.inbox = reinterpret_cast<float*>(s.x + q.stages * BN * 128);
+  s.swx = s.inbox + inbox_floats<BN>(q.C, q.slots);
+  s.rinv = s.swx + 128 * 33;
+  s.full = reinterpret_cast<uint64_t*>(s.rinv + 32);
+  s.empty = s.full + kMaxStages;
+  s.accf = s.empty + kMaxStages;
+  s.acce = s.accf + 2;
+  s.done = s.acce + 2;
+  s.inbox_full = s.done + 1;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(s.inbox_full + kMaxSlots);
+  s.sflag = reinterpret_cast<volatile int*>(s.tmem_slot + 1);  // [1] abort
+  return s;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_tc_csk(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tx,
+             const TcParams p, const CskPlan q) {
+  constexpr int H = BN / 2;  // operand rows: H hi parts, then H lo parts
+  constexpr int kXBytes = BN * 128;
+  constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
+  constexpr uint32_t kIdesc = tc::idesc_bf16(128, BN);
+  constexpr uint32_t kPartBytes = 128 * H * 4;  // one CTA's partial sums of one tile
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const Smem sm = carve<BN>(base, q);
+  const int S = q.stages, C = q.C;
+  volatile int* abort_flag = sm.sflag + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = C > 1 ? cluster_rank() : 0u;
+  const int cid = blockIdx.x / C, NC = gridDim.x / C;
+  const int Tc = cid < p.RB ? (p.RB - cid + NC - 1) / NC : 0;  // tiles cid, cid + NC, ...
+  const int kb0 = (int)((long long)rank * p.KS / C);
+  const int kb1 = (int)((long long)(rank + 1) * p.KS / C);
+  const int owned = Tc > (int)rank ? (Tc - (int)rank + C - 1) / C : 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      tc::mbar_init(&sm.full[s], 1);
+      tc::mbar_init(&sm.empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(&sm.accf[a], 1);
+      tc::mbar_init(&sm.acce[a], 4);
+    }
+    tc::mbar_init(sm.done, 1);
+    for (int s = 0; s < kMaxSlots; ++s) tc::mbar_init(&sm.inbox_full[s], 1);
+    // each tile this CTA owns receives the partial sums of the C - 1 other ranks
+    if (C > 1)
+      for (int s = 0; s < owned; ++s) tc::mbar_expect_tx(&sm.inbox_full[s], (C - 1) * kPartBytes);
+    sm.sflag[0] = 0;
+    sm.sflag[1] = 0;
+    tc::mbar_fence_init();
+    tc::tma_prefetch_desc(&tw);
+    tc::tma_prefetch_desc(&tx);
+  }
+  if (warp == 1) tc::tmem_alloc(sm.tmem_slot, kTmemCols);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  if (C > 1) cluster_sync();  // peers' barriers are initialised before any st.async reaches them
+  const uint32_t tmem = *sm.tmem_slot;
+  pdl_launch();
+
+  if (warp == 0) {
+    if (lane == 0) {  // ---- TMA producer
+      const uint64_t pol_w = tc::policy_evict_first(), pol_x = tc::policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      // the weights never depend on the previous kernel: the first stages' weight tiles are
+      // requested before waiting for it, their operand tiles once it has finished
+      int pend_k[kMaxStages], pend_st[kMaxStages];
+      int npend = 0;
+      bool dep_done = false;
+      auto flush_pending = [&]() {
+        pdl_wait();
+        dep_done = true;
+        for (int i = 0; i < npend; ++i)
+          tc::tma_load_2d(sm.x + pend_st[i] * kXBytes, &tx, &sm.full[pend_st[i]], pend_k[i] * 64, 0,
+                          pol_x);
+        npend = 0;
+      };
+      for (int j = 0; j < Tc && ok; ++j) {
+        const int rb = cid + j * NC;
+        const int y0 = p.epi == EPI_SWIGLU ? rb * 64 : rb * 128;
+        const int y1 = p.epi == EPI_SWIGLU ? p.F + rb * 64 : rb * 128 + 64;
+        for (int k = kb0; k < kb1; ++k) {
+          if (!wait_or_abort(&sm.empty[stage], phase ^ 1, abort_flag)) {
+            report_timeout(p, abort_flag, 1);
+            ok = false;
+            break;
+          }
+          tc::mbar_expect_tx(&sm.full[stage], kABytes + kXBytes);
+          tc::tma_load_2d(sm.a + stage * kABytes, &tw, &sm.full[stage], k * 64, y0, pol_w);
+          tc::tma_load_2d(sm.a + stage * kABytes + 8192, &tw, &sm.full[stage], k * 64, y1, pol_w);
+          if (dep_done) {
+            tc::tma_load_2d(sm.x + stage * kXBytes, &tx, &sm.full[stage], k * 64, 0, pol_x);
+          } else {
+            pend_k[npend] = k;
+            pend_st[npend] = stage;
+            if (++npend == S) flush_pending();
+          }
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!dep_done) flush_pending();
+      // never leave with copies in flight: wait for the last loads issued to each stage
+      for (int i = 0; i < S && i < issued; ++i) {
+        if (--stage < 0) {
+          stage = S - 1;
+          phase ^= 1;
+        }
+        tc::mbar_wait(&sm.full[stage], phase);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // ---- MMA issuer
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int j = 0; j < Tc && ok; ++j) {
+        if (!wait_or_abort(&sm.acce[acc], acc_phase ^ 1, abort_flag)) {
+          report_timeout(p, abort_flag, 2);
+          break;
+        }
+        tc::tc_fence_after();
+        const uint32_t d = tmem + acc * BN;
+        for (int k = kb0; k < kb1; ++k) {
+          if (!wait_or_abort(&sm.full[stage], phase, abort_flag)) {
+            report_timeout(p, abort_flag, 3);
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sm.a + stage * kABytes));
+          const uint64_t xd = tc::sdesc_sw128(tc::smem_u32(sm.x + stage * kXBytes));
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc::mma_bf16(d, ad + 2 * kk, xd + 2 * kk, kIdesc, (k > kb0 || kk > 0) ? 1u : 0u);
+          tc::mma_commit(&sm.empty[stage]);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc::mma_commit(&sm.accf[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      // all MMAs of this thread complete before TMEM is released
+      tc::mma_commit(sm.done);
+      tc::mbar_wait(sm.done, 0);
+    }
+  } else {  // ---- epilogue warps 2..5: TMEM lanes 32q .. 32q + 31 = tile rows
+    pdl_wait();  // outputs and norm statistics are shared with the previous kernel
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;
+    if (p.ss_in) {  // RMSNorm factor of each decode row, from the per-tile sums of squares
+      if (r < p.n_act) {
+        float s = 0.f;
+        for (int t = 0; t < p.ss_tiles; ++t) s += p.ss_in[(size_t)t * p.ss_ld + r];
+        sm.rinv[r] = rsqrtf(s / (float)p.K + p.eps);
+      }
+      tc::named_bar_sync(1, 128);
+    }
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int j = 0; j < Tc; ++j) {
+      const int rb = cid + j * NC;
+      const uint32_t owner = (uint32_t)(j % C);
+      const int slot = j / C;
+      if (!wait_or_abort(&sm.accf[acc], acc_phase, abort_flag)) {
+        report_timeout(p, abort_flag, 4);
+        break;
+      }
+      tc::tc_fence_after();
+      uint32_t raw[BN];
+      const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll
+      for (int c = 0; c < BN / 16; ++c) tc::tmem_ld16(taddr + 16 * c, raw + 16 * c);
+      tc::tmem_ld_wait();
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&sm.acce[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+      float vals[H];
+#pragma unroll
+      for (int n = 0; n < H; ++n) vals[n] = __uint_as_float(raw[n]) + __uint_as_float(raw[n + H]);
+      if (rank == owner) {
+        float res[H];
+        load_residual<H>(p, rb, r, 0, res);  // in flight while the partials arrive
+        float sum[H];
+        if (C > 1) {
+          if (!wait_or_abort(&sm.inbox_full[slot], 0, abort_flag)) {
+            report_timeout(p, abort_flag, 5);
+            break;
+          }
+#pragma unroll
+          for (int n = 0; n < H; ++n) sum[n] = 0.f;
+          for (int src = 0; src < C; ++src) {  // rank order: a fixed summation order
+            if (src == (int)rank) {
+#pragma unroll
+              for (int n = 0; n < H; ++n) sum[n] += vals[n];
+            } else {
+              const float4* in = reinterpret_cast<const float4*>(
+                  sm.inbox + ((size_t)(slot * C + src) * 128 + r) * H);
+#pragma unroll
+              for (int c = 0; c < H / 4; ++c) {
+                const float4 v = in[c];
+                sum[4 * c] += v.x;
+                sum[4 * c + 1] += v.y;
+                sum[4 * c + 2] += v.z;
+                sum[4 * c + 3] += v.w;
+              }
+            }
+          }
+        } else {
+#pragma unroll
+          for (int n = 0; n < H; ++n) sum[n] = vals[n];
+        }
+        finish<H>(p, rb, r, sum, 0, sm.swx, sm.rinv, res);
+      } else {
+        // hand this CTA's partial sums of the tile to its owner
+        const uint32_t dst = peer_addr(
+            tc::smem_u32(sm.inbox + ((size_t)(slot * C + rank) * 128 + r) * H), owner);
+        const uint32_t bar = peer_addr(tc::smem_u32(&sm.inbox_full[slot]), owner);
+#pragma unroll
+        for (int c = 0; c < H / 4; ++c)
+          st_async_f4(dst + 16 * c, vals[4 * c], vals[4 * c + 1], vals[4 * c + 2], vals[4 * c + 3],
+                      bar);
+      }
+    }
+    // an owner leaves only after its inbox has been filled (bounded: a peer that gave up sends
+    // nothing), so no st.async can land in a CTA that has exited
+    if (C > 1 && threadIdx.x == 64)
+      for (int s = 0; s < owned; ++s) tc::mbar_wait(&sm.inbox_full[s], 0);
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+  if (C > 1) cluster_sync();
+}
+
+// cluster dims and PDL on one launch
+template <int BN>
+cudaError_t launch_csk(const CUtensorMap& tw, const CUtensorMap& tx, const TcParams& p,
+                       const CskPlan& q, cudaStream_t s) {
+  const size_t smem = csk_smem_bytes<BN>(q);
+  auto kern = k_tc_csk<BN>;
+  cudaError_t rc = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (rc != cudaSuccess) return rc;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(q.NC * q.C);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = q.C;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  count_launch();
+  return cudaLaunchKernelEx(&cfg, kern, tw, tx, p, q);
+}
+
+// most clusters of C CTAs (each with `smem` bytes) resident at once, cached per configuration
+template <int BN>
+int active_clusters(int C, size_t smem) {
+  static std::map<std::pair<int, size_t>, int> cache;
+  auto key = std::make_pair(C, smem);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  auto kern = k_tc_csk<BN>;
+  int n = 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
+      cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();
+  return cache[key] = n;
+}
+
+}  // namespace
+
+// The cluster shape is chosen from the matrix shape alone (the same for every operand width),
+// so a row's result does not depend on how many rows share the step: minimise the k-blocks
+// the busiest CTA streams, ceil(RB / NC) * ceil(KS / C), over cluster sizes whose clusters can
+// all be resident at once.
+bool csk_plan(int RB, int KS, int BN, int num_sms, CskPlan* out) {
+  if (RB <= 0 || KS <= 0 || num_sms <= 0) return false;
+  static const int kSizes[] = {1, 2, 3, 4, 6, 8};
+  double best = 1e30;
+  CskPlan bp{};
+  for (int C : kSizes) {
+    if (C > KS || C > num_sms) continue;
+    // shape part of the plan, sized for the widest operand (N = 64)
+    CskPlan q{};
+    q.C = C;
+    q.NC = std::min(RB, num_sms / C);
+    const int tmax = (RB + q.NC - 1) / q.NC;
+    q.slots = C > 1 ? (tmax + C - 1) / C : 0;
+    if (q.slots > kMaxSlots) continue;
+    q.stages = kMaxStages;
+    while (q.stages > 4 && csk_smem_bytes<64>(q) > (size_t)kSmemBudget) --q.stages;
+    if (csk_smem_bytes<64>(q) > (size_t)kSmemBudget) continue;
+    const int fit = active_clusters<64>(C, csk_smem_bytes<64>(q));
+    if (fit <= 0) continue;
+    if (fit < q.NC) q.NC = fit;
+    const int tmax2 = (RB + q.NC - 1) / q.NC;
+    q.slots = C > 1 ? (tmax2 + C - 1) / C : 0;
+    if (q.slots > kMaxSlots) continue;
+    const double cost = (double)tmax2 * ((KS + C - 1) / C) + (C > 1 ? 2.0 : 0.0) + 0.01 * C;
+    if (cost < best) {
+      best = cost;
+      bp = q;
+    }
+  }
+  if (best >= 1e30) return false;
+  // pipeline depth for this operand width
+  bp.stages = kMaxStages;
+  auto smem = [&](const CskPlan& q) {
+    return BN == 16 ? csk_smem_bytes<16>(q) : BN == 32 ? csk_smem_bytes<32>(q) : csk_smem_bytes<64>(q);
+  };
+  while (bp.stages > 4 && smem(bp) > (size_t)kSmemBudget) --bp.stages;
+  if (smem(bp) > (size_t)kSmemBudget) return false;
+  *out = bp;
+  return true;
+}
+
+bool launch_tc_csk(const CUtensorMap& tw, const CUtensorMap& tx, TcParams p, int BN, int num_sms,
+                   cudaStream_t s) {
+  if (p.K % 64 || p.K <= 0 || p.n_act <= 0 || 2 * p.n_act > BN) return false;
+  if (p.epi == EPI_SWIGLU && (p.F % 64 || p.M != 2 * p.F)) return false;
+  p.RB = p.epi == EPI_SWIGLU ? p.F / 64 : (p.M + 127) / 128;
+  p.KS = p.K / 64;
+  p.NT = 1;
+  static std::map<std::tuple<int, int, int, int>, CskPlan> plans;
+  const auto key = std::make_tuple(p.RB, p.KS, BN, num_sms);
+  auto it = plans.find(key);
+  CskPlan q;
+  if (it != plans.end()) {
+    q = it->second;
+  } else {
+    if (!csk_plan(p.RB, p.KS, BN, num_sms, &q)) return false;
+    plans[key] = q;
+  }
+  cudaError_t rc;
+  if (BN == 16) rc = launch_csk<16>(tw, tx, p, q, s);
+  else if (BN == 32) rc = launch_csk<32>(tw, tx, p, q, s);
+  else if (BN == 64) rc = launch_csk<64>(tw, tx, p, q, s);
+  else return false;
+  return rc == cudaSuccess;
+}

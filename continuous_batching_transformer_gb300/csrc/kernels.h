@@ -86,6 +86,21 @@ int tc_plain_bn(int n);
 bool launch_tc_linear(const CUtensorMap& tw, const CUtensorMap& tx, TcParams p, bool split,
                       int BN, int num_sms, size_t part_floats, cudaStream_t s);
 
+// ---- cluster split-K decode projections (gemm_csk.cu) -----------------------------------------
+// Clusters of C CTAs; cluster c takes row tiles c, c + NC, ...; rank r streams k-blocks
+// [r*KS/C, (r+1)*KS/C) of each and hands its partial sums to the tile's owner through
+// distributed shared memory.
+struct CskPlan {
+  int C;       // CTAs per cluster (split of K)
+  int NC;      // clusters
+  int stages;  // pipeline depth
+  int slots;   // inbox slots: most tiles one CTA owns
+};
+bool csk_plan(int RB, int KS, int BN, int num_sms, CskPlan* out);
+// y = x W^T over n_act <= BN/2 decode rows (hi/lo operand), any TcParams epilogue
+bool launch_tc_csk(const CUtensorMap& tw, const CUtensorMap& tx, TcParams p, int BN, int num_sms,
+                   cudaStream_t s);
+
 // ---- tensor-core decode attention (attn_tc.cu) ------------------------------------------------
 struct AttnDecodeArgs {
   const uint8_t* qtile;      // [B][Hkv] Q operand images written by the RoPE kernel
