@@ -79,11 +79,13 @@ struct cbt_engine {
   struct LayerMaps {
     CUtensorMap qkv, o, gu, d;
   };
-  std::vector<LayerMaps> wmaps;
-  CUtensorMap lm_map;
+  std::vector<LayerMaps> wmaps;     // 64 x 64 boxes (prefill)
+  std::vector<LayerMaps> wmaps_kb;  // kCskBlocks 64-column blocks of a 128-row tile per box (decode)
+  CUtensorMap lm_map, lm_map_kb;
   int act_rows = 0;
   uint16_t *act_h = nullptr, *act_o = nullptr, *act_u = nullptr;
   std::map<std::pair<const void*, int>, CUtensorMap> xmaps;  // (operand buffer, N tile)
+  std::map<std::pair<const void*, int>, CUtensorMap> xmaps_kb;
   float* tc_part = nullptr;
   size_t tc_part_floats = 0;
   int* tc_cnt = nullptr;
@@ -267,6 +269,17 @@ extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_w
                 make_tmap_bf16(&e->wmaps[l].d, L.wd.w, c.d_ff, c.d_model, 64, 64);
     }
     maps_ok = maps_ok && make_tmap_bf16(&e->lm_map, w->lm_head.w, c.d_model, c.vocab, 64, 64);
+    e->wmaps_kb.resize(c.n_layers);
+    for (int l = 0; l < c.n_layers && maps_ok; ++l) {
+      const cbt_layer_weights& L = w->layers[l];
+      maps_ok = make_tmap_kblocks(&e->wmaps_kb[l].qkv, L.wqkv.w, c.d_model, nqkv, 128, kCskBlocks, 0) &&
+                make_tmap_kblocks(&e->wmaps_kb[l].o, L.wo.w, qd, c.d_model, 128, kCskBlocks, 0) &&
+                make_tmap_kblocks(&e->wmaps_kb[l].gu, L.wgu.w, c.d_model, 2 * c.d_ff, 64, kCskBlocks,
+                                  c.d_ff) &&
+                make_tmap_kblocks(&e->wmaps_kb[l].d, L.wd.w, c.d_ff, c.d_model, 128, kCskBlocks, 0);
+    }
+    maps_ok = maps_ok &&
+              make_tmap_kblocks(&e->lm_map_kb, w->lm_head.w, c.d_model, c.vocab, 128, kCskBlocks, 0);
     // the whole arena seen as K rows (head_dim wide) and as V^T rows (64 keys wide)
     const uint64_t arena_elems = p->kv_arena_bytes / 2;
     maps_ok = maps_ok && arena_elems / 64 < (1ull << 31) &&
@@ -528,17 +541,27 @@ static const CUtensorMap* xmap(cbt_engine* e, const uint16_t* buf, int K, int BN
   return &(e->xmaps[key] = m);
 }
 
+// the operand buffer seen in blocks of kCskBlocks 64-column tiles (decode projections)
+static const CUtensorMap* xmap_kb(cbt_engine* e, const uint16_t* buf, int K, int BN) {
+  auto key = std::make_pair(static_cast<const void*>(buf), BN);
+  auto it = e->xmaps_kb.find(key);
+  if (it != e->xmaps_kb.end()) return &it->second;
+  CUtensorMap m;
+  if (!make_tmap_kblocks(&m, buf, K, e->act_rows, BN, kCskBlocks, 0)) return nullptr;
+  return &(e->xmaps_kb[key] = m);
+}
+
 // y = x W^T over n rows on the tensor cores, operand x in the bf16 buffer xbuf [rows][K].
 // norm_in: the operand is x * g and each column is scaled by its RMSNorm factor, from the
 // sums of squares in e->ss.  next_gain (EPI_ADD): also write the updated rows' sums of squares
 // to e->ss and x * next_gain into e->act_h, the operand of the projection that follows.
-static bool tc_projection(cbt_engine* e, const CUtensorMap& wmap, const uint16_t* xbuf, int n,
-                          int K, int M, Epilogue epi, float* out, int ldo, uint16_t* act_out,
-                          int act_ld, bool norm_in = false, const uint16_t* next_gain = nullptr,
-                          int layer = 0) {
+static bool tc_projection(cbt_engine* e, const CUtensorMap& wmap, const CUtensorMap& wmap_kb,
+                          const uint16_t* xbuf, int n, int K, int M, Epilogue epi, float* out,
+                          int ldo, uint16_t* act_out, int act_ld, bool norm_in = false,
+                          const uint16_t* next_gain = nullptr, int layer = 0) {
   const bool split = n <= 32;
   const int BN = split ? tc_split_bn(n) : tc_plain_bn(n);
-  const CUtensorMap* xm = xmap(e, xbuf, K, BN);
+  const CUtensorMap* xm = split ? xmap_kb(e, xbuf, K, BN) : xmap(e, xbuf, K, BN);
   if (!xm) return false;
   TcParams p{};
   p.ss_ld = e->ss_ld;
@@ -581,7 +604,7 @@ static bool tc_projection(cbt_engine* e, const CUtensorMap& wmap, const uint16_t
   int t = tbegin(e, CBT_KCLASS_PROJ);
   // decode rows: cluster split-K (partial sums meet in distributed shared memory); prefill
   // tokens: whole tiles per CTA
-  bool ok = split ? launch_tc_csk(wmap, *xm, p, BN, e->num_sms, e->stream)
+  bool ok = split ? launch_tc_csk(wmap_kb, *xm, p, BN, e->num_sms, e->stream)
                   : launch_tc_linear(wmap, *xm, p, split, BN, e->num_sms, e->tc_part_floats,
                                      e->stream);
   tend(e, t, weight_bytes(e->cfg, M, K) + 4.0 * n * K + 4.0 * n * Mo * (epi == EPI_ADD ? 2 : 1));
@@ -627,7 +650,7 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
     // decode on the tensor cores rotates q and k, appends K/V and lays out the attention's Q
     // operand in the QKV projection's epilogue; otherwise a separate kernel does it
     if (tcp)
-      ok &= tc_projection(e, e->wmaps[l].qkv, e->act_h, n, d, qd + 2 * kvd,
+      ok &= tc_projection(e, e->wmaps[l].qkv, e->wmaps_kb[l].qkv, e->act_h, n, d, qd + 2 * kvd,
                           fused ? EPI_QKV : EPI_STORE, e->qkv, qd + 2 * kvd, nullptr, 0, fused,
                           nullptr, l);
     else
@@ -662,7 +685,7 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
     }
     tend(e, t, attn_bytes);
     if (tcp)
-      ok &= tc_projection(e, e->wmaps[l].o, e->act_o, n, qd, d, EPI_ADD, e->x, d, nullptr, 0,
+      ok &= tc_projection(e, e->wmaps[l].o, e->wmaps_kb[l].o, e->act_o, n, qd, d, EPI_ADD, e->x, d, nullptr, 0,
                           false, fused ? fn : nullptr);
     else
       projection(e, e->o, n, qd, L.wo, d, EPI_ADD, e->x);
@@ -673,13 +696,13 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
       tend(e, t, 8.0 * n * d);
     }
     if (tcp) {
-      ok &= tc_projection(e, e->wmaps[l].gu, e->act_h, n, d, 2 * F, EPI_SWIGLU, nullptr, 0,
+      ok &= tc_projection(e, e->wmaps[l].gu, e->wmaps_kb[l].gu, e->act_h, n, d, 2 * F, EPI_SWIGLU, nullptr, 0,
                           e->act_u, F, fused);
       // the down projection's epilogue prepares the next layer's (or the final) RMSNorm
       const uint16_t* next_g = l + 1 < c.n_layers
                                    ? static_cast<const uint16_t*>(e->layers[l + 1].attn_norm)
                                    : static_cast<const uint16_t*>(e->w.final_norm);
-      ok &= tc_projection(e, e->wmaps[l].d, e->act_u, n, F, d, EPI_ADD, e->x, d, nullptr, 0,
+      ok &= tc_projection(e, e->wmaps[l].d, e->wmaps_kb[l].d, e->act_u, n, F, d, EPI_ADD, e->x, d, nullptr, 0,
                           false, fused ? next_g : nullptr);
     } else {
       projection(e, e->h, n, d, L.wgu, 2 * F, EPI_SWIGLU, e->act);
@@ -702,7 +725,7 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
   }
   float* lg = logits ? logits : e->logits;
   if (tcp) {
-    if (!tc_projection(e, e->lm_map, e->act_h, n_out, d, c.vocab, EPI_STORE, lg, c.vocab, nullptr,
+    if (!tc_projection(e, e->lm_map, e->lm_map_kb, e->act_h, n_out, d, c.vocab, EPI_STORE, lg, c.vocab, nullptr,
                        0, fused))
       return cudaErrorNotSupported;
   } else {

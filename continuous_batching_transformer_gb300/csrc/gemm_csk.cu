@@ -91,7 +91,7 @@ __host__ __device__ constexpr size_t inbox_floats(int C, int slots) {
 
 template <int BN>
 __host__ __device__ size_t csk_smem_bytes(const CskPlan& q) {
-  return 1024 + (size_t)q.stages * (kABytes + BN * 128) + inbox_floats<BN>(q.C, q.slots) * 4 +
+  return 1024 + (size_t)q.stages * q.nk * (kABytes + BN * 128) + inbox_floats<BN>(q.C, q.slots) * 4 +
          (128 * 33 + 32) * 4 + 512;
 }
 
@@ -99,8 +99,8 @@ template <int BN>
 __device__ __forceinline__ Smem carve(uint8_t* smem, const CskPlan& q) {
   Smem s;
   s.a = smem;
-  s.x = s.a + q.stages * kABytes;
-  s.inbox = reinterpret_cast<float*>(s.x + q.stages * BN * 128);
+  s.x = s.a + q.stages * q.nk * kABytes;
+  s.inbox = reinterpret_cast<float*>(s.x + q.stages * q.nk * BN * 128);
   s.swx = s.inbox + inbox_floats<BN>(q.C, q.slots);
   s.rinv = s.swx + 128 * 33;
   s.full = reinterpret_cast<uint64_t*>(s.rinv + 32);
@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     k_tc_csk(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tx,
              const TcParams p, const CskPlan q) {
   constexpr int H = BN / 2;  // operand rows: H hi parts, then H lo parts
-  constexpr int kXBytes = BN * 128;
+  constexpr int kXBytes = BN * 128;  // operand tile of one 64-column block
   constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
   constexpr uint32_t kIdesc = tc::idesc_bf16(128, BN);
   constexpr uint32_t kPartBytes = 128 * H * 4;  // one CTA's partial sums of one tile
@@ -127,15 +127,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const Smem sm = carve<BN>(base, q);
-  const int S = q.stages, C = q.C;
+  const int S = q.stages, C = q.C, NK = q.nk;
+  const int stage_a = NK * kABytes, stage_x = NK * kXBytes;  // bytes per stage
   volatile int* abort_flag = sm.sflag + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = C > 1 ? cluster_rank() : 0u;
   const int cid = blockIdx.x / C, NC = gridDim.x / C;
   const int Tc = cid < p.RB ? (p.RB - cid + NC - 1) / NC : 0;  // tiles cid, cid + NC, ...
-  const int kb0 = (int)((long long)rank * p.KS / C);
-  const int kb1 = (int)((long long)(rank + 1) * p.KS / C);
+  // this rank's stages: super-blocks of NK 64-column blocks [sb0, sb1) of each tile
+  const int SB = p.KS / NK;
+  const int sb0 = (int)((long long)rank * SB / C);
+  const int sb1 = (int)((long long)(rank + 1) * SB / C);
   const int owned = Tc > (int)rank ? (Tc - (int)rank + C - 1) / C : 0;
 
   if (threadIdx.x == 0) {
@@ -182,27 +185,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         pdl_wait();
         dep_done = true;
         for (int i = 0; i < npend; ++i)
-          tc::tma_load_2d(sm.x + pend_st[i] * kXBytes, &tx, &sm.full[pend_st[i]], pend_k[i] * 64, 0,
+          tc::tma_load_3d(sm.x + pend_st[i] * stage_x, &tx, &sm.full[pend_st[i]], 0, 0, pend_k[i] * NK,
                           pol_x);
         npend = 0;
       };
       for (int j = 0; j < Tc && ok; ++j) {
         const int rb = cid + j * NC;
-        const int y0 = p.epi == EPI_SWIGLU ? rb * 64 : rb * 128;
-        const int y1 = p.epi == EPI_SWIGLU ? p.F + rb * 64 : rb * 128 + 64;
-        for (int k = kb0; k < kb1; ++k) {
+        for (int sb = sb0; sb < sb1; ++sb) {
           if (!wait_or_abort(&sm.empty[stage], phase ^ 1, abort_flag)) {
             report_timeout(p, abort_flag, 1);
             ok = false;
             break;
           }
-          tc::mbar_expect_tx(&sm.full[stage], kABytes + kXBytes);
-          tc::tma_load_2d(sm.a + stage * kABytes, &tw, &sm.full[stage], k * 64, y0, pol_w);
-          tc::tma_load_2d(sm.a + stage * kABytes + 8192, &tw, &sm.full[stage], k * 64, y1, pol_w);
+          tc::mbar_expect_tx(&sm.full[stage], stage_a + stage_x);
+          // NK blocks of the tile's 128 weight rows (SwiGLU: 64 gate rows, then the same 64
+          // features' up rows) in one box, each block a swizzled [128][64] tile
+          if (p.epi == EPI_SWIGLU)
+            tc::tma_load_4d(sm.a + stage * stage_a, &tw, &sm.full[stage], 0, rb * 64, 0, sb * NK, pol_w);
+          else
+            tc::tma_load_3d(sm.a + stage * stage_a, &tw, &sm.full[stage], 0, rb * 128, sb * NK, pol_w);
           if (dep_done) {
-            tc::tma_load_2d(sm.x + stage * kXBytes, &tx, &sm.full[stage], k * 64, 0, pol_x);
+            tc::tma_load_3d(sm.x + stage * stage_x, &tx, &sm.full[stage], 0, 0, sb * NK, pol_x);
           } else {
-            pend_k[npend] = k;
+            pend_k[npend] = sb;
             pend_st[npend] = stage;
             if (++npend == S) flush_pending();
           }
@@ -235,18 +240,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::tc_fence_after();
         const uint32_t d = tmem + acc * BN;
-        for (int k = kb0; k < kb1; ++k) {
+        for (int sb = sb0; sb < sb1; ++sb) {
           if (!wait_or_abort(&sm.full[stage], phase, abort_flag)) {
             report_timeout(p, abort_flag, 3);
             ok = false;
             break;
           }
           tc::tc_fence_after();
-          const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sm.a + stage * kABytes));
-          const uint64_t xd = tc::sdesc_sw128(tc::smem_u32(sm.x + stage * kXBytes));
+          for (int jj = 0; jj < NK; ++jj) {
+            const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sm.a + stage * stage_a + jj * kABytes));
+            const uint64_t xd = tc::sdesc_sw128(tc::smem_u32(sm.x + stage * stage_x + jj * kXBytes));
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc::mma_bf16(d, ad + 2 * kk, xd + 2 * kk, kIdesc, (k > kb0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk)
+              tc::mma_bf16(d, ad + 2 * kk, xd + 2 * kk, kIdesc,
+                           (sb > sb0 || jj > 0 || kk > 0) ? 1u : 0u);
+          }
           tc::mma_commit(&sm.empty[stage]);
           if (++stage == S) {
             stage = 0;
@@ -425,17 +433,20 @@ bool csk_plan(int RB, int KS, int BN, int num_sms, CskPlan* out) {
   static const int kSizes[] = {1, 2, 3, 4, 6, 8};
   double best = 1e30;
   CskPlan bp{};
+  if (KS % kCskBlocks) return false;
+  const int SB = KS / kCskBlocks;
   for (int C : kSizes) {
-    if (C > KS || C > num_sms) continue;
+    if (C > SB || C > num_sms) continue;
     // shape part of the plan, sized for the widest operand (N = 64)
     CskPlan q{};
+    q.nk = kCskBlocks;
     q.C = C;
     q.NC = std::min(RB, num_sms / C);
     const int tmax = (RB + q.NC - 1) / q.NC;
     q.slots = C > 1 ? (tmax + C - 1) / C : 0;
     if (q.slots > kMaxSlots) continue;
     q.stages = kMaxStages;
-    while (q.stages > 4 && csk_smem_bytes<64>(q) > (size_t)kSmemBudget) --q.stages;
+    while (q.stages > 3 && csk_smem_bytes<64>(q) > (size_t)kSmemBudget) --q.stages;
     if (csk_smem_bytes<64>(q) > (size_t)kSmemBudget) continue;
     const int fit = active_clusters<64>(C, csk_smem_bytes<64>(q));
     if (fit <= 0) continue;
@@ -443,7 +454,7 @@ bool csk_plan(int RB, int KS, int BN, int num_sms, CskPlan* out) {
     const int tmax2 = (RB + q.NC - 1) / q.NC;
     q.slots = C > 1 ? (tmax2 + C - 1) / C : 0;
     if (q.slots > kMaxSlots) continue;
-    const double cost = (double)tmax2 * ((KS + C - 1) / C) + (C > 1 ? 2.0 : 0.0) + 0.01 * C;
+    const double cost = (double)tmax2 * ((SB + C - 1) / C) * kCskBlocks + (C > 1 ? 2.0 : 0.0) + 0.01 * C;
     if (cost < best) {
       best = cost;
       bp = q;
@@ -455,7 +466,7 @@ bool csk_plan(int RB, int KS, int BN, int num_sms, CskPlan* out) {
   auto smem = [&](const CskPlan& q) {
     return BN == 16 ? csk_smem_bytes<16>(q) : BN == 32 ? csk_smem_bytes<32>(q) : csk_smem_bytes<64>(q);
   };
-  while (bp.stages > 4 && smem(bp) > (size_t)kSmemBudget) --bp.stages;
+  while (bp.stages > 3 && smem(bp) > (size_t)kSmemBudget) --bp.stages;
   if (smem(bp) > (size_t)kSmemBudget) return false;
   *out = bp;
   return true;

@@ -393,6 +393,31 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t r
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_tmap_kblocks(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint32_t box_rows,
+                       uint32_t nk, uint64_t pair_rows) {
+  auto fn = encode_fn();
+  if (!fn || !base || (reinterpret_cast<uintptr_t>(base) & 15) || K % 64 || nk < 1 || box_rows > 256)
+    return false;
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  if (pair_rows == 0) {
+    // [k-block][row][64 columns]: one box is nk consecutive 64-column blocks of box_rows rows
+    cuuint64_t dims[3] = {64, rows, K / 64};
+    cuuint64_t strides[2] = {K * 2, 128};
+    cuuint32_t box[3] = {64, box_rows, nk};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
+  // rows [0, 2 pair_rows) as two halves (gate, up): [k-block][half][row][64 columns]
+  if (rows != 2 * pair_rows) return false;
+  cuuint64_t dims[4] = {64, pair_rows, 2, K / 64};
+  cuuint64_t strides[3] = {K * 2, pair_rows * K * 2, 128};
+  cuuint32_t box[4] = {64, box_rows, 2, nk};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int tc_split_bn(int n) { return n <= 8 ? 16 : (n <= 16 ? 32 : 64); }
 int tc_plain_bn(int n) { return n <= 64 ? 64 : (n <= 128 ? 128 : 256); }
 

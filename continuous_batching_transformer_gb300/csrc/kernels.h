@@ -80,6 +80,12 @@ struct TcParams {
 
 bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
                     uint32_t box_inner, uint32_t box_rows);
+// A bf16 [rows][K] matrix seen as 64-column blocks, so one TMA box brings nk consecutive blocks
+// of box_rows rows, each landing as a 128-byte-swizzled [box_rows][64] tile: 3-D map
+// {64, rows, K/64}.  pair_rows > 0 (SwiGLU's [gate; up], rows = 2 pair_rows): 4-D map
+// {64, pair_rows, 2, K/64}, a box brings box_rows gate rows then the same up rows per block.
+bool make_tmap_kblocks(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint32_t box_rows,
+                       uint32_t nk, uint64_t pair_rows);
 // N tile for hi/lo (split) activations of n rows, and for plain bf16 activations
 int tc_split_bn(int n);
 int tc_plain_bn(int n);
@@ -95,9 +101,13 @@ struct CskPlan {
   int NC;      // clusters
   int stages;  // pipeline depth
   int slots;   // inbox slots: most tiles one CTA owns
+  int nk;      // 64-column blocks per stage (one TMA box of weights, one of operand)
 };
+constexpr int kCskBlocks = 2;  // nk of the decode projections' tensor maps
 bool csk_plan(int RB, int KS, int BN, int num_sms, CskPlan* out);
-// y = x W^T over n_act <= BN/2 decode rows (hi/lo operand), any TcParams epilogue
+// y = x W^T over n_act <= BN/2 decode rows (hi/lo operand), any TcParams epilogue.  tw: the
+// weights as make_tmap_kblocks(.., 128 rows (SwiGLU: 64 + 64), kCskBlocks, ..); tx: the operand
+// as make_tmap_kblocks(.., BN rows, kCskBlocks, 0).
 bool launch_tc_csk(const CUtensorMap& tw, const CUtensorMap& tx, TcParams p, int BN, int num_sms,
                    cudaStream_t s);
 
