@@ -79,31 +79,44 @@ __device__ __forceinline__ void report_timeout(const TcParams& p, volatile int* 
 struct Smem {
   uint8_t *a, *x;
   float *inbox, *swx, *rinv;
+  float *cosv, *sinv;  // shared copies of the RoPE tables [n_act][64] (QKV)
+  QueryRow* rows;      // shared copy of the row table [32] (QKV)
   uint64_t *full, *empty, *accf, *acce, *done, *inbox_full;
   uint32_t* tmem_slot;
   volatile int* sflag;
 };
 
+// inbox of a CTA: per owned tile, the partial sums of the C - 1 other ranks
 template <int BN>
 __host__ __device__ constexpr size_t inbox_floats(int C, int slots) {
-  return (size_t)slots * C * 128 * (BN / 2);
+  return (size_t)slots * (C - 1) * 128 * (BN / 2);
 }
 
+// shared copies of the RoPE tables: BN/2 rows x up to 64 pairs, cos and sin
 template <int BN>
-__host__ __device__ size_t csk_smem_bytes(const CskPlan& q) {
+__host__ __device__ constexpr size_t rope_floats() {
+  return (size_t)(BN / 2) * 64 * 2;
+}
+
+// qkv: the launch keeps shared copies of the RoPE tables and the row table
+template <int BN>
+__host__ __device__ size_t csk_smem_bytes(const CskPlan& q, bool qkv) {
   return 1024 + (size_t)q.stages * q.nk * (kABytes + BN * 128) + inbox_floats<BN>(q.C, q.slots) * 4 +
-         (128 * 33 + 32) * 4 + 512;
+         (128 * 33 + 32) * 4 + (qkv ? rope_floats<BN>() * 4 + 32 * sizeof(QueryRow) : 0) + 512;
 }
 
 template <int BN>
-__device__ __forceinline__ Smem carve(uint8_t* smem, const CskPlan& q) {
+__device__ __forceinline__ Smem carve(uint8_t* smem, const CskPlan& q, bool qkv) {
   Smem s;
   s.a = smem;
   s.x = s.a + q.stages * q.nk * kABytes;
   s.inbox = reinterpret_cast<float*>(s.x + q.stages * q.nk * BN * 128);
   s.swx = s.inbox + inbox_floats<BN>(q.C, q.slots);
   s.rinv = s.swx + 128 * 33;
-  s.full = reinterpret_cast<uint64_t*>(s.rinv + 32);
+  s.cosv = s.rinv + 32;
+  s.sinv = s.cosv + (qkv ? rope_floats<BN>() / 2 : 0);
+  s.rows = reinterpret_cast<QueryRow*>(s.sinv + (qkv ? rope_floats<BN>() / 2 : 0));
+  s.full = reinterpret_cast<uint64_t*>(s.rows + (qkv ? 32 : 0));
   s.empty = s.full + kMaxStages;
   s.accf = s.empty + kMaxStages;
   s.acce = s.accf + 2;
@@ -126,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  const Smem sm = carve<BN>(base, q);
+  const Smem sm = carve<BN>(base, q, p.epi == EPI_QKV);
   const int S = q.stages, C = q.C, NK = q.nk;
   const int stage_a = NK * kABytes, stage_x = NK * kXBytes;  // bytes per stage
   volatile int* abort_flag = sm.sflag + 1;
@@ -282,14 +295,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < p.ss_tiles; ++t) s += p.ss_in[(size_t)t * p.ss_ld + r];
         sm.rinv[r] = rsqrtf(s / (float)p.K + p.eps);
       }
-      tc::named_bar_sync(1, 128);
     }
+    tcepi::EpiSrc src = tcepi::epi_src_global(p);
+    if (p.epi == EPI_QKV) {
+      // the row table and the RoPE tables in shared memory, loaded while the weights stream
+      const int half = p.head_dim >> 1;
+      for (int i = r; i < p.n_act * half; i += 128) {
+        sm.cosv[i] = p.cosv[i];
+        sm.sinv[i] = p.sinv[i];
+      }
+      if (r < p.n_act) sm.rows[r] = p.rows[r];
+      src.rows = sm.rows;
+      src.cosv = sm.cosv;
+      src.sinv = sm.sinv;
+    }
+    tc::named_bar_sync(1, 128);
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int j = 0; j < Tc; ++j) {
       const int rb = cid + j * NC;
       const uint32_t owner = (uint32_t)(j % C);
       const int slot = j / C;
+      // the owner's global inputs of this tile, requested before its accumulator is ready
+      float res[H];
+      if (rank == owner) {
+        load_residual<H>(p, rb, r, 0, res);
+        src.gn = tcepi::load_next_gain(p, rb, r);
+        src.has_gn = true;
+      }
       if (!wait_or_abort(&sm.accf[acc], acc_phase, abort_flag)) {
         report_timeout(p, abort_flag, 4);
         break;
@@ -311,8 +344,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int n = 0; n < H; ++n) vals[n] = __uint_as_float(raw[n]) + __uint_as_float(raw[n + H]);
       if (rank == owner) {
-        float res[H];
-        load_residual<H>(p, rb, r, 0, res);  // in flight while the partials arrive
         float sum[H];
         if (C > 1) {
           if (!wait_or_abort(&sm.inbox_full[slot], 0, abort_flag)) {
@@ -326,8 +357,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int n = 0; n < H; ++n) sum[n] += vals[n];
             } else {
+              const int from = src - (src > (int)rank);  // sender slots skip the owner
               const float4* in = reinterpret_cast<const float4*>(
-                  sm.inbox + ((size_t)(slot * C + src) * 128 + r) * H);
+                  sm.inbox + ((size_t)(slot * (C - 1) + from) * 128 + r) * H);
 #pragma unroll
               for (int c = 0; c < H / 4; ++c) {
                 const float4 v = in[c];
@@ -342,11 +374,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int n = 0; n < H; ++n) sum[n] = vals[n];
         }
-        finish<H>(p, rb, r, sum, 0, sm.swx, sm.rinv, res);
+        finish<H>(p, rb, r, sum, 0, sm.swx, sm.rinv, res, src);
       } else {
         // hand this CTA's partial sums of the tile to its owner
+        const int from = (int)rank - ((int)rank > (int)owner);
         const uint32_t dst = peer_addr(
-            tc::smem_u32(sm.inbox + ((size_t)(slot * C + rank) * 128 + r) * H), owner);
+            tc::smem_u32(sm.inbox + ((size_t)(slot * (C - 1) + from) * 128 + r) * H), owner);
         const uint32_t bar = peer_addr(tc::smem_u32(&sm.inbox_full[slot]), owner);
 #pragma unroll
         for (int c = 0; c < H / 4; ++c)
@@ -372,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int BN>
 cudaError_t launch_csk(const CUtensorMap& tw, const CUtensorMap& tx, const TcParams& p,
                        const CskPlan& q, cudaStream_t s) {
-  const size_t smem = csk_smem_bytes<BN>(q);
+  const size_t smem = csk_smem_bytes<BN>(q, p.epi == EPI_QKV);
   auto kern = k_tc_csk<BN>;
   cudaError_t rc = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (rc != cudaSuccess) return rc;
@@ -445,10 +478,9 @@ bool csk_plan(int RB, int KS, int BN, int num_sms, CskPlan* out) {
     const int tmax = (RB + q.NC - 1) / q.NC;
     q.slots = C > 1 ? (tmax + C - 1) / C : 0;
     if (q.slots > kMaxSlots) continue;
-    q.stages = kMaxStages;
-    while (q.stages > 3 && csk_smem_bytes<64>(q) > (size_t)kSmemBudget) --q.stages;
-    if (csk_smem_bytes<64>(q) > (size_t)kSmemBudget) continue;
-    const int fit = active_clusters<64>(C, csk_smem_bytes<64>(q));
+    q.stages = 2;  // the shallowest pipeline a launch may get
+    if (csk_smem_bytes<64>(q, true) > (size_t)kSmemBudget) continue;
+    const int fit = active_clusters<64>(C, csk_smem_bytes<64>(q, true));
     if (fit <= 0) continue;
     if (fit < q.NC) q.NC = fit;
     const int tmax2 = (RB + q.NC - 1) / q.NC;
@@ -461,12 +493,13 @@ bool csk_plan(int RB, int KS, int BN, int num_sms, CskPlan* out) {
     }
   }
   if (best >= 1e30) return false;
-  // pipeline depth for this operand width
+  // pipeline depth for this operand width (the deepest that fits any epilogue)
   bp.stages = kMaxStages;
   auto smem = [&](const CskPlan& q) {
-    return BN == 16 ? csk_smem_bytes<16>(q) : BN == 32 ? csk_smem_bytes<32>(q) : csk_smem_bytes<64>(q);
+    return BN == 16 ? csk_smem_bytes<16>(q, true)
+                    : BN == 32 ? csk_smem_bytes<32>(q, true) : csk_smem_bytes<64>(q, true);
   };
-  while (bp.stages > 3 && smem(bp) > (size_t)kSmemBudget) --bp.stages;
+  while (bp.stages > 2 && smem(bp) > (size_t)kSmemBudget) --bp.stages;
   if (smem(bp) > (size_t)kSmemBudget) return false;
   *out = bp;
   return true;

@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kb == 0 && ke == p.KS) {
           float res[H];
           load_residual<H>(p, rb, r, 0, res);
-          finish<H>(p, rb, r, vals, 0, swx, rinv, res);
+          finish<H>(p, rb, r, vals, 0, swx, rinv, res, tcepi::epi_src_global(p));
         } else {
           const int first = cta_of_unit(p.U, gridDim.x, (long long)tile * p.KS);
           const int slot = blockIdx.x - first;
@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   for (int n = 0; n < H; ++n) sum[n] += ld[i][n];
                 }
             }
-            finish<H>(p, rb, r, sum, 0, swx, rinv, res);
+            finish<H>(p, rb, r, sum, 0, swx, rinv, res, tcepi::epi_src_global(p));
             if (threadIdx.x == 64) p.cnt[tile] = 0;
           }
         }
@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           load_residual<32>(p, rb, r, nt * BN + c0, res);
 #pragma unroll
           for (int j = 0; j < 32; ++j) vals[j] = __uint_as_float(raw[j]);
-          finish<32>(p, rb, r, vals, nt * BN + c0, swx, rinv, res);
+          finish<32>(p, rb, r, vals, nt * BN + c0, swx, rinv, res, tcepi::epi_src_global(p));
         }
         tc::tc_fence_before();
         __syncwarp();

@@ -22,12 +22,35 @@ __device__ __forceinline__ void load_residual(const TcParams& p, int rb, int r, 
   }
 }
 
+// Where finish() reads the values it needs besides the accumulator: the row table and the RoPE
+// cos/sin (global memory, or shared-memory copies), and optionally the next RMSNorm gain of
+// this thread's output row, loaded earlier (each global load here is a round trip at the end
+// of the projection, when latency is all that is left).
+struct EpiSrc {
+  const QueryRow* rows;  // [n_act]
+  const float* cosv;     // [n_act][head_dim / 2]
+  const float* sinv;
+  float gn;              // next_gain[m] (valid when has_gn)
+  bool has_gn;
+};
+
+__device__ __forceinline__ EpiSrc epi_src_global(const TcParams& p) {
+  return EpiSrc{p.rows, p.cosv, p.sinv, 0.f, false};
+}
+
+// next_gain of tile row r of row block rb (EPI_ADD with a next operand), 0 otherwise
+__device__ __forceinline__ float load_next_gain(const TcParams& p, int rb, int r) {
+  const int m = rb * 128 + r;
+  return (p.next_act && m < p.M) ? bf16_to_f32(p.next_gain[m]) : 0.f;
+}
+
 // Final epilogue of CNT (<= 32) columns (tokens tok0 .. tok0+CNT-1) of tile row r of row
 // block rb.  All 128 epilogue threads call it together.  rinv (when p.ss_in) holds each
 // column's RMSNorm factor; res the residual values from load_residual (EPI_ADD).
 template <int CNT>
 __device__ __forceinline__ void finish(const TcParams& p, int rb, int r, float* vals, int tok0,
-                                       float* swx, const float* rinv, const float* res) {
+                                       float* swx, const float* rinv, const float* res,
+                                       const EpiSrc& src) {
   if (p.ss_in) {
 #pragma unroll
     for (int j = 0; j < CNT; ++j) vals[j] *= rinv[j];
@@ -42,8 +65,8 @@ __device__ __forceinline__ void finish(const TcParams& p, int rb, int r, float* 
 #pragma unroll
     for (int j = 0; j < CNT; ++j) {
       const bool ok = rope && j < p.n_act;
-      cs[j] = ok ? __ldg(p.cosv + j * half + (i & (half - 1))) : 1.f;
-      sn[j] = ok ? __ldg(p.sinv + j * half + (i & (half - 1))) : 0.f;
+      cs[j] = ok ? src.cosv[j * half + (i & (half - 1))] : 1.f;
+      sn[j] = ok ? src.sinv[j * half + (i & (half - 1))] : 0.f;
     }
     tc::named_bar_sync(1, 128);
 #pragma unroll
@@ -69,7 +92,7 @@ __device__ __forceinline__ void finish(const TcParams& p, int rb, int r, float* 
         *reinterpret_cast<uint16_t*>(tile + sw128_offset(8 + head % G, i, 2048)) =
             f32_to_bf16(qv - bf16_to_f32(hi));
       } else {
-        const QueryRow qr = p.rows[j];
+        const QueryRow qr = src.rows[j];
         if (head < p.n_heads + p.n_kv_heads)
           p.arena[k_index(qr, p.layer, head - p.n_heads, qr.pos, i, p.n_kv_heads, hd)] =
               f32_to_bf16(v);
@@ -82,7 +105,7 @@ __device__ __forceinline__ void finish(const TcParams& p, int rb, int r, float* 
   }
   if (p.epi != EPI_SWIGLU) {
     const int m = rb * 128 + r;
-    const float gn = (p.next_act && m < p.M) ? bf16_to_f32(p.next_gain[m]) : 0.f;
+    const float gn = src.has_gn ? src.gn : load_next_gain(p, rb, r);
     float sq[CNT];
 #pragma unroll
     for (int j = 0; j < CNT; ++j) {
