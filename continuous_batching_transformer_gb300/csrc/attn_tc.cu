@@ -94,8 +94,9 @@ __global__ void __launch_bounds__(160, kCtasPerSm)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;  // columns 0..15: S^T, 16..31: O^T
-  pdl_wait();  // the Q operand and the K/V appended at t_s come from the previous kernel
   pdl_launch();
+  // the work list and the row table are step inputs copied before the step's first kernel, so
+  // they may be read before waiting for the previous kernel
   const int n_items = *n_items_dev;
 
   if (warp == 4) {
@@ -104,11 +105,46 @@ __global__ void __launch_bounds__(160, kCtasPerSm)
       const uint64_t pol = tc::policy_evict_first();
       uint32_t qn = 0, kn = 0, vn = 0;
       bool ok = true;
+      auto load_kv = [&](const QueryRow& r, const AttnItem& w, int sub) -> bool {
+        const long long krow = kv_block(r, layer, 0, w.g, n_kv_heads, HD) / HD;
+        const long long vrow = kv_block(r, layer, 1, w.g, n_kv_heads, HD) / 64;
+        if (!tc::mbar_wait(kempty, (kn & 1) ^ 1)) {
+          flag_timeout(err, abort_flag, 22);
+          return false;
+        }
+        tc::mbar_expect_tx(kfull, kKBytes);
+#pragma unroll
+        for (int h = 0; h < nKh; ++h)
+          tc::tma_load_2d(sK + h * kBox, &tk, kfull, h * 64, (int)(krow + sub * kSub), pol);
+        ++kn;
+        if (!tc::mbar_wait(vempty, (vn & 1) ^ 1)) {
+          flag_timeout(err, abort_flag, 23);
+          return false;
+        }
+        tc::mbar_expect_tx(vfull, kVBytes);
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          tc::tma_load_2d(sV + j * kBox, &tv, vfull, 0, (int)(vrow + (long long)(2 * sub + j) * HD),
+                          pol);
+        ++vn;
+        return true;
+      };
+      // Keys and values before the new position were written by earlier steps: the first
+      // sub-chunk's tiles are requested before waiting for the previous kernel (which appends
+      // the new position and writes Q), unless the sub-chunk holds the new position.
+      int pre_sub = -1;
+      if ((int)blockIdx.x < n_items) {
+        const AttnItem w = items[blockIdx.x];
+        const QueryRow r = rows[w.b];
+        if (w.s0 < r.pos / kSub) {
+          ok = load_kv(r, w, w.s0);
+          pre_sub = w.s0;
+        }
+      }
+      pdl_wait();
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
         const AttnItem w = items[it];
         const QueryRow r = rows[w.b];
-        const long long krow = kv_block(r, layer, 0, w.g, n_kv_heads, HD) / HD;
-        const long long vrow = kv_block(r, layer, 1, w.g, n_kv_heads, HD) / 64;
         if (!tc::mbar_wait(qempty, (qn & 1) ^ 1)) {
           flag_timeout(err, abort_flag, 21);
           break;
@@ -116,28 +152,9 @@ __global__ void __launch_bounds__(160, kCtasPerSm)
         tc::mbar_expect_tx(qfull, kQBytes);
         tc::bulk_load(sQ, qtile + ((size_t)w.b * n_kv_heads + w.g) * kQBytes, kQBytes, qfull);
         ++qn;
-        for (int sub = w.s0; sub < w.s1; ++sub) {
-          if (!tc::mbar_wait(kempty, (kn & 1) ^ 1)) {
-            flag_timeout(err, abort_flag, 22);
-            ok = false;
-            break;
-          }
-          tc::mbar_expect_tx(kfull, kKBytes);
-#pragma unroll
-          for (int h = 0; h < nKh; ++h)
-            tc::tma_load_2d(sK + h * kBox, &tk, kfull, h * 64, (int)(krow + sub * kSub), pol);
-          ++kn;
-          if (!tc::mbar_wait(vempty, (vn & 1) ^ 1)) {
-            flag_timeout(err, abort_flag, 23);
-            ok = false;
-            break;
-          }
-          tc::mbar_expect_tx(vfull, kVBytes);
-#pragma unroll
-          for (int j = 0; j < 2; ++j)
-            tc::tma_load_2d(sV + j * kBox, &tv, vfull, 0, (int)(vrow + (long long)(2 * sub + j) * HD),
-                            pol);
-          ++vn;
+        for (int sub = w.s0; sub < w.s1 && ok; ++sub) {
+          if (it == (int)blockIdx.x && sub == pre_sub) continue;  // already requested
+          ok = load_kv(r, w, sub);
         }
       }
       // no copies in flight at exit: the last Q, K and V loads have landed
@@ -147,6 +164,7 @@ __global__ void __launch_bounds__(160, kCtasPerSm)
     }
   } else {
     // ---- compute warps: MMA issue (thread 0), softmax (thread = key), accumulate (thread = dim)
+    pdl_wait();  // Q, the new K/V and the partial buffers are shared with earlier kernels
     uint32_t qn = 0, kn = 0, vn = 0, sn = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
@@ -286,35 +304,68 @@ __global__ void __launch_bounds__(160, kCtasPerSm)
 }
 
 // Combine the partials of each (row, q head): o = sum_i o_i e^(m_i - M) / sum_i l_i e^(m_i - M)
-// and write it as the bf16 (hi/lo) operand of the output projection.
-__global__ void k_attn_merge(const float* __restrict__ part_o, const float2* __restrict__ part_ml,
-                             const int* __restrict__ item_base, const int* __restrict__ item_count,
-                             int n_heads, int n_kv_heads, int head_dim, uint16_t* act, int lo_rows) {
+// and write it as the bf16 (hi/lo) operand of the output projection.  One 128-thread block per
+// (row, q head): the threads reduce the splits' (m, l) pairs, then warp w sums splits w, w + 4,
+// ... (lane = head_dim / 32 output dimensions) with their loads in flight together, and the four
+// warps' sums are added in a fixed order.  The order depends only on the row's own splits.
+__global__ void __launch_bounds__(128)
+    k_attn_merge(const float* __restrict__ part_o, const float2* __restrict__ part_ml,
+                 const int* __restrict__ item_base, const int* __restrict__ item_count, int B,
+                 int n_heads, int n_kv_heads, int head_dim, uint16_t* act, int lo_rows) {
   pdl_wait();
   pdl_launch();
-  const int b = blockIdx.y, hq = blockIdx.x;
+  __shared__ float red[4];
+  __shared__ float wsum[4][128];
+  const int hq = blockIdx.x, b = blockIdx.y;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int G = n_heads / n_kv_heads, g = hq / G, h = hq % G;
   const int cnt = item_count[b];
   const int first = item_base[b] + g * cnt;
-  float M = -INFINITY;
-  for (int i = 0; i < cnt; ++i) M = fmaxf(M, part_ml[(size_t)(first + i) * G + h].x);
-  float L = 0.f;
-  for (int i = 0; i < cnt; ++i) {
-    const float2 ml = part_ml[(size_t)(first + i) * G + h];
-    L += ml.y * __expf(ml.x - M);
+  const float2* ml = part_ml + (size_t)first * G + h;  // split i at ml[i * G]
+  float m = -INFINITY;
+  for (int i = t; i < cnt; i += 128) m = fmaxf(m, ml[(size_t)i * G].x);
+  m = warp_max(m);
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  const float M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  __syncthreads();
+  float l = 0.f;
+  for (int i = t; i < cnt; i += 128) {
+    const float2 v = ml[(size_t)i * G];
+    l += v.y * __expf(v.x - M);
   }
-  const float invL = 1.f / L;
-  const int K = n_heads * head_dim;
-  for (int d = threadIdx.x; d < head_dim; d += blockDim.x) {
-    float o = 0.f;
-    for (int i = 0; i < cnt; ++i) {
-      const float wgt = __expf(part_ml[(size_t)(first + i) * G + h].x - M);
-      o += part_o[((size_t)(first + i) * G + h) * head_dim + d] * wgt;
+  l = warp_sum(l);
+  if (lane == 0) red[warp] = l;
+  __syncthreads();
+  const float invL = 1.f / (red[0] + red[1] + red[2] + red[3]);
+  const int per = head_dim / 32;  // 4 (head_dim 128) or 2 (64)
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+  for (int i = warp; i < cnt; i += 4) {
+    const float2 v = ml[(size_t)i * G];
+    const float wgt = __expf(v.x - M);
+    const float* po = part_o + ((size_t)(first + i) * G + h) * head_dim + lane * per;
+    if (per == 4) {
+      const float4 o = __ldcg(reinterpret_cast<const float4*>(po));
+      acc[0] += o.x * wgt;
+      acc[1] += o.y * wgt;
+      acc[2] += o.z * wgt;
+      acc[3] += o.w * wgt;
+    } else {
+      const float2 o = __ldcg(reinterpret_cast<const float2*>(po));
+      acc[0] += o.x * wgt;
+      acc[1] += o.y * wgt;
     }
-    o *= invL;
+  }
+  for (int j = 0; j < per; ++j) wsum[warp][lane * per + j] = acc[j];
+  __syncthreads();
+  if (t < head_dim) {
+    const float o = (((wsum[0][t] + wsum[1][t]) + wsum[2][t]) + wsum[3][t]) * invL;
+    const int K = n_heads * head_dim;
+    const int col = hq * head_dim + t;
     const uint16_t hi = f32_to_bf16(o);
-    act[(size_t)b * K + hq * head_dim + d] = hi;
-    if (lo_rows > 0) act[(size_t)(lo_rows + b) * K + hq * head_dim + d] = f32_to_bf16(o - bf16_to_f32(hi));
+    act[(size_t)b * K + col] = hi;
+    if (lo_rows > 0) act[(size_t)(lo_rows + b) * K + col] = f32_to_bf16(o - bf16_to_f32(hi));
   }
 }
 
@@ -343,7 +394,8 @@ bool launch_attn_decode_tc(const CUtensorMap& tk, const CUtensorMap& tv, const A
   else if (a.head_dim == 64) rc = launch_decode<64>(tk, tv, a, grid, s);
   else return false;
   if (rc != cudaSuccess) return false;
-  rc = launch_pdl(k_attn_merge, dim3(a.n_heads, a.B), dim3(128), 0, s, a.part_o, a.part_ml,
-                  a.item_base, a.item_count, a.n_heads, a.n_kv_heads, a.head_dim, a.act, a.act_lo);
+  rc = launch_pdl(k_attn_merge, dim3(a.n_heads, a.B), dim3(128), 0, s, a.part_o,
+                  a.part_ml, a.item_base, a.item_count, a.B, a.n_heads, a.n_kv_heads, a.head_dim,
+                  a.act, a.act_lo);
   return rc == cudaSuccess;
 }

@@ -742,7 +742,7 @@ static void drop_graphs(cbt_engine* e);
 // Work list of the tensor-core decode attention for the rows in e->hrows[0..B): per row and kv
 // head, runs of kSubsPerItem 128-key sub-chunks over positions [0, pos].  Grows the item and
 // partial buffers when needed and copies the list to the device on the engine stream.
-static constexpr int kSubsPerItem = 2;
+static constexpr int kSubsPerItem = 1;
 
 static cudaError_t plan_decode_attention(cbt_engine* e, int B) {
   const int Hkv = e->cfg.n_kv_heads, G = e->cfg.n_heads / Hkv, hd = e->cfg.head_dim;
