@@ -100,6 +100,7 @@ class Engine:
                                 self.stream.cuda_stream)
         self.handle = B.engine_create(weights.cfg, weights.struct, params)
         self.max_batch = max_batch
+        self.max_prefill_tokens = max_prefill_tokens
 
     def close(self):
         if self.handle:

@@ -1,0 +1,150 @@
+"""Continuous batching over a request trace, on the engine's public calls only.
+
+Requests arrive over time (``synth.recipes.trace_requests``: Poisson arrivals, ragged prompts,
+geometric output lengths).  At every step boundary the driver
+
+1. retires the rows that have produced all their tokens (``retire`` frees their slabs),
+2. admits the requests that have arrived, up to ``live_cap`` live rows and the engine's
+   prefill token budget, in one ``prefill_segmented`` call (each prompt in its own slab,
+   positions restarting at 0; the argmax of each segment's last logits is the request's
+   first token),
+3. runs one ``decode_step_batch`` over every live row (the previous step's tokens stay on the
+   device: the step reads them from and writes the next ones to a device token buffer).
+
+A row that has produced ``output_len`` tokens (the first one from the prefill) leaves at the
+next boundary.  Time to first token is measured from the request's arrival to the end of the
+prefill that produced it; time per output token is the mean gap between a request's later
+tokens.  ``realtime=False`` replays the trace with every request arriving at t = 0 (a
+throughput measurement); ``realtime=True`` waits for the arrival times.
+"""
+from __future__ import annotations
+
+import time
+from collections import deque
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+import synth
+
+
+@dataclass
+class TraceResult:
+    generated: int = 0                                  # tokens produced by every request
+    wall_s: float = 0.0
+    steps: int = 0                                      # decode steps
+    step_rows: list = field(default_factory=list)       # live rows of each decode step
+    step_s: list = field(default_factory=list)          # duration of each decode step
+    step_kv_tokens: list = field(default_factory=list)  # live positions the step's attention read
+    prefill_tokens: int = 0
+    prefill_s: float = 0.0
+    ttft_s: dict = field(default_factory=dict)          # request index -> time to first token
+    tpot_s: dict = field(default_factory=dict)          # request index -> time per output token
+    tokens: dict = field(default_factory=dict)          # request index -> generated tokens
+
+
+def prompt_tokens(req, seed: int, vocab: int) -> np.ndarray:
+    """The request's prompt: its own seeded token stream."""
+    return synth.tokens(req.prompt_len, seed, synth.stream_tokens(req.row), vocab)
+
+
+def run_trace(eng, reqs, seed: int, live_cap: int = 8, realtime: bool = False,
+              record_tokens: bool = False, max_prefill_tokens: int | None = None,
+              slab_margin: int = 8) -> TraceResult:
+    """Serve `reqs` on `eng` (an ``Engine``) with continuous batching; see the module text."""
+    dev = eng.weights.device
+    vocab = eng.shape.vocab
+    stream = eng.stream
+    live_cap = min(live_cap, eng.max_batch)
+    budget = max_prefill_tokens or eng.max_prefill_tokens
+    order = sorted(range(len(reqs)), key=lambda i: (0.0 if not realtime else reqs[i].arrival_s, i))
+    pending = deque(order)
+    live = []  # per row: [request index, slab, tokens produced, time of last token]
+    res = TraceResult()
+    tok = torch.zeros(eng.max_batch, dtype=torch.int32, device=dev)  # the live rows' last tokens
+    nxt = torch.zeros(eng.max_batch, dtype=torch.int32, device=dev)
+    t0 = time.perf_counter()
+
+    def now() -> float:
+        return time.perf_counter() - t0
+
+    def arrived(i) -> bool:
+        return not realtime or reqs[i].arrival_s <= now()
+
+    while pending or live:
+        # 1. retire finished rows; the others keep their order and their last tokens
+        keep = [k for k, r in enumerate(live) if r[2] < reqs[r[0]].output_len]
+        if len(keep) < len(live):
+            eng.retire([r[1] for k, r in enumerate(live) if r[2] >= reqs[r[0]].output_len])
+            if keep:
+                tok[:len(keep)] = tok[torch.tensor(keep, dtype=torch.long, device=dev)]
+            live = [live[k] for k in keep]
+        # 2. admit arrivals
+        if realtime and not live and pending and not arrived(pending[0]):
+            time.sleep(max(0.0, reqs[pending[0]].arrival_s - now()))
+        admit = []
+        total = 0
+        while (pending and len(live) + len(admit) < live_cap and arrived(pending[0])
+               and total + reqs[pending[0]].prompt_len <= budget):
+            i = pending.popleft()
+            admit.append(i)
+            total += reqs[i].prompt_len
+        if admit:
+            slabs = [eng.kv_slab_alloc(reqs[i].prompt_len + reqs[i].output_len + slab_margin)
+                     for i in admit]
+            host = np.concatenate([prompt_tokens(reqs[i], seed, vocab) for i in admit])
+            dtok = torch.from_numpy(host.astype(np.int32)).to(dev, non_blocking=False)
+            first = torch.empty(len(admit), dtype=torch.int32, device=dev)
+            ta = time.perf_counter()
+            eng.prefill_segmented(slabs, [reqs[i].prompt_len for i in admit], dtok, None, first)
+            stream.synchronize()
+            tb = time.perf_counter()
+            res.prefill_tokens += total
+            res.prefill_s += tb - ta
+            firsts = first.cpu().tolist() if record_tokens else None
+            # the new rows join the live set; their first token is the next step's input
+            rows_before = len(live)
+            for k, i in enumerate(admit):
+                live.append([i, slabs[k], 1, tb - t0])
+                res.ttft_s[i] = (tb - t0) - (reqs[i].arrival_s if realtime else 0.0)
+                res.generated += 1
+                if record_tokens:
+                    res.tokens[i] = [firsts[k]]
+            tok[rows_before:rows_before + len(admit)] = first
+            continue  # a boundary again: new rows may already be complete (output_len 1)
+        if not live:
+            continue
+        # 3. one decode step over the live rows
+        B = len(live)
+        ta = time.perf_counter()
+        eng.decode_step_batch([r[1] for r in live], tok[:B], None, nxt[:B])
+        stream.synchronize()
+        tb = time.perf_counter()
+        res.steps += 1
+        res.step_rows.append(B)
+        res.step_s.append(tb - ta)
+        # row r reads positions [0, prompt + produced] (the new token is appended first)
+        res.step_kv_tokens.append(sum(reqs[r[0]].prompt_len + r[2] for r in live))
+        step_tokens = nxt[:B].cpu().tolist() if record_tokens else None
+        for k, r in enumerate(live):
+            r[2] += 1
+            res.generated += 1
+            if record_tokens:
+                res.tokens[r[0]].append(step_tokens[k])
+            if r[2] >= reqs[r[0]].output_len:
+                n = reqs[r[0]].output_len
+                first_t = res.ttft_s[r[0]] + (reqs[r[0]].arrival_s if realtime else 0.0)
+                res.tpot_s[r[0]] = ((tb - t0) - first_t) / max(1, n - 1)
+        # the next step's inputs are this step's outputs, row for row (finished rows leave at
+        # the boundary)
+        tok[:B] = nxt[:B]
+    res.wall_s = now()
+    return res
+
+
+def percentiles(values, qs=(50, 95)):
+    v = np.asarray(list(values), dtype=np.float64)
+    if v.size == 0:
+        return {f"p{q}": None for q in qs}
+    return {f"p{q}": float(np.percentile(v, q)) for q in qs}

@@ -1,0 +1,58 @@
+"""Continuous batching over a small request trace on the tiny decoder: requests are admitted
+by segmented prefill at step boundaries, share decode steps with whatever else is live, and
+leave when done.  Each request's greedy tokens must equal the oracle's for that request alone
+(prefill of its prompt, then greedy decode); where they differ, the oracle's top two logits
+must be within the bf16 tolerance (a near-tie), after which the trajectories may part."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from continuous_batching_transformer_gb300.model import DeviceWeights, Engine
+from continuous_batching_transformer_gb300.trace import prompt_tokens, run_trace
+from synth.recipes import TINY, Request
+from tests.gpu_harness import TOL, ensure_built
+
+pytestmark = pytest.mark.gpu
+
+# (arrival, prompt length, output length, token stream): more requests than batch slots, so
+# rows join and leave mid-trace; one request ends on its prefill token
+REQS = [Request(0.0, 5, 4, 11), Request(0.0, 17, 7, 12), Request(0.0, 32, 2, 13),
+        Request(0.0, 9, 9, 14), Request(0.0, 24, 5, 15), Request(0.0, 3, 1, 16),
+        Request(0.0, 12, 6, 17)]
+
+
+def oracle_greedy(om, req, seed):
+    toks = prompt_tokens(req, seed, TINY.vocab)
+    cache = oracle.KVCache(TINY, req.prompt_len + req.output_len + 2)
+    ref = oracle.prefill_segmented(om, [cache], [req.prompt_len], toks)
+    logits = [ref[0]]
+    out = [oracle.argmax(ref[0])]
+    while len(out) < req.output_len:
+        r = oracle.decode_step_batch(om, [cache], np.array([out[-1]], dtype=np.int32))
+        logits.append(r[0])
+        out.append(oracle.argmax(r[0]))
+    return out, logits
+
+
+def test_trace_rows_match_oracle():
+    ensure_built()
+    dev = torch.device("cuda:0")
+    w = DeviceWeights(TINY, dev)
+    om = oracle.OracleModel(TINY)
+    eng = Engine(w, arena_bytes=32 << 20, max_batch=3, max_prefill_tokens=64)
+    res = run_trace(eng, REQS, seed=0, live_cap=3, record_tokens=True)
+    assert eng.device_error() == (0, 0)
+    assert res.generated == sum(r.output_len for r in REQS)
+    assert eng.stats().live_slabs == 0  # every request's slab was retired
+    assert max(res.step_rows) == 3 and min(res.step_rows) >= 1
+    for i, req in enumerate(REQS):
+        got = res.tokens[i]
+        assert len(got) == req.output_len
+        want, logits = oracle_greedy(om, req, 0)
+        for t, (g, wv) in enumerate(zip(got, want)):
+            if g != wv:
+                top2 = np.sort(logits[t])[-2:]
+                assert top2[1] - top2[0] < TOL["bf16"], f"request {i} token {t}: {g} != {wv}"
+                break
+    eng.close()
