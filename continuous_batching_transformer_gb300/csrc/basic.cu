@@ -156,7 +156,7 @@ void launch_rope_table(const QueryRow* rows, int n, int head_dim, double theta, 
 // ---- RoPE q, k in place at the token's position; append k, v to its own slab at pos ------
 __global__ void k_rope_append(float* qkv, const QueryRow* rows, int layer, int n_heads,
                               int n_kv_heads, int head_dim, const float* cosv, const float* sinv,
-                              uint16_t* arena, uint8_t* qtile) {
+                              uint16_t* arena, uint8_t* qtile, uint16_t* qb, int q_lo_row) {
   pdl_wait();
   pdl_launch();
   int t = blockIdx.x;
@@ -179,6 +179,18 @@ __global__ void k_rope_append(float* qkv, const QueryRow* rows, int layer, int n
       uint16_t* kd = arena + k_index(r, layer, h - n_heads, r.pos, 0, n_kv_heads, head_dim);
       kd[i] = f32_to_bf16(ra);
       kd[i + half] = f32_to_bf16(rb);
+    } else if (qb) {
+      // the prefill attention's Q operand, scaled by 1/sqrt(head_dim): bf16 high parts at row
+      // t, the bf16 rounding of the remainders at row q_lo_row + t
+      const float qs = rsqrtf((float)head_dim);
+      const float a = ra * qs, b = rb * qs;
+      const uint16_t ah = f32_to_bf16(a), bh = f32_to_bf16(b);
+      uint16_t* hi = qb + (size_t)t * qd + (size_t)h * head_dim;
+      uint16_t* lo = hi + (size_t)q_lo_row * qd;
+      hi[i] = ah;
+      hi[i + half] = bh;
+      lo[i] = f32_to_bf16(a - bf16_to_f32(ah));
+      lo[i + half] = f32_to_bf16(b - bf16_to_f32(bh));
     } else if (qtile) {
       // the decode attention's Q operand of this row and kv head: [16 rows][head_dim] bf16 in
       // the MMA's swizzled layout; row j < G holds the hi part of q head g*G + j scaled by
@@ -205,10 +217,11 @@ __global__ void k_rope_append(float* qkv, const QueryRow* rows, int layer, int n
 
 void launch_rope_append(float* qkv, const QueryRow* rows, int n, int layer, int n_heads,
                         int n_kv_heads, int head_dim, const float* cosv, const float* sinv,
-                        uint16_t* arena, uint8_t* qtile, cudaStream_t s) {
+                        uint16_t* arena, uint8_t* qtile, uint16_t* qb, int q_lo_row,
+                        cudaStream_t s) {
   if (n <= 0) return;
   launch_pdl(k_rope_append, dim3(n), dim3(256), 0, s, qkv, rows, layer, n_heads, n_kv_heads,
-             head_dim, cosv, sinv, arena, qtile);
+             head_dim, cosv, sinv, arena, qtile, qb, q_lo_row);
 }
 
 // ---- V of one layer between the plain [kv head][position][head_dim] layout and a slab ------

@@ -102,6 +102,14 @@ struct cbt_engine {
   size_t att_items_cap = 0;
   int item_total = 0;
   uint8_t* qtile = nullptr;  // [max_batch][Hkv] Q operand images of the decode attention
+  // tensor-core prefill attention: bf16 q of the call's tokens, its TMA map, the work units
+  uint16_t* qb = nullptr;  // [2][qb_rows][qd]: high parts, then remainders
+  int qb_rows = 0;
+  CUtensorMap q_map;
+  std::vector<PrefillUnit> hunits;
+  PrefillUnit* pf_units = nullptr;
+  size_t pf_cap = 0;
+  int pf_n = 0;
   float* ss = nullptr;       // [d/128][ss_ld] per-tile sums of squares of the residual rows
   int ss_ld = 0;
   // staging buffer for host-side import/export of V
@@ -149,7 +157,7 @@ static void free_scratch(cbt_engine* e) {
                   e->xg,      e->logits,   e->cosv, e->sinv,  e->next_tok, e->last_idx,
                   e->rows,    e->err,      e->act_h, e->act_o, e->act_u,  e->tc_part,
                   e->tc_cnt,  e->items,    e->item_meta, e->att_o, e->att_ml, e->stage,
-                  e->qtile,   e->ss};
+                  e->qtile,   e->ss,       e->qb,     e->pf_units};
   for (void* q : ptrs)
     if (q) cudaFree(q);
 }
@@ -242,7 +250,7 @@ extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_w
     int dev = 0;
     chk(cudaGetDevice(&dev));
     chk(cudaDeviceGetAttribute(&e->num_sms, cudaDevAttrMultiProcessorCount, dev));
-    e->act_rows = std::max(64, T);
+    e->act_rows = std::max(64, 2 * T);  // hi rows, then (prefill) the lo rows from row T
     chk(dmalloc(&e->act_h, (size_t)e->act_rows * std::max(c.d_model, qd), &tot));
     chk(dmalloc(&e->act_o, (size_t)e->act_rows * qd, &tot));
     chk(dmalloc(&e->act_u, (size_t)e->act_rows * c.d_ff, &tot));
@@ -292,6 +300,12 @@ extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_w
       chk(dmalloc(&e->item_meta, (size_t)2 * p->max_batch + 1, &tot));
       const size_t qbytes = (size_t)p->max_batch * c.n_kv_heads * 16 * c.head_dim * 2;
       chk(dmalloc(&e->qtile, qbytes, &tot));
+      e->qb_rows = std::max(T, 128);  // at least one 128-row TMA box
+      const size_t qb_elems = (size_t)2 * e->qb_rows * qd;
+      chk(dmalloc(&e->qb, qb_elems, &tot));
+      if (rc == cudaSuccess) rc = cudaMemsetAsync(e->qb, 0, qb_elems * 2, e->stream);
+      maps_ok = maps_ok && rc == cudaSuccess &&
+                make_tmap_bf16(&e->q_map, e->qb, qd, 2 * e->qb_rows, 64, 128);
       if (rc == cudaSuccess) rc = cudaMemsetAsync(e->qtile, 0, qbytes, e->stream);
       e->ss_ld = std::max(32, p->max_batch);
       chk(dmalloc(&e->ss, (size_t)((c.d_model + 127) / 128) * e->ss_ld, &tot));
@@ -528,9 +542,11 @@ static void projection(cbt_engine* e, const float* x, int n, int K, const cbt_li
   tend(e, t, weight_bytes(c, M, K) + 4.0 * n * K + 4.0 * n * Mo * (epi == EPI_ADD ? 2 : 1));
 }
 
-// Tensor-core path.  Up to 32 rows go through the projections as bf16 hi/lo pairs (lo parts
-// at row BN/2 of the operand buffer); more rows as plain bf16.
-static int tc_lo_rows(int n) { return n <= 32 ? tc_split_bn(n) / 2 : 0; }
+// Tensor-core path: operands are bf16 hi/lo pairs (x = hi + lo).  Up to 32 rows keep their lo
+// parts at row BN/2 of the operand buffer (the MMA's padded N side), more rows at row tmax.
+static int tc_lo_rows(const cbt_engine* e, int n) {
+  return n <= 32 ? tc_split_bn(n) / 2 : e->tmax;
+}
 
 static const CUtensorMap* xmap(cbt_engine* e, const uint16_t* buf, int K, int BN) {
   auto key = std::make_pair(static_cast<const void*>(buf), BN);
@@ -585,7 +601,7 @@ static bool tc_projection(cbt_engine* e, const CUtensorMap& wmap, const CUtensor
     p.ss_out = e->ss;
     p.next_gain = next_gain;
     p.next_act = e->act_h;
-    p.next_lo = split ? BN / 2 : 0;
+    p.next_lo = tc_lo_rows(e, n);
   }
   p.M = M;
   p.K = K;
@@ -596,7 +612,7 @@ static bool tc_projection(cbt_engine* e, const CUtensorMap& wmap, const CUtensor
   p.ldo = ldo;
   p.act = act_out;
   p.act_ld = act_ld;
-  p.act_lo = split ? BN / 2 : 0;
+  p.act_lo = tc_lo_rows(e, n);
   p.part = e->tc_part;
   p.cnt = e->tc_cnt;
   p.err = e->err;
@@ -628,7 +644,7 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
   // decode on the tensor cores folds every RMSNorm into the projection that consumes it:
   // the residual-add epilogues and the embedding leave per-tile sums of squares in e->ss
   const bool fused = tcp && !gather && n <= 32;
-  const int lo = tc_lo_rows(n), lo_out = tc_lo_rows(n_out);
+  const int lo = tc_lo_rows(e, n), lo_out = tc_lo_rows(e, n_out);
   bool ok = true;
   int t = tbegin(e, CBT_KCLASS_OTHER);
   launch_embed(tokens, n, static_cast<const uint16_t*>(e->w.embed), d, c.vocab, e->x, e->err,
@@ -656,9 +672,11 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
     else
       projection(e, e->h, n, d, L.wqkv, qd + 2 * kvd, EPI_STORE, e->qkv);
     t = tbegin(e, CBT_KCLASS_ATTN);
+    const bool tc_prefill = tcp && gather && e->pf_n > 0;
     if (!fused)
       launch_rope_append(e->qkv, e->rows, n, l, c.n_heads, c.n_kv_heads, c.head_dim, e->cosv,
-                         e->sinv, arena, (tcp && !gather) ? e->qtile : nullptr, s);
+                         e->sinv, arena, (tcp && !gather) ? e->qtile : nullptr,
+                         tc_prefill ? e->qb : nullptr, e->qb_rows, s);
     if (tcp && !gather) {  // decode: split-K flash decoding on the tensor cores
       AttnDecodeArgs a{};
       a.qtile = e->qtile;
@@ -679,8 +697,13 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
       a.err = e->err;
       ok &= launch_attn_decode_tc(e->kv_kmap, e->kv_vmap, a, e->num_sms, s);
     } else {
-      launch_attention_naive(e->qkv, e->rows, n, l, c.n_heads, c.n_kv_heads, c.head_dim, max_keys,
-                             arena, e->o, s);
+      if (tc_prefill)  // flash attention per segment on the tensor cores
+        ok &= launch_attn_prefill_tc(e->q_map, e->kv_kmap, e->kv_vmap, e->pf_units, e->pf_n,
+                                     e->qb_rows, l, c.n_heads, c.n_kv_heads, c.head_dim, e->o,
+                                     e->err, e->num_sms, s);
+      else
+        launch_attention_naive(e->qkv, e->rows, n, l, c.n_heads, c.n_kv_heads, c.head_dim,
+                               max_keys, arena, e->o, s);
       if (tcp) launch_f32_to_act(e->o, n, qd, e->act_o, lo, s);
     }
     tend(e, t, attn_bytes);
@@ -862,6 +885,60 @@ extern "C" cbt_status cbt_decode_step_batch(cbt_engine* e, const int32_t* ids, i
   return CBT_OK;
 }
 
+// Work units of the tensor-core prefill attention: per segment, 128-query block and q head,
+// the longest blocks (most key blocks) first so the persistent grid ends evenly.  Copies the
+// list to the device (growing the buffer) on the engine stream; pf_n = 0 leaves the call on
+// the plain attention kernel.
+static cudaError_t plan_prefill_attention(cbt_engine* e, const int32_t* ids, const int32_t* lens,
+                                          int K) {
+  e->pf_n = 0;
+  const int hd = e->cfg.head_dim;
+  if (!e->use_tc || (hd != 64 && hd != 128)) return cudaSuccess;
+  e->hunits.clear();
+  struct Blk {
+    int work;
+    PrefillUnit u;
+  };
+  std::vector<Blk> blks;
+  int tok = 0;
+  for (int s = 0; s < K; ++s) {
+    const Slab& sl = e->slabs[ids[s]];
+    const int L = lens[s];
+    for (int q = 0; q < L; q += 128) {
+      PrefillUnit u{};
+      u.base = (long long)(sl.offset / 2);
+      u.cap = sl.lcap;
+      u.tok0 = tok + q;
+      u.q0 = sl.pos + q;
+      u.nq = std::min(128, L - q);
+      u.len = sl.pos + L;
+      const int work = (u.q0 + u.nq - 1) / 128 + 1;
+      for (int h = 0; h < e->cfg.n_heads; ++h) {
+        u.head = h;
+        blks.push_back(Blk{work, u});
+      }
+    }
+    tok += L;
+  }
+  std::stable_sort(blks.begin(), blks.end(), [](const Blk& a, const Blk& b) { return a.work > b.work; });
+  for (const Blk& b : blks) e->hunits.push_back(b.u);
+  const size_t n = e->hunits.size();
+  cudaError_t rc = cudaSuccess;
+  if (n > e->pf_cap) {
+    rc = cudaStreamSynchronize(e->stream);
+    if (e->pf_units) cudaFree(e->pf_units);
+    e->pf_units = nullptr;
+    e->pf_cap = 0;
+    if (rc == cudaSuccess) rc = cudaMalloc(reinterpret_cast<void**>(&e->pf_units), n * sizeof(PrefillUnit));
+    if (rc != cudaSuccess) return rc;
+    e->pf_cap = n;
+  }
+  rc = cudaMemcpyAsync(e->pf_units, e->hunits.data(), n * sizeof(PrefillUnit),
+                       cudaMemcpyHostToDevice, e->stream);
+  if (rc == cudaSuccess) e->pf_n = (int)n;
+  return rc;
+}
+
 extern "C" cbt_status cbt_prefill_segmented(cbt_engine* e, const int32_t* ids,
                                             const int32_t* lens, int32_t K, const int32_t* tokens,
                                             float* logits, int32_t* next_tokens) {
@@ -897,6 +974,7 @@ extern "C" cbt_status cbt_prefill_segmented(cbt_engine* e, const int32_t* ids,
   if (rc == cudaSuccess)
     rc = cudaMemcpyAsync(e->last_idx, e->hidx.data(), sizeof(int32_t) * K, cudaMemcpyHostToDevice,
                          e->stream);
+  if (rc == cudaSuccess) rc = plan_prefill_attention(e, ids, lens, K);
   if (rc == cudaSuccess)
     rc = forward(e, (int)T, tokens, max_keys, total_keys, true, K, logits, next_tokens);
   if (rc != cudaSuccess) return rc == cudaErrorNotSupported ? CBT_ERR_UNSUPPORTED : CBT_ERR_CUDA;

@@ -19,7 +19,10 @@
 // ((x * g) W^T), so the residual-add epilogue that produces x also writes x * g (the next
 // projection's operand, hi/lo) and x's sums of squares over its 128-row tile; the consuming
 // projection scales each accumulated column by the row's rsqrt(mean(x^2) + eps).
-// Prefill (!SPLIT): plain bf16 activations, N tiles of up to 256 tokens, whole tiles per CTA.
+// Prefill (!SPLIT): N tiles of up to 128 tokens, whole tiles per CTA.  The activations are
+// bf16 hi/lo pairs here too (lo parts at row act_lo + t): each stage carries both operand
+// tiles and the MMA chain runs over both into the same accumulator, so the result is that
+// of the fp32 operand up to the weights' own rounding.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -96,7 +99,8 @@ template <int BN, int STAGES, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     k_tc_linear(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tx,
                 const TcParams p) {
-  constexpr int kXBytes = BN * 128;
+  constexpr int kXTile = BN * 128;                     // one [BN rows][64] operand tile
+  constexpr int kXBytes = SPLIT ? kXTile : 2 * kXTile;  // prefill stages: hi and lo tiles
   constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
   constexpr uint32_t kIdesc = tc::idesc_bf16(128, BN);
   extern __shared__ uint8_t smem_raw[];
@@ -156,9 +160,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto flush_pending = [&]() {
         pdl_wait();
         dep_done = true;
-        for (int i = 0; i < npend; ++i)
+        for (int i = 0; i < npend; ++i) {
           tc::tma_load_2d(sX + pend_st[i] * kXBytes, &tx, &full[pend_st[i]], pend_k[i] * 64,
                           pend_nt[i] * BN, pol_x);
+          if (!SPLIT)
+            tc::tma_load_2d(sX + pend_st[i] * kXBytes + kXTile, &tx, &full[pend_st[i]],
+                            pend_k[i] * 64, p.act_lo + pend_nt[i] * BN, pol_x);
+        }
         npend = 0;
       };
       while (ok && sch.next(p, tile, kb, ke)) {
@@ -176,6 +184,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tma_load_2d(sA + stage * kABytes + 8192, &tw, &full[stage], k * 64, y1, pol_w);
           if (dep_done) {
             tc::tma_load_2d(sX + stage * kXBytes, &tx, &full[stage], k * 64, nt * BN, pol_x);
+            if (!SPLIT)
+              tc::tma_load_2d(sX + stage * kXBytes + kXTile, &tx, &full[stage], k * 64,
+                              p.act_lo + nt * BN, pol_x);
           } else {
             pend_k[npend] = k;
             pend_nt[npend] = nt;
@@ -223,6 +234,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             tc::mma_bf16(d, ad + 2 * kk, xd + 2 * kk, kIdesc, (k > kb || kk > 0) ? 1u : 0u);
+          if (!SPLIT) {  // the lo parts into the same accumulator
+            const uint64_t ld = tc::sdesc_sw128(tc::smem_u32(sX + stage * kXBytes + kXTile));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) tc::mma_bf16(d, ad + 2 * kk, ld + 2 * kk, kIdesc, 1u);
+          }
           tc::mma_commit(&empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
@@ -357,7 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int BN, int STAGES, bool SPLIT>
 cudaError_t launch_inst(const CUtensorMap& tw, const CUtensorMap& tx, const TcParams& p, int grid,
                         cudaStream_t s) {
-  constexpr size_t smem = 1024 + STAGES * (kABytes + BN * 128) + 512 + 128 * 33 * 4 + 256;
+  constexpr size_t smem =
+      1024 + STAGES * (kABytes + BN * 128 * (SPLIT ? 1 : 2)) + 512 + 128 * 33 * 4 + 256;
   static_assert(smem <= 227 * 1024, "shared memory budget");
   auto kern = k_tc_linear<BN, STAGES, SPLIT>;
   cudaError_t rc = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -419,7 +436,7 @@ bool make_tmap_kblocks(CUtensorMap* m, const void* base, uint64_t K, uint64_t ro
 }
 
 int tc_split_bn(int n) { return n <= 8 ? 16 : (n <= 16 ? 32 : 64); }
-int tc_plain_bn(int n) { return n <= 64 ? 64 : (n <= 128 ? 128 : 256); }
+int tc_plain_bn(int n) { return n <= 64 ? 64 : 128; }
 
 // Plan and launch one projection.  p carries shapes, epilogue and outputs; this fills the
 // schedule.  Returns false if the shape is outside what the kernel supports.
@@ -428,6 +445,7 @@ bool launch_tc_linear(const CUtensorMap& tw, const CUtensorMap& tx, TcParams p, 
   if (p.K % 64 || p.K <= 0 || p.n_act <= 0) return false;
   if (p.epi == EPI_SWIGLU && (p.F % 64 || p.M != 2 * p.F)) return false;
   if (!split && p.ss_in) return false;  // the per-column RMSNorm factors exist for decode rows only
+  if (!split && p.act_lo < p.n_act) return false;  // prefill operands carry their lo parts
   p.RB = p.epi == EPI_SWIGLU ? p.F / 64 : (p.M + 127) / 128;
   p.KS = p.K / 64;
   if (split) {
@@ -465,9 +483,8 @@ bool launch_tc_linear(const CUtensorMap& tw, const CUtensorMap& tx, TcParams p, 
   const int tiles = p.RB * p.NT;
   const int G = std::min(tiles, num_sms);
   cudaError_t rc;
-  if (BN == 64) rc = launch_inst<64, 8, false>(tw, tx, p, G, s);
-  else if (BN == 128) rc = launch_inst<128, 6, false>(tw, tx, p, G, s);
-  else if (BN == 256) rc = launch_inst<256, 4, false>(tw, tx, p, G, s);
+  if (BN == 64) rc = launch_inst<64, 6, false>(tw, tx, p, G, s);
+  else if (BN == 128) rc = launch_inst<128, 4, false>(tw, tx, p, G, s);
   else return false;
   return rc == cudaSuccess;
 }

@@ -155,7 +155,27 @@ void launch_rope_table(const QueryRow* rows, int n, int head_dim, double theta, 
 // qtile, also write each row's Q operand images for the decode attention ([n][Hkv][16][hd])
 void launch_rope_append(float* qkv, const QueryRow* rows, int n, int layer, int n_heads,
                         int n_kv_heads, int head_dim, const float* cosv, const float* sinv,
-                        uint16_t* arena, uint8_t* qtile, cudaStream_t s);
+                        uint16_t* arena, uint8_t* qtile, uint16_t* qb, int q_lo_row,
+                        cudaStream_t s);
+// qb (prefill): also the rotated q, scaled by 1/sqrt(head_dim), as a bf16 high part at
+// qb[t][n_heads*head_dim] and the bf16 rounding of the remainder at qb[q_lo_row + t][...]
+
+// ---- tensor-core segmented prefill attention (attn_prefill.cu) ---------------------------------
+// One unit: q head `head` of the 128-query block starting at position q0 of a segment whose
+// keys are positions [0, len) of the slab at (base, cap); its queries are packed tokens
+// [tok0, tok0 + nq).
+struct PrefillUnit {
+  long long base;
+  int cap, tok0, q0, nq, len, head;
+};
+// tq: the bf16 q buffer as [2][q_lo_row][n_heads*head_dim] rows (high parts, then the
+// remainders), box {64, 128}; tk, tv: the KV arena as
+// in the decode attention.  o: fp32 [tokens][n_heads*head_dim], softmax(q.K^T) V of each token
+// over positions [0, its own] of its segment.
+bool launch_attn_prefill_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const PrefillUnit* units, int n_units, int q_lo_row, int layer,
+                            int n_heads, int n_kv_heads, int head_dim, float* o, int* err,
+                            int num_sms, cudaStream_t s);
 // softmax attention of each token over [0, pos] of its own slab
 void launch_attention_naive(const float* qkv, const QueryRow* rows, int n, int layer, int n_heads,
                             int n_kv_heads, int head_dim, int max_keys, const uint16_t* arena,

@@ -1,0 +1,93 @@
+"""GPU parity of segmented prefill with segments longer than one 128-query block: the
+tensor-core flash attention walks several key blocks, ragged tails and grouped-query heads.
+Each case packs several segments into one call, then extends two of them with a second call
+whose segments start mid-block (positions not a multiple of 128), then takes one decode step;
+logits are checked element by element against the CPU oracle (bf16 tolerance 2e-2)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from continuous_batching_transformer_gb300.model import DeviceWeights, Engine
+from synth.recipes import ModelShape
+from tests.gpu_harness import TOL, check_logits, ensure_built, to_dev
+
+pytestmark = pytest.mark.gpu
+
+# head_dim 64 (no grouping) and head_dim 128 (two q heads per kv head)
+SHAPES = {
+    "hd64": ModelShape("prefill-hd64", 2, 256, 4, 4, 64, 768, 1024, 1e-6, 1e4, gain_sigma=0.1),
+    "hd128-gqa": ModelShape("prefill-hd128", 2, 512, 4, 2, 128, 1024, 2048, 1e-5, 1e6,
+                            gain_sigma=0.1),
+}
+# first call: one token, exactly one block, a block plus one, several blocks with a tail
+LENS = [300, 1, 128, 129, 37]
+# second call: extends segments 0 and 3 from positions 300 and 129
+EXT = {0: 150, 3: 70}
+
+
+def seeded_tokens(n: int, seed: int, vocab: int) -> np.ndarray:
+    return np.asarray(np.random.default_rng(seed).integers(0, vocab, n), np.int32)
+
+
+def run_case(shape: ModelShape, lens, ext, cap: int):
+    ensure_built()
+    dev = torch.device("cuda:0")
+    w = DeviceWeights(shape, dev)
+    om = oracle.OracleModel(shape)
+    eng = Engine(w, arena_bytes=256 << 20, max_batch=8,
+                 max_prefill_tokens=max(sum(lens), sum(ext.values())))
+    slabs = [eng.kv_slab_alloc(cap) for _ in lens]
+    caches = [oracle.KVCache(shape, cap) for _ in lens]
+    toks = [seeded_tokens(n, 100 + r, shape.vocab) for r, n in enumerate(lens)]
+    logits = torch.empty((len(lens), shape.vocab), dtype=torch.float32, device=dev)
+    nxt = torch.empty(len(lens), dtype=torch.int32, device=dev)
+    eng.prefill_segmented(slabs, lens, to_dev(np.concatenate(toks), dev), logits, nxt)
+    ref = oracle.prefill_segmented(om, caches, lens, np.concatenate(toks))
+    errs = [check_logits(logits.cpu().numpy(), ref, TOL["bf16"], f"{shape.name} prefill")]
+
+    # second call: segments that start part-way into a key block
+    rows = sorted(ext)
+    more = [seeded_tokens(ext[r], 200 + r, shape.vocab) for r in rows]
+    lg2 = torch.empty((len(rows), shape.vocab), dtype=torch.float32, device=dev)
+    nx2 = torch.empty(len(rows), dtype=torch.int32, device=dev)
+    eng.prefill_segmented([slabs[r] for r in rows], [ext[r] for r in rows],
+                          to_dev(np.concatenate(more), dev), lg2, nx2)
+    ref2 = []
+    for r, t in zip(rows, more):
+        start = caches[r].len
+        n = len(t)
+        want = np.zeros(n, np.int32)
+        want[-1] = 1
+        ref2.append(oracle.forward(om, [caches[r]], np.zeros(n, np.int32),
+                                   np.arange(start, start + n, dtype=np.int32), t, want)[0])
+    errs.append(check_logits(lg2.cpu().numpy(), np.stack(ref2), TOL["bf16"],
+                             f"{shape.name} extension"))
+    for r in rows:
+        assert eng.position(slabs[r]) == lens[r] + ext[r]
+
+    # one decode step over every row reads the prefilled K/V back
+    feed = [oracle.argmax(x) for x in ref]
+    for k, r in enumerate(rows):
+        feed[r] = oracle.argmax(ref2[k])
+    feed = np.asarray(feed, np.int32)
+    eng.decode_step_batch(slabs, to_dev(feed, dev), logits, nxt)
+    ref3 = oracle.decode_step_batch(om, caches, feed)
+    errs.append(check_logits(logits.cpu().numpy(), ref3, TOL["bf16"], f"{shape.name} decode"))
+    assert eng.device_error() == (0, 0)
+    eng.close()
+    return max(errs)
+
+
+@pytest.mark.parametrize("name", sorted(SHAPES))
+def test_prefill_multi_block(name):
+    err = run_case(SHAPES[name], LENS, EXT, cap=512)
+    print(f"{name}: max |logit - oracle| = {err:.3e}")
+
+
+def test_prefill_7b_shape_two_layers():
+    """The 7B widths (d_model 4096, 32 q / 8 kv heads, head_dim 128, SwiGLU 14336, vocab
+    32000) at two layers, so the oracle finishes in seconds."""
+    shape = ModelShape("mistral-7b-shape-2L", 2, 4096, 32, 8, 128, 14336, 32000, 1e-5, 1e6)
+    err = run_case(shape, [300, 129, 40], {0: 100, 1: 27}, cap=512)
+    print(f"7b-shape 2 layers: max |logit - oracle| = {err:.3e}")
