@@ -82,6 +82,13 @@ struct cbt_engine {
   std::vector<LayerMaps> wmaps;     // 64 x 64 boxes (prefill)
   std::vector<LayerMaps> wmaps_kb;  // kCskBlocks 64-column blocks of a 128-row tile per box (decode)
   CUtensorMap lm_map, lm_map_kb;
+  // 4-bit affine weights: native block copies for the tensor-core decode projections
+  struct Q4Layer {
+    uint8_t *qkv = nullptr, *o = nullptr, *gu = nullptr, *d = nullptr;
+  };
+  std::vector<Q4Layer> q4w;
+  uint8_t* q4_lm = nullptr;
+  uint8_t* q4_arena = nullptr;
   int act_rows = 0;
   uint16_t *act_h = nullptr, *act_o = nullptr, *act_u = nullptr;
   std::map<std::pair<const void*, int>, CUtensorMap> xmaps;  // (operand buffer, N tile)
@@ -157,7 +164,7 @@ static void free_scratch(cbt_engine* e) {
                   e->xg,      e->logits,   e->cosv, e->sinv,  e->next_tok, e->last_idx,
                   e->rows,    e->err,      e->act_h, e->act_o, e->act_u,  e->tc_part,
                   e->tc_cnt,  e->items,    e->item_meta, e->att_o, e->att_ml, e->stage,
-                  e->qtile,   e->ss,       e->qb,     e->pf_units};
+                  e->qtile,   e->ss,       e->qb,     e->pf_units, e->q4_arena};
   for (void* q : ptrs)
     if (q) cudaFree(q);
 }
@@ -245,8 +252,10 @@ extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_w
   chk(dmalloc(&e->err, 2, &tot));
   if (rc == cudaSuccess) rc = cudaMemsetAsync(e->err, 0, 2 * sizeof(int), e->stream);
   bool maps_ok = true;
-  if (rc == cudaSuccess && c.weight_format == CBT_WEIGHTS_BF16) {
-    // tensor-core path: weight descriptors, bf16 operand buffers, stream-K scratch
+  const bool bf16w = c.weight_format == CBT_WEIGHTS_BF16;
+  if (rc == cudaSuccess && (bf16w || (c.d_model % 128 == 0 && qd % 128 == 0 && c.d_ff % 128 == 0))) {
+    // tensor-core path: weight descriptors (bf16) or native 4-bit blocks, bf16 operand
+    // buffers, stream-K scratch
     int dev = 0;
     chk(cudaGetDevice(&dev));
     chk(cudaDeviceGetAttribute(&e->num_sms, cudaDevAttrMultiProcessorCount, dev));
@@ -269,16 +278,17 @@ extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_w
       }
     }
     e->wmaps.resize(c.n_layers);
-    for (int l = 0; l < c.n_layers && maps_ok; ++l) {
+    e->wmaps_kb.resize(c.n_layers);
+    e->q4w.resize(c.n_layers);
+    for (int l = 0; l < c.n_layers && maps_ok && bf16w; ++l) {
       const cbt_layer_weights& L = w->layers[l];
       maps_ok = make_tmap_bf16(&e->wmaps[l].qkv, L.wqkv.w, c.d_model, nqkv, 64, 64) &&
                 make_tmap_bf16(&e->wmaps[l].o, L.wo.w, qd, c.d_model, 64, 64) &&
                 make_tmap_bf16(&e->wmaps[l].gu, L.wgu.w, c.d_model, 2 * c.d_ff, 64, 64) &&
                 make_tmap_bf16(&e->wmaps[l].d, L.wd.w, c.d_ff, c.d_model, 64, 64);
     }
-    maps_ok = maps_ok && make_tmap_bf16(&e->lm_map, w->lm_head.w, c.d_model, c.vocab, 64, 64);
-    e->wmaps_kb.resize(c.n_layers);
-    for (int l = 0; l < c.n_layers && maps_ok; ++l) {
+    maps_ok = maps_ok && (!bf16w || make_tmap_bf16(&e->lm_map, w->lm_head.w, c.d_model, c.vocab, 64, 64));
+    for (int l = 0; l < c.n_layers && maps_ok && bf16w; ++l) {
       const cbt_layer_weights& L = w->layers[l];
       maps_ok = make_tmap_kblocks(&e->wmaps_kb[l].qkv, L.wqkv.w, c.d_model, nqkv, 128, kCskBlocks, 0) &&
                 make_tmap_kblocks(&e->wmaps_kb[l].o, L.wo.w, qd, c.d_model, 128, kCskBlocks, 0) &&
@@ -286,8 +296,38 @@ extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_w
                                   c.d_ff) &&
                 make_tmap_kblocks(&e->wmaps_kb[l].d, L.wd.w, c.d_ff, c.d_model, 128, kCskBlocks, 0);
     }
-    maps_ok = maps_ok &&
-              make_tmap_kblocks(&e->lm_map_kb, w->lm_head.w, c.d_model, c.vocab, 128, kCskBlocks, 0);
+    maps_ok = maps_ok && (!bf16w || make_tmap_kblocks(&e->lm_map_kb, w->lm_head.w, c.d_model,
+                                                      c.vocab, 128, kCskBlocks, 0));
+    if (!bf16w && maps_ok && rc == cudaSuccess) {
+      // every 4-bit matrix once into the native block layout of the decode projections
+      struct Mat {
+        const cbt_linear* lin;
+        int M, K, F;
+        uint8_t** dst;
+      };
+      std::vector<Mat> mats;
+      for (int l = 0; l < c.n_layers; ++l) {
+        const cbt_layer_weights& L = w->layers[l];
+        mats.push_back({&L.wqkv, nqkv, c.d_model, 0, &e->q4w[l].qkv});
+        mats.push_back({&L.wo, c.d_model, qd, 0, &e->q4w[l].o});
+        mats.push_back({&L.wgu, 2 * c.d_ff, c.d_model, c.d_ff, &e->q4w[l].gu});
+        mats.push_back({&L.wd, c.d_model, c.d_ff, 0, &e->q4w[l].d});
+      }
+      mats.push_back({&w->lm_head, c.vocab, c.d_model, 0, &e->q4_lm});
+      size_t total = 0;
+      for (const Mat& m : mats) total += q4_native_bytes(m.M, m.K, m.F);
+      chk(dmalloc(&e->q4_arena, total, &tot));
+      size_t off = 0;
+      for (const Mat& m : mats) {
+        if (rc != cudaSuccess || !maps_ok) break;
+        *m.dst = e->q4_arena + off;
+        maps_ok = launch_q4_repack(static_cast<const uint32_t*>(m.lin->w),
+                                   static_cast<const uint16_t*>(m.lin->scales),
+                                   static_cast<const uint16_t*>(m.lin->biases), m.M, m.K, m.F,
+                                   *m.dst, e->stream);
+        off += q4_native_bytes(m.M, m.K, m.F);
+      }
+    }
     // the whole arena seen as K rows (head_dim wide) and as V^T rows (64 keys wide)
     const uint64_t arena_elems = p->kv_arena_bytes / 2;
     maps_ok = maps_ok && arena_elems / 64 < (1ull << 31) &&
@@ -572,7 +612,7 @@ static const CUtensorMap* xmap_kb(cbt_engine* e, const uint16_t* buf, int K, int
 // sums of squares in e->ss.  next_gain (EPI_ADD): also write the updated rows' sums of squares
 // to e->ss and x * next_gain into e->act_h, the operand of the projection that follows.
 static bool tc_projection(cbt_engine* e, const CUtensorMap& wmap, const CUtensorMap& wmap_kb,
-                          const uint16_t* xbuf, int n, int K, int M, Epilogue epi, float* out,
+                          const uint8_t* q4w, const uint16_t* xbuf, int n, int K, int M, Epilogue epi, float* out,
                           int ldo, uint16_t* act_out, int act_ld, bool norm_in = false,
                           const uint16_t* next_gain = nullptr, int layer = 0) {
   const bool split = n <= 32;
@@ -620,9 +660,15 @@ static bool tc_projection(cbt_engine* e, const CUtensorMap& wmap, const CUtensor
   int t = tbegin(e, CBT_KCLASS_PROJ);
   // decode rows: cluster split-K (partial sums meet in distributed shared memory); prefill
   // tokens: whole tiles per CTA
-  bool ok = split ? launch_tc_csk(wmap_kb, *xm, p, BN, e->num_sms, e->stream)
-                  : launch_tc_linear(wmap, *xm, p, split, BN, e->num_sms, e->tc_part_floats,
-                                     e->stream);
+  bool ok;
+  if (e->cfg.weight_format != CBT_WEIGHTS_BF16) {
+    p.wq = q4w;
+    ok = split && launch_q4_csk(*xm, p, BN, e->num_sms, e->stream);
+  } else {
+    ok = split ? launch_tc_csk(wmap_kb, *xm, p, BN, e->num_sms, e->stream)
+               : launch_tc_linear(wmap, *xm, p, split, BN, e->num_sms, e->tc_part_floats,
+                                  e->stream);
+  }
   tend(e, t, weight_bytes(e->cfg, M, K) + 4.0 * n * K + 4.0 * n * Mo * (epi == EPI_ADD ? 2 : 1));
   return ok;
 }
@@ -640,7 +686,8 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
   const double attn_bytes = 2.0 * 2.0 * kvd * (double)total_keys  // K and V read (bf16)
                             + 4.0 * n * (qd + 2 * kvd)              // q, k, v in
                             + 2.0 * 2.0 * n * kvd + 4.0 * n * qd;   // K/V appended, o out
-  const bool tcp = e->use_tc;
+  // 4-bit weights go through the tensor cores for up to 32 rows (the decode projections)
+  const bool tcp = e->use_tc && (e->cfg.weight_format == CBT_WEIGHTS_BF16 || n <= 32);
   // decode on the tensor cores folds every RMSNorm into the projection that consumes it:
   // the residual-add epilogues and the embedding leave per-tile sums of squares in e->ss
   const bool fused = tcp && !gather && n <= 32;
@@ -666,7 +713,7 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
     // decode on the tensor cores rotates q and k, appends K/V and lays out the attention's Q
     // operand in the QKV projection's epilogue; otherwise a separate kernel does it
     if (tcp)
-      ok &= tc_projection(e, e->wmaps[l].qkv, e->wmaps_kb[l].qkv, e->act_h, n, d, qd + 2 * kvd,
+      ok &= tc_projection(e, e->wmaps[l].qkv, e->wmaps_kb[l].qkv, e->q4w[l].qkv, e->act_h, n, d, qd + 2 * kvd,
                           fused ? EPI_QKV : EPI_STORE, e->qkv, qd + 2 * kvd, nullptr, 0, fused,
                           nullptr, l);
     else
@@ -708,7 +755,7 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
     }
     tend(e, t, attn_bytes);
     if (tcp)
-      ok &= tc_projection(e, e->wmaps[l].o, e->wmaps_kb[l].o, e->act_o, n, qd, d, EPI_ADD, e->x, d, nullptr, 0,
+      ok &= tc_projection(e, e->wmaps[l].o, e->wmaps_kb[l].o, e->q4w[l].o, e->act_o, n, qd, d, EPI_ADD, e->x, d, nullptr, 0,
                           false, fused ? fn : nullptr);
     else
       projection(e, e->o, n, qd, L.wo, d, EPI_ADD, e->x);
@@ -719,13 +766,13 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
       tend(e, t, 8.0 * n * d);
     }
     if (tcp) {
-      ok &= tc_projection(e, e->wmaps[l].gu, e->wmaps_kb[l].gu, e->act_h, n, d, 2 * F, EPI_SWIGLU, nullptr, 0,
+      ok &= tc_projection(e, e->wmaps[l].gu, e->wmaps_kb[l].gu, e->q4w[l].gu, e->act_h, n, d, 2 * F, EPI_SWIGLU, nullptr, 0,
                           e->act_u, F, fused);
       // the down projection's epilogue prepares the next layer's (or the final) RMSNorm
       const uint16_t* next_g = l + 1 < c.n_layers
                                    ? static_cast<const uint16_t*>(e->layers[l + 1].attn_norm)
                                    : static_cast<const uint16_t*>(e->w.final_norm);
-      ok &= tc_projection(e, e->wmaps[l].d, e->wmaps_kb[l].d, e->act_u, n, F, d, EPI_ADD, e->x, d, nullptr, 0,
+      ok &= tc_projection(e, e->wmaps[l].d, e->wmaps_kb[l].d, e->q4w[l].d, e->act_u, n, F, d, EPI_ADD, e->x, d, nullptr, 0,
                           false, fused ? next_g : nullptr);
     } else {
       projection(e, e->h, n, d, L.wgu, 2 * F, EPI_SWIGLU, e->act);
@@ -748,7 +795,7 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
   }
   float* lg = logits ? logits : e->logits;
   if (tcp) {
-    if (!tc_projection(e, e->lm_map, e->lm_map_kb, e->act_h, n_out, d, c.vocab, EPI_STORE, lg, c.vocab, nullptr,
+    if (!tc_projection(e, e->lm_map, e->lm_map_kb, e->q4_lm, e->act_h, n_out, d, c.vocab, EPI_STORE, lg, c.vocab, nullptr,
                        0, fused))
       return cudaErrorNotSupported;
   } else {

@@ -23,6 +23,7 @@
 #include <tuple>
 
 #include "kernels.h"
+#include "csk_common.cuh"
 #include "tc_common.cuh"
 #include "tc_epilogue.cuh"
 
@@ -37,39 +38,9 @@ constexpr int kMaxStages = 8;
 constexpr int kMaxSlots = 4;        // tiles one CTA owns in a launch
 constexpr int kSmemBudget = 227 * 1024;
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// address of the same shared-memory location in CTA `rank` of the cluster
-__device__ __forceinline__ uint32_t peer_addr(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-// 16 bytes into a peer's shared memory; completes `bytes` on the peer's mbarrier
-__device__ __forceinline__ void st_async_f4(uint32_t raddr, float a, float b, float c, float d,
-                                            uint32_t rbar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-          raddr),
-      "f"(a), "f"(b), "f"(c), "f"(d), "r"(rbar)
-      : "memory");
-}
-
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  for (uint32_t i = 0; i < tc::kSpinLimit; ++i) {
-    if (tc::mbar_try_wait(bar, parity)) return true;
-    if ((i & 1023) == 1023 && *abort) return false;
-    if (i > 256) __nanosleep(32);
-  }
-  return false;
-}
+using csk::cluster_rank;
+using csk::cluster_sync;
+using csk::wait_or_abort;
 
 __device__ __forceinline__ void report_timeout(const TcParams& p, volatile int* abort, int role) {
   *abort = 1;
@@ -343,49 +314,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       float vals[H];
 #pragma unroll
       for (int n = 0; n < H; ++n) vals[n] = __uint_as_float(raw[n]) + __uint_as_float(raw[n + H]);
-      if (rank == owner) {
-        float sum[H];
-        if (C > 1) {
-          if (!wait_or_abort(&sm.inbox_full[slot], 0, abort_flag)) {
-            report_timeout(p, abort_flag, 5);
-            break;
-          }
-#pragma unroll
-          for (int n = 0; n < H; ++n) sum[n] = 0.f;
-          for (int src = 0; src < C; ++src) {  // rank order: a fixed summation order
-            if (src == (int)rank) {
-#pragma unroll
-              for (int n = 0; n < H; ++n) sum[n] += vals[n];
-            } else {
-              const int from = src - (src > (int)rank);  // sender slots skip the owner
-              const float4* in = reinterpret_cast<const float4*>(
-                  sm.inbox + ((size_t)(slot * (C - 1) + from) * 128 + r) * H);
-#pragma unroll
-              for (int c = 0; c < H / 4; ++c) {
-                const float4 v = in[c];
-                sum[4 * c] += v.x;
-                sum[4 * c + 1] += v.y;
-                sum[4 * c + 2] += v.z;
-                sum[4 * c + 3] += v.w;
-              }
-            }
-          }
-        } else {
-#pragma unroll
-          for (int n = 0; n < H; ++n) sum[n] = vals[n];
-        }
-        finish<H>(p, rb, r, sum, 0, sm.swx, sm.rinv, res, src);
-      } else {
-        // hand this CTA's partial sums of the tile to its owner
-        const int from = (int)rank - ((int)rank > (int)owner);
-        const uint32_t dst = peer_addr(
-            tc::smem_u32(sm.inbox + ((size_t)(slot * (C - 1) + from) * 128 + r) * H), owner);
-        const uint32_t bar = peer_addr(tc::smem_u32(&sm.inbox_full[slot]), owner);
-#pragma unroll
-        for (int c = 0; c < H / 4; ++c)
-          st_async_f4(dst + 16 * c, vals[4 * c], vals[4 * c + 1], vals[4 * c + 2], vals[4 * c + 3],
-                      bar);
+      float sum[H];
+      const int got = csk::combine_partials<H>(vals, sum, sm.inbox, sm.inbox_full, slot, rank,
+                                               owner, C, r, abort_flag);
+      if (got < 0) {
+        report_timeout(p, abort_flag, 5);
+        break;
       }
+      if (got > 0) finish<H>(p, rb, r, sum, 0, sm.swx, sm.rinv, res, src);
     }
     // an owner leaves only after its inbox has been filled (bounded: a peer that gave up sends
     // nothing), so no st.async can land in a CTA that has exited

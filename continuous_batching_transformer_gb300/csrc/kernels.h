@@ -75,6 +75,8 @@ struct TcParams {
   const float* sinv;
   uint16_t* arena;
   uint8_t* qtile;
+  // 4-bit affine weights in the native block layout of gemm_q4.cu (launch_q4_csk only)
+  const uint8_t* wq;
 };
 
 
@@ -110,6 +112,21 @@ bool csk_plan(int RB, int KS, int BN, int num_sms, CskPlan* out);
 // as make_tmap_kblocks(.., BN rows, kCskBlocks, 0).
 bool launch_tc_csk(const CUtensorMap& tw, const CUtensorMap& tx, TcParams p, int BN, int num_sms,
                    cudaStream_t s);
+
+// ---- 4-bit affine decode projections (gemm_q4.cu) --------------------------------------------
+// Native layout: per (128-row tile, 128-column super-block) one block of kQ4BlockBytes (codes
+// as [4][128 rows][16 bytes], then bf16 scale/bias pairs of the block's two 64-column groups).
+constexpr int kQ4BlockBytes = 128 * 64 + 128 * 8;
+// bytes of the native copy of an [M][K] matrix (F > 0: SwiGLU gate/up pair, M = 2F); 0 when K
+// is not a multiple of 128
+size_t q4_native_bytes(int M, int K, int F);
+// write the native copy from the interchange format (cbt_linear: codes [M][K/8] uint32, bf16
+// scales and biases [M][K/64])
+bool launch_q4_repack(const uint32_t* packed, const uint16_t* scales, const uint16_t* biases,
+                      int M, int K, int F, uint8_t* out, cudaStream_t s);
+// y = x W^T over n_act <= BN/2 decode rows (hi/lo operand) with W = p.wq; tx as for
+// launch_tc_csk.  Any TcParams epilogue.
+bool launch_q4_csk(const CUtensorMap& tx, TcParams p, int BN, int num_sms, cudaStream_t s);
 
 // ---- tensor-core decode attention (attn_tc.cu) ------------------------------------------------
 struct AttnDecodeArgs {

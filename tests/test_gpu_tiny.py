@@ -110,3 +110,54 @@ def test_gqa_shape_parity(fmt):
         check_logits(logits.cpu().numpy(), ref, TOL[fmt], f"{fmt} decode {step}")
         feed = np.array([oracle.argmax(r) for r in ref], dtype=np.int32)
     eng.close()
+
+
+@pytest.mark.parametrize("B", [1, 5, 12, 24])
+def test_affine4_decode_operand_widths(B):
+    """4-bit affine weights through the tensor-core projections at every operand width (N
+    tiles of 16, 32 and 64 operand rows): B rows with ragged prompts (each prefilled by its own
+    call, so every call is a skinny one), two greedy steps against the oracle, and the last
+    row's logits equal, bit for bit, to those of the row decoded alone."""
+    ensure_built()
+    shape = ModelShape("gqa-check-affine4", 2, 512, 4, 2, 128, 1024, 2048, 1e-5, 1e6,
+                       gain_sigma=0.1, weight_format="affine4")
+    dev = torch.device("cuda:0")
+    w = DeviceWeights(shape, dev)
+    om = oracle.OracleModel(shape)
+    lens = [1 + (7 * r) % 23 for r in range(B)]
+    toks = [np.asarray(np.random.default_rng(50 + r).integers(0, shape.vocab, n), np.int32)
+            for r, n in enumerate(lens)]
+
+    def engine_with(rows):
+        eng = Engine(w, arena_bytes=64 << 20, max_batch=32, max_prefill_tokens=64)
+        slabs, firsts = [], []
+        lg = torch.empty((1, shape.vocab), dtype=torch.float32, device=dev)
+        for r in rows:
+            slabs.append(eng.kv_slab_alloc(64))
+            eng.prefill_segmented([slabs[-1]], [lens[r]], to_dev(toks[r], dev), lg)
+            firsts.append(lg.cpu().numpy()[0].copy())
+        return eng, slabs, np.stack(firsts)
+
+    eng, slabs, first = engine_with(range(B))
+    caches = [oracle.KVCache(shape, 64) for _ in lens]
+    ref = oracle.prefill_segmented(om, caches, lens, np.concatenate(toks))
+    check_logits(first, ref, TOL["affine4"], "affine4 prefill")
+    feeds, outs = [], []
+    feed = np.array([oracle.argmax(r) for r in ref], dtype=np.int32)
+    logits = torch.empty((B, shape.vocab), dtype=torch.float32, device=dev)
+    for step in range(2):
+        eng.decode_step_batch(slabs, to_dev(feed, dev), logits)
+        got = logits.cpu().numpy().copy()
+        ref = oracle.decode_step_batch(om, caches, feed)
+        check_logits(got, ref, TOL["affine4"], f"affine4 B={B} decode {step}")
+        feeds.append(feed)
+        outs.append(got)
+        feed = np.array([oracle.argmax(r) for r in ref], dtype=np.int32)
+    assert eng.device_error() == (0, 0)
+    eng.close()
+    solo, s1, _ = engine_with([B - 1])
+    lg1 = torch.empty((1, shape.vocab), dtype=torch.float32, device=dev)
+    for step in range(2):
+        solo.decode_step_batch(s1, to_dev(feeds[step][B - 1:], dev), lg1)
+        np.testing.assert_array_equal(lg1.cpu().numpy()[0], outs[step][B - 1])
+    solo.close()
