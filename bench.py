@@ -46,8 +46,10 @@ def measured_traffic(kind: str):
     import hashlib
     try:
         info = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))[kind]
-        src = open(os.path.join(ROOT, info["source"]), "rb").read()
-        if hashlib.sha256(src).hexdigest() != info["sha256"]:
+        h = hashlib.sha256()
+        for f in info.get("sources", [info.get("source")]):
+            h.update(open(os.path.join(ROOT, f), "rb").read())
+        if h.hexdigest() != info["sha256"]:
             return None
         return info["dram_bytes_per_launch"]
     except Exception:
@@ -299,7 +301,8 @@ def gpu_arm(args, rank: int, world: int):
                          "frac": achieved / hbm_peak if achieved else None,
                          "share_of_step": proj_ms / kt_ms if kt_ms > 0 else None,
                          "launch_groups": proj_n, "timed_steps": KT,
-                         "traffic": measured_traffic("projection")},
+                         "traffic": measured_traffic("projection" if wl.shape.weight_format == "bf16"
+                                                     else "projection_affine4")},
             "attention_roofline": {"kernel": "RoPE + KV append + split-K decode attention + merge",
                                    "bound": "hbm", "achieved": attn_gbs, "peak": hbm_peak,
                                    "unit": "GB/s",
