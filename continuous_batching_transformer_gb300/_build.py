@@ -17,8 +17,12 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libcbt.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE,
-                     "-I" + CSRC, "--expt-relaxed-constexpr"]
+# -fmad=false: a row's result must not depend on how many rows share the step, and the
+# kernels are instantiated per operand width; left free, the compiler contracts a*b + c into
+# a fused multiply-add differently in different instantiations (seen: the hi/lo split of an
+# epilogue's output), so every fused multiply-add in the sources is an explicit fmaf.
+NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-Xcompiler", "-fPIC",
+                     "-I" + INCLUDE, "-I" + CSRC, "--expt-relaxed-constexpr"]
 
 
 def _sources():

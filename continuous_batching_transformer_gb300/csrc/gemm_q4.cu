@@ -4,8 +4,9 @@
 // The codes enter the MMA as exact integers, so no dequantised weight is ever rounded:
 //   * a converter warp group unpacks each 128-row x 128-column block of codes from shared
 //     memory into tensor memory as bf16 (128 + q), two per 32-bit column -- the layout in which
-//     tcgen05.mma reads its A operand from TMEM -- and adds up the operand's 64-column groups
-//     (sum_k x[k] of each operand row) on the CUDA cores;
+//     tcgen05.mma reads its A operand from TMEM;
+//   * the MMA warps add up the operand's 64-column groups (sum_k x[k] of each operand row) on
+//     the CUDA cores before issuing the stage's MMAs;
 //   * each group of 64 columns is its own MMA chain (codes x operand) into a ring of TMEM
 //     accumulators;
 //   * the epilogue warps fold every group in with its scale and bias, in fp32:
@@ -14,7 +15,7 @@
 // the fp32 operand and the exactly dequantised weights, up to fp32 accumulation.
 // A 4-bit block carries four times the weights of a bf16 one per byte, so a stage needs four
 // times the MMAs per byte streamed; one thread issues a tcgen05.mma only every ~60 ns, so three
-// warps issue them, taking the stages in turn.
+// warps issue them, taking the stages in turn, and eight warps share the unpacking.
 //
 // Everything else is the cluster split-K of gemm_csk.cu: tile t belongs to cluster t % NC, rank
 // r of the cluster streams super-blocks [r SB / C, (r + 1) SB / C) of each of its tiles, the
@@ -49,9 +50,10 @@ using csk::wait_or_abort;
 using tcepi::finish;
 using tcepi::load_residual;
 
-constexpr int kMmaWarps = 3;  // MMA issuers, taking the stages in turn
-constexpr int kConvWarp0 = 1 + kMmaWarps, kEpiWarp0 = kConvWarp0 + 4;
-constexpr int kThreads = 32 * (kEpiWarp0 + 4);  // TMA, MMA issuers, 4 converters, 4 epilogue
+constexpr int kMmaWarps = 3;  // MMA issuers (and operand group sums), taking stages in turn
+constexpr int kConvWarps = 8;  // two per TMEM lane quarter, one 64-column group each
+constexpr int kConvWarp0 = 1 + kMmaWarps, kEpiWarp0 = kConvWarp0 + kConvWarps;
+constexpr int kThreads = 32 * (kEpiWarp0 + 4);  // TMA, MMA issuers, converters, 4 epilogue
 constexpr int kNK = 2;         // 64-column groups per stage
 constexpr int kCodeBytes = 128 * 64;
 constexpr int kWBytes = kQ4BlockBytes;  // codes + scales/biases of one stage
@@ -80,7 +82,7 @@ __device__ __forceinline__ void report_timeout(const TcParams& p, volatile int* 
 
 struct Smem {
   uint8_t *x, *w;
-  float* xs;  // [stages][kNK][BN]: each operand row's sum over each 64-column group
+  float* xs;  // [stages][kNK][BN/2]: each operand row's sum (hi + lo) over each group
   float *inbox, *swx, *rinv;
   float *cosv, *sinv;
   QueryRow* rows;
@@ -99,7 +101,7 @@ __host__ __device__ constexpr size_t rope_floats() {
 }
 template <int BN>
 __host__ __device__ size_t q4_smem_bytes(const CskPlan& q, bool qkv) {
-  return 1024 + (size_t)q.stages * (kNK * BN * 128 + kWBytes + kNK * BN * 4) +
+  return 1024 + (size_t)q.stages * (kNK * BN * 128 + kWBytes + kNK * (BN / 2) * 4) +
          inbox_floats<BN>(q.C, q.slots) * 4 + (128 * 33 + 32) * 4 +
          (qkv ? rope_floats<BN>() * 4 + 32 * sizeof(QueryRow) : 0) + 640;
 }
@@ -110,7 +112,7 @@ __device__ __forceinline__ Smem carve(uint8_t* smem, const CskPlan& q, bool qkv)
   s.x = smem;  // operand tiles first: each stage's tiles stay 1024-byte aligned (swizzle)
   s.w = s.x + q.stages * kNK * BN * 128;
   s.xs = reinterpret_cast<float*>(s.w + q.stages * kWBytes);
-  s.inbox = s.xs + q.stages * kNK * BN;
+  s.inbox = s.xs + q.stages * kNK * (BN / 2);
   s.swx = s.inbox + inbox_floats<BN>(q.C, q.slots);
   s.rinv = s.swx + 128 * 33;
   s.cosv = s.rinv + 32;
@@ -168,10 +170,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < S; ++s) {
       tc::mbar_init(&sm.full[s], 1);
       tc::mbar_init(&sm.empty[s], 1 + 4);  // the MMA commit and the four epilogue warps
-      tc::mbar_init(&sm.xsf[s], 4);        // the four converter warps
+      tc::mbar_init(&sm.xsf[s], 1);        // the stage's MMA warp
     }
     for (int a = 0; a < kRA; ++a) {
-      tc::mbar_init(&sm.afull[a], 4);
+      tc::mbar_init(&sm.afull[a], kConvWarps);
       tc::mbar_init(&sm.aempty[a], 1);
     }
     for (int a = 0; a < RG; ++a) {
@@ -235,18 +237,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_wait(&sm.full[i % S], (i / S) & 1);
     }
   } else if (warp <= kMmaWarps) {
+    // ---- MMA warps: stage i goes to warp i % kMmaWarps.  The whole warp adds up the stage's
+    // operand groups (row n's hi and lo parts, 16-byte chunks, 8 lanes a row), then lane 0
+    // issues the stage's MMAs.
     const int mw = warp - 1;
-    if (lane == 0) {  // ---- MMA issuers: stage i goes to issuer i % kMmaWarps
-      for (int i = mw; i < nst; i += kMmaWarps) {
-        const int stage = i % S, as = i % kRA;
-        if (!wait_or_abort(&sm.full[stage], (i / S) & 1, abort_flag) ||
-            !wait_or_abort(&sm.afull[as], (i / kRA) & 1, abort_flag)) {
+    for (int i = mw; i < nst; i += kMmaWarps) {
+      const int stage = i % S, as = i % kRA;
+      if (!wait_or_abort(&sm.full[stage], (i / S) & 1, abort_flag)) {
+        if (lane == 0) report_timeout(p, abort_flag, 2);
+        break;
+      }
+      float* xs = sm.xs + stage * kNK * H;
+#pragma unroll
+      for (int jj = 0; jj < kNK; ++jj) {
+        const uint8_t* tile = sm.x + stage * stage_x + jj * kXBytes;
+#pragma unroll
+        for (int e = 0; e < H / 4; ++e) {  // H rows x 8 chunks = 8H pairs, 32 lanes
+          const int pidx = lane + 32 * e, row = pidx >> 3, c = pidx & 7, lo = row + H;
+          const uint4 v = *reinterpret_cast<const uint4*>(tile + row * 128 + ((c ^ (row & 7)) << 4));
+          const uint4 u = *reinterpret_cast<const uint4*>(tile + lo * 128 + ((c ^ (lo & 7)) << 4));
+          float sum = ((bf16_lo(v.x) + bf16_hi(v.x)) + (bf16_lo(v.y) + bf16_hi(v.y))) +
+                      ((bf16_lo(v.z) + bf16_hi(v.z)) + (bf16_lo(v.w) + bf16_hi(v.w)));
+          sum += ((bf16_lo(u.x) + bf16_hi(u.x)) + (bf16_lo(u.y) + bf16_hi(u.y))) +
+                 ((bf16_lo(u.z) + bf16_hi(u.z)) + (bf16_lo(u.w) + bf16_hi(u.w)));
+          sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+          sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+          sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+          if (c == 0) xs[jj * H + row] = sum;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&sm.xsf[stage]);
+      bool ok = true;
+      if (lane == 0) {
+        if (!wait_or_abort(&sm.afull[as], (i / kRA) & 1, abort_flag)) {
           report_timeout(p, abort_flag, 2);
-          break;
+          ok = false;
         }
         tc::tc_fence_after();
-        bool ok = true;
-        for (int jj = 0; jj < kNK; ++jj) {
+        for (int jj = 0; jj < kNK && ok; ++jj) {
           const int g = i * kNK + jj, slot = g % RG;
           if (!wait_or_abort(&sm.acce[slot], ((g / RG) & 1) ^ 1, abort_flag)) {
             report_timeout(p, abort_flag, 3);
@@ -262,19 +291,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mma_bf16_ta(dq, acol + 8 * kk, xd + 2 * kk, kIdesc, kk > 0 ? 1u : 0u);
           tc::mma_commit(&sm.accf[slot]);
         }
-        if (!ok) break;
-        tc::mma_commit(&sm.aempty[as]);
-        tc::mma_commit(&sm.empty[stage]);
+        if (ok) {
+          tc::mma_commit(&sm.aempty[as]);
+          tc::mma_commit(&sm.empty[stage]);
+        }
       }
-      // all MMAs of this thread complete before TMEM is released
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+    }
+    // all MMAs of this thread complete before TMEM is released
+    if (lane == 0) {
       tc::mma_commit(&sm.done[mw]);
       tc::mbar_wait(&sm.done[mw], 0);
     }
   } else if (warp < kEpiWarp0) {
-    // ---- converters: codes of tile row r into the A ring in TMEM, then the operand's group sums
-    const int qd = warp & 3;
+    // ---- converters: warp (quarter qd, group half) unpacks columns [64 half, 64 half + 64) of
+    // tile rows 32 qd .. 32 qd + 31 into the A ring in TMEM
+    const int qd = warp & 3, half = (warp - kConvWarp0) >> 2;
     const int r = qd * 32 + lane;
-    const int t = (warp - kConvWarp0) * 32 + lane;  // 0..127 over the four warps
     const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16);
     for (int i = 0; i < nst; ++i) {
       const int stage = i % S, as = i % kRA;
@@ -284,43 +317,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       const uint8_t* codes = sm.w + stage * kWBytes + r * 16;
+      uint32_t a[32];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {  // columns [64 half, 64 half + 64): one group
-        uint32_t a[32];
+      for (int cc = 0; cc < 2; ++cc) {
+        const uint4 v = *reinterpret_cast<const uint4*>(codes + (2 * half + cc) * 2048);
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const uint4 v = *reinterpret_cast<const uint4*>(codes + (2 * half + cc) * 2048);
-          const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+        for (int k = 0; k < 4; ++k)
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-#pragma unroll
-            for (int pp = 0; pp < 4; ++pp) a[cc * 16 + k * 4 + pp] = unpack_pair(wv[k], pp);
-        }
-        tc::tmem_st32(lane_base + (uint32_t)(as * 64 + half * 32), a);
+          for (int pp = 0; pp < 4; ++pp) a[cc * 16 + k * 4 + pp] = unpack_pair(wv[k], pp);
       }
+      tc::tmem_st32(lane_base + (uint32_t)(as * 64 + half * 32), a);
       tc::tmem_st_wait();
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sm.afull[as]);
-      // sum over each group of each operand row: (row, 16-byte chunk) pairs, 8 lanes a row
-      float* xs = sm.xs + stage * kNK * BN;
-#pragma unroll
-      for (int jj = 0; jj < kNK; ++jj) {
-        const uint8_t* tile = sm.x + stage * stage_x + jj * kXBytes;
-#pragma unroll
-        for (int e = 0; e < BN / 16; ++e) {
-          const int pidx = t + 128 * e, row = pidx >> 3, c = pidx & 7;
-          const uint4 v = *reinterpret_cast<const uint4*>(tile + row * 128 + ((c ^ (row & 7)) << 4));
-          float sum = bf16_lo(v.x) + bf16_hi(v.x) + bf16_lo(v.y) + bf16_hi(v.y) + bf16_lo(v.z) +
-                      bf16_hi(v.z) + bf16_lo(v.w) + bf16_hi(v.w);
-          sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-          sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-          sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-          if (c == 0) xs[jj * BN + row] = sum;
-        }
-      }
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&sm.xsf[stage]);
     }
   } else {  // ---- epilogue warps: TMEM lanes 32q .. 32q + 31 = tile rows
     pdl_wait();
@@ -374,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint2 sbw =
             *reinterpret_cast<const uint2*>(sm.w + stage * kWBytes + kCodeBytes + r * 8);
         const uint32_t sbv[2] = {sbw.x, sbw.y};
-        const float* xs = sm.xs + stage * kNK * BN;
+        const float* xs = sm.xs + stage * kNK * H;
 #pragma unroll
         for (int jj = 0; jj < kNK; ++jj) {
           const int g = i * kNK + jj, slot = g % RG;
@@ -398,11 +409,19 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc::tmem_ld8(ta + H + c0, ql);
             }
             tc::tmem_ld_wait();
+            float xv[CH];
+#pragma unroll
+            for (int n = 0; n < CH; n += 4) {
+              const float4 f = *reinterpret_cast<const float4*>(xs + jj * H + c0 + n);
+              xv[n] = f.x;
+              xv[n + 1] = f.y;
+              xv[n + 2] = f.z;
+              xv[n + 3] = f.w;
+            }
 #pragma unroll
             for (int n = 0; n < CH; ++n) {
               const float vq = __uint_as_float(qh[n]) + __uint_as_float(ql[n]);
-              const float v1 = xs[jj * BN + c0 + n] + xs[jj * BN + H + c0 + n];
-              y[c0 + n] = fmaf(s, vq, fmaf(b1, v1, y[c0 + n]));
+              y[c0 + n] = fmaf(s, vq, fmaf(b1, xv[n], y[c0 + n]));
             }
           }
           tc::tc_fence_before();
