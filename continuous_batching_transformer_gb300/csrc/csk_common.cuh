@@ -32,6 +32,16 @@ __device__ __forceinline__ void st_async_f4(uint32_t raddr, float a, float b, fl
       : "memory");
 }
 
+// the same, suspending between polls instead of spinning
+__device__ __forceinline__ bool wait_or_abort_sleep(uint64_t* bar, uint32_t parity,
+                                                    volatile int* abort) {
+  for (uint32_t i = 0; i < (1u << 23); ++i) {
+    if (tc::mbar_try_wait_sleep(bar, parity, 1000)) return true;
+    if ((i & 63) == 63 && *abort) return false;
+  }
+  return false;
+}
+
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
   for (uint32_t i = 0; i < tc::kSpinLimit; ++i) {
     if (tc::mbar_try_wait(bar, parity)) return true;

@@ -5,8 +5,8 @@
 //   * a converter warp group unpacks each 128-row x 128-column block of codes from shared
 //     memory into tensor memory as bf16 (128 + q), two per 32-bit column -- the layout in which
 //     tcgen05.mma reads its A operand from TMEM;
-//   * the MMA warps add up the operand's 64-column groups (sum_k x[k] of each operand row) on
-//     the CUDA cores before issuing the stage's MMAs;
+//   * the same warps add up the operand's 64-column groups (sum_k x[k] of each operand row) on
+//     the CUDA cores;
 //   * each group of 64 columns is its own MMA chain (codes x operand) into a ring of TMEM
 //     accumulators;
 //   * the epilogue warps fold every group in with its scale and bias, in fp32:
@@ -14,8 +14,12 @@
 // The operand is the bf16 hi/lo pair of the other decode projections, so the result is that of
 // the fp32 operand and the exactly dequantised weights, up to fp32 accumulation.
 // A 4-bit block carries four times the weights of a bf16 one per byte, so a stage needs four
-// times the MMAs per byte streamed; one thread issues a tcgen05.mma only every ~60 ns, so three
-// warps issue them, taking the stages in turn, and eight warps share the unpacking.
+// times the MMAs per byte streamed; one thread issues a tcgen05.mma only every ~60 ns, so two
+// warps issue them (one per stage parity), and eight warps unpack.  An
+// mbarrier wait tells phases apart only by parity, so a waiter that could run two phases ahead
+// of a barrier would misread it: every barrier instance is used by its waiters in order (the
+// issuers of one parity touch only the stages, A slots and accumulator slots of that parity,
+// which needs an even pipeline depth).
 //
 // Everything else is the cluster split-K of gemm_csk.cu: tile t belongs to cluster t % NC, rank
 // r of the cluster streams super-blocks [r SB / C, (r + 1) SB / C) of each of its tiles, the
@@ -46,12 +50,16 @@ namespace {
 
 using csk::cluster_rank;
 using csk::cluster_sync;
-using csk::wait_or_abort;
 using tcepi::finish;
+// every wait of this kernel suspends instead of spinning: most warps wait most of the time
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  return csk::wait_or_abort_sleep(bar, parity, abort);
+}
 using tcepi::load_residual;
 
-constexpr int kMmaWarps = 3;  // MMA issuers (and operand group sums), taking stages in turn
+constexpr int kMmaWarps = 2;   // MMA issuers: warp par takes the stages of parity par
 constexpr int kConvWarps = 8;  // two per TMEM lane quarter, one 64-column group each
+// 15 warps: at most four share an SM sub-partition's 16 K registers, so 128 per thread
 constexpr int kConvWarp0 = 1 + kMmaWarps, kEpiWarp0 = kConvWarp0 + kConvWarps;
 constexpr int kThreads = 32 * (kEpiWarp0 + 4);  // TMA, MMA issuers, converters, 4 epilogue
 constexpr int kNK = 2;         // 64-column groups per stage
@@ -68,12 +76,6 @@ template <int BN>
 __host__ __device__ constexpr int acc_slots() {
   return BN == 64 ? 4 : 8;
 }
-// The issuers take stages out of order, and an mbarrier wait tells phases apart only by
-// parity, so an issuer must never find an accumulator slot two uses behind.  A slot returns
-// every slots / kNK stages, so its use two back belongs to the stage 2 * slots / kNK = slots
-// stages earlier (kNK = 2); a stage is issued only after it was loaded, and it was loaded only
-// after the epilogue had finished the stage `stages` earlier.  Hence stages <= slots.
-__host__ __device__ constexpr int max_stages_for_slots(int slots) { return slots; }
 
 __device__ __forceinline__ void report_timeout(const TcParams& p, volatile int* abort, int role) {
   *abort = 1;
@@ -169,8 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       tc::mbar_init(&sm.full[s], 1);
-      tc::mbar_init(&sm.empty[s], 1 + 4);  // the MMA commit and the four epilogue warps
-      tc::mbar_init(&sm.xsf[s], 1);        // the stage's MMA warp
+      tc::mbar_init(&sm.empty[s], 1 + 4);     // the stage's MMA commit, the epilogue warps
+      tc::mbar_init(&sm.xsf[s], kConvWarps);  // each converter warp's rows of the group sums
     }
     for (int a = 0; a < kRA; ++a) {
       tc::mbar_init(&sm.afull[a], kConvWarps);
@@ -237,45 +239,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_wait(&sm.full[i % S], (i / S) & 1);
     }
   } else if (warp <= kMmaWarps) {
-    // ---- MMA warps: stage i goes to warp i % kMmaWarps.  The whole warp adds up the stage's
-    // operand groups (row n's hi and lo parts, 16-byte chunks, 8 lanes a row), then lane 0
-    // issues the stage's MMAs.
-    const int mw = warp - 1;
-    for (int i = mw; i < nst; i += kMmaWarps) {
-      const int stage = i % S, as = i % kRA;
-      if (!wait_or_abort(&sm.full[stage], (i / S) & 1, abort_flag)) {
-        if (lane == 0) report_timeout(p, abort_flag, 2);
-        break;
-      }
-      float* xs = sm.xs + stage * kNK * H;
-#pragma unroll
-      for (int jj = 0; jj < kNK; ++jj) {
-        const uint8_t* tile = sm.x + stage * stage_x + jj * kXBytes;
-#pragma unroll
-        for (int e = 0; e < H / 4; ++e) {  // H rows x 8 chunks = 8H pairs, 32 lanes
-          const int pidx = lane + 32 * e, row = pidx >> 3, c = pidx & 7, lo = row + H;
-          const uint4 v = *reinterpret_cast<const uint4*>(tile + row * 128 + ((c ^ (row & 7)) << 4));
-          const uint4 u = *reinterpret_cast<const uint4*>(tile + lo * 128 + ((c ^ (lo & 7)) << 4));
-          float sum = ((bf16_lo(v.x) + bf16_hi(v.x)) + (bf16_lo(v.y) + bf16_hi(v.y))) +
-                      ((bf16_lo(v.z) + bf16_hi(v.z)) + (bf16_lo(v.w) + bf16_hi(v.w)));
-          sum += ((bf16_lo(u.x) + bf16_hi(u.x)) + (bf16_lo(u.y) + bf16_hi(u.y))) +
-                 ((bf16_lo(u.z) + bf16_hi(u.z)) + (bf16_lo(u.w) + bf16_hi(u.w)));
-          sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-          sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-          sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-          if (c == 0) xs[jj * H + row] = sum;
-        }
-      }
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&sm.xsf[stage]);
+    // ---- MMA warps: warp par issues the eight MMAs (two groups) of stages par, par + 2, ...
+    // Once the stage's codes are in tensor memory (so its loads have landed), lane 0 waits for
+    // the groups' accumulator slots and issues.
+    const int par = warp - 1;
+    if (lane == 0) {
       bool ok = true;
-      if (lane == 0) {
-        if (!wait_or_abort(&sm.afull[as], (i / kRA) & 1, abort_flag)) {
-          report_timeout(p, abort_flag, 2);
-          ok = false;
+      for (int i = par; i < nst && ok; i += 2) {
+        const int stage = i % S, as = i % kRA;
+        // afull first: the converters saw the stage land, so the stage's own full phase is
+        // the one complete now (waited too, for the operand tile's visibility to the MMA)
+        if (!wait_or_abort(&sm.afull[as], (i / kRA) & 1, abort_flag) ||
+            !wait_or_abort(&sm.full[stage], (i / S) & 1, abort_flag)) {
+          report_timeout(p, abort_flag, 3);
+          break;
         }
-        tc::tc_fence_after();
-        for (int jj = 0; jj < kNK && ok; ++jj) {
+        for (int jj = 0; jj < kNK; ++jj) {
           const int g = i * kNK + jj, slot = g % RG;
           if (!wait_or_abort(&sm.acce[slot], ((g / RG) & 1) ^ 1, abort_flag)) {
             report_timeout(p, abort_flag, 3);
@@ -284,28 +263,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc::tc_fence_after();
           const uint32_t dq = tmem + kAccCol + (uint32_t)(slot * BN);
-          const uint64_t xd = tc::sdesc_sw128(tc::smem_u32(sm.x + stage * stage_x + jj * kXBytes));
+          const uint64_t xd =
+              tc::sdesc_sw128(tc::smem_u32(sm.x + stage * stage_x + jj * kXBytes));
           const uint32_t acol = tmem + (uint32_t)(as * 64 + jj * 32);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             tc::mma_bf16_ta(dq, acol + 8 * kk, xd + 2 * kk, kIdesc, kk > 0 ? 1u : 0u);
           tc::mma_commit(&sm.accf[slot]);
         }
-        if (ok) {
-          tc::mma_commit(&sm.aempty[as]);
-          tc::mma_commit(&sm.empty[stage]);
-        }
+        if (!ok) break;
+        tc::mma_commit(&sm.aempty[as]);
+        tc::mma_commit(&sm.empty[stage]);
       }
-      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
-    }
-    // all MMAs of this thread complete before TMEM is released
-    if (lane == 0) {
-      tc::mma_commit(&sm.done[mw]);
-      tc::mbar_wait(&sm.done[mw], 0);
+      // all MMAs of this thread complete before TMEM is released
+      tc::mma_commit(&sm.done[par]);
+      tc::mbar_wait(&sm.done[par], 0);
     }
   } else if (warp < kEpiWarp0) {
     // ---- converters: warp (quarter qd, group half) unpacks columns [64 half, 64 half + 64) of
-    // tile rows 32 qd .. 32 qd + 31 into the A ring in TMEM
+    // tile rows 32 qd .. 32 qd + 31 into the A ring in TMEM, then adds up operand rows
+    // [qd H/4, (qd + 1) H/4) of the group (hi and lo parts, 16-byte chunks, 8 lanes a row)
     const int qd = warp & 3, half = (warp - kConvWarp0) >> 2;
     const int r = qd * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16);
@@ -332,6 +309,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sm.afull[as]);
+      float* xs = sm.xs + stage * kNK * H;
+      const uint8_t* tile = sm.x + stage * stage_x + half * kXBytes;
+#pragma unroll
+      for (int e = 0; e < (2 * H + 31) / 32; ++e) {  // (row, chunk): H/4 x 8
+        const int pidx = lane + 32 * e;
+        const bool valid = pidx < 2 * H;
+        const int row = qd * (H / 4) + (pidx >> 3), c = pidx & 7, lo = row + H;
+        float sum = 0.f;
+        if (valid) {
+          const uint4 v = *reinterpret_cast<const uint4*>(tile + row * 128 + ((c ^ (row & 7)) << 4));
+          const uint4 u = *reinterpret_cast<const uint4*>(tile + lo * 128 + ((c ^ (lo & 7)) << 4));
+          sum = ((bf16_lo(v.x) + bf16_hi(v.x)) + (bf16_lo(v.y) + bf16_hi(v.y))) +
+                ((bf16_lo(v.z) + bf16_hi(v.z)) + (bf16_lo(v.w) + bf16_hi(v.w)));
+          sum += ((bf16_lo(u.x) + bf16_hi(u.x)) + (bf16_lo(u.y) + bf16_hi(u.y))) +
+                 ((bf16_lo(u.z) + bf16_hi(u.z)) + (bf16_lo(u.w) + bf16_hi(u.w)));
+        }
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+        if (valid && c == 0) xs[half * H + row] = sum;
+      }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&sm.xsf[stage]);
     }
   } else {  // ---- epilogue warps: TMEM lanes 32q .. 32q + 31 = tile rows
     pdl_wait();
@@ -386,47 +386,94 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<const uint2*>(sm.w + stage * kWBytes + kCodeBytes + r * 8);
         const uint32_t sbv[2] = {sbw.x, sbw.y};
         const float* xs = sm.xs + stage * kNK * H;
+        if constexpr (H <= 16) {
+          // both groups of the stage: wait for both accumulators, one round of TMEM loads
+          uint32_t qh[kNK][H], ql[kNK][H];
 #pragma unroll
-        for (int jj = 0; jj < kNK; ++jj) {
-          const int g = i * kNK + jj, slot = g % RG;
-          const float s = bf16_to_f32((uint16_t)(sbv[jj] & 0xFFFFu));
-          const float b1 = bf16_to_f32((uint16_t)(sbv[jj] >> 16)) - 128.f * s;
-          if (!wait_or_abort(&sm.accf[slot], (g / RG) & 1, abort_flag)) {
-            report_timeout(p, abort_flag, 6);
-            ok = false;
-            break;
+          for (int jj = 0; jj < kNK; ++jj) {
+            const int g = i * kNK + jj, slot = g % RG;
+            if (!wait_or_abort(&sm.accf[slot], (g / RG) & 1, abort_flag)) {
+              report_timeout(p, abort_flag, 6);
+              ok = false;
+              break;
+            }
           }
+          if (!ok) break;
           tc::tc_fence_after();
-          const uint32_t ta = lane_base + kAccCol + (uint32_t)(slot * BN);
 #pragma unroll
-          for (int c0 = 0; c0 < H; c0 += CH) {
-            uint32_t qh[CH], ql[CH];
-            if constexpr (CH == 16) {
-              tc::tmem_ld16(ta + c0, qh);
-              tc::tmem_ld16(ta + H + c0, ql);
+          for (int jj = 0; jj < kNK; ++jj) {
+            const uint32_t ta = lane_base + kAccCol + (uint32_t)(((i * kNK + jj) % RG) * BN);
+            if constexpr (H == 16) {
+              tc::tmem_ld16(ta, qh[jj]);
+              tc::tmem_ld16(ta + H, ql[jj]);
             } else {
-              tc::tmem_ld8(ta + c0, qh);
-              tc::tmem_ld8(ta + H + c0, ql);
-            }
-            tc::tmem_ld_wait();
-            float xv[CH];
-#pragma unroll
-            for (int n = 0; n < CH; n += 4) {
-              const float4 f = *reinterpret_cast<const float4*>(xs + jj * H + c0 + n);
-              xv[n] = f.x;
-              xv[n + 1] = f.y;
-              xv[n + 2] = f.z;
-              xv[n + 3] = f.w;
-            }
-#pragma unroll
-            for (int n = 0; n < CH; ++n) {
-              const float vq = __uint_as_float(qh[n]) + __uint_as_float(ql[n]);
-              y[c0 + n] = fmaf(s, vq, fmaf(b1, xv[n], y[c0 + n]));
+              tc::tmem_ld8(ta, qh[jj]);
+              tc::tmem_ld8(ta + H, ql[jj]);
             }
           }
+          tc::tmem_ld_wait();
           tc::tc_fence_before();
           __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&sm.acce[slot]);
+          if (lane == 0)
+            for (int jj = 0; jj < kNK; ++jj) tc::mbar_arrive(&sm.acce[(i * kNK + jj) % RG]);
+#pragma unroll
+          for (int jj = 0; jj < kNK; ++jj) {
+            const float s = bf16_to_f32((uint16_t)(sbv[jj] & 0xFFFFu));
+            const float b1 = bf16_to_f32((uint16_t)(sbv[jj] >> 16)) - 128.f * s;
+#pragma unroll
+            for (int n = 0; n < H; n += 4) {
+              const float4 f = *reinterpret_cast<const float4*>(xs + jj * H + n);
+              const float xv[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float vq = __uint_as_float(qh[jj][n + e]) + __uint_as_float(ql[jj][n + e]);
+                y[n + e] = fmaf(s, vq, fmaf(b1, xv[e], y[n + e]));
+              }
+            }
+          }
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < kNK; ++jj) {
+            const int g = i * kNK + jj, slot = g % RG;
+            const float s = bf16_to_f32((uint16_t)(sbv[jj] & 0xFFFFu));
+            const float b1 = bf16_to_f32((uint16_t)(sbv[jj] >> 16)) - 128.f * s;
+            if (!wait_or_abort(&sm.accf[slot], (g / RG) & 1, abort_flag)) {
+              report_timeout(p, abort_flag, 6);
+              ok = false;
+              break;
+            }
+            tc::tc_fence_after();
+            const uint32_t ta = lane_base + kAccCol + (uint32_t)(slot * BN);
+#pragma unroll
+            for (int c0 = 0; c0 < H; c0 += CH) {
+              uint32_t qh[CH], ql[CH];
+              if constexpr (CH == 16) {
+                tc::tmem_ld16(ta + c0, qh);
+                tc::tmem_ld16(ta + H + c0, ql);
+              } else {
+                tc::tmem_ld8(ta + c0, qh);
+                tc::tmem_ld8(ta + H + c0, ql);
+              }
+              tc::tmem_ld_wait();
+              float xv[CH];
+#pragma unroll
+              for (int n = 0; n < CH; n += 4) {
+                const float4 f = *reinterpret_cast<const float4*>(xs + jj * H + c0 + n);
+                xv[n] = f.x;
+                xv[n + 1] = f.y;
+                xv[n + 2] = f.z;
+                xv[n + 3] = f.w;
+              }
+#pragma unroll
+              for (int n = 0; n < CH; ++n) {
+                const float vq = __uint_as_float(qh[n]) + __uint_as_float(ql[n]);
+                y[c0 + n] = fmaf(s, vq, fmaf(b1, xv[n], y[c0 + n]));
+              }
+            }
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&sm.acce[slot]);
+          }
         }
         if (!ok) break;
         __syncwarp();
@@ -542,10 +589,9 @@ bool q4_plan(int RB, int KS, int BN, int num_sms, CskPlan* out) {
     return BN == 16 ? q4_smem_bytes<16>(q, true)
                     : BN == 32 ? q4_smem_bytes<32>(q, true) : q4_smem_bytes<64>(q, true);
   };
-  const int slot_cap = max_stages_for_slots(BN == 64 ? acc_slots<64>() : acc_slots<16>());
-  bp.stages = std::min(bp.stages, slot_cap);
   while (bp.stages > 2 && smem(bp) > (size_t)kSmemBudget) --bp.stages;
-  if (smem(bp) > (size_t)kSmemBudget) return false;
+  bp.stages &= ~1;  // even: the issuers of one stage parity own half of the stages
+  if (bp.stages < 2 || smem(bp) > (size_t)kSmemBudget) return false;
   *out = bp;
   return true;
 }
@@ -624,7 +670,7 @@ bool launch_q4_csk(const CUtensorMap& tx, TcParams p, int BN, int num_sms, cudaS
     if (!q4_plan(p.RB, p.KS, BN, num_sms, &q)) return false;
     plans[key] = q;
   }
-  if (q.stages > max_stages_for_slots(BN == 64 ? acc_slots<64>() : acc_slots<16>())) return false;
+  if (q.stages % 2) return false;
   cudaError_t rc;
   if (BN == 16) rc = launch_q4<16>(tx, p, q, s);
   else if (BN == 32) rc = launch_q4<32>(tx, p, q, s);
