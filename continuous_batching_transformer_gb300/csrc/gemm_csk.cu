@@ -37,6 +37,7 @@ constexpr int kABytes = 128 * 128;  // 128 rows x 64 bf16
 constexpr int kMaxStages = 8;
 constexpr int kMaxSlots = 4;        // tiles one CTA owns in a launch
 constexpr int kSmemBudget = 227 * 1024;
+constexpr int kAcc = 4;             // accumulators per tile (see k_tc_csk)
 
 using csk::cluster_rank;
 using csk::cluster_sync;
@@ -104,7 +105,11 @@ __global__ void __launch_bounds__(kThreads, 1)
              const TcParams p, const CskPlan q) {
   constexpr int H = BN / 2;  // operand rows: H hi parts, then H lo parts
   constexpr int kXBytes = BN * 128;  // operand tile of one 64-column block
-  constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
+  // two buffers (tiles in flight) of kAcc accumulators: super-block sb accumulates into
+  // accumulator (sb - sb0) % kAcc, and the epilogue adds them in fp32 (round to nearest) --
+  // the tensor core's own fp32 accumulation rounds toward zero, and the split divides that
+  // bias by kAcc
+  constexpr uint32_t kTmemCols = 2 * kAcc * BN < 32 ? 32 : 2 * kAcc * BN;
   constexpr uint32_t kIdesc = tc::idesc_bf16(128, BN);
   constexpr uint32_t kPartBytes = 128 * H * 4;  // one CTA's partial sums of one tile
   extern __shared__ uint8_t smem_raw[];
@@ -223,8 +228,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc::tc_fence_after();
-        const uint32_t d = tmem + acc * BN;
+        const uint32_t d0 = tmem + (uint32_t)(acc * kAcc * BN);
         for (int sb = sb0; sb < sb1; ++sb) {
+          const uint32_t d = d0 + (uint32_t)(((sb - sb0) % kAcc) * BN);
           if (!wait_or_abort(&sm.full[stage], phase, abort_flag)) {
             report_timeout(p, abort_flag, 3);
             ok = false;
@@ -237,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               tc::mma_bf16(d, ad + 2 * kk, xd + 2 * kk, kIdesc,
-                           (sb > sb0 || jj > 0 || kk > 0) ? 1u : 0u);
+                           (sb - sb0 >= kAcc || jj > 0 || kk > 0) ? 1u : 0u);
           }
           tc::mma_commit(&sm.empty[stage]);
           if (++stage == S) {
@@ -299,11 +305,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc::tc_fence_after();
-      uint32_t raw[BN];
-      const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(acc * BN);
+      float vals[H];
 #pragma unroll
-      for (int c = 0; c < BN / 16; ++c) tc::tmem_ld16(taddr + 16 * c, raw + 16 * c);
-      tc::tmem_ld_wait();
+      for (int n = 0; n < H; ++n) vals[n] = 0.f;
+      const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(acc * kAcc * BN);
+      const int nacc = sb1 - sb0 < kAcc ? sb1 - sb0 : kAcc;
+      for (int a = 0; a < nacc; ++a) {  // accumulators in a fixed order; hi + lo per column
+        uint32_t raw[BN];
+#pragma unroll
+        for (int c = 0; c < BN / 16; ++c)
+          tc::tmem_ld16(taddr + (uint32_t)(a * BN) + 16 * c, raw + 16 * c);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int n = 0; n < H; ++n) vals[n] += __uint_as_float(raw[n]) + __uint_as_float(raw[n + H]);
+      }
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sm.acce[acc]);
@@ -311,9 +326,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc = 0;
         acc_phase ^= 1;
       }
-      float vals[H];
-#pragma unroll
-      for (int n = 0; n < H; ++n) vals[n] = __uint_as_float(raw[n]) + __uint_as_float(raw[n + H]);
       float sum[H];
       const int got = csk::combine_partials<H>(vals, sum, sm.inbox, sm.inbox_full, slot, rank,
                                                owner, C, r, abort_flag);
