@@ -305,16 +305,17 @@ __global__ void __launch_bounds__(160, kCtasPerSm)
 
 // Combine the partials of each (row, q head): o = sum_i o_i e^(m_i - M) / sum_i l_i e^(m_i - M)
 // and write it as the bf16 (hi/lo) operand of the output projection.  One 128-thread block per
-// (row, q head): the threads reduce the splits' (m, l) pairs, then warp w sums splits w, w + 4,
-// ... (lane = head_dim / 32 output dimensions) with their loads in flight together, and the four
-// warps' sums are added in a fixed order.  The order depends only on the row's own splits.
+// (row, q head), one pass over the partials: warp w takes splits w, w + 4, ... in order with
+// a running maximum (lane = head_dim / 32 output dimensions; the loads of several splits are
+// in flight together), then the four warps' (max, sum, output) are combined in a fixed order.
+// The order depends only on the row's own splits.
 __global__ void __launch_bounds__(128)
     k_attn_merge(const float* __restrict__ part_o, const float2* __restrict__ part_ml,
                  const int* __restrict__ item_base, const int* __restrict__ item_count, int B,
                  int n_heads, int n_kv_heads, int head_dim, uint16_t* act, int lo_rows) {
   pdl_wait();
   pdl_launch();
-  __shared__ float red[4];
+  __shared__ float wm[4], wl[4];
   __shared__ float wsum[4][128];
   const int hq = blockIdx.x, b = blockIdx.y;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
@@ -322,45 +323,45 @@ __global__ void __launch_bounds__(128)
   const int cnt = item_count[b];
   const int first = item_base[b] + g * cnt;
   const float2* ml = part_ml + (size_t)first * G + h;  // split i at ml[i * G]
-  float m = -INFINITY;
-  for (int i = t; i < cnt; i += 128) m = fmaxf(m, ml[(size_t)i * G].x);
-  m = warp_max(m);
-  if (lane == 0) red[warp] = m;
-  __syncthreads();
-  const float M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-  __syncthreads();
-  float l = 0.f;
-  for (int i = t; i < cnt; i += 128) {
-    const float2 v = ml[(size_t)i * G];
-    l += v.y * __expf(v.x - M);
-  }
-  l = warp_sum(l);
-  if (lane == 0) red[warp] = l;
-  __syncthreads();
-  const float invL = 1.f / (red[0] + red[1] + red[2] + red[3]);
   const int per = head_dim / 32;  // 4 (head_dim 128) or 2 (64)
+  float m = -INFINITY, l = 0.f;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
   for (int i = warp; i < cnt; i += 4) {
-    const float2 v = ml[(size_t)i * G];
-    const float wgt = __expf(v.x - M);
+    const float2 v = __ldcg(ml + (size_t)i * G);
     const float* po = part_o + ((size_t)(first + i) * G + h) * head_dim + lane * per;
+    float o[4];
     if (per == 4) {
-      const float4 o = __ldcg(reinterpret_cast<const float4*>(po));
-      acc[0] += o.x * wgt;
-      acc[1] += o.y * wgt;
-      acc[2] += o.z * wgt;
-      acc[3] += o.w * wgt;
+      const float4 f = __ldcg(reinterpret_cast<const float4*>(po));
+      o[0] = f.x; o[1] = f.y; o[2] = f.z; o[3] = f.w;
     } else {
-      const float2 o = __ldcg(reinterpret_cast<const float2*>(po));
-      acc[0] += o.x * wgt;
-      acc[1] += o.y * wgt;
+      const float2 f = __ldcg(reinterpret_cast<const float2*>(po));
+      o[0] = f.x; o[1] = f.y; o[2] = 0.f; o[3] = 0.f;
     }
+    const float mn = fmaxf(m, v.x);
+    const float sc = m == -INFINITY ? 0.f : __expf(m - mn);
+    const float wgt = __expf(v.x - mn);
+    l = fmaf(l, sc, v.y * wgt);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[j] = fmaf(acc[j], sc, o[j] * wgt);
+    m = mn;
+  }
+  if (lane == 0) {
+    wm[warp] = m;
+    wl[warp] = l;
   }
   for (int j = 0; j < per; ++j) wsum[warp][lane * per + j] = acc[j];
   __syncthreads();
   if (t < head_dim) {
-    const float o = (((wsum[0][t] + wsum[1][t]) + wsum[2][t]) + wsum[3][t]) * invL;
+    const float M = fmaxf(fmaxf(wm[0], wm[1]), fmaxf(wm[2], wm[3]));
+    float L = 0.f, o = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {  // a warp without splits has m = -inf and contributes 0
+      const float sc = wm[w] == -INFINITY ? 0.f : __expf(wm[w] - M);
+      L = fmaf(wl[w], sc, L);
+      o = fmaf(wsum[w][t], sc, o);
+    }
+    o = o / L;
     const int K = n_heads * head_dim;
     const int col = hq * head_dim + t;
     const uint16_t hi = f32_to_bf16(o);
