@@ -663,7 +663,7 @@ static bool tc_projection(cbt_engine* e, const CUtensorMap& wmap, const CUtensor
   bool ok;
   if (e->cfg.weight_format != CBT_WEIGHTS_BF16) {
     p.wq = q4w;
-    ok = split && launch_q4_csk(*xm, p, BN, e->num_sms, e->stream);
+    ok = split && launch_q4_rd(p, xbuf, tc_lo_rows(e, n), e->num_sms, e->stream);
   } else {
     ok = split ? launch_tc_csk(wmap_kb, *xm, p, BN, e->num_sms, e->stream)
                : launch_tc_linear(wmap, *xm, p, split, BN, e->num_sms, e->tc_part_floats,

@@ -1,0 +1,555 @@
+// gemm_q4r.cu -- decode projections y = x W^T over 4-bit affine weights (groups of 64 columns,
+// w = s * q + b with q in 0..15 and bf16 s, b), dequantised in registers.
+//
+// A decode step has few rows (B <= 32), so the contraction is a weight stream: every weight is
+// used by at most B operand rows.  Here the codes never leave the registers between the load and
+// the multiply:
+//   * each warp copies its 16 rows of a 128-row x 128-column weight block (1 KB of codes plus
+//     the rows' scales and biases) into a private shared-memory ring with cp.async, three
+//     blocks ahead, so no other warp ever waits for it;
+//   * it turns each pair of codes into one bf16x2 register holding (128 + q, 128 + q') -- the
+//     codes sit in the low mantissa bits of 128.0, so the values are exact -- and feeds them as
+//     the A fragment of mma.sync m16n8k16 (A from registers is what keeps the dequantisation
+//     in registers; tcgen05 takes A only from shared or tensor memory);
+//   * the B fragment is the operand, 8 rows per n8 block (bf16 hi parts, then lo parts, so the
+//     operand carries fp32-grade precision), staged once per CTA in shared memory for the
+//     CTA's whole k-range together with each operand row's sum over every group of 64 columns;
+//   * every group of 64 columns is its own accumulation, folded in with the row's scale and
+//     bias in fp32:  y += s * sum_k (128 + q_k) x_k  +  (b - 128 s) * sum_k x_k.
+// No dequantised weight is rounded; the result is that of the exact dequantised weights and
+// the fp32 operand up to fp32 accumulation.
+//
+// Work split (the cluster split-K of the bf16 decode projections): tile t of 128 rows belongs
+// to cluster t % NC; rank r of the cluster takes superblocks [r SB / C, (r + 1) SB / C) of its
+// tiles; inside a CTA, warps 0-7 take the first half of those superblocks and warps 8-15 the
+// second half, warp w holding tile rows 16 (w % 8) .. + 15.  The two halves meet in shared
+// memory, the C ranks in the tile owner's shared memory (st.async, added in rank order), and
+// the owner's warps 0-3 run the shared epilogue (RMSNorm scale, residual add and the next
+// norm's statistics and operand, SwiGLU, RoPE + K/V append + the attention's Q operand).
+//
+// Batch rows are taken 8 at a time (gridDim.y passes, each over the same weights): a row's
+// arithmetic -- the k split, the group order, the fold -- depends on the matrix shape alone,
+// so a row's result does not depend on how many rows share the step.
+//
+// The weights are the native block layout of gemm_q4.cu: per (128-row tile, 128-column
+// superblock) [4 chunks][128 rows][16 bytes] of codes (chunk c holds columns 32c .. 32c + 31 of
+// a row as four words; word i's pair p: bits 4p..4p+3 column 8i + 2p, bits 16+4p..19+4p column
+// 8i + 2p + 1), then [128 rows][s0, b0, s1, b1] bf16.
+#include <algorithm>
+#include <map>
+#include <tuple>
+
+#include "csk_common.cuh"
+#include "kernels.h"
+#include "tc_common.cuh"
+#include "tc_epilogue.cuh"
+
+namespace {
+
+constexpr int kWarps = 16;               // two sets of 8 warps, one per half of the k-range
+constexpr int kThreads = 32 * kWarps;
+constexpr int kDepth = 4;                // ring slots per warp (kDepth - 1 blocks in flight)
+constexpr int kChunkPitch = 320;         // a ring chunk: 16 rows x 16 bytes, padded so the
+                                         // fragment loads of one half-warp hit 32 distinct banks
+constexpr int kScaleOff = 4 * kChunkPitch;
+constexpr int kStage = kScaleOff + 16 * 8;  // codes of 16 rows, then their scales and biases
+constexpr int kCodeBytes = 128 * 64;
+constexpr int kMaxSlots = 4;
+constexpr int kMaxSbPerRank = 24;        // bounds the operand slice kept in shared memory
+constexpr int kSmemBudget = 227 * 1024;
+
+struct Q4rPlan {
+  int C;       // CTAs per cluster (split of the k-range)
+  int NC;      // clusters
+  int slots;   // inbox slots: most tiles one CTA owns
+  int sb_max;  // most superblocks of one rank
+};
+
+__host__ __device__ constexpr size_t align16(size_t v) { return (v + 15) & ~size_t(15); }
+
+// Shared-memory carve-up for N operand columns (H = N / 2 batch rows)
+struct Layout {
+  size_t ring, xs, xsum, sacc, inbox, swx, rinv, cosv, sinv, rows, bars, flags, total;
+  int pitch;  // bytes per operand row of xs
+};
+
+__host__ __device__ inline Layout layout(int N, const Q4rPlan& q) {
+  const int H = N / 2;
+  Layout L;
+  L.pitch = q.sb_max * 256 + 16;  // == 16 (mod 128): conflict-free 16-byte fragment loads
+  size_t o = 0;
+  L.ring = o;
+  o += (size_t)kWarps * kDepth * kStage;
+  L.xs = o;
+  o = align16(o + (size_t)N * L.pitch);
+  L.xsum = o;
+  o = align16(o + (size_t)2 * q.sb_max * N * 4);
+  L.sacc = o;
+  o = align16(o + (size_t)2 * 2 * 128 * H * 4);  // [tile parity][warp set][128 rows][H]
+  L.inbox = o;
+  o = align16(o + (size_t)q.slots * (q.C > 1 ? q.C - 1 : 0) * 128 * H * 4);
+  L.swx = o;
+  o = align16(o + (size_t)(128 * (H + 1) + 32) * 4);
+  L.rinv = o;
+  o = align16(o + 32 * 4);
+  L.cosv = o;
+  o = align16(o + (size_t)H * 64 * 4);
+  L.sinv = o;
+  o = align16(o + (size_t)H * 64 * 4);
+  L.rows = o;
+  o = align16(o + (size_t)8 * sizeof(QueryRow));
+  L.bars = o;
+  o = align16(o + kMaxSlots * 8);
+  L.flags = o;
+  o += 16;
+  L.total = o;
+  return L;
+}
+
+// 16 bytes global -> shared (L2 only); src_bytes < 16: the rest of the 16 bytes are zero-filled
+__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(tc::smem_u32(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async16s(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a));
+  return v;
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// D += A B for one m16n8k16 tile: bf16 inputs, fp32 accumulators
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// pair p of a native code word as a bf16x2 word (128 + q_even, 128 + q_odd)
+__device__ __forceinline__ uint32_t unpack_pair(uint32_t w, int p) {
+  return ((w >> (4 * p)) & 0x000F000Fu) | 0x43004300u;
+}
+
+__device__ __forceinline__ void report_timeout(const TcParams& p, volatile int* abort, int role) {
+  *abort = 1;
+  if (atomicCAS(p.err, 0, CBT_DEV_TIMEOUT) == 0) p.err[1] = 500 + role;
+}
+
+// The projection's parameters for batch rows [8 pass, 8 pass + 8): every per-row pointer moves
+// to the pass's first row; lo-part row offsets are absolute and stay.
+__device__ __forceinline__ TcParams pass_params(const TcParams& p0, int pass) {
+  TcParams p = p0;
+  const int r0 = 8 * pass;
+  p.n_act = min(8, p0.n_act - r0);
+  if (p.out) p.out += (size_t)r0 * p.ldo;
+  if (p.next_act) p.next_act += (size_t)r0 * p.ldo;
+  if (p.act) p.act += (size_t)r0 * p.act_ld;
+  if (p.ss_in) p.ss_in += r0;
+  if (p.ss_out) p.ss_out += r0;
+  if (p.rows) p.rows += r0;
+  if (p.cosv) p.cosv += (size_t)r0 * (p.head_dim / 2);
+  if (p.sinv) p.sinv += (size_t)r0 * (p.head_dim / 2);
+  if (p.qtile) p.qtile += (size_t)r0 * p.n_kv_heads * 16 * p.head_dim * 2;
+  return p;
+}
+
+// One CTA: k-range [sb0, sb1) of tiles cid, cid + NC, ... for batch rows [8 y, 8 y + 8).
+// NB8 n8 blocks of operand columns: NB8 = 1 takes up to 4 rows (hi parts in columns 0-3, lo
+// parts in 4-7), NB8 = 2 up to 8 rows (hi block, then lo block).
+template <int NB8>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_q4_rd(const __grid_constant__ TcParams p0, const uint16_t* __restrict__ x, int x_lo,
+            const Q4rPlan q) {
+  constexpr int N = 8 * NB8, H = N / 2;
+  extern __shared__ __align__(16) uint8_t smem[];
+  const Layout L = layout(N, q);
+  uint8_t* ring = smem + L.ring;
+  uint8_t* xs = smem + L.xs;
+  float* xsum = reinterpret_cast<float*>(smem + L.xsum);
+  float* sacc = reinterpret_cast<float*>(smem + L.sacc);
+  float* inbox = reinterpret_cast<float*>(smem + L.inbox);
+  float* swx = reinterpret_cast<float*>(smem + L.swx);
+  float* rinv = reinterpret_cast<float*>(smem + L.rinv);
+  float* scos = reinterpret_cast<float*>(smem + L.cosv);
+  float* ssin = reinterpret_cast<float*>(smem + L.sinv);
+  QueryRow* srows = reinterpret_cast<QueryRow*>(smem + L.rows);
+  uint64_t* inbox_full = reinterpret_cast<uint64_t*>(smem + L.bars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.flags);
+
+  const int pass = blockIdx.y;
+  const TcParams p = pass_params(p0, pass);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int C = q.C;
+  const uint32_t rank = C > 1 ? csk::cluster_rank() : 0u;
+  const int cid = blockIdx.x / C, NC = gridDim.x / C;
+  const int Tc = cid < p.RB ? (p.RB - cid + NC - 1) / NC : 0;
+  const int SB = p.K / 128;
+  const int sb0 = (int)((long long)rank * SB / C);
+  const int sb1 = (int)((long long)(rank + 1) * SB / C);
+  const int nsb = sb1 - sb0;
+  const int owned = Tc > (int)rank ? (Tc - (int)rank + C - 1) / C : 0;
+  const int pitch = nsb * 256 + 16;
+  // warp set h takes local superblocks [kbase, kbase + nh) of every tile
+  const int h = warp >> 3, rw = 16 * (warp & 7);
+  const int n0 = (nsb + 1) >> 1;
+  const int nh = h ? nsb - n0 : n0, kbase = h ? n0 : 0;
+  const int nst = Tc * nh;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kMaxSlots; ++s) tc::mbar_init(&inbox_full[s], 1);
+    if (C > 1)
+      for (int s = 0; s < owned; ++s)
+        tc::mbar_expect_tx(&inbox_full[s], (uint32_t)((C - 1) * 128 * H * 4));
+    abort_flag[0] = 0;
+    tc::mbar_fence_init();
+  }
+  __syncthreads();
+  if (C > 1) csk::cluster_sync();
+  pdl_launch();
+
+  // ---- weight blocks: this warp's 16 rows, kDepth - 1 blocks ahead (weights only: these may
+  // be requested before the previous kernel has finished)
+  const uint32_t wring = tc::smem_u32(ring) + (uint32_t)(warp * kDepth * kStage);
+  // issue cursor: the next block's address (tile by tile, local superblock by superblock) and
+  // its ring slot
+  const uint8_t* wnext = p.wq + ((size_t)cid * SB + sb0 + kbase) * kQ4BlockBytes;
+  const size_t tile_skip = ((size_t)NC * SB - nh) * kQ4BlockBytes;  // last block -> next tile
+  // this lane's pieces: codes (chunk, row) = (piece / 16, piece % 16) for pieces lane and
+  // lane + 32; lanes 0-7 also copy 16 bytes of the rows' scales and biases
+  const int pc0 = lane >> 4, pr0 = lane & 15;
+  const uint32_t src0 = pc0 * 2048 + (rw + pr0) * 16, dst0 = pc0 * kChunkPitch + pr0 * 16;
+  const uint32_t srcs = kCodeBytes + rw * 8 + lane * 16, dsts = kScaleOff + lane * 16;
+  int is_n = 0, is_k = 0;
+  uint32_t is_dst = wring;
+  auto issue = [&]() {
+    if (is_n < nst) {
+      cp_async16s(is_dst + dst0, wnext + src0);
+      cp_async16s(is_dst + dst0 + 2 * kChunkPitch, wnext + src0 + 2 * 2048);
+      if (lane < 8) cp_async16s(is_dst + dsts, wnext + srcs);
+      wnext += kQ4BlockBytes;
+      if (++is_k == nh) {
+        is_k = 0;
+        wnext += tile_skip;
+      }
+      ++is_n;
+      is_dst = is_dst + kStage == wring + kDepth * kStage ? wring : is_dst + kStage;
+    }
+    cp_async_commit();
+  };
+  for (int s = 0; s < kDepth - 1; ++s) issue();
+
+  pdl_wait();
+  // ---- the operand slice of this k-range (zero columns past the pass's rows), all pieces in
+  // flight at once; RMSNorm factors and the QKV epilogue's per-row inputs meanwhile
+  {
+    const int per_row = nsb * 16;  // 16-byte pieces
+    for (int idx = threadIdx.x; idx < N * per_row; idx += kThreads) {
+      const int n = idx / per_row, c = idx - n * per_row;
+      const int b = n % H;
+      const bool valid = b < p.n_act;
+      const size_t row = n >= H ? (size_t)(x_lo + 8 * pass + b) : (size_t)(8 * pass + b);
+      const uint16_t* src = valid ? x + row * p.K + (size_t)sb0 * 128 + (size_t)c * 8 : x;
+      cp_async16_zfill(xs + (size_t)n * pitch + c * 16, src, valid ? 16u : 0u);
+    }
+    cp_async_commit();
+  }
+  if (p.ss_in && threadIdx.x < p.n_act) {
+    float s = 0.f;
+    for (int tt = 0; tt < p.ss_tiles; ++tt) s += p.ss_in[(size_t)tt * p.ss_ld + threadIdx.x];
+    rinv[threadIdx.x] = rsqrtf(s / (float)p.K + p.eps);
+  }
+  tcepi::EpiSrc src = tcepi::epi_src_global(p);
+  if (p.epi == EPI_QKV) {
+    const int half = p.head_dim >> 1;
+    for (int i = threadIdx.x; i < p.n_act * half; i += kThreads) {
+      scos[i] = p.cosv[i];
+      ssin[i] = p.sinv[i];
+    }
+    if (threadIdx.x < p.n_act) srows[threadIdx.x] = p.rows[threadIdx.x];
+    src.rows = srows;
+    src.cosv = scos;
+    src.sinv = ssin;
+  }
+  cp_async_wait<0>();  // the operand slice (and the weight blocks requested before it)
+  __syncthreads();
+  // each operand column's sum over every group of 64 columns, in a fixed order
+  for (int idx = threadIdx.x; idx < 2 * nsb * N; idx += kThreads) {
+    const int gl = idx / N, n = idx - gl * N;
+    const uint4* v = reinterpret_cast<const uint4*>(xs + (size_t)n * pitch + gl * 128);
+    float s = 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 u = v[c];
+      s += bf16_lo(u.x);
+      s += bf16_hi(u.x);
+      s += bf16_lo(u.y);
+      s += bf16_hi(u.y);
+      s += bf16_lo(u.z);
+      s += bf16_hi(u.z);
+      s += bf16_lo(u.w);
+      s += bf16_hi(u.w);
+    }
+    xsum[gl * N + n] = s;
+  }
+  __syncthreads();
+
+  float y[NB8][4];
+#pragma unroll
+  for (int nb = 0; nb < NB8; ++nb)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) y[nb][c] = 0.f;
+  // per-lane views: code words of rows g / g + 8 (chunk 2G + t/2, half t&1), scales, operand
+  const uint32_t lane_w = (t >> 1) * kChunkPitch + g * 16 + 8 * (t & 1);
+  const uint32_t xlane = tc::smem_u32(xs) + (uint32_t)(g * pitch + 32 * t + kbase * 256);
+  const uint32_t xsl = tc::smem_u32(xsum) + (uint32_t)((2 * kbase * N + 2 * t) * 4);
+  const uint32_t pitch8 = 8u * (uint32_t)pitch;
+  uint32_t st = wring;  // the ring slot consumed next
+  for (int j = 0; j < Tc; ++j) {
+    float res[H];
+    const uint32_t owner = (uint32_t)(j % C);
+    if (warp < 4 && rank == owner) {  // epilogue inputs of this tile, requested early
+      const int rb = cid + j * NC;
+      tcepi::load_residual<H>(p, rb, threadIdx.x, 0, res);
+      src.gn = tcepi::load_next_gain(p, rb, threadIdx.x);
+      src.has_gn = true;
+    }
+    for (int k = 0; k < nh; ++k) {
+      issue();
+      cp_async_wait<kDepth - 1>();  // block of this stage has landed (this lane's copies) ...
+      __syncwarp();                 // ... and every lane's
+      const uint2 sA = lds64(st + kScaleOff + g * 8);
+      const uint2 sB = lds64(st + kScaleOff + (g + 8) * 8);
+#pragma unroll
+      for (int G = 0; G < 2; ++G) {
+        // lane (g, t): columns 64 G + 16 t .. + 15 of rows g and g + 8, two code words each
+        const uint2 wA = lds64(st + lane_w + G * 2 * kChunkPitch);
+        const uint2 wB = lds64(st + lane_w + G * 2 * kChunkPitch + 128);
+        const uint32_t xg = xlane + k * 256 + G * 128;
+        const uint32_t xsg = xsl + (2 * k + G) * N * 4;
+        float acc[NB8][4];
+#pragma unroll
+        for (int nb = 0; nb < NB8; ++nb)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[nb][e] = 0.f;
+#pragma unroll
+        for (int jp = 0; jp < 2; ++jp) {
+          // word jp holds columns 16 t + 8 jp .. + 7: MMA 2 jp takes its pairs 0 and 1, MMA
+          // 2 jp + 1 its pairs 2 and 3 (k index 2t, 2t+1 -> first pair, 2t+8, 2t+9 -> second)
+          const uint32_t a = jp ? wA.y : wA.x, b = jp ? wB.y : wB.x;
+          const uint32_t A0[4] = {unpack_pair(a, 0), unpack_pair(b, 0), unpack_pair(a, 1),
+                                  unpack_pair(b, 1)};
+          const uint32_t A1[4] = {unpack_pair(a, 2), unpack_pair(b, 2), unpack_pair(a, 3),
+                                  unpack_pair(b, 3)};
+#pragma unroll
+          for (int nb = 0; nb < NB8; ++nb) {
+            // operand column nb * 8 + g, the same eight columns as bf16 pairs
+            const uint4 xv = lds128(xg + nb * pitch8 + 16 * jp);
+            mma16816(acc[nb], A0, xv.x, xv.y);
+            mma16816(acc[nb], A1, xv.z, xv.w);
+          }
+        }
+        const uint32_t swa = G ? sA.y : sA.x, swb = G ? sB.y : sB.x;
+        const float s_a = bf16_lo(swa), s_b = bf16_lo(swb);
+        const float c_a = fmaf(-128.f, s_a, bf16_hi(swa)), c_b = fmaf(-128.f, s_b, bf16_hi(swb));
+#pragma unroll
+        for (int nb = 0; nb < NB8; ++nb) {
+          const uint2 Xw = lds64(xsg + nb * 32);
+          const float2 X = make_float2(__uint_as_float(Xw.x), __uint_as_float(Xw.y));
+          y[nb][0] = fmaf(s_a, acc[nb][0], fmaf(c_a, X.x, y[nb][0]));
+          y[nb][1] = fmaf(s_a, acc[nb][1], fmaf(c_a, X.y, y[nb][1]));
+          y[nb][2] = fmaf(s_b, acc[nb][2], fmaf(c_b, X.x, y[nb][2]));
+          y[nb][3] = fmaf(s_b, acc[nb][3], fmaf(c_b, X.y, y[nb][3]));
+        }
+      }
+      st = st + kStage == wring + kDepth * kStage ? wring : st + kStage;
+      __syncwarp();  // the slot is refilled by the next iteration's copies
+    }
+
+    // ---- end of tile j: hi + lo parts into the warp set's half of the hand-off buffer
+    float* sa = sacc + (size_t)((j & 1) * 2 + h) * 128 * H;
+    if constexpr (NB8 == 1) {
+      float v[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) v[c] = y[0][c] + __shfl_xor_sync(0xffffffffu, y[0][c], 2);
+      if (t < 2) {
+        *reinterpret_cast<float2*>(sa + (rw + g) * H + 2 * t) = make_float2(v[0], v[1]);
+        *reinterpret_cast<float2*>(sa + (rw + g + 8) * H + 2 * t) = make_float2(v[2], v[3]);
+      }
+    } else {
+#pragma unroll
+      for (int nb = 0; nb < NB8 / 2; ++nb) {
+        const float* lo = y[nb + NB8 / 2];
+        *reinterpret_cast<float2*>(sa + (rw + g) * H + nb * 8 + 2 * t) =
+            make_float2(y[nb][0] + lo[0], y[nb][1] + lo[1]);
+        *reinterpret_cast<float2*>(sa + (rw + g + 8) * H + nb * 8 + 2 * t) =
+            make_float2(y[nb][2] + lo[2], y[nb][3] + lo[3]);
+      }
+    }
+#pragma unroll
+    for (int nb = 0; nb < NB8; ++nb)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) y[nb][c] = 0.f;
+    tc::named_bar_sync(2, kThreads);
+    if (warp < 4) {
+      // ---- tile row r: both halves, then the cluster's partials, then the epilogue
+      const int r = threadIdx.x;
+      const float* s0 = sacc + (size_t)((j & 1) * 2) * 128 * H + r * H;
+      const float* s1 = s0 + 128 * H;
+      float vals[H];
+#pragma unroll
+      for (int b = 0; b < H; ++b) vals[b] = s0[b] + s1[b];
+      const int rb = cid + j * NC;
+      float sum[H];
+      const int got = csk::combine_partials<H>(vals, sum, inbox, inbox_full, j / C, rank, owner,
+                                               C, r, abort_flag);
+      if (got < 0) report_timeout(p, abort_flag, 1);
+      tc::named_bar_sync(1, 128);  // the same decision in all 128 threads
+      if (got > 0 && *abort_flag == 0) tcepi::finish<H>(p, rb, r, sum, 0, swx, rinv, res, src);
+    }
+  }
+  cp_async_wait<0>();  // (only empty groups remain: every issued block was consumed)
+  if (C > 1 && threadIdx.x == 0)
+    for (int s = 0; s < owned; ++s) tc::mbar_wait(&inbox_full[s], 0);
+  if (C > 1) csk::cluster_sync();
+}
+
+template <int NB8>
+size_t q4r_smem(const Q4rPlan& q) {
+  return layout(8 * NB8, q).total;
+}
+
+template <int NB8>
+int q4r_active_clusters(int C, size_t smem) {
+  static std::map<std::pair<int, size_t>, int> cache;
+  const auto key = std::make_pair(C, smem);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  auto kern = k_q4_rd<NB8>;
+  int n = 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
+      cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();
+  return cache[key] = n;
+}
+
+// The split of the k-range (C) follows from the matrix shape alone -- so a row's arithmetic
+// does not depend on the number of rows -- by the cost of the busiest CTA at one CTA per SM:
+// superblocks it streams, plus a little for each cluster hand-off.
+bool q4r_split(int RB, int SB, int num_sms, Q4rPlan* out) {
+  static const int kSizes[] = {1, 2, 3, 4, 6, 8};
+  double best = 1e30;
+  Q4rPlan bp{};
+  for (int C : kSizes) {
+    if (C > SB || C > num_sms) continue;
+    Q4rPlan q{};
+    q.C = C;
+    q.sb_max = (SB + C - 1) / C;
+    if (q.sb_max > kMaxSbPerRank) continue;
+    q.NC = std::min(RB, num_sms / C);
+    const int tmax = (RB + q.NC - 1) / q.NC;
+    q.slots = C > 1 ? (tmax + C - 1) / C : 0;
+    if (q.slots > kMaxSlots || q4r_smem<2>(q) > (size_t)kSmemBudget) continue;
+    const double cost = (double)tmax * q.sb_max + (C > 1 ? 1.0 : 0.0) + 0.01 * C;
+    if (cost < best) {
+      best = cost;
+      bp = q;
+    }
+  }
+  if (best >= 1e30) return false;
+  *out = bp;
+  return true;
+}
+
+template <int NB8>
+bool q4r_launch(const TcParams& p, const uint16_t* x, int x_lo, Q4rPlan q, int passes,
+                int num_sms, cudaStream_t s) {
+  // clusters that fit at once (one CTA per SM), and the inbox slots that count needs
+  size_t smem = q4r_smem<NB8>(q);
+  int fit = q4r_active_clusters<NB8>(q.C, smem);
+  if (fit <= 0) return false;
+  if (fit < q.NC) {
+    q.NC = fit;
+    const int tmax = (p.RB + q.NC - 1) / q.NC;
+    q.slots = q.C > 1 ? (tmax + q.C - 1) / q.C : 0;
+    if (q.slots > kMaxSlots) return false;
+    smem = q4r_smem<NB8>(q);
+    if (smem > (size_t)kSmemBudget) return false;
+  }
+  auto kern = k_q4_rd<NB8>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return false;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(q.NC * q.C, passes);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = q.C;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  count_launch();
+  return cudaLaunchKernelEx(&cfg, kern, p, x, x_lo, q) == cudaSuccess;
+}
+
+}  // namespace
+
+bool launch_q4_rd(TcParams p, const uint16_t* x, int x_lo, int num_sms, cudaStream_t s) {
+  if (!p.wq || !x || p.K % 128 || p.K <= 0 || p.n_act <= 0 || p.n_act > 32) return false;
+  if (p.epi == EPI_SWIGLU && (p.F % 64 || p.M != 2 * p.F)) return false;
+  if (p.epi == EPI_QKV && (p.head_dim > 128 || p.head_dim % 2)) return false;
+  p.RB = p.epi == EPI_SWIGLU ? p.F / 64 : (p.M + 127) / 128;
+  p.KS = p.K / 64;
+  p.NT = 1;
+  static std::map<std::tuple<int, int, int>, Q4rPlan> plans;
+  const auto key = std::make_tuple(p.RB, p.K / 128, num_sms);
+  auto it = plans.find(key);
+  Q4rPlan q;
+  if (it != plans.end()) {
+    q = it->second;
+  } else {
+    if (!q4r_split(p.RB, p.K / 128, num_sms, &q)) return false;
+    plans[key] = q;
+  }
+  const int passes = (p.n_act + 7) / 8;
+  return p.n_act <= 4 ? q4r_launch<1>(p, x, x_lo, q, passes, num_sms, s)
+                      : q4r_launch<2>(p, x, x_lo, q, passes, num_sms, s);
+}

@@ -127,6 +127,10 @@ bool launch_q4_repack(const uint32_t* packed, const uint16_t* scales, const uint
 // y = x W^T over n_act <= BN/2 decode rows (hi/lo operand) with W = p.wq; tx as for
 // launch_tc_csk.  Any TcParams epilogue.
 bool launch_q4_csk(const CUtensorMap& tx, TcParams p, int BN, int num_sms, cudaStream_t s);
+// The same projection with the codes dequantised in registers (gemm_q4r.cu): x is the operand
+// buffer (bf16 rows of K columns: hi parts at rows b, lo parts at rows x_lo + b), n_act <= 32
+// rows taken 8 at a time.  Any TcParams epilogue.
+bool launch_q4_rd(TcParams p, const uint16_t* x, int x_lo, int num_sms, cudaStream_t s);
 
 // ---- tensor-core decode attention (attn_tc.cu) ------------------------------------------------
 struct AttnDecodeArgs {
