@@ -4,7 +4,7 @@
 // A decode step has few rows (B <= 32), so the contraction is a weight stream: every weight is
 // used by at most B operand rows.  Here the codes never leave the registers between the load and
 // the multiply:
-//   * each warp copies its 16 rows of a 128-row x 128-column weight block (1 KB of codes plus
+//   * each warp copies its 32 rows of a 128-row x 128-column weight block (2 KB of codes plus
 //     the rows' scales and biases) into a private shared-memory ring with cp.async, three
 //     blocks ahead, so no other warp ever waits for it;
 //   * it turns each pair of codes into one bf16x2 register holding (128 + q, 128 + q') -- the
@@ -21,8 +21,9 @@
 //
 // Work split (the cluster split-K of the bf16 decode projections): tile t of 128 rows belongs
 // to cluster t % NC; rank r of the cluster takes superblocks [r SB / C, (r + 1) SB / C) of its
-// tiles; inside a CTA, warps 0-7 take the first half of those superblocks and warps 8-15 the
-// second half, warp w holding tile rows 16 (w % 8) .. + 15.  The two halves meet in shared
+// tiles; inside a CTA, warps 0-3 take the first half of those superblocks and warps 4-7 the
+// second half, warp w holding tile rows 32 (w % 4) .. + 31 as two m16 row blocks that share
+// the operand fragments.  The two halves meet in shared
 // memory, the C ranks in the tile owner's shared memory (st.async, added in rank order), and
 // the owner's warps 0-3 run the shared epilogue (RMSNorm scale, residual add and the next
 // norm's statistics and operand, SwiGLU, RoPE + K/V append + the attention's Q operand).
@@ -46,13 +47,14 @@
 
 namespace {
 
-constexpr int kWarps = 16;               // two sets of 8 warps, one per half of the k-range
+constexpr int kWarps = 8;                // two sets of 4 warps, one per half of the k-range
 constexpr int kThreads = 32 * kWarps;
+constexpr int kRows = 32;                // tile rows per warp (two m16 row blocks)
 constexpr int kDepth = 4;                // ring slots per warp (kDepth - 1 blocks in flight)
-constexpr int kChunkPitch = 320;         // a ring chunk: 16 rows x 16 bytes, padded so the
+constexpr int kChunkPitch = 576;         // a ring chunk: 32 rows x 16 bytes, padded so the
                                          // fragment loads of one half-warp hit 32 distinct banks
 constexpr int kScaleOff = 4 * kChunkPitch;
-constexpr int kStage = kScaleOff + 16 * 8;  // codes of 16 rows, then their scales and biases
+constexpr int kStage = kScaleOff + kRows * 8;  // codes of 32 rows, then their scales and biases
 constexpr int kCodeBytes = 128 * 64;
 constexpr int kMaxSlots = 4;
 constexpr int kMaxSbPerRank = 24;        // bounds the operand slice kept in shared memory
@@ -112,8 +114,11 @@ __device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, uin
                "r"(src_bytes)
                : "memory");
 }
-__device__ __forceinline__ void cp_async16s(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+// 16 bytes global -> shared (L2 only), with an L2 eviction policy
+__device__ __forceinline__ void cp_async16s(uint32_t dst, const void* src, uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "l"(pol)
+               : "memory");
 }
 __device__ __forceinline__ uint2 lds64(uint32_t a) {
   uint2 v;
@@ -144,9 +149,32 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// pair p of a native code word as a bf16x2 word (128 + q_even, 128 + q_odd)
-__device__ __forceinline__ uint32_t unpack_pair(uint32_t w, int p) {
-  return ((w >> (4 * p)) & 0x000F000Fu) | 0x43004300u;
+// the same with a zero accumulator in
+__device__ __forceinline__ void mma16816_z(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                           uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%10, %10, %10, %10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+// (a & m) | c in one logic op; m and c are held in registers (opaque_const), so each pair of
+// codes costs one shift and this one instruction
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t m, uint32_t c) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(m), "r"(c));
+  return r;
+}
+// a constant the compiler keeps in a register instead of re-creating it at every use
+__device__ __forceinline__ uint32_t opaque_const(uint32_t v) {
+  uint32_t r;
+  asm volatile("mov.b32 %0, %1;" : "=r"(r) : "r"(v));
+  return r;
+}
+// pair p of a native code word as a bf16x2 word (128 + q_even, 128 + q_odd): the codes sit in
+// the low mantissa bits of 128.0 (m = 0x000F000F, c = 0x43004300)
+__device__ __forceinline__ uint32_t unpack_pair(uint32_t w, int p, uint32_t m, uint32_t c) {
+  return and_or(w >> (4 * p), m, c);
 }
 
 __device__ __forceinline__ void report_timeout(const TcParams& p, volatile int* abort, int role) {
@@ -209,8 +237,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nsb = sb1 - sb0;
   const int owned = Tc > (int)rank ? (Tc - (int)rank + C - 1) / C : 0;
   const int pitch = nsb * 256 + 16;
-  // warp set h takes local superblocks [kbase, kbase + nh) of every tile
-  const int h = warp >> 3, rw = 16 * (warp & 7);
+  // warp set h takes local superblocks [kbase, kbase + nh) of every tile; warp w of a set holds
+  // tile rows 32 w .. 32 w + 31
+  const int h = warp >> 2, rw = kRows * (warp & 3);
   const int n0 = (nsb + 1) >> 1;
   const int nh = h ? nsb - n0 : n0, kbase = h ? n0 : 0;
   const int nst = Tc * nh;
@@ -230,33 +259,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- weight blocks: this warp's 16 rows, kDepth - 1 blocks ahead (weights only: these may
   // be requested before the previous kernel has finished)
   const uint32_t wring = tc::smem_u32(ring) + (uint32_t)(warp * kDepth * kStage);
-  // issue cursor: the next block's address (tile by tile, local superblock by superblock) and
-  // its ring slot
-  const uint8_t* wnext = p.wq + ((size_t)cid * SB + sb0 + kbase) * kQ4BlockBytes;
+  // issue cursor: this lane's source addresses in the next block (code row rw + lane of each
+  // chunk; lanes 0-15 also 16 bytes of the rows' scales and biases), and its ring slot
+  const uint8_t* blk0 = p.wq + ((size_t)cid * SB + sb0 + kbase) * kQ4BlockBytes;
+  const uint8_t* pcode = blk0 + (rw + lane) * 16;
+  const uint8_t* pscale = blk0 + kCodeBytes + rw * 8 + (lane & 15) * 16;
   const size_t tile_skip = ((size_t)NC * SB - nh) * kQ4BlockBytes;  // last block -> next tile
-  // this lane's pieces: codes (chunk, row) = (piece / 16, piece % 16) for pieces lane and
-  // lane + 32; lanes 0-7 also copy 16 bytes of the rows' scales and biases
-  const int pc0 = lane >> 4, pr0 = lane & 15;
-  const uint32_t src0 = pc0 * 2048 + (rw + pr0) * 16, dst0 = pc0 * kChunkPitch + pr0 * 16;
-  const uint32_t srcs = kCodeBytes + rw * 8 + lane * 16, dsts = kScaleOff + lane * 16;
+  // the weights are read once per step: first out of L2, leaving room for the prefetch
+  const uint64_t pol_w = tc::policy_evict_first();
   int is_n = 0, is_k = 0;
-  uint32_t is_dst = wring;
+  uint32_t is_dst = wring + lane * 16;
+  const uint32_t ring_end = wring + kDepth * kStage;
   auto issue = [&]() {
     if (is_n < nst) {
-      cp_async16s(is_dst + dst0, wnext + src0);
-      cp_async16s(is_dst + dst0 + 2 * kChunkPitch, wnext + src0 + 2 * 2048);
-      if (lane < 8) cp_async16s(is_dst + dsts, wnext + srcs);
-      wnext += kQ4BlockBytes;
+      cp_async16s(is_dst, pcode, pol_w);
+      cp_async16s(is_dst + kChunkPitch, pcode + 2048, pol_w);
+      cp_async16s(is_dst + 2 * kChunkPitch, pcode + 2 * 2048, pol_w);
+      cp_async16s(is_dst + 3 * kChunkPitch, pcode + 3 * 2048, pol_w);
+      if (lane < 16) cp_async16s(is_dst + kScaleOff, pscale, pol_w);
+      pcode += kQ4BlockBytes;
+      pscale += kQ4BlockBytes;
       if (++is_k == nh) {
         is_k = 0;
-        wnext += tile_skip;
+        pcode += tile_skip;
+        pscale += tile_skip;
       }
       ++is_n;
-      is_dst = is_dst + kStage == wring + kDepth * kStage ? wring : is_dst + kStage;
+      is_dst += kStage;
+      if (is_dst >= ring_end) is_dst -= kDepth * kStage;
     }
     cp_async_commit();
   };
   for (int s = 0; s < kDepth - 1; ++s) issue();
+  if (threadIdx.x == 0 && pass == 0)  // the next kernel's weights, while HBM has room
+    tc::l2_prefetch_share(p.pf, p.pf_bytes, blockIdx.x, gridDim.x);
 
   pdl_wait();
   // ---- the operand slice of this k-range (zero columns past the pass's rows), all pieces in
@@ -313,17 +349,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
-  float y[NB8][4];
+  float y[2][NB8][4];  // [row block u][n8 block][fragment]
 #pragma unroll
-  for (int nb = 0; nb < NB8; ++nb)
+  for (int u = 0; u < 2; ++u)
 #pragma unroll
-    for (int c = 0; c < 4; ++c) y[nb][c] = 0.f;
-  // per-lane views: code words of rows g / g + 8 (chunk 2G + t/2, half t&1), scales, operand
+    for (int nb = 0; nb < NB8; ++nb)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) y[u][nb][c] = 0.f;
+  // per-lane views: code words of rows 16u + g / 16u + g + 8 (chunk 2G + t/2, half t&1),
+  // scales, operand
   const uint32_t lane_w = (t >> 1) * kChunkPitch + g * 16 + 8 * (t & 1);
   const uint32_t xlane = tc::smem_u32(xs) + (uint32_t)(g * pitch + 32 * t + kbase * 256);
   const uint32_t xsl = tc::smem_u32(xsum) + (uint32_t)((2 * kbase * N + 2 * t) * 4);
   const uint32_t pitch8 = 8u * (uint32_t)pitch;
   uint32_t st = wring;  // the ring slot consumed next
+  const uint32_t km = opaque_const(0x000F000Fu), kc = opaque_const(0x43004300u);
   for (int j = 0; j < Tc; ++j) {
     float res[H];
     const uint32_t owner = (uint32_t)(j % C);
@@ -337,78 +377,95 @@ __global__ void __launch_bounds__(kThreads, 1)
       issue();
       cp_async_wait<kDepth - 1>();  // block of this stage has landed (this lane's copies) ...
       __syncwarp();                 // ... and every lane's
-      const uint2 sA = lds64(st + kScaleOff + g * 8);
-      const uint2 sB = lds64(st + kScaleOff + (g + 8) * 8);
+      uint2 sv[2][2];               // [u][row g, row g + 8]: (s0, b0), (s1, b1)
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        sv[u][0] = lds64(st + kScaleOff + (16 * u + g) * 8);
+        sv[u][1] = lds64(st + kScaleOff + (16 * u + g + 8) * 8);
+      }
 #pragma unroll
       for (int G = 0; G < 2; ++G) {
-        // lane (g, t): columns 64 G + 16 t .. + 15 of rows g and g + 8, two code words each
-        const uint2 wA = lds64(st + lane_w + G * 2 * kChunkPitch);
-        const uint2 wB = lds64(st + lane_w + G * 2 * kChunkPitch + 128);
+        // operand fragments of group G (both row blocks use them): column nb * 8 + g, the
+        // sixteen columns 64 G + 16 t .. + 15 as bf16 pairs, 8 per MMA pair jp
         const uint32_t xg = xlane + k * 256 + G * 128;
-        const uint32_t xsg = xsl + (2 * k + G) * N * 4;
-        float acc[NB8][4];
-#pragma unroll
-        for (int nb = 0; nb < NB8; ++nb)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc[nb][e] = 0.f;
-#pragma unroll
-        for (int jp = 0; jp < 2; ++jp) {
-          // word jp holds columns 16 t + 8 jp .. + 7: MMA 2 jp takes its pairs 0 and 1, MMA
-          // 2 jp + 1 its pairs 2 and 3 (k index 2t, 2t+1 -> first pair, 2t+8, 2t+9 -> second)
-          const uint32_t a = jp ? wA.y : wA.x, b = jp ? wB.y : wB.x;
-          const uint32_t A0[4] = {unpack_pair(a, 0), unpack_pair(b, 0), unpack_pair(a, 1),
-                                  unpack_pair(b, 1)};
-          const uint32_t A1[4] = {unpack_pair(a, 2), unpack_pair(b, 2), unpack_pair(a, 3),
-                                  unpack_pair(b, 3)};
-#pragma unroll
-          for (int nb = 0; nb < NB8; ++nb) {
-            // operand column nb * 8 + g, the same eight columns as bf16 pairs
-            const uint4 xv = lds128(xg + nb * pitch8 + 16 * jp);
-            mma16816(acc[nb], A0, xv.x, xv.y);
-            mma16816(acc[nb], A1, xv.z, xv.w);
-          }
-        }
-        const uint32_t swa = G ? sA.y : sA.x, swb = G ? sB.y : sB.x;
-        const float s_a = bf16_lo(swa), s_b = bf16_lo(swb);
-        const float c_a = fmaf(-128.f, s_a, bf16_hi(swa)), c_b = fmaf(-128.f, s_b, bf16_hi(swb));
+        uint4 xv[2][NB8];
+        float2 X[NB8];
 #pragma unroll
         for (int nb = 0; nb < NB8; ++nb) {
-          const uint2 Xw = lds64(xsg + nb * 32);
-          const float2 X = make_float2(__uint_as_float(Xw.x), __uint_as_float(Xw.y));
-          y[nb][0] = fmaf(s_a, acc[nb][0], fmaf(c_a, X.x, y[nb][0]));
-          y[nb][1] = fmaf(s_a, acc[nb][1], fmaf(c_a, X.y, y[nb][1]));
-          y[nb][2] = fmaf(s_b, acc[nb][2], fmaf(c_b, X.x, y[nb][2]));
-          y[nb][3] = fmaf(s_b, acc[nb][3], fmaf(c_b, X.y, y[nb][3]));
+          xv[0][nb] = lds128(xg + nb * pitch8);
+          xv[1][nb] = lds128(xg + nb * pitch8 + 16);
+          const uint2 Xw = lds64(xsl + ((2 * k + G) * N + nb * 8) * 4);
+          X[nb] = make_float2(__uint_as_float(Xw.x), __uint_as_float(Xw.y));
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          // lane (g, t): columns 64 G + 16 t .. + 15 of rows 16u + g and 16u + g + 8
+          const uint32_t wa = st + lane_w + G * 2 * kChunkPitch + u * 256;
+          const uint2 wA = lds64(wa), wB = lds64(wa + 128);
+          float acc[NB8][4];
+#pragma unroll
+          for (int jp = 0; jp < 2; ++jp) {
+            // word jp holds columns 16 t + 8 jp .. + 7: MMA 2 jp takes its pairs 0 and 1,
+            // MMA 2 jp + 1 its pairs 2 and 3 (k index 2t, 2t+1 -> first pair, 2t+8, 2t+9 ->
+            // second)
+            const uint32_t a = jp ? wA.y : wA.x, b = jp ? wB.y : wB.x;
+            const uint32_t A0[4] = {unpack_pair(a, 0, km, kc), unpack_pair(b, 0, km, kc),
+                                    unpack_pair(a, 1, km, kc), unpack_pair(b, 1, km, kc)};
+            const uint32_t A1[4] = {unpack_pair(a, 2, km, kc), unpack_pair(b, 2, km, kc),
+                                    unpack_pair(a, 3, km, kc), unpack_pair(b, 3, km, kc)};
+#pragma unroll
+            for (int nb = 0; nb < NB8; ++nb) {
+              if (jp == 0) mma16816_z(acc[nb], A0, xv[0][nb].x, xv[0][nb].y);
+              else mma16816(acc[nb], A0, xv[jp][nb].x, xv[jp][nb].y);
+              mma16816(acc[nb], A1, xv[jp][nb].z, xv[jp][nb].w);
+            }
+          }
+          const uint32_t swa = G ? sv[u][0].y : sv[u][0].x, swb = G ? sv[u][1].y : sv[u][1].x;
+          const float s_a = bf16_lo(swa), s_b = bf16_lo(swb);
+          const float c_a = fmaf(-128.f, s_a, bf16_hi(swa));
+          const float c_b = fmaf(-128.f, s_b, bf16_hi(swb));
+#pragma unroll
+          for (int nb = 0; nb < NB8; ++nb) {
+            y[u][nb][0] = fmaf(s_a, acc[nb][0], fmaf(c_a, X[nb].x, y[u][nb][0]));
+            y[u][nb][1] = fmaf(s_a, acc[nb][1], fmaf(c_a, X[nb].y, y[u][nb][1]));
+            y[u][nb][2] = fmaf(s_b, acc[nb][2], fmaf(c_b, X[nb].x, y[u][nb][2]));
+            y[u][nb][3] = fmaf(s_b, acc[nb][3], fmaf(c_b, X[nb].y, y[u][nb][3]));
+          }
         }
       }
-      st = st + kStage == wring + kDepth * kStage ? wring : st + kStage;
+      st += kStage;
+      if (st >= ring_end) st = wring;
       __syncwarp();  // the slot is refilled by the next iteration's copies
     }
 
     // ---- end of tile j: hi + lo parts into the warp set's half of the hand-off buffer
     float* sa = sacc + (size_t)((j & 1) * 2 + h) * 128 * H;
-    if constexpr (NB8 == 1) {
-      float v[4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) v[c] = y[0][c] + __shfl_xor_sync(0xffffffffu, y[0][c], 2);
-      if (t < 2) {
-        *reinterpret_cast<float2*>(sa + (rw + g) * H + 2 * t) = make_float2(v[0], v[1]);
-        *reinterpret_cast<float2*>(sa + (rw + g + 8) * H + 2 * t) = make_float2(v[2], v[3]);
-      }
-    } else {
+    for (int u = 0; u < 2; ++u) {
+      const int r0 = rw + 16 * u + g;
+      if constexpr (NB8 == 1) {
+        float v[4];
 #pragma unroll
-      for (int nb = 0; nb < NB8 / 2; ++nb) {
-        const float* lo = y[nb + NB8 / 2];
-        *reinterpret_cast<float2*>(sa + (rw + g) * H + nb * 8 + 2 * t) =
-            make_float2(y[nb][0] + lo[0], y[nb][1] + lo[1]);
-        *reinterpret_cast<float2*>(sa + (rw + g + 8) * H + nb * 8 + 2 * t) =
-            make_float2(y[nb][2] + lo[2], y[nb][3] + lo[3]);
+        for (int c = 0; c < 4; ++c) v[c] = y[u][0][c] + __shfl_xor_sync(0xffffffffu, y[u][0][c], 2);
+        if (t < 2) {
+          *reinterpret_cast<float2*>(sa + r0 * H + 2 * t) = make_float2(v[0], v[1]);
+          *reinterpret_cast<float2*>(sa + (r0 + 8) * H + 2 * t) = make_float2(v[2], v[3]);
+        }
+      } else {
+#pragma unroll
+        for (int nb = 0; nb < NB8 / 2; ++nb) {
+          const float* lo = y[u][nb + NB8 / 2];
+          *reinterpret_cast<float2*>(sa + r0 * H + nb * 8 + 2 * t) =
+              make_float2(y[u][nb][0] + lo[0], y[u][nb][1] + lo[1]);
+          *reinterpret_cast<float2*>(sa + (r0 + 8) * H + nb * 8 + 2 * t) =
+              make_float2(y[u][nb][2] + lo[2], y[u][nb][3] + lo[3]);
+        }
       }
+#pragma unroll
+      for (int nb = 0; nb < NB8; ++nb)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) y[u][nb][c] = 0.f;
     }
-#pragma unroll
-    for (int nb = 0; nb < NB8; ++nb)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) y[nb][c] = 0.f;
     tc::named_bar_sync(2, kThreads);
     if (warp < 4) {
       // ---- tile row r: both halves, then the cluster's partials, then the epilogue
