@@ -75,7 +75,7 @@ struct TcParams {
   const float* sinv;
   uint16_t* arena;
   uint8_t* qtile;
-  // 4-bit affine weights in the native block layout of gemm_q4.cu (launch_q4_csk only)
+  // 4-bit affine weights in the native block layout of gemm_q4.cu (launch_q4_rd only)
   const uint8_t* wq;
   // L2 prefetch of the weights the next kernel of the step streams (pf_bytes == 0: none), spread
   // over the CTAs of the launch while this one's own weight loads are marked evict-first
@@ -117,8 +117,8 @@ bool csk_plan(int RB, int KS, int BN, int num_sms, CskPlan* out);
 bool launch_tc_csk(const CUtensorMap& tw, const CUtensorMap& tx, TcParams p, int BN, int num_sms,
                    cudaStream_t s);
 
-// ---- 4-bit affine decode projections (gemm_q4.cu) --------------------------------------------
-// Native layout: per (128-row tile, 128-column super-block) one block of kQ4BlockBytes (codes
+// ---- 4-bit affine decode projections (gemm_q4.cu: device layout; gemm_q4r.cu: kernel) ------
+// Native layout: per (128-row tile, 128-column superblock) one block of kQ4BlockBytes (codes
 // as [4][128 rows][16 bytes], then bf16 scale/bias pairs of the block's two 64-column groups).
 constexpr int kQ4BlockBytes = 128 * 64 + 128 * 8;
 // bytes of the native copy of an [M][K] matrix (F > 0: SwiGLU gate/up pair, M = 2F); 0 when K
@@ -128,12 +128,9 @@ size_t q4_native_bytes(int M, int K, int F);
 // scales and biases [M][K/64])
 bool launch_q4_repack(const uint32_t* packed, const uint16_t* scales, const uint16_t* biases,
                       int M, int K, int F, uint8_t* out, cudaStream_t s);
-// y = x W^T over n_act <= BN/2 decode rows (hi/lo operand) with W = p.wq; tx as for
-// launch_tc_csk.  Any TcParams epilogue.
-bool launch_q4_csk(const CUtensorMap& tx, TcParams p, int BN, int num_sms, cudaStream_t s);
-// The same projection with the codes dequantised in registers (gemm_q4r.cu): x is the operand
-// buffer (bf16 rows of K columns: hi parts at rows b, lo parts at rows x_lo + b), n_act <= 32
-// rows taken 8 at a time.  Any TcParams epilogue.
+// y = x W^T over n_act <= 32 decode rows with W = p.wq in the native layout, the codes
+// dequantised in registers; x is the operand buffer (bf16 rows of K columns: hi parts at rows b,
+// lo parts at rows x_lo + b), the rows taken 8 at a time.  Any TcParams epilogue.
 bool launch_q4_rd(TcParams p, const uint16_t* x, int x_lo, int num_sms, cudaStream_t s);
 
 // ---- tensor-core decode attention (attn_tc.cu) ------------------------------------------------
