@@ -274,6 +274,11 @@ def gpu_arm(args, rank: int, world: int):
         achieved = proj_bytes / (proj_ms / 1e3) / 1e9 if proj_ms > 0 else None
         attn_gbs = attn_bytes / (attn_ms / 1e3) / 1e9 if attn_ms > 0 else None
         kt_ms = ms / K * KT  # the timed region's duration for KT steps
+        if wl.shape.weight_format == "bf16":
+            traffic = measured_traffic("projection")
+        else:  # the 4-bit projections stream their weights once per 8 rows
+            traffic = measured_traffic("projection_affine4")
+            traffic = traffic * ((Bsz + 7) // 8) if traffic is not None else None
         result = {
             "metric": METRIC,
             "value": Bsz * K * world / (ms_max / 1e3),
@@ -301,8 +306,7 @@ def gpu_arm(args, rank: int, world: int):
                          "frac": achieved / hbm_peak if achieved else None,
                          "share_of_step": proj_ms / kt_ms if kt_ms > 0 else None,
                          "launch_groups": proj_n, "timed_steps": KT,
-                         "traffic": measured_traffic("projection" if wl.shape.weight_format == "bf16"
-                                                     else "projection_affine4")},
+                         "traffic": traffic},
             "attention_roofline": {"kernel": "RoPE + KV append + split-K decode attention + merge",
                                    "bound": "hbm", "achieved": attn_gbs, "peak": hbm_peak,
                                    "unit": "GB/s",

@@ -614,8 +614,7 @@ static const CUtensorMap* xmap_kb(cbt_engine* e, const uint16_t* buf, int K, int
 static bool tc_projection(cbt_engine* e, const CUtensorMap& wmap, const CUtensorMap& wmap_kb,
                           const uint8_t* q4w, const uint16_t* xbuf, int n, int K, int M, Epilogue epi, float* out,
                           int ldo, uint16_t* act_out, int act_ld, bool norm_in = false,
-                          const uint16_t* next_gain = nullptr, int layer = 0,
-                          const void* pf = nullptr, size_t pf_bytes = 0) {
+                          const uint16_t* next_gain = nullptr, int layer = 0) {
   const bool split = n <= 32;
   const int BN = split ? tc_split_bn(n) : tc_plain_bn(n);
   const CUtensorMap* xm = split ? xmap_kb(e, xbuf, K, BN) : xmap(e, xbuf, K, BN);
@@ -657,8 +656,6 @@ static bool tc_projection(cbt_engine* e, const CUtensorMap& wmap, const CUtensor
   p.part = e->tc_part;
   p.cnt = e->tc_cnt;
   p.err = e->err;
-  p.pf = pf;
-  p.pf_bytes = pf_bytes;
   const int Mo = epi == EPI_SWIGLU ? M / 2 : M;
   int t = tbegin(e, CBT_KCLASS_PROJ);
   // decode rows: cluster split-K (partial sums meet in distributed shared memory); prefill
@@ -696,19 +693,6 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
   const bool fused = tcp && !gather && n <= 32;
   const int lo = tc_lo_rows(e, n), lo_out = tc_lo_rows(e, n_out);
   bool ok = true;
-  // 4-bit decode: the weights of projection `which` (0 QKV, 1 O, 2 gate/up, 3 down) of layer l
-  // (past the last layer: the lm_head), which the projection before it prefetches into L2
-  auto q4n = [&](int l, int which) -> std::pair<const void*, size_t> {
-    if (c.weight_format != CBT_WEIGHTS_AFFINE4 || !fused) return {nullptr, 0};
-    if (l >= c.n_layers) return {e->q4_lm, q4_native_bytes(c.vocab, d, 0)};
-    const auto& w = e->q4w[l];
-    switch (which) {
-      case 0: return {w.qkv, q4_native_bytes(qd + 2 * kvd, d, 0)};
-      case 1: return {w.o, q4_native_bytes(d, qd, 0)};
-      case 2: return {w.gu, q4_native_bytes(2 * F, d, F)};
-      default: return {w.d, q4_native_bytes(d, F, 0)};
-    }
-  };
   int t = tbegin(e, CBT_KCLASS_OTHER);
   launch_embed(tokens, n, static_cast<const uint16_t*>(e->w.embed), d, c.vocab, e->x, e->err,
                fused ? e->ss : nullptr, e->ss_ld,
@@ -731,7 +715,7 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
     if (tcp)
       ok &= tc_projection(e, e->wmaps[l].qkv, e->wmaps_kb[l].qkv, e->q4w[l].qkv, e->act_h, n, d, qd + 2 * kvd,
                           fused ? EPI_QKV : EPI_STORE, e->qkv, qd + 2 * kvd, nullptr, 0, fused,
-                          nullptr, l, q4n(l, 1).first, q4n(l, 1).second);
+                          nullptr, l);
     else
       projection(e, e->h, n, d, L.wqkv, qd + 2 * kvd, EPI_STORE, e->qkv);
     t = tbegin(e, CBT_KCLASS_ATTN);
@@ -772,7 +756,7 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
     tend(e, t, attn_bytes);
     if (tcp)
       ok &= tc_projection(e, e->wmaps[l].o, e->wmaps_kb[l].o, e->q4w[l].o, e->act_o, n, qd, d, EPI_ADD, e->x, d, nullptr, 0,
-                          false, fused ? fn : nullptr, 0, q4n(l, 2).first, q4n(l, 2).second);
+                          false, fused ? fn : nullptr);
     else
       projection(e, e->o, n, qd, L.wo, d, EPI_ADD, e->x);
     if (!fused) {
@@ -783,14 +767,13 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
     }
     if (tcp) {
       ok &= tc_projection(e, e->wmaps[l].gu, e->wmaps_kb[l].gu, e->q4w[l].gu, e->act_h, n, d, 2 * F, EPI_SWIGLU, nullptr, 0,
-                          e->act_u, F, fused, nullptr, 0, q4n(l, 3).first, q4n(l, 3).second);
+                          e->act_u, F, fused);
       // the down projection's epilogue prepares the next layer's (or the final) RMSNorm
       const uint16_t* next_g = l + 1 < c.n_layers
                                    ? static_cast<const uint16_t*>(e->layers[l + 1].attn_norm)
                                    : static_cast<const uint16_t*>(e->w.final_norm);
       ok &= tc_projection(e, e->wmaps[l].d, e->wmaps_kb[l].d, e->q4w[l].d, e->act_u, n, F, d, EPI_ADD, e->x, d, nullptr, 0,
-                          false, fused ? next_g : nullptr, 0, q4n(l + 1, 0).first,
-                          q4n(l + 1, 0).second);
+                          false, fused ? next_g : nullptr);
     } else {
       projection(e, e->h, n, d, L.wgu, 2 * F, EPI_SWIGLU, e->act);
       projection(e, e->act, n, F, L.wd, d, EPI_ADD, e->x);

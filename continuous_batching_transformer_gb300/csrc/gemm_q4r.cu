@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint8_t* pcode = blk0 + (rw + lane) * 16;
   const uint8_t* pscale = blk0 + kCodeBytes + rw * 8 + (lane & 15) * 16;
   const size_t tile_skip = ((size_t)NC * SB - nh) * kQ4BlockBytes;  // last block -> next tile
-  // the weights are read once per step: first out of L2, leaving room for the prefetch
+  // the weights are read once per step: first out of L2
   const uint64_t pol_w = tc::policy_evict_first();
   int is_n = 0, is_k = 0;
   uint32_t is_dst = wring + lane * 16;
@@ -291,8 +291,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     cp_async_commit();
   };
   for (int s = 0; s < kDepth - 1; ++s) issue();
-  if (threadIdx.x == 0 && pass == 0)  // the next kernel's weights, while HBM has room
-    tc::l2_prefetch_share(p.pf, p.pf_bytes, blockIdx.x, gridDim.x);
 
   pdl_wait();
   // ---- the operand slice of this k-range (zero columns past the pass's rows), all pieces in

@@ -77,10 +77,6 @@ struct TcParams {
   uint8_t* qtile;
   // 4-bit affine weights in the native block layout of gemm_q4.cu (launch_q4_rd only)
   const uint8_t* wq;
-  // L2 prefetch of the weights the next kernel of the step streams (pf_bytes == 0: none), spread
-  // over the CTAs of the launch while this one's own weight loads are marked evict-first
-  const void* pf;
-  size_t pf_bytes;
 };
 
 

@@ -74,25 +74,6 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
-// Bring [p, p + bytes) into L2 (bulk, asynchronous, no completion to wait for); p and bytes
-// multiples of 16
-__device__ __forceinline__ void l2_prefetch_bulk(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-// This CTA's share (CTA `id` of `n`) of an L2 prefetch of [base, base + bytes), issued by one
-// thread in pieces of at most 64 KB
-__device__ __forceinline__ void l2_prefetch_share(const void* base, size_t bytes, int id, int n) {
-  if (!base || bytes < 16 || n <= 0) return;
-  const size_t units = bytes / 16;  // whole 16-byte units only
-  const size_t u0 = units * id / n, u1 = units * (id + 1) / n;
-  const uint8_t* p = static_cast<const uint8_t*>(base) + u0 * 16;
-  for (size_t left = (u1 - u0) * 16; left > 0;) {
-    const uint32_t b = left > 65536 ? 65536u : (uint32_t)left;
-    l2_prefetch_bulk(p, b);
-    p += b;
-    left -= b;
-  }
-}
 // 2-D tiled load; x is the inner (contiguous) coordinate in elements, y the row
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uint64_t* bar, int x,
                                             int y, uint64_t policy) {
