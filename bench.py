@@ -375,20 +375,23 @@ def trace_arm(args):
     outputs geometric with mean 256, live cap 8): every generated token over the wall-clock
     time, with time to first token, time per output token and the decode steps' roofline
     fraction.  `7b-bf16-trace` waits for the arrival times; `7b-bf16-trace-t0` lets every
-    request arrive at t = 0 (a throughput replay)."""
+    request arrive at t = 0 (a throughput replay).  `-chunked` in the name admits prompts in
+    chunks of 2048 tokens with one decode step between chunks (the batching design's joiner
+    prefill) instead of whole prompts at a boundary."""
     import numpy as np
     import torch
 
     import continuous_batching_transformer_gb300 as cbt
     from continuous_batching_transformer_gb300 import binding as B
     from continuous_batching_transformer_gb300.model import DeviceWeights, Engine
-    from continuous_batching_transformer_gb300.trace import percentiles, run_trace
+    from continuous_batching_transformer_gb300.trace import decode_gaps, percentiles, run_trace
     from synth.recipes import MISTRAL_7B, Request, trace_requests
 
     device = torch.device("cuda:0")
     torch.cuda.set_device(device)
     cbt.build()
     realtime = not args.workload.endswith("-t0")
+    chunk = 2048 if "-chunked" in args.workload else None
     seed = 1
     reqs = trace_requests(64, 2.0, 256, 4096, 256.0, 4096, seed)
     live_cap = 8
@@ -402,7 +405,7 @@ def trace_arm(args):
     run_trace(eng, warm, seed, live_cap=live_cap)
     launches0 = B.kernel_launches()
     clk = ClockSampler(None)
-    res = run_trace(eng, reqs, seed, live_cap=live_cap, realtime=realtime)
+    res = run_trace(eng, reqs, seed, live_cap=live_cap, realtime=realtime, chunk_tokens=chunk)
     clocks = clk.stop()
     launches = B.kernel_launches() - launches0
     shape = MISTRAL_7B
@@ -415,8 +418,10 @@ def trace_arm(args):
         "ms_per_step": 1e3 * float(np.mean(res.step_s)) if res.step_s else None,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded weights, prompts and arrival times)",
-        "config": {"workload": "trace-64req-poisson2-" + ("realtime" if realtime else "t0"),
-                   "model": shape.name, "live_cap": live_cap, "parallelism": "1 gpu"},
+        "config": {"workload": "trace-64req-poisson2-" + ("realtime" if realtime else "t0")
+                               + ("-chunk2048" if chunk else ""),
+                   "model": shape.name, "live_cap": live_cap, "admission_chunk": chunk,
+                   "parallelism": "1 gpu"},
         "trace": {"requests": len(reqs), "generated_tokens": res.generated,
                   "wall_s": res.wall_s, "decode_steps": res.steps,
                   "mean_live_rows": float(np.mean(res.step_rows)) if res.step_rows else 0.0,
@@ -424,6 +429,7 @@ def trace_arm(args):
                   "decode_s": float(np.sum(res.step_s)),
                   "ttft_s": percentiles(res.ttft_s.values()),
                   "tpot_s": percentiles(res.tpot_s.values()),
+                  "decode_gap_s": percentiles(decode_gaps(res), (50, 95, 100)),
                   "decode_step_frac_of_8TBps": percentiles(step_frac, (5, 50, 95))},
         "gpu_launches": int(launches),
         "clocks": clocks,

@@ -36,6 +36,8 @@ class TraceResult:
     steps: int = 0                                      # decode steps
     step_rows: list = field(default_factory=list)       # live rows of each decode step
     step_s: list = field(default_factory=list)          # duration of each decode step
+    step_start: list = field(default_factory=list)      # its start, seconds from the trace start
+    step_reqs: list = field(default_factory=list)       # the request indices it decoded
     step_kv_tokens: list = field(default_factory=list)  # live positions the step's attention read
     prefill_tokens: int = 0
     prefill_s: float = 0.0
@@ -51,8 +53,12 @@ def prompt_tokens(req, seed: int, vocab: int) -> np.ndarray:
 
 def run_trace(eng, reqs, seed: int, live_cap: int = 8, realtime: bool = False,
               record_tokens: bool = False, max_prefill_tokens: int | None = None,
-              slab_margin: int = 8) -> TraceResult:
-    """Serve `reqs` on `eng` (an ``Engine``) with continuous batching; see the module text."""
+              slab_margin: int = 8, chunk_tokens: int | None = None) -> TraceResult:
+    """Serve `reqs` on `eng` (an ``Engine``) with continuous batching; see the module text.
+    With `chunk_tokens`, prompts are admitted in chunks instead (``run_trace_chunked``)."""
+    if chunk_tokens:
+        return run_trace_chunked(eng, reqs, seed, chunk_tokens, live_cap, realtime,
+                                 record_tokens, slab_margin)
     dev = eng.weights.device
     vocab = eng.shape.vocab
     stream = eng.stream
@@ -124,6 +130,8 @@ def run_trace(eng, reqs, seed: int, live_cap: int = 8, realtime: bool = False,
         res.steps += 1
         res.step_rows.append(B)
         res.step_s.append(tb - ta)
+        res.step_start.append(ta - t0)
+        res.step_reqs.append(tuple(r[0] for r in live))
         # row r reads positions [0, prompt + produced] (the new token is appended first)
         res.step_kv_tokens.append(sum(reqs[r[0]].prompt_len + r[2] for r in live))
         step_tokens = nxt[:B].cpu().tolist() if record_tokens else None
@@ -141,6 +149,136 @@ def run_trace(eng, reqs, seed: int, live_cap: int = 8, realtime: bool = False,
         tok[:B] = nxt[:B]
     res.wall_s = now()
     return res
+
+
+def run_trace_chunked(eng, reqs, seed: int, chunk_tokens: int, live_cap: int = 8,
+                      realtime: bool = False, record_tokens: bool = False,
+                      slab_margin: int = 8) -> TraceResult:
+    """Continuous batching with chunked admission (the batching design's joiner prefill: one
+    chunk per scheduler iteration, one decode step between chunks, so a running row waits at
+    most one chunk for each joiner).  At every boundary the driver
+
+    1. retires finished rows,
+    2. opens a slab for each arrived request while live + joining rows stay within
+       ``live_cap``,
+    3. prefills one chunk of at most ``chunk_tokens`` prompt tokens in one
+       ``prefill_segmented`` call, taken from the joining rows in arrival order (each segment
+       continues its slab where the previous chunk stopped); a row whose prompt is complete
+       takes the argmax of its last logits as its first token and joins the live rows,
+    4. runs one ``decode_step_batch`` over the live rows.
+
+    Time to first token ends with the chunk that completes the prompt."""
+    dev = eng.weights.device
+    vocab = eng.shape.vocab
+    stream = eng.stream
+    live_cap = min(live_cap, eng.max_batch)
+    chunk_tokens = min(chunk_tokens, eng.max_prefill_tokens)
+    order = sorted(range(len(reqs)), key=lambda i: (0.0 if not realtime else reqs[i].arrival_s, i))
+    pending = deque(order)
+    joining = []  # per row: [request index, slab, prompt tokens prefilled]
+    live = []     # per row: [request index, slab, tokens produced, time of last token]
+    prompts = {}
+    res = TraceResult()
+    tok = torch.zeros(eng.max_batch, dtype=torch.int32, device=dev)
+    nxt = torch.zeros(eng.max_batch, dtype=torch.int32, device=dev)
+    t0 = time.perf_counter()
+
+    def now() -> float:
+        return time.perf_counter() - t0
+
+    def arrived(i) -> bool:
+        return not realtime or reqs[i].arrival_s <= now()
+
+    def retire_done():
+        nonlocal live
+        keep = [k for k, r in enumerate(live) if r[2] < reqs[r[0]].output_len]
+        if len(keep) < len(live):
+            eng.retire([r[1] for k, r in enumerate(live) if r[2] >= reqs[r[0]].output_len])
+            if keep:
+                tok[:len(keep)] = tok[torch.tensor(keep, dtype=torch.long, device=dev)]
+            live = [live[k] for k in keep]
+
+    while pending or live or joining:
+        retire_done()
+        if realtime and not live and not joining and pending and not arrived(pending[0]):
+            time.sleep(max(0.0, reqs[pending[0]].arrival_s - now()))
+        while pending and len(live) + len(joining) < live_cap and arrived(pending[0]):
+            i = pending.popleft()
+            slab = eng.kv_slab_alloc(reqs[i].prompt_len + reqs[i].output_len + slab_margin)
+            joining.append([i, slab, 0])
+            prompts[i] = prompt_tokens(reqs[i], seed, vocab)
+        if joining:
+            segs, left = [], chunk_tokens
+            for row in joining:
+                if left == 0:
+                    break
+                n = min(reqs[row[0]].prompt_len - row[2], left)
+                segs.append((row, row[2], row[2] + n))
+                left -= n
+            host = np.concatenate([prompts[row[0]][a:b] for row, a, b in segs])
+            dtok = torch.from_numpy(host.astype(np.int32)).to(dev, non_blocking=False)
+            first = torch.empty(len(segs), dtype=torch.int32, device=dev)
+            ta = time.perf_counter()
+            eng.prefill_segmented([row[1] for row, _, _ in segs], [b - a for _, a, b in segs],
+                                  dtok, None, first)
+            stream.synchronize()
+            tb = time.perf_counter()
+            res.prefill_tokens += len(host)
+            res.prefill_s += tb - ta
+            done = [k for k, (row, _, b) in enumerate(segs) if b == reqs[row[0]].prompt_len]
+            firsts = first.cpu().tolist() if (record_tokens and done) else None
+            rows_before = len(live)
+            for row, _, b in segs:
+                row[2] = b
+            for k in done:
+                i, slab = segs[k][0][0], segs[k][0][1]
+                live.append([i, slab, 1, tb - t0])
+                res.ttft_s[i] = (tb - t0) - (reqs[i].arrival_s if realtime else 0.0)
+                res.generated += 1
+                if record_tokens:
+                    res.tokens[i] = [firsts[k]]
+            if done:
+                idx = torch.tensor(done, dtype=torch.long, device=dev)
+                tok[rows_before:rows_before + len(done)] = first[idx]
+            joining = [row for row in joining if row[2] < reqs[row[0]].prompt_len]
+            retire_done()  # rows complete on their first token leave before the step
+        if not live:
+            continue
+        B = len(live)
+        ta = time.perf_counter()
+        eng.decode_step_batch([r[1] for r in live], tok[:B], None, nxt[:B])
+        stream.synchronize()
+        tb = time.perf_counter()
+        res.steps += 1
+        res.step_rows.append(B)
+        res.step_s.append(tb - ta)
+        res.step_start.append(ta - t0)
+        res.step_reqs.append(tuple(r[0] for r in live))
+        res.step_kv_tokens.append(sum(reqs[r[0]].prompt_len + r[2] for r in live))
+        step_tokens = nxt[:B].cpu().tolist() if record_tokens else None
+        for k, r in enumerate(live):
+            r[2] += 1
+            res.generated += 1
+            if record_tokens:
+                res.tokens[r[0]].append(step_tokens[k])
+            if r[2] >= reqs[r[0]].output_len:
+                n = reqs[r[0]].output_len
+                first_t = res.ttft_s[r[0]] + (reqs[r[0]].arrival_s if realtime else 0.0)
+                res.tpot_s[r[0]] = ((tb - t0) - first_t) / max(1, n - 1)
+        tok[:B] = nxt[:B]
+    res.wall_s = now()
+    return res
+
+
+def decode_gaps(res: TraceResult):
+    """Time between the end of one decode step and the start of the next, for consecutive
+    steps that share a row: the admission work a running row waits for between two of its
+    tokens (idle time with no row running is not a stall)."""
+    out = []
+    for i in range(len(res.step_s) - 1):
+        if set(res.step_reqs[i]) & set(res.step_reqs[i + 1]):
+            out.append(res.step_start[i + 1] - (res.step_start[i] + res.step_s[i]))
+    return out
 
 
 def percentiles(values, qs=(50, 95)):

@@ -318,6 +318,22 @@ def prefill_segmented(m: OracleModel, caches, seg_lens, tokens) -> np.ndarray:
     return logits
 
 
+def prefill_continue(m: OracleModel, caches, seg_lens, tokens) -> np.ndarray:
+    """Segmented prefill where segment s continues cache s at its current length (a prompt
+    admitted in chunks: the mlx-bun batching design, section 4.2 "Joiner prefill", one chunk
+    per scheduler iteration).  Token j of segment s sits at position caches[s].len + j and
+    attends to [0, that position] of its own cache; returns each segment's last logits.  With
+    empty caches this is prefill_segmented."""
+    lens = [int(n) for n in seg_lens]
+    if any(n <= 0 for n in lens) or sum(lens) != len(tokens):
+        raise ValueError("segment lengths do not cover the tokens")
+    seq = np.repeat(np.arange(len(lens), dtype=np.int32), lens)
+    pos = np.concatenate([np.arange(c.len, c.len + n, dtype=np.int32) for c, n in zip(caches, lens)])
+    want = np.zeros(len(tokens), dtype=np.int32)
+    want[np.cumsum(lens) - 1] = 1
+    return forward(m, caches, seq, pos, tokens, want)
+
+
 def prefill_sequence(m: OracleModel, cache: KVCache, tokens) -> np.ndarray:
     toks = np.ascontiguousarray(tokens, dtype=np.int32)
     logits = np.empty(m.shape.vocab, dtype=np.float32)

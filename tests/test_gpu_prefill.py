@@ -142,3 +142,48 @@ def test_prefill_7b_full_depth_sampled():
     assert eng.device_error() == (0, 0)
     eng.close()
     print(f"7b full depth: prefill {e1:.3e}, decode from the same K/V {e2:.3e}")
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "affine4"])
+def test_chunked_prefill_mixed_calls(fmt):
+    """Prompts admitted in chunks (the batching design's joiner prefill, one chunk per call):
+    each call mixes segments that continue their slab mid-block with segments that start a
+    fresh slab, and the chunks cross 128-query blocks at unaligned positions.  Every call's
+    last-token logits, and two decode steps after the last chunk, against the oracle's
+    continuation of the same chunks."""
+    ensure_built()
+    dev = torch.device("cuda:0")
+    shape = ModelShape("chunk-check", 2, 512, 4, 2, 128, 1024, 2048, 1e-5, 1e6, gain_sigma=0.1,
+                       weight_format=fmt)
+    w = DeviceWeights(shape, dev)
+    om = oracle.OracleModel(shape)
+    lens = [300, 45, 200]
+    toks = [seeded_tokens(n, 400 + r, shape.vocab) for r, n in enumerate(lens)]
+    # (row, start, end) per call: row 0 in three chunks, row 2 joins in call 2; call 4 is a
+    # chunk of 20 tokens (the 4-bit format's projections take up to 32 rows in one pass)
+    calls = [[(0, 0, 150), (1, 0, 45)], [(0, 150, 211), (2, 0, 77)], [(2, 77, 180)],
+             [(0, 211, 300), (2, 180, 200)]]
+    eng = Engine(w, arena_bytes=64 << 20, max_batch=8, max_prefill_tokens=256)
+    slabs = [eng.kv_slab_alloc(320) for _ in lens]
+    caches = [oracle.KVCache(shape, 320) for _ in lens]
+    last = {}
+    for c, call in enumerate(calls):
+        seg = [b - a for _, a, b in call]
+        t = np.concatenate([toks[r][a:b] for r, a, b in call])
+        lg = torch.empty((len(call), shape.vocab), dtype=torch.float32, device=dev)
+        eng.prefill_segmented([slabs[r] for r, _, _ in call], seg, to_dev(t, dev), lg)
+        ref = oracle.prefill_continue(om, [caches[r] for r, _, _ in call], seg, t)
+        check_logits(lg.cpu().numpy(), ref, TOL[fmt], f"{fmt} chunk call {c}")
+        for k, (r, _, b) in enumerate(call):
+            assert eng.position(slabs[r]) == b
+            if b == lens[r]:
+                last[r] = ref[k]
+    feed = np.asarray([oracle.argmax(last[r]) for r in range(len(lens))], np.int32)
+    logits = torch.empty((len(lens), shape.vocab), dtype=torch.float32, device=dev)
+    for step in range(2):
+        eng.decode_step_batch(slabs, to_dev(feed, dev), logits)
+        ref = oracle.decode_step_batch(om, caches, feed)
+        check_logits(logits.cpu().numpy(), ref, TOL[fmt], f"{fmt} decode {step} after chunks")
+        feed = np.asarray([oracle.argmax(x) for x in ref], np.int32)
+    assert eng.device_error() == (0, 0)
+    eng.close()

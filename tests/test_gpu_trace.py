@@ -35,13 +35,16 @@ def oracle_greedy(om, req, seed):
     return out, logits
 
 
-def test_trace_rows_match_oracle():
+@pytest.mark.parametrize("chunk", [None, 16])
+def test_trace_rows_match_oracle(chunk):
+    """chunk None: whole prompts per admission; 16: prompts admitted 16 tokens per call, one
+    decode step between chunks (the 17- to 32-token prompts take two or three calls)."""
     ensure_built()
     dev = torch.device("cuda:0")
     w = DeviceWeights(TINY, dev)
     om = oracle.OracleModel(TINY)
     eng = Engine(w, arena_bytes=32 << 20, max_batch=3, max_prefill_tokens=64)
-    res = run_trace(eng, REQS, seed=0, live_cap=3, record_tokens=True)
+    res = run_trace(eng, REQS, seed=0, live_cap=3, record_tokens=True, chunk_tokens=chunk)
     assert eng.device_error() == (0, 0)
     assert res.generated == sum(r.output_len for r in REQS)
     assert eng.stats().live_slabs == 0  # every request's slab was retired

@@ -305,6 +305,33 @@ def test_segmented_equals_per_sequence(pin_model):
         assert np.array_equal(seg[r].k, c.k) and np.array_equal(seg[r].v, c.v) and seg[r].len == n
 
 
+def test_chunked_prefill_equals_one_pass(pin_model):
+    """A prompt admitted in chunks (each continuing its cache, other rows' chunks and new rows
+    sharing the calls) ends with the logits and K/V of one segmented prefill of the prompt."""
+    lens = [13, 5, 9]
+    toks = [synth.tokens(n, 9, synth.stream_tokens(r), PIN_SHAPE.vocab) for r, n in enumerate(lens)]
+    one = [oracle.KVCache(PIN_SHAPE, 16) for _ in lens]
+    ref = oracle.prefill_segmented(pin_model, one, lens, np.concatenate(toks))
+    ch = [oracle.KVCache(PIN_SHAPE, 16) for _ in lens]
+    # call 1: rows 0 and 1 start (4 and 5 tokens: row 1 completes); call 2: row 0 continues
+    # (7 more), row 2 starts (3); call 3: both finish
+    calls = [[(0, 0, 4), (1, 0, 5)], [(0, 4, 11), (2, 0, 3)], [(0, 11, 13), (2, 3, 9)]]
+    last = {}
+    for call in calls:
+        caches = [ch[r] for r, _, _ in call]
+        lg = oracle.prefill_continue(pin_model, caches, [b - a for _, a, b in call],
+                                     np.concatenate([toks[r][a:b] for r, a, b in call]))
+        for k, (r, _, b) in enumerate(call):
+            if b == lens[r]:
+                last[r] = lg[k]
+    for r, n in enumerate(lens):
+        assert np.array_equal(last[r], ref[r])
+        assert ch[r].len == n
+        assert np.array_equal(ch[r].k, one[r].k) and np.array_equal(ch[r].v, one[r].v)
+    with pytest.raises(ValueError):
+        oracle.prefill_continue(pin_model, [ch[0]], [2], np.zeros(3, np.int32))
+
+
 def test_no_cross_row_leakage(pin_model):
     caches, _ = _prefilled(pin_model, [6, 6, 6])
     other = [_clone(c) for c in caches]
