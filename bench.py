@@ -161,6 +161,22 @@ def setup_decode(wl, device, extra_positions: int):
     return w, eng, slabs, ctx, tok
 
 
+def slowest_over_ranks(seconds: float, dist=None, device=None) -> float:
+    """The largest of every rank's `seconds` (each replica times its own steps; the job takes
+    as long as the slowest).  Without a process group, the value itself."""
+    import torch
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replicas_throughput(rows_per_rank: int, steps: int, world: int, slowest_s: float) -> float:
+    """Whole-job tokens per second of `world` independent replicas: every rank decodes
+    `rows_per_rank` rows for `steps` steps; the job ends with the slowest rank."""
+    return rows_per_rank * steps * world / slowest_s
+
+
 def gpu_arm(args, rank: int, world: int):
     import torch
 
@@ -226,10 +242,7 @@ def gpu_arm(args, rank: int, world: int):
     proj_ms, proj_n, proj_bytes = B.engine_timing(eng.handle, B.KCLASS_PROJ)
     attn_ms, attn_n, attn_bytes = B.engine_timing(eng.handle, B.KCLASS_ATTN)
     B.engine_set_timing(eng.handle, 0)
-    t = torch.tensor([ms], dtype=torch.float64, device=device)
-    if dist:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
+    ms_max = slowest_over_ranks(ms, dist, device)
     code, info = eng.device_error()
     if code != 0:
         raise SystemExit(f"device error word set: code {code} info {info}")
@@ -258,10 +271,7 @@ def gpu_arm(args, rank: int, world: int):
             stream.synchronize()
             h_tok.copy_(h_out)
     e2e_s = time.perf_counter() - t0
-    t = torch.tensor([e2e_s], dtype=torch.float64, device=device)
-    if dist:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    e2e_s = float(t.item())
+    e2e_s = slowest_over_ranks(e2e_s, dist, device)
 
     result = None
     if rank == 0:
@@ -281,7 +291,7 @@ def gpu_arm(args, rank: int, world: int):
             traffic = traffic * ((Bsz + 7) // 8) if traffic is not None else None
         result = {
             "metric": METRIC,
-            "value": Bsz * K * world / (ms_max / 1e3),
+            "value": replicas_throughput(Bsz, K, world, ms_max / 1e3),
             "unit": "tok/s",
             "n_gpus": world,
             "steps": K,
@@ -312,7 +322,7 @@ def gpu_arm(args, rank: int, world: int):
                                    "unit": "GB/s",
                                    "frac": attn_gbs / hbm_peak if attn_gbs else None,
                                    "share_of_step": attn_ms / kt_ms if kt_ms > 0 else None},
-            "e2e": {"value": Bsz * K * world / e2e_s, "unit": "tok/s",
+            "e2e": {"value": replicas_throughput(Bsz, K, world, e2e_s), "unit": "tok/s",
                     "h2d_bytes_per_step": 4 * Bsz, "d2h_bytes_per_step": 4 * Bsz},
             "gpu_launches": int(launches),
             "clocks": clk,
