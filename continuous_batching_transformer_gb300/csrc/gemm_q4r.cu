@@ -521,8 +521,10 @@ int q4r_active_clusters(int C, size_t smem) {
 }
 
 // The split of the k-range (C) follows from the matrix shape alone -- so a row's arithmetic
-// does not depend on the number of rows -- by the cost of the busiest CTA at one CTA per SM:
-// superblocks it streams, plus a little for each cluster hand-off.
+// does not depend on the number of rows -- by the cost of the busiest CTA: superblocks it
+// streams, plus a little for each cluster hand-off.  How many clusters of C CTAs run at once is
+// asked of the occupancy calculator (clusters are placed within GPCs, so fewer than
+// num_sms / C may fit), at the widest operand's shared memory.
 bool q4r_split(int RB, int SB, int num_sms, Q4rPlan* out) {
   static const int kSizes[] = {1, 2, 3, 4, 6, 8};
   double best = 1e30;
@@ -534,9 +536,18 @@ bool q4r_split(int RB, int SB, int num_sms, Q4rPlan* out) {
     q.sb_max = (SB + C - 1) / C;
     if (q.sb_max > kMaxSbPerRank) continue;
     q.NC = std::min(RB, num_sms / C);
-    const int tmax = (RB + q.NC - 1) / q.NC;
-    q.slots = C > 1 ? (tmax + C - 1) / C : 0;
+    q.slots = C > 1 ? ((RB + q.NC - 1) / q.NC + C - 1) / C : 0;
     if (q.slots > kMaxSlots || q4r_smem<2>(q) > (size_t)kSmemBudget) continue;
+    const int fit = q4r_active_clusters<2>(C, q4r_smem<2>(q));
+    if (fit <= 0) continue;
+    if (fit < q.NC) {
+      q.NC = fit;
+      q.slots = C > 1 ? ((RB + q.NC - 1) / q.NC + C - 1) / C : 0;
+      if (q.slots > kMaxSlots || q4r_smem<2>(q) > (size_t)kSmemBudget ||
+          q4r_active_clusters<2>(C, q4r_smem<2>(q)) < q.NC)
+        continue;
+    }
+    const int tmax = (RB + q.NC - 1) / q.NC;
     const double cost = (double)tmax * q.sb_max + (C > 1 ? 1.0 : 0.0) + 0.01 * C;
     if (cost < best) {
       best = cost;
@@ -549,20 +560,10 @@ bool q4r_split(int RB, int SB, int num_sms, Q4rPlan* out) {
 }
 
 template <int NB8>
-bool q4r_launch(const TcParams& p, const uint16_t* x, int x_lo, Q4rPlan q, int passes,
-                int num_sms, cudaStream_t s) {
-  // clusters that fit at once (one CTA per SM), and the inbox slots that count needs
-  size_t smem = q4r_smem<NB8>(q);
-  int fit = q4r_active_clusters<NB8>(q.C, smem);
-  if (fit <= 0) return false;
-  if (fit < q.NC) {
-    q.NC = fit;
-    const int tmax = (p.RB + q.NC - 1) / q.NC;
-    q.slots = q.C > 1 ? (tmax + q.C - 1) / q.C : 0;
-    if (q.slots > kMaxSlots) return false;
-    smem = q4r_smem<NB8>(q);
-    if (smem > (size_t)kSmemBudget) return false;
-  }
+bool q4r_launch(const TcParams& p, const uint16_t* x, int x_lo, const Q4rPlan& q, int passes,
+                cudaStream_t s) {
+  // the plan's clusters fit at the widest operand's shared memory, so at this one too
+  const size_t smem = q4r_smem<NB8>(q);
   auto kern = k_q4_rd<NB8>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
@@ -605,6 +606,6 @@ bool launch_q4_rd(TcParams p, const uint16_t* x, int x_lo, int num_sms, cudaStre
     plans[key] = q;
   }
   const int passes = (p.n_act + 7) / 8;
-  return p.n_act <= 4 ? q4r_launch<1>(p, x, x_lo, q, passes, num_sms, s)
-                      : q4r_launch<2>(p, x, x_lo, q, passes, num_sms, s);
+  return p.n_act <= 4 ? q4r_launch<1>(p, x, x_lo, q, passes, s)
+                      : q4r_launch<2>(p, x, x_lo, q, passes, s);
 }
