@@ -10,7 +10,7 @@ import torch
 
 import bench
 import oracle
-from synth.recipes import DECODE_7B_B8, decode_7b_fixed
+from synth.recipes import DECODE_7B_B8, LONG_7B_B32, decode_7b_fixed
 from tests.gpu_harness import TOL, check_logits, ensure_built, to_dev
 
 pytestmark = pytest.mark.gpu
@@ -53,3 +53,17 @@ def test_7b_bf16_b8_ragged_contexts():
 
 def test_7b_affine4_b4_ctx2048():
     run_sampled(decode_7b_fixed(4, 2048, "affine4"), [0, 3], TOL["affine4"])
+
+
+def test_7b_bf16_b32_long_contexts():
+    """The long-context workload (32 rows of 8k-16k tokens, about 64 GB of KV): the rows
+    with the longest and the shortest context, where the split-K attention has the most and
+    the fewest partials to merge."""
+    ctx = [int(c) for c in LONG_7B_B32.context_lengths()]
+    run_sampled(LONG_7B_B32, [int(np.argmax(ctx)), int(np.argmin(ctx))], TOL["bf16"])
+
+
+def test_7b_affine4_b16_two_passes():
+    """4-bit weights at B = 16: the projections take the rows in two passes of 8 over the
+    same weights; rows from both passes."""
+    run_sampled(decode_7b_fixed(16, 2048, "affine4"), [0, 9, 15], TOL["affine4"])
