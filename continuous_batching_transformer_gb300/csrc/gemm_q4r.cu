@@ -59,6 +59,7 @@ constexpr int kCodeBytes = 128 * 64;
 constexpr int kMaxSlots = 4;
 constexpr int kMaxSbPerRank = 24;        // bounds the operand slice kept in shared memory
 constexpr int kSmemBudget = 227 * 1024;
+constexpr int kMaxSsTiles = 64;          // RMSNorm statistics tiles (d_model <= 8192)
 
 struct Q4rPlan {
   int C;       // CTAs per cluster (split of the k-range)
@@ -71,7 +72,7 @@ __host__ __device__ constexpr size_t align16(size_t v) { return (v + 15) & ~size
 
 // Shared-memory carve-up for N operand columns (H = N / 2 batch rows)
 struct Layout {
-  size_t ring, xs, xsum, sacc, inbox, swx, rinv, cosv, sinv, rows, bars, flags, total;
+  size_t ring, xs, xsum, sacc, inbox, swx, rinv, cosv, sinv, rows, ssq, bars, flags, total;
   int pitch;  // bytes per operand row of xs
 };
 
@@ -100,6 +101,8 @@ __host__ __device__ inline Layout layout(int N, const Q4rPlan& q) {
   o = align16(o + (size_t)H * 64 * 4);
   L.rows = o;
   o = align16(o + (size_t)8 * sizeof(QueryRow));
+  L.ssq = o;
+  o = align16(o + (size_t)kMaxSsTiles * 8 * 4);
   L.bars = o;
   o = align16(o + kMaxSlots * 8);
   L.flags = o;
@@ -109,9 +112,8 @@ __host__ __device__ inline Layout layout(int N, const Q4rPlan& q) {
 }
 
 // 16 bytes global -> shared (L2 only); src_bytes < 16: the rest of the 16 bytes are zero-filled
-__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(tc::smem_u32(dst)), "l"(src),
-               "r"(src_bytes)
+__device__ __forceinline__ void cp_async16_zfill_s(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                : "memory");
 }
 // 16 bytes global -> shared (L2 only), with an L2 eviction policy
@@ -220,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* scos = reinterpret_cast<float*>(smem + L.cosv);
   float* ssin = reinterpret_cast<float*>(smem + L.sinv);
   QueryRow* srows = reinterpret_cast<QueryRow*>(smem + L.rows);
+  float* ssq = reinterpret_cast<float*>(smem + L.ssq);
   uint64_t* inbox_full = reinterpret_cast<uint64_t*>(smem + L.bars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.flags);
 
@@ -296,22 +299,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- the operand slice of this k-range (zero columns past the pass's rows), all pieces in
   // flight at once; RMSNorm factors and the QKV epilogue's per-row inputs meanwhile
   {
-    const int per_row = nsb * 16;  // 16-byte pieces
-    for (int idx = threadIdx.x; idx < N * per_row; idx += kThreads) {
-      const int n = idx / per_row, c = idx - n * per_row;
+    const int per_row = nsb * 16;  // 16-byte pieces; warp w copies operand rows w, w + 8, ...
+    for (int n = warp; n < N; n += kWarps) {
       const int b = n % H;
       const bool valid = b < p.n_act;
       const size_t row = n >= H ? (size_t)(x_lo + 8 * pass + b) : (size_t)(8 * pass + b);
-      const uint16_t* src = valid ? x + row * p.K + (size_t)sb0 * 128 + (size_t)c * 8 : x;
-      cp_async16_zfill(xs + (size_t)n * pitch + c * 16, src, valid ? 16u : 0u);
+      const uint16_t* src = x + row * p.K + (size_t)sb0 * 128;
+      const uint32_t dst = tc::smem_u32(xs + (size_t)n * pitch);
+      for (int c = lane; c < per_row; c += 32)
+        cp_async16_zfill_s(dst + c * 16, valid ? src + c * 8 : x, valid ? 16u : 0u);
     }
     cp_async_commit();
   }
-  if (p.ss_in && threadIdx.x < p.n_act) {
-    float s = 0.f;
-    for (int tt = 0; tt < p.ss_tiles; ++tt) s += p.ss_in[(size_t)tt * p.ss_ld + threadIdx.x];
-    rinv[threadIdx.x] = rsqrtf(s / (float)p.K + p.eps);
-  }
+  // the folded RMSNorm's per-tile sums of squares: every value requested at once (one per
+  // thread), added up in tile order after the barrier
+  if (p.ss_in)
+    for (int i = threadIdx.x; i < p.ss_tiles * p.n_act; i += kThreads) {
+      const int tt = i / p.n_act, b = i - tt * p.n_act;
+      ssq[i] = __ldcg(p.ss_in + (size_t)tt * p.ss_ld + b);
+    }
   tcepi::EpiSrc src = tcepi::epi_src_global(p);
   if (p.epi == EPI_QKV) {
     const int half = p.head_dim >> 1;
@@ -326,6 +332,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   cp_async_wait<0>();  // the operand slice (and the weight blocks requested before it)
   __syncthreads();
+  if (p.ss_in && threadIdx.x < p.n_act) {
+    float s = 0.f;
+    for (int tt = 0; tt < p.ss_tiles; ++tt) s += ssq[tt * p.n_act + threadIdx.x];
+    rinv[threadIdx.x] = rsqrtf(s / (float)p.K + p.eps);
+  }
   // each operand column's sum over every group of 64 columns, in a fixed order
   for (int idx = threadIdx.x; idx < 2 * nsb * N; idx += kThreads) {
     const int gl = idx / N, n = idx - gl * N;
@@ -592,6 +603,7 @@ bool launch_q4_rd(TcParams p, const uint16_t* x, int x_lo, int num_sms, cudaStre
   if (!p.wq || !x || p.K % 128 || p.K <= 0 || p.n_act <= 0 || p.n_act > 32) return false;
   if (p.epi == EPI_SWIGLU && (p.F % 64 || p.M != 2 * p.F)) return false;
   if (p.epi == EPI_QKV && (p.head_dim > 128 || p.head_dim % 2)) return false;
+  if (p.ss_in && p.ss_tiles > kMaxSsTiles) return false;
   p.RB = p.epi == EPI_SWIGLU ? p.F / 64 : (p.M + 127) / 128;
   p.KS = p.K / 64;
   p.NT = 1;
