@@ -502,6 +502,33 @@ extern "C" cbt_status cbt_kv_slab_export(cbt_engine* e, int32_t id, void* k, voi
   return slab_copy(e, id, k, v, n, on_host, false);
 }
 
+extern "C" cbt_status cbt_kv_slab_copy_prefix(cbt_engine* e, int32_t src_id, int32_t dst_id,
+                                              int32_t n) {
+  if (!e) return CBT_ERR_NULL;
+  auto si = e->slabs.find(src_id), di = e->slabs.find(dst_id);
+  if (si == e->slabs.end() || di == e->slabs.end()) return CBT_ERR_BAD_SLAB;
+  if (src_id == dst_id || n < 0) return CBT_ERR_INVALID;
+  const Slab& src = si->second;
+  Slab& dst = di->second;
+  if (n > src.pos || n > dst.cap) return CBT_ERR_CAPACITY;
+  if (n > 0) {
+    // every (layer, K|V, kv head) block is a run of positions at the same place in both slabs:
+    // one strided copy of whole 64-position groups (a V block keeps each group of 64 positions
+    // transposed; both layouts' capacities are multiples of 64, so the groups line up)
+    const cbt_model_config& c = e->cfg;
+    const size_t row = (size_t)c.head_dim * 2;
+    const size_t width = (size_t)((n + 63) / 64 * 64) * row;
+    const size_t blocks = (size_t)c.n_layers * 2 * c.n_kv_heads;
+    const char* from = static_cast<const char*>(e->p.kv_arena) + src.offset;
+    char* to = static_cast<char*>(e->p.kv_arena) + dst.offset;
+    if (cudaMemcpy2DAsync(to, (size_t)dst.lcap * row, from, (size_t)src.lcap * row, width, blocks,
+                          cudaMemcpyDeviceToDevice, e->stream) != cudaSuccess)
+      return CBT_ERR_CUDA;
+  }
+  dst.pos = n;
+  return CBT_OK;
+}
+
 // ---- measurement ------------------------------------------------------------------------
 static cudaEvent_t next_event(cbt_engine* e) {
   if (e->ev_used == e->ev_pool.size()) {

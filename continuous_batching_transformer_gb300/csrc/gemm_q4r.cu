@@ -23,10 +23,11 @@
 // to cluster t % NC; rank r of the cluster takes superblocks [r SB / C, (r + 1) SB / C) of its
 // tiles; inside a CTA, warps 0-3 take the first half of those superblocks and warps 4-7 the
 // second half, warp w holding tile rows 32 (w % 4) .. + 31 as two m16 row blocks that share
-// the operand fragments.  The two halves meet in shared
-// memory, the C ranks in the tile owner's shared memory (st.async, added in rank order), and
-// the owner's warps 0-3 run the shared epilogue (RMSNorm scale, residual add and the next
-// norm's statistics and operand, SwiGLU, RoPE + K/V append + the attention's Q operand).
+// the operand fragments.  The two halves meet in shared memory, the C ranks in the tile
+// owner's shared memory (st.async, added in rank order), and the owner's warps 0-3 run the
+// shared epilogue (RMSNorm scale, residual add and the next norm's statistics and operand,
+// SwiGLU, RoPE + K/V append + the attention's Q operand).  C is chosen from the matrix shape
+// and the number of clusters of C CTAs that fit on the GPU at once.
 //
 // Batch rows are taken 8 at a time (gridDim.y passes, each over the same weights): a row's
 // arithmetic -- the k split, the group order, the fold -- depends on the matrix shape alone,

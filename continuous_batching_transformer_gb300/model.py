@@ -130,6 +130,10 @@ class Engine:
         on_host = k.device.type == "cpu"
         B.kv_slab_import(self.handle, slab, k.data_ptr(), v.data_ptr(), n_tokens, on_host)
 
+    def copy_prefix(self, src: int, dst: int, n_tokens: int) -> None:
+        """dst takes positions [0, n_tokens) of src (a shared prompt prefix computed once)."""
+        B.kv_slab_copy_prefix(self.handle, src, dst, n_tokens)
+
     def export_kv(self, slab: int, k: torch.Tensor, v: torch.Tensor, n_tokens: int) -> None:
         on_host = k.device.type == "cpu"
         B.kv_slab_export(self.handle, slab, k.data_ptr(), v.data_ptr(), n_tokens, on_host)

@@ -184,6 +184,19 @@ cbt_status cbt_kv_slab_import(cbt_engine* e, int32_t slab_id, const void* k, con
 cbt_status cbt_kv_slab_export(cbt_engine* e, int32_t slab_id, void* k, void* v,
                               int32_t n_tokens, int32_t on_host);
 
+/* Prefix reuse: copy positions [0, n_tokens) of slab src_id's K and V into slab dst_id and set
+ * dst's position to n_tokens, so a prefill of dst continues after a prefix that was computed
+ * once (the mlx-bun batching design, sections 1 and 4.2: sub-agents share long system
+ * prompts; a joiner's prefill starts from the longest cached prefix, so N agents sharing a
+ * prompt reuse one prefill).  Here the reuse is a device-to-device copy of the prefix's bytes
+ * (n_tokens x 2 x n_layers x n_kv_heads x head_dim bf16), queued on the engine stream; the
+ * slabs stay independent afterwards.
+ *   src_id, dst_id  distinct live slabs; n_tokens <= src's position and <= dst's capacity.
+ * Errors (nothing queued, nothing changed): CBT_ERR_BAD_SLAB, CBT_ERR_INVALID (same slab or
+ * n_tokens < 0), CBT_ERR_CAPACITY, CBT_ERR_CUDA. */
+cbt_status cbt_kv_slab_copy_prefix(cbt_engine* e, int32_t src_id, int32_t dst_id,
+                                   int32_t n_tokens);
+
 /* Segmented prefill of K prompts (forward_batch_segmented).
  *   slab_ids  host int32 [K], distinct live slabs.  Segment s's tokens go to positions
  *             [p_s, p_s + seg_lens[s]) of its slab, p_s being the slab's current position

@@ -172,3 +172,47 @@ def test_quantizer_matches_oracle_bytes(weights):
     assert np.array_equal(packed.cpu().numpy().view(np.uint32), p)
     assert np.array_equal(sc.cpu().numpy().view(np.uint16), s)
     assert np.array_equal(bi.cpu().numpy().view(np.uint16), b)
+
+
+def test_prefix_copy_then_continue(weights):
+    """Prefix reuse: one row prefills a 100-token system prompt plus its own 30 tokens; a second
+    row takes the first 100 positions by copy and prefills only its own 20 tokens.  Its logits
+    (and two decode steps of both rows) match the oracle's full computation; host errors queue
+    nothing and change nothing."""
+    import oracle
+    from tests.gpu_harness import TOL, check_logits
+    dev = torch.device("cuda:0")
+    rng = np.random.default_rng(77)
+    system = rng.integers(0, TINY.vocab, 100).astype(np.int32)
+    own = [rng.integers(0, TINY.vocab, n).astype(np.int32) for n in (30, 20)]
+    eng = Engine(weights, arena_bytes=B.slab_bytes(weights.cfg, 1024), max_batch=4,
+                 max_prefill_tokens=160)
+    a, b, c = eng.kv_slab_alloc(192), eng.kv_slab_alloc(160), eng.kv_slab_alloc(64)
+    lg = torch.empty((1, TINY.vocab), dtype=torch.float32, device=dev)
+    eng.prefill_segmented([a], [130], to_dev(np.concatenate([system, own[0]]), dev), lg)
+    la = lg.cpu().numpy().copy()
+    assert status_of(eng.copy_prefix, a, a, 10) == -1        # same slab
+    assert status_of(eng.copy_prefix, a, b, 131) == -6       # beyond the source's position
+    assert status_of(eng.copy_prefix, a, c, 100) == -6       # beyond the target's capacity
+    assert status_of(eng.copy_prefix, a, 999, 10) == -3      # unknown slab
+    assert eng.position(b) == 0 and eng.position(c) == 0
+    eng.copy_prefix(a, b, 100)
+    assert eng.position(b) == 100
+    eng.prefill_segmented([b], [20], to_dev(own[1], dev), lg)
+    lb = lg.cpu().numpy().copy()
+
+    om = oracle.OracleModel(TINY)
+    ca, cb = oracle.KVCache(TINY, 192), oracle.KVCache(TINY, 160)
+    ra = oracle.prefill_segmented(om, [ca], [130], np.concatenate([system, own[0]]))
+    rb = oracle.prefill_segmented(om, [cb], [120], np.concatenate([system, own[1]]))
+    check_logits(la, ra, TOL["bf16"], "row a prefill")
+    check_logits(lb, rb, TOL["bf16"], "row b after the copied prefix")
+    feed = np.array([oracle.argmax(ra[0]), oracle.argmax(rb[0])], np.int32)
+    lg2 = torch.empty((2, TINY.vocab), dtype=torch.float32, device=dev)
+    for step in range(2):
+        eng.decode_step_batch([a, b], to_dev(feed, dev), lg2)
+        ref = oracle.decode_step_batch(om, [ca, cb], feed)
+        check_logits(lg2.cpu().numpy(), ref, TOL["bf16"], f"decode {step}")
+        feed = np.array([oracle.argmax(x) for x in ref], np.int32)
+    assert eng.device_error() == (0, 0)
+    eng.close()
