@@ -136,9 +136,9 @@ class ClockSampler:
 
 
 # ---- the GPU arm ------------------------------------------------------------------------------
-def setup_decode(wl, device, extra_positions: int):
+def setup_decode(wl, device, extra_positions: int, page_tokens: int = 0):
     """Engine + slabs for a decode workload: synthetic KV of each row loaded into its slab,
-    each row's next token ready on the device."""
+    each row's next token ready on the device.  page_tokens > 0: a paged engine."""
     import numpy as np
     import torch
 
@@ -149,8 +149,12 @@ def setup_decode(wl, device, extra_positions: int):
     ctx = [int(c) for c in wl.context_lengths()]
     caps = [c + extra_positions for c in ctx]
     w = DeviceWeights(shape, device)
-    arena = sum(B.slab_bytes(w.cfg, c) for c in caps)
-    eng = Engine(w, arena_bytes=arena, max_batch=len(ctx), max_prefill_tokens=len(ctx))
+    if page_tokens:
+        arena = sum(B.slab_bytes(w.cfg, page_tokens) * (-(-c // page_tokens)) for c in caps)
+    else:
+        arena = sum(B.slab_bytes(w.cfg, c) for c in caps)
+    eng = Engine(w, arena_bytes=arena, max_batch=len(ctx), max_prefill_tokens=len(ctx),
+                 page_tokens=page_tokens)
     slabs = []
     for r, (c, cap) in enumerate(zip(ctx, caps)):
         s = eng.kv_slab_alloc(cap)

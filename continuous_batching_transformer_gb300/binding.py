@@ -65,7 +65,8 @@ class Weights(ctypes.Structure):
 
 class EngineParams(ctypes.Structure):
     _fields_ = [("kv_arena", c_void), ("kv_arena_bytes", ctypes.c_size_t),
-                ("max_batch", c_int32), ("max_prefill_tokens", c_int32), ("stream", c_void)]
+                ("max_batch", c_int32), ("max_prefill_tokens", c_int32), ("stream", c_void),
+                ("kv_page_tokens", c_int32)]
 
 
 class Stats(ctypes.Structure):

@@ -54,8 +54,8 @@ template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attn_prefill(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const PrefillUnit* __restrict__ units,
-                   int n_units, int q_lo_row, int layer, int n_heads, int n_kv_heads,
-                   float* __restrict__ o, int* err) {
+                   const long long* __restrict__ pagetab, int n_units, int q_lo_row, int layer,
+                   int n_heads, int n_kv_heads, float* __restrict__ o, int* err) {
   constexpr int nKh = HD / 64;               // 64-dim boxes of Q and K
   constexpr uint32_t kQBytes = 2 * nKh * kBox;  // Q tile [hi, lo][128 queries][HD]
   constexpr uint32_t kKBytes = nKh * kBox;   // K tile [128 keys][HD]
@@ -118,8 +118,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const PrefillUnit u = units[ui];
         const int g = u.head / G;
         const QueryRow r{u.base, 0, u.cap};
-        const long long krow = kv_block(r, layer, 0, g, n_kv_heads, HD) / HD;
-        const long long vrow = kv_block(r, layer, 1, g, n_kv_heads, HD) / 64;
+        long long krow = kv_block(r, layer, 0, g, n_kv_heads, HD) / HD;
+        long long vrow = kv_block(r, layer, 1, g, n_kv_heads, HD) / 64;
         if (!wait_or_abort(qempty, (un & 1) ^ 1, abort_flag)) {
           flag_timeout(err, abort_flag, 1);
           break;
@@ -135,6 +135,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nkb = key_blocks(u);
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb) {
+          if (u.pages >= 0) {  // paged: the key block's own page (blocks never straddle pages)
+            const QueryRow rp{pagetab[u.pages + kb * kBlk / u.cap], 0, u.cap};
+            krow = kv_block(rp, layer, 0, g, n_kv_heads, HD) / HD;
+            vrow = kv_block(rp, layer, 1, g, n_kv_heads, HD) / 64;
+          }
           const int st = (int)(kn % kRing);
           if (!wait_or_abort(&kempty[st], ((kn / kRing) & 1) ^ 1, abort_flag)) {
             flag_timeout(err, abort_flag, 2);
@@ -360,9 +365,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int HD>
 cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const PrefillUnit* units, int n_units, int q_lo_row, int layer,
-                           int n_heads, int n_kv_heads, float* o, int* err, int grid,
-                           cudaStream_t s) {
+                           const PrefillUnit* units, const long long* pagetab, int n_units,
+                           int q_lo_row, int layer, int n_heads, int n_kv_heads, float* o,
+                           int* err, int grid, cudaStream_t s) {
   constexpr int nKh = HD / 64;
   constexpr size_t smem =
       1024 + 2 * nKh * kBox + kRing * nKh * kBox + 2 * HD * 128 + 4 * kBox + 256;
@@ -371,23 +376,25 @@ cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const C
       cudaFuncSetAttribute(k_attn_prefill<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (rc != cudaSuccess) return rc;
   return launch_pdl(k_attn_prefill<HD>, dim3(grid), dim3(kThreads), smem, s, tq, tk, tv, units,
-                    n_units, q_lo_row, layer, n_heads, n_kv_heads, o, err);
+                    pagetab, n_units, q_lo_row, layer, n_heads, n_kv_heads, o, err);
 }
 
 }  // namespace
 
 bool launch_attn_prefill_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const PrefillUnit* units, int n_units, int q_lo_row, int layer,
-                            int n_heads, int n_kv_heads, int head_dim, float* o, int* err,
-                            int num_sms, cudaStream_t s) {
+                            const PrefillUnit* units, const long long* pagetab, int n_units,
+                            int q_lo_row, int layer, int n_heads, int n_kv_heads, int head_dim,
+                            float* o, int* err, int num_sms, cudaStream_t s) {
   if (n_units <= 0) return true;
   if (n_heads % n_kv_heads) return false;
   const int grid = n_units < num_sms ? n_units : num_sms;
   cudaError_t rc;
   if (head_dim == 128)
-    rc = launch_prefill<128>(tq, tk, tv, units, n_units, q_lo_row, layer, n_heads, n_kv_heads, o, err, grid, s);
+    rc = launch_prefill<128>(tq, tk, tv, units, pagetab, n_units, q_lo_row, layer, n_heads,
+                             n_kv_heads, o, err, grid, s);
   else if (head_dim == 64)
-    rc = launch_prefill<64>(tq, tk, tv, units, n_units, q_lo_row, layer, n_heads, n_kv_heads, o, err, grid, s);
+    rc = launch_prefill<64>(tq, tk, tv, units, pagetab, n_units, q_lo_row, layer, n_heads,
+                            n_kv_heads, o, err, grid, s);
   else
     return false;
   return rc == cudaSuccess;

@@ -105,7 +105,8 @@ __global__ void __launch_bounds__(160, kCtasPerSm)
       const uint64_t pol = tc::policy_evict_first();
       uint32_t qn = 0, kn = 0, vn = 0;
       bool ok = true;
-      auto load_kv = [&](const QueryRow& r, const AttnItem& w, int sub) -> bool {
+      auto load_kv = [&](const QueryRow& row, const AttnItem& w, int sub) -> bool {
+        const QueryRow r{w.kbase, row.pos, row.cap};  // the slab or page holding the item
         const long long krow = kv_block(r, layer, 0, w.g, n_kv_heads, HD) / HD;
         const long long vrow = kv_block(r, layer, 1, w.g, n_kv_heads, HD) / 64;
         if (!tc::mbar_wait(kempty, (kn & 1) ^ 1)) {

@@ -224,10 +224,10 @@ void launch_rope_append(float* qkv, const QueryRow* rows, int n, int layer, int 
              head_dim, cosv, sinv, arena, qtile, qb, q_lo_row);
 }
 
-// ---- V of one layer between the plain [kv head][position][head_dim] layout and a slab ------
-// (to_slab: plain -> slab, else slab -> plain); positions [0, n)
+// ---- V of one layer between the plain [kv head][plain_n positions][head_dim] layout and a slab
+// (or page) -- to_slab: plain -> slab, else slab -> plain; positions [t0, t0 + n)
 __global__ void k_v_convert(uint16_t* plain, uint16_t* arena, QueryRow r, int layer,
-                            int n_kv_heads, int n, int head_dim, int to_slab) {
+                            int n_kv_heads, int t0, int n, int plain_n, int head_dim, int to_slab) {
   pdl_wait();
   pdl_launch();
   long long tot = (long long)n_kv_heads * n * head_dim;
@@ -235,24 +235,29 @@ __global__ void k_v_convert(uint16_t* plain, uint16_t* arena, QueryRow r, int la
        i += (long long)gridDim.x * blockDim.x) {
     int d = (int)(i % head_dim);
     long long rest = i / head_dim;
-    int t = (int)(rest % n), g = (int)(rest / n);
+    int t = t0 + (int)(rest % n), g = (int)(rest / n);
     long long at = v_index(r, layer, g, t, d, n_kv_heads, head_dim);
-    if (to_slab) arena[at] = plain[i];
-    else plain[i] = arena[at];
+    long long pi = ((long long)g * plain_n + t) * head_dim + d;
+    if (to_slab) arena[at] = plain[pi];
+    else plain[pi] = arena[at];
   }
 }
 
 void launch_v_convert(uint16_t* plain, uint16_t* arena, const QueryRow& r, int layer,
-                      int n_kv_heads, int n, int head_dim, bool to_slab, cudaStream_t s) {
+                      int n_kv_heads, int t0, int n, int plain_n, int head_dim, bool to_slab,
+                      cudaStream_t s) {
   long long tot = (long long)n_kv_heads * n * head_dim;
   if (tot <= 0) return;
   int grid = (int)std::min<long long>((tot + 255) / 256, 4096);
-  launch_pdl(k_v_convert, dim3(grid), dim3(256), 0, s, plain, arena, r, layer, n_kv_heads, n, head_dim, to_slab ? 1 : 0);
+  launch_pdl(k_v_convert, dim3(grid), dim3(256), 0, s, plain, arena, r, layer, n_kv_heads, t0, n,
+             plain_n, head_dim, to_slab ? 1 : 0);
 }
 
 // ---- plain attention: one block per (token, q head), keys [0, pos] of its own slab -------
-__global__ void k_attention_naive(const float* qkv, const QueryRow* rows, int layer, int n_heads,
-                                  int n_kv_heads, int head_dim, const uint16_t* arena, float* o) {
+__global__ void k_attention_naive(const float* qkv, const QueryRow* rows,
+                                  const long long* pagetab, const int* tok_pages, int layer,
+                                  int n_heads, int n_kv_heads, int head_dim,
+                                  const uint16_t* arena, float* o) {
   pdl_wait();
   pdl_launch();
   extern __shared__ float sm[];
@@ -267,12 +272,16 @@ __global__ void k_attention_naive(const float* qkv, const QueryRow* rows, int la
   const float* q = qkv + (size_t)t * (qd + 2 * kvd) + (size_t)hq * head_dim;
   for (int j = threadIdx.x; j < head_dim; j += blockDim.x) qs[j] = q[j];
   __syncthreads();
-  const uint16_t* K = arena + kv_block(r, layer, 0, g, n_kv_heads, head_dim);
-  const uint16_t* V = arena + kv_block(r, layer, 1, g, n_kv_heads, head_dim);
+  // the slab (or, for a paged sequence, the page) holding key k, as a QueryRow
+  const int tp = tok_pages ? tok_pages[t] : -1;
+  auto holder = [&](int k) -> QueryRow {
+    return tp < 0 ? r : QueryRow{pagetab[tp + k / r.cap], 0, r.cap};
+  };
   float scale = rsqrtf((float)head_dim);
   float mx = -INFINITY;
   for (int k = threadIdx.x; k < nk; k += blockDim.x) {
-    const uint4* kr = reinterpret_cast<const uint4*>(K + (size_t)k * head_dim);
+    const uint4* kr = reinterpret_cast<const uint4*>(
+        arena + k_index(holder(k), layer, g, k, 0, n_kv_heads, head_dim));
     float dot = 0.f;
     for (int c = 0; c < head_dim / 8; ++c) {
       uint4 w = kr[c];
@@ -316,20 +325,26 @@ __global__ void k_attention_naive(const float* qkv, const QueryRow* rows, int la
   float* orow = o + (size_t)t * qd + (size_t)hq * head_dim;
   for (int j = threadIdx.x; j < head_dim; j += blockDim.x) {
     float acc = 0.f;
-    for (int k = 0; k < nk; ++k)
-      acc = fmaf(sc[k], bf16_to_f32(V[((size_t)(k >> 6) * head_dim + j) * 64 + (k & 63)]), acc);
+    for (int k0 = 0; k0 < nk; k0 += r.cap) {  // one slab, or page by page
+      const QueryRow h = holder(k0);
+      const int k1 = min(nk, k0 + r.cap);
+      for (int k = k0; k < k1; ++k)
+        acc = fmaf(sc[k], bf16_to_f32(arena[v_index(h, layer, g, k, j, n_kv_heads, head_dim)]), acc);
+    }
     orow[j] = acc * inv;
   }
 }
 
-void launch_attention_naive(const float* qkv, const QueryRow* rows, int n, int layer, int n_heads,
-                            int n_kv_heads, int head_dim, int max_keys, const uint16_t* arena,
-                            float* o, cudaStream_t s) {
+void launch_attention_naive(const float* qkv, const QueryRow* rows, const long long* pagetab,
+                            const int* tok_pages, int n, int layer, int n_heads, int n_kv_heads,
+                            int head_dim, int max_keys, const uint16_t* arena, float* o,
+                            cudaStream_t s) {
   if (n <= 0) return;
   size_t smem = sizeof(float) * (size_t)(head_dim + max_keys);
   if (smem > 48 * 1024)
     cudaFuncSetAttribute(k_attention_naive, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  launch_pdl(k_attention_naive, dim3(dim3(n, n_heads)), dim3(128), smem, s, qkv, rows, layer, n_heads, n_kv_heads,
+  launch_pdl(k_attention_naive, dim3(dim3(n, n_heads)), dim3(128), smem, s, qkv, rows, pagetab,
+             tok_pages, layer, n_heads, n_kv_heads,
                                                          head_dim, arena, o);
 }
 

@@ -20,7 +20,11 @@ CBT_D uint16_t f32_to_bf16(float f) {
 }
 
 // Where a decode row or a prefill token reads and writes its KV: the slab's element offset
-// in the arena, the token's position and the slab's capacity (a multiple of 64).
+// in the arena, the token's position and the slab's capacity (a multiple of 64).  A paged
+// sequence keeps its positions in pages of `cap` positions (a multiple of 128), the page
+// holding positions [s, s + cap) at element offset o; its rows carry base = o - s * head_dim,
+// so the index helpers below take global positions unchanged (a page starts on a multiple of
+// 64, so its V groups line up too).
 // Slab layout (bf16): [layer][K|V][kv head] blocks of cap * head_dim elements; inside a K
 // block key t, dim d sits at t*head_dim + d (one row per key); inside a V block the keys are
 // grouped by 64 and transposed: key t, dim d sits at ((t/64)*head_dim + d)*64 + t%64, so a
@@ -54,9 +58,11 @@ CBT_HD uint32_t sw128_offset(int row, int col, int group_stride) {
   return (uint32_t)(g * group_stride + row * 128 + (((c >> 3) ^ (row & 7)) << 4) + (c & 7) * 2);
 }
 
-// One unit of decode attention: kv head g of row b over 128-key sub-chunks [s0, s1)
+// One unit of decode attention: kv head g of row b over 128-key sub-chunks [s0, s1), whose
+// keys sit in the slab (or page) at kbase (a QueryRow base: see above)
 struct AttnItem {
   int b, g, s0, s1;
+  long long kbase;
 };
 
 // Device error word: the first error wins (code, info).

@@ -2,7 +2,9 @@
 //
 // Host side only.  One engine drives one model on one stream.  Slabs are extents of the
 // caller's KV arena handed out by a first-fit allocator with coalescing; each carries its
-// capacity and current position (the host mirror of t_s, bumped as steps are queued).
+// capacity and current position (the host mirror of t_s, bumped as steps are queued).  A
+// paged engine (kv_page_tokens > 0) gives a slab fixed-size pages from the same allocator as
+// its positions are first written, and hands the kernels each page's base.
 // A decode step or a prefill call writes a small per-token row table (slab offset, position,
 // capacity) to the device and then queues the whole forward pass on the engine stream.
 #include <cuda_runtime.h>
@@ -28,11 +30,12 @@ namespace {
 constexpr size_t kSlabAlign = 4096;
 
 struct Slab {
-  size_t offset;  // bytes into the arena
+  size_t offset;  // bytes into the arena (contiguous slabs)
   size_t bytes;
   int cap;        // positions the caller asked for (the limit of pos)
   int pos;
   int lcap;       // cap rounded up to 64: the layout's capacity
+  std::vector<size_t> pages;  // paged engines: byte offset of each page, in position order
 };
 
 template <class T>
@@ -55,6 +58,16 @@ struct cbt_engine {
   // allocator
   std::map<size_t, size_t> free_ext;  // offset -> bytes
   std::unordered_map<int, Slab> slabs;
+  int page = 0;            // kv_page_tokens: positions per page (0: contiguous slabs)
+  size_t page_bytes = 0;
+  // per prefill call: the page bases (QueryRow bases) of every paged segment, and each
+  // token's offset into them (read by the prefill attention kernels)
+  std::vector<long long> hpagetab;
+  std::vector<int> htok_pages;
+  long long* pagetab = nullptr;
+  int* tok_pages = nullptr;
+  size_t pagetab_cap = 0, tok_pages_cap = 0;
+  std::vector<const Slab*> hslab;  // the slab of each decode row, for the attention work list
   int next_id = 1;
   size_t in_use = 0;
 
@@ -164,7 +177,8 @@ static void free_scratch(cbt_engine* e) {
                   e->xg,      e->logits,   e->cosv, e->sinv,  e->next_tok, e->last_idx,
                   e->rows,    e->err,      e->act_h, e->act_o, e->act_u,  e->tc_part,
                   e->tc_cnt,  e->items,    e->item_meta, e->att_o, e->att_ml, e->stage,
-                  e->qtile,   e->ss,       e->qb,     e->pf_units, e->q4_arena};
+                  e->qtile,   e->ss,       e->qb,     e->pf_units, e->q4_arena, e->pagetab,
+                  e->tok_pages};
   for (void* q : ptrs)
     if (q) cudaFree(q);
 }
@@ -201,7 +215,8 @@ extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_w
   const int qd = c.n_heads * c.head_dim;
   if (c.d_model % 256 || qd % 256 || c.d_ff % 256) return CBT_ERR_UNSUPPORTED;
   if (p->max_batch <= 0 || p->max_prefill_tokens <= 0 || p->kv_arena_bytes < kSlabAlign ||
-      (reinterpret_cast<uintptr_t>(p->kv_arena) & 255))
+      (reinterpret_cast<uintptr_t>(p->kv_arena) & 255) || p->kv_page_tokens < 0 ||
+      p->kv_page_tokens % 128)
     return CBT_ERR_INVALID;
   if (!linear_ok(w->lm_head, c.weight_format)) return CBT_ERR_NULL;
   for (int l = 0; l < c.n_layers; ++l) {
@@ -221,6 +236,8 @@ extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_w
   e->p = *p;
   e->stream = static_cast<cudaStream_t>(p->stream);
   e->free_ext[0] = p->kv_arena_bytes & ~(kSlabAlign - 1);
+  e->page = p->kv_page_tokens;
+  e->page_bytes = e->page ? cbt_slab_bytes(&c, e->page) : 0;
 
   const int T = std::max(p->max_batch, p->max_prefill_tokens);
   e->tmax = T;
@@ -376,32 +393,91 @@ extern "C" cbt_status cbt_engine_destroy(cbt_engine* e) {
 }
 
 // ---- slab allocator ---------------------------------------------------------------------
-extern "C" cbt_status cbt_kv_slab_alloc(cbt_engine* e, int32_t cap, int32_t* id) {
-  if (!e || !id) return CBT_ERR_NULL;
-  if (cap <= 0) return CBT_ERR_INVALID;
-  size_t need = cbt_slab_bytes(&e->cfg, cap);
+// first fit: an extent of `need` bytes, or false
+static bool take_extent(cbt_engine* e, size_t need, size_t* off_out) {
   for (auto it = e->free_ext.begin(); it != e->free_ext.end(); ++it) {
     if (it->second >= need) {
       size_t off = it->first, rest = it->second - need;
       e->free_ext.erase(it);
       if (rest) e->free_ext[off + need] = rest;
-      int sid = e->next_id++;
-      e->slabs[sid] = Slab{off, need, cap, 0, round_cap(cap)};
       e->in_use += need;
-      *id = sid;
-      return CBT_OK;
+      *off_out = off;
+      return true;
     }
   }
-  return CBT_ERR_POOL_EXHAUSTED;
+  return false;
+}
+
+static void give_extent(cbt_engine* e, size_t off, size_t bytes);
+
+// The QueryRow base and capacity of the slab, or the page, that holds position pos: a page
+// holding positions [s, s + page) at element offset o has base o - s * head_dim, so the
+// kernels' index helpers take global positions.
+static long long row_base(const cbt_engine* e, const Slab& sl, int pos) {
+  if (!e->page) return (long long)(sl.offset / 2);
+  const int pg = pos / e->page;
+  return (long long)(sl.pages[pg] / 2) - (long long)pg * e->page * e->cfg.head_dim;
+}
+static int row_cap(const cbt_engine* e, const Slab& sl) { return e->page ? e->page : sl.lcap; }
+
+// Paged engines: pages for positions [0, upto) of each listed slab, taken in order; on
+// running out, the pages taken by this call go back and false is returned.
+static bool ensure_pages(cbt_engine* e, const std::vector<std::pair<int, long long>>& need) {
+  if (!e->page) return true;
+  std::vector<std::pair<int, size_t>> added;
+  for (const auto& nd : need) {
+    Slab& sl = e->slabs[nd.first];
+    while ((long long)sl.pages.size() * e->page < nd.second) {
+      size_t off;
+      if (!take_extent(e, e->page_bytes, &off)) {
+        for (auto it = added.rbegin(); it != added.rend(); ++it) {
+          e->slabs[it->first].pages.pop_back();
+          give_extent(e, it->second, e->page_bytes);
+        }
+        return false;
+      }
+      sl.pages.push_back(off);
+      added.push_back({nd.first, off});
+    }
+  }
+  return true;
+}
+
+extern "C" cbt_status cbt_kv_slab_alloc(cbt_engine* e, int32_t cap, int32_t* id) {
+  if (!e || !id) return CBT_ERR_NULL;
+  if (cap <= 0) return CBT_ERR_INVALID;
+  if (e->page) {  // pages are taken as positions are written
+    int sid = e->next_id++;
+    e->slabs[sid] = Slab{0, 0, cap, 0, round_cap(cap), {}};
+    *id = sid;
+    return CBT_OK;
+  }
+  size_t need = cbt_slab_bytes(&e->cfg, cap), off;
+  if (!take_extent(e, need, &off)) return CBT_ERR_POOL_EXHAUSTED;
+  int sid = e->next_id++;
+  e->slabs[sid] = Slab{off, need, cap, 0, round_cap(cap), {}};
+  *id = sid;
+  return CBT_OK;
 }
 
 extern "C" cbt_status cbt_kv_slab_free(cbt_engine* e, int32_t id) {
   if (!e) return CBT_ERR_NULL;
   auto it = e->slabs.find(id);
   if (it == e->slabs.end()) return CBT_ERR_BAD_SLAB;
+  if (e->page) {
+    for (size_t off : it->second.pages) give_extent(e, off, e->page_bytes);
+    e->slabs.erase(it);
+    return CBT_OK;
+  }
   size_t off = it->second.offset, bytes = it->second.bytes;
-  e->in_use -= bytes;
   e->slabs.erase(it);
+  give_extent(e, off, bytes);
+  return CBT_OK;
+}
+
+// return an extent to the free list, merged with its neighbours
+static void give_extent(cbt_engine* e, size_t off, size_t bytes) {
+  e->in_use -= bytes;
   auto nx = e->free_ext.lower_bound(off);
   if (nx != e->free_ext.end() && off + bytes == nx->first) {  // merge with the next extent
     bytes += nx->second;
@@ -411,11 +487,10 @@ extern "C" cbt_status cbt_kv_slab_free(cbt_engine* e, int32_t id) {
     auto pv = std::prev(nx);
     if (pv->first + pv->second == off) {
       pv->second += bytes;
-      return CBT_OK;
+      return;
     }
   }
   e->free_ext[off] = bytes;
-  return CBT_OK;
 }
 
 extern "C" cbt_status cbt_retire(cbt_engine* e, const int32_t* ids, int32_t n) {
@@ -447,9 +522,9 @@ static cbt_status slab_copy(cbt_engine* e, int32_t id, void* k, void* v, int32_t
   Slab& s = it->second;
   if (n < 0) return CBT_ERR_INVALID;
   if (n > s.cap || (!to_slab && n > s.pos)) return CBT_ERR_CAPACITY;
+  if (to_slab && !ensure_pages(e, {{id, (long long)n}})) return CBT_ERR_POOL_EXHAUSTED;
   const cbt_model_config& c = e->cfg;
   const size_t row = (size_t)c.head_dim * 2;
-  char* arena = static_cast<char*>(e->p.kv_arena) + s.offset;
   cudaMemcpyKind kind = on_host ? (to_slab ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToHost)
                                 : cudaMemcpyDeviceToDevice;
   cudaError_t rc = cudaSuccess;
@@ -463,26 +538,32 @@ static cbt_status slab_copy(cbt_engine* e, int32_t id, void* k, void* v, int32_t
     if (rc != cudaSuccess) return CBT_ERR_CUDA;
     e->stage_elems = layer_elems;
   }
-  const QueryRow qr{(long long)(s.offset / 2), 0, s.lcap};
+  // runs of positions: the whole slab, or page by page
+  const int P = row_cap(e, s);
+  const int runs = e->page ? (n + P - 1) / P : (n > 0 ? 1 : 0);
   for (int l = 0; l < c.n_layers && rc == cudaSuccess && n > 0; ++l) {
-    // K: the slab's K block holds rows [0, n) of head_dim elements per kv head
-    char* user = static_cast<char*>(k) + (size_t)l * c.n_kv_heads * n * row;
-    char* slab = arena + ((size_t)l * 2) * c.n_kv_heads * (size_t)s.lcap * row;
-    size_t upitch = (size_t)n * row, spitch = (size_t)s.lcap * row;
-    if (to_slab)
-      rc = cudaMemcpy2DAsync(slab, spitch, user, upitch, upitch, c.n_kv_heads, kind, e->stream);
-    else
-      rc = cudaMemcpy2DAsync(user, upitch, slab, spitch, upitch, c.n_kv_heads, kind, e->stream);
-    if (rc != cudaSuccess) break;
-    // V: transposed 64-key groups in the slab, converted on the device
     uint16_t* vu = static_cast<uint16_t*>(v) + (size_t)l * layer_elems;
     uint16_t* plain = on_host ? e->stage : vu;
     if (on_host && to_slab)
       rc = cudaMemcpyAsync(plain, vu, layer_elems * 2, cudaMemcpyHostToDevice, e->stream);
-    if (rc != cudaSuccess) break;
-    launch_v_convert(plain, static_cast<uint16_t*>(e->p.kv_arena), qr, l, c.n_kv_heads, n,
-                     c.head_dim, to_slab, e->stream);
-    rc = cudaGetLastError();
+    for (int r = 0; r < runs && rc == cudaSuccess; ++r) {
+      const int a = e->page ? r * P : 0, cnt = e->page ? std::min(n, a + P) - a : n;
+      char* blk = static_cast<char*>(e->p.kv_arena) + (e->page ? s.pages[r] : s.offset);
+      // K: rows [a, a + cnt) of each kv head's [position][head_dim] block
+      char* user = static_cast<char*>(k) + ((size_t)l * c.n_kv_heads * n + a) * row;
+      char* slab = blk + ((size_t)l * 2) * c.n_kv_heads * (size_t)P * row;
+      size_t upitch = (size_t)n * row, spitch = (size_t)P * row, width = (size_t)cnt * row;
+      if (to_slab)
+        rc = cudaMemcpy2DAsync(slab, spitch, user, upitch, width, c.n_kv_heads, kind, e->stream);
+      else
+        rc = cudaMemcpy2DAsync(user, upitch, slab, spitch, width, c.n_kv_heads, kind, e->stream);
+      if (rc != cudaSuccess) break;
+      // V: transposed 64-key groups in the slab, converted on the device
+      const QueryRow qr{row_base(e, s, a), 0, P};
+      launch_v_convert(plain, static_cast<uint16_t*>(e->p.kv_arena), qr, l, c.n_kv_heads, a, cnt,
+                       n, c.head_dim, to_slab, e->stream);
+      rc = cudaGetLastError();
+    }
     if (rc == cudaSuccess && on_host && !to_slab)
       rc = cudaMemcpyAsync(vu, plain, layer_elems * 2, cudaMemcpyDeviceToHost, e->stream);
   }
@@ -511,18 +592,23 @@ extern "C" cbt_status cbt_kv_slab_copy_prefix(cbt_engine* e, int32_t src_id, int
   const Slab& src = si->second;
   Slab& dst = di->second;
   if (n > src.pos || n > dst.cap) return CBT_ERR_CAPACITY;
-  if (n > 0) {
-    // every (layer, K|V, kv head) block is a run of positions at the same place in both slabs:
-    // one strided copy of whole 64-position groups (a V block keeps each group of 64 positions
-    // transposed; both layouts' capacities are multiples of 64, so the groups line up)
-    const cbt_model_config& c = e->cfg;
-    const size_t row = (size_t)c.head_dim * 2;
-    const size_t width = (size_t)((n + 63) / 64 * 64) * row;
-    const size_t blocks = (size_t)c.n_layers * 2 * c.n_kv_heads;
-    const char* from = static_cast<const char*>(e->p.kv_arena) + src.offset;
-    char* to = static_cast<char*>(e->p.kv_arena) + dst.offset;
-    if (cudaMemcpy2DAsync(to, (size_t)dst.lcap * row, from, (size_t)src.lcap * row, width, blocks,
-                          cudaMemcpyDeviceToDevice, e->stream) != cudaSuccess)
+  if (!ensure_pages(e, {{dst_id, (long long)n}})) return CBT_ERR_POOL_EXHAUSTED;
+  // every (layer, K|V, kv head) block is a run of positions at the same place in both slabs (or
+  // pages): one strided copy per run, of whole 64-position groups (a V block keeps each group
+  // of 64 positions transposed; capacities and page sizes are multiples of 64, so the groups
+  // line up)
+  const cbt_model_config& c = e->cfg;
+  const size_t row = (size_t)c.head_dim * 2;
+  const size_t blocks = (size_t)c.n_layers * 2 * c.n_kv_heads;
+  const int runs = e->page ? (n + e->page - 1) / e->page : (n > 0 ? 1 : 0);
+  for (int r = 0; r < runs; ++r) {
+    const int m = e->page ? std::min(e->page, n - r * e->page) : n;
+    const size_t width = (size_t)((m + 63) / 64 * 64) * row;
+    const char* from = static_cast<const char*>(e->p.kv_arena) + (e->page ? src.pages[r] : src.offset);
+    char* to = static_cast<char*>(e->p.kv_arena) + (e->page ? dst.pages[r] : dst.offset);
+    const size_t sp = (size_t)row_cap(e, src) * row, dp = (size_t)row_cap(e, dst) * row;
+    if (cudaMemcpy2DAsync(to, dp, from, sp, width, blocks, cudaMemcpyDeviceToDevice, e->stream) !=
+        cudaSuccess)
       return CBT_ERR_CUDA;
   }
   dst.pos = n;
@@ -772,11 +858,14 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
       ok &= launch_attn_decode_tc(e->kv_kmap, e->kv_vmap, a, e->num_sms, s);
     } else {
       if (tc_prefill)  // flash attention per segment on the tensor cores
-        ok &= launch_attn_prefill_tc(e->q_map, e->kv_kmap, e->kv_vmap, e->pf_units, e->pf_n,
+        ok &= launch_attn_prefill_tc(e->q_map, e->kv_kmap, e->kv_vmap, e->pf_units, e->pagetab,
+                                     e->pf_n,
                                      e->qb_rows, l, c.n_heads, c.n_kv_heads, c.head_dim, e->o,
                                      e->err, e->num_sms, s);
       else
-        launch_attention_naive(e->qkv, e->rows, n, l, c.n_heads, c.n_kv_heads, c.head_dim,
+        launch_attention_naive(e->qkv, e->rows, e->page ? e->pagetab : nullptr,
+                               e->page ? e->tok_pages : nullptr, n, l, c.n_heads, c.n_kv_heads,
+                               c.head_dim,
                                max_keys, arena, e->o, s);
       if (tcp) launch_f32_to_act(e->o, n, qd, e->act_o, lo, s);
     }
@@ -835,6 +924,7 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
 }
 
 static void drop_graphs(cbt_engine* e);
+static cudaError_t upload_page_tables(cbt_engine* e);
 
 // Work list of the tensor-core decode attention for the rows in e->hrows[0..B): per row and kv
 // head, runs of kSubsPerItem 128-key sub-chunks over positions [0, pos].  Grows the item and
@@ -849,10 +939,12 @@ static cudaError_t plan_decode_attention(cbt_engine* e, int B) {
     const int splits = (nsub + kSubsPerItem - 1) / kSubsPerItem;
     e->hitem_base[b] = (int)e->hitems.size();
     e->hitem_count[b] = splits;
+    // an item's sub-chunks lie in one page (pages are multiples of 128 * kSubsPerItem keys)
     for (int g = 0; g < Hkv; ++g)
       for (int sp = 0; sp < splits; ++sp)
         e->hitems.push_back(AttnItem{b, g, sp * kSubsPerItem,
-                                     std::min(nsub, (sp + 1) * kSubsPerItem)});
+                                     std::min(nsub, (sp + 1) * kSubsPerItem),
+                                     row_base(e, *e->hslab[b], sp * kSubsPerItem * 128)});
   }
   const size_t n = e->hitems.size();
   cudaError_t rc = cudaSuccess;
@@ -934,18 +1026,36 @@ extern "C" cbt_status cbt_decode_step_batch(cbt_engine* e, const int32_t* ids, i
   std::unordered_set<int> seen;
   int max_keys = 0;
   long long total_keys = 0;
+  std::vector<std::pair<int, long long>> need;
   for (int b = 0; b < B; ++b) {
     auto it = e->slabs.find(ids[b]);
     if (it == e->slabs.end()) return CBT_ERR_BAD_SLAB;
     if (!seen.insert(ids[b]).second) return CBT_ERR_DUP_SLAB;
     const Slab& sl = it->second;
     if (sl.pos + 1 > sl.cap) return CBT_ERR_CAPACITY;
-    e->hrows[b] = QueryRow{(long long)(sl.offset / 2), sl.pos, sl.lcap};
+    need.push_back({ids[b], sl.pos + 1});
+  }
+  if (!ensure_pages(e, need)) return CBT_ERR_POOL_EXHAUSTED;
+  e->hslab.resize(B);
+  for (int b = 0; b < B; ++b) {
+    const Slab& sl = e->slabs[ids[b]];
+    e->hrows[b] = QueryRow{row_base(e, sl, sl.pos), sl.pos, row_cap(e, sl)};
+    e->hslab[b] = &sl;
     max_keys = std::max(max_keys, sl.pos + 1);
     total_keys += sl.pos + 1;
   }
   cudaError_t rc = cudaMemcpyAsync(e->rows, e->hrows.data(), sizeof(QueryRow) * B,
                                    cudaMemcpyHostToDevice, e->stream);
+  if (rc == cudaSuccess && e->page) {  // for the CUDA-core attention (rows above its limits)
+    e->hpagetab.clear();
+    e->htok_pages.assign(B, -1);
+    for (int b = 0; b < B; ++b) {
+      e->htok_pages[b] = (int)e->hpagetab.size();
+      for (size_t pg = 0; pg < e->hslab[b]->pages.size(); ++pg)
+        e->hpagetab.push_back(row_base(e, *e->hslab[b], (int)pg * e->page));
+    }
+    rc = upload_page_tables(e);
+  }
   if (rc == cudaSuccess && e->use_tc) rc = plan_decode_attention(e, B);
   if (rc == cudaSuccess) {
     if (e->use_tc && e->timing_mask == 0 && e->stream != nullptr)
@@ -963,6 +1073,38 @@ extern "C" cbt_status cbt_decode_step_batch(cbt_engine* e, const int32_t* ids, i
 // the longest blocks (most key blocks) first so the persistent grid ends evenly.  Copies the
 // list to the device (growing the buffer) on the engine stream; pf_n = 0 leaves the call on
 // the plain attention kernel.
+// Paged engines: the call's page bases and each token's (or decode row's) offset into them, to
+// the device (buffers grow as needed, after the work that may still read them)
+static cudaError_t upload_page_tables(cbt_engine* e) {
+  cudaError_t rc = cudaSuccess;
+  const size_t np = std::max<size_t>(1, e->hpagetab.size()), nt = std::max<size_t>(1, e->htok_pages.size());
+  if (np > e->pagetab_cap || nt > e->tok_pages_cap) {
+    rc = cudaStreamSynchronize(e->stream);
+    if (np > e->pagetab_cap) {
+      if (e->pagetab) cudaFree(e->pagetab);
+      e->pagetab = nullptr;
+      e->pagetab_cap = 0;
+      if (rc == cudaSuccess) rc = cudaMalloc(reinterpret_cast<void**>(&e->pagetab), 2 * np * sizeof(long long));
+      if (rc == cudaSuccess) e->pagetab_cap = 2 * np;
+    }
+    if (nt > e->tok_pages_cap) {
+      if (e->tok_pages) cudaFree(e->tok_pages);
+      e->tok_pages = nullptr;
+      e->tok_pages_cap = 0;
+      if (rc == cudaSuccess) rc = cudaMalloc(reinterpret_cast<void**>(&e->tok_pages), 2 * nt * sizeof(int));
+      if (rc == cudaSuccess) e->tok_pages_cap = 2 * nt;
+    }
+    if (rc != cudaSuccess) return rc;
+  }
+  if (!e->hpagetab.empty())
+    rc = cudaMemcpyAsync(e->pagetab, e->hpagetab.data(), e->hpagetab.size() * sizeof(long long),
+                         cudaMemcpyHostToDevice, e->stream);
+  if (rc == cudaSuccess && !e->htok_pages.empty())
+    rc = cudaMemcpyAsync(e->tok_pages, e->htok_pages.data(), e->htok_pages.size() * sizeof(int),
+                         cudaMemcpyHostToDevice, e->stream);
+  return rc;
+}
+
 static cudaError_t plan_prefill_attention(cbt_engine* e, const int32_t* ids, const int32_t* lens,
                                           int K) {
   e->pf_n = 0;
@@ -980,8 +1122,9 @@ static cudaError_t plan_prefill_attention(cbt_engine* e, const int32_t* ids, con
     const int L = lens[s];
     for (int q = 0; q < L; q += 128) {
       PrefillUnit u{};
-      u.base = (long long)(sl.offset / 2);
-      u.cap = sl.lcap;
+      u.base = row_base(e, sl, 0);
+      u.cap = row_cap(e, sl);
+      u.pages = e->page ? e->htok_pages[tok] : -1;
       u.tok0 = tok + q;
       u.q0 = sl.pos + q;
       u.nq = std::min(128, L - q);
@@ -1036,11 +1179,23 @@ extern "C" cbt_status cbt_prefill_segmented(cbt_engine* e, const int32_t* ids,
     total_keys += (long long)lens[s] * sl.pos + (long long)lens[s] * (lens[s] + 1) / 2;
   }
   if (T > e->p.max_prefill_tokens) return CBT_ERR_TOKENS;
+  std::vector<std::pair<int, long long>> need;
+  for (int s = 0; s < K; ++s) need.push_back({ids[s], (long long)e->slabs[ids[s]].pos + lens[s]});
+  if (!ensure_pages(e, need)) return CBT_ERR_POOL_EXHAUSTED;
+  // paged segments: every page base of the segment once, each token pointing at its segment's
+  e->hpagetab.clear();
+  e->htok_pages.assign(T, -1);
   int g = 0;
   for (int s = 0; s < K; ++s) {
     const Slab& sl = e->slabs[ids[s]];
-    for (int j = 0; j < lens[s]; ++j, ++g)
-      e->hrows[g] = QueryRow{(long long)(sl.offset / 2), sl.pos + j, sl.lcap};
+    const int first = (int)e->hpagetab.size();
+    if (e->page)
+      for (size_t pg = 0; pg < sl.pages.size(); ++pg)
+        e->hpagetab.push_back(row_base(e, sl, (int)pg * e->page));
+    for (int j = 0; j < lens[s]; ++j, ++g) {
+      e->hrows[g] = QueryRow{row_base(e, sl, sl.pos + j), sl.pos + j, row_cap(e, sl)};
+      if (e->page) e->htok_pages[g] = first;
+    }
     e->hidx[s] = g - 1;
   }
   cudaError_t rc = cudaMemcpyAsync(e->rows, e->hrows.data(), sizeof(QueryRow) * T,
@@ -1048,6 +1203,7 @@ extern "C" cbt_status cbt_prefill_segmented(cbt_engine* e, const int32_t* ids,
   if (rc == cudaSuccess)
     rc = cudaMemcpyAsync(e->last_idx, e->hidx.data(), sizeof(int32_t) * K, cudaMemcpyHostToDevice,
                          e->stream);
+  if (rc == cudaSuccess && e->page) rc = upload_page_tables(e);
   if (rc == cudaSuccess) rc = plan_prefill_attention(e, ids, lens, K);
   if (rc == cudaSuccess)
     rc = forward(e, (int)T, tokens, max_keys, total_keys, true, K, logits, next_tokens);

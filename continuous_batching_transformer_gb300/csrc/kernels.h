@@ -148,9 +148,11 @@ struct AttnDecodeArgs {
 // tk: the KV arena as [rows][head_dim] bf16, box {64, 128}; tv: as [rows][64], box {64, head_dim}
 bool launch_attn_decode_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnDecodeArgs& a,
                            int num_sms, cudaStream_t s);
-// V of one layer between a plain [kv head][position][head_dim] buffer and a slab
+// V of one layer between a plain [kv head][plain_n positions][head_dim] buffer and a slab (or
+// page): positions [t0, t0 + n)
 void launch_v_convert(uint16_t* plain, uint16_t* arena, const QueryRow& r, int layer,
-                      int n_kv_heads, int n, int head_dim, bool to_slab, cudaStream_t s);
+                      int n_kv_heads, int t0, int n, int plain_n, int head_dim, bool to_slab,
+                      cudaStream_t s);
 
 // RMSNorm rows of x into a bf16 operand: hi parts at rows [0, n), lo parts at rows
 // [lo_rows, lo_rows + n) when lo_rows > 0
@@ -185,19 +187,24 @@ void launch_rope_append(float* qkv, const QueryRow* rows, int n, int layer, int 
 struct PrefillUnit {
   long long base;
   int cap, tok0, q0, nq, len, head;
+  int pages;  // paged segment: its page bases (QueryRow bases) at pagetab[pages + key / cap]
+              // (-1: one slab at base)
 };
 // tq: the bf16 q buffer as [2][q_lo_row][n_heads*head_dim] rows (high parts, then the
 // remainders), box {64, 128}; tk, tv: the KV arena as
 // in the decode attention.  o: fp32 [tokens][n_heads*head_dim], softmax(q.K^T) V of each token
 // over positions [0, its own] of its segment.
 bool launch_attn_prefill_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const PrefillUnit* units, int n_units, int q_lo_row, int layer,
+                            const PrefillUnit* units, const long long* pagetab, int n_units,
+                            int q_lo_row, int layer,
                             int n_heads, int n_kv_heads, int head_dim, float* o, int* err,
                             int num_sms, cudaStream_t s);
-// softmax attention of each token over [0, pos] of its own slab
-void launch_attention_naive(const float* qkv, const QueryRow* rows, int n, int layer, int n_heads,
-                            int n_kv_heads, int head_dim, int max_keys, const uint16_t* arena,
-                            float* o, cudaStream_t s);
+// softmax attention of each token over [0, pos] of its own slab; a paged token's keys sit in
+// the pages pagetab[tok_pages[t] + key / cap] (tok_pages NULL or -1: one slab)
+void launch_attention_naive(const float* qkv, const QueryRow* rows, const long long* pagetab,
+                            const int* tok_pages, int n, int layer, int n_heads, int n_kv_heads,
+                            int head_dim, int max_keys, const uint16_t* arena, float* o,
+                            cudaStream_t s);
 // projection y = x W^T with an epilogue; picks the skinny or the tiled kernel
 void launch_linear(const float* x, int n, int K, const LinearW& W, int M, Epilogue epi, float* out,
                    float* partials, size_t partial_floats, cudaStream_t s);

@@ -125,6 +125,16 @@ typedef struct {
   int32_t max_batch;         /* most rows per decode step and most segments per prefill */
   int32_t max_prefill_tokens;/* most tokens (sum of seg_lens) per prefill call */
   void* stream;              /* cudaStream_t all work is queued on; NULL = legacy default */
+  int32_t kv_page_tokens;    /* 0: each slab is one extent of the arena, reserved at
+                              * cbt_kv_slab_alloc for its whole capacity.  > 0 (a multiple of
+                              * 128): paged KV -- a slab takes pages of this many positions
+                              * from the arena as its positions are first written (prefill,
+                              * decode, import, copy_prefix), so a slab's capacity is only a
+                              * limit and no capacity is held unused; a call that needs a page
+                              * the arena cannot give fails with CBT_ERR_POOL_EXHAUSTED before
+                              * queuing anything (pages it took are returned).  Page p of a
+                              * slab holds positions [p * kv_page_tokens, (p + 1) *
+                              * kv_page_tokens) in the layout described at cbt_slab_bytes. */
 } cbt_engine_params;
 
 typedef struct {

@@ -64,6 +64,10 @@ def test_create_rejects_null_and_bad_config(lib):
     assert lib.cbt_engine_create(ctypes.byref(bad), ctypes.byref(w), ctypes.byref(p), ctypes.byref(h)) == -11
     p0 = B.EngineParams(fake, 1 << 20, 0, 64, None)                        # max_batch 0
     assert lib.cbt_engine_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(p0), ctypes.byref(h)) == -1
+    for pages in (100, -128):                                              # page size: k * 128
+        pp = B.EngineParams(fake, 1 << 20, 4, 64, None, pages)
+        assert lib.cbt_engine_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(pp),
+                                     ctypes.byref(h)) == -1
     lw[1] = B.LayerWeights(B.Linear(None, None, None), lw[0].wo, lw[0].wgu, lw[0].wd, fake, fake)
     assert lib.cbt_engine_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(p), ctypes.byref(h)) == -2
     assert not h.value
@@ -90,6 +94,7 @@ def test_calls_reject_null_engine(lib):
     assert lib.cbt_decode_step_batch(None, None, 1, None, None, None) == -2
     assert lib.cbt_prefill_segmented(None, None, None, 1, None, None, None) == -2
     assert lib.cbt_retire(None, None, 0) == -2
+    assert lib.cbt_kv_slab_copy_prefix(None, 1, 2, 3) == -2
     assert lib.cbt_quantize_affine4(None, 1, 64, 64, None, None, None, None) == -2
     fake = ctypes.c_void_p(0x1000)
     assert lib.cbt_quantize_affine4(fake, 4, 96, 64, fake, fake, fake, None) == -1  # cols % group

@@ -16,10 +16,11 @@ from tests.gpu_harness import TOL, check_logits, ensure_built, to_dev
 pytestmark = pytest.mark.gpu
 
 
-def run_sampled(wl, rows, tol):
+def run_sampled(wl, rows, tol, page_tokens=0):
     ensure_built()
     dev = torch.device("cuda:0")
-    w, eng, slabs, ctx, tok = bench.setup_decode(wl, dev, extra_positions=8)
+    w, eng, slabs, ctx, tok = bench.setup_decode(wl, dev, extra_positions=8,
+                                                 page_tokens=page_tokens)
     Bsz, V = len(slabs), wl.shape.vocab
     logits = torch.empty((Bsz, V), dtype=torch.float32, device=dev)
     nxt = torch.empty(Bsz, dtype=torch.int32, device=dev)
@@ -67,3 +68,9 @@ def test_7b_affine4_b16_two_passes():
     """4-bit weights at B = 16: the projections take the rows in two passes of 8 over the
     same weights; rows from both passes."""
     run_sampled(decode_7b_fixed(16, 2048, "affine4"), [0, 9, 15], TOL["affine4"])
+
+
+def test_7b_bf16_b8_paged_kv():
+    """The headline workload on a paged engine (pages of 128 positions; the synthetic KV is
+    imported page by page)."""
+    run_sampled(DECODE_7B_B8, [0, 5], TOL["bf16"], page_tokens=128)
