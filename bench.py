@@ -199,7 +199,8 @@ def gpu_arm(args, rank: int, world: int):
         dist.barrier()
     wl = workload_by_name(args.workload, args.layers)
     K, W = args.steps, args.warmup
-    w, eng, slabs, ctx, tok0 = setup_decode(wl, device, extra_positions=3 * (K + W) + 8)
+    w, eng, slabs, ctx, tok0 = setup_decode(wl, device, extra_positions=3 * (K + W) + 8,
+                                            page_tokens=args.page_tokens)
     Bsz = len(slabs)
     V = wl.shape.vocab
     stream = eng.stream
@@ -307,6 +308,7 @@ def gpu_arm(args, rank: int, world: int):
             "dtype": "bf16" if wl.shape.weight_format == "bf16" else "affine4-w/bf16",
             "data": "synthetic (seeded N(0,0.02) weights, seeded KV slabs and tokens)",
             "config": {"workload": wl.name, "model": wl.shape.name, "batch_per_gpu": Bsz,
+                       "kv_page_tokens": args.page_tokens,
                        "ctx_lengths": ctx, "parallelism": f"replicas x{world}" if world > 1 else "1 gpu",
                        "l2": "inputs larger than L2 (weights alone are %.1f GB per step)"
                              % (wl.shape.weight_bytes_per_step() / 1e9)},
@@ -461,6 +463,8 @@ def main():
     ap.add_argument("--workload", default="7b-bf16-b8")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--reference-budget", type=float, default=60.0)
+    ap.add_argument("--page-tokens", type=int, default=0,
+                    help="paged KV with pages of this many positions (a multiple of 128)")
     ap.add_argument("--layers", type=int, default=None,
                     help="profiling aid: same shapes, fewer layers (small device footprint)")
     args = ap.parse_args()
