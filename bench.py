@@ -401,27 +401,38 @@ def trace_arm(args):
     from continuous_batching_transformer_gb300 import binding as B
     from continuous_batching_transformer_gb300.model import DeviceWeights, Engine
     from continuous_batching_transformer_gb300.trace import decode_gaps, percentiles, run_trace
-    from synth.recipes import MISTRAL_7B, Request, trace_requests
+    from synth.recipes import MISTRAL_7B, Request, agent_requests, trace_requests
 
     device = torch.device("cuda:0")
     torch.cuda.set_device(device)
     cbt.build()
-    realtime = not args.workload.endswith("-t0")
+    agents = "-agents" in args.workload
+    realtime = not (args.workload.endswith("-t0") or agents)
     chunk = 2048 if "-chunked" in args.workload else None
-    seed = 1
-    reqs = trace_requests(64, 2.0, 256, 4096, 256.0, 4096, seed)
+    reuse = "-reuse" in args.workload
+    if agents:  # 32 sub-agents sharing a 2048-token system prompt, all arriving at t = 0
+        seed = 2
+        reqs = agent_requests(32, 2048, 64, 512, 128.0, 1024, seed)
+    else:
+        seed = 1
+        reqs = trace_requests(64, 2.0, 256, 4096, 256.0, 4096, seed)
     live_cap = 8
     w = DeviceWeights(MISTRAL_7B, device)
     cap = max(r.prompt_len + r.output_len for r in reqs) + 8
-    arena = live_cap * B.slab_bytes(w.cfg, cap)
-    eng = Engine(w, arena_bytes=arena, max_batch=live_cap,
+    arena = (live_cap + 1) * B.slab_bytes(w.cfg, cap)  # + a shared prefix's own slab
+    # the agents' slabs differ in size and come and go: paged KV, so no extent fragments
+    page = 128 if agents else 0
+    if page:
+        arena = (live_cap + 1) * B.slab_bytes(w.cfg, page) * (-(-cap // page))
+    eng = Engine(w, arena_bytes=arena, max_batch=live_cap, page_tokens=page,
                  max_prefill_tokens=live_cap * max(r.prompt_len for r in reqs))
     # warm-up: every batch size once (captured decode steps), prefill of short prompts
     warm = [Request(0.0, 64, 4 + 2 * i, 900 + i) for i in range(live_cap)]
     run_trace(eng, warm, seed, live_cap=live_cap)
     launches0 = B.kernel_launches()
     clk = ClockSampler(None)
-    res = run_trace(eng, reqs, seed, live_cap=live_cap, realtime=realtime, chunk_tokens=chunk)
+    res = run_trace(eng, reqs, seed, live_cap=live_cap, realtime=realtime, chunk_tokens=chunk,
+                    reuse_prefix=reuse)
     clocks = clk.stop()
     launches = B.kernel_launches() - launches0
     shape = MISTRAL_7B
@@ -434,9 +445,11 @@ def trace_arm(args):
         "ms_per_step": 1e3 * float(np.mean(res.step_s)) if res.step_s else None,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded weights, prompts and arrival times)",
-        "config": {"workload": "trace-64req-poisson2-" + ("realtime" if realtime else "t0")
-                               + ("-chunk2048" if chunk else ""),
+        "config": {"workload": ("agents-32req-prefix2048" if agents else
+                                "trace-64req-poisson2-" + ("realtime" if realtime else "t0"))
+                               + ("-chunk2048" if chunk else "") + ("-prefix-reuse" if reuse else ""),
                    "model": shape.name, "live_cap": live_cap, "admission_chunk": chunk,
+                   "kv_page_tokens": page,
                    "parallelism": "1 gpu"},
         "trace": {"requests": len(reqs), "generated_tokens": res.generated,
                   "wall_s": res.wall_s, "decode_steps": res.steps,
@@ -471,7 +484,7 @@ def main():
     args.warmup = max(3, args.warmup)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    if args.impl == "gb300" and args.workload.startswith("7b-bf16-trace"):
+    if args.impl == "gb300" and args.workload.startswith(("7b-bf16-trace", "7b-bf16-agents")):
         res = trace_arm(args)
     elif args.impl == "reference":
         res = reference_arm(args, rank)

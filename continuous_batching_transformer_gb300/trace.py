@@ -47,18 +47,61 @@ class TraceResult:
 
 
 def prompt_tokens(req, seed: int, vocab: int) -> np.ndarray:
-    """The request's prompt: its own seeded token stream."""
-    return synth.tokens(req.prompt_len, seed, synth.stream_tokens(req.row), vocab)
+    """The request's prompt: its shared prefix (if any), then its own seeded token stream."""
+    own = synth.tokens(req.prompt_len - req.prefix_len, seed, synth.stream_tokens(req.row), vocab)
+    if not req.prefix_len:
+        return own
+    pre = synth.tokens(req.prefix_len, seed, synth.stream_tokens(req.prefix_row), vocab)
+    return np.concatenate([pre, own])
+
+
+class SharedPrefixes:
+    """Prefix reuse (the batching design: sub-agents share long system prompts and reuse one
+    prefill): each shared prefix is prefilled once into a slab of its own, and a request's
+    slab starts as a copy of it (``copy_prefix``), so only the request's own tokens are
+    prefilled.  Without reuse every prompt is prefilled whole."""
+
+    def __init__(self, eng, seed: int, res: TraceResult, reuse: bool):
+        self.eng, self.seed, self.res, self.reuse = eng, seed, res, reuse
+        self.slabs = {}
+
+    def start(self, req, slab) -> int:
+        """Prompt tokens already in `slab` (its copied shared prefix) -- 0 without reuse."""
+        if not (self.reuse and req.prefix_len):
+            return 0
+        if req.prompt_len <= req.prefix_len:
+            raise ValueError("a request needs at least one token of its own after the prefix")
+        key = (req.prefix_row, req.prefix_len)
+        if key not in self.slabs:
+            src = self.eng.kv_slab_alloc(req.prefix_len)
+            toks = synth.tokens(req.prefix_len, self.seed, synth.stream_tokens(req.prefix_row),
+                                self.eng.shape.vocab)
+            ta = time.perf_counter()
+            self.eng.prefill_segmented([src], [req.prefix_len],
+                                       torch.from_numpy(toks).to(self.eng.weights.device))
+            self.eng.stream.synchronize()
+            self.res.prefill_s += time.perf_counter() - ta
+            self.res.prefill_tokens += req.prefix_len
+            self.slabs[key] = src
+        self.eng.copy_prefix(self.slabs[key], slab, req.prefix_len)
+        return req.prefix_len
+
+    def close(self):
+        if self.slabs:
+            self.eng.retire(list(self.slabs.values()))
+        self.slabs = {}
 
 
 def run_trace(eng, reqs, seed: int, live_cap: int = 8, realtime: bool = False,
               record_tokens: bool = False, max_prefill_tokens: int | None = None,
-              slab_margin: int = 8, chunk_tokens: int | None = None) -> TraceResult:
+              slab_margin: int = 8, chunk_tokens: int | None = None,
+              reuse_prefix: bool = False) -> TraceResult:
     """Serve `reqs` on `eng` (an ``Engine``) with continuous batching; see the module text.
-    With `chunk_tokens`, prompts are admitted in chunks instead (``run_trace_chunked``)."""
+    With `chunk_tokens`, prompts are admitted in chunks instead (``run_trace_chunked``); with
+    `reuse_prefix`, shared prompt prefixes are prefilled once (``SharedPrefixes``)."""
     if chunk_tokens:
         return run_trace_chunked(eng, reqs, seed, chunk_tokens, live_cap, realtime,
-                                 record_tokens, slab_margin)
+                                 record_tokens, slab_margin, reuse_prefix)
     dev = eng.weights.device
     vocab = eng.shape.vocab
     stream = eng.stream
@@ -68,6 +111,7 @@ def run_trace(eng, reqs, seed: int, live_cap: int = 8, realtime: bool = False,
     pending = deque(order)
     live = []  # per row: [request index, slab, tokens produced, time of last token]
     res = TraceResult()
+    shared = SharedPrefixes(eng, seed, res, reuse_prefix)
     tok = torch.zeros(eng.max_batch, dtype=torch.int32, device=dev)  # the live rows' last tokens
     nxt = torch.zeros(eng.max_batch, dtype=torch.int32, device=dev)
     t0 = time.perf_counter()
@@ -91,19 +135,26 @@ def run_trace(eng, reqs, seed: int, live_cap: int = 8, realtime: bool = False,
             time.sleep(max(0.0, reqs[pending[0]].arrival_s - now()))
         admit = []
         total = 0
+
+        def to_fill(i):  # prompt tokens a request's admission prefills
+            return reqs[i].prompt_len - (reqs[i].prefix_len if reuse_prefix else 0)
+
         while (pending and len(live) + len(admit) < live_cap and arrived(pending[0])
-               and total + reqs[pending[0]].prompt_len <= budget):
+               and total + to_fill(pending[0]) <= budget):
             i = pending.popleft()
             admit.append(i)
-            total += reqs[i].prompt_len
+            total += to_fill(i)
         if admit:
             slabs = [eng.kv_slab_alloc(reqs[i].prompt_len + reqs[i].output_len + slab_margin)
                      for i in admit]
-            host = np.concatenate([prompt_tokens(reqs[i], seed, vocab) for i in admit])
+            done = [shared.start(reqs[i], s) for i, s in zip(admit, slabs)]
+            host = np.concatenate([prompt_tokens(reqs[i], seed, vocab)[d:]
+                                   for i, d in zip(admit, done)])
             dtok = torch.from_numpy(host.astype(np.int32)).to(dev, non_blocking=False)
             first = torch.empty(len(admit), dtype=torch.int32, device=dev)
             ta = time.perf_counter()
-            eng.prefill_segmented(slabs, [reqs[i].prompt_len for i in admit], dtok, None, first)
+            eng.prefill_segmented(slabs, [reqs[i].prompt_len - d for i, d in zip(admit, done)],
+                                  dtok, None, first)
             stream.synchronize()
             tb = time.perf_counter()
             res.prefill_tokens += total
@@ -147,13 +198,14 @@ def run_trace(eng, reqs, seed: int, live_cap: int = 8, realtime: bool = False,
         # the next step's inputs are this step's outputs, row for row (finished rows leave at
         # the boundary)
         tok[:B] = nxt[:B]
+    shared.close()
     res.wall_s = now()
     return res
 
 
 def run_trace_chunked(eng, reqs, seed: int, chunk_tokens: int, live_cap: int = 8,
                       realtime: bool = False, record_tokens: bool = False,
-                      slab_margin: int = 8) -> TraceResult:
+                      slab_margin: int = 8, reuse_prefix: bool = False) -> TraceResult:
     """Continuous batching with chunked admission (the batching design's joiner prefill: one
     chunk per scheduler iteration, one decode step between chunks, so a running row waits at
     most one chunk for each joiner).  At every boundary the driver
@@ -179,6 +231,7 @@ def run_trace_chunked(eng, reqs, seed: int, chunk_tokens: int, live_cap: int = 8
     live = []     # per row: [request index, slab, tokens produced, time of last token]
     prompts = {}
     res = TraceResult()
+    shared = SharedPrefixes(eng, seed, res, reuse_prefix)
     tok = torch.zeros(eng.max_batch, dtype=torch.int32, device=dev)
     nxt = torch.zeros(eng.max_batch, dtype=torch.int32, device=dev)
     t0 = time.perf_counter()
@@ -205,7 +258,7 @@ def run_trace_chunked(eng, reqs, seed: int, chunk_tokens: int, live_cap: int = 8
         while pending and len(live) + len(joining) < live_cap and arrived(pending[0]):
             i = pending.popleft()
             slab = eng.kv_slab_alloc(reqs[i].prompt_len + reqs[i].output_len + slab_margin)
-            joining.append([i, slab, 0])
+            joining.append([i, slab, shared.start(reqs[i], slab)])
             prompts[i] = prompt_tokens(reqs[i], seed, vocab)
         if joining:
             segs, left = [], chunk_tokens
@@ -266,6 +319,7 @@ def run_trace_chunked(eng, reqs, seed: int, chunk_tokens: int, live_cap: int = 8
                 first_t = res.ttft_s[r[0]] + (reqs[r[0]].arrival_s if realtime else 0.0)
                 res.tpot_s[r[0]] = ((tb - t0) - first_t) / max(1, n - 1)
         tok[:B] = nxt[:B]
+    shared.close()
     res.wall_s = now()
     return res
 

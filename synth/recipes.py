@@ -114,6 +114,8 @@ class Request:
     prompt_len: int
     output_len: int
     row: int             # synthetic token stream id
+    prefix_len: int = 0  # the prompt starts with this many tokens of a shared prefix ...
+    prefix_row: int = 0  # ... drawn from this token stream (the same for every request)
 
 
 def trace_requests(n: int = 64, rate_per_s: float = 2.0, prompt_lo: int = 256,
@@ -132,4 +134,20 @@ def trace_requests(n: int = 64, rate_per_s: float = 2.0, prompt_lo: int = 256,
         t += -math.log1p(-u_gap[i]) / rate_per_s
         k = 1 + int(math.floor(math.log1p(-u_out[i]) / math.log1p(-p)))
         reqs.append(Request(t, int(plen[i]), min(k, out_cap), 1000 + i))
+    return reqs
+
+
+def agent_requests(n: int = 32, prefix_len: int = 2048, own_lo: int = 64, own_hi: int = 512,
+                   mean_out: float = 128.0, out_cap: int = 1024, seed: int = 2) -> list:
+    """Sub-agents of one harness: n requests at t = 0 whose prompts are one shared system
+    prompt of prefix_len tokens followed by an own part of U[own_lo, own_hi] tokens; outputs
+    geometric with the given mean, capped."""
+    u_out = (words(n, seed, stream_misc(21)) >> np.uint64(11)).astype(np.float64) / float(1 << 53)
+    own = uniform_ints(n, seed, stream_misc(22), own_lo, own_hi)
+    p = 1.0 / mean_out
+    reqs = []
+    for i in range(n):
+        k = 1 + int(math.floor(math.log1p(-u_out[i]) / math.log1p(-p)))
+        reqs.append(Request(0.0, prefix_len + int(own[i]), min(k, out_cap), 3000 + i,
+                            prefix_len, 2999))
     return reqs

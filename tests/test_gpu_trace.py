@@ -10,7 +10,7 @@ import torch
 import oracle
 from continuous_batching_transformer_gb300.model import DeviceWeights, Engine
 from continuous_batching_transformer_gb300.trace import prompt_tokens, run_trace
-from synth.recipes import TINY, Request
+from synth.recipes import TINY, Request, agent_requests
 from tests.gpu_harness import TOL, ensure_built
 
 pytestmark = pytest.mark.gpu
@@ -50,6 +50,34 @@ def test_trace_rows_match_oracle(chunk):
     assert eng.stats().live_slabs == 0  # every request's slab was retired
     assert max(res.step_rows) == 3 and min(res.step_rows) >= 1
     for i, req in enumerate(REQS):
+        got = res.tokens[i]
+        assert len(got) == req.output_len
+        want, logits = oracle_greedy(om, req, 0)
+        for t, (g, wv) in enumerate(zip(got, want)):
+            if g != wv:
+                top2 = np.sort(logits[t])[-2:]
+                assert top2[1] - top2[0] < TOL["bf16"], f"request {i} token {t}: {g} != {wv}"
+                break
+    eng.close()
+
+
+@pytest.mark.parametrize("chunk", [None, 8])
+def test_shared_prefix_trace_matches_oracle(chunk):
+    """Sub-agents sharing a 20-token system prompt, with prefix reuse: the prompt is prefilled
+    once and copied into each request's slab, so a request prefills only its own tokens.
+    Each request's greedy tokens against the oracle's for its whole prompt."""
+    ensure_built()
+    dev = torch.device("cuda:0")
+    w = DeviceWeights(TINY, dev)
+    om = oracle.OracleModel(TINY)
+    reqs = agent_requests(5, 20, 3, 12, 4.0, 7, seed=3)
+    eng = Engine(w, arena_bytes=32 << 20, max_batch=3, max_prefill_tokens=64)
+    res = run_trace(eng, reqs, seed=0, live_cap=3, record_tokens=True, chunk_tokens=chunk,
+                    reuse_prefix=True)
+    assert eng.device_error() == (0, 0)
+    assert res.prefill_tokens == 20 + sum(r.prompt_len - 20 for r in reqs)
+    assert eng.stats().live_slabs == 0
+    for i, req in enumerate(reqs):
         got = res.tokens[i]
         assert len(got) == req.output_len
         want, logits = oracle_greedy(om, req, 0)

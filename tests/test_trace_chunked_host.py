@@ -7,7 +7,9 @@ from types import SimpleNamespace
 import torch
 
 from continuous_batching_transformer_gb300.trace import run_trace
-from synth.recipes import Request
+import pytest
+
+from synth.recipes import Request, agent_requests
 
 
 class FakeEngine:
@@ -40,6 +42,11 @@ class FakeEngine:
             self.pos[s] += n
             if next_tokens is not None:
                 next_tokens[k] = s
+
+    def copy_prefix(self, src, dst, n):
+        assert src in self.live and dst in self.live and self.pos[src] >= n
+        self.calls.append(("copy", (src, dst, n)))
+        self.pos[dst] = n
 
     def decode_step_batch(self, slabs, last_tokens, logits=None, next_tokens=None):
         assert len(slabs) <= self.max_batch and all(s in self.live for s in slabs)
@@ -74,3 +81,28 @@ def test_chunked_admission_policy():
     assert max(res.step_rows) <= 3
     # each request's slab saw exactly its whole prompt
     assert sorted(prefilled.values()) == sorted(r.prompt_len for r in reqs)
+
+
+@pytest.mark.parametrize("chunk", [None, 16])
+def test_shared_prefix_reuse(chunk):
+    """Requests sharing a 40-token prefix: with reuse the prefix is prefilled once, every
+    request's slab starts as a copy of it, and only the requests' own tokens are prefilled."""
+    reqs = agent_requests(6, 40, 3, 20, 3.0, 6, seed=5)
+    eng = FakeEngine(max_batch=3, max_prefill_tokens=64)
+    res = run_trace(eng, reqs, seed=0, live_cap=3, chunk_tokens=chunk, reuse_prefix=True)
+    own = sum(r.prompt_len - r.prefix_len for r in reqs)
+    assert res.prefill_tokens == own + 40
+    assert res.generated == sum(r.output_len for r in reqs)
+    copies = [what for kind, what in eng.calls if kind == "copy"]
+    assert len(copies) == len(reqs) and all(n == 40 for _, _, n in copies)
+    assert len({src for src, _, _ in copies}) == 1     # one prefix slab
+    assert not eng.live                                 # it is retired at the end too
+    # every prefill of a request's slab starts at or after its copied prefix
+    copied = {dst for _, dst, _ in copies}
+    for kind, what in eng.calls:
+        if kind == "prefill":
+            for s, start, n in what:
+                assert s not in copied or start >= 40
+    plain = FakeEngine(max_batch=3, max_prefill_tokens=64)
+    res2 = run_trace(plain, reqs, seed=0, live_cap=3, chunk_tokens=chunk)
+    assert res2.prefill_tokens == sum(r.prompt_len for r in reqs)
