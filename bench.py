@@ -409,7 +409,7 @@ def trace_arm(args):
     agents = "-agents" in args.workload
     realtime = not (args.workload.endswith("-t0") or agents)
     chunk = 2048 if "-chunked" in args.workload else None
-    reuse = "-reuse" in args.workload
+    reuse = "share" if "-share" in args.workload else ("-reuse" in args.workload)
     if agents:  # 32 sub-agents sharing a 2048-token system prompt, all arriving at t = 0
         seed = 2
         reqs = agent_requests(32, 2048, 64, 512, 128.0, 1024, seed)
@@ -447,7 +447,8 @@ def trace_arm(args):
         "data": "synthetic (seeded weights, prompts and arrival times)",
         "config": {"workload": ("agents-32req-prefix2048" if agents else
                                 "trace-64req-poisson2-" + ("realtime" if realtime else "t0"))
-                               + ("-chunk2048" if chunk else "") + ("-prefix-reuse" if reuse else ""),
+                               + ("-chunk2048" if chunk else "") + ("-prefix-share" if reuse == "share" else
+                                  "-prefix-reuse" if reuse else ""),
                    "model": shape.name, "live_cap": live_cap, "admission_chunk": chunk,
                    "kv_page_tokens": page,
                    "parallelism": "1 gpu"},
@@ -455,6 +456,7 @@ def trace_arm(args):
                   "wall_s": res.wall_s, "decode_steps": res.steps,
                   "mean_live_rows": float(np.mean(res.step_rows)) if res.step_rows else 0.0,
                   "prefill_tokens": res.prefill_tokens, "prefill_s": res.prefill_s,
+                  "kv_bytes_peak": res.kv_bytes_peak,
                   "decode_s": float(np.sum(res.step_s)),
                   "ttft_s": percentiles(res.ttft_s.values()),
                   "tpot_s": percentiles(res.tpot_s.values()),

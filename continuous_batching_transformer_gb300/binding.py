@@ -32,7 +32,8 @@ EXPORTS = ["cbt_status_str", "cbt_engine_create", "cbt_engine_destroy", "cbt_sla
            "cbt_kv_slab_import", "cbt_kv_slab_export", "cbt_prefill_segmented",
            "cbt_decode_step_batch", "cbt_last_device_error", "cbt_engine_stats",
            "cbt_kernel_launches", "cbt_quantize_affine4", "cbt_engine_set_timing",
-           "cbt_engine_timing", "cbt_greedy_head_noalloc", "cbt_kv_slab_copy_prefix"]
+           "cbt_engine_timing", "cbt_greedy_head_noalloc", "cbt_kv_slab_copy_prefix",
+           "cbt_kv_slab_share_prefix"]
 KCLASS_PROJ, KCLASS_ATTN, KCLASS_OTHER = 0, 1, 2
 
 
@@ -104,6 +105,7 @@ def lib():
         L.cbt_kv_slab_import.argtypes = [c_void, c_int32, c_void, c_void, c_int32, c_int32]
         L.cbt_kv_slab_export.argtypes = [c_void, c_int32, c_void, c_void, c_int32, c_int32]
         L.cbt_kv_slab_copy_prefix.argtypes = [c_void, c_int32, c_int32, c_int32]
+        L.cbt_kv_slab_share_prefix.argtypes = [c_void, c_int32, c_int32, c_int32]
         L.cbt_prefill_segmented.argtypes = [c_void, c_void, c_void, c_int32, c_void, c_void,
                                             c_void]
         L.cbt_decode_step_batch.argtypes = [c_void, c_void, c_int32, c_void, c_void, c_void]
@@ -184,6 +186,10 @@ def kv_slab_import(e: int, slab_id: int, k_ptr: int, v_ptr: int, n_tokens: int,
 
 def kv_slab_copy_prefix(e: int, src: int, dst: int, n_tokens: int) -> None:
     _check(lib().cbt_kv_slab_copy_prefix(e, src, dst, n_tokens), "cbt_kv_slab_copy_prefix")
+
+
+def kv_slab_share_prefix(e: int, src: int, dst: int, n_tokens: int) -> None:
+    _check(lib().cbt_kv_slab_share_prefix(e, src, dst, n_tokens), "cbt_kv_slab_share_prefix")
 
 
 def kv_slab_export(e: int, slab_id: int, k_ptr: int, v_ptr: int, n_tokens: int,

@@ -4,7 +4,8 @@
 // caller's KV arena handed out by a first-fit allocator with coalescing; each carries its
 // capacity and current position (the host mirror of t_s, bumped as steps are queued).  A
 // paged engine (kv_page_tokens > 0) gives a slab fixed-size pages from the same allocator as
-// its positions are first written, and hands the kernels each page's base.
+// its positions are first written, and hands the kernels each page's base; a page may be held
+// by several slabs (a shared prompt prefix) and is copied before the first write into it.
 // A decode step or a prefill call writes a small per-token row table (slab offset, position,
 // capacity) to the device and then queues the whole forward pass on the engine stream.
 #include <cuda_runtime.h>
@@ -60,6 +61,7 @@ struct cbt_engine {
   std::unordered_map<int, Slab> slabs;
   int page = 0;            // kv_page_tokens: positions per page (0: contiguous slabs)
   size_t page_bytes = 0;
+  std::unordered_map<size_t, int> extra_holders;  // shared pages: holders beyond the first
   // per prefill call: the page bases (QueryRow bases) of every paged segment, and each
   // token's offset into them (read by the prefill attention kernels)
   std::vector<long long> hpagetab;
@@ -420,27 +422,76 @@ static long long row_base(const cbt_engine* e, const Slab& sl, int pos) {
 }
 static int row_cap(const cbt_engine* e, const Slab& sl) { return e->page ? e->page : sl.lcap; }
 
-// Paged engines: pages for positions [0, upto) of each listed slab, taken in order; on
-// running out, the pages taken by this call go back and false is returned.
-static bool ensure_pages(cbt_engine* e, const std::vector<std::pair<int, long long>>& need) {
-  if (!e->page) return true;
-  std::vector<std::pair<int, size_t>> added;
-  for (const auto& nd : need) {
-    Slab& sl = e->slabs[nd.first];
-    while ((long long)sl.pages.size() * e->page < nd.second) {
-      size_t off;
-      if (!take_extent(e, e->page_bytes, &off)) {
-        for (auto it = added.rbegin(); it != added.rend(); ++it) {
-          e->slabs[it->first].pages.pop_back();
-          give_extent(e, it->second, e->page_bytes);
-        }
-        return false;
+// pages obtainable from the free list (in a paged engine every extent taken is one page, so
+// each free extent is a run of page slots, the last one possibly followed by a remainder)
+static size_t free_pages(const cbt_engine* e) {
+  size_t n = 0;
+  for (const auto& kv : e->free_ext) n += kv.second / e->page_bytes;
+  return n;
+}
+
+// one holder lets go of a page; the last one returns it to the arena
+static void release_page(cbt_engine* e, size_t off) {
+  auto it = e->extra_holders.find(off);
+  if (it == e->extra_holders.end()) {
+    give_extent(e, off, e->page_bytes);
+  } else if (--it->second == 0) {
+    e->extra_holders.erase(it);
+  }
+}
+
+struct PageWrite {
+  int id;
+  long long lo, hi;  // the call writes positions [lo, hi) of slab id
+};
+
+// Paged engines, before a call queues writes: each listed slab gets pages for positions
+// [0, hi), and every page that [lo, hi) touches and another slab also holds is replaced by a
+// private copy of it (the copy queued on the stream ahead of the write).  The pages needed are
+// counted first, the counting following the same order as the replacement (a page whose
+// other holders all copied it away becomes private), so a call the arena cannot serve fails
+// with CBT_ERR_POOL_EXHAUSTED before anything changes.
+static cbt_status prepare_writes(cbt_engine* e, const std::vector<PageWrite>& writes) {
+  if (!e->page) return CBT_OK;
+  const long long P = e->page;
+  size_t need = 0;
+  std::unordered_map<size_t, int> copied;
+  for (const PageWrite& w : writes) {
+    const Slab& sl = e->slabs[w.id];
+    const long long have = (long long)sl.pages.size(), want = (w.hi + P - 1) / P;
+    if (want > have) need += (size_t)(want - have);
+    for (long long pg = w.lo / P; w.lo < w.hi && pg < std::min(have, want); ++pg) {
+      auto it = e->extra_holders.find(sl.pages[pg]);
+      if (it != e->extra_holders.end() && it->second > copied[sl.pages[pg]]) {
+        ++need;
+        ++copied[sl.pages[pg]];
       }
-      sl.pages.push_back(off);
-      added.push_back({nd.first, off});
     }
   }
-  return true;
+  if (need > free_pages(e)) return CBT_ERR_POOL_EXHAUSTED;
+  char* arena = static_cast<char*>(e->p.kv_arena);
+  for (const PageWrite& w : writes) {
+    Slab& sl = e->slabs[w.id];
+    const long long have = (long long)sl.pages.size(), want = (w.hi + P - 1) / P;
+    for (long long pg = w.lo / P; w.lo < w.hi && pg < std::min(have, want); ++pg) {
+      if (!e->extra_holders.count(sl.pages[pg])) continue;
+      size_t off = 0;
+      take_extent(e, e->page_bytes, &off);  // cannot fail: counted above
+      if (cudaMemcpyAsync(arena + off, arena + sl.pages[pg], e->page_bytes,
+                          cudaMemcpyDeviceToDevice, e->stream) != cudaSuccess) {
+        give_extent(e, off, e->page_bytes);
+        return CBT_ERR_CUDA;
+      }
+      release_page(e, sl.pages[pg]);
+      sl.pages[pg] = off;
+    }
+    while ((long long)sl.pages.size() < want) {
+      size_t off = 0;
+      take_extent(e, e->page_bytes, &off);
+      sl.pages.push_back(off);
+    }
+  }
+  return CBT_OK;
 }
 
 extern "C" cbt_status cbt_kv_slab_alloc(cbt_engine* e, int32_t cap, int32_t* id) {
@@ -465,7 +516,7 @@ extern "C" cbt_status cbt_kv_slab_free(cbt_engine* e, int32_t id) {
   auto it = e->slabs.find(id);
   if (it == e->slabs.end()) return CBT_ERR_BAD_SLAB;
   if (e->page) {
-    for (size_t off : it->second.pages) give_extent(e, off, e->page_bytes);
+    for (size_t off : it->second.pages) release_page(e, off);
     e->slabs.erase(it);
     return CBT_OK;
   }
@@ -522,7 +573,10 @@ static cbt_status slab_copy(cbt_engine* e, int32_t id, void* k, void* v, int32_t
   Slab& s = it->second;
   if (n < 0) return CBT_ERR_INVALID;
   if (n > s.cap || (!to_slab && n > s.pos)) return CBT_ERR_CAPACITY;
-  if (to_slab && !ensure_pages(e, {{id, (long long)n}})) return CBT_ERR_POOL_EXHAUSTED;
+  if (to_slab) {
+    const cbt_status st = prepare_writes(e, {{id, 0, (long long)n}});
+    if (st != CBT_OK) return st;
+  }
   const cbt_model_config& c = e->cfg;
   const size_t row = (size_t)c.head_dim * 2;
   cudaMemcpyKind kind = on_host ? (to_slab ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToHost)
@@ -592,7 +646,8 @@ extern "C" cbt_status cbt_kv_slab_copy_prefix(cbt_engine* e, int32_t src_id, int
   const Slab& src = si->second;
   Slab& dst = di->second;
   if (n > src.pos || n > dst.cap) return CBT_ERR_CAPACITY;
-  if (!ensure_pages(e, {{dst_id, (long long)n}})) return CBT_ERR_POOL_EXHAUSTED;
+  const cbt_status st = prepare_writes(e, {{dst_id, 0, (long long)n}});
+  if (st != CBT_OK) return st;
   // every (layer, K|V, kv head) block is a run of positions at the same place in both slabs (or
   // pages): one strided copy per run, of whole 64-position groups (a V block keeps each group
   // of 64 positions transposed; capacities and page sizes are multiples of 64, so the groups
@@ -610,6 +665,26 @@ extern "C" cbt_status cbt_kv_slab_copy_prefix(cbt_engine* e, int32_t src_id, int
     if (cudaMemcpy2DAsync(to, dp, from, sp, width, blocks, cudaMemcpyDeviceToDevice, e->stream) !=
         cudaSuccess)
       return CBT_ERR_CUDA;
+  }
+  dst.pos = n;
+  return CBT_OK;
+}
+
+extern "C" cbt_status cbt_kv_slab_share_prefix(cbt_engine* e, int32_t src_id, int32_t dst_id,
+                                               int32_t n) {
+  if (!e) return CBT_ERR_NULL;
+  auto si = e->slabs.find(src_id), di = e->slabs.find(dst_id);
+  if (si == e->slabs.end() || di == e->slabs.end()) return CBT_ERR_BAD_SLAB;
+  if (src_id == dst_id || n < 0 || di->second.pos != 0) return CBT_ERR_INVALID;
+  if (!e->page) return cbt_kv_slab_copy_prefix(e, src_id, dst_id, n);
+  const Slab& src = si->second;
+  Slab& dst = di->second;
+  if (n > src.pos || n > dst.cap) return CBT_ERR_CAPACITY;
+  for (size_t off : dst.pages) release_page(e, off);
+  dst.pages.clear();
+  for (int pg = 0; pg < (n + e->page - 1) / e->page; ++pg) {
+    dst.pages.push_back(src.pages[pg]);
+    ++e->extra_holders[src.pages[pg]];
   }
   dst.pos = n;
   return CBT_OK;
@@ -1026,16 +1101,17 @@ extern "C" cbt_status cbt_decode_step_batch(cbt_engine* e, const int32_t* ids, i
   std::unordered_set<int> seen;
   int max_keys = 0;
   long long total_keys = 0;
-  std::vector<std::pair<int, long long>> need;
+  std::vector<PageWrite> writes;
   for (int b = 0; b < B; ++b) {
     auto it = e->slabs.find(ids[b]);
     if (it == e->slabs.end()) return CBT_ERR_BAD_SLAB;
     if (!seen.insert(ids[b]).second) return CBT_ERR_DUP_SLAB;
     const Slab& sl = it->second;
     if (sl.pos + 1 > sl.cap) return CBT_ERR_CAPACITY;
-    need.push_back({ids[b], sl.pos + 1});
+    writes.push_back({ids[b], sl.pos, sl.pos + 1});
   }
-  if (!ensure_pages(e, need)) return CBT_ERR_POOL_EXHAUSTED;
+  const cbt_status st = prepare_writes(e, writes);
+  if (st != CBT_OK) return st;
   e->hslab.resize(B);
   for (int b = 0; b < B; ++b) {
     const Slab& sl = e->slabs[ids[b]];
@@ -1179,9 +1255,13 @@ extern "C" cbt_status cbt_prefill_segmented(cbt_engine* e, const int32_t* ids,
     total_keys += (long long)lens[s] * sl.pos + (long long)lens[s] * (lens[s] + 1) / 2;
   }
   if (T > e->p.max_prefill_tokens) return CBT_ERR_TOKENS;
-  std::vector<std::pair<int, long long>> need;
-  for (int s = 0; s < K; ++s) need.push_back({ids[s], (long long)e->slabs[ids[s]].pos + lens[s]});
-  if (!ensure_pages(e, need)) return CBT_ERR_POOL_EXHAUSTED;
+  std::vector<PageWrite> writes;
+  for (int s = 0; s < K; ++s) {
+    const long long p0 = e->slabs[ids[s]].pos;
+    writes.push_back({ids[s], p0, p0 + lens[s]});
+  }
+  const cbt_status pst = prepare_writes(e, writes);
+  if (pst != CBT_OK) return pst;
   // paged segments: every page base of the segment once, each token pointing at its segment's
   e->hpagetab.clear();
   e->htok_pages.assign(T, -1);

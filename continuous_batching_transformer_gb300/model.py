@@ -138,6 +138,11 @@ class Engine:
         """dst takes positions [0, n_tokens) of src (a shared prompt prefix computed once)."""
         B.kv_slab_copy_prefix(self.handle, src, dst, n_tokens)
 
+    def share_prefix(self, src: int, dst: int, n_tokens: int) -> None:
+        """dst (at position 0) takes positions [0, n_tokens) of src by reference: on a paged
+        engine the pages are shared and copied only when one of the slabs writes into one."""
+        B.kv_slab_share_prefix(self.handle, src, dst, n_tokens)
+
     def export_kv(self, slab: int, k: torch.Tensor, v: torch.Tensor, n_tokens: int) -> None:
         on_host = k.device.type == "cpu"
         B.kv_slab_export(self.handle, slab, k.data_ptr(), v.data_ptr(), n_tokens, on_host)

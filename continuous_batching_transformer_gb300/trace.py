@@ -44,6 +44,11 @@ class TraceResult:
     ttft_s: dict = field(default_factory=dict)          # request index -> time to first token
     tpot_s: dict = field(default_factory=dict)          # request index -> time per output token
     tokens: dict = field(default_factory=dict)          # request index -> generated tokens
+    kv_bytes_peak: int = 0                              # most KV arena bytes held after a call
+
+    def note_kv(self, eng):
+        if hasattr(eng, "stats"):
+            self.kv_bytes_peak = max(self.kv_bytes_peak, int(eng.stats().slab_bytes_in_use))
 
 
 def prompt_tokens(req, seed: int, vocab: int) -> np.ndarray:
@@ -58,15 +63,20 @@ def prompt_tokens(req, seed: int, vocab: int) -> np.ndarray:
 class SharedPrefixes:
     """Prefix reuse (the batching design: sub-agents share long system prompts and reuse one
     prefill): each shared prefix is prefilled once into a slab of its own, and a request's
-    slab starts as a copy of it (``copy_prefix``), so only the request's own tokens are
-    prefilled.  Without reuse every prompt is prefilled whole."""
+    slab starts from it, so only the request's own tokens are prefilled.  `reuse` True or
+    "copy": the slab starts as a copy of the prefix (``copy_prefix``); "share": it holds the
+    prefix's pages by reference (``share_prefix``: a paged engine copies a page only when a
+    slab writes into it, so N requests hold one copy of the prompt).  Without reuse every
+    prompt is prefilled whole."""
 
-    def __init__(self, eng, seed: int, res: TraceResult, reuse: bool):
+    def __init__(self, eng, seed: int, res: TraceResult, reuse):
+        if reuse not in (False, True, "copy", "share"):
+            raise ValueError(f"reuse must be False, True, 'copy' or 'share', not {reuse!r}")
         self.eng, self.seed, self.res, self.reuse = eng, seed, res, reuse
         self.slabs = {}
 
     def start(self, req, slab) -> int:
-        """Prompt tokens already in `slab` (its copied shared prefix) -- 0 without reuse."""
+        """Prompt tokens already in `slab` (its shared prefix) -- 0 without reuse."""
         if not (self.reuse and req.prefix_len):
             return 0
         if req.prompt_len <= req.prefix_len:
@@ -83,7 +93,10 @@ class SharedPrefixes:
             self.res.prefill_s += time.perf_counter() - ta
             self.res.prefill_tokens += req.prefix_len
             self.slabs[key] = src
-        self.eng.copy_prefix(self.slabs[key], slab, req.prefix_len)
+        if self.reuse == "share":
+            self.eng.share_prefix(self.slabs[key], slab, req.prefix_len)
+        else:
+            self.eng.copy_prefix(self.slabs[key], slab, req.prefix_len)
         return req.prefix_len
 
     def close(self):
@@ -95,10 +108,11 @@ class SharedPrefixes:
 def run_trace(eng, reqs, seed: int, live_cap: int = 8, realtime: bool = False,
               record_tokens: bool = False, max_prefill_tokens: int | None = None,
               slab_margin: int = 8, chunk_tokens: int | None = None,
-              reuse_prefix: bool = False) -> TraceResult:
+              reuse_prefix: bool | str = False) -> TraceResult:
     """Serve `reqs` on `eng` (an ``Engine``) with continuous batching; see the module text.
     With `chunk_tokens`, prompts are admitted in chunks instead (``run_trace_chunked``); with
-    `reuse_prefix`, shared prompt prefixes are prefilled once (``SharedPrefixes``)."""
+    `reuse_prefix` (True or "copy", or "share"), shared prompt prefixes are prefilled once
+    (``SharedPrefixes``)."""
     if chunk_tokens:
         return run_trace_chunked(eng, reqs, seed, chunk_tokens, live_cap, realtime,
                                  record_tokens, slab_margin, reuse_prefix)
@@ -159,6 +173,7 @@ def run_trace(eng, reqs, seed: int, live_cap: int = 8, realtime: bool = False,
             tb = time.perf_counter()
             res.prefill_tokens += total
             res.prefill_s += tb - ta
+            res.note_kv(eng)
             firsts = first.cpu().tolist() if record_tokens else None
             # the new rows join the live set; their first token is the next step's input
             rows_before = len(live)
@@ -179,6 +194,7 @@ def run_trace(eng, reqs, seed: int, live_cap: int = 8, realtime: bool = False,
         stream.synchronize()
         tb = time.perf_counter()
         res.steps += 1
+        res.note_kv(eng)
         res.step_rows.append(B)
         res.step_s.append(tb - ta)
         res.step_start.append(ta - t0)
@@ -205,7 +221,7 @@ def run_trace(eng, reqs, seed: int, live_cap: int = 8, realtime: bool = False,
 
 def run_trace_chunked(eng, reqs, seed: int, chunk_tokens: int, live_cap: int = 8,
                       realtime: bool = False, record_tokens: bool = False,
-                      slab_margin: int = 8, reuse_prefix: bool = False) -> TraceResult:
+                      slab_margin: int = 8, reuse_prefix: bool | str = False) -> TraceResult:
     """Continuous batching with chunked admission (the batching design's joiner prefill: one
     chunk per scheduler iteration, one decode step between chunks, so a running row waits at
     most one chunk for each joiner).  At every boundary the driver
@@ -278,6 +294,7 @@ def run_trace_chunked(eng, reqs, seed: int, chunk_tokens: int, live_cap: int = 8
             tb = time.perf_counter()
             res.prefill_tokens += len(host)
             res.prefill_s += tb - ta
+            res.note_kv(eng)
             done = [k for k, (row, _, b) in enumerate(segs) if b == reqs[row[0]].prompt_len]
             firsts = first.cpu().tolist() if (record_tokens and done) else None
             rows_before = len(live)
@@ -303,6 +320,7 @@ def run_trace_chunked(eng, reqs, seed: int, chunk_tokens: int, live_cap: int = 8
         stream.synchronize()
         tb = time.perf_counter()
         res.steps += 1
+        res.note_kv(eng)
         res.step_rows.append(B)
         res.step_s.append(tb - ta)
         res.step_start.append(ta - t0)

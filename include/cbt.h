@@ -134,7 +134,11 @@ typedef struct {
                               * the arena cannot give fails with CBT_ERR_POOL_EXHAUSTED before
                               * queuing anything (pages it took are returned).  Page p of a
                               * slab holds positions [p * kv_page_tokens, (p + 1) *
-                              * kv_page_tokens) in the layout described at cbt_slab_bytes. */
+                              * kv_page_tokens) in the layout described at cbt_slab_bytes.
+                              * Pages may be shared between slabs (cbt_kv_slab_share_prefix);
+                              * a call that writes a position in a shared page first queues a
+                              * copy of that page into a new page of the writing slab (copy on
+                              * write), and that page counts towards the same pool check. */
 } cbt_engine_params;
 
 typedef struct {
@@ -206,6 +210,22 @@ cbt_status cbt_kv_slab_export(cbt_engine* e, int32_t slab_id, void* k, void* v,
  * n_tokens < 0), CBT_ERR_CAPACITY, CBT_ERR_CUDA. */
 cbt_status cbt_kv_slab_copy_prefix(cbt_engine* e, int32_t src_id, int32_t dst_id,
                                    int32_t n_tokens);
+
+/* Prefix sharing (the same pages, the mlx-bun batching design, sections 1 and 4.2): slab dst_id
+ * takes positions [0, n_tokens) of slab src_id without a copy and its position becomes n_tokens.
+ * On a paged engine dst holds src's first ceil(n_tokens / kv_page_tokens) pages by reference
+ * (no device work, no arena bytes); the first later write into a shared page by either slab
+ * (prefill, decode, import, copy_prefix into it) copies that one page first, so neither slab
+ * ever sees the other's later positions, and a page returns to the arena when its last holder
+ * frees it.  On a contiguous engine there are no pages to share and the call is
+ * cbt_kv_slab_copy_prefix.
+ *   src_id, dst_id  distinct live slabs; dst at position 0 (pages it holds are released);
+ *                   n_tokens <= src's position and <= dst's capacity.
+ * Errors (nothing queued, nothing changed): CBT_ERR_BAD_SLAB, CBT_ERR_INVALID (same slab,
+ * n_tokens < 0 or dst's position not 0), CBT_ERR_CAPACITY, and on a contiguous engine those of
+ * cbt_kv_slab_copy_prefix. */
+cbt_status cbt_kv_slab_share_prefix(cbt_engine* e, int32_t src_id, int32_t dst_id,
+                                    int32_t n_tokens);
 
 /* Segmented prefill of K prompts (forward_batch_segmented).
  *   slab_ids  host int32 [K], distinct live slabs.  Segment s's tokens go to positions

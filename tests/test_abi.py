@@ -95,6 +95,7 @@ def test_calls_reject_null_engine(lib):
     assert lib.cbt_prefill_segmented(None, None, None, 1, None, None, None) == -2
     assert lib.cbt_retire(None, None, 0) == -2
     assert lib.cbt_kv_slab_copy_prefix(None, 1, 2, 3) == -2
+    assert lib.cbt_kv_slab_share_prefix(None, 1, 2, 3) == -2
     assert lib.cbt_quantize_affine4(None, 1, 64, 64, None, None, None, None) == -2
     fake = ctypes.c_void_p(0x1000)
     assert lib.cbt_quantize_affine4(fake, 4, 96, 64, fake, fake, fake, None) == -1  # cols % group

@@ -138,3 +138,137 @@ def test_paged_allocation_errors_and_state():
     assert torch.equal(k3, k[:, :, :100]) and torch.equal(v3, v[:, :, :100])
     assert eng.device_error() == (0, 0)
     eng.close()
+
+
+def shared_prefix_run(w, mode):
+    """A 200-token prompt prefilled into s; d1 starts from its 200 positions and d2 from its
+    first 150 (shared pages, or copies), each prefills tokens of its own (both land in the
+    prompt's second page, which s still holds), all three decode a step, s retires, d1 and d2
+    decode again.  Every call's logits, and the arena bytes held after each stage."""
+    dev = torch.device("cuda:0")
+    pb = B.slab_bytes(w.cfg, PAGE)
+    eng = Engine(w, arena_bytes=8 * pb, max_batch=4, max_prefill_tokens=512, page_tokens=PAGE)
+    pre = seeded(200, 21, TINY.vocab)
+    own = np.concatenate([seeded(30, 22, TINY.vocab), seeded(20, 23, TINY.vocab)])
+    lg = torch.empty((3, TINY.vocab), dtype=torch.float32, device=dev)
+    out, used = [], []
+    s = eng.kv_slab_alloc(400)
+    eng.prefill_segmented([s], [200], to_dev(pre, dev), lg[:1])
+    out.append(lg[:1].cpu().numpy().copy())
+    d1, d2 = eng.kv_slab_alloc(400), eng.kv_slab_alloc(400)
+    reuse = eng.share_prefix if mode == "share" else eng.copy_prefix
+    reuse(s, d1, 200)
+    reuse(s, d2, 150)
+    used.append(eng.stats().slab_bytes_in_use // pb)
+    eng.prefill_segmented([d1, d2], [30, 20], to_dev(own, dev), lg[:2])
+    out.append(lg[:2].cpu().numpy().copy())
+    used.append(eng.stats().slab_bytes_in_use // pb)
+    eng.decode_step_batch([s, d1, d2], to_dev(np.array([7, 8, 9], np.int32), dev), lg)
+    out.append(lg.cpu().numpy().copy())
+    used.append(eng.stats().slab_bytes_in_use // pb)
+    eng.retire([s])
+    used.append(eng.stats().slab_bytes_in_use // pb)
+    eng.decode_step_batch([d1, d2], to_dev(np.array([10, 11], np.int32), dev), lg[:2])
+    out.append(lg[:2].cpu().numpy().copy())
+    assert eng.device_error() == (0, 0)
+    eng.close()
+    return out, used, pre, own
+
+
+def test_shared_prefix_pages_match_oracle_and_copy():
+    """Prefix sharing: the shared run's logits follow the oracle (each sequence computed from
+    its whole prompt in one pass) and equal, bit for bit, the same run with prefix copies; the
+    shared run holds one copy of the prompt's pages and copies only the page both sequences
+    write into."""
+    ensure_built()
+    w = DeviceWeights(TINY, torch.device("cuda:0"))
+    om = oracle.OracleModel(TINY)
+    shared, used_s, pre, own = shared_prefix_run(w, "share")
+    copied, used_c, _, _ = shared_prefix_run(w, "copy")
+    cs, c1, c2 = (oracle.KVCache(TINY, 400) for _ in range(3))
+    refs = [oracle.prefill_segmented(om, [cs], [200], pre),
+            oracle.prefill_segmented(om, [c1, c2], [230, 170],
+                                     np.concatenate([pre, own[:30], pre[:150], own[30:]])),
+            oracle.decode_step_batch(om, [cs, c1, c2], np.array([7, 8, 9], np.int32)),
+            oracle.decode_step_batch(om, [c1, c2], np.array([10, 11], np.int32))]
+    for k, (a, b, r) in enumerate(zip(shared, copied, refs)):
+        check_logits(a, r, TOL["bf16"], f"shared prefix call {k}")
+        np.testing.assert_array_equal(a, b)
+    # shared: 2 pages after sharing; d1 and d2 each copy the second page when they write into
+    # it; s's retirement returns only its second page (the first is still held by d1 and d2)
+    assert used_s == [2, 4, 4, 3]
+    assert used_c == [6, 6, 6, 4]
+
+
+def test_shared_pages_copy_on_write_under_a_full_arena():
+    """A write into a shared page needs a free page for its copy: with none free the call fails
+    before queuing anything and changes nothing; once a page is returned it goes through, and
+    the other holders keep their contents."""
+    ensure_built()
+    dev = torch.device("cuda:0")
+    w = DeviceWeights(TINY, dev)
+    om = oracle.OracleModel(TINY)
+    pb = B.slab_bytes(w.cfg, PAGE)
+    eng = Engine(w, arena_bytes=3 * pb, max_batch=4, max_prefill_tokens=512, page_tokens=PAGE)
+    pre, o1, o2 = seeded(200, 31, TINY.vocab), seeded(30, 32, TINY.vocab), seeded(20, 33, TINY.vocab)
+    lg = torch.empty((1, TINY.vocab), dtype=torch.float32, device=dev)
+    s, d1 = eng.kv_slab_alloc(400), eng.kv_slab_alloc(400)
+    eng.prefill_segmented([s], [200], to_dev(pre, dev), lg)
+    # errors: a non-empty destination, the same slab, more positions than the source holds
+    assert status_of(eng.share_prefix, s, s, 10) == -1
+    assert status_of(eng.share_prefix, s, d1, 201) == -6
+    assert status_of(eng.share_prefix, s, 12345, 10) == -3
+    eng.share_prefix(s, d1, 200)
+    assert status_of(eng.share_prefix, s, d1, 100) == -1 and eng.position(d1) == 200
+    eng.prefill_segmented([d1], [30], to_dev(o1, dev), lg)      # copies page 1: arena full
+    assert eng.stats().slab_bytes_in_use == 3 * pb
+    d2 = eng.kv_slab_alloc(400)
+    eng.share_prefix(s, d2, 200)
+    assert status_of(eng.prefill_segmented, [d2], [20], to_dev(o2, dev)) == -7
+    assert eng.position(d2) == 200 and eng.stats().slab_bytes_in_use == 3 * pb
+    k1 = torch.empty((TINY.n_layers, TINY.n_kv_heads, 230, TINY.head_dim), dtype=torch.bfloat16)
+    v1 = torch.empty_like(k1)
+    eng.export_kv(d1, k1, v1, 230)
+    eng.retire([d1])                                            # returns d1's copy of page 1
+    assert eng.stats().slab_bytes_in_use == 2 * pb
+    eng.prefill_segmented([d2], [20], to_dev(o2, dev), lg)      # copies page 1 again
+    c2 = oracle.KVCache(TINY, 400)
+    ref = oracle.prefill_segmented(om, [c2], [220], np.concatenate([pre, o2]))
+    check_logits(lg.cpu().numpy(), ref, TOL["bf16"], "prefill after a copy on write")
+    assert eng.stats().slab_bytes_in_use == 3 * pb
+    # an import over a shared first page: no page for the copy until s retires
+    d3 = eng.kv_slab_alloc(400)
+    eng.share_prefix(s, d3, 100)
+    g = torch.Generator().manual_seed(5)
+    k = torch.randn((TINY.n_layers, TINY.n_kv_heads, 100, TINY.head_dim), generator=g).to(torch.bfloat16)
+    v = torch.randn(k.shape, generator=g).to(torch.bfloat16)
+    assert status_of(eng.import_kv, d3, k, v, 100) == -7 and eng.position(d3) == 100
+    eng.retire([s])
+    eng.import_kv(d3, k, v, 100)
+    k3, v3 = torch.empty_like(k), torch.empty_like(v)
+    eng.export_kv(d3, k3, v3, 100)
+    assert torch.equal(k3, k) and torch.equal(v3, v)
+    # d2 still reads the prompt it shared (positions [0, 200) as d1 saw them)
+    k2 = torch.empty((TINY.n_layers, TINY.n_kv_heads, 200, TINY.head_dim), dtype=torch.bfloat16)
+    v2 = torch.empty_like(k2)
+    eng.export_kv(d2, k2, v2, 200)
+    assert torch.equal(k2, k1[:, :, :200]) and torch.equal(v2, v1[:, :, :200])
+    assert eng.device_error() == (0, 0)
+    eng.close()
+
+
+def test_share_on_a_contiguous_engine_copies():
+    ensure_built()
+    dev = torch.device("cuda:0")
+    w = DeviceWeights(TINY, dev)
+    eng = Engine(w, arena_bytes=2 * B.slab_bytes(w.cfg, 128), max_batch=2, max_prefill_tokens=128)
+    s, d = eng.kv_slab_alloc(128), eng.kv_slab_alloc(128)
+    eng.prefill_segmented([s], [50], to_dev(seeded(50, 41, TINY.vocab), dev))
+    eng.share_prefix(s, d, 50)
+    assert eng.position(d) == 50
+    shape = (TINY.n_layers, TINY.n_kv_heads, 50, TINY.head_dim)
+    ks, vs, kd, vd = (torch.empty(shape, dtype=torch.bfloat16) for _ in range(4))
+    eng.export_kv(s, ks, vs, 50)
+    eng.export_kv(d, kd, vd, 50)
+    assert torch.equal(ks, kd) and torch.equal(vs, vd)
+    eng.close()

@@ -61,19 +61,21 @@ def test_trace_rows_match_oracle(chunk):
     eng.close()
 
 
-@pytest.mark.parametrize("chunk", [None, 8])
-def test_shared_prefix_trace_matches_oracle(chunk):
+@pytest.mark.parametrize("chunk,mode", [(None, True), (8, True), (None, "share"), (8, "share")])
+def test_shared_prefix_trace_matches_oracle(chunk, mode):
     """Sub-agents sharing a 20-token system prompt, with prefix reuse: the prompt is prefilled
-    once and copied into each request's slab, so a request prefills only its own tokens.
-    Each request's greedy tokens against the oracle's for its whole prompt."""
+    once and copied into each request's slab (or, on a paged engine, its page shared), so a
+    request prefills only its own tokens.  Each request's greedy tokens against the oracle's
+    for its whole prompt."""
     ensure_built()
     dev = torch.device("cuda:0")
     w = DeviceWeights(TINY, dev)
     om = oracle.OracleModel(TINY)
     reqs = agent_requests(5, 20, 3, 12, 4.0, 7, seed=3)
-    eng = Engine(w, arena_bytes=32 << 20, max_batch=3, max_prefill_tokens=64)
+    eng = Engine(w, arena_bytes=32 << 20, max_batch=3, max_prefill_tokens=64,
+                 page_tokens=128 if mode == "share" else 0)
     res = run_trace(eng, reqs, seed=0, live_cap=3, record_tokens=True, chunk_tokens=chunk,
-                    reuse_prefix=True)
+                    reuse_prefix=mode)
     assert eng.device_error() == (0, 0)
     assert res.prefill_tokens == 20 + sum(r.prompt_len - 20 for r in reqs)
     assert eng.stats().live_slabs == 0

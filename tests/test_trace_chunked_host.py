@@ -48,6 +48,11 @@ class FakeEngine:
         self.calls.append(("copy", (src, dst, n)))
         self.pos[dst] = n
 
+    def share_prefix(self, src, dst, n):
+        assert src in self.live and dst in self.live and self.pos[src] >= n and self.pos[dst] == 0
+        self.calls.append(("share", (src, dst, n)))
+        self.pos[dst] = n
+
     def decode_step_batch(self, slabs, last_tokens, logits=None, next_tokens=None):
         assert len(slabs) <= self.max_batch and all(s in self.live for s in slabs)
         self.calls.append(("decode", list(slabs)))
@@ -84,16 +89,20 @@ def test_chunked_admission_policy():
 
 
 @pytest.mark.parametrize("chunk", [None, 16])
-def test_shared_prefix_reuse(chunk):
+@pytest.mark.parametrize("mode", [True, "share"])
+def test_shared_prefix_reuse(chunk, mode):
     """Requests sharing a 40-token prefix: with reuse the prefix is prefilled once, every
-    request's slab starts as a copy of it, and only the requests' own tokens are prefilled."""
+    request's slab starts from it (a copy, or its pages shared), and only the requests' own
+    tokens are prefilled."""
     reqs = agent_requests(6, 40, 3, 20, 3.0, 6, seed=5)
     eng = FakeEngine(max_batch=3, max_prefill_tokens=64)
-    res = run_trace(eng, reqs, seed=0, live_cap=3, chunk_tokens=chunk, reuse_prefix=True)
+    res = run_trace(eng, reqs, seed=0, live_cap=3, chunk_tokens=chunk, reuse_prefix=mode)
     own = sum(r.prompt_len - r.prefix_len for r in reqs)
     assert res.prefill_tokens == own + 40
     assert res.generated == sum(r.output_len for r in reqs)
-    copies = [what for kind, what in eng.calls if kind == "copy"]
+    kind_used = "share" if mode == "share" else "copy"
+    assert not any(kind == ("copy" if mode == "share" else "share") for kind, _ in eng.calls)
+    copies = [what for kind, what in eng.calls if kind == kind_used]
     assert len(copies) == len(reqs) and all(n == 40 for _, _, n in copies)
     assert len({src for src, _, _ in copies}) == 1     # one prefix slab
     assert not eng.live                                 # it is retired at the end too
@@ -106,3 +115,9 @@ def test_shared_prefix_reuse(chunk):
     plain = FakeEngine(max_batch=3, max_prefill_tokens=64)
     res2 = run_trace(plain, reqs, seed=0, live_cap=3, chunk_tokens=chunk)
     assert res2.prefill_tokens == sum(r.prompt_len for r in reqs)
+
+
+def test_reuse_mode_checked():
+    with pytest.raises(ValueError):
+        run_trace(FakeEngine(), agent_requests(2, 40, 3, 20, 3.0, 6, seed=5), seed=0,
+                  reuse_prefix="pages")
