@@ -68,7 +68,9 @@ class Model(ctypes.Structure):
 
 
 class KV(ctypes.Structure):
-    _fields_ = [("capacity", c_int), ("len", c_int), ("k", c_void), ("v", c_void)]
+    _fields_ = [("capacity", c_int), ("len", c_int), ("k", c_void), ("v", c_void),
+                ("kq", c_void), ("vq", c_void), ("ks", c_void), ("kb", c_void), ("vs", c_void),
+                ("vb", c_void), ("qlen", c_int)]
 
 
 def lib():
@@ -89,6 +91,10 @@ def lib():
         L.orc_argmax.argtypes = [c_void, c_int]
         L.orc_quantize_affine4.argtypes = [c_void, c_int, c_int, c_int, c_void, c_void, c_void]
         L.orc_dequantize_affine4.argtypes = [c_void, c_void, c_void, c_int, c_int, c_int, c_void]
+        L.orc_quantize_kv8.argtypes = [c_void, c_int, c_int, c_void, c_void, c_void]
+        L.orc_attention_kv8.argtypes = [c_void, c_void, c_void, c_void, c_void, c_void, c_void,
+                                        c_int, c_int, c_void]
+        L.orc_kv8_convert.argtypes = [P(Config), P(KV)]
         L.orc_forward.argtypes = [P(Model), P(KV), c_int, c_int, c_void, c_void, c_void, c_void,
                                   c_void]
         L.orc_decode_step_batch.argtypes = [P(Model), P(KV), c_int, c_void, c_void]
@@ -169,6 +175,28 @@ def dequantize_affine4(packed, scales, biases, group: int = 64) -> np.ndarray:
     return out
 
 
+def quantize_kv8(x_bf16: np.ndarray):
+    """8-bit affine rows (groups of 64 along the last axis): codes, bf16 scales, bf16 biases."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    rows, cols = x.shape
+    codes = np.empty((rows, cols), dtype=np.uint8)
+    scales = np.empty((rows, cols // 64), dtype=np.uint16)
+    biases = np.empty((rows, cols // 64), dtype=np.uint16)
+    if lib().orc_quantize_kv8(_ptr(x), rows, cols, _ptr(codes), _ptr(scales), _ptr(biases)) != 0:
+        raise ValueError("bad quantisation shape")
+    return codes, scales, biases
+
+
+def attention_kv8(q: np.ndarray, k8, v8) -> np.ndarray:
+    """Attention of one query over 8-bit K/V rows: k8 and v8 are (codes, scales, biases)."""
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    parts = [np.ascontiguousarray(a) for a in (*k8, *v8)]
+    out = np.empty(q.size, dtype=np.float32)
+    lib().orc_attention_kv8(_ptr(q), *[_ptr(a) for a in parts], parts[0].shape[0], q.size,
+                            _ptr(out))
+    return out
+
+
 # ---- the model ----------------------------------------------------------------------
 class LinearW:
     """One projection in the oracle's format: bf16 [out, in], or 4-bit affine triple."""
@@ -240,18 +268,42 @@ class OracleModel:
 
 
 class KVCache:
-    """One sequence's cache, bf16 bits [n_layers, n_kv_heads, capacity, head_dim] for K and V."""
+    """One sequence's cache, bf16 bits [n_layers, n_kv_heads, capacity, head_dim] for K and V;
+    with kv_bits = 8 also their 8-bit affine codes (groups of 64 along head_dim) and bf16
+    scales/biases, which attention reads once the cache's first call has converted it."""
 
-    def __init__(self, shape: ModelShape, capacity: int):
+    def __init__(self, shape: ModelShape, capacity: int, kv_bits: int = 16):
+        if kv_bits not in (8, 16):
+            raise ValueError("kv_bits is 16 (bf16) or 8 (8-bit affine)")
         self.shape = shape
         dims = (shape.n_layers, shape.n_kv_heads, capacity, shape.head_dim)
         self.k = np.zeros(dims, dtype=np.uint16)
         self.v = np.zeros(dims, dtype=np.uint16)
         self.capacity = capacity
         self.len = 0
+        self.kv_bits = kv_bits
+        self.qlen = 0
+        self.q8 = None
+        if kv_bits == 8:
+            gdims = dims[:-1] + (shape.head_dim // 64,)
+            self.q8 = {"kq": np.zeros(dims, np.uint8), "vq": np.zeros(dims, np.uint8),
+                       "ks": np.zeros(gdims, np.uint16), "kb": np.zeros(gdims, np.uint16),
+                       "vs": np.zeros(gdims, np.uint16), "vb": np.zeros(gdims, np.uint16)}
 
     def struct(self) -> KV:
-        return KV(self.capacity, self.len, _ptr(self.k), _ptr(self.v))
+        q = self.q8 or {}
+        return KV(self.capacity, self.len, _ptr(self.k), _ptr(self.v),
+                  *[_ptr(q.get(n)) for n in ("kq", "vq", "ks", "kb", "vs", "vb")], self.qlen)
+
+    def convert(self) -> None:
+        """Quantise positions [qlen, len) (an 8-bit cache filled with bf16 K/V directly)."""
+        st = self.struct()
+        s = self.shape
+        m = Config(s.n_layers, s.d_model, s.n_heads, s.n_kv_heads, s.head_dim, s.d_ff, s.vocab,
+                   s.rms_eps, s.rope_theta, 0, s.group_size)
+        if lib().orc_kv8_convert(ctypes.byref(m), ctypes.byref(st)) != 0:
+            raise ValueError("not an 8-bit cache")
+        self.qlen = st.qlen
 
     def fill_synthetic(self, row: int, n_tok: int, seed: int) -> None:
         """Positions [0, n_tok) from the seeded KV draws of synthetic row `row`."""
@@ -262,6 +314,9 @@ class KVCache:
                            s.kv_sigma)
             dst[:, :, :n_tok, :] = src
         self.len = n_tok
+        if self.kv_bits == 8:
+            self.qlen = 0
+            self.convert()
 
 
 def _kv_array(caches):
@@ -274,6 +329,7 @@ def _kv_array(caches):
 def _sync_back(arr, caches):
     for i, c in enumerate(caches):
         c.len = arr[i].len
+        c.qlen = arr[i].qlen
 
 
 def forward(m: OracleModel, caches, seq, pos, tok, want) -> np.ndarray:

@@ -59,15 +59,15 @@ void orc_rope(float* vec, int head_dim, int pos, double theta) {
 }
 
 /* ---- softmax attention of one query over n_keys cached keys/values ----------------- */
-void orc_attention(const float* q, const uint16_t* k, const uint16_t* v, int n_keys,
-                   int head_dim, float* out) {
+/* softmax(q.K^T / sqrt(hd)) V over n_keys rows of K and V given as doubles */
+static void attention_values(const float* q, const double* k, const double* v, int n_keys,
+                             int head_dim, float* out) {
   double* s = (double*)malloc(sizeof(double) * (size_t)(n_keys > 0 ? n_keys : 1));
   double inv_sqrt = 1.0 / sqrt((double)head_dim);
   double mx = -INFINITY;
   for (int t = 0; t < n_keys; ++t) {
     double dot = 0.0;
-    for (int d = 0; d < head_dim; ++d)
-      dot += (double)q[d] * (double)orc_bf16_to_f32(k[(size_t)t * head_dim + d]);
+    for (int d = 0; d < head_dim; ++d) dot += (double)q[d] * k[(size_t)t * head_dim + d];
     s[t] = dot * inv_sqrt;
     if (s[t] > mx) mx = s[t];
   }
@@ -78,10 +78,79 @@ void orc_attention(const float* q, const uint16_t* k, const uint16_t* v, int n_k
   }
   for (int d = 0; d < head_dim; ++d) {
     double acc = 0.0;
-    for (int t = 0; t < n_keys; ++t) acc += s[t] * (double)orc_bf16_to_f32(v[(size_t)t * head_dim + d]);
+    for (int t = 0; t < n_keys; ++t) acc += s[t] * v[(size_t)t * head_dim + d];
     out[d] = (float)(acc / z);
   }
   free(s);
+}
+
+void orc_attention(const float* q, const uint16_t* k, const uint16_t* v, int n_keys,
+                   int head_dim, float* out) {
+  size_t n = (size_t)(n_keys > 0 ? n_keys : 1) * head_dim;
+  double* kd = (double*)malloc(sizeof(double) * n);
+  double* vd = (double*)malloc(sizeof(double) * n);
+  for (size_t i = 0; i < (size_t)n_keys * head_dim; ++i) {
+    kd[i] = orc_bf16_to_f32(k[i]);
+    vd[i] = orc_bf16_to_f32(v[i]);
+  }
+  attention_values(q, kd, vd, n_keys, head_dim, out);
+  free(kd);
+  free(vd);
+}
+
+/* ---- 8-bit affine KV: x^ = scale * q + bias per group of 64 along head_dim --------- */
+int orc_quantize_kv8(const uint16_t* x, int rows, int cols, uint8_t* codes, uint16_t* scales,
+                     uint16_t* biases) {
+  if (rows < 0 || cols <= 0 || cols % 64 != 0) return ORC_EINVAL;
+  const int ng = cols / 64;
+  for (int r = 0; r < rows; ++r) {
+    for (int g = 0; g < ng; ++g) {
+      const uint16_t* src = x + (size_t)r * cols + (size_t)g * 64;
+      double mn = orc_bf16_to_f32(src[0]), mx = mn;
+      for (int i = 1; i < 64; ++i) {
+        double v = orc_bf16_to_f32(src[i]);
+        if (v < mn) mn = v;
+        if (v > mx) mx = v;
+      }
+      uint16_t sb = orc_f32_to_bf16((float)((mx - mn) / 255.0));
+      uint16_t bb = orc_f32_to_bf16((float)mn);
+      double sc = orc_bf16_to_f32(sb), bi = orc_bf16_to_f32(bb);
+      scales[(size_t)r * ng + g] = sb;
+      biases[(size_t)r * ng + g] = bb;
+      for (int i = 0; i < 64; ++i) {
+        int q = 0;
+        if (sc != 0.0) {
+          double t = rint(((double)orc_bf16_to_f32(src[i]) - bi) / sc);
+          q = t < 0.0 ? 0 : (t > 255.0 ? 255 : (int)t);
+        }
+        codes[(size_t)r * cols + (size_t)g * 64 + i] = (uint8_t)q;
+      }
+    }
+  }
+  return ORC_OK;
+}
+
+static double kv8_value(const uint8_t* codes, const uint16_t* scales, const uint16_t* biases,
+                        int hd, int t, int d) {
+  size_t gi = (size_t)t * (hd / 64) + d / 64;
+  return (double)orc_bf16_to_f32(scales[gi]) * codes[(size_t)t * hd + d] +
+         (double)orc_bf16_to_f32(biases[gi]);
+}
+
+void orc_attention_kv8(const float* q, const uint8_t* kq, const uint16_t* ks, const uint16_t* kb,
+                       const uint8_t* vq, const uint16_t* vs, const uint16_t* vb, int n_keys,
+                       int head_dim, float* out) {
+  size_t n = (size_t)(n_keys > 0 ? n_keys : 1) * head_dim;
+  double* kd = (double*)malloc(sizeof(double) * n);
+  double* vd = (double*)malloc(sizeof(double) * n);
+  for (int t = 0; t < n_keys; ++t)
+    for (int d = 0; d < head_dim; ++d) {
+      kd[(size_t)t * head_dim + d] = kv8_value(kq, ks, kb, head_dim, t, d);
+      vd[(size_t)t * head_dim + d] = kv8_value(vq, vs, vb, head_dim, t, d);
+    }
+  attention_values(q, kd, vd, n_keys, head_dim, out);
+  free(kd);
+  free(vd);
 }
 
 double orc_silu(double z) { return z / (1.0 + exp(-z)); }
@@ -182,12 +251,30 @@ static size_t kv_index(const orc_config* c, int cap, int layer, int kvh, int pos
   return ((((size_t)layer * c->n_kv_heads + kvh) * cap) + pos) * (size_t)c->head_dim;
 }
 
+/* quantise the K and V rows at (layer, kv head, position) of an 8-bit cache */
+static void kv8_store(const orc_config* c, orc_kv* C, int l, int g, int p) {
+  size_t at = kv_index(c, C->capacity, l, g, p), ga = at / 64;
+  orc_quantize_kv8(C->k + at, 1, c->head_dim, C->kq + at, C->ks + ga, C->kb + ga);
+  orc_quantize_kv8(C->v + at, 1, c->head_dim, C->vq + at, C->vs + ga, C->vb + ga);
+}
+
+int orc_kv8_convert(const orc_config* c, orc_kv* kv) {
+  if (!kv->kq || c->head_dim % 64 != 0) return ORC_EINVAL;
+  for (int l = 0; l < c->n_layers; ++l)
+    for (int g = 0; g < c->n_kv_heads; ++g)
+      for (int p = kv->qlen; p < kv->len; ++p) kv8_store(c, kv, l, g, p);
+  kv->qlen = kv->len;
+  return ORC_OK;
+}
+
 int orc_forward(const orc_model* m, orc_kv* kv, int n_kv, int n, const int* seq, const int* pos,
                 const int* tok, const int* want, float* logits) {
   const orc_config* c = &m->cfg;
   const int d = c->d_model, hd = c->head_dim, H = c->n_heads, Hkv = c->n_kv_heads;
   const int qd = H * hd, kvd = Hkv * hd, F = c->d_ff, V = c->vocab;
   if (n < 0 || H % Hkv != 0 || hd % 2 != 0) return ORC_EINVAL;
+  for (int s = 0; s < n_kv; ++s)
+    if (kv[s].kq && hd % 64 != 0) return ORC_EINVAL;
   /* each sequence's tokens: consecutive positions from its current length, inside capacity */
   int* next = (int*)malloc(sizeof(int) * (size_t)(n_kv > 0 ? n_kv : 1));
   for (int s = 0; s < n_kv; ++s) next[s] = kv[s].len;
@@ -200,6 +287,9 @@ int orc_forward(const orc_model* m, orc_kv* kv, int n_kv, int n, const int* seq,
     }
     next[s]++;
   }
+  /* 8-bit caches that already hold codes quantise what this call appends and read codes */
+  int* quant = (int*)malloc(sizeof(int) * (size_t)(n_kv > 0 ? n_kv : 1));
+  for (int s = 0; s < n_kv; ++s) quant[s] = kv[s].kq != NULL && kv[s].qlen > 0;
   float* x = (float*)malloc(sizeof(float) * (size_t)n * d);
   float* h = (float*)malloc(sizeof(float) * (size_t)n * d);
   float* q = (float*)malloc(sizeof(float) * (size_t)n * qd);
@@ -236,13 +326,20 @@ int orc_forward(const orc_model* m, orc_kv* kv, int n_kv, int n, const int* seq,
           C->k[at + e] = orc_f32_to_bf16(kk[e]);
           C->v[at + e] = orc_f32_to_bf16(vv[e]);
         }
+        if (quant[seq[i]]) kv8_store(c, C, l, g, p);
       }
+      const int qm = quant[seq[i]];
 #pragma omp parallel for schedule(static)
       for (int j = 0; j < H; ++j) {
         int g = j / (H / Hkv);
         size_t base = kv_index(c, C->capacity, l, g, 0);
-        orc_attention(q + (size_t)i * qd + (size_t)j * hd, C->k + base, C->v + base, p + 1, hd,
-                      o + (size_t)i * qd + (size_t)j * hd);
+        if (qm)
+          orc_attention_kv8(q + (size_t)i * qd + (size_t)j * hd, C->kq + base, C->ks + base / 64,
+                            C->kb + base / 64, C->vq + base, C->vs + base / 64, C->vb + base / 64,
+                            p + 1, hd, o + (size_t)i * qd + (size_t)j * hd);
+        else
+          orc_attention(q + (size_t)i * qd + (size_t)j * hd, C->k + base, C->v + base, p + 1, hd,
+                        o + (size_t)i * qd + (size_t)j * hd);
       }
     }
     orc_linear_apply(c, &L->wo, d, qd, o, n, a);
@@ -255,7 +352,14 @@ int orc_forward(const orc_model* m, orc_kv* kv, int n_kv, int n, const int* seq,
     orc_linear_apply(c, &L->wd, d, F, gt, n, a);
     for (size_t t = 0; t < (size_t)n * d; ++t) x[t] = x[t] + a[t];
   }
-  for (int s = 0; s < n_kv; ++s) kv[s].len = next[s];
+  for (int s = 0; s < n_kv; ++s) {
+    kv[s].len = next[s];
+    /* a first call ran on bf16 K/V: its positions are converted now; later calls quantised
+     * their positions as they appended them */
+    if (kv[s].kq && quant[s]) kv[s].qlen = kv[s].len;
+    else if (kv[s].kq && kv[s].len > 0) orc_kv8_convert(c, &kv[s]);
+  }
+  free(quant);
 
   /* final norm + lm_head for the wanted tokens only (slice before the head) */
   int nw = 0;

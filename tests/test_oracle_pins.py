@@ -395,3 +395,130 @@ def test_synth_deterministic_and_normal():
     k1 = synth.kv(0, 0, 2, 4, 9, 64, 0, 0.32)
     k2 = synth.kv(0, 0, 2, 4, 5, 64, 0, 0.32)
     assert np.array_equal(k1[:, :, :5], k2)  # KV draws do not depend on the context length
+
+
+# ---- 8-bit affine KV -------------------------------------------------------------------
+def _bf16_bits(x):
+    """Exact bf16 bit patterns of values that bf16 holds exactly (checked)."""
+    f = np.asarray(x, dtype=np.float32)
+    bits = (f.view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal((bits.astype(np.uint32) << 16).view(np.float32), f)
+    return bits
+
+
+def test_kv8_hand_example():
+    """Groups whose values lie on an exact grid quantise losslessly: a group spanning
+    [0, 255/8] has scale 1/8 and bias 0, one spanning [-4, -4 + 255/32] scale 1/32 and bias -4,
+    and every code is the grid index.  A value halfway between two steps rounds to the even
+    code; a constant group has scale 0, bias equal to the value and all codes 0."""
+    rng = np.random.default_rng(3)
+    qa = rng.integers(0, 256, 64)
+    qa[5], qa[40] = 0, 255
+    qb = rng.integers(0, 256, 64)
+    qb[0], qb[63] = 255, 0
+    row0 = np.concatenate([qa / 8.0, -4.0 + qb / 32.0])
+    ties = np.zeros(64)
+    ties[1], ties[2], ties[3] = 255 / 8.0, 1.5 / 8.0, 2.5 / 8.0    # steps 1.5 -> 2, 2.5 -> 2
+    row1 = np.concatenate([ties, np.full(64, 1.5)])
+    codes, scales, biases = oracle.quantize_kv8(_bf16_bits(np.stack([row0, row1])))
+    assert list(codes[0, :64]) == list(qa) and list(codes[0, 64:]) == list(qb)
+    assert list(scales[0]) == list(_bf16_bits([1 / 8.0, 1 / 32.0]))
+    assert list(biases[0]) == list(_bf16_bits([0.0, -4.0]))
+    assert codes[1, 1] == 255 and codes[1, 2] == 2 and codes[1, 3] == 2 and codes[1, 0] == 0
+    assert scales[1, 1] == 0 and biases[1, 1] == _bf16_bits([1.5])[0]
+    assert not codes[1, 64:].any()
+
+
+def test_kv8_round_trip_bound():
+    """Random rows: every value read back is within half a step of the original, plus what
+    the bf16 rounding of the scale and bias can add over 255 steps."""
+    rng = np.random.default_rng(4)
+    x = _bf16_bits(oracle_f32_from_bits(oracle.bf16_round(rng.normal(0, 1.3, (40, 128)))))
+    codes, scales, biases = oracle.quantize_kv8(x)
+    xf = oracle_f32_from_bits(x).astype(np.float64).reshape(40, 2, 64)
+    sc = oracle_f32_from_bits(scales).astype(np.float64)[..., None]
+    bi = oracle_f32_from_bits(biases).astype(np.float64)[..., None]
+    back = sc * codes.reshape(40, 2, 64) + bi
+    mn, mx = xf.min(-1, keepdims=True), xf.max(-1, keepdims=True)
+    slack = np.abs(bi - mn) + 255 * np.abs(sc - (mx - mn) / 255)
+    assert np.all(np.abs(back - xf) <= sc / 2 + slack + 1e-12)
+    assert codes.min() == 0 and codes.max() == 255
+
+
+def oracle_f32_from_bits(bits):
+    return (np.asarray(bits, dtype=np.uint32) << 16).view(np.float32)
+
+
+def _grid_kv(rng, n, hd):
+    """bf16 rows whose groups of 64 are exact grids (lossless under 8-bit quantisation)."""
+    q = rng.integers(0, 256, (n, hd // 64, 64))
+    q[:, :, 0], q[:, :, 1] = 0, 255
+    step = 2.0 ** rng.integers(-9, -5, (n, hd // 64, 1))
+    return _bf16_bits(((q - 128) * step).reshape(n, hd))
+
+
+def test_kv8_attention_over_lossless_codes_equals_bf16():
+    rng = np.random.default_rng(5)
+    for n, hd in ((1, 64), (37, 128)):
+        k, v = _grid_kv(rng, n, hd), _grid_kv(rng, n, hd)
+        q = rng.normal(0, 1, hd).astype(np.float32)
+        got = oracle.attention_kv8(q, oracle.quantize_kv8(k), oracle.quantize_kv8(v))
+        np.testing.assert_array_equal(got, oracle.attention(q, k, v))
+
+
+KV8_SHAPE = ModelShape("kv8-pin", 2, 256, 4, 2, 128, 512, 512, 1e-5, 1e4, gain_sigma=0.1)
+
+
+def test_kv8_cache_conversion_points():
+    """An 8-bit cache's first call (the prompt) runs on bf16 K/V -- its logits equal the bf16
+    cache's bit for bit -- and is then converted; a decode step quantises the position it
+    appends and reads every position through its codes, so its logits move off the bf16
+    cache's by no more than the quantisation error allows, and each position's codes are the
+    quantiser's output for that position's bf16 row."""
+    m = oracle.OracleModel(KV8_SHAPE)
+    rng = np.random.default_rng(6)
+    toks = rng.integers(0, KV8_SHAPE.vocab, 21).astype(np.int32)
+    c8, c16 = oracle.KVCache(KV8_SHAPE, 32, kv_bits=8), oracle.KVCache(KV8_SHAPE, 32)
+    l8 = oracle.prefill_segmented(m, [c8], [20], toks[:20])
+    l16 = oracle.prefill_segmented(m, [c16], [20], toks[:20])
+    np.testing.assert_array_equal(l8, l16)
+    assert c8.qlen == 20 and np.array_equal(c8.k, c16.k) and np.array_equal(c8.v, c16.v)
+    d8 = oracle.decode_step_batch(m, [c8], toks[20:21])
+    d16 = oracle.decode_step_batch(m, [c16], toks[20:21])
+    assert c8.qlen == 21
+    assert 0 < np.abs(d8 - d16).max() < 5e-2
+    hd = KV8_SHAPE.head_dim
+    for name, src in (("k", c8.k), ("v", c8.v)):
+        rows = src[:, :, :21, :].reshape(-1, hd)
+        codes, scales, biases = oracle.quantize_kv8(rows)
+        np.testing.assert_array_equal(c8.q8[name + "q"][:, :, :21, :].reshape(-1, hd), codes)
+        np.testing.assert_array_equal(c8.q8[name + "s"][:, :, :21, :].reshape(-1, hd // 64), scales)
+        np.testing.assert_array_equal(c8.q8[name + "b"][:, :, :21, :].reshape(-1, hd // 64), biases)
+
+
+def test_kv8_decode_over_a_lossless_prefix():
+    """A cache whose prompt K/V are exact grids loses nothing in its conversion; a decode step
+    over it differs from the bf16 cache's only through the appended position's rounding, and
+    planting a different code at one prompt position changes the result."""
+    m = oracle.OracleModel(KV8_SHAPE)
+    rng = np.random.default_rng(7)
+    s = KV8_SHAPE
+    c8, c16 = oracle.KVCache(s, 16, kv_bits=8), oracle.KVCache(s, 16)
+    for c in (c8, c16):
+        r = np.random.default_rng(8)
+        for arr in (c.k, c.v):
+            arr[:, :, :12, :] = _grid_kv(r, s.n_layers * s.n_kv_heads * 12, s.head_dim).reshape(
+                s.n_layers, s.n_kv_heads, 12, s.head_dim)
+        c.len = 12
+    c8.convert()
+    tok = rng.integers(0, s.vocab, 1).astype(np.int32)
+    d8 = oracle.decode_step_batch(m, [c8], tok)
+    d16 = oracle.decode_step_batch(m, [c16], tok)
+    assert np.abs(d8 - d16).max() < 5e-2
+    c8b = oracle.KVCache(s, 16, kv_bits=8)
+    c8b.k[:], c8b.v[:] = c8.k, c8.v
+    c8b.len = 12
+    c8b.convert()
+    c8b.q8["kq"][1, 0, 3, 7] ^= 0x40
+    c8b.len, c8b.qlen = 12, 12
+    assert not np.array_equal(oracle.decode_step_batch(m, [c8b], tok), d8)
