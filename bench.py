@@ -80,10 +80,11 @@ def _workload_by_name(name: str):
     raise SystemExit(f"unknown workload {name}")
 
 
-def step_bytes(shape, ctx_lens) -> float:
+def step_bytes(shape, ctx_lens, kv_bits: int = 16) -> float:
     """Algorithmic HBM bytes of one decode step: every linear weight once, each row's live KV
-    (positions 0..t_b after the append) once, the appended K/V, the logits written."""
-    kv_tok = shape.kv_bytes_per_token()
+    (positions 0..t_b after the append) once, the appended K/V, the logits written.  8-bit KV:
+    a code per element plus a bf16 scale and bias per 64 elements."""
+    kv_tok = shape.kv_bytes_per_token() * (1.0625 / 2 if kv_bits == 8 else 1.0)
     return float(shape.weight_bytes_per_step() + sum((int(c) + 1) * kv_tok for c in ctx_lens)
                  + len(ctx_lens) * (kv_tok + 4 * shape.vocab))
 
@@ -136,9 +137,10 @@ class ClockSampler:
 
 
 # ---- the GPU arm ------------------------------------------------------------------------------
-def setup_decode(wl, device, extra_positions: int, page_tokens: int = 0):
+def setup_decode(wl, device, extra_positions: int, page_tokens: int = 0, kv_bits: int = 16):
     """Engine + slabs for a decode workload: synthetic KV of each row loaded into its slab,
-    each row's next token ready on the device.  page_tokens > 0: a paged engine."""
+    each row's next token ready on the device.  page_tokens > 0: a paged engine; kv_bits = 8:
+    8-bit KV (the arena also holds the decode rows' staging and one import's bf16 slab)."""
     import numpy as np
     import torch
 
@@ -151,10 +153,13 @@ def setup_decode(wl, device, extra_positions: int, page_tokens: int = 0):
     w = DeviceWeights(shape, device)
     if page_tokens:
         arena = sum(B.slab_bytes(w.cfg, page_tokens) * (-(-c // page_tokens)) for c in caps)
+    elif kv_bits == 8:
+        arena = (sum(B.slab_bytes_kv8(w.cfg, c) for c in caps) + B.slab_bytes(w.cfg, max(ctx))
+                 + len(ctx) * B.slab_bytes(w.cfg, 128))
     else:
         arena = sum(B.slab_bytes(w.cfg, c) for c in caps)
     eng = Engine(w, arena_bytes=arena, max_batch=len(ctx), max_prefill_tokens=len(ctx),
-                 page_tokens=page_tokens)
+                 page_tokens=page_tokens, kv_bits=kv_bits)
     slabs = []
     for r, (c, cap) in enumerate(zip(ctx, caps)):
         s = eng.kv_slab_alloc(cap)
@@ -200,7 +205,7 @@ def gpu_arm(args, rank: int, world: int):
     wl = workload_by_name(args.workload, args.layers)
     K, W = args.steps, args.warmup
     w, eng, slabs, ctx, tok0 = setup_decode(wl, device, extra_positions=3 * (K + W) + 8,
-                                            page_tokens=args.page_tokens)
+                                            page_tokens=args.page_tokens, kv_bits=args.kv_bits)
     Bsz = len(slabs)
     V = wl.shape.vocab
     stream = eng.stream
@@ -284,7 +289,7 @@ def gpu_arm(args, rank: int, world: int):
         hbm_peak = peaks["hbm_gbs"] if peaks else 6800.0
         peak_src = "of measured" if peaks else "of fallback"
         ctx_mean = [c + W + K / 2.0 for c in ctx]  # mean live context over the timed steps
-        sb = step_bytes(wl.shape, ctx_mean)
+        sb = step_bytes(wl.shape, ctx_mean, args.kv_bits)
         step_s = ms_max / K / 1e3
         achieved = proj_bytes / (proj_ms / 1e3) / 1e9 if proj_ms > 0 else None
         attn_gbs = attn_bytes / (attn_ms / 1e3) / 1e9 if attn_ms > 0 else None
@@ -305,10 +310,11 @@ def gpu_arm(args, rank: int, world: int):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "bf16" if wl.shape.weight_format == "bf16" else "affine4-w/bf16",
+            "dtype": ("bf16" if wl.shape.weight_format == "bf16" else "affine4-w/bf16")
+                     + ("/kv-affine8" if args.kv_bits == 8 else ""),
             "data": "synthetic (seeded N(0,0.02) weights, seeded KV slabs and tokens)",
             "config": {"workload": wl.name, "model": wl.shape.name, "batch_per_gpu": Bsz,
-                       "kv_page_tokens": args.page_tokens,
+                       "kv_page_tokens": args.page_tokens, "kv_bits": args.kv_bits,
                        "ctx_lengths": ctx, "parallelism": f"replicas x{world}" if world > 1 else "1 gpu",
                        "l2": "inputs larger than L2 (weights alone are %.1f GB per step)"
                              % (wl.shape.weight_bytes_per_step() / 1e9)},
@@ -478,6 +484,8 @@ def main():
     ap.add_argument("--workload", default="7b-bf16-b8")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--reference-budget", type=float, default=60.0)
+    ap.add_argument("--kv-bits", type=int, default=16, choices=(8, 16),
+                    help="KV precision: 16 (bf16) or 8 (8-bit affine, groups of 64)")
     ap.add_argument("--page-tokens", type=int, default=0,
                     help="paged KV with pages of this many positions (a multiple of 128)")
     ap.add_argument("--layers", type=int, default=None,

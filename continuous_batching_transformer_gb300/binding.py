@@ -33,7 +33,7 @@ EXPORTS = ["cbt_status_str", "cbt_engine_create", "cbt_engine_destroy", "cbt_sla
            "cbt_decode_step_batch", "cbt_last_device_error", "cbt_engine_stats",
            "cbt_kernel_launches", "cbt_quantize_affine4", "cbt_engine_set_timing",
            "cbt_engine_timing", "cbt_greedy_head_noalloc", "cbt_kv_slab_copy_prefix",
-           "cbt_kv_slab_share_prefix"]
+           "cbt_kv_slab_share_prefix", "cbt_slab_bytes_kv8", "cbt_quantize_kv8"]
 KCLASS_PROJ, KCLASS_ATTN, KCLASS_OTHER = 0, 1, 2
 
 
@@ -67,7 +67,7 @@ class Weights(ctypes.Structure):
 class EngineParams(ctypes.Structure):
     _fields_ = [("kv_arena", c_void), ("kv_arena_bytes", ctypes.c_size_t),
                 ("max_batch", c_int32), ("max_prefill_tokens", c_int32), ("stream", c_void),
-                ("kv_page_tokens", c_int32)]
+                ("kv_page_tokens", c_int32), ("kv_bits", c_int32)]
 
 
 class Stats(ctypes.Structure):
@@ -98,6 +98,9 @@ def lib():
         L.cbt_engine_destroy.argtypes = [c_void]
         L.cbt_slab_bytes.argtypes = [P(ModelConfig), c_int32]
         L.cbt_slab_bytes.restype = ctypes.c_size_t
+        L.cbt_slab_bytes_kv8.argtypes = [P(ModelConfig), c_int32]
+        L.cbt_slab_bytes_kv8.restype = ctypes.c_size_t
+        L.cbt_quantize_kv8.argtypes = [c_void, c_int32, c_int32, c_void, c_void, c_void, c_void]
         L.cbt_kv_slab_alloc.argtypes = [c_void, c_int32, P(c_int32)]
         L.cbt_kv_slab_free.argtypes = [c_void, c_int32]
         L.cbt_retire.argtypes = [c_void, c_void, c_int32]
@@ -121,7 +124,8 @@ def lib():
         L.cbt_engine_timing.argtypes = [c_void, c_int32, P(ctypes.c_double), P(ctypes.c_int64),
                                         P(ctypes.c_double)]
         for name in EXPORTS:
-            if name not in ("cbt_status_str", "cbt_slab_bytes", "cbt_kernel_launches"):
+            if name not in ("cbt_status_str", "cbt_slab_bytes", "cbt_slab_bytes_kv8",
+                            "cbt_kernel_launches"):
                 getattr(L, name).restype = c_int32
         _lib = L
     return _lib
@@ -155,6 +159,16 @@ def engine_destroy(e: int) -> None:
 
 def slab_bytes(cfg: ModelConfig, capacity: int) -> int:
     return lib().cbt_slab_bytes(ctypes.byref(cfg), capacity)
+
+
+def slab_bytes_kv8(cfg: ModelConfig, capacity: int) -> int:
+    return lib().cbt_slab_bytes_kv8(ctypes.byref(cfg), capacity)
+
+
+def quantize_kv8(x_ptr: int, rows: int, cols: int, codes_ptr: int, scales_ptr: int,
+                 biases_ptr: int, stream: int = 0) -> None:
+    _check(lib().cbt_quantize_kv8(x_ptr, rows, cols, codes_ptr, scales_ptr, biases_ptr, stream),
+           "cbt_quantize_kv8")
 
 
 def kv_slab_alloc(e: int, capacity: int) -> int:

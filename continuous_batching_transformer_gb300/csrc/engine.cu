@@ -62,6 +62,13 @@ struct cbt_engine {
   int page = 0;            // kv_page_tokens: positions per page (0: contiguous slabs)
   size_t page_bytes = 0;
   std::unordered_map<size_t, int> extra_holders;  // shared pages: holders beyond the first
+  // 8-bit KV (kv_bits = 8): slabs hold codes; each decode row's new K/V is written in bf16 to
+  // its own one-page staging slab (stage_off + b * stage_bytes) and quantised from there; the
+  // per-call conversion records (decode rows, prefill segments, an import) on the device
+  int kv_bits = 16;
+  size_t stage_off = 0, stage_bytes = 0;
+  Kv8Job* kv8_jobs = nullptr;
+  std::vector<Kv8Job> hjobs;
   // per prefill call: the page bases (QueryRow bases) of every paged segment, and each
   // token's offset into them (read by the prefill attention kernels)
   std::vector<long long> hpagetab;
@@ -180,7 +187,7 @@ static void free_scratch(cbt_engine* e) {
                   e->rows,    e->err,      e->act_h, e->act_o, e->act_u,  e->tc_part,
                   e->tc_cnt,  e->items,    e->item_meta, e->att_o, e->att_ml, e->stage,
                   e->qtile,   e->ss,       e->qb,     e->pf_units, e->q4_arena, e->pagetab,
-                  e->tok_pages};
+                  e->tok_pages, e->kv8_jobs};
   for (void* q : ptrs)
     if (q) cudaFree(q);
 }
@@ -198,6 +205,19 @@ extern "C" size_t cbt_slab_bytes(const cbt_model_config* c, int32_t cap) {
   if (!c || cap <= 0) return 0;
   size_t b = (size_t)c->n_layers * 2 * c->n_kv_heads * (size_t)round_cap(cap) * c->head_dim * 2;
   return (b + kSlabAlign - 1) & ~(kSlabAlign - 1);
+}
+
+extern "C" size_t cbt_slab_bytes_kv8(const cbt_model_config* c, int32_t cap) {
+  if (!c || cap <= 0 || c->head_dim % 64) return 0;
+  size_t b = (size_t)c->n_layers * 2 * c->n_kv_heads * (size_t)kv8_block_bytes(round_cap(cap), c->head_dim);
+  return (b + kSlabAlign - 1) & ~(kSlabAlign - 1);
+}
+
+static bool take_extent(cbt_engine* e, size_t need, size_t* off_out);
+
+// bytes of one of the engine's slabs
+static size_t slab_bytes(const cbt_engine* e, int cap) {
+  return e->kv_bits == 8 ? cbt_slab_bytes_kv8(&e->cfg, cap) : cbt_slab_bytes(&e->cfg, cap);
 }
 
 extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_weights* w,
@@ -218,8 +238,9 @@ extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_w
   if (c.d_model % 256 || qd % 256 || c.d_ff % 256) return CBT_ERR_UNSUPPORTED;
   if (p->max_batch <= 0 || p->max_prefill_tokens <= 0 || p->kv_arena_bytes < kSlabAlign ||
       (reinterpret_cast<uintptr_t>(p->kv_arena) & 255) || p->kv_page_tokens < 0 ||
-      p->kv_page_tokens % 128)
+      p->kv_page_tokens % 128 || (p->kv_bits != 0 && p->kv_bits != 16 && p->kv_bits != 8))
     return CBT_ERR_INVALID;
+  if (p->kv_bits == 8 && p->kv_page_tokens) return CBT_ERR_UNSUPPORTED;
   if (!linear_ok(w->lm_head, c.weight_format)) return CBT_ERR_NULL;
   for (int l = 0; l < c.n_layers; ++l) {
     const cbt_layer_weights& L = w->layers[l];
@@ -240,6 +261,16 @@ extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_w
   e->free_ext[0] = p->kv_arena_bytes & ~(kSlabAlign - 1);
   e->page = p->kv_page_tokens;
   e->page_bytes = e->page ? cbt_slab_bytes(&c, e->page) : 0;
+  e->kv_bits = p->kv_bits == 8 ? 8 : 16;
+  if (e->kv_bits == 8) {  // the decode rows' staging slabs, one 128-position page each
+    e->stage_bytes = cbt_slab_bytes(&c, 128);
+    size_t off = 0;
+    if (!take_extent(e, (size_t)p->max_batch * e->stage_bytes, &off)) {
+      delete e;
+      return CBT_ERR_POOL_EXHAUSTED;
+    }
+    e->stage_off = off;
+  }
 
   const int T = std::max(p->max_batch, p->max_prefill_tokens);
   e->tmax = T;
@@ -269,6 +300,7 @@ extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_w
   chk(dmalloc(&e->last_idx, (size_t)p->max_batch, &tot));
   chk(dmalloc(&e->rows, (size_t)T, &tot));
   chk(dmalloc(&e->err, 2, &tot));
+  if (e->kv_bits == 8) chk(dmalloc(&e->kv8_jobs, (size_t)p->max_batch, &tot));
   if (rc == cudaSuccess) rc = cudaMemsetAsync(e->err, 0, 2 * sizeof(int), e->stream);
   bool maps_ok = true;
   const bool bf16w = c.weight_format == CBT_WEIGHTS_BF16;
@@ -372,6 +404,7 @@ extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_w
     e->use_tc = maps_ok && c.d_ff % 64 == 0;
   }
   if (rc == cudaSuccess) rc = cudaStreamSynchronize(e->stream);
+  if (rc == cudaSuccess && maps_ok && e->kv_bits == 8 && !e->use_tc) maps_ok = false;
   if (rc != cudaSuccess || !maps_ok) {
     free_scratch(e);
     delete e;
@@ -503,7 +536,7 @@ extern "C" cbt_status cbt_kv_slab_alloc(cbt_engine* e, int32_t cap, int32_t* id)
     *id = sid;
     return CBT_OK;
   }
-  size_t need = cbt_slab_bytes(&e->cfg, cap), off;
+  size_t need = slab_bytes(e, cap), off;
   if (!take_extent(e, need, &off)) return CBT_ERR_POOL_EXHAUSTED;
   int sid = e->next_id++;
   e->slabs[sid] = Slab{off, need, cap, 0, round_cap(cap), {}};
@@ -565,9 +598,70 @@ extern "C" cbt_status cbt_kv_slab_position(cbt_engine* e, int32_t id, int32_t* p
   return CBT_OK;
 }
 
+// ---- 8-bit KV: bf16 intermediates and their conversion ---------------------------------------
+// A bf16 slab of capacity cap for a call's intermediate K/V (0 if the arena has no room).
+static int temp_bf16_slab(cbt_engine* e, int cap) {
+  const size_t need = cbt_slab_bytes(&e->cfg, cap);
+  size_t off = 0;
+  if (!take_extent(e, need, &off)) return 0;
+  const int sid = e->next_id++;
+  e->slabs[sid] = Slab{off, need, cap, 0, round_cap(cap), {}};
+  return sid;
+}
+
+// Host bookkeeping only: work queued later on the stream runs after what used the slab.
+static void drop_temp(cbt_engine* e, int sid) {
+  auto it = e->slabs.find(sid);
+  give_extent(e, it->second.offset, it->second.bytes);
+  e->slabs.erase(it);
+}
+
+// Queue the quantisation of e->hjobs (every layer) into their 8-bit slabs.
+static cudaError_t convert_jobs(cbt_engine* e) {
+  int max_n = 0;
+  for (const Kv8Job& j : e->hjobs) max_n = std::max(max_n, j.n);
+  cudaError_t rc = cudaMemcpyAsync(e->kv8_jobs, e->hjobs.data(), sizeof(Kv8Job) * e->hjobs.size(),
+                                   cudaMemcpyHostToDevice, e->stream);
+  if (rc != cudaSuccess) return rc;
+  launch_kv8_convert(e->kv8_jobs, (int)e->hjobs.size(), max_n, 0, e->cfg.n_layers,
+                     e->cfg.n_kv_heads, e->cfg.head_dim, static_cast<uint8_t*>(e->p.kv_arena),
+                     e->stream);
+  return cudaGetLastError();
+}
+
+static cbt_status slab_copy_bf16(cbt_engine* e, int32_t id, void* k, void* v, int32_t n,
+                                 int32_t on_host, bool to_slab);
+
+// Import into an 8-bit slab: the plain K/V go to a bf16 intermediate slab, which is quantised.
 static cbt_status slab_copy(cbt_engine* e, int32_t id, void* k, void* v, int32_t n, int32_t on_host,
                             bool to_slab) {
   if (!e || !k || !v) return CBT_ERR_NULL;
+  if (e->kv_bits != 8) return slab_copy_bf16(e, id, k, v, n, on_host, to_slab);
+  auto it = e->slabs.find(id);
+  if (it == e->slabs.end()) return CBT_ERR_BAD_SLAB;
+  if (!to_slab) return CBT_ERR_UNSUPPORTED;
+  if (n < 0) return CBT_ERR_INVALID;
+  if (n > it->second.cap) return CBT_ERR_CAPACITY;
+  if (n == 0) {
+    it->second.pos = 0;
+    return CBT_OK;
+  }
+  const int tmp = temp_bf16_slab(e, n);
+  if (!tmp) return CBT_ERR_POOL_EXHAUSTED;
+  cbt_status st = slab_copy_bf16(e, tmp, k, v, n, on_host, true);
+  if (st == CBT_OK) {
+    const Slab& t = e->slabs[tmp];
+    Slab& d = e->slabs[id];
+    e->hjobs.assign(1, Kv8Job{(long long)(t.offset / 2), t.lcap, 0, n, d.lcap, (long long)d.offset});
+    if (convert_jobs(e) != cudaSuccess) st = CBT_ERR_CUDA;
+  }
+  drop_temp(e, tmp);
+  if (st == CBT_OK) e->slabs[id].pos = n;
+  return st;
+}
+
+static cbt_status slab_copy_bf16(cbt_engine* e, int32_t id, void* k, void* v, int32_t n,
+                                 int32_t on_host, bool to_slab) {
   auto it = e->slabs.find(id);
   if (it == e->slabs.end()) return CBT_ERR_BAD_SLAB;
   Slab& s = it->second;
@@ -640,6 +734,7 @@ extern "C" cbt_status cbt_kv_slab_export(cbt_engine* e, int32_t id, void* k, voi
 extern "C" cbt_status cbt_kv_slab_copy_prefix(cbt_engine* e, int32_t src_id, int32_t dst_id,
                                               int32_t n) {
   if (!e) return CBT_ERR_NULL;
+  if (e->kv_bits == 8) return CBT_ERR_UNSUPPORTED;
   auto si = e->slabs.find(src_id), di = e->slabs.find(dst_id);
   if (si == e->slabs.end() || di == e->slabs.end()) return CBT_ERR_BAD_SLAB;
   if (src_id == dst_id || n < 0) return CBT_ERR_INVALID;
@@ -871,14 +966,16 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
   cudaStream_t s = e->stream;
   const int d = c.d_model, qd = e->qd(), kvd = e->kvd(), F = c.d_ff;
   uint16_t* arena = static_cast<uint16_t*>(e->p.kv_arena);
-  const double attn_bytes = 2.0 * 2.0 * kvd * (double)total_keys  // K and V read (bf16)
+  const bool kv8 = e->kv_bits == 8;
+  // K and V read per key: bf16, or 8-bit codes plus a bf16 scale and bias per 64
+  const double attn_bytes = 2.0 * (kv8 ? 1.0625 : 2.0) * kvd * (double)total_keys
                             + 4.0 * n * (qd + 2 * kvd)              // q, k, v in
                             + 2.0 * 2.0 * n * kvd + 4.0 * n * qd;   // K/V appended, o out
   // 4-bit weights go through the tensor cores for up to 32 rows (the decode projections)
   const bool tcp = e->use_tc && (e->cfg.weight_format == CBT_WEIGHTS_BF16 || n <= 32);
   // decode on the tensor cores folds every RMSNorm into the projection that consumes it:
   // the residual-add epilogues and the embedding leave per-tile sums of squares in e->ss
-  const bool fused = tcp && !gather && n <= 32;
+  const bool fused = tcp && !gather && n <= 32 && !kv8;
   const int lo = tc_lo_rows(e, n), lo_out = tc_lo_rows(e, n_out);
   bool ok = true;
   int t = tbegin(e, CBT_KCLASS_OTHER);
@@ -910,9 +1007,33 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
     const bool tc_prefill = tcp && gather && e->pf_n > 0;
     if (!fused)
       launch_rope_append(e->qkv, e->rows, n, l, c.n_heads, c.n_kv_heads, c.head_dim, e->cosv,
-                         e->sinv, arena, (tcp && !gather) ? e->qtile : nullptr,
+                         e->sinv, arena, (tcp && !gather && !kv8) ? e->qtile : nullptr,
                          tc_prefill ? e->qb : nullptr, e->qb_rows, s);
-    if (tcp && !gather) {  // decode: split-K flash decoding on the tensor cores
+    if (kv8 && !gather) {
+      // 8-bit KV decode: the RoPE kernel above put each row's new K/V in its staging page;
+      // quantise them into the row's slab, then split attention over the codes
+      launch_kv8_convert(e->kv8_jobs, n, 1, l, 1, c.n_kv_heads, c.head_dim,
+                         static_cast<uint8_t*>(e->p.kv_arena), s);
+      Kv8AttnArgs a{};
+      a.qkv = e->qkv;
+      a.rows = e->kv8_jobs;
+      a.items = e->items;
+      a.n_items = e->item_meta + 2 * e->p.max_batch;
+      a.item_base = e->item_meta;
+      a.item_count = e->item_meta + e->p.max_batch;
+      a.arena = static_cast<const uint8_t*>(e->p.kv_arena);
+      a.B = n;
+      a.layer = l;
+      a.n_heads = c.n_heads;
+      a.n_kv_heads = c.n_kv_heads;
+      a.head_dim = c.head_dim;
+      a.part_o = e->att_o;
+      a.part_ml = e->att_ml;
+      a.o = e->o;
+      a.err = e->err;
+      ok &= launch_attn_decode_kv8(a, e->num_sms, s);
+      if (tcp) launch_f32_to_act(e->o, n, qd, e->act_o, lo, s);
+    } else if (tcp && !gather) {  // decode: split-K flash decoding on the tensor cores
       AttnDecodeArgs a{};
       a.qtile = e->qtile;
       a.rows = e->rows;
@@ -1113,15 +1234,28 @@ extern "C" cbt_status cbt_decode_step_batch(cbt_engine* e, const int32_t* ids, i
   const cbt_status st = prepare_writes(e, writes);
   if (st != CBT_OK) return st;
   e->hslab.resize(B);
+  e->hjobs.clear();
   for (int b = 0; b < B; ++b) {
     const Slab& sl = e->slabs[ids[b]];
-    e->hrows[b] = QueryRow{row_base(e, sl, sl.pos), sl.pos, row_cap(e, sl)};
+    if (e->kv_bits == 8) {
+      // the new K/V go to row b's staging page (positions [s, s + 128) around pos), and from
+      // there into the 8-bit slab
+      const long long sb = (long long)((e->stage_off + (size_t)b * e->stage_bytes) / 2) -
+                           (long long)(sl.pos / 128) * 128 * e->cfg.head_dim;
+      e->hrows[b] = QueryRow{sb, sl.pos, 128};
+      e->hjobs.push_back(Kv8Job{sb, 128, sl.pos, 1, sl.lcap, (long long)sl.offset});
+    } else {
+      e->hrows[b] = QueryRow{row_base(e, sl, sl.pos), sl.pos, row_cap(e, sl)};
+    }
     e->hslab[b] = &sl;
     max_keys = std::max(max_keys, sl.pos + 1);
     total_keys += sl.pos + 1;
   }
   cudaError_t rc = cudaMemcpyAsync(e->rows, e->hrows.data(), sizeof(QueryRow) * B,
                                    cudaMemcpyHostToDevice, e->stream);
+  if (rc == cudaSuccess && e->kv_bits == 8)
+    rc = cudaMemcpyAsync(e->kv8_jobs, e->hjobs.data(), sizeof(Kv8Job) * B, cudaMemcpyHostToDevice,
+                         e->stream);
   if (rc == cudaSuccess && e->page) {  // for the CUDA-core attention (rows above its limits)
     e->hpagetab.clear();
     e->htok_pages.assign(B, -1);
@@ -1232,10 +1366,60 @@ static cudaError_t plan_prefill_attention(cbt_engine* e, const int32_t* ids, con
   return rc;
 }
 
+static cbt_status prefill_impl(cbt_engine* e, const int32_t* ids, const int32_t* lens, int32_t K,
+                               const int32_t* tokens, float* logits, int32_t* next_tokens);
+
+// 8-bit engines (the mlx-bun batching design's conversion point: a row prefills in bf16 and is
+// then converted): each segment is prefilled into a bf16 intermediate slab, then quantised
+// into its own slab.  Only fresh slabs (position 0).
+static cbt_status prefill_kv8(cbt_engine* e, const int32_t* ids, const int32_t* lens, int32_t K,
+                              const int32_t* tokens, float* logits, int32_t* next_tokens) {
+  if (K < 0) return CBT_ERR_INVALID;
+  if (K == 0) return CBT_OK;
+  if (!ids || !lens || !tokens) return CBT_ERR_NULL;
+  if (K > e->p.max_batch) return CBT_ERR_BATCH;
+  std::unordered_set<int> seen;
+  for (int s = 0; s < K; ++s) {
+    auto it = e->slabs.find(ids[s]);
+    if (it == e->slabs.end()) return CBT_ERR_BAD_SLAB;
+    if (!seen.insert(ids[s]).second) return CBT_ERR_DUP_SLAB;
+    if (lens[s] <= 0) return CBT_ERR_INVALID;
+    if ((long long)it->second.pos + lens[s] > it->second.cap) return CBT_ERR_CAPACITY;
+    if (it->second.pos != 0) return CBT_ERR_UNSUPPORTED;
+  }
+  std::vector<int32_t> tmp(K, 0);
+  cbt_status st = CBT_OK;
+  for (int s = 0; s < K && st == CBT_OK; ++s) {
+    tmp[s] = temp_bf16_slab(e, lens[s]);
+    if (!tmp[s]) st = CBT_ERR_POOL_EXHAUSTED;
+  }
+  if (st == CBT_OK) st = prefill_impl(e, tmp.data(), lens, K, tokens, logits, next_tokens);
+  if (st == CBT_OK) {
+    e->hjobs.clear();
+    for (int s = 0; s < K; ++s) {
+      const Slab& t = e->slabs[tmp[s]];
+      const Slab& d = e->slabs[ids[s]];
+      e->hjobs.push_back(Kv8Job{(long long)(t.offset / 2), t.lcap, 0, lens[s], d.lcap, (long long)d.offset});
+    }
+    if (convert_jobs(e) != cudaSuccess) st = CBT_ERR_CUDA;
+  }
+  for (int s = 0; s < K; ++s)
+    if (tmp[s]) drop_temp(e, tmp[s]);
+  if (st == CBT_OK)
+    for (int s = 0; s < K; ++s) e->slabs[ids[s]].pos = lens[s];
+  return st;
+}
+
 extern "C" cbt_status cbt_prefill_segmented(cbt_engine* e, const int32_t* ids,
                                             const int32_t* lens, int32_t K, const int32_t* tokens,
                                             float* logits, int32_t* next_tokens) {
   if (!e) return CBT_ERR_NULL;
+  if (e->kv_bits == 8) return prefill_kv8(e, ids, lens, K, tokens, logits, next_tokens);
+  return prefill_impl(e, ids, lens, K, tokens, logits, next_tokens);
+}
+
+static cbt_status prefill_impl(cbt_engine* e, const int32_t* ids, const int32_t* lens, int32_t K,
+                               const int32_t* tokens, float* logits, int32_t* next_tokens) {
   if (K < 0) return CBT_ERR_INVALID;
   if (K == 0) return CBT_OK;
   if (!ids || !lens || !tokens) return CBT_ERR_NULL;
@@ -1323,6 +1507,19 @@ extern "C" cbt_status cbt_engine_stats(cbt_engine* e, cbt_stats* out) {
 extern "C" int64_t cbt_kernel_launches(cbt_engine* e) {
   (void)e;
   return kernel_launch_count();
+}
+
+extern "C" cbt_status cbt_quantize_kv8(const void* x, int32_t rows, int32_t cols, void* codes,
+                                       void* scales, void* biases, void* stream) {
+  if (!x || !codes || !scales || !biases) return CBT_ERR_NULL;
+  if (rows < 0 || cols <= 0 || cols % 64 || (reinterpret_cast<uintptr_t>(x) & 3) ||
+      (reinterpret_cast<uintptr_t>(codes) & 1) || (reinterpret_cast<uintptr_t>(scales) & 1) ||
+      (reinterpret_cast<uintptr_t>(biases) & 1))
+    return CBT_ERR_INVALID;
+  launch_quantize_kv8(static_cast<const uint16_t*>(x), rows, cols, static_cast<uint8_t*>(codes),
+                      static_cast<uint16_t*>(scales), static_cast<uint16_t*>(biases),
+                      static_cast<cudaStream_t>(stream));
+  return cudaGetLastError() == cudaSuccess ? CBT_OK : CBT_ERR_CUDA;
 }
 
 extern "C" cbt_status cbt_quantize_affine4(const void* w, int32_t rows, int32_t cols, int32_t group,

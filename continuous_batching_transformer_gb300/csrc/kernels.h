@@ -148,6 +148,41 @@ struct AttnDecodeArgs {
 // tk: the KV arena as [rows][head_dim] bf16, box {64, 128}; tv: as [rows][64], box {64, head_dim}
 bool launch_attn_decode_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnDecodeArgs& a,
                            int num_sms, cudaStream_t s);
+// ---- 8-bit affine KV (kv8.cu) ------------------------------------------------------------------
+// An 8-bit slab block (layer, K|V, kv head) of capacity cap: codes [cap][head_dim] uint8, then
+// bf16 scales and bf16 biases [cap][head_dim / 64]
+CBT_HD long long kv8_block_bytes(int cap, int head_dim) {
+  return (long long)cap * (head_dim + head_dim / 16);
+}
+// Positions [t0, t0 + n) of a bf16 slab (or a staging page: a QueryRow base and capacity) to
+// be quantised into the 8-bit slab at byte offset dst (layout capacity dst_cap).  The decode
+// attention reads the same records as its rows: the 8-bit slab and t0 = the row's position.
+struct Kv8Job {
+  long long src_base;
+  int src_cap, t0, n, dst_cap;
+  long long dst;
+};
+void launch_quantize_kv8(const uint16_t* x, int rows, int cols, uint8_t* codes, uint16_t* scales,
+                         uint16_t* biases, cudaStream_t s);
+// jobs: device [n_jobs]; layers [l0, l0 + nl); max_n = most positions of a job
+void launch_kv8_convert(const Kv8Job* jobs, int n_jobs, int max_n, int l0, int nl, int n_kv_heads,
+                        int head_dim, uint8_t* arena, cudaStream_t s);
+struct Kv8AttnArgs {
+  const float* qkv;      // [B][q | k | v] fp32, q rotated (the RoPE kernel's output)
+  const Kv8Job* rows;    // [B]: each row's 8-bit slab and position
+  const AttnItem* items; // the decode work list (one 128-key sub-chunk per item)
+  const int* n_items;
+  const int* item_base;  // [B]
+  const int* item_count; // [B]
+  const uint8_t* arena;
+  int B, layer, n_heads, n_kv_heads, head_dim;
+  float* part_o;         // [n_items][G][head_dim]
+  float2* part_ml;       // [n_items][G]
+  float* o;              // [B][n_heads * head_dim], softmax(q.K^T / sqrt(hd)) V per q head
+  int* err;
+};
+bool launch_attn_decode_kv8(const Kv8AttnArgs& a, int num_sms, cudaStream_t s);
+
 // V of one layer between a plain [kv head][plain_n positions][head_dim] buffer and a slab (or
 // page): positions [t0, t0 + n)
 void launch_v_convert(uint16_t* plain, uint16_t* arena, const QueryRow& r, int layer,

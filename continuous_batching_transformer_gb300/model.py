@@ -92,16 +92,17 @@ class Engine:
 
     def __init__(self, weights: DeviceWeights, arena_bytes: int, max_batch: int,
                  max_prefill_tokens: int, stream: torch.cuda.Stream | None = None,
-                 page_tokens: int = 0):
+                 page_tokens: int = 0, kv_bits: int = 16):
         """page_tokens > 0 (a multiple of 128): paged KV, slabs take pages of that many
-        positions from the arena as they grow."""
+        positions from the arena as they grow.  kv_bits = 8: 8-bit affine KV."""
         self.weights = weights
         self.shape = weights.shape
         self.arena = torch.empty(arena_bytes, dtype=torch.uint8, device=weights.device)
         self.stream = stream or torch.cuda.current_stream(weights.device)
         params = B.EngineParams(self.arena.data_ptr(), arena_bytes, max_batch, max_prefill_tokens,
-                                self.stream.cuda_stream, page_tokens)
+                                self.stream.cuda_stream, page_tokens, kv_bits)
         self.page_tokens = page_tokens
+        self.kv_bits = kv_bits
         self.handle = B.engine_create(weights.cfg, weights.struct, params)
         self.max_batch = max_batch
         self.max_prefill_tokens = max_prefill_tokens

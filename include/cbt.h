@@ -73,6 +73,7 @@ typedef int32_t cbt_status;
 #define CBT_DEV_OK 0
 #define CBT_DEV_TOKEN_RANGE 1 /* a token id outside [0, vocab) */
 #define CBT_DEV_TIMEOUT 2     /* a kernel's bounded wait ran out; it stopped early (info: role) */
+#define CBT_DEV_WORK_ITEM 3   /* an attention work item its kernel cannot take (info: item) */
 
 #define CBT_WEIGHTS_BF16 0    /* bf16, row-major [out][in] */
 #define CBT_WEIGHTS_AFFINE4 1 /* 4-bit affine, see cbt_linear */
@@ -139,6 +140,27 @@ typedef struct {
                               * a call that writes a position in a shared page first queues a
                               * copy of that page into a new page of the writing slab (copy on
                               * write), and that page counts towards the same pool check. */
+  int32_t kv_bits;           /* 0 or 16: bf16 KV.  8: 8-bit affine KV (the mlx-bun batching
+                              * design's quantised KV): per position and (layer, K|V, kv head),
+                              * head_dim codes plus a bf16 scale and bias per 64 dims; a value
+                              * reads back as scale * code + bias, with scale = bf16((max -
+                              * min) / 255), bias = bf16(min), code = clamp(rint((x - bias) /
+                              * scale), 0, 255) over its group of 64 (cbt_quantize_kv8).  A
+                              * sequence's prompt is prefilled in bf16 and then converted, so
+                              * prefill logits equal the bf16 engine's; every decode step
+                              * quantises its new K/V before attention reads all positions
+                              * through their codes.  Slabs take cbt_slab_bytes_kv8 bytes; the
+                              * engine also holds max_batch * cbt_slab_bytes(cfg, 128) bytes of
+                              * the arena for the decode rows' bf16 staging (CBT_ERR_POOL_EXHAUSTED
+                              * from cbt_engine_create if it does not fit).  Needs contiguous
+                              * slabs (kv_page_tokens = 0, else CBT_ERR_UNSUPPORTED) and the
+                              * tensor-core path.  Not available on an 8-bit engine
+                              * (CBT_ERR_UNSUPPORTED): prefill into a slab that already holds
+                              * positions, cbt_kv_slab_export, cbt_kv_slab_copy_prefix,
+                              * cbt_kv_slab_share_prefix.  cbt_kv_slab_import quantises what it
+                              * imports.  During a call, intermediate bf16 slabs of the
+                              * prompts' (or the import's) size are taken from the arena and
+                              * returned. */
 } cbt_engine_params;
 
 typedef struct {
@@ -153,6 +175,21 @@ typedef struct {
 } cbt_stats;
 
 typedef struct cbt_engine cbt_engine;
+
+/* Bytes of an 8-bit KV slab of capacity cap (kv_bits = 8): per (layer, K|V, kv head) block
+ * codes [round64(cap)][head_dim] uint8, then bf16 scales and bf16 biases
+ * [round64(cap)][head_dim / 64]; the total rounded up to 4 KiB.  0 if head_dim is not a
+ * multiple of 64 or cap <= 0. */
+size_t cbt_slab_bytes_kv8(const cbt_model_config* c, int32_t cap);
+
+/* 8-bit affine quantisation of bf16 rows, groups of 64 along each row (the kv_bits = 8 format).
+ *   x       device bf16 [rows][cols], 4-byte aligned; cols a multiple of 64.
+ *   codes   device uint8 [rows][cols] (2-byte aligned); scales, biases device bf16
+ *           [rows][cols / 64].
+ *   stream  cudaStream_t (NULL: legacy default stream); queued, not synchronised.
+ * CBT_ERR_NULL, CBT_ERR_INVALID (shape or alignment), CBT_ERR_CUDA. */
+cbt_status cbt_quantize_kv8(const void* x, int32_t rows, int32_t cols, void* codes, void* scales,
+                            void* biases, void* stream);
 
 const char* cbt_status_str(cbt_status s);
 
