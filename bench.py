@@ -346,9 +346,10 @@ def gpu_arm(args, rank: int, world: int):
 
 
 # ---- the oracle (CPU) ----------------------------------------------------------------------------
-def oracle_decode_sample(wl, max_steps: int, budget_s: float):
-    """Time the oracle's batched decode step on the same workload: all rows, weights streamed
-    once per step, for up to max_steps steps or until budget_s has passed."""
+def oracle_decode_sample(wl, max_steps: int, budget_s: float, kv_bits: int = 16):
+    """Time the oracle's batched decode step on the same workload (KV in the same format): all
+    rows, weights streamed once per step, for up to max_steps steps or until budget_s has
+    passed."""
     import numpy as np
 
     import oracle
@@ -356,7 +357,7 @@ def oracle_decode_sample(wl, max_steps: int, budget_s: float):
     ctx = [int(c) for c in wl.context_lengths()]
     caches = []
     for r, c in enumerate(ctx):
-        kc = oracle.KVCache(wl.shape, c + max_steps + 2)
+        kc = oracle.KVCache(wl.shape, c + max_steps + 2, kv_bits=kv_bits)
         kc.fill_synthetic(r, c, wl.seed)
         caches.append(kc)
     feed = np.array([wl.row_tokens(r, c + 1)[c] for r, c in enumerate(ctx)], dtype=np.int32)
@@ -370,7 +371,8 @@ def oracle_decode_sample(wl, max_steps: int, budget_s: float):
     return {"value": len(ctx) * done / t_total, "unit": "tok/s", "cores": oracle.num_threads(),
             "kind": "oracle",
             "sample": f"{done} decode step(s) of all {len(ctx)} rows of {wl.name} "
-                      f"(full 32-layer model, {t_total:.1f} s of CPU time)"}, done, t_total
+                      f"(full 32-layer model, {'8-bit' if kv_bits == 8 else 'bf16'} KV, "
+                      f"{t_total:.1f} s of CPU time)"}, done, t_total
 
 
 def reference_arm(args, rank: int):
@@ -378,12 +380,13 @@ def reference_arm(args, rank: int):
         return None
     wl = workload_by_name(args.workload, args.layers)
     cb, done, t_total = oracle_decode_sample(wl, max_steps=max(1, args.steps),
-                                             budget_s=args.reference_budget)
+                                             budget_s=args.reference_budget, kv_bits=args.kv_bits)
     return {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "tok/s",
             "n_gpus": 0, "steps": done, "warmup": 0, "ms_per_step": 1e3 * t_total / done,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": wl.name, "model": wl.shape.name,
-                                            "batch_per_gpu": len(wl.context_lengths())},
+                                            "batch_per_gpu": len(wl.context_lengths()),
+                                            "kv_bits": args.kv_bits},
             "cpu_baseline": cb,
             "e2e": {"value": cb["value"], "unit": "tok/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -502,7 +505,7 @@ def main():
         res = gpu_arm(args, rank, world)
         if rank == 0 and not args.no_cpu_baseline:
             wl = workload_by_name(args.workload, args.layers)
-            cb, _, _ = oracle_decode_sample(wl, max_steps=2, budget_s=15.0)
+            cb, _, _ = oracle_decode_sample(wl, max_steps=2, budget_s=15.0, kv_bits=args.kv_bits)
             res["cpu_baseline"] = cb
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)
