@@ -85,6 +85,25 @@ def test_slab_bytes(lib):
     assert B.slab_bytes(tiny, 2) == 64 * 2048  # 2048 bytes per position
     assert B.slab_bytes(tiny, 65) == 128 * 2048
     assert B.slab_bytes(tiny, 0) == 0
+    # 8-bit KV: per position and (layer, K|V, kv head) head_dim codes + a bf16 scale and bias per
+    # 64 dims: 32 x 2 x 8 x (128 + 4 + 4) = 69632 bytes per position
+    assert B.slab_bytes_kv8(cfg, 2048) == 2048 * 69632
+    assert B.slab_bytes_kv8(cfg, 1) == 64 * 69632
+    assert B.slab_bytes_kv8(tiny, 100) == -(-(128 * 2 * 2 * 4 * (64 + 2 + 2)) // 4096) * 4096
+    assert B.slab_bytes_kv8(tiny, 0) == 0
+    odd = B.ModelConfig(2, 256, 4, 4, 96, 1024, 1024, 1e-6, 1e4, 0, 64)
+    assert B.slab_bytes_kv8(odd, 64) == 0          # head_dim not a multiple of 64
+
+
+def test_quantize_kv8_argument_checks(lib):
+    """Rejected before anything is queued (no GPU needed): NULL buffers, a row length that is
+    not a multiple of 64, misaligned buffers."""
+    fake = ctypes.c_void_p(0x1000)
+    assert lib.cbt_quantize_kv8(None, 4, 64, fake, fake, fake, None) == -2
+    assert lib.cbt_quantize_kv8(fake, 4, 96, fake, fake, fake, None) == -1
+    assert lib.cbt_quantize_kv8(ctypes.c_void_p(0x1002), 4, 64, fake, fake, fake, None) == -1
+    assert lib.cbt_quantize_kv8(fake, 4, 64, ctypes.c_void_p(0x1001), fake, fake, None) == -1
+    assert lib.cbt_quantize_kv8(fake, -1, 64, fake, fake, fake, None) == -1
 
 
 def test_calls_reject_null_engine(lib):
