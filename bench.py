@@ -137,10 +137,12 @@ class ClockSampler:
 
 
 # ---- the GPU arm ------------------------------------------------------------------------------
-def setup_decode(wl, device, extra_positions: int, page_tokens: int = 0, kv_bits: int = 16):
+def setup_decode(wl, device, extra_positions: int, page_tokens: int = 0, kv_bits: int = 16,
+                 weights=None):
     """Engine + slabs for a decode workload: synthetic KV of each row loaded into its slab,
     each row's next token ready on the device.  page_tokens > 0: a paged engine; kv_bits = 8:
-    8-bit KV (the arena also holds the decode rows' staging and one import's bf16 slab)."""
+    8-bit KV (the arena also holds the decode rows' staging and one import's bf16 slab).
+    weights: DeviceWeights of the workload's shape to reuse (else they are drawn here)."""
     import numpy as np
     import torch
 
@@ -150,7 +152,7 @@ def setup_decode(wl, device, extra_positions: int, page_tokens: int = 0, kv_bits
     shape = wl.shape
     ctx = [int(c) for c in wl.context_lengths()]
     caps = [c + extra_positions for c in ctx]
-    w = DeviceWeights(shape, device)
+    w = weights if weights is not None else DeviceWeights(shape, device)
     if page_tokens:
         arena = sum(B.slab_bytes(w.cfg, page_tokens) * (-(-c // page_tokens)) for c in caps)
     elif kv_bits == 8:
@@ -340,9 +342,73 @@ def gpu_arm(args, rank: int, world: int):
             "clocks": clk,
         }
     eng.close()
+    if result is not None and world == 1 and not args.no_sweep and not args.layers:
+        result["sweep"] = sweep_arm(device, w, 10, 3, result["roofline"]["peak"])
     if dist:
         dist.destroy_process_group()
     return result
+
+
+def time_steps(eng, slabs, tok0, steps: int, warmup: int) -> float:
+    """Milliseconds per greedy decode step (the captured step replayed), CUDA events on the
+    engine stream around `steps` steps after `warmup` untimed ones."""
+    import torch
+    bufs = [tok0.clone(), torch.empty_like(tok0)]
+    for i in range(warmup):
+        eng.decode_step_batch(slabs, bufs[i % 2], None, bufs[(i + 1) % 2])
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(eng.stream):
+        ev0.record(eng.stream)
+        for i in range(warmup, warmup + steps):
+            eng.decode_step_batch(slabs, bufs[i % 2], None, bufs[(i + 1) % 2])
+        ev1.record(eng.stream)
+    torch.cuda.synchronize()
+    return ev0.elapsed_time(ev1) / steps
+
+
+SWEEP = ([f"7b-bf16-b{b}-ctx2048" for b in (1, 2, 4, 8, 16, 32)] + ["7b-bf16-b32-long"]
+         + [f"7b-affine4-b{b}-ctx2048" for b in (1, 2, 4, 8, 16, 32)])
+
+
+def sweep_arm(device, bf16_weights, steps: int, warmup: int, hbm_peak: float):
+    """The batch-size sweep of the metric: bf16 and 4-bit weights at B = 1..32 (context 2048)
+    and the long-context workload (32 rows of 8k-16k positions), each timed like the headline
+    line, with its own step roofline."""
+    import torch
+
+    from continuous_batching_transformer_gb300.model import DeviceWeights
+    from synth.recipes import MISTRAL_7B_Q4
+
+    out = []
+    q4 = None
+    for name in SWEEP:
+        wl = workload_by_name(name)
+        if wl.shape.weight_format == "bf16":
+            w = bf16_weights
+        else:
+            if q4 is None:
+                q4 = DeviceWeights(MISTRAL_7B_Q4, device)
+            w = q4
+        _, eng, slabs, ctx, tok0 = setup_decode(wl, device, extra_positions=steps + warmup + 4,
+                                                weights=w)
+        ms = time_steps(eng, slabs, tok0, steps, warmup)
+        code, info = eng.device_error()
+        eng.close()
+        del eng
+        torch.cuda.empty_cache()
+        if code != 0:
+            raise SystemExit(f"{name}: device error word set: code {code} info {info}")
+        ctx_mean = [c + warmup + steps / 2.0 for c in ctx]
+        sb = step_bytes(wl.shape, ctx_mean)
+        gbs = sb / (ms / 1e3) / 1e9
+        out.append({"workload": wl.name, "batch": len(ctx), "ms_per_step": ms,
+                    "tok_s": len(ctx) / (ms / 1e3), "algorithmic_bytes_per_step": sb,
+                    "achieved_gbs": gbs, "frac_of_8TBps": gbs / NOMINAL_HBM_GBS,
+                    "frac_of_measured_hbm": gbs / hbm_peak})
+    del q4
+    torch.cuda.empty_cache()
+    return out
 
 
 # ---- the oracle (CPU) ----------------------------------------------------------------------------
@@ -486,6 +552,9 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="7b-bf16-b8")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the B = 1..32 sweep (bf16 and 4-bit, ctx 2048) and the long-context "
+                         "line that the default run appends as 'sweep'")
     ap.add_argument("--reference-budget", type=float, default=60.0)
     ap.add_argument("--kv-bits", type=int, default=16, choices=(8, 16),
                     help="KV precision: 16 (bf16) or 8 (8-bit affine, groups of 64)")

@@ -75,10 +75,10 @@ __global__ void k_rmsnorm(const float* x, const uint16_t* gain, int d, float eps
   for (int j = threadIdx.x; j < d; j += blockDim.x) hr[j] = xr[j] * r * bf16_to_f32(gain[j]);
 }
 
-void launch_rmsnorm(const float* x, const uint16_t* gain, int n, int d, float eps, float* h,
-                    cudaStream_t s) {
-  if (n <= 0) return;
-  launch_pdl(k_rmsnorm, dim3(n), dim3(256), 0, s, x, gain, d, eps, h);
+cudaError_t launch_rmsnorm(const float* x, const uint16_t* gain, int n, int d, float eps,
+                           float* h, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  return launch_pdl(k_rmsnorm, dim3(n), dim3(256), 0, s, x, gain, d, eps, h);
 }
 
 // bf16 operand of a tensor-core projection: hi = bf16(v), and lo = bf16(v - hi) in rows
@@ -383,9 +383,9 @@ __global__ void k_argmax(const float* logits, int vocab, int32_t* out) {
   }
 }
 
-void launch_argmax(const float* logits, int n, int vocab, int32_t* out, cudaStream_t s) {
-  if (n <= 0) return;
-  launch_pdl(k_argmax, dim3(n), dim3(512), 0, s, logits, vocab, out);
+cudaError_t launch_argmax(const float* logits, int n, int vocab, int32_t* out, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  return launch_pdl(k_argmax, dim3(n), dim3(512), 0, s, logits, vocab, out);
 }
 
 __global__ void k_gather_rows(const float* src, const int32_t* idx, int d, float* dst) {

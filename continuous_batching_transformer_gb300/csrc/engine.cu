@@ -241,6 +241,10 @@ extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_w
       p->kv_page_tokens % 128 || (p->kv_bits != 0 && p->kv_bits != 16 && p->kv_bits != 8))
     return CBT_ERR_INVALID;
   if (p->kv_bits == 8 && p->kv_page_tokens) return CBT_ERR_UNSUPPORTED;
+  // the 8-bit decode attention is built for 1, 2, 4 or 8 q heads per kv head
+  if (p->kv_bits == 8 && c.n_heads / c.n_kv_heads != 1 && c.n_heads / c.n_kv_heads != 2 &&
+      c.n_heads / c.n_kv_heads != 4 && c.n_heads / c.n_kv_heads != 8)
+    return CBT_ERR_UNSUPPORTED;
   if (!linear_ok(w->lm_head, c.weight_format)) return CBT_ERR_NULL;
   for (int l = 0; l < c.n_layers; ++l) {
     const cbt_layer_weights& L = w->layers[l];

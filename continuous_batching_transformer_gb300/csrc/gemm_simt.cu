@@ -196,45 +196,48 @@ int pick_slice(int K) {
 }
 
 template <int NB>
-void run_gemv(const float* x, int n, int K, const LinearW& W, int M, int Ks, float* part,
-              cudaStream_t s) {
+cudaError_t run_gemv(const float* x, int n, int K, const LinearW& W, int M, int Ks, float* part,
+                     cudaStream_t s) {
   dim3 grid((M + GEMV_ROWS - 1) / GEMV_ROWS, K / Ks);
   size_t smem = sizeof(float) * (size_t)NB * Ks;
+  cudaError_t rc;
   if (W.fmt == CBT_WEIGHTS_BF16) {
-    cudaFuncSetAttribute(gemv_splitk<NB, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    launch_pdl((gemv_splitk<NB, false>), dim3(grid), dim3(GEMV_THREADS), smem, s, x, n, K, W, M, Ks, part);
-  } else {
-    cudaFuncSetAttribute(gemv_splitk<NB, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    launch_pdl((gemv_splitk<NB, true>), dim3(grid), dim3(GEMV_THREADS), smem, s, x, n, K, W, M, Ks, part);
+    rc = cudaFuncSetAttribute(gemv_splitk<NB, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (rc != cudaSuccess) return rc;
+    return launch_pdl((gemv_splitk<NB, false>), dim3(grid), dim3(GEMV_THREADS), smem, s, x, n, K, W, M, Ks, part);
   }
+  rc = cudaFuncSetAttribute(gemv_splitk<NB, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (rc != cudaSuccess) return rc;
+  return launch_pdl((gemv_splitk<NB, true>), dim3(grid), dim3(GEMV_THREADS), smem, s, x, n, K, W, M, Ks, part);
 }
 
 template <int EPI>
-void run_tiled(const float* x, int n, int K, const LinearW& W, int M, float* out, cudaStream_t s) {
+cudaError_t run_tiled(const float* x, int n, int K, const LinearW& W, int M, float* out, cudaStream_t s) {
   int Mo = EPI == EPI_SWIGLU ? M / 2 : M;
   dim3 grid((Mo + TM - 1) / TM, (n + TT - 1) / TT);
   if (W.fmt == CBT_WEIGHTS_BF16)
-    launch_pdl((gemm_tiled<false, EPI>), dim3(grid), dim3(256), 0, s, x, n, K, W, M, out);
-  else
-    launch_pdl((gemm_tiled<true, EPI>), dim3(grid), dim3(256), 0, s, x, n, K, W, M, out);
+    return launch_pdl((gemm_tiled<false, EPI>), dim3(grid), dim3(256), 0, s, x, n, K, W, M, out);
+  return launch_pdl((gemm_tiled<true, EPI>), dim3(grid), dim3(256), 0, s, x, n, K, W, M, out);
 }
 
 }  // namespace
 
-void launch_linear(const float* x, int n, int K, const LinearW& W, int M, Epilogue epi, float* out,
-                   float* partials, size_t partial_floats, cudaStream_t s) {
-  if (n <= 0) return;
+cudaError_t launch_linear(const float* x, int n, int K, const LinearW& W, int M, Epilogue epi,
+                          float* out, float* partials, size_t partial_floats, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
   int Ks = pick_slice(K);
   if (n <= 32 && Ks > 0 && (size_t)(K / Ks) * n * M <= partial_floats) {
-    if (n <= 8) run_gemv<8>(x, n, K, W, M, Ks, partials, s);
-    else if (n <= 16) run_gemv<16>(x, n, K, W, M, Ks, partials, s);
-    else run_gemv<32>(x, n, K, W, M, Ks, partials, s);
+    cudaError_t rc;
+    if (n <= 8) rc = run_gemv<8>(x, n, K, W, M, Ks, partials, s);
+    else if (n <= 16) rc = run_gemv<16>(x, n, K, W, M, Ks, partials, s);
+    else rc = run_gemv<32>(x, n, K, W, M, Ks, partials, s);
+    if (rc != cudaSuccess) return rc;
     int Mo = epi == EPI_SWIGLU ? M / 2 : M;
     long long tot = (long long)n * Mo;
-    launch_pdl(splitk_reduce, dim3((unsigned)((tot + 255) / 256)), dim3(256), 0, s, partials, K / Ks, n, M, epi, out);
-    return;
+    return launch_pdl(splitk_reduce, dim3((unsigned)((tot + 255) / 256)), dim3(256), 0, s,
+                      partials, K / Ks, n, M, epi, out);
   }
-  if (epi == EPI_STORE) run_tiled<EPI_STORE>(x, n, K, W, M, out, s);
-  else if (epi == EPI_ADD) run_tiled<EPI_ADD>(x, n, K, W, M, out, s);
-  else run_tiled<EPI_SWIGLU>(x, n, K, W, M, out, s);
+  if (epi == EPI_STORE) return run_tiled<EPI_STORE>(x, n, K, W, M, out, s);
+  if (epi == EPI_ADD) return run_tiled<EPI_ADD>(x, n, K, W, M, out, s);
+  return run_tiled<EPI_SWIGLU>(x, n, K, W, M, out, s);
 }

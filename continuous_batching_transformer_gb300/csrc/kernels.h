@@ -201,8 +201,8 @@ void launch_embed(const int32_t* tokens, int n, const uint16_t* table, int d, in
                   int* err, float* ss, int ss_ld, const uint16_t* gain, uint16_t* act,
                   int lo_rows, cudaStream_t s);
 // RMSNorm rows of x into h
-void launch_rmsnorm(const float* x, const uint16_t* gain, int n, int d, float eps, float* h,
-                    cudaStream_t s);
+cudaError_t launch_rmsnorm(const float* x, const uint16_t* gain, int n, int d, float eps,
+                           float* h, cudaStream_t s);
 // per-token RoPE cos/sin for the positions in rows (fp32 [n][hd/2] each), in double
 void launch_rope_table(const QueryRow* rows, int n, int head_dim, double theta, float* cosv,
                        float* sinv, cudaStream_t s);
@@ -241,10 +241,10 @@ void launch_attention_naive(const float* qkv, const QueryRow* rows, const long l
                             int head_dim, int max_keys, const uint16_t* arena, float* o,
                             cudaStream_t s);
 // projection y = x W^T with an epilogue; picks the skinny or the tiled kernel
-void launch_linear(const float* x, int n, int K, const LinearW& W, int M, Epilogue epi, float* out,
-                   float* partials, size_t partial_floats, cudaStream_t s);
+cudaError_t launch_linear(const float* x, int n, int K, const LinearW& W, int M, Epilogue epi,
+                          float* out, float* partials, size_t partial_floats, cudaStream_t s);
 // greedy argmax per row, lowest index on ties
-void launch_argmax(const float* logits, int n, int vocab, int32_t* out, cudaStream_t s);
+cudaError_t launch_argmax(const float* logits, int n, int vocab, int32_t* out, cudaStream_t s);
 // gather rows idx[i] of src [*, d] into dst [i, d]
 void launch_gather_rows(const float* src, const int32_t* idx, int n, int d, float* dst,
                         cudaStream_t s);

@@ -276,13 +276,10 @@ __global__ void k_attn_merge_kv8(Kv8AttnArgs a, int G, int head_dim) {
 template <int G, int HD>
 bool launch_attn_kv8_t(const Kv8AttnArgs& a, int num_sms, cudaStream_t s) {
   const size_t smem = sizeof(AttnSmem<G, HD>);
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(k_attn_decode_kv8<G, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
-      return false;
-    attr_set = true;
-  }
+  // set on every launch: the attribute belongs to the current device's copy of the kernel
+  if (cudaFuncSetAttribute(k_attn_decode_kv8<G, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return false;
   const int per_sm = std::max(1, std::min(4, (int)((200u << 10) / smem)));
   if (launch_pdl(k_attn_decode_kv8<G, HD>, dim3(num_sms * per_sm), dim3(kAttnThreads), smem, s, a) !=
       cudaSuccess)

@@ -74,8 +74,10 @@ extern "C" cbt_status cbt_greedy_head_noalloc(const cbt_model_config* cfg, const
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   LinearW W{lm_head->w, static_cast<const uint16_t*>(lm_head->scales),
             static_cast<const uint16_t*>(lm_head->biases), cfg->weight_format};
-  launch_rmsnorm(hidden, static_cast<const uint16_t*>(final_norm), n, d, cfg->rms_eps, h, s);
-  launch_linear(h, n, d, W, V, EPI_STORE, logits, part, part_cap, s);
-  if (next_tokens) launch_argmax(logits, n, V, next_tokens, s);
-  return cudaGetLastError() == cudaSuccess ? CBT_OK : CBT_ERR_CUDA;
+  // each launch's own status: an error left behind by unrelated earlier work is not this call's
+  cudaError_t rc = launch_rmsnorm(hidden, static_cast<const uint16_t*>(final_norm), n, d,
+                                  cfg->rms_eps, h, s);
+  if (rc == cudaSuccess) rc = launch_linear(h, n, d, W, V, EPI_STORE, logits, part, part_cap, s);
+  if (rc == cudaSuccess && next_tokens) rc = launch_argmax(logits, n, V, next_tokens, s);
+  return rc == cudaSuccess ? CBT_OK : CBT_ERR_CUDA;
 }

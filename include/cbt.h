@@ -153,8 +153,9 @@ typedef struct {
                               * engine also holds max_batch * cbt_slab_bytes(cfg, 128) bytes of
                               * the arena for the decode rows' bf16 staging (CBT_ERR_POOL_EXHAUSTED
                               * from cbt_engine_create if it does not fit).  Needs contiguous
-                              * slabs (kv_page_tokens = 0, else CBT_ERR_UNSUPPORTED) and the
-                              * tensor-core path.  Not available on an 8-bit engine
+                              * slabs (kv_page_tokens = 0), n_heads / n_kv_heads in {1, 2, 4,
+                              * 8} and the tensor-core path; cbt_engine_create returns
+                              * CBT_ERR_UNSUPPORTED otherwise.  Not available on an 8-bit engine
                               * (CBT_ERR_UNSUPPORTED): prefill into a slab that already holds
                               * positions, cbt_kv_slab_export, cbt_kv_slab_copy_prefix,
                               * cbt_kv_slab_share_prefix.  cbt_kv_slab_import quantises what it
@@ -335,8 +336,11 @@ cbt_status cbt_quantize_affine4(const void* w, int32_t rows, int32_t cols, int32
  * last stage of a decode step on hidden states the caller already has:
  *   logits[r] = RMSNorm(hidden[r], final_norm, cfg->rms_eps) lm_head^T,
  *   next_tokens[r] = argmax(logits[r]) (lowest id on ties),
- * the same kernels decode_step_batch ends with, but its scratch (the normalised rows and
- * the split-K partial sums of the projection) lives in one fixed array in the library's
+ * the operations decode_step_batch ends with, computed by the library's CUDA-core kernels
+ * (an RMSNorm kernel, a split-K projection whose partial sums are added in a fixed order,
+ * the argmax kernel) rather than the tensor-core projection of a decode step, so its logits
+ * agree with decode_step_batch's within rounding, not bit for bit.  Its scratch (the
+ * normalised rows and the split-K partial sums) lives in one fixed array in the library's
  * device memory, CBT_NOALLOC_SCRATCH_BYTES large.  Every GPU that loads the library holds
  * that array until the process exits.
  *   cfg          model config (d_model, vocab, rms_eps, weight_format, group_size are used)
@@ -347,7 +351,9 @@ cbt_status cbt_quantize_affine4(const void* w, int32_t rows, int32_t cols, int32
  *   logits       device float [n][vocab], written
  *   next_tokens  device int32 [n], written; may be NULL
  *   stream       cudaStream_t to queue on (NULL = legacy default stream)
- * Returns CBT_ERR_LIMIT, before queuing anything, when n > CBT_NOALLOC_MAX_ROWS or when
+ * Returns CBT_ERR_CUDA if one of its own launches fails (an error left by earlier, unrelated
+ * work is neither reported nor cleared), and CBT_ERR_LIMIT, before queuing anything, when
+ * n > CBT_NOALLOC_MAX_ROWS or when
  * n*d_model + (d_model/slice)*n*vocab floats (slice = 1024, 512 or 256, the largest that
  * divides d_model) exceed the fixed scratch.  It calls no cudaMalloc, cudaFree or any
  * allocating library routine.  The first call on each device looks up the array's device

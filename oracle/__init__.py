@@ -213,6 +213,18 @@ class LinearW:
         return Linear(_ptr(self.w), _ptr(self.packed), _ptr(self.scales), _ptr(self.biases))
 
 
+def project(lin: LinearW, x: np.ndarray, group: int = 64) -> np.ndarray:
+    """y = x W^T for one stand-alone projection (bf16 or 4-bit affine, as `lin` holds it)."""
+    fmt = 0 if lin.w is not None else 1
+    cfg = Config(1, lin.in_dim, 1, 1, 2, 1, lin.out_dim, 0.0, 1.0, fmt, group)
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1, lin.in_dim)
+    y = np.empty((x.shape[0], lin.out_dim), dtype=np.float32)
+    st = lin.struct()
+    lib().orc_linear_apply(ctypes.byref(cfg), ctypes.byref(st), lin.out_dim, lin.in_dim, _ptr(x),
+                           x.shape[0], _ptr(y))
+    return y
+
+
 class OracleModel:
     """Synthetic weights of a ModelShape, drawn from ``synth`` in the oracle's own layout
     (separate Wq, Wk, Wv, Wg, Wu matrices, each [out, in])."""

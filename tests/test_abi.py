@@ -118,3 +118,29 @@ def test_calls_reject_null_engine(lib):
     assert lib.cbt_quantize_affine4(None, 1, 64, 64, None, None, None, None) == -2
     fake = ctypes.c_void_p(0x1000)
     assert lib.cbt_quantize_affine4(fake, 4, 96, 64, fake, fake, fake, None) == -1  # cols % group
+
+
+def test_kv8_engine_rejects_unsupported_head_groups(lib):
+    """8-bit KV decode attention is built for 1, 2, 4 or 8 q heads per kv head: any other ratio
+    is refused by cbt_engine_create before anything reaches the device."""
+    fake = 0x1000
+    h = ctypes.c_void_p()
+
+    def create(n_heads, n_kv_heads, kv_bits):
+        cfg = B.ModelConfig(2, 256, n_heads, n_kv_heads, 64, 1024, 1024, 1e-6, 1e4, 0, 64)
+        lw = (B.LayerWeights * 2)()
+        for l in range(2):
+            lin = B.Linear(fake, None, None)
+            lw[l] = B.LayerWeights(lin, lin, lin, lin, fake, fake)
+        w = B.Weights(fake, B.Linear(fake, None, None), fake,
+                      ctypes.cast(lw, ctypes.POINTER(B.LayerWeights)))
+        p = B.EngineParams(fake, 1 << 30, 4, 64, None, 0, kv_bits)
+        return lib.cbt_engine_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(p),
+                                     ctypes.byref(h))
+
+    for heads, kv in ((12, 4), (20, 4), (24, 4), (28, 4), (16, 1)):  # 3, 5, 6, 7, 16 per kv head
+        assert create(heads, kv, 8) == -11, (heads, kv)
+        assert not h.value
+    # a supported ratio gets past the check (here it then fails on the missing device)
+    assert create(16, 4, 8) != -11
+    assert not h.value

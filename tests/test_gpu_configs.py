@@ -1,0 +1,244 @@
+"""The 7B-shaped workloads as they are specified, against the oracle through the C ABI:
+
+- the bf16 decode workload run for its full 128 greedy steps (the K/V each step appends is read
+  back by every later step, over 32 layers);
+- the 4-bit affine weights at the batch sizes of the sweep not covered elsewhere (B = 1, 2, 8;
+  B = 1 takes the one-column instantiation of the register-dequant projection);
+- a slice of the continuous-batching trace: the trace's own prompts (256 to 4096 tokens)
+  admitted by segmented prefill while other rows decode, rows joining and retiring.
+
+A full 7B prefill of thousands of tokens, or 128 separate oracle decode steps, is beyond the
+oracle's test budget.  Two exact devices keep it bounded:
+
+- teacher forcing: the logits of decode step i depend only on the tokens fed at steps <= i, so
+  the oracle replays the tokens the GPU fed a row in ONE causal pass over those positions;
+- hand-off: the K/V a prefill wrote (exported through the C ABI) become the oracle's cache.  At
+  sampled positions p the oracle recomputes token p from the GPU's K/V of positions [0, p):
+  its K/V at p in every layer must match what the GPU stored there, and at a segment's last
+  position its logits must match the prefill's logits.  Decode steps are then recomputed from
+  the exported cache.
+"""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import bench
+import oracle
+from continuous_batching_transformer_gb300.model import DeviceWeights, Engine
+from continuous_batching_transformer_gb300.trace import prompt_tokens
+from synth.recipes import DECODE_7B_B8, MISTRAL_7B, decode_7b_fixed, trace_requests
+from tests.gpu_harness import TOL, check_logits, ensure_built, to_dev
+
+pytestmark = pytest.mark.gpu
+
+_oracle_models = {}
+
+
+def oracle_model(shape):
+    """One oracle model per shape for the whole module (building a 7B one takes tens of
+    seconds)."""
+    if shape.name not in _oracle_models:
+        _oracle_models.clear()
+        gc.collect()
+        _oracle_models[shape.name] = oracle.OracleModel(shape)
+    return _oracle_models[shape.name]
+
+
+def release():
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def test_7b_bf16_b8_all_128_greedy_steps():
+    """The 8-row workload with contexts 512..4096 for the 128 greedy steps it specifies, each
+    step fed the previous step's device-side next tokens (no host round trip).  The row with the
+    shortest context is checked at every step against the oracle's teacher-forced replay of the
+    tokens the GPU fed it; the GPU's token register must hold the argmax of its own logits."""
+    ensure_built()
+    dev = torch.device("cuda:0")
+    wl = DECODE_7B_B8
+    steps = wl.steps
+    assert steps == 128
+    w, eng, slabs, ctx, tok = bench.setup_decode(wl, dev, extra_positions=steps + 8)
+    Bsz, V = len(slabs), wl.shape.vocab
+    r = int(np.argmin(ctx))
+    logits = torch.empty((Bsz, V), dtype=torch.float32, device=dev)
+    hist = torch.empty((steps, V), dtype=torch.float32, device=dev)
+    fed = torch.empty(steps + 1, dtype=torch.int32, device=dev)
+    bufs = [tok.clone(), torch.empty_like(tok)]
+    with torch.cuda.stream(eng.stream):
+        for i in range(steps):
+            cur, nxt = bufs[i % 2], bufs[(i + 1) % 2]
+            eng.decode_step_batch(slabs, cur, logits, nxt)
+            hist[i].copy_(logits[r])
+            fed[i].copy_(cur[r])
+        fed[steps].copy_(bufs[steps % 2][r])
+    eng.stream.synchronize()
+    got = hist.cpu().numpy()
+    fed_h = fed.cpu().numpy()
+    assert eng.device_error() == (0, 0)
+    assert [eng.position(s) for s in slabs] == [c + steps for c in ctx]
+    eng.close()
+    del w, eng, hist, logits
+    release()
+    for i in range(steps):  # the register holds the GPU's own greedy token
+        assert fed_h[i + 1] == int(np.argmax(got[i])), f"step {i}: register vs argmax"
+
+    m = oracle_model(wl.shape)
+    kc = oracle.KVCache(wl.shape, ctx[r] + steps + 2)
+    kc.fill_synthetic(r, ctx[r], wl.seed)
+    pos = np.arange(ctx[r], ctx[r] + steps, dtype=np.int32)
+    ref = oracle.forward(m, [kc], np.zeros(steps, np.int32), pos, fed_h[:steps],
+                         np.ones(steps, np.int32))
+    errs = [check_logits(got[i:i + 1], ref[i:i + 1], TOL["bf16"], f"row {r} step {i}")
+            for i in range(steps)]
+    print(f"128 steps, row {r} (ctx {ctx[r]}): max |logit - oracle| = {max(errs):.3e}")
+
+
+@pytest.mark.parametrize("B,row", [(1, 0), (2, 1), (8, 7)])
+def test_7b_affine4_sweep_batches(B, row):
+    """4-bit affine weights (group 64) at ctx 2048, two greedy steps, one sampled row."""
+    ensure_built()
+    wl = decode_7b_fixed(B, 2048, "affine4")
+    dev = torch.device("cuda:0")
+    w, eng, slabs, ctx, tok = bench.setup_decode(wl, dev, extra_positions=8)
+    V = wl.shape.vocab
+    logits = torch.empty((B, V), dtype=torch.float32, device=dev)
+    nxt = torch.empty(B, dtype=torch.int32, device=dev)
+    m = oracle_model(wl.shape)
+    kc = oracle.KVCache(wl.shape, ctx[row] + 4)
+    kc.fill_synthetic(row, ctx[row], wl.seed)
+    feed = tok.cpu().numpy()
+    for step in range(2):
+        eng.decode_step_batch(slabs, to_dev(feed, dev), logits, nxt)
+        ref = oracle.decode_step_batch(m, [kc], feed[[row]])
+        err = check_logits(logits.cpu().numpy()[[row]], ref, TOL["affine4"],
+                           f"{wl.name} row {row} step {step}")
+        feed = nxt.cpu().numpy().copy()
+        feed[row] = oracle.argmax(ref[0])
+    assert eng.device_error() == (0, 0)
+    eng.close()
+    del w
+    release()
+    print(f"{wl.name}: max |logit - oracle| = {err:.3e}")
+
+
+def exported_kv(eng, slab, n):
+    s = eng.shape
+    dims = (s.n_layers, s.n_kv_heads, n, s.head_dim)
+    k = torch.empty(dims, dtype=torch.bfloat16)
+    v = torch.empty(dims, dtype=torch.bfloat16)
+    eng.export_kv(slab, k, v, n)
+    eng.stream.synchronize()
+    return k.view(torch.int16).numpy().view(np.uint16), v.view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_values(a):
+    return (a.astype(np.uint32) << 16).view(np.float32)
+
+
+def check_kv_at(shape, got_k, got_v, cache, p, what):
+    """The oracle's K/V at position p against the GPU's: bf16 roundings of the same value,
+    so within one bf16 step (2^-8 relative) plus the drift a 32-layer forward allows."""
+    for name, g, o in (("K", got_k[:, :, p], cache.k[:, :, p]), ("V", got_v[:, :, p], cache.v[:, :, p])):
+        gf, of = bf16_values(g), bf16_values(o)
+        tol = 2.0 ** -7 * np.abs(of) + 0.01 * shape.kv_sigma
+        bad = np.abs(gf - of) > tol
+        assert not bad.any(), (f"{what}: {name} at position {p}: {int(bad.sum())} values off, "
+                               f"max |gpu - oracle| = {np.abs(gf - of).max():.3e}")
+
+
+def test_7b_trace_slice_joins_and_retires():
+    """The trace workload's first four requests (prompts of U[256, 4096] tokens, seed 1) on the
+    7B bf16 shape: requests 0 and 1 are admitted by one segmented prefill and decode two steps;
+    requests 2 and 3 join through a second segmented prefill and all four decode two steps;
+    request 0 retires and the other three decode one more step.  Checked by hand-off and
+    teacher forcing (module text)."""
+    ensure_built()
+    dev = torch.device("cuda:0")
+    shape = MISTRAL_7B
+    V = shape.vocab
+    reqs = trace_requests(64, 2.0, 256, 4096, 256.0, 4096, seed=1)[:4]
+    lens = [r.prompt_len for r in reqs]
+    prompts = [prompt_tokens(r, 1, V) for r in reqs]
+    w = DeviceWeights(shape, dev)
+    from continuous_batching_transformer_gb300 import binding as B
+    caps = [n + 8 for n in lens]
+    eng = Engine(w, arena_bytes=sum(B.slab_bytes(w.cfg, c) for c in caps), max_batch=8,
+                 max_prefill_tokens=max(lens[0] + lens[1], lens[2] + lens[3]))
+    slabs = [eng.kv_slab_alloc(c) for c in caps]
+    pre_logits, exports = {}, {}
+    dec_logits = {i: [] for i in range(4)}
+    dec_fed = {i: [] for i in range(4)}
+    tokbuf = torch.zeros(4, dtype=torch.int32, device=dev)
+    nxt = torch.zeros(4, dtype=torch.int32, device=dev)
+
+    def admit(idx):
+        lg = torch.empty((len(idx), V), dtype=torch.float32, device=dev)
+        nx = torch.empty(len(idx), dtype=torch.int32, device=dev)
+        toks = np.concatenate([prompts[i] for i in idx])
+        eng.prefill_segmented([slabs[i] for i in idx], [lens[i] for i in idx], to_dev(toks, dev),
+                              lg, nx)
+        host_lg, host_nx = lg.cpu().numpy(), nx.cpu().numpy()
+        for j, i in enumerate(idx):
+            pre_logits[i] = host_lg[j].copy()
+            tokbuf[i] = int(host_nx[j])
+            exports[i] = exported_kv(eng, slabs[i], lens[i])
+
+    def decode(live):
+        lg = torch.empty((len(live), V), dtype=torch.float32, device=dev)
+        feed = tokbuf[live].contiguous()
+        nx = torch.empty(len(live), dtype=torch.int32, device=dev)
+        eng.decode_step_batch([slabs[i] for i in live], feed, lg, nx)
+        host_lg, host_feed, host_nx = lg.cpu().numpy(), feed.cpu().numpy(), nx.cpu().numpy()
+        for j, i in enumerate(live):
+            dec_logits[i].append(host_lg[j].copy())
+            dec_fed[i].append(int(host_feed[j]))
+            tokbuf[i] = int(host_nx[j])
+
+    admit([0, 1])
+    for _ in range(2):
+        decode([0, 1])
+    admit([2, 3])
+    for _ in range(2):
+        decode([0, 1, 2, 3])
+    eng.retire([slabs[0]])
+    decode([1, 2, 3])
+    assert eng.device_error() == (0, 0)
+    assert [eng.position(s) for s in slabs[1:]] == [lens[1] + 5, lens[2] + 3, lens[3] + 3]
+    eng.close()
+    del w
+    release()
+
+    m = oracle_model(shape)
+    for i in range(4):
+        n = lens[i]
+        k, v = exports[i]
+        for p in sorted({0, 128, n // 2, n - 1}):
+            if p >= n:
+                continue
+            c = oracle.KVCache(shape, p + 1)
+            c.k[:, :, :p] = k[:, :, :p]
+            c.v[:, :, :p] = v[:, :, :p]
+            c.len = p
+            lg = oracle.forward(m, [c], np.zeros(1, np.int32), np.array([p], np.int32),
+                                prompts[i][p:p + 1], np.ones(1, np.int32))
+            check_kv_at(shape, k, v, c, p, f"request {i} (prompt {n})")
+            if p == n - 1:
+                check_logits(pre_logits[i][None], lg, TOL["bf16"], f"request {i} prefill logits")
+        # decode steps from the exported cache, teacher-forced on the tokens the GPU fed
+        steps = len(dec_fed[i])
+        c = oracle.KVCache(shape, n + steps + 1)
+        c.k[:, :, :n] = k
+        c.v[:, :, :n] = v
+        c.len = n
+        ref = oracle.forward(m, [c], np.zeros(steps, np.int32),
+                             np.arange(n, n + steps, dtype=np.int32),
+                             np.array(dec_fed[i], np.int32), np.ones(steps, np.int32))
+        for s in range(steps):
+            check_logits(dec_logits[i][s][None], ref[s:s + 1], TOL["bf16"],
+                         f"request {i} decode step {s}")
+        # the first decode step fed the GPU's own greedy token of the prefill
+        assert dec_fed[i][0] == int(np.argmax(pre_logits[i])), f"request {i}: first token"

@@ -150,3 +150,32 @@ def test_kv8_sizes_and_unsupported_calls():
     assert eng.position(a) == 10 and eng.position(b) == 0
     assert eng.device_error() == (0, 0)
     eng.close()
+
+
+G4 = ModelShape("kv8-g4", 2, 512, 8, 2, 128, 1024, 2048, 1e-5, 1e6, gain_sigma=0.1)
+G8 = ModelShape("kv8-g8", 2, 512, 16, 2, 64, 1024, 2048, 1e-5, 1e6, gain_sigma=0.1)
+GQA_Q4 = ModelShape("kv8-gqa-affine4", 2, 512, 4, 2, 128, 1024, 2048, 1e-5, 1e6, gain_sigma=0.1,
+                    weight_format="affine4")
+
+
+@pytest.mark.parametrize("shape", [G4, G8, GQA_Q4], ids=["g4-hd128", "g8-hd64", "affine4-g2"])
+def test_kv8_head_groups_and_staging_page_change(shape):
+    """4 and 8 q heads per kv head (the 7B shape's ratio and the widest), and 4-bit affine
+    weights with 8-bit KV; prompts of 126 and 127 positions so that the decode steps write
+    positions 126..130, crossing from the decode rows' first 128-position staging page into the
+    next, plus a short and a 300-position prompt."""
+    ensure_built()
+    w = DeviceWeights(shape, torch.device("cuda:0"))
+    om = oracle.OracleModel(shape)
+    lens = [126, 127, 7, 300]
+    caches = [oracle.KVCache(shape, n + 8, kv_bits=8) for n in lens]
+    toks = np.concatenate([seeded(n, 700 + r, shape.vocab) for r, n in enumerate(lens)])
+    refs = [oracle.prefill_segmented(om, caches, lens, toks)]
+    feeds = []
+    for _ in range(4):
+        feeds.append(np.array([oracle.argmax(x) for x in refs[-1]], np.int32))
+        refs.append(oracle.decode_step_batch(om, caches, feeds[-1]))
+    got, _ = run(w, shape, 8, lens, feeds)
+    tol = TOL["affine4" if shape.weight_format == "affine4" else "bf16"]
+    for k, (g, r) in enumerate(zip(got, refs)):
+        check_logits(g, r, tol, f"kv8 {shape.name} call {k}")

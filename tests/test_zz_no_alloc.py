@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
 from continuous_batching_transformer_gb300 import binding as B
 from continuous_batching_transformer_gb300.model import config_struct
@@ -81,6 +82,63 @@ def test_noalloc_head_matches_decode_step():
         outs.append(lg.clone())
     assert torch.equal(outs[0], outs[1])
     B.engine_destroy(eng)
+
+
+def oracle_head(hidden, fnorm, lm_bf16, fmt):
+    """The oracle's final RMSNorm, lm_head projection and greedy argmax of each row."""
+    g = fnorm.view(torch.int16).cpu().numpy().view(np.uint16)
+    w = lm_bf16.view(torch.int16).cpu().numpy().view(np.uint16)
+    h = np.stack([oracle.rmsnorm(r, g, TINY.rms_eps) for r in hidden.cpu().numpy()])
+    logits = oracle.project(oracle.LinearW(w, fmt, 64), h)
+    return logits, np.array([oracle.argmax(r) for r in logits], dtype=np.int32)
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "affine4"])
+def test_noalloc_head_matches_oracle(fmt):
+    """The head on its own against the oracle's RMSNorm + lm_head + argmax, bf16 weights and
+    4-bit affine weights (quantised on the device by cbt_quantize_affine4; the oracle quantises
+    the same bf16 values with its own quantiser), two calls in a row."""
+    ensure_built()
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    cfg = config_struct(TINY)
+    d, V, n = TINY.d_model, TINY.vocab, 7
+    lm = torch.empty((V, d), dtype=torch.bfloat16, device=dev)
+    synth.dev_normal_bf16(lm.data_ptr(), V * d, 13, synth.stream_weight(-1, synth.LM_HEAD))
+    fnorm = torch.empty(d, dtype=torch.bfloat16, device=dev)
+    synth.dev_normal_bf16(fnorm.data_ptr(), d, 13, synth.stream_weight(-1, synth.FINAL_NORM),
+                          mean=1.0, sigma=0.1)
+    hid = torch.empty((n, d), dtype=torch.bfloat16, device=dev)
+    synth.dev_normal_bf16(hid.data_ptr(), n * d, 13, synth.stream_weight(-1, synth.EMBED), sigma=1.0)
+    hidden = hid.float().contiguous()
+    keep = []
+    if fmt == "bf16":
+        lin = B.Linear(lm.data_ptr(), None, None)
+    else:
+        cfg.weight_format = B.WEIGHTS_AFFINE4
+        packed = torch.empty((V, d // 8), dtype=torch.int32, device=dev)
+        sc = torch.empty((V, d // 64), dtype=torch.bfloat16, device=dev)
+        bi = torch.empty_like(sc)
+        B.quantize_affine4(lm.data_ptr(), V, d, 64, packed.data_ptr(), sc.data_ptr(),
+                           bi.data_ptr(), stream.cuda_stream)
+        keep += [packed, sc, bi]
+        lin = B.Linear(packed.data_ptr(), sc.data_ptr(), bi.data_ptr())
+    torch.cuda.synchronize()
+    ref_logits, ref_next = oracle_head(hidden, fnorm, lm, fmt)
+    for call in range(2):
+        lg = torch.full((n, V), float("nan"), dtype=torch.float32, device=dev)
+        nx = torch.full((n,), -1, dtype=torch.int32, device=dev)
+        B.greedy_head_noalloc(cfg, hidden.data_ptr(), n, fnorm.data_ptr(), lin, lg.data_ptr(),
+                              nx.data_ptr(), stream.cuda_stream)
+        stream.synchronize()
+        got = lg.cpu().numpy()
+        err = float(np.abs(got - ref_logits).max())
+        assert err <= TOL[fmt], f"{fmt} call {call}: max |noalloc - oracle| = {err}"
+        for r in range(n):  # greedy tokens equal, except at a near-tie within the tolerance
+            g, o = int(nx[r]), int(ref_next[r])
+            if g != o:
+                assert ref_logits[r][o] - ref_logits[r][g] < TOL[fmt], (fmt, call, r, g, o)
 
 
 def test_noalloc_head_rejects_sizes_above_its_scratch():
