@@ -82,9 +82,9 @@ def _workload_by_name(name: str):
 
 def step_bytes(shape, ctx_lens, kv_bits: int = 16) -> float:
     """Algorithmic HBM bytes of one decode step: every linear weight once, each row's live KV
-    (positions 0..t_b after the append) once, the appended K/V, the logits written.  8-bit KV:
-    a code per element plus a bf16 scale and bias per 64 elements."""
-    kv_tok = shape.kv_bytes_per_token() * (1.0625 / 2 if kv_bits == 8 else 1.0)
+    (positions 0..t_b after the append) once, the appended K/V, the logits written.  Quantised
+    KV: kv_bits / 8 bytes of code per element plus a bf16 scale and bias per 64 elements."""
+    kv_tok = shape.kv_bytes_per_token() * ((kv_bits / 8 + 1 / 16) / 2 if kv_bits in (4, 8) else 1.0)
     return float(shape.weight_bytes_per_step() + sum((int(c) + 1) * kv_tok for c in ctx_lens)
                  + len(ctx_lens) * (kv_tok + 4 * shape.vocab))
 
@@ -141,7 +141,7 @@ def setup_decode(wl, device, extra_positions: int, page_tokens: int = 0, kv_bits
                  weights=None):
     """Engine + slabs for a decode workload: synthetic KV of each row loaded into its slab,
     each row's next token ready on the device.  page_tokens > 0: a paged engine; kv_bits = 8:
-    8-bit KV (the arena also holds the decode rows' staging and one import's bf16 slab).
+    quantised KV (the arena also holds the decode rows' staging and one import's bf16 slab).
     weights: DeviceWeights of the workload's shape to reuse (else they are drawn here)."""
     import numpy as np
     import torch
@@ -155,8 +155,8 @@ def setup_decode(wl, device, extra_positions: int, page_tokens: int = 0, kv_bits
     w = weights if weights is not None else DeviceWeights(shape, device)
     if page_tokens:
         arena = sum(B.slab_bytes(w.cfg, page_tokens) * (-(-c // page_tokens)) for c in caps)
-    elif kv_bits == 8:
-        arena = (sum(B.slab_bytes_kv8(w.cfg, c) for c in caps) + B.slab_bytes(w.cfg, max(ctx))
+    elif kv_bits in (4, 8):
+        arena = (sum(B.slab_bytes_kvq(w.cfg, c, kv_bits) for c in caps) + B.slab_bytes(w.cfg, max(ctx))
                  + len(ctx) * B.slab_bytes(w.cfg, 128))
     else:
         arena = sum(B.slab_bytes(w.cfg, c) for c in caps)
@@ -313,7 +313,7 @@ def gpu_arm(args, rank: int, world: int):
             "scaling": "weak",
             "vs_baseline": None,
             "dtype": ("bf16" if wl.shape.weight_format == "bf16" else "affine4-w/bf16")
-                     + ("/kv-affine8" if args.kv_bits == 8 else ""),
+                     + (f"/kv-affine{args.kv_bits}" if args.kv_bits in (4, 8) else ""),
             "data": "synthetic (seeded N(0,0.02) weights, seeded KV slabs and tokens)",
             "config": {"workload": wl.name, "model": wl.shape.name, "batch_per_gpu": Bsz,
                        "kv_page_tokens": args.page_tokens, "kv_bits": args.kv_bits,
@@ -437,7 +437,7 @@ def oracle_decode_sample(wl, max_steps: int, budget_s: float, kv_bits: int = 16)
     return {"value": len(ctx) * done / t_total, "unit": "tok/s", "cores": oracle.num_threads(),
             "kind": "oracle",
             "sample": f"{done} decode step(s) of all {len(ctx)} rows of {wl.name} "
-                      f"(full 32-layer model, {'8-bit' if kv_bits == 8 else 'bf16'} KV, "
+                      f"(full 32-layer model, {f'{kv_bits}-bit' if kv_bits in (4, 8) else 'bf16'} KV, "
                       f"{t_total:.1f} s of CPU time)"}, done, t_total
 
 
@@ -556,8 +556,8 @@ def main():
                     help="skip the B = 1..32 sweep (bf16 and 4-bit, ctx 2048) and the long-context "
                          "line that the default run appends as 'sweep'")
     ap.add_argument("--reference-budget", type=float, default=60.0)
-    ap.add_argument("--kv-bits", type=int, default=16, choices=(8, 16),
-                    help="KV precision: 16 (bf16) or 8 (8-bit affine, groups of 64)")
+    ap.add_argument("--kv-bits", type=int, default=16, choices=(4, 8, 16),
+                    help="KV precision: 16 (bf16), 8 or 4 (affine, groups of 64)")
     ap.add_argument("--page-tokens", type=int, default=0,
                     help="paged KV with pages of this many positions (a multiple of 128)")
     ap.add_argument("--layers", type=int, default=None,

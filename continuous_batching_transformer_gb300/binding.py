@@ -33,7 +33,8 @@ EXPORTS = ["cbt_status_str", "cbt_engine_create", "cbt_engine_destroy", "cbt_sla
            "cbt_decode_step_batch", "cbt_last_device_error", "cbt_engine_stats",
            "cbt_kernel_launches", "cbt_quantize_affine4", "cbt_engine_set_timing",
            "cbt_engine_timing", "cbt_greedy_head_noalloc", "cbt_kv_slab_copy_prefix",
-           "cbt_kv_slab_share_prefix", "cbt_slab_bytes_kv8", "cbt_quantize_kv8"]
+           "cbt_kv_slab_share_prefix", "cbt_slab_bytes_kv8", "cbt_quantize_kv8",
+           "cbt_slab_bytes_kvq", "cbt_quantize_kv"]
 KCLASS_PROJ, KCLASS_ATTN, KCLASS_OTHER = 0, 1, 2
 
 
@@ -101,6 +102,10 @@ def lib():
         L.cbt_slab_bytes_kv8.argtypes = [P(ModelConfig), c_int32]
         L.cbt_slab_bytes_kv8.restype = ctypes.c_size_t
         L.cbt_quantize_kv8.argtypes = [c_void, c_int32, c_int32, c_void, c_void, c_void, c_void]
+        L.cbt_slab_bytes_kvq.argtypes = [P(ModelConfig), c_int32, c_int32]
+        L.cbt_slab_bytes_kvq.restype = ctypes.c_size_t
+        L.cbt_quantize_kv.argtypes = [c_void, c_int32, c_int32, c_int32, c_void, c_void, c_void,
+                                      c_void]
         L.cbt_kv_slab_alloc.argtypes = [c_void, c_int32, P(c_int32)]
         L.cbt_kv_slab_free.argtypes = [c_void, c_int32]
         L.cbt_retire.argtypes = [c_void, c_void, c_int32]
@@ -125,7 +130,7 @@ def lib():
                                         P(ctypes.c_double)]
         for name in EXPORTS:
             if name not in ("cbt_status_str", "cbt_slab_bytes", "cbt_slab_bytes_kv8",
-                            "cbt_kernel_launches"):
+                            "cbt_slab_bytes_kvq", "cbt_kernel_launches"):
                 getattr(L, name).restype = c_int32
         _lib = L
     return _lib
@@ -163,6 +168,16 @@ def slab_bytes(cfg: ModelConfig, capacity: int) -> int:
 
 def slab_bytes_kv8(cfg: ModelConfig, capacity: int) -> int:
     return lib().cbt_slab_bytes_kv8(ctypes.byref(cfg), capacity)
+
+
+def slab_bytes_kvq(cfg: ModelConfig, capacity: int, bits: int) -> int:
+    return lib().cbt_slab_bytes_kvq(ctypes.byref(cfg), capacity, bits)
+
+
+def quantize_kv(x_ptr: int, rows: int, cols: int, bits: int, codes_ptr: int, scales_ptr: int,
+                biases_ptr: int, stream: int = 0) -> None:
+    _check(lib().cbt_quantize_kv(x_ptr, rows, cols, bits, codes_ptr, scales_ptr, biases_ptr,
+                                 stream), "cbt_quantize_kv")
 
 
 def quantize_kv8(x_ptr: int, rows: int, cols: int, codes_ptr: int, scales_ptr: int,

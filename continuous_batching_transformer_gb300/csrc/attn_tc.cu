@@ -313,7 +313,8 @@ __global__ void __launch_bounds__(160, kCtasPerSm)
 __global__ void __launch_bounds__(128)
     k_attn_merge(const float* __restrict__ part_o, const float2* __restrict__ part_ml,
                  const int* __restrict__ item_base, const int* __restrict__ item_count, int B,
-                 int n_heads, int n_kv_heads, int head_dim, uint16_t* act, int lo_rows) {
+                 int n_heads, int n_kv_heads, int head_dim, uint16_t* act, int lo_rows,
+                 float* out_f32) {
   pdl_wait();
   pdl_launch();
   __shared__ float wm[4], wl[4];
@@ -365,6 +366,10 @@ __global__ void __launch_bounds__(128)
     o = o / L;
     const int K = n_heads * head_dim;
     const int col = hq * head_dim + t;
+    if (out_f32) {
+      out_f32[(size_t)b * K + col] = o;
+      return;
+    }
     const uint16_t hi = f32_to_bf16(o);
     act[(size_t)b * K + col] = hi;
     if (lo_rows > 0) act[(size_t)(lo_rows + b) * K + col] = f32_to_bf16(o - bf16_to_f32(hi));
@@ -396,8 +401,11 @@ bool launch_attn_decode_tc(const CUtensorMap& tk, const CUtensorMap& tv, const A
   else if (a.head_dim == 64) rc = launch_decode<64>(tk, tv, a, grid, s);
   else return false;
   if (rc != cudaSuccess) return false;
-  rc = launch_pdl(k_attn_merge, dim3(a.n_heads, a.B), dim3(128), 0, s, a.part_o,
-                  a.part_ml, a.item_base, a.item_count, a.B, a.n_heads, a.n_kv_heads, a.head_dim,
-                  a.act, a.act_lo);
-  return rc == cudaSuccess;
+  return launch_attn_merge(a, s);
+}
+
+bool launch_attn_merge(const AttnDecodeArgs& a, cudaStream_t s) {
+  return launch_pdl(k_attn_merge, dim3(a.n_heads, a.B), dim3(128), 0, s, a.part_o, a.part_ml,
+                    a.item_base, a.item_count, a.B, a.n_heads, a.n_kv_heads, a.head_dim, a.act,
+                    a.act_lo, a.out_f32) == cudaSuccess;
 }

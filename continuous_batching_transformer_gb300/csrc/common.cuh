@@ -63,6 +63,8 @@ CBT_HD uint32_t sw128_offset(int row, int col, int group_stride) {
 struct AttnItem {
   int b, g, s0, s1;
   long long kbase;
+  int cap, p0;  // quantised KV: kbase is the byte offset of the slab or page, cap its layout
+                // capacity, p0 its first position
 };
 
 // Device error word: the first error wins (code, info).

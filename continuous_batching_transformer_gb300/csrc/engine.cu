@@ -37,6 +37,7 @@ struct Slab {
   int pos;
   int lcap;       // cap rounded up to 64: the layout's capacity
   std::vector<size_t> pages;  // paged engines: byte offset of each page, in position order
+  bool flat = false;  // a call's bf16 intermediate: one extent even on a paged engine
 };
 
 template <class T>
@@ -62,12 +63,16 @@ struct cbt_engine {
   int page = 0;            // kv_page_tokens: positions per page (0: contiguous slabs)
   size_t page_bytes = 0;
   std::unordered_map<size_t, int> extra_holders;  // shared pages: holders beyond the first
-  // 8-bit KV (kv_bits = 8): slabs hold codes; each decode row's new K/V is written in bf16 to
-  // its own one-page staging slab (stage_off + b * stage_bytes) and quantised from there; the
-  // per-call conversion records (decode rows, prefill segments, an import) on the device
+  // quantised KV (kv_bits = 8 or 4): slabs hold codes; each decode row's new K/V is written in
+  // bf16 to its own one-page staging slab (stage_off + b * stage_bytes) and quantised from there;
+  // the per-call conversion records (decode rows, prefill segments, an import) on the device
   int kv_bits = 16;
+  bool quant() const { return kv_bits != 16; }
+  bool q_codes = false;  // this forward pass: prefill tokens attend over codes (continuing slabs)
+  int q_jobs = 0, q_jobs_max_n = 0;
   size_t stage_off = 0, stage_bytes = 0;
   Kv8Job* kv8_jobs = nullptr;
+  size_t kv8_jobs_cap = 0;
   std::vector<Kv8Job> hjobs;
   // per prefill call: the page bases (QueryRow bases) of every paged segment, and each
   // token's offset into them (read by the prefill attention kernels)
@@ -207,17 +212,22 @@ extern "C" size_t cbt_slab_bytes(const cbt_model_config* c, int32_t cap) {
   return (b + kSlabAlign - 1) & ~(kSlabAlign - 1);
 }
 
-extern "C" size_t cbt_slab_bytes_kv8(const cbt_model_config* c, int32_t cap) {
-  if (!c || cap <= 0 || c->head_dim % 64) return 0;
-  size_t b = (size_t)c->n_layers * 2 * c->n_kv_heads * (size_t)kv8_block_bytes(round_cap(cap), c->head_dim);
+extern "C" size_t cbt_slab_bytes_kvq(const cbt_model_config* c, int32_t cap, int32_t bits) {
+  if (!c || cap <= 0 || c->head_dim % 64 || (bits != 8 && bits != 4)) return 0;
+  size_t b = (size_t)c->n_layers * 2 * c->n_kv_heads *
+             (size_t)kvq_block_bytes(round_cap(cap), c->head_dim, bits);
   return (b + kSlabAlign - 1) & ~(kSlabAlign - 1);
+}
+
+extern "C" size_t cbt_slab_bytes_kv8(const cbt_model_config* c, int32_t cap) {
+  return cbt_slab_bytes_kvq(c, cap, 8);
 }
 
 static bool take_extent(cbt_engine* e, size_t need, size_t* off_out);
 
 // bytes of one of the engine's slabs
 static size_t slab_bytes(const cbt_engine* e, int cap) {
-  return e->kv_bits == 8 ? cbt_slab_bytes_kv8(&e->cfg, cap) : cbt_slab_bytes(&e->cfg, cap);
+  return e->quant() ? cbt_slab_bytes_kvq(&e->cfg, cap, e->kv_bits) : cbt_slab_bytes(&e->cfg, cap);
 }
 
 extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_weights* w,
@@ -238,11 +248,12 @@ extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_w
   if (c.d_model % 256 || qd % 256 || c.d_ff % 256) return CBT_ERR_UNSUPPORTED;
   if (p->max_batch <= 0 || p->max_prefill_tokens <= 0 || p->kv_arena_bytes < kSlabAlign ||
       (reinterpret_cast<uintptr_t>(p->kv_arena) & 255) || p->kv_page_tokens < 0 ||
-      p->kv_page_tokens % 128 || (p->kv_bits != 0 && p->kv_bits != 16 && p->kv_bits != 8))
+      p->kv_page_tokens % 128 ||
+      (p->kv_bits != 0 && p->kv_bits != 16 && p->kv_bits != 8 && p->kv_bits != 4))
     return CBT_ERR_INVALID;
-  if (p->kv_bits == 8 && p->kv_page_tokens) return CBT_ERR_UNSUPPORTED;
-  // the 8-bit decode attention is built for 1, 2, 4 or 8 q heads per kv head
-  if (p->kv_bits == 8 && c.n_heads / c.n_kv_heads != 1 && c.n_heads / c.n_kv_heads != 2 &&
+  const bool qkv = p->kv_bits == 8 || p->kv_bits == 4;
+  // the quantised-KV decode attention is built for 1, 2, 4 or 8 q heads per kv head
+  if (qkv && c.n_heads / c.n_kv_heads != 1 && c.n_heads / c.n_kv_heads != 2 &&
       c.n_heads / c.n_kv_heads != 4 && c.n_heads / c.n_kv_heads != 8)
     return CBT_ERR_UNSUPPORTED;
   if (!linear_ok(w->lm_head, c.weight_format)) return CBT_ERR_NULL;
@@ -264,9 +275,9 @@ extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_w
   e->stream = static_cast<cudaStream_t>(p->stream);
   e->free_ext[0] = p->kv_arena_bytes & ~(kSlabAlign - 1);
   e->page = p->kv_page_tokens;
-  e->page_bytes = e->page ? cbt_slab_bytes(&c, e->page) : 0;
-  e->kv_bits = p->kv_bits == 8 ? 8 : 16;
-  if (e->kv_bits == 8) {  // the decode rows' staging slabs, one 128-position page each
+  e->kv_bits = qkv ? p->kv_bits : 16;
+  e->page_bytes = e->page ? slab_bytes(e, e->page) : 0;
+  if (e->quant()) {  // the decode rows' staging slabs, one 128-position page each
     e->stage_bytes = cbt_slab_bytes(&c, 128);
     size_t off = 0;
     if (!take_extent(e, (size_t)p->max_batch * e->stage_bytes, &off)) {
@@ -304,7 +315,10 @@ extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_w
   chk(dmalloc(&e->last_idx, (size_t)p->max_batch, &tot));
   chk(dmalloc(&e->rows, (size_t)T, &tot));
   chk(dmalloc(&e->err, 2, &tot));
-  if (e->kv_bits == 8) chk(dmalloc(&e->kv8_jobs, (size_t)p->max_batch, &tot));
+  if (e->quant()) {
+    e->kv8_jobs_cap = (size_t)std::max(p->max_batch, 64);
+    chk(dmalloc(&e->kv8_jobs, e->kv8_jobs_cap, &tot));
+  }
   if (rc == cudaSuccess) rc = cudaMemsetAsync(e->err, 0, 2 * sizeof(int), e->stream);
   bool maps_ok = true;
   const bool bf16w = c.weight_format == CBT_WEIGHTS_BF16;
@@ -408,7 +422,7 @@ extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_w
     e->use_tc = maps_ok && c.d_ff % 64 == 0;
   }
   if (rc == cudaSuccess) rc = cudaStreamSynchronize(e->stream);
-  if (rc == cudaSuccess && maps_ok && e->kv_bits == 8 && !e->use_tc) maps_ok = false;
+  if (rc == cudaSuccess && maps_ok && e->quant() && !e->use_tc) maps_ok = false;
   if (rc != cudaSuccess || !maps_ok) {
     free_scratch(e);
     delete e;
@@ -452,12 +466,26 @@ static void give_extent(cbt_engine* e, size_t off, size_t bytes);
 // The QueryRow base and capacity of the slab, or the page, that holds position pos: a page
 // holding positions [s, s + page) at element offset o has base o - s * head_dim, so the
 // kernels' index helpers take global positions.
+static bool paged(const cbt_engine* e, const Slab& sl) { return e->page && !sl.flat; }
+
 static long long row_base(const cbt_engine* e, const Slab& sl, int pos) {
-  if (!e->page) return (long long)(sl.offset / 2);
+  if (!paged(e, sl)) return (long long)(sl.offset / 2);
   const int pg = pos / e->page;
   return (long long)(sl.pages[pg] / 2) - (long long)pg * e->page * e->cfg.head_dim;
 }
-static int row_cap(const cbt_engine* e, const Slab& sl) { return e->page ? e->page : sl.lcap; }
+static int row_cap(const cbt_engine* e, const Slab& sl) { return paged(e, sl) ? e->page : sl.lcap; }
+
+// Quantised KV: the slab or page holding position pos (byte offset, layout capacity, first
+// position)
+struct QLoc {
+  long long off;
+  int cap, p0;
+};
+static QLoc qloc(const cbt_engine* e, const Slab& sl, int pos) {
+  if (!paged(e, sl)) return QLoc{(long long)sl.offset, sl.lcap, 0};
+  const int pg = pos / e->page;
+  return QLoc{(long long)sl.pages[pg], e->page, pg * e->page};
+}
 
 // pages obtainable from the free list (in a paged engine every extent taken is one page, so
 // each free extent is a run of page slots, the last one possibly followed by a remainder)
@@ -495,6 +523,7 @@ static cbt_status prepare_writes(cbt_engine* e, const std::vector<PageWrite>& wr
   std::unordered_map<size_t, int> copied;
   for (const PageWrite& w : writes) {
     const Slab& sl = e->slabs[w.id];
+    if (sl.flat) continue;
     const long long have = (long long)sl.pages.size(), want = (w.hi + P - 1) / P;
     if (want > have) need += (size_t)(want - have);
     for (long long pg = w.lo / P; w.lo < w.hi && pg < std::min(have, want); ++pg) {
@@ -509,6 +538,7 @@ static cbt_status prepare_writes(cbt_engine* e, const std::vector<PageWrite>& wr
   char* arena = static_cast<char*>(e->p.kv_arena);
   for (const PageWrite& w : writes) {
     Slab& sl = e->slabs[w.id];
+    if (sl.flat) continue;
     const long long have = (long long)sl.pages.size(), want = (w.hi + P - 1) / P;
     for (long long pg = w.lo / P; w.lo < w.hi && pg < std::min(have, want); ++pg) {
       if (!e->extra_holders.count(sl.pages[pg])) continue;
@@ -602,14 +632,17 @@ extern "C" cbt_status cbt_kv_slab_position(cbt_engine* e, int32_t id, int32_t* p
   return CBT_OK;
 }
 
-// ---- 8-bit KV: bf16 intermediates and their conversion ---------------------------------------
-// A bf16 slab of capacity cap for a call's intermediate K/V (0 if the arena has no room).
+// ---- quantised KV: bf16 intermediates and their conversion ------------------------------------
+// A bf16 slab of capacity cap for a call's intermediate K/V, one extent of the arena even on a
+// paged engine (0 if the arena has no room).
 static int temp_bf16_slab(cbt_engine* e, int cap) {
   const size_t need = cbt_slab_bytes(&e->cfg, cap);
   size_t off = 0;
   if (!take_extent(e, need, &off)) return 0;
   const int sid = e->next_id++;
-  e->slabs[sid] = Slab{off, need, cap, 0, round_cap(cap), {}};
+  Slab t{off, need, cap, 0, round_cap(cap), {}};
+  t.flat = true;
+  e->slabs[sid] = t;
   return sid;
 }
 
@@ -620,31 +653,115 @@ static void drop_temp(cbt_engine* e, int sid) {
   e->slabs.erase(it);
 }
 
-// Queue the quantisation of e->hjobs (every layer) into their 8-bit slabs.
+// Conversion records for positions [t0, t0 + n) of a bf16 source (QueryRow base and capacity)
+// into quantised slab dst: one record per page the positions touch (one for a slab).
+static void add_jobs(cbt_engine* e, long long src_base, int src_cap, int t0, int n, const Slab& dst) {
+  int p = t0;
+  while (p < t0 + n) {
+    const QLoc q = qloc(e, dst, p);
+    const int end = paged(e, dst) ? std::min(t0 + n, q.p0 + q.cap) : t0 + n;
+    e->hjobs.push_back(Kv8Job{src_base, src_cap, p, end - p, q.cap, q.off, q.p0});
+    p = end;
+  }
+}
+
+static void drop_graphs(cbt_engine* e);
+
+// Copy e->hjobs to the device (growing the buffer after the work that may still read it).
+static cudaError_t upload_jobs(cbt_engine* e) {
+  cudaError_t rc = cudaSuccess;
+  if (e->hjobs.size() > e->kv8_jobs_cap) {
+    rc = cudaStreamSynchronize(e->stream);
+    drop_graphs(e);  // captured steps hold the old buffer address
+    cudaFree(e->kv8_jobs);
+    e->kv8_jobs = nullptr;
+    e->kv8_jobs_cap = 0;
+    const size_t cap = std::max(e->hjobs.size(), 2 * e->kv8_jobs_cap);
+    if (rc == cudaSuccess) rc = cudaMalloc(reinterpret_cast<void**>(&e->kv8_jobs), cap * sizeof(Kv8Job));
+    if (rc != cudaSuccess) return rc;
+    e->kv8_jobs_cap = cap;
+  }
+  e->q_jobs = (int)e->hjobs.size();
+  e->q_jobs_max_n = 0;
+  for (const Kv8Job& j : e->hjobs) e->q_jobs_max_n = std::max(e->q_jobs_max_n, j.n);
+  if (e->hjobs.empty()) return cudaSuccess;
+  return cudaMemcpyAsync(e->kv8_jobs, e->hjobs.data(), sizeof(Kv8Job) * e->hjobs.size(),
+                         cudaMemcpyHostToDevice, e->stream);
+}
+
+// Queue the quantisation of e->hjobs (every layer) into their slabs.
 static cudaError_t convert_jobs(cbt_engine* e) {
-  int max_n = 0;
-  for (const Kv8Job& j : e->hjobs) max_n = std::max(max_n, j.n);
-  cudaError_t rc = cudaMemcpyAsync(e->kv8_jobs, e->hjobs.data(), sizeof(Kv8Job) * e->hjobs.size(),
-                                   cudaMemcpyHostToDevice, e->stream);
+  cudaError_t rc = upload_jobs(e);
   if (rc != cudaSuccess) return rc;
-  launch_kv8_convert(e->kv8_jobs, (int)e->hjobs.size(), max_n, 0, e->cfg.n_layers,
-                     e->cfg.n_kv_heads, e->cfg.head_dim, static_cast<uint8_t*>(e->p.kv_arena),
-                     e->stream);
-  return cudaGetLastError();
+  if (!launch_kvq_convert(e->kv8_jobs, e->q_jobs, e->q_jobs_max_n, 0, e->cfg.n_layers,
+                          e->cfg.n_kv_heads, e->cfg.head_dim, e->kv_bits,
+                          static_cast<uint8_t*>(e->p.kv_arena), e->stream))
+    return cudaErrorLaunchFailure;
+  return cudaSuccess;
 }
 
 static cbt_status slab_copy_bf16(cbt_engine* e, int32_t id, void* k, void* v, int32_t n,
                                  int32_t on_host, bool to_slab);
+static cudaError_t upload_page_tables(cbt_engine* e);
 
-// Import into an 8-bit slab: the plain K/V go to a bf16 intermediate slab, which is quantised.
+// Export of a quantised slab: every position's K and V as bf16 (scale * code + bias in double,
+// rounded to fp32, then to bf16), layer by layer through the device.
+static cbt_status export_quant(cbt_engine* e, const Slab& s, void* k, void* v, int32_t n,
+                               int32_t on_host) {
+  const cbt_model_config& c = e->cfg;
+  const size_t layer_elems = (size_t)c.n_kv_heads * n * c.head_dim;
+  cudaError_t rc = cudaSuccess;
+  if (on_host && e->stage_elems < 2 * layer_elems) {  // device staging of one layer's K and V
+    rc = cudaStreamSynchronize(e->stream);
+    if (e->stage) cudaFree(e->stage);
+    e->stage = nullptr;
+    e->stage_elems = 0;
+    if (rc == cudaSuccess) rc = cudaMalloc(reinterpret_cast<void**>(&e->stage), 4 * layer_elems);
+    if (rc != cudaSuccess) return CBT_ERR_CUDA;
+    e->stage_elems = 2 * layer_elems;
+  }
+  e->hpagetab.clear();
+  if (paged(e, s))
+    for (size_t off : s.pages) e->hpagetab.push_back((long long)off);
+  else
+    e->hpagetab.push_back((long long)s.offset);
+  e->htok_pages.clear();
+  rc = upload_page_tables(e);
+  const int cap = paged(e, s) ? e->page : s.lcap;
+  for (int l = 0; l < c.n_layers && rc == cudaSuccess; ++l) {
+    uint16_t* ku = static_cast<uint16_t*>(k) + (size_t)l * layer_elems;
+    uint16_t* vu = static_cast<uint16_t*>(v) + (size_t)l * layer_elems;
+    uint16_t* kd = on_host ? e->stage : ku;
+    uint16_t* vd = on_host ? e->stage + layer_elems : vu;
+    if (!launch_kvq_export(static_cast<const uint8_t*>(e->p.kv_arena), e->pagetab, cap, l,
+                           c.n_kv_heads, c.head_dim, n, e->kv_bits, kd, vd, e->stream)) {
+      rc = cudaErrorLaunchFailure;
+      break;
+    }
+    if (on_host) {
+      rc = cudaMemcpyAsync(ku, kd, layer_elems * 2, cudaMemcpyDeviceToHost, e->stream);
+      if (rc == cudaSuccess)
+        rc = cudaMemcpyAsync(vu, vd, layer_elems * 2, cudaMemcpyDeviceToHost, e->stream);
+      if (rc == cudaSuccess) rc = cudaStreamSynchronize(e->stream);  // the staging is reused
+    }
+  }
+  return rc == cudaSuccess ? CBT_OK : CBT_ERR_CUDA;
+}
+
+// Import into a quantised slab: the plain K/V go to a bf16 intermediate slab, which is
+// quantised; export dequantises (export_quant).
 static cbt_status slab_copy(cbt_engine* e, int32_t id, void* k, void* v, int32_t n, int32_t on_host,
                             bool to_slab) {
   if (!e || !k || !v) return CBT_ERR_NULL;
-  if (e->kv_bits != 8) return slab_copy_bf16(e, id, k, v, n, on_host, to_slab);
+  if (!e->quant()) return slab_copy_bf16(e, id, k, v, n, on_host, to_slab);
   auto it = e->slabs.find(id);
   if (it == e->slabs.end()) return CBT_ERR_BAD_SLAB;
-  if (!to_slab) return CBT_ERR_UNSUPPORTED;
   if (n < 0) return CBT_ERR_INVALID;
+  if (!to_slab) {
+    if (n > it->second.pos) return CBT_ERR_CAPACITY;
+    if (n == 0) return CBT_OK;
+    return export_quant(e, it->second, k, v, n, on_host);
+  }
   if (n > it->second.cap) return CBT_ERR_CAPACITY;
   if (n == 0) {
     it->second.pos = 0;
@@ -652,11 +769,12 @@ static cbt_status slab_copy(cbt_engine* e, int32_t id, void* k, void* v, int32_t
   }
   const int tmp = temp_bf16_slab(e, n);
   if (!tmp) return CBT_ERR_POOL_EXHAUSTED;
-  cbt_status st = slab_copy_bf16(e, tmp, k, v, n, on_host, true);
+  cbt_status st = prepare_writes(e, {{id, 0, (long long)n}});
+  if (st == CBT_OK) st = slab_copy_bf16(e, tmp, k, v, n, on_host, true);
   if (st == CBT_OK) {
     const Slab& t = e->slabs[tmp];
-    Slab& d = e->slabs[id];
-    e->hjobs.assign(1, Kv8Job{(long long)(t.offset / 2), t.lcap, 0, n, d.lcap, (long long)d.offset});
+    e->hjobs.clear();
+    add_jobs(e, (long long)(t.offset / 2), t.lcap, 0, n, e->slabs[id]);
     if (convert_jobs(e) != cudaSuccess) st = CBT_ERR_CUDA;
   }
   drop_temp(e, tmp);
@@ -692,15 +810,16 @@ static cbt_status slab_copy_bf16(cbt_engine* e, int32_t id, void* k, void* v, in
   }
   // runs of positions: the whole slab, or page by page
   const int P = row_cap(e, s);
-  const int runs = e->page ? (n + P - 1) / P : (n > 0 ? 1 : 0);
+  const bool pg = paged(e, s);
+  const int runs = pg ? (n + P - 1) / P : (n > 0 ? 1 : 0);
   for (int l = 0; l < c.n_layers && rc == cudaSuccess && n > 0; ++l) {
     uint16_t* vu = static_cast<uint16_t*>(v) + (size_t)l * layer_elems;
     uint16_t* plain = on_host ? e->stage : vu;
     if (on_host && to_slab)
       rc = cudaMemcpyAsync(plain, vu, layer_elems * 2, cudaMemcpyHostToDevice, e->stream);
     for (int r = 0; r < runs && rc == cudaSuccess; ++r) {
-      const int a = e->page ? r * P : 0, cnt = e->page ? std::min(n, a + P) - a : n;
-      char* blk = static_cast<char*>(e->p.kv_arena) + (e->page ? s.pages[r] : s.offset);
+      const int a = pg ? r * P : 0, cnt = pg ? std::min(n, a + P) - a : n;
+      char* blk = static_cast<char*>(e->p.kv_arena) + (pg ? s.pages[r] : s.offset);
       // K: rows [a, a + cnt) of each kv head's [position][head_dim] block
       char* user = static_cast<char*>(k) + ((size_t)l * c.n_kv_heads * n + a) * row;
       char* slab = blk + ((size_t)l * 2) * c.n_kv_heads * (size_t)P * row;
@@ -735,10 +854,37 @@ extern "C" cbt_status cbt_kv_slab_export(cbt_engine* e, int32_t id, void* k, voi
   return slab_copy(e, id, k, v, n, on_host, false);
 }
 
+// Quantised slabs: each (layer, K|V, kv head) block holds codes, scales and biases position by
+// position, so the prefix is three strided copies per run of positions (the slab, or a page).
+static cbt_status copy_prefix_quant(cbt_engine* e, const Slab& src, const Slab& dst, int n) {
+  const cbt_model_config& c = e->cfg;
+  const int hd = c.head_dim, bits = e->kv_bits, row = hd * bits / 8, ng = hd / 64;
+  const size_t blocks = (size_t)c.n_layers * 2 * c.n_kv_heads;
+  char* arena = static_cast<char*>(e->p.kv_arena);
+  for (int p = 0; p < n;) {
+    const QLoc a = qloc(e, src, p), b = qloc(e, dst, p);
+    const int end = std::min(n, std::min(a.p0 + a.cap, b.p0 + b.cap));
+    const size_t m = (size_t)(end - p);
+    const size_t la = (size_t)(p - a.p0), lb = (size_t)(p - b.p0);
+    const size_t pa = (size_t)kvq_block_bytes(a.cap, hd, bits), pb = (size_t)kvq_block_bytes(b.cap, hd, bits);
+    // codes, then scales, then biases of positions [p, end)
+    const size_t sa[3] = {la * row, (size_t)a.cap * row + la * ng * 2,
+                          (size_t)a.cap * row + (size_t)a.cap * ng * 2 + la * ng * 2};
+    const size_t sb[3] = {lb * row, (size_t)b.cap * row + lb * ng * 2,
+                          (size_t)b.cap * row + (size_t)b.cap * ng * 2 + lb * ng * 2};
+    const size_t w[3] = {m * row, m * ng * 2, m * ng * 2};
+    for (int r = 0; r < 3; ++r)
+      if (cudaMemcpy2DAsync(arena + b.off + sb[r], pb, arena + a.off + sa[r], pa, w[r], blocks,
+                            cudaMemcpyDeviceToDevice, e->stream) != cudaSuccess)
+        return CBT_ERR_CUDA;
+    p = end;
+  }
+  return CBT_OK;
+}
+
 extern "C" cbt_status cbt_kv_slab_copy_prefix(cbt_engine* e, int32_t src_id, int32_t dst_id,
                                               int32_t n) {
   if (!e) return CBT_ERR_NULL;
-  if (e->kv_bits == 8) return CBT_ERR_UNSUPPORTED;
   auto si = e->slabs.find(src_id), di = e->slabs.find(dst_id);
   if (si == e->slabs.end() || di == e->slabs.end()) return CBT_ERR_BAD_SLAB;
   if (src_id == dst_id || n < 0) return CBT_ERR_INVALID;
@@ -747,6 +893,11 @@ extern "C" cbt_status cbt_kv_slab_copy_prefix(cbt_engine* e, int32_t src_id, int
   if (n > src.pos || n > dst.cap) return CBT_ERR_CAPACITY;
   const cbt_status st = prepare_writes(e, {{dst_id, 0, (long long)n}});
   if (st != CBT_OK) return st;
+  if (e->quant()) {
+    const cbt_status qs = copy_prefix_quant(e, src, dst, n);
+    if (qs == CBT_OK) dst.pos = n;
+    return qs;
+  }
   // every (layer, K|V, kv head) block is a run of positions at the same place in both slabs (or
   // pages): one strided copy per run, of whole 64-position groups (a V block keeps each group
   // of 64 positions transposed; capacities and page sizes are multiples of 64, so the groups
@@ -970,16 +1121,17 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
   cudaStream_t s = e->stream;
   const int d = c.d_model, qd = e->qd(), kvd = e->kvd(), F = c.d_ff;
   uint16_t* arena = static_cast<uint16_t*>(e->p.kv_arena);
-  const bool kv8 = e->kv_bits == 8;
-  // K and V read per key: bf16, or 8-bit codes plus a bf16 scale and bias per 64
-  const double attn_bytes = 2.0 * (kv8 ? 1.0625 : 2.0) * kvd * (double)total_keys
+  const bool quant = e->quant();
+  // K and V read per element: bf16, or bits / 8 bytes of codes plus a bf16 scale and bias per 64
+  const double kv_el = quant ? e->kv_bits / 8.0 + 1.0 / 16.0 : 2.0;
+  const double attn_bytes = 2.0 * kv_el * kvd * (double)total_keys
                             + 4.0 * n * (qd + 2 * kvd)              // q, k, v in
                             + 2.0 * 2.0 * n * kvd + 4.0 * n * qd;   // K/V appended, o out
   // 4-bit weights go through the tensor cores for up to 32 rows (the decode projections)
   const bool tcp = e->use_tc && (e->cfg.weight_format == CBT_WEIGHTS_BF16 || n <= 32);
   // decode on the tensor cores folds every RMSNorm into the projection that consumes it:
   // the residual-add epilogues and the embedding leave per-tile sums of squares in e->ss
-  const bool fused = tcp && !gather && n <= 32 && !kv8;
+  const bool fused = tcp && !gather && n <= 32;
   const int lo = tc_lo_rows(e, n), lo_out = tc_lo_rows(e, n_out);
   bool ok = true;
   int t = tbegin(e, CBT_KCLASS_OTHER);
@@ -1011,31 +1163,50 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
     const bool tc_prefill = tcp && gather && e->pf_n > 0;
     if (!fused)
       launch_rope_append(e->qkv, e->rows, n, l, c.n_heads, c.n_kv_heads, c.head_dim, e->cosv,
-                         e->sinv, arena, (tcp && !gather && !kv8) ? e->qtile : nullptr,
+                         e->sinv, arena, (!gather && (tcp || quant)) ? e->qtile : nullptr,
                          tc_prefill ? e->qb : nullptr, e->qb_rows, s);
-    if (kv8 && !gather) {
-      // 8-bit KV decode: the RoPE kernel above put each row's new K/V in its staging page;
-      // quantise them into the row's slab, then split attention over the codes
-      launch_kv8_convert(e->kv8_jobs, n, 1, l, 1, c.n_kv_heads, c.head_dim,
-                         static_cast<uint8_t*>(e->p.kv_arena), s);
-      Kv8AttnArgs a{};
-      a.qkv = e->qkv;
-      a.rows = e->kv8_jobs;
-      a.items = e->items;
-      a.n_items = e->item_meta + 2 * e->p.max_batch;
-      a.item_base = e->item_meta;
-      a.item_count = e->item_meta + e->p.max_batch;
-      a.arena = static_cast<const uint8_t*>(e->p.kv_arena);
-      a.B = n;
-      a.layer = l;
-      a.n_heads = c.n_heads;
-      a.n_kv_heads = c.n_kv_heads;
-      a.head_dim = c.head_dim;
-      a.part_o = e->att_o;
-      a.part_ml = e->att_ml;
-      a.o = e->o;
-      a.err = e->err;
-      ok &= launch_attn_decode_kv8(a, e->num_sms, s);
+    uint8_t* arena8 = static_cast<uint8_t*>(e->p.kv_arena);
+    if (quant && !gather) {
+      // quantised KV decode: each row's new K/V went to its staging page (the QKV epilogue, or
+      // the RoPE kernel above); quantise them into the row's slab, then split attention over
+      // the codes on the tensor cores and the merge into the O projection's operand
+      ok &= launch_kvq_convert(e->kv8_jobs, n, 1, l, 1, c.n_kv_heads, c.head_dim, e->kv_bits,
+                               arena8, s);
+      KvqAttnArgs qa{};
+      qa.qtile = e->qtile;
+      qa.rows = e->rows;
+      qa.items = e->items;
+      qa.n_items = e->item_meta + 2 * e->p.max_batch;
+      qa.arena = arena8;
+      qa.layer = l;
+      qa.n_heads = c.n_heads;
+      qa.n_kv_heads = c.n_kv_heads;
+      qa.head_dim = c.head_dim;
+      qa.part_o = e->att_o;
+      qa.part_ml = e->att_ml;
+      qa.err = e->err;
+      ok &= launch_attn_decode_q(qa, e->kv_bits, e->num_sms, s);
+      AttnDecodeArgs ma{};
+      ma.item_base = e->item_meta;
+      ma.item_count = e->item_meta + e->p.max_batch;
+      ma.B = n;
+      ma.n_heads = c.n_heads;
+      ma.n_kv_heads = c.n_kv_heads;
+      ma.head_dim = c.head_dim;
+      ma.part_o = e->att_o;
+      ma.part_ml = e->att_ml;
+      ma.act = e->act_o;
+      ma.act_lo = lo;
+      ma.out_f32 = tcp ? nullptr : e->o;  // the CUDA-core O projection reads fp32
+      ok &= launch_attn_merge(ma, s);
+    } else if (quant && e->q_codes) {
+      // prefill tokens continuing quantised slabs: their K/V (in a bf16 intermediate) are
+      // quantised first, then each token attends over the codes of [0, its position]
+      ok &= launch_kvq_convert(e->kv8_jobs, e->q_jobs, e->q_jobs_max_n, l, 1, c.n_kv_heads,
+                               c.head_dim, e->kv_bits, arena8, s);
+      ok &= launch_attn_prefill_q(e->qkv, e->rows, e->pagetab, e->tok_pages, e->tok_pages + n, n, l,
+                                  c.n_heads, c.n_kv_heads, c.head_dim, max_keys, e->kv_bits,
+                                  arena8, e->o, s);
       if (tcp) launch_f32_to_act(e->o, n, qd, e->act_o, lo, s);
     } else if (tcp && !gather) {  // decode: split-K flash decoding on the tensor cores
       AttnDecodeArgs a{};
@@ -1141,10 +1312,17 @@ static cudaError_t plan_decode_attention(cbt_engine* e, int B) {
     e->hitem_count[b] = splits;
     // an item's sub-chunks lie in one page (pages are multiples of 128 * kSubsPerItem keys)
     for (int g = 0; g < Hkv; ++g)
-      for (int sp = 0; sp < splits; ++sp)
-        e->hitems.push_back(AttnItem{b, g, sp * kSubsPerItem,
-                                     std::min(nsub, (sp + 1) * kSubsPerItem),
-                                     row_base(e, *e->hslab[b], sp * kSubsPerItem * 128)});
+      for (int sp = 0; sp < splits; ++sp) {
+        AttnItem it{b, g, sp * kSubsPerItem, std::min(nsub, (sp + 1) * kSubsPerItem),
+                    row_base(e, *e->hslab[b], sp * kSubsPerItem * 128), 0, 0};
+        if (e->quant()) {  // the quantised slab or page: byte offset, capacity, first position
+          const QLoc q = qloc(e, *e->hslab[b], sp * kSubsPerItem * 128);
+          it.kbase = q.off;
+          it.cap = q.cap;
+          it.p0 = q.p0;
+        }
+        e->hitems.push_back(it);
+      }
   }
   const size_t n = e->hitems.size();
   cudaError_t rc = cudaSuccess;
@@ -1241,13 +1419,14 @@ extern "C" cbt_status cbt_decode_step_batch(cbt_engine* e, const int32_t* ids, i
   e->hjobs.clear();
   for (int b = 0; b < B; ++b) {
     const Slab& sl = e->slabs[ids[b]];
-    if (e->kv_bits == 8) {
+    if (e->quant()) {
       // the new K/V go to row b's staging page (positions [s, s + 128) around pos), and from
-      // there into the 8-bit slab
+      // there into the quantised slab (or the page holding pos)
       const long long sb = (long long)((e->stage_off + (size_t)b * e->stage_bytes) / 2) -
                            (long long)(sl.pos / 128) * 128 * e->cfg.head_dim;
       e->hrows[b] = QueryRow{sb, sl.pos, 128};
-      e->hjobs.push_back(Kv8Job{sb, 128, sl.pos, 1, sl.lcap, (long long)sl.offset});
+      const QLoc q = qloc(e, sl, sl.pos);
+      e->hjobs.push_back(Kv8Job{sb, 128, sl.pos, 1, q.cap, q.off, q.p0});
     } else {
       e->hrows[b] = QueryRow{row_base(e, sl, sl.pos), sl.pos, row_cap(e, sl)};
     }
@@ -1257,7 +1436,7 @@ extern "C" cbt_status cbt_decode_step_batch(cbt_engine* e, const int32_t* ids, i
   }
   cudaError_t rc = cudaMemcpyAsync(e->rows, e->hrows.data(), sizeof(QueryRow) * B,
                                    cudaMemcpyHostToDevice, e->stream);
-  if (rc == cudaSuccess && e->kv_bits == 8)
+  if (rc == cudaSuccess && e->quant())
     rc = cudaMemcpyAsync(e->kv8_jobs, e->hjobs.data(), sizeof(Kv8Job) * B, cudaMemcpyHostToDevice,
                          e->stream);
   if (rc == cudaSuccess && e->page) {  // for the CUDA-core attention (rows above its limits)
@@ -1373,44 +1552,124 @@ static cudaError_t plan_prefill_attention(cbt_engine* e, const int32_t* ids, con
 static cbt_status prefill_impl(cbt_engine* e, const int32_t* ids, const int32_t* lens, int32_t K,
                                const int32_t* tokens, float* logits, int32_t* next_tokens);
 
-// 8-bit engines (the mlx-bun batching design's conversion point: a row prefills in bf16 and is
-// then converted): each segment is prefilled into a bf16 intermediate slab, then quantised
-// into its own slab.  Only fresh slabs (position 0).
-static cbt_status prefill_kv8(cbt_engine* e, const int32_t* ids, const int32_t* lens, int32_t K,
-                              const int32_t* tokens, float* logits, int32_t* next_tokens) {
+// Quantised engines.  A segment that starts a sequence (its slab at position 0) follows the
+// mlx-bun batching design's conversion point: it is prefilled in bf16 (a bf16 intermediate slab)
+// and its K/V are then quantised into its own slab.  A segment that continues a sequence (a
+// later chunk of its prompt) attends over codes, as every step after the first does: its K/V go
+// to a bf16 intermediate, are quantised into the slab layer by layer, and each token attends
+// over the codes of positions [0, its own].  Runs of consecutive segments of one kind are
+// separate passes (segments never see each other, so this changes no result).
+static cbt_status prefill_quant(cbt_engine* e, const int32_t* ids, const int32_t* lens, int32_t K,
+                                const int32_t* tokens, float* logits, int32_t* next_tokens) {
   if (K < 0) return CBT_ERR_INVALID;
   if (K == 0) return CBT_OK;
   if (!ids || !lens || !tokens) return CBT_ERR_NULL;
   if (K > e->p.max_batch) return CBT_ERR_BATCH;
   std::unordered_set<int> seen;
+  long long T = 0;
   for (int s = 0; s < K; ++s) {
     auto it = e->slabs.find(ids[s]);
     if (it == e->slabs.end()) return CBT_ERR_BAD_SLAB;
     if (!seen.insert(ids[s]).second) return CBT_ERR_DUP_SLAB;
     if (lens[s] <= 0) return CBT_ERR_INVALID;
     if ((long long)it->second.pos + lens[s] > it->second.cap) return CBT_ERR_CAPACITY;
-    if (it->second.pos != 0) return CBT_ERR_UNSUPPORTED;
+    T += lens[s];
   }
+  if (T > e->p.max_prefill_tokens) return CBT_ERR_TOKENS;
+  // every intermediate first, then the destination pages, so a call the arena cannot serve
+  // changes nothing
   std::vector<int32_t> tmp(K, 0);
   cbt_status st = CBT_OK;
+  std::vector<PageWrite> writes;
   for (int s = 0; s < K && st == CBT_OK; ++s) {
-    tmp[s] = temp_bf16_slab(e, lens[s]);
+    const Slab& d = e->slabs[ids[s]];
+    const int f64 = d.pos & ~63;  // the intermediate holds positions [f64, pos + len)
+    tmp[s] = temp_bf16_slab(e, d.pos + lens[s] - f64);
     if (!tmp[s]) st = CBT_ERR_POOL_EXHAUSTED;
+    writes.push_back({ids[s], d.pos, (long long)d.pos + lens[s]});
   }
-  if (st == CBT_OK) st = prefill_impl(e, tmp.data(), lens, K, tokens, logits, next_tokens);
-  if (st == CBT_OK) {
-    e->hjobs.clear();
-    for (int s = 0; s < K; ++s) {
-      const Slab& t = e->slabs[tmp[s]];
-      const Slab& d = e->slabs[ids[s]];
-      e->hjobs.push_back(Kv8Job{(long long)(t.offset / 2), t.lcap, 0, lens[s], d.lcap, (long long)d.offset});
+  if (st == CBT_OK) st = prepare_writes(e, writes);
+  if (st != CBT_OK) {
+    for (int s = 0; s < K; ++s)
+      if (tmp[s]) drop_temp(e, tmp[s]);
+    return st;
+  }
+  const int V = e->cfg.vocab, hd = e->cfg.head_dim;
+  long long tok0 = 0;
+  for (int r0 = 0; r0 < K && st == CBT_OK;) {
+    const bool fresh = e->slabs[ids[r0]].pos == 0;
+    int r1 = r0;
+    long long n_run = 0;
+    while (r1 < K && (e->slabs[ids[r1]].pos == 0) == fresh) n_run += lens[r1++];
+    const int32_t* run_tokens = tokens + tok0;
+    float* run_logits = logits ? logits + (size_t)r0 * V : nullptr;
+    int32_t* run_next = next_tokens ? next_tokens + r0 : nullptr;
+    if (fresh) {
+      st = prefill_impl(e, tmp.data() + r0, lens + r0, r1 - r0, run_tokens, run_logits, run_next);
+      if (st == CBT_OK) {
+        e->hjobs.clear();
+        for (int s = r0; s < r1; ++s) {
+          const Slab& t = e->slabs[tmp[s]];
+          add_jobs(e, (long long)(t.offset / 2), t.lcap, 0, lens[s], e->slabs[ids[s]]);
+        }
+        if (convert_jobs(e) != cudaSuccess) st = CBT_ERR_CUDA;
+      }
+    } else {
+      // rows: each token's bf16 intermediate (its QueryRow base maps positions from f64);
+      // conversion records per layer; page tables of the codes each token attends over
+      e->hjobs.clear();
+      e->hpagetab.clear();
+      e->htok_pages.assign(2 * n_run, 0);
+      long long total_keys = 0;
+      int max_keys = 0, g = 0;
+      for (int s = r0; s < r1; ++s) {
+        const Slab& d = e->slabs[ids[s]];
+        const Slab& t = e->slabs[tmp[s]];
+        const int f64 = d.pos & ~63;
+        const long long base = (long long)(t.offset / 2) - (long long)f64 * hd;
+        add_jobs(e, base, t.lcap, d.pos, lens[s], d);
+        const int first = (int)e->hpagetab.size();
+        if (paged(e, d))
+          for (size_t off : d.pages) e->hpagetab.push_back((long long)off);
+        else
+          e->hpagetab.push_back((long long)d.offset);
+        for (int j = 0; j < lens[s]; ++j, ++g) {
+          e->hrows[g] = QueryRow{base, d.pos + j, t.lcap};
+          e->htok_pages[g] = first;
+          e->htok_pages[n_run + g] = paged(e, d) ? e->page : d.lcap;
+        }
+        e->hidx[s - r0] = g - 1;
+        max_keys = std::max(max_keys, d.pos + lens[s]);
+        total_keys += (long long)lens[s] * d.pos + (long long)lens[s] * (lens[s] + 1) / 2;
+      }
+      cudaError_t rc = upload_jobs(e);
+      if (rc == cudaSuccess)
+        rc = cudaMemcpyAsync(e->rows, e->hrows.data(), sizeof(QueryRow) * n_run,
+                             cudaMemcpyHostToDevice, e->stream);
+      if (rc == cudaSuccess)
+        rc = cudaMemcpyAsync(e->last_idx, e->hidx.data(), sizeof(int32_t) * (r1 - r0),
+                             cudaMemcpyHostToDevice, e->stream);
+      if (rc == cudaSuccess) rc = upload_page_tables(e);
+      e->pf_n = 0;  // the codes are read by their own attention kernel
+      if (rc == cudaSuccess) {
+        e->q_codes = true;
+        rc = forward(e, (int)n_run, run_tokens, max_keys, total_keys, true, r1 - r0, run_logits,
+                     run_next);
+        e->q_codes = false;
+      }
+      if (rc != cudaSuccess) st = rc == cudaErrorNotSupported ? CBT_ERR_UNSUPPORTED : CBT_ERR_CUDA;
+      if (st == CBT_OK) {
+        e->prefill_tokens += n_run;
+        for (int s = r0; s < r1; ++s) e->slabs[ids[s]].pos += lens[s];
+      }
     }
-    if (convert_jobs(e) != cudaSuccess) st = CBT_ERR_CUDA;
+    if (st == CBT_OK && fresh)
+      for (int s = r0; s < r1; ++s) e->slabs[ids[s]].pos = lens[s];
+    tok0 += n_run;
+    r0 = r1;
   }
   for (int s = 0; s < K; ++s)
     if (tmp[s]) drop_temp(e, tmp[s]);
-  if (st == CBT_OK)
-    for (int s = 0; s < K; ++s) e->slabs[ids[s]].pos = lens[s];
   return st;
 }
 
@@ -1418,7 +1677,7 @@ extern "C" cbt_status cbt_prefill_segmented(cbt_engine* e, const int32_t* ids,
                                             const int32_t* lens, int32_t K, const int32_t* tokens,
                                             float* logits, int32_t* next_tokens) {
   if (!e) return CBT_ERR_NULL;
-  if (e->kv_bits == 8) return prefill_kv8(e, ids, lens, K, tokens, logits, next_tokens);
+  if (e->quant()) return prefill_quant(e, ids, lens, K, tokens, logits, next_tokens);
   return prefill_impl(e, ids, lens, K, tokens, logits, next_tokens);
 }
 
@@ -1457,12 +1716,12 @@ static cbt_status prefill_impl(cbt_engine* e, const int32_t* ids, const int32_t*
   for (int s = 0; s < K; ++s) {
     const Slab& sl = e->slabs[ids[s]];
     const int first = (int)e->hpagetab.size();
-    if (e->page)
+    if (paged(e, sl))
       for (size_t pg = 0; pg < sl.pages.size(); ++pg)
         e->hpagetab.push_back(row_base(e, sl, (int)pg * e->page));
     for (int j = 0; j < lens[s]; ++j, ++g) {
       e->hrows[g] = QueryRow{row_base(e, sl, sl.pos + j), sl.pos + j, row_cap(e, sl)};
-      if (e->page) e->htok_pages[g] = first;
+      if (paged(e, sl)) e->htok_pages[g] = first;
     }
     e->hidx[s] = g - 1;
   }
@@ -1513,17 +1772,24 @@ extern "C" int64_t cbt_kernel_launches(cbt_engine* e) {
   return kernel_launch_count();
 }
 
+extern "C" cbt_status cbt_quantize_kv(const void* x, int32_t rows, int32_t cols, int32_t bits,
+                                      void* codes, void* scales, void* biases, void* stream) {
+  if (!x || !codes || !scales || !biases) return CBT_ERR_NULL;
+  if (bits != 8 && bits != 4) return CBT_ERR_INVALID;
+  if (rows < 0 || cols <= 0 || cols % 64 || (reinterpret_cast<uintptr_t>(x) & 3) ||
+      (bits == 8 && (reinterpret_cast<uintptr_t>(codes) & 1)) ||
+      (reinterpret_cast<uintptr_t>(scales) & 1) || (reinterpret_cast<uintptr_t>(biases) & 1))
+    return CBT_ERR_INVALID;
+  return launch_quantize_kv(static_cast<const uint16_t*>(x), rows, cols, bits,
+                            static_cast<uint8_t*>(codes), static_cast<uint16_t*>(scales),
+                            static_cast<uint16_t*>(biases), static_cast<cudaStream_t>(stream))
+             ? CBT_OK
+             : CBT_ERR_CUDA;
+}
+
 extern "C" cbt_status cbt_quantize_kv8(const void* x, int32_t rows, int32_t cols, void* codes,
                                        void* scales, void* biases, void* stream) {
-  if (!x || !codes || !scales || !biases) return CBT_ERR_NULL;
-  if (rows < 0 || cols <= 0 || cols % 64 || (reinterpret_cast<uintptr_t>(x) & 3) ||
-      (reinterpret_cast<uintptr_t>(codes) & 1) || (reinterpret_cast<uintptr_t>(scales) & 1) ||
-      (reinterpret_cast<uintptr_t>(biases) & 1))
-    return CBT_ERR_INVALID;
-  launch_quantize_kv8(static_cast<const uint16_t*>(x), rows, cols, static_cast<uint8_t*>(codes),
-                      static_cast<uint16_t*>(scales), static_cast<uint16_t*>(biases),
-                      static_cast<cudaStream_t>(stream));
-  return cudaGetLastError() == cudaSuccess ? CBT_OK : CBT_ERR_CUDA;
+  return cbt_quantize_kv(x, rows, cols, 8, codes, scales, biases, stream);
 }
 
 extern "C" cbt_status cbt_quantize_affine4(const void* w, int32_t rows, int32_t cols, int32_t group,

@@ -144,44 +144,59 @@ struct AttnDecodeArgs {
   uint16_t* act;             // attention output as the O projection's bf16 operand
   int act_lo;                // lo rows offset (0: plain bf16)
   int* err;
+  float* out_f32;            // if set, the merge writes fp32 [B][n_heads * head_dim] here instead
 };
 // tk: the KV arena as [rows][head_dim] bf16, box {64, 128}; tv: as [rows][64], box {64, head_dim}
 bool launch_attn_decode_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnDecodeArgs& a,
                            int num_sms, cudaStream_t s);
-// ---- 8-bit affine KV (kv8.cu) ------------------------------------------------------------------
-// An 8-bit slab block (layer, K|V, kv head) of capacity cap: codes [cap][head_dim] uint8, then
-// bf16 scales and bf16 biases [cap][head_dim / 64]
-CBT_HD long long kv8_block_bytes(int cap, int head_dim) {
-  return (long long)cap * (head_dim + head_dim / 16);
+// ---- affine KV of 8 or 4 bits (kvq.cu) ---------------------------------------------------------
+// A quantised slab (or page) block (layer, K|V, kv head) of capacity cap: codes
+// [cap][head_dim * bits / 8] uint8 (4 bits: element 2i in the low nibble of byte i), then bf16
+// scales and bf16 biases [cap][head_dim / 64]
+CBT_HD long long kvq_block_bytes(int cap, int head_dim, int bits) {
+  return (long long)cap * (head_dim * bits / 8 + head_dim / 16);
 }
 // Positions [t0, t0 + n) of a bf16 slab (or a staging page: a QueryRow base and capacity) to
-// be quantised into the 8-bit slab at byte offset dst (layout capacity dst_cap).  The decode
-// attention reads the same records as its rows: the 8-bit slab and t0 = the row's position.
+// be quantised into the quantised slab or page at byte offset dst (layout capacity dst_cap),
+// whose first position is dst_p0 (0 for a contiguous slab).
 struct Kv8Job {
   long long src_base;
   int src_cap, t0, n, dst_cap;
   long long dst;
+  int dst_p0;
 };
-void launch_quantize_kv8(const uint16_t* x, int rows, int cols, uint8_t* codes, uint16_t* scales,
-                         uint16_t* biases, cudaStream_t s);
+bool launch_quantize_kv(const uint16_t* x, int rows, int cols, int bits, uint8_t* codes,
+                        uint16_t* scales, uint16_t* biases, cudaStream_t s);
 // jobs: device [n_jobs]; layers [l0, l0 + nl); max_n = most positions of a job
-void launch_kv8_convert(const Kv8Job* jobs, int n_jobs, int max_n, int l0, int nl, int n_kv_heads,
-                        int head_dim, uint8_t* arena, cudaStream_t s);
-struct Kv8AttnArgs {
-  const float* qkv;      // [B][q | k | v] fp32, q rotated (the RoPE kernel's output)
-  const Kv8Job* rows;    // [B]: each row's 8-bit slab and position
-  const AttnItem* items; // the decode work list (one 128-key sub-chunk per item)
+bool launch_kvq_convert(const Kv8Job* jobs, int n_jobs, int max_n, int l0, int nl, int n_kv_heads,
+                        int head_dim, int bits, uint8_t* arena, cudaStream_t s);
+struct KvqAttnArgs {
+  const uint8_t* qtile;  // [B][Hkv] Q operand images written by the QKV projection's epilogue
+  const QueryRow* rows;  // [B]: each row's position (pos)
+  const AttnItem* items; // the decode work list (one 128-key sub-chunk per item; kbase = byte
+                         // offset of the quantised slab or page holding it, cap, p0)
   const int* n_items;
-  const int* item_base;  // [B]
-  const int* item_count; // [B]
   const uint8_t* arena;
-  int B, layer, n_heads, n_kv_heads, head_dim;
+  int layer, n_heads, n_kv_heads, head_dim;
   float* part_o;         // [n_items][G][head_dim]
   float2* part_ml;       // [n_items][G]
-  float* o;              // [B][n_heads * head_dim], softmax(q.K^T / sqrt(hd)) V per q head
   int* err;
 };
-bool launch_attn_decode_kv8(const Kv8AttnArgs& a, int num_sms, cudaStream_t s);
+bool launch_attn_decode_q(const KvqAttnArgs& a, int bits, int num_sms, cudaStream_t s);
+// attention of prefill tokens over quantised positions [0, pos]: token t's pages (one slab: a
+// single entry) are at qpages[tok_first[t] + key / tok_cap[t]]; q from qkv (rotated), o fp32
+bool launch_attn_prefill_q(const float* qkv, const QueryRow* rows, const long long* qpages,
+                           const int* tok_first, const int* tok_cap, int n, int layer, int n_heads,
+                           int n_kv_heads, int head_dim, int max_keys, int bits,
+                           const uint8_t* arena, float* o, cudaStream_t s);
+// positions [0, n) of one layer of a quantised slab (pages[pos / cap]) as plain bf16
+// [n_kv_heads][n][head_dim] K and V
+bool launch_kvq_export(const uint8_t* arena, const long long* pages, int cap, int layer,
+                       int n_kv_heads, int head_dim, int n, int bits, uint16_t* k, uint16_t* v,
+                       cudaStream_t s);
+// the split-K merge of the decode attention (attn_tc.cu): partials of each (row, q head)
+// combined in item order into the O projection's bf16 hi/lo operand
+bool launch_attn_merge(const AttnDecodeArgs& a, cudaStream_t s);
 
 // V of one layer between a plain [kv head][plain_n positions][head_dim] buffer and a slab (or
 // page): positions [t0, t0 + n)

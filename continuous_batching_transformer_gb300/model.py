@@ -94,7 +94,7 @@ class Engine:
                  max_prefill_tokens: int, stream: torch.cuda.Stream | None = None,
                  page_tokens: int = 0, kv_bits: int = 16):
         """page_tokens > 0 (a multiple of 128): paged KV, slabs take pages of that many
-        positions from the arena as they grow.  kv_bits = 8: 8-bit affine KV."""
+        positions from the arena as they grow.  kv_bits = 8 or 4: affine KV of that many bits."""
         self.weights = weights
         self.shape = weights.shape
         self.arena = torch.empty(arena_bytes, dtype=torch.uint8, device=weights.device)

@@ -140,28 +140,31 @@ typedef struct {
                               * a call that writes a position in a shared page first queues a
                               * copy of that page into a new page of the writing slab (copy on
                               * write), and that page counts towards the same pool check. */
-  int32_t kv_bits;           /* 0 or 16: bf16 KV.  8: 8-bit affine KV (the mlx-bun batching
-                              * design's quantised KV): per position and (layer, K|V, kv head),
-                              * head_dim codes plus a bf16 scale and bias per 64 dims; a value
-                              * reads back as scale * code + bias, with scale = bf16((max -
-                              * min) / 255), bias = bf16(min), code = clamp(rint((x - bias) /
-                              * scale), 0, 255) over its group of 64 (cbt_quantize_kv8).  A
-                              * sequence's prompt is prefilled in bf16 and then converted, so
-                              * prefill logits equal the bf16 engine's; every decode step
-                              * quantises its new K/V before attention reads all positions
-                              * through their codes.  Slabs take cbt_slab_bytes_kv8 bytes; the
-                              * engine also holds max_batch * cbt_slab_bytes(cfg, 128) bytes of
-                              * the arena for the decode rows' bf16 staging (CBT_ERR_POOL_EXHAUSTED
-                              * from cbt_engine_create if it does not fit).  Needs contiguous
-                              * slabs (kv_page_tokens = 0), n_heads / n_kv_heads in {1, 2, 4,
-                              * 8} and the tensor-core path; cbt_engine_create returns
-                              * CBT_ERR_UNSUPPORTED otherwise.  Not available on an 8-bit engine
-                              * (CBT_ERR_UNSUPPORTED): prefill into a slab that already holds
-                              * positions, cbt_kv_slab_export, cbt_kv_slab_copy_prefix,
-                              * cbt_kv_slab_share_prefix.  cbt_kv_slab_import quantises what it
-                              * imports.  During a call, intermediate bf16 slabs of the
-                              * prompts' (or the import's) size are taken from the arena and
-                              * returned. */
+  int32_t kv_bits;           /* 0 or 16: bf16 KV.  8 or 4: affine KV of that many bits (the
+                              * mlx-bun batching design's quantised KV, "--kv-quant 4|8"): per
+                              * position and (layer, K|V, kv head), head_dim codes plus a bf16
+                              * scale and bias per 64 dims; a value reads back as scale * code +
+                              * bias, with L = 2^kv_bits - 1, scale = bf16((max - min) / L),
+                              * bias = bf16(min), code = clamp(rint((x - bias) / scale), 0, L)
+                              * over its group of 64 (cbt_quantize_kv).  A segment that starts a
+                              * sequence (its slab at position 0) is prefilled in bf16 and then
+                              * converted (the design's conversion point), so its prefill logits
+                              * equal the bf16 engine's; every later call -- a decode step, or a
+                              * prefill segment continuing the slab (a chunked prompt) --
+                              * quantises each position it appends before attention reads all
+                              * positions through their codes.  Slabs (and pages) take
+                              * cbt_slab_bytes_kvq bytes; the engine also holds max_batch *
+                              * cbt_slab_bytes(cfg, 128) bytes of the arena for the decode rows'
+                              * bf16 staging (CBT_ERR_POOL_EXHAUSTED from cbt_engine_create if it
+                              * does not fit).  Needs n_heads / n_kv_heads in {1, 2, 4, 8} and
+                              * the tensor-core path (cbt_engine_create returns
+                              * CBT_ERR_UNSUPPORTED otherwise); works with paged KV.
+                              * cbt_kv_slab_import quantises what it imports; cbt_kv_slab_export
+                              * gives each value as bf16(fp32(scale * code + bias)), the product
+                              * and sum taken in double; cbt_kv_slab_copy_prefix copies codes,
+                              * scales and biases; cbt_kv_slab_share_prefix shares pages.  During
+                              * a call, intermediate bf16 slabs of the prompts' (or the import's)
+                              * size are taken from the arena and returned. */
 } cbt_engine_params;
 
 typedef struct {
@@ -177,18 +180,25 @@ typedef struct {
 
 typedef struct cbt_engine cbt_engine;
 
-/* Bytes of an 8-bit KV slab of capacity cap (kv_bits = 8): per (layer, K|V, kv head) block
- * codes [round64(cap)][head_dim] uint8, then bf16 scales and bf16 biases
- * [round64(cap)][head_dim / 64]; the total rounded up to 4 KiB.  0 if head_dim is not a
- * multiple of 64 or cap <= 0. */
+/* Bytes of a quantised KV slab (or page) of capacity cap at kv_bits = bits (8 or 4): per
+ * (layer, K|V, kv head) block codes [round64(cap)][head_dim * bits / 8] uint8 (at 4 bits element
+ * 2i in the low nibble of byte i, 2i + 1 in its high nibble), then bf16 scales and bf16 biases
+ * [round64(cap)][head_dim / 64]; the total rounded up to 4 KiB.  0 if head_dim is not a multiple
+ * of 64, cap <= 0 or bits is not 8 or 4.  cbt_slab_bytes_kv8(c, cap) = cbt_slab_bytes_kvq(c,
+ * cap, 8). */
+size_t cbt_slab_bytes_kvq(const cbt_model_config* c, int32_t cap, int32_t bits);
 size_t cbt_slab_bytes_kv8(const cbt_model_config* c, int32_t cap);
 
-/* 8-bit affine quantisation of bf16 rows, groups of 64 along each row (the kv_bits = 8 format).
+/* Affine quantisation of bf16 rows, groups of 64 along each row (the kv_bits = bits format).
  *   x       device bf16 [rows][cols], 4-byte aligned; cols a multiple of 64.
- *   codes   device uint8 [rows][cols] (2-byte aligned); scales, biases device bf16
- *           [rows][cols / 64].
+ *   bits    8 or 4.
+ *   codes   device uint8 [rows][cols * bits / 8] (2-byte aligned at 8 bits); scales, biases
+ *           device bf16 [rows][cols / 64].
  *   stream  cudaStream_t (NULL: legacy default stream); queued, not synchronised.
- * CBT_ERR_NULL, CBT_ERR_INVALID (shape or alignment), CBT_ERR_CUDA. */
+ * CBT_ERR_NULL, CBT_ERR_INVALID (bits, shape or alignment), CBT_ERR_CUDA.
+ * cbt_quantize_kv8 is cbt_quantize_kv with bits = 8. */
+cbt_status cbt_quantize_kv(const void* x, int32_t rows, int32_t cols, int32_t bits, void* codes,
+                           void* scales, void* biases, void* stream);
 cbt_status cbt_quantize_kv8(const void* x, int32_t rows, int32_t cols, void* codes, void* scales,
                             void* biases, void* stream);
 

@@ -70,7 +70,7 @@ class Model(ctypes.Structure):
 class KV(ctypes.Structure):
     _fields_ = [("capacity", c_int), ("len", c_int), ("k", c_void), ("v", c_void),
                 ("kq", c_void), ("vq", c_void), ("ks", c_void), ("kb", c_void), ("vs", c_void),
-                ("vb", c_void), ("qlen", c_int)]
+                ("vb", c_void), ("qlen", c_int), ("bits", c_int)]
 
 
 def lib():
@@ -92,9 +92,14 @@ def lib():
         L.orc_quantize_affine4.argtypes = [c_void, c_int, c_int, c_int, c_void, c_void, c_void]
         L.orc_dequantize_affine4.argtypes = [c_void, c_void, c_void, c_int, c_int, c_int, c_void]
         L.orc_quantize_kv8.argtypes = [c_void, c_int, c_int, c_void, c_void, c_void]
+        L.orc_quantize_kv.argtypes = [c_void, c_int, c_int, c_int, c_void, c_void, c_void]
         L.orc_attention_kv8.argtypes = [c_void, c_void, c_void, c_void, c_void, c_void, c_void,
                                         c_int, c_int, c_void]
-        L.orc_kv8_convert.argtypes = [P(Config), P(KV)]
+        L.orc_attention_kvq.argtypes = [c_void, c_void, c_void, c_void, c_void, c_void, c_void,
+                                        c_int, c_int, c_int, c_void]
+        L.orc_kv_convert.argtypes = [P(Config), P(KV)]
+        L.orc_kvq_export_value.argtypes = [ctypes.c_uint16, ctypes.c_uint16, c_int]
+        L.orc_kvq_export_value.restype = ctypes.c_uint16
         L.orc_forward.argtypes = [P(Model), P(KV), c_int, c_int, c_void, c_void, c_void, c_void,
                                   c_void]
         L.orc_decode_step_batch.argtypes = [P(Model), P(KV), c_int, c_void, c_void]
@@ -175,6 +180,20 @@ def dequantize_affine4(packed, scales, biases, group: int = 64) -> np.ndarray:
     return out
 
 
+def quantize_kv(x_bf16: np.ndarray, bits: int):
+    """Affine rows of 8 or 4 bits (groups of 64 along the last axis): codes (cols * bits / 8
+    bytes a row; 4 bits: element 2i in the low nibble of byte i), bf16 scales, bf16 biases."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    rows, cols = x.shape
+    codes = np.empty((rows, cols * bits // 8), dtype=np.uint8)
+    scales = np.empty((rows, cols // 64), dtype=np.uint16)
+    biases = np.empty((rows, cols // 64), dtype=np.uint16)
+    if lib().orc_quantize_kv(_ptr(x), rows, cols, bits, _ptr(codes), _ptr(scales),
+                             _ptr(biases)) != 0:
+        raise ValueError("bad quantisation shape")
+    return codes, scales, biases
+
+
 def quantize_kv8(x_bf16: np.ndarray):
     """8-bit affine rows (groups of 64 along the last axis): codes, bf16 scales, bf16 biases."""
     x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
@@ -187,6 +206,16 @@ def quantize_kv8(x_bf16: np.ndarray):
     return codes, scales, biases
 
 
+def attention_kvq(q: np.ndarray, kq, vq, bits: int) -> np.ndarray:
+    """Attention of one query over quantised K/V rows: kq and vq are (codes, scales, biases)."""
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    parts = [np.ascontiguousarray(a) for a in (*kq, *vq)]
+    out = np.empty(q.size, dtype=np.float32)
+    lib().orc_attention_kvq(_ptr(q), *[_ptr(a) for a in parts], parts[1].shape[0], q.size, bits,
+                            _ptr(out))
+    return out
+
+
 def attention_kv8(q: np.ndarray, k8, v8) -> np.ndarray:
     """Attention of one query over 8-bit K/V rows: k8 and v8 are (codes, scales, biases)."""
     q = np.ascontiguousarray(q, dtype=np.float32)
@@ -194,6 +223,26 @@ def attention_kv8(q: np.ndarray, k8, v8) -> np.ndarray:
     out = np.empty(q.size, dtype=np.float32)
     lib().orc_attention_kv8(_ptr(q), *[_ptr(a) for a in parts], parts[0].shape[0], q.size,
                             _ptr(out))
+    return out
+
+
+def kvq_export_values(codes: np.ndarray, scales: np.ndarray, biases: np.ndarray,
+                      bits: int) -> np.ndarray:
+    """bf16 bits of quantised rows as an export gives them (scale * code + bias in double,
+    rounded to fp32, then to bf16); codes [rows][cols * bits / 8], scales/biases
+    [rows][cols / 64]."""
+    rows, ng = scales.shape
+    cols = ng * 64
+    L = lib()
+    out = np.empty((rows, cols), dtype=np.uint16)
+    for r in range(rows):
+        for i in range(cols):
+            if bits == 8:
+                q = int(codes[r, i])
+            else:
+                byte = int(codes[r, i // 2])
+                q = (byte >> 4) if (i & 1) else (byte & 0xF)
+            out[r, i] = L.orc_kvq_export_value(int(scales[r, i // 64]), int(biases[r, i // 64]), q)
     return out
 
 
@@ -281,12 +330,13 @@ class OracleModel:
 
 class KVCache:
     """One sequence's cache, bf16 bits [n_layers, n_kv_heads, capacity, head_dim] for K and V;
-    with kv_bits = 8 also their 8-bit affine codes (groups of 64 along head_dim) and bf16
-    scales/biases, which attention reads once the cache's first call has converted it."""
+    with kv_bits = 8 or 4 also their affine codes (groups of 64 along head_dim; head_dim *
+    kv_bits / 8 bytes a position) and bf16 scales/biases, which attention reads once the
+    cache's first call has converted it."""
 
     def __init__(self, shape: ModelShape, capacity: int, kv_bits: int = 16):
-        if kv_bits not in (8, 16):
-            raise ValueError("kv_bits is 16 (bf16) or 8 (8-bit affine)")
+        if kv_bits not in (4, 8, 16):
+            raise ValueError("kv_bits is 16 (bf16), 8 or 4 (affine)")
         self.shape = shape
         dims = (shape.n_layers, shape.n_kv_heads, capacity, shape.head_dim)
         self.k = np.zeros(dims, dtype=np.uint16)
@@ -296,25 +346,27 @@ class KVCache:
         self.kv_bits = kv_bits
         self.qlen = 0
         self.q8 = None
-        if kv_bits == 8:
+        if kv_bits in (4, 8):
             gdims = dims[:-1] + (shape.head_dim // 64,)
-            self.q8 = {"kq": np.zeros(dims, np.uint8), "vq": np.zeros(dims, np.uint8),
+            cdims = dims[:-1] + (shape.head_dim * kv_bits // 8,)
+            self.q8 = {"kq": np.zeros(cdims, np.uint8), "vq": np.zeros(cdims, np.uint8),
                        "ks": np.zeros(gdims, np.uint16), "kb": np.zeros(gdims, np.uint16),
                        "vs": np.zeros(gdims, np.uint16), "vb": np.zeros(gdims, np.uint16)}
 
     def struct(self) -> KV:
         q = self.q8 or {}
         return KV(self.capacity, self.len, _ptr(self.k), _ptr(self.v),
-                  *[_ptr(q.get(n)) for n in ("kq", "vq", "ks", "kb", "vs", "vb")], self.qlen)
+                  *[_ptr(q.get(n)) for n in ("kq", "vq", "ks", "kb", "vs", "vb")], self.qlen,
+                  self.kv_bits if self.q8 else 0)
 
     def convert(self) -> None:
-        """Quantise positions [qlen, len) (an 8-bit cache filled with bf16 K/V directly)."""
+        """Quantise positions [qlen, len) (a quantised cache filled with bf16 K/V directly)."""
         st = self.struct()
         s = self.shape
         m = Config(s.n_layers, s.d_model, s.n_heads, s.n_kv_heads, s.head_dim, s.d_ff, s.vocab,
                    s.rms_eps, s.rope_theta, 0, s.group_size)
-        if lib().orc_kv8_convert(ctypes.byref(m), ctypes.byref(st)) != 0:
-            raise ValueError("not an 8-bit cache")
+        if lib().orc_kv_convert(ctypes.byref(m), ctypes.byref(st)) != 0:
+            raise ValueError("not a quantised cache")
         self.qlen = st.qlen
 
     def fill_synthetic(self, row: int, n_tok: int, seed: int) -> None:
@@ -326,7 +378,7 @@ class KVCache:
                            s.kv_sigma)
             dst[:, :, :n_tok, :] = src
         self.len = n_tok
-        if self.kv_bits == 8:
+        if self.kv_bits in (4, 8):
             self.qlen = 0
             self.convert()
 

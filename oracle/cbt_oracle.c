@@ -98,12 +98,23 @@ void orc_attention(const float* q, const uint16_t* k, const uint16_t* v, int n_k
   free(vd);
 }
 
-/* ---- 8-bit affine KV: x^ = scale * q + bias per group of 64 along head_dim --------- */
-int orc_quantize_kv8(const uint16_t* x, int rows, int cols, uint8_t* codes, uint16_t* scales,
-                     uint16_t* biases) {
-  if (rows < 0 || cols <= 0 || cols % 64 != 0) return ORC_EINVAL;
+/* ---- affine KV, 8 or 4 bits: x^ = scale * q + bias per group of 64 along head_dim ------ */
+/* Codes of a row of `cols` values take cols * bits / 8 bytes; at 4 bits element 2i sits in the
+ * low nibble of byte i and element 2i + 1 in its high nibble (the weights' packing order). */
+static int kv_code(const uint8_t* codes, int cols, int bits, size_t row, int i) {
+  if (bits == 8) return codes[row * (size_t)cols + i];
+  const uint8_t byte = codes[row * (size_t)(cols / 2) + i / 2];
+  return (i & 1) ? (byte >> 4) : (byte & 0xF);
+}
+
+int orc_quantize_kv(const uint16_t* x, int rows, int cols, int bits, uint8_t* codes,
+                    uint16_t* scales, uint16_t* biases) {
+  if (rows < 0 || cols <= 0 || cols % 64 != 0 || (bits != 8 && bits != 4)) return ORC_EINVAL;
   const int ng = cols / 64;
+  const int levels = (1 << bits) - 1;
+  const size_t row_bytes = (size_t)cols * bits / 8;
   for (int r = 0; r < rows; ++r) {
+    memset(codes + (size_t)r * row_bytes, 0, row_bytes);
     for (int g = 0; g < ng; ++g) {
       const uint16_t* src = x + (size_t)r * cols + (size_t)g * 64;
       double mn = orc_bf16_to_f32(src[0]), mx = mn;
@@ -112,7 +123,7 @@ int orc_quantize_kv8(const uint16_t* x, int rows, int cols, uint8_t* codes, uint
         if (v < mn) mn = v;
         if (v > mx) mx = v;
       }
-      uint16_t sb = orc_f32_to_bf16((float)((mx - mn) / 255.0));
+      uint16_t sb = orc_f32_to_bf16((float)((mx - mn) / (double)levels));
       uint16_t bb = orc_f32_to_bf16((float)mn);
       double sc = orc_bf16_to_f32(sb), bi = orc_bf16_to_f32(bb);
       scales[(size_t)r * ng + g] = sb;
@@ -121,36 +132,58 @@ int orc_quantize_kv8(const uint16_t* x, int rows, int cols, uint8_t* codes, uint
         int q = 0;
         if (sc != 0.0) {
           double t = rint(((double)orc_bf16_to_f32(src[i]) - bi) / sc);
-          q = t < 0.0 ? 0 : (t > 255.0 ? 255 : (int)t);
+          q = t < 0.0 ? 0 : (t > (double)levels ? levels : (int)t);
         }
-        codes[(size_t)r * cols + (size_t)g * 64 + i] = (uint8_t)q;
+        const int e = g * 64 + i;
+        if (bits == 8)
+          codes[(size_t)r * row_bytes + e] = (uint8_t)q;
+        else
+          codes[(size_t)r * row_bytes + e / 2] |= (uint8_t)(q << (4 * (e & 1)));
       }
     }
   }
   return ORC_OK;
 }
 
-static double kv8_value(const uint8_t* codes, const uint16_t* scales, const uint16_t* biases,
-                        int hd, int t, int d) {
+int orc_quantize_kv8(const uint16_t* x, int rows, int cols, uint8_t* codes, uint16_t* scales,
+                     uint16_t* biases) {
+  return orc_quantize_kv(x, rows, cols, 8, codes, scales, biases);
+}
+
+static double kvq_value(const uint8_t* codes, const uint16_t* scales, const uint16_t* biases,
+                        int hd, int bits, int t, int d) {
   size_t gi = (size_t)t * (hd / 64) + d / 64;
-  return (double)orc_bf16_to_f32(scales[gi]) * codes[(size_t)t * hd + d] +
+  return (double)orc_bf16_to_f32(scales[gi]) * kv_code(codes, hd, bits, (size_t)t, d) +
          (double)orc_bf16_to_f32(biases[gi]);
 }
 
-void orc_attention_kv8(const float* q, const uint8_t* kq, const uint16_t* ks, const uint16_t* kb,
+void orc_attention_kvq(const float* q, const uint8_t* kq, const uint16_t* ks, const uint16_t* kb,
                        const uint8_t* vq, const uint16_t* vs, const uint16_t* vb, int n_keys,
-                       int head_dim, float* out) {
+                       int head_dim, int bits, float* out) {
   size_t n = (size_t)(n_keys > 0 ? n_keys : 1) * head_dim;
   double* kd = (double*)malloc(sizeof(double) * n);
   double* vd = (double*)malloc(sizeof(double) * n);
   for (int t = 0; t < n_keys; ++t)
     for (int d = 0; d < head_dim; ++d) {
-      kd[(size_t)t * head_dim + d] = kv8_value(kq, ks, kb, head_dim, t, d);
-      vd[(size_t)t * head_dim + d] = kv8_value(vq, vs, vb, head_dim, t, d);
+      kd[(size_t)t * head_dim + d] = kvq_value(kq, ks, kb, head_dim, bits, t, d);
+      vd[(size_t)t * head_dim + d] = kvq_value(vq, vs, vb, head_dim, bits, t, d);
     }
   attention_values(q, kd, vd, n_keys, head_dim, out);
   free(kd);
   free(vd);
+}
+
+void orc_attention_kv8(const float* q, const uint8_t* kq, const uint16_t* ks, const uint16_t* kb,
+                       const uint8_t* vq, const uint16_t* vs, const uint16_t* vb, int n_keys,
+                       int head_dim, float* out) {
+  orc_attention_kvq(q, kq, ks, kb, vq, vs, vb, n_keys, head_dim, 8, out);
+}
+
+/* the value an exported position of a quantised cache holds: scale * code + bias evaluated
+ * in double, rounded to fp32, then to bf16 */
+uint16_t orc_kvq_export_value(uint16_t scale, uint16_t bias, int code) {
+  double v = (double)orc_bf16_to_f32(scale) * code + (double)orc_bf16_to_f32(bias);
+  return orc_f32_to_bf16((float)v);
 }
 
 double orc_silu(double z) { return z / (1.0 + exp(-z)); }
@@ -251,18 +284,18 @@ static size_t kv_index(const orc_config* c, int cap, int layer, int kvh, int pos
   return ((((size_t)layer * c->n_kv_heads + kvh) * cap) + pos) * (size_t)c->head_dim;
 }
 
-/* quantise the K and V rows at (layer, kv head, position) of an 8-bit cache */
-static void kv8_store(const orc_config* c, orc_kv* C, int l, int g, int p) {
-  size_t at = kv_index(c, C->capacity, l, g, p), ga = at / 64;
-  orc_quantize_kv8(C->k + at, 1, c->head_dim, C->kq + at, C->ks + ga, C->kb + ga);
-  orc_quantize_kv8(C->v + at, 1, c->head_dim, C->vq + at, C->vs + ga, C->vb + ga);
+/* quantise the K and V rows at (layer, kv head, position) of a quantised cache */
+static void kvq_store(const orc_config* c, orc_kv* C, int l, int g, int p) {
+  size_t at = kv_index(c, C->capacity, l, g, p), ga = at / 64, ca = at * C->bits / 8;
+  orc_quantize_kv(C->k + at, 1, c->head_dim, C->bits, C->kq + ca, C->ks + ga, C->kb + ga);
+  orc_quantize_kv(C->v + at, 1, c->head_dim, C->bits, C->vq + ca, C->vs + ga, C->vb + ga);
 }
 
-int orc_kv8_convert(const orc_config* c, orc_kv* kv) {
-  if (!kv->kq || c->head_dim % 64 != 0) return ORC_EINVAL;
+int orc_kv_convert(const orc_config* c, orc_kv* kv) {
+  if (!kv->kq || c->head_dim % 64 != 0 || (kv->bits != 8 && kv->bits != 4)) return ORC_EINVAL;
   for (int l = 0; l < c->n_layers; ++l)
     for (int g = 0; g < c->n_kv_heads; ++g)
-      for (int p = kv->qlen; p < kv->len; ++p) kv8_store(c, kv, l, g, p);
+      for (int p = kv->qlen; p < kv->len; ++p) kvq_store(c, kv, l, g, p);
   kv->qlen = kv->len;
   return ORC_OK;
 }
@@ -274,7 +307,7 @@ int orc_forward(const orc_model* m, orc_kv* kv, int n_kv, int n, const int* seq,
   const int qd = H * hd, kvd = Hkv * hd, F = c->d_ff, V = c->vocab;
   if (n < 0 || H % Hkv != 0 || hd % 2 != 0) return ORC_EINVAL;
   for (int s = 0; s < n_kv; ++s)
-    if (kv[s].kq && hd % 64 != 0) return ORC_EINVAL;
+    if (kv[s].kq && (hd % 64 != 0 || (kv[s].bits != 8 && kv[s].bits != 4))) return ORC_EINVAL;
   /* each sequence's tokens: consecutive positions from its current length, inside capacity */
   int* next = (int*)malloc(sizeof(int) * (size_t)(n_kv > 0 ? n_kv : 1));
   for (int s = 0; s < n_kv; ++s) next[s] = kv[s].len;
@@ -326,7 +359,7 @@ int orc_forward(const orc_model* m, orc_kv* kv, int n_kv, int n, const int* seq,
           C->k[at + e] = orc_f32_to_bf16(kk[e]);
           C->v[at + e] = orc_f32_to_bf16(vv[e]);
         }
-        if (quant[seq[i]]) kv8_store(c, C, l, g, p);
+        if (quant[seq[i]]) kvq_store(c, C, l, g, p);
       }
       const int qm = quant[seq[i]];
 #pragma omp parallel for schedule(static)
@@ -334,9 +367,10 @@ int orc_forward(const orc_model* m, orc_kv* kv, int n_kv, int n, const int* seq,
         int g = j / (H / Hkv);
         size_t base = kv_index(c, C->capacity, l, g, 0);
         if (qm)
-          orc_attention_kv8(q + (size_t)i * qd + (size_t)j * hd, C->kq + base, C->ks + base / 64,
-                            C->kb + base / 64, C->vq + base, C->vs + base / 64, C->vb + base / 64,
-                            p + 1, hd, o + (size_t)i * qd + (size_t)j * hd);
+          orc_attention_kvq(q + (size_t)i * qd + (size_t)j * hd, C->kq + base * C->bits / 8,
+                            C->ks + base / 64, C->kb + base / 64, C->vq + base * C->bits / 8,
+                            C->vs + base / 64, C->vb + base / 64, p + 1, hd, C->bits,
+                            o + (size_t)i * qd + (size_t)j * hd);
         else
           orc_attention(q + (size_t)i * qd + (size_t)j * hd, C->k + base, C->v + base, p + 1, hd,
                         o + (size_t)i * qd + (size_t)j * hd);
@@ -357,7 +391,7 @@ int orc_forward(const orc_model* m, orc_kv* kv, int n_kv, int n, const int* seq,
     /* a first call ran on bf16 K/V: its positions are converted now; later calls quantised
      * their positions as they appended them */
     if (kv[s].kq && quant[s]) kv[s].qlen = kv[s].len;
-    else if (kv[s].kq && kv[s].len > 0) orc_kv8_convert(c, &kv[s]);
+    else if (kv[s].kq && kv[s].len > 0) orc_kv_convert(c, &kv[s]);
   }
   free(quant);
 

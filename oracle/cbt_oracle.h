@@ -75,13 +75,13 @@ typedef struct {
   int len; /* positions [0, len) hold valid K/V */
   uint16_t* k;
   uint16_t* v;
-  /* 8-bit affine KV (the mlx-bun batching design's quantised KV: affine groups of 64 along
-   * head_dim, as its weights).  kq == NULL: a plain bf16 cache.  Otherwise codes
-   * [n_layers][n_kv_heads][capacity][head_dim] and bf16 scale/bias
-   * [n_layers][n_kv_heads][capacity][head_dim/64] for K and V.  A sequence's first call runs
-   * on its bf16 K/V and is then converted (the design's "prefill bf16, then to quantized"); from
-   * then on (qlen > 0) every appended position is quantised at once and attention reads every
-   * position through its codes.  Positions [0, qlen) hold codes. */
+  /* Affine KV of `bits` = 8 or 4 bits (the mlx-bun batching design's quantised KV, "--kv-quant
+   * 4|8": affine groups of 64 along head_dim, as its weights).  kq == NULL: a plain bf16
+   * cache.  Otherwise codes [n_layers][n_kv_heads][capacity][head_dim * bits / 8] and bf16
+   * scale/bias [n_layers][n_kv_heads][capacity][head_dim/64] for K and V.  A sequence's first
+   * call runs on its bf16 K/V and is then converted (the design's "prefill bf16, then to
+   * quantized"); from then on (qlen > 0) every appended position is quantised at once and
+   * attention reads every position through its codes.  Positions [0, qlen) hold codes. */
   uint8_t* kq;
   uint8_t* vq;
   uint16_t* ks;
@@ -89,6 +89,7 @@ typedef struct {
   uint16_t* vs;
   uint16_t* vb;
   int qlen;
+  int bits;
 } orc_kv;
 
 /* status codes */
@@ -110,17 +111,28 @@ int orc_quantize_affine4(const uint16_t* w, int rows, int cols, int group, uint3
                          uint16_t* scales, uint16_t* biases);
 void orc_dequantize_affine4(const uint32_t* packed, const uint16_t* scales,
                             const uint16_t* biases, int rows, int cols, int group, double* out);
-/* 8-bit affine KV rows: per group of 64 values of a row, scale = bf16((max - min) / 255),
- * bias = bf16(min), q = clamp(rint((x - bias) / scale), 0, 255) (q = 0 when scale = 0); the
- * value read back is scale * q + bias.  cols must be a multiple of 64. */
+/* Affine KV rows of `bits` = 8 or 4: per group of 64 values of a row, L = 2^bits - 1,
+ * scale = bf16((max - min) / L), bias = bf16(min), q = clamp(rint((x - bias) / scale), 0, L)
+ * (q = 0 when scale = 0); the value read back is scale * q + bias.  cols must be a multiple of
+ * 64; a row's codes take cols * bits / 8 bytes (4 bits: element 2i in the low nibble of byte i,
+ * 2i + 1 in its high nibble). */
+int orc_quantize_kv(const uint16_t* x, int rows, int cols, int bits, uint8_t* codes,
+                    uint16_t* scales, uint16_t* biases);
 int orc_quantize_kv8(const uint16_t* x, int rows, int cols, uint8_t* codes, uint16_t* scales,
                      uint16_t* biases);
-/* attention of one query over n_keys 8-bit K/V rows (codes [n][hd], scale/bias [n][hd/64]) */
+/* attention of one query over n_keys quantised K/V rows (codes [n][hd * bits / 8],
+ * scale/bias [n][hd/64]) */
+void orc_attention_kvq(const float* q, const uint8_t* kq, const uint16_t* ks, const uint16_t* kb,
+                       const uint8_t* vq, const uint16_t* vs, const uint16_t* vb, int n_keys,
+                       int head_dim, int bits, float* out);
 void orc_attention_kv8(const float* q, const uint8_t* kq, const uint16_t* ks, const uint16_t* kb,
                        const uint8_t* vq, const uint16_t* vs, const uint16_t* vb, int n_keys,
                        int head_dim, float* out);
-/* quantise positions [qlen, len) of an 8-bit cache from its bf16 rows; qlen becomes len */
-int orc_kv8_convert(const orc_config* cfg, orc_kv* kv);
+/* quantise positions [qlen, len) of a quantised cache from its bf16 rows; qlen becomes len */
+int orc_kv_convert(const orc_config* cfg, orc_kv* kv);
+/* What export gives for a quantised position (a reading of the pages, which define no export):
+ * scale * code + bias in double, rounded to fp32 and then to bf16. */
+uint16_t orc_kvq_export_value(uint16_t scale, uint16_t bias, int code);
 
 /* ---- the model ------------------------------------------------------------------ */
 /* General forward: n tokens; token i belongs to cache kv[seq[i]] at position pos[i] and

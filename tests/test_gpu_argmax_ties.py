@@ -82,7 +82,7 @@ def test_greedy_ties_take_the_lowest_id():
     torch.cuda.set_device(dev)
     cfg = config_struct(TINY)
     w, layers, embed, fnorm, lm_lin, keep = tied_model(dev)
-    arena = torch.empty(B.slab_bytes(cfg, 64) * 12, dtype=torch.uint8, device=dev)
+    arena = torch.empty(B.slab_bytes(cfg, 64) * 16, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     eng = B.engine_create(cfg, w, B.EngineParams(arena.data_ptr(), arena.numel(), 12, 64,
                                                  stream.cuda_stream))

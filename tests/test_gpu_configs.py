@@ -140,14 +140,18 @@ def bf16_values(a):
 
 
 def check_kv_at(shape, got_k, got_v, cache, p, what):
-    """The oracle's K/V at position p against the GPU's: bf16 roundings of the same value,
-    so within one bf16 step (2^-8 relative) plus the drift a 32-layer forward allows."""
+    """The oracle's K/V at position p against the GPU's: bf16 roundings of values that differ
+    only by the rounding drift of the hidden state through up to 31 layers (the same drift the
+    logit tolerance allows).  Every value within two bf16 steps (2^-6 relative) plus 1% of the
+    KV spread, and at most one value in a thousand more than one step apart."""
     for name, g, o in (("K", got_k[:, :, p], cache.k[:, :, p]), ("V", got_v[:, :, p], cache.v[:, :, p])):
         gf, of = bf16_values(g), bf16_values(o)
-        tol = 2.0 ** -7 * np.abs(of) + 0.01 * shape.kv_sigma
-        bad = np.abs(gf - of) > tol
+        err = np.abs(gf - of)
+        bad = err > 2.0 ** -6 * np.abs(of) + 0.01 * shape.kv_sigma
         assert not bad.any(), (f"{what}: {name} at position {p}: {int(bad.sum())} values off, "
-                               f"max |gpu - oracle| = {np.abs(gf - of).max():.3e}")
+                               f"max |gpu - oracle| = {err.max():.3e}")
+        far = err > 2.0 ** -7 * np.abs(of) + 1e-6
+        assert far.mean() <= 1e-3, f"{what}: {name} at position {p}: {int(far.sum())} values over one step"
 
 
 def test_7b_trace_slice_joins_and_retires():

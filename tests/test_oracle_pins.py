@@ -522,3 +522,117 @@ def test_kv8_decode_over_a_lossless_prefix():
     c8b.q8["kq"][1, 0, 3, 7] ^= 0x40
     c8b.len, c8b.qlen = 12, 12
     assert not np.array_equal(oracle.decode_step_batch(m, [c8b], tok), d8)
+
+
+# ---- 4-bit affine KV (the batching design's "--kv-quant 4|8": groups of 64 along head_dim) ------
+def test_kv4_hand_example_and_nibble_order():
+    """Groups on exact 16-level grids quantise losslessly: [0, 15/4] has scale 1/4 and bias 0,
+    [-2, -2 + 15/8] scale 1/8 and bias -2, every code the grid index.  Element 2i sits in the
+    low nibble of byte i, 2i + 1 in its high nibble.  A value halfway between steps rounds to
+    the even code (1.5 -> 2, 2.5 -> 2); a constant group has scale 0 and all codes 0."""
+    rng = np.random.default_rng(13)
+    qa = rng.integers(0, 16, 64)
+    qa[3], qa[50] = 0, 15
+    qb = rng.integers(0, 16, 64)
+    qb[0], qb[63] = 15, 0
+    row0 = np.concatenate([qa / 4.0, -2.0 + qb / 8.0])
+    ties = np.zeros(64)
+    ties[1], ties[2], ties[3] = 15 / 4.0, 1.5 / 4.0, 2.5 / 4.0
+    row1 = np.concatenate([ties, np.full(64, -0.75)])
+    codes, scales, biases = oracle.quantize_kv(_bf16_bits(np.stack([row0, row1])), 4)
+    assert codes.shape == (2, 64)
+    q0 = np.concatenate([qa, qb])
+    assert list(codes[0]) == [int(q0[2 * i]) | (int(q0[2 * i + 1]) << 4) for i in range(64)]
+    assert list(scales[0]) == list(_bf16_bits([1 / 4.0, 1 / 8.0]))
+    assert list(biases[0]) == list(_bf16_bits([0.0, -2.0]))
+    # codes of row 1, group 0: element 1 -> 15, 2 -> 2, 3 -> 2 (bytes 0 and 1)
+    assert codes[1, 0] == (0 | (15 << 4)) and codes[1, 1] == (2 | (2 << 4))
+    assert scales[1, 1] == 0 and biases[1, 1] == _bf16_bits([-0.75])[0]
+    assert not codes[1, 32:].any()
+
+
+def test_kv4_round_trip_bound():
+    rng = np.random.default_rng(14)
+    x = _bf16_bits(oracle_f32_from_bits(oracle.bf16_round(rng.normal(0, 1.3, (40, 128)))))
+    codes, scales, biases = oracle.quantize_kv(x, 4)
+    q = np.stack([codes & 0xF, codes >> 4], axis=-1).reshape(40, 128).astype(np.float64)
+    xf = oracle_f32_from_bits(x).astype(np.float64).reshape(40, 2, 64)
+    sc = oracle_f32_from_bits(scales).astype(np.float64)[..., None]
+    bi = oracle_f32_from_bits(biases).astype(np.float64)[..., None]
+    back = sc * q.reshape(40, 2, 64) + bi
+    mn, mx = xf.min(-1, keepdims=True), xf.max(-1, keepdims=True)
+    slack = np.abs(bi - mn) + 15 * np.abs(sc - (mx - mn) / 15)
+    assert np.all(np.abs(back - xf) <= sc / 2 + slack + 1e-12)
+    assert q.min() == 0 and q.max() == 15
+    # the 8-bit quantiser on the same rows is the kv8 format, unchanged
+    c8 = oracle.quantize_kv(x, 8)
+    for a, b in zip(c8, oracle.quantize_kv8(x)):
+        assert np.array_equal(a, b)
+
+
+def _grid_kv4(rng, n, hd):
+    """bf16 rows whose groups of 64 are exact 16-level grids (lossless at 4 bits)."""
+    q = rng.integers(0, 16, (n, hd // 64, 64))
+    q[:, :, 0], q[:, :, 1] = 0, 15
+    step = 2.0 ** rng.integers(-5, -1, (n, hd // 64, 1))
+    return _bf16_bits(((q - 8) * step).reshape(n, hd))
+
+
+def test_kv4_attention_over_lossless_codes_equals_bf16():
+    rng = np.random.default_rng(15)
+    for n, hd in ((1, 64), (29, 128)):
+        k, v = _grid_kv4(rng, n, hd), _grid_kv4(rng, n, hd)
+        q = rng.normal(0, 1, hd).astype(np.float32)
+        got = oracle.attention_kvq(q, oracle.quantize_kv(k, 4), oracle.quantize_kv(v, 4), 4)
+        np.testing.assert_array_equal(got, oracle.attention(q, k, v))
+
+
+def test_kv4_cache_conversion_points():
+    """As for 8 bits: the prompt runs on bf16 K/V (logits equal the bf16 cache's bit for bit),
+    the cache is then converted, a decode step quantises what it appends, and the codes of
+    every position are the 4-bit quantiser's output for its bf16 row; over a lossless prefix a
+    decode step differs from the bf16 cache's only through the appended position."""
+    m = oracle.OracleModel(KV8_SHAPE)
+    rng = np.random.default_rng(16)
+    toks = rng.integers(0, KV8_SHAPE.vocab, 21).astype(np.int32)
+    c4, c16 = oracle.KVCache(KV8_SHAPE, 32, kv_bits=4), oracle.KVCache(KV8_SHAPE, 32)
+    np.testing.assert_array_equal(oracle.prefill_segmented(m, [c4], [20], toks[:20]),
+                                  oracle.prefill_segmented(m, [c16], [20], toks[:20]))
+    assert c4.qlen == 20
+    d4 = oracle.decode_step_batch(m, [c4], toks[20:21])
+    d16 = oracle.decode_step_batch(m, [c16], toks[20:21])
+    assert c4.qlen == 21 and np.abs(d4 - d16).max() > 0
+    hd = KV8_SHAPE.head_dim
+    for name, src in (("k", c4.k), ("v", c4.v)):
+        codes, scales, biases = oracle.quantize_kv(src[:, :, :21, :].reshape(-1, hd), 4)
+        np.testing.assert_array_equal(c4.q8[name + "q"][:, :, :21, :].reshape(-1, hd // 2), codes)
+        np.testing.assert_array_equal(c4.q8[name + "s"][:, :, :21, :].reshape(-1, hd // 64), scales)
+        np.testing.assert_array_equal(c4.q8[name + "b"][:, :, :21, :].reshape(-1, hd // 64), biases)
+    s = KV8_SHAPE
+    g4, g16 = oracle.KVCache(s, 16, kv_bits=4), oracle.KVCache(s, 16)
+    for c in (g4, g16):
+        r = np.random.default_rng(17)
+        for arr in (c.k, c.v):
+            arr[:, :, :12, :] = _grid_kv4(r, s.n_layers * s.n_kv_heads * 12, s.head_dim).reshape(
+                s.n_layers, s.n_kv_heads, 12, s.head_dim)
+        c.len = 12
+    g4.convert()
+    tok = toks[:1]
+    assert np.abs(oracle.decode_step_batch(m, [g4], tok) - oracle.decode_step_batch(m, [g16], tok)).max() < 0.25
+
+
+def test_kvq_export_value_hand_example():
+    """Export of a quantised position: scale * code + bias in double, to fp32, to bf16.
+    scale 1/8, bias -4, code 37: -4 + 37/8 = 0.625 exactly.  scale 1.5 * 2^-7, bias 1, code
+    255: 1 + 255 * 0.01171875 = 3.98828125; bf16 steps are 2^-6 in [2, 4), and 3.98828125 is
+    255.25 steps, so it rounds to 255 steps = 3.984375."""
+    L = oracle.lib()
+    b = lambda v: int(_bf16_bits([v])[0])
+    assert L.orc_kvq_export_value(b(1 / 8.0), b(-4.0), 37) == b(0.625)
+    assert L.orc_kvq_export_value(b(1.5 * 2 ** -7), b(1.0), 255) == b(3.984375)
+    # the Python helper unpacks 4-bit codes in the stated nibble order
+    codes = np.array([[0x21] + [0] * 31], dtype=np.uint8)
+    sc = np.array([[b(1.0)]], dtype=np.uint16)
+    bi = np.array([[b(0.0)]], dtype=np.uint16)
+    vals = oracle.kvq_export_values(codes, sc, bi, 4)
+    assert vals[0, 0] == b(1.0) and vals[0, 1] == b(2.0) and not vals[0, 2:].any()
