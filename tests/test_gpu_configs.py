@@ -140,18 +140,20 @@ def bf16_values(a):
 
 
 def check_kv_at(shape, got_k, got_v, cache, p, what):
-    """The oracle's K/V at position p against the GPU's: bf16 roundings of values that differ
-    only by the rounding drift of the hidden state through up to 31 layers (the same drift the
-    logit tolerance allows).  Every value within two bf16 steps (2^-6 relative) plus 1% of the
-    KV spread, and at most one value in a thousand more than one step apart."""
+    """The oracle's K/V at position p against the GPU's.  Both are bf16 roundings of values that
+    differ only by the rounding drift of the hidden state through up to 31 layers (the drift the
+    logit tolerance allows), so a rounding boundary can split them by a few bf16 steps: each
+    (layer, kv head) vector within 2^-7 relative L2 error, every value within 5% of the KV
+    spread.  A wrong position, head or layer is off by the order of the spread itself."""
     for name, g, o in (("K", got_k[:, :, p], cache.k[:, :, p]), ("V", got_v[:, :, p], cache.v[:, :, p])):
-        gf, of = bf16_values(g), bf16_values(o)
+        gf, of = bf16_values(g).astype(np.float64), bf16_values(o).astype(np.float64)
         err = np.abs(gf - of)
-        bad = err > 2.0 ** -6 * np.abs(of) + 0.01 * shape.kv_sigma
-        assert not bad.any(), (f"{what}: {name} at position {p}: {int(bad.sum())} values off, "
-                               f"max |gpu - oracle| = {err.max():.3e}")
-        far = err > 2.0 ** -7 * np.abs(of) + 1e-6
-        assert far.mean() <= 1e-3, f"{what}: {name} at position {p}: {int(far.sum())} values over one step"
+        rel = np.linalg.norm(gf - of, axis=-1) / np.maximum(np.linalg.norm(of, axis=-1), 1e-30)
+        worst = np.unravel_index(np.argmax(rel), rel.shape)
+        assert rel.max() <= 2.0 ** -7, (f"{what}: {name} at position {p}: relative error "
+                                        f"{rel.max():.2e} at (layer, head) {worst}")
+        assert err.max() <= 0.05 * shape.kv_sigma, (f"{what}: {name} at position {p}: "
+                                                    f"max |gpu - oracle| = {err.max():.3e}")
 
 
 def test_7b_trace_slice_joins_and_retires():
