@@ -89,6 +89,59 @@ def step_bytes(shape, ctx_lens, kv_bits: int = 16) -> float:
                  + len(ctx_lens) * (kv_tok + 4 * shape.vocab))
 
 
+def projection_bytes(shape, n: int) -> float:
+    """Algorithmic bytes of one step's projections: every weight once, the operand rows in
+    (fp32 activations), the outputs out (twice for a residual add)."""
+    d, qd, kvd, F, V = shape.d_model, shape.q_dim, shape.kv_dim, shape.d_ff, shape.vocab
+    act = shape.n_layers * (4 * n * (d + qd + 2 * kvd) + 4 * n * (qd + 2 * d) + 4 * n * (d + F)
+                            + 4 * n * (F + 2 * d)) + 4 * n * (d + V)
+    return float(shape.weight_bytes_per_step() + act)
+
+
+def attention_bytes(shape, ctx_lens, kv_bits: int = 16) -> float:
+    """Algorithmic bytes of one step's attention: each row's live KV once (positions 0..t_b),
+    the new K/V appended, q in and o out, over every layer."""
+    kv_tok = shape.kv_bytes_per_token() * ((kv_bits / 8 + 1 / 16) / 2 if kv_bits in (4, 8) else 1.0)
+    n = len(ctx_lens)
+    return float(sum((int(c) + 1) * kv_tok for c in ctx_lens) + n * kv_tok
+                 + shape.n_layers * n * 4 * 2 * shape.q_dim)
+
+
+def interval_union_ns(iv) -> float:
+    """Total length of the union of [begin, end] intervals."""
+    tot, cur_b, cur_e = 0, None, None
+    for b, e in sorted(iv):
+        if cur_e is None or b > cur_e:
+            if cur_e is not None:
+                tot += cur_e - cur_b
+            cur_b, cur_e = b, e
+        else:
+            cur_e = max(cur_e, e)
+    if cur_e is not None:
+        tot += cur_e - cur_b
+    return float(tot)
+
+
+def stamped_class_times(eng, step, i0: int, n_steps: int):
+    """Median over n_steps replayed steps of the projection and attention classes' time in the
+    step (ms), from the engine's stamps; and the projection launches per step."""
+    from continuous_batching_transformer_gb300 import binding as B
+    B.engine_set_stamps(eng.handle, True)
+    for i in range(i0, i0 + 2):  # capture the stamped step
+        step(i)
+    proj, attn, n_proj = [], [], 0
+    for i in range(i0 + 2, i0 + 2 + n_steps):
+        step(i)
+        recs = B.engine_stamps(eng.handle)
+        p_iv = [(b, e) for c, b, e in recs if c == B.KCLASS_PROJ and e >= b]
+        a_iv = [(b, e) for c, b, e in recs if c == B.KCLASS_ATTN and e >= b]
+        proj.append(interval_union_ns(p_iv) / 1e6)
+        attn.append(interval_union_ns(a_iv) / 1e6)
+        n_proj = len(p_iv)
+    B.engine_set_stamps(eng.handle, False)
+    return statistics.median(proj), statistics.median(attn), n_proj
+
+
 # ---- clocks sampled during the timed region ---------------------------------------------------
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -244,16 +297,11 @@ def gpu_arm(args, rank: int, world: int):
     launches = B.kernel_launches(eng.handle) - launches0
     ms = ev0.elapsed_time(ev1)
     clk = clocks.stop() if clocks else None
-    # Kernel rooflines: the same steps again with CUDA events around every projection and
-    # every attention launch group (the engine then launches kernel by kernel instead of
-    # replaying its captured step; the kernels and their work are the same).
+    # Kernel rooflines inside the replayed step: with stamps on, every projection and attention
+    # launch of a step records when its CTAs could start dependent work and when the last one
+    # ended (globaltimer); a class's time in the step is the union of its launches' intervals.
     KT = max(4, min(K, 16))
-    B.engine_set_timing(eng.handle, (1 << B.KCLASS_PROJ) | (1 << B.KCLASS_ATTN))
-    for i in range(W + K, W + K + KT):
-        step(i)
-    proj_ms, proj_n, proj_bytes = B.engine_timing(eng.handle, B.KCLASS_PROJ)
-    attn_ms, attn_n, attn_bytes = B.engine_timing(eng.handle, B.KCLASS_ATTN)
-    B.engine_set_timing(eng.handle, 0)
+    proj_ms, attn_ms, proj_n = stamped_class_times(eng, step, W + K, KT)
     ms_max = slowest_over_ranks(ms, dist, device)
     code, info = eng.device_error()
     if code != 0:
@@ -263,7 +311,7 @@ def gpu_arm(args, rank: int, world: int):
     # next tokens back to the host, every step
     h_tok = torch.empty(Bsz, dtype=torch.int32, pin_memory=True)
     h_out = torch.empty(Bsz, dtype=torch.int32, pin_memory=True)
-    h_tok.copy_(bufs[(W + K + KT) % 2].cpu())
+    h_tok.copy_(bufs[(W + K + KT + 2) % 2].cpu())
     d_tok = torch.empty_like(tok0)
     d_out = torch.empty_like(tok0)
     for i in range(3):
@@ -286,16 +334,18 @@ def gpu_arm(args, rank: int, world: int):
     e2e_s = slowest_over_ranks(e2e_s, dist, device)
 
     result = None
+    ctx_mean = [c + W + K / 2.0 for c in ctx]  # mean live context over the timed steps
     if rank == 0:
         peaks = measured_peaks()
         hbm_peak = peaks["hbm_gbs"] if peaks else 6800.0
         peak_src = "of measured" if peaks else "of fallback"
-        ctx_mean = [c + W + K / 2.0 for c in ctx]  # mean live context over the timed steps
         sb = step_bytes(wl.shape, ctx_mean, args.kv_bits)
         step_s = ms_max / K / 1e3
+        proj_bytes = projection_bytes(wl.shape, Bsz)
+        attn_bytes = attention_bytes(wl.shape, ctx_mean, args.kv_bits)
         achieved = proj_bytes / (proj_ms / 1e3) / 1e9 if proj_ms > 0 else None
         attn_gbs = attn_bytes / (attn_ms / 1e3) / 1e9 if attn_ms > 0 else None
-        kt_ms = ms / K * KT  # the timed region's duration for KT steps
+        step_ms = ms_max / K
         if wl.shape.weight_format == "bf16":
             traffic = measured_traffic("projection")
         else:  # the 4-bit projections stream their weights once per 8 rows
@@ -328,14 +378,16 @@ def gpu_arm(args, rank: int, world: int):
                          "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
                          "peak_source": peak_src, "unit": "GB/s",
                          "frac": achieved / hbm_peak if achieved else None,
-                         "share_of_step": proj_ms / kt_ms if kt_ms > 0 else None,
-                         "launch_groups": proj_n, "timed_steps": KT,
+                         "share_of_step": proj_ms / step_ms if step_ms > 0 else None,
+                         "launches_per_step": proj_n, "stamped_steps": KT,
+                         "timing": "in the replayed step: union of the launches' globaltimer "
+                                   "intervals, median over the stamped steps",
                          "traffic": traffic},
             "attention_roofline": {"kernel": "RoPE + KV append + split-K decode attention + merge",
                                    "bound": "hbm", "achieved": attn_gbs, "peak": hbm_peak,
                                    "unit": "GB/s",
                                    "frac": attn_gbs / hbm_peak if attn_gbs else None,
-                                   "share_of_step": attn_ms / kt_ms if kt_ms > 0 else None},
+                                   "share_of_step": attn_ms / step_ms if step_ms > 0 else None},
             "e2e": {"value": replicas_throughput(Bsz, K, world, e2e_s), "unit": "tok/s",
                     "h2d_bytes_per_step": 4 * Bsz, "d2h_bytes_per_step": 4 * Bsz},
             "gpu_launches": int(launches),

@@ -34,7 +34,7 @@ EXPORTS = ["cbt_status_str", "cbt_engine_create", "cbt_engine_destroy", "cbt_sla
            "cbt_kernel_launches", "cbt_quantize_affine4", "cbt_engine_set_timing",
            "cbt_engine_timing", "cbt_greedy_head_noalloc", "cbt_kv_slab_copy_prefix",
            "cbt_kv_slab_share_prefix", "cbt_slab_bytes_kv8", "cbt_quantize_kv8",
-           "cbt_slab_bytes_kvq", "cbt_quantize_kv"]
+           "cbt_slab_bytes_kvq", "cbt_quantize_kv", "cbt_engine_set_stamps", "cbt_engine_stamps"]
 KCLASS_PROJ, KCLASS_ATTN, KCLASS_OTHER = 0, 1, 2
 
 
@@ -126,6 +126,8 @@ def lib():
         L.cbt_greedy_head_noalloc.argtypes = [P(ModelConfig), c_void, c_int32, c_void, P(Linear),
                                               c_void, c_void, c_void]
         L.cbt_engine_set_timing.argtypes = [c_void, c_int32]
+        L.cbt_engine_set_stamps.argtypes = [c_void, c_int32]
+        L.cbt_engine_stamps.argtypes = [c_void, c_int32, P(c_int32), c_void, c_void]
         L.cbt_engine_timing.argtypes = [c_void, c_int32, P(ctypes.c_double), P(ctypes.c_int64),
                                         P(ctypes.c_double)]
         for name in EXPORTS:
@@ -287,3 +289,19 @@ def quantize_affine4(w_ptr: int, rows: int, cols: int, group: int, packed_ptr: i
                      scales_ptr: int, biases_ptr: int, stream: int = 0) -> None:
     _check(lib().cbt_quantize_affine4(w_ptr, rows, cols, group, packed_ptr, scales_ptr,
                                       biases_ptr, stream), "cbt_quantize_affine4")
+
+
+def engine_set_stamps(e: int, enable: bool) -> None:
+    _check(lib().cbt_engine_set_stamps(e, 1 if enable else 0), "cbt_engine_set_stamps")
+
+
+def engine_stamps(e: int, cap: int = 1024):
+    """The last decode step's stamps: a list of (class, begin_ns, end_ns)."""
+    import numpy as np
+    n = c_int32()
+    cls = np.zeros(cap, dtype=np.int32)
+    t = np.zeros(2 * cap, dtype=np.uint64)
+    _check(lib().cbt_engine_stamps(e, cap, ctypes.byref(n), cls.ctypes.data, t.ctypes.data),
+           "cbt_engine_stamps")
+    k = min(cap, n.value)
+    return [(int(cls[i]), int(t[2 * i]), int(t[2 * i + 1])) for i in range(k)]

@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(160, kCtasPerSm)
                   const uint8_t* __restrict__ qtile, const QueryRow* __restrict__ rows,
                   const AttnItem* __restrict__ items, const int* __restrict__ n_items_dev,
                   int layer, int n_kv_heads, int G, float* __restrict__ part_o,
-                  float2* __restrict__ part_ml, int* err) {
+                  float2* __restrict__ part_ml, int* err, unsigned long long* stamp) {
   constexpr int nKh = HD / 64;                          // K boxes (64 dims each)
   constexpr uint32_t kQBytes = 16 * HD * 2;             // Q operand image
   constexpr uint32_t kKBytes = kSub * HD * 2;           // K tile
@@ -166,6 +166,7 @@ __global__ void __launch_bounds__(160, kCtasPerSm)
   } else {
     // ---- compute warps: MMA issue (thread 0), softmax (thread = key), accumulate (thread = dim)
     pdl_wait();  // Q, the new K/V and the partial buffers are shared with earlier kernels
+    if (tid == 0) stamp_begin(stamp);
     uint32_t qn = 0, kn = 0, vn = 0, sn = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
@@ -302,6 +303,7 @@ __global__ void __launch_bounds__(160, kCtasPerSm)
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, 32);
   }
+  if (tid == 0) stamp_end(stamp);
 }
 
 // Combine the partials of each (row, q head): o = sum_i o_i e^(m_i - M) / sum_i l_i e^(m_i - M)
@@ -314,9 +316,10 @@ __global__ void __launch_bounds__(128)
     k_attn_merge(const float* __restrict__ part_o, const float2* __restrict__ part_ml,
                  const int* __restrict__ item_base, const int* __restrict__ item_count, int B,
                  int n_heads, int n_kv_heads, int head_dim, uint16_t* act, int lo_rows,
-                 float* out_f32) {
+                 float* out_f32, unsigned long long* stamp) {
   pdl_wait();
   pdl_launch();
+  if (threadIdx.x == 0) stamp_begin(stamp);
   __shared__ float wm[4], wl[4];
   __shared__ float wsum[4][128];
   const int hq = blockIdx.x, b = blockIdx.y;
@@ -366,6 +369,7 @@ __global__ void __launch_bounds__(128)
     o = o / L;
     const int K = n_heads * head_dim;
     const int col = hq * head_dim + t;
+    if (t == 0) stamp_end(stamp);
     if (out_f32) {
       out_f32[(size_t)b * K + col] = o;
       return;
@@ -387,7 +391,7 @@ cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const At
   if (rc != cudaSuccess) return rc;
   return launch_pdl(k_attn_decode<HD>, dim3(grid), dim3(160), smem, s, tk, tv, a.qtile, a.rows,
                     a.items, a.n_items, a.layer, a.n_kv_heads, a.n_heads / a.n_kv_heads, a.part_o,
-                    a.part_ml, a.err);
+                    a.part_ml, a.err, a.stamp);
 }
 
 }  // namespace
@@ -407,5 +411,5 @@ bool launch_attn_decode_tc(const CUtensorMap& tk, const CUtensorMap& tv, const A
 bool launch_attn_merge(const AttnDecodeArgs& a, cudaStream_t s) {
   return launch_pdl(k_attn_merge, dim3(a.n_heads, a.B), dim3(128), 0, s, a.part_o, a.part_ml,
                     a.item_base, a.item_count, a.B, a.n_heads, a.n_kv_heads, a.head_dim, a.act,
-                    a.act_lo, a.out_f32) == cudaSuccess;
+                    a.act_lo, a.out_f32, a.stamp_merge) == cudaSuccess;
 }

@@ -91,6 +91,21 @@ CBT_D float warp_max(float v) {
 CBT_D void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 CBT_D void pdl_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Measurement stamps: a launch given a stamp slot s (2 words) records the earliest time one of
+// its CTAs could start dependent work (min into s[0]) and the latest time one of its CTAs ended
+// (max into s[1]), in globaltimer nanoseconds.  NULL: no stamps.
+CBT_D unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+CBT_D void stamp_begin(unsigned long long* s) {
+  if (s) atomicMin(s, globaltimer_ns());
+}
+CBT_D void stamp_end(unsigned long long* s) {
+  if (s) atomicMax(s + 1, globaltimer_ns());
+}
+
 // Epilogues of a projection y = x W^T.
 enum Epilogue : int {
   EPI_STORE = 0,   // out[n][m] = y

@@ -29,6 +29,7 @@ void count_launch(int n) { g_launches += n; }
 namespace {
 
 constexpr size_t kSlabAlign = 4096;
+constexpr int kStampSlots = 1024;  // stamped launches recorded per decode step
 
 struct Slab {
   size_t offset;  // bytes into the arena (contiguous slabs)
@@ -150,7 +151,16 @@ struct cbt_engine {
   uint16_t* stage = nullptr;
   size_t stage_elems = 0;
   // captured decode steps, keyed by (B, last_tokens, logits, next_tokens)
-  std::map<std::tuple<int, const void*, const void*, const void*>, cudaGraphExec_t> graphs;
+  struct Captured {
+    cudaGraphExec_t exec;
+    std::vector<int> stamp_cls;  // kernel class of each stamp slot of the captured step
+  };
+  std::map<std::tuple<int, const void*, const void*, const void*, bool>, Captured> graphs;
+  // measurement stamps (cbt_engine_set_stamps): per stamped launch of a step, [begin, end]
+  bool stamps_on = false;
+  unsigned long long* stamp_buf = nullptr;  // [kStampSlots][2]
+  int stamp_n = 0;
+  std::vector<int> stamp_cls, last_stamp_cls;
 
   // measurement: event pairs around launch groups of selected kernel classes
   struct TimeRec {
@@ -440,7 +450,8 @@ extern "C" cbt_status cbt_engine_destroy(cbt_engine* e) {
   cudaError_t rc = cudaStreamSynchronize(e->stream);
   free_scratch(e);
   for (cudaEvent_t ev : e->ev_pool) cudaEventDestroy(ev);
-  for (auto& kv : e->graphs) cudaGraphExecDestroy(kv.second);
+  for (auto& kv : e->graphs) cudaGraphExecDestroy(kv.second.exec);
+  if (e->stamp_buf) cudaFree(e->stamp_buf);
   delete e;
   return rc == cudaSuccess ? CBT_OK : CBT_ERR_CUDA;
 }
@@ -996,6 +1007,37 @@ extern "C" cbt_status cbt_engine_timing(cbt_engine* e, int32_t cls, double* ms, 
   return CBT_OK;
 }
 
+extern "C" cbt_status cbt_engine_set_stamps(cbt_engine* e, int32_t enable) {
+  if (!e) return CBT_ERR_NULL;
+  if (cudaStreamSynchronize(e->stream) != cudaSuccess) return CBT_ERR_CUDA;
+  if (enable && !e->stamp_buf &&
+      cudaMalloc(reinterpret_cast<void**>(&e->stamp_buf), 2 * kStampSlots * sizeof(unsigned long long)) !=
+          cudaSuccess) {
+    e->stamp_buf = nullptr;
+    return CBT_ERR_CUDA;
+  }
+  e->stamps_on = enable != 0;
+  e->last_stamp_cls.clear();
+  return CBT_OK;
+}
+
+extern "C" cbt_status cbt_engine_stamps(cbt_engine* e, int32_t cap, int32_t* n, int32_t* classes,
+                                        uint64_t* times) {
+  if (!e || !n) return CBT_ERR_NULL;
+  if (cap < 0) return CBT_ERR_INVALID;
+  if (cudaStreamSynchronize(e->stream) != cudaSuccess) return CBT_ERR_CUDA;
+  const int m = (int)e->last_stamp_cls.size();
+  *n = m;
+  if (!e->stamp_buf || m == 0 || cap == 0) return CBT_OK;
+  if (!classes || !times) return CBT_ERR_NULL;
+  const int k = std::min(cap, m);
+  for (int i = 0; i < k; ++i) classes[i] = e->last_stamp_cls[i];
+  if (cudaMemcpy(times, e->stamp_buf, 2 * (size_t)k * sizeof(uint64_t), cudaMemcpyDeviceToHost) !=
+      cudaSuccess)
+    return CBT_ERR_CUDA;
+  return CBT_OK;
+}
+
 static double weight_bytes(const cbt_model_config& c, long long M, long long K) {
   if (c.weight_format == CBT_WEIGHTS_BF16) return 2.0 * M * K;
   return 0.5 * M * K + 4.0 * M * (K / c.group_size);  // codes + bf16 scale and bias
@@ -1043,6 +1085,13 @@ static const CUtensorMap* xmap_kb(cbt_engine* e, const uint16_t* buf, int K, int
   CUtensorMap m;
   if (!make_tmap_kblocks(&m, buf, K, e->act_rows, BN, kCskBlocks, 0)) return nullptr;
   return &(e->xmaps_kb[key] = m);
+}
+
+// The next stamp slot of this step for a launch of class cls (NULL when stamps are off).
+static unsigned long long* next_stamp(cbt_engine* e, int cls) {
+  if (!e->stamps_on || e->stamp_n >= kStampSlots) return nullptr;
+  e->stamp_cls.push_back(cls);
+  return e->stamp_buf + 2 * (size_t)e->stamp_n++;
 }
 
 // y = x W^T over n rows on the tensor cores, operand x in the bf16 buffer xbuf [rows][K].
@@ -1094,6 +1143,7 @@ static bool tc_projection(cbt_engine* e, const CUtensorMap& wmap, const CUtensor
   p.part = e->tc_part;
   p.cnt = e->tc_cnt;
   p.err = e->err;
+  if (n <= 32) p.stamp = next_stamp(e, CBT_KCLASS_PROJ);  // the decode projections
   const int Mo = epi == EPI_SWIGLU ? M / 2 : M;
   int t = tbegin(e, CBT_KCLASS_PROJ);
   // decode rows: cluster split-K (partial sums meet in distributed shared memory); prefill
@@ -1134,6 +1184,8 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
   const bool fused = tcp && !gather && n <= 32;
   const int lo = tc_lo_rows(e, n), lo_out = tc_lo_rows(e, n_out);
   bool ok = true;
+  e->stamp_n = 0;
+  e->stamp_cls.clear();
   int t = tbegin(e, CBT_KCLASS_OTHER);
   launch_embed(tokens, n, static_cast<const uint16_t*>(e->w.embed), d, c.vocab, e->x, e->err,
                fused ? e->ss : nullptr, e->ss_ld,
@@ -1185,6 +1237,7 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
       qa.part_o = e->att_o;
       qa.part_ml = e->att_ml;
       qa.err = e->err;
+      qa.stamp = next_stamp(e, CBT_KCLASS_ATTN);
       ok &= launch_attn_decode_q(qa, e->kv_bits, e->num_sms, s);
       AttnDecodeArgs ma{};
       ma.item_base = e->item_meta;
@@ -1198,6 +1251,7 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
       ma.act = e->act_o;
       ma.act_lo = lo;
       ma.out_f32 = tcp ? nullptr : e->o;  // the CUDA-core O projection reads fp32
+      ma.stamp_merge = next_stamp(e, CBT_KCLASS_ATTN);
       ok &= launch_attn_merge(ma, s);
     } else if (quant && e->q_codes) {
       // prefill tokens continuing quantised slabs: their K/V (in a bf16 intermediate) are
@@ -1226,6 +1280,8 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
       a.act = e->act_o;
       a.act_lo = lo;
       a.err = e->err;
+      a.stamp = next_stamp(e, CBT_KCLASS_ATTN);
+      a.stamp_merge = next_stamp(e, CBT_KCLASS_ATTN);
       ok &= launch_attn_decode_tc(e->kv_kmap, e->kv_vmap, a, e->num_sms, s);
     } else {
       if (tc_prefill)  // flash attention per segment on the tensor cores
@@ -1364,14 +1420,14 @@ static cudaError_t plan_decode_attention(cbt_engine* e, int B) {
 // (row table, attention work list and its length) lives in device buffers written before the
 // launch, so a captured graph stays valid while those buffers keep their addresses.
 static void drop_graphs(cbt_engine* e) {
-  for (auto& kv : e->graphs) cudaGraphExecDestroy(kv.second);
+  for (auto& kv : e->graphs) cudaGraphExecDestroy(kv.second.exec);
   e->graphs.clear();
 }
 
 static cudaError_t run_decode_graph(cbt_engine* e, int B, const int32_t* tokens, int max_keys,
                                     long long total_keys, float* logits, int32_t* next) {
   auto key = std::make_tuple(B, static_cast<const void*>(tokens), static_cast<const void*>(logits),
-                             static_cast<const void*>(next));
+                             static_cast<const void*>(next), e->stamps_on);
   auto it = e->graphs.find(key);
   if (it == e->graphs.end()) {
     if (e->graphs.size() >= 16) drop_graphs(e);
@@ -1388,9 +1444,10 @@ static cudaError_t run_decode_graph(cbt_engine* e, int B, const int32_t* tokens,
     rc = cudaGraphInstantiate(&ex, g, 0);
     cudaGraphDestroy(g);
     if (rc != cudaSuccess) return rc;
-    it = e->graphs.emplace(key, ex).first;
+    it = e->graphs.emplace(key, cbt_engine::Captured{ex, e->stamp_cls}).first;
   }
-  return cudaGraphLaunch(it->second, e->stream);
+  e->last_stamp_cls = it->second.stamp_cls;
+  return cudaGraphLaunch(it->second.exec, e->stream);
 }
 
 extern "C" cbt_status cbt_decode_step_batch(cbt_engine* e, const int32_t* ids, int32_t B,
@@ -1450,11 +1507,18 @@ extern "C" cbt_status cbt_decode_step_batch(cbt_engine* e, const int32_t* ids, i
     rc = upload_page_tables(e);
   }
   if (rc == cudaSuccess && e->use_tc) rc = plan_decode_attention(e, B);
+  if (rc == cudaSuccess && e->stamps_on) {  // begin slots to the maximum, end slots to 0
+    rc = cudaMemset2DAsync(e->stamp_buf, 16, 0xFF, 8, kStampSlots, e->stream);
+    if (rc == cudaSuccess)
+      rc = cudaMemset2DAsync(e->stamp_buf + 1, 16, 0, 8, kStampSlots, e->stream);
+  }
   if (rc == cudaSuccess) {
-    if (e->use_tc && e->timing_mask == 0 && e->stream != nullptr)
+    if (e->use_tc && e->timing_mask == 0 && e->stream != nullptr) {
       rc = run_decode_graph(e, B, last_tokens, max_keys, total_keys, logits, next_tokens);
-    else
+    } else {
       rc = forward(e, B, last_tokens, max_keys, total_keys, false, B, logits, next_tokens);
+      e->last_stamp_cls = e->stamp_cls;
+    }
   }
   if (rc != cudaSuccess) return rc == cudaErrorNotSupported ? CBT_ERR_UNSUPPORTED : CBT_ERR_CUDA;
   for (int b = 0; b < B; ++b) e->slabs[ids[b]].pos += 1;

@@ -274,6 +274,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   } else {  // ---- epilogue warps 2..5: TMEM lanes 32q .. 32q + 31 = tile rows
     pdl_wait();  // outputs and norm statistics are shared with the previous kernel
+    if (threadIdx.x == 64) stamp_begin(p.stamp);
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;
     if (p.ss_in) {  // RMSNorm factor of each decode row, from the per-tile sums of squares
@@ -356,6 +357,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
+  if (threadIdx.x == 0) stamp_end(p.stamp);
   if (C > 1) cluster_sync();
 }
 

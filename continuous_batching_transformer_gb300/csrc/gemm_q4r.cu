@@ -297,6 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int s = 0; s < kDepth - 1; ++s) issue();
 
   pdl_wait();
+  if (threadIdx.x == 0) stamp_begin(p.stamp);
   // ---- the operand slice of this k-range (zero columns past the pass's rows), all pieces in
   // flight at once; RMSNorm factors and the QKV epilogue's per-row inputs meanwhile
   {
@@ -495,6 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   cp_async_wait<0>();  // (only empty groups remain: every issued block was consumed)
+  if (threadIdx.x == 0) stamp_end(p.stamp);
   if (C > 1 && threadIdx.x == 0)
     for (int s = 0; s < owned; ++s) tc::mbar_wait(&inbox_full[s], 0);
   if (C > 1) csk::cluster_sync();

@@ -77,6 +77,7 @@ struct TcParams {
   uint8_t* qtile;
   // 4-bit affine weights in the native block layout of gemm_q4.cu (launch_q4_rd only)
   const uint8_t* wq;
+  unsigned long long* stamp;  // measurement stamp slot (common.cuh), or NULL
 };
 
 
@@ -145,6 +146,8 @@ struct AttnDecodeArgs {
   int act_lo;                // lo rows offset (0: plain bf16)
   int* err;
   float* out_f32;            // if set, the merge writes fp32 [B][n_heads * head_dim] here instead
+  unsigned long long* stamp;        // measurement stamp slots (common.cuh) of the attention and
+  unsigned long long* stamp_merge;  // of the merge, or NULL
 };
 // tk: the KV arena as [rows][head_dim] bf16, box {64, 128}; tv: as [rows][64], box {64, head_dim}
 bool launch_attn_decode_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnDecodeArgs& a,
@@ -181,6 +184,7 @@ struct KvqAttnArgs {
   float* part_o;         // [n_items][G][head_dim]
   float2* part_ml;       // [n_items][G]
   int* err;
+  unsigned long long* stamp;  // measurement stamp slot, or NULL
 };
 bool launch_attn_decode_q(const KvqAttnArgs& a, int bits, int num_sms, cudaStream_t s);
 // attention of prefill tokens over quantised positions [0, pos]: token t's pages (one slab: a

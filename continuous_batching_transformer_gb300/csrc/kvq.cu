@@ -208,6 +208,7 @@ __global__ void __launch_bounds__(kAttnThreads)
   const int gq = lane >> 2, tq = lane & 3;  // fragment row group and thread in group
   pdl_wait();
   pdl_launch();
+  if (tid == 0) stamp_begin(a.stamp);
   const int total = *a.n_items;
 
   // stage an item: codes of its keys (rows past the row's position zero-filled), their scales
@@ -422,6 +423,7 @@ __global__ void __launch_bounds__(kAttnThreads)
     }
   }
   cp_async_wait_all();  // no copy in flight at exit
+  if (tid == 0) stamp_end(a.stamp);
 }
 
 template <int G, int HD, int BITS>

@@ -330,6 +330,18 @@ cbt_status cbt_engine_set_timing(cbt_engine* e, int32_t class_mask);
 cbt_status cbt_engine_timing(cbt_engine* e, int32_t kclass, double* total_ms, int64_t* intervals,
                              double* algorithmic_bytes);
 
+/* In-step stamps (measurement).  With enable != 0, every later decode step -- replayed steps
+ * included -- records for each of its projection and attention launches (CBT_KCLASS_PROJ,
+ * CBT_KCLASS_ATTN) the earliest time one of the launch's CTAs could start work that depends on
+ * the previous kernel and the latest time one of them ended, in globaltimer nanoseconds.  The
+ * stamps change no result.  cbt_engine_stamps synchronises the stream and copies the records of
+ * the last decode step: *n = their number; for i < min(cap, *n) classes[i] = the launch's class,
+ * times[2i] = begin, times[2i + 1] = end.  (A step's launches overlap through programmatic
+ * dependent launch; the union of a class's intervals is its share of the step.) */
+cbt_status cbt_engine_set_stamps(cbt_engine* e, int32_t enable);
+cbt_status cbt_engine_stamps(cbt_engine* e, int32_t cap, int32_t* n, int32_t* classes,
+                             uint64_t* times);
+
 /* MLX-style 4-bit affine quantisation of a bf16 matrix on the device, groups of `group`
  * (64) along each row: scale = bf16((max - min) / 15), bias = bf16(min),
  * q = clamp(rint((w - bias) / scale), 0, 15) (ties to even; 0 when scale == 0), packed

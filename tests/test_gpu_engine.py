@@ -216,3 +216,33 @@ def test_prefix_copy_then_continue(weights):
         feed = np.array([oracle.argmax(x) for x in ref], np.int32)
     assert eng.device_error() == (0, 0)
     eng.close()
+
+
+def test_decode_stamps_cover_every_projection_and_attention_launch():
+    """cbt_engine_set_stamps: a replayed decode step records a [begin, end] interval for each
+    projection (4 per layer and the lm_head) and each attention launch (attention and merge per
+    layer); stamps change no result."""
+    ensure_built()
+    from continuous_batching_transformer_gb300 import binding as B
+    dev = torch.device("cuda:0")
+    w = DeviceWeights(TINY, dev)
+    eng = Engine(w, arena_bytes=32 << 20, max_batch=4, max_prefill_tokens=64)
+    slabs = [eng.kv_slab_alloc(64) for _ in range(3)]
+    eng.prefill_segmented(slabs, [5, 9, 3], torch.arange(17, dtype=torch.int32, device=dev))
+    tok = torch.tensor([1, 2, 3], dtype=torch.int32, device=dev)
+    lg0 = torch.empty((3, TINY.vocab), dtype=torch.float32, device=dev)
+    lg1 = torch.empty_like(lg0)
+    eng.decode_step_batch(slabs, tok, lg0)
+    B.engine_set_stamps(eng.handle, True)
+    for _ in range(2):
+        eng.decode_step_batch(slabs, tok, lg1)
+    recs = B.engine_stamps(eng.handle)
+    B.engine_set_stamps(eng.handle, False)
+    n_proj = sum(1 for c, _, _ in recs if c == B.KCLASS_PROJ)
+    n_attn = sum(1 for c, _, _ in recs if c == B.KCLASS_ATTN)
+    assert n_proj == 4 * TINY.n_layers + 1 and n_attn == 2 * TINY.n_layers
+    assert all(0 < b <= e for _, b, e in recs)
+    span = max(e for _, _, e in recs) - min(b for _, b, _ in recs)
+    assert span < 1e9  # one step, in nanoseconds
+    assert eng.device_error() == (0, 0)
+    eng.close()
