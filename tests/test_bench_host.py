@@ -21,4 +21,4 @@ def test_byte_counts():
     assert 32 * 1.5e6 < extra < 32 * 2.5e6
     # attention: 131072 bytes of KV per live position per row, plus the appended one
     assert bench.attention_bytes(s, [99], 16) > 101 * 131072
-    assert abs(bench.attention_bytes(s, [99], 8) / bench.attention_bytes(s, [99], 16) - 1.0625 / 2) < 0.01
+    assert abs(bench.attention_bytes(s, [9999], 8) / bench.attention_bytes(s, [9999], 16) - 1.0625 / 2) < 0.01
