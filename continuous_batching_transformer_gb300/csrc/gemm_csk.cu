@@ -265,12 +265,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // this CTA's arrival at barrier k - 1 comes first: its release fence then waits for no
         // weight tile in flight, and the next phase's weights stream while the other CTAs arrive
         if (k > 0) {
-          // (the previous phases' pending operands first: that arrival needs their MMAs)
-          if (npend > 0 && !flush_pending()) {
-            report_timeout(p0, abort_flag, 6);
-            ok = false;
-            break;
-          }
           volatile uint64_t* tgt = sm.bar_target + (k - 1);
           uint32_t i = 0;
           for (; i < tc::kSpinLimit && *tgt == 0 && !*abort_flag; ++i)
