@@ -262,19 +262,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; k < NP && ok; ++k) {
         const CskPhase& A = ch.ph[k];
         const Geo g = geo_of(A.p, cid, NC, C, rank, NK);
-        // this CTA's arrival at barrier k - 1 comes first: its release fence then waits for no
-        // weight tile in flight, and the next phase's weights stream while the other CTAs arrive
-        if (k > 0) {
-          volatile uint64_t* tgt = sm.bar_target + (k - 1);
-          uint32_t i = 0;
-          for (; i < tc::kSpinLimit && *tgt == 0 && !*abort_flag; ++i)
-            if (i > 64) __nanosleep(64);
-          if (*tgt == 0) {
-            report_timeout(p0, abort_flag, 8);
-            ok = false;
-            break;
-          }
-        }
         for (int j = 0; j < g.Tc && ok; ++j) {
           const int rb = cid + j * NC;
           for (int sb = g.sb0; sb < g.sb1; ++sb) {
