@@ -434,9 +434,7 @@ extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_w
                 make_tmap_bf16(&e->q_map, e->qb, qd, 2 * e->qb_rows, 64, 128);
       if (rc == cudaSuccess) rc = cudaMemsetAsync(e->qtile, 0, qbytes, e->stream);
       e->ss_ld = std::max(32, p->max_batch);
-      // one set of chain-barrier counters per layer: every chained launch of a step counts
-      // from zero
-      chk(dmalloc(&e->chain_bar, (size_t)kMaxCskPhases * c.n_layers, &tot));
+      chk(dmalloc(&e->chain_bar, (size_t)kMaxCskPhases, &tot));
       chk(dmalloc(&e->ss, (size_t)((c.d_model + 127) / 128) * e->ss_ld, &tot));
     }
     e->use_tc = maps_ok && c.d_ff % 64 == 0;
@@ -1187,12 +1185,11 @@ static void open_chain(cbt_engine* e) {
   e->chain_t = tbegin(e, CBT_KCLASS_PROJ);
 }
 
-static bool close_chain(cbt_engine* e, int n, int layer) {
+static bool close_chain(cbt_engine* e, int n) {
   e->chain_open = false;
   const int BN = tc_split_bn(n);
   const bool ok = launch_tc_csk_chain(e->chain.data(), (int)e->chain.size(), BN, e->num_sms,
-                                      e->chain_bar + (size_t)layer * kMaxCskPhases,
-                                      next_stamp(e, CBT_KCLASS_PROJ), e->stream);
+                                      e->chain_bar, next_stamp(e, CBT_KCLASS_PROJ), e->stream);
   tend(e, e->chain_t, e->chain_bytes);
   e->chain.clear();
   return ok;
@@ -1226,9 +1223,8 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
   bool ok = true;
   e->stamp_n = 0;
   e->stamp_cls.clear();
-  if (chained && cudaMemsetAsync(e->chain_bar, 0,
-                                 (size_t)kMaxCskPhases * c.n_layers * sizeof(unsigned long long),
-                                 s) != cudaSuccess)
+  if (chained &&
+      cudaMemsetAsync(e->chain_bar, 0, kMaxCskPhases * sizeof(unsigned long long), s) != cudaSuccess)
     return cudaErrorLaunchFailure;
   float* lg = logits ? logits : e->logits;
   auto qkv_proj = [&](int l) {
@@ -1373,7 +1369,7 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
                           false, fused ? next_g : nullptr);
       if (chained) {
         ok &= l + 1 < c.n_layers ? qkv_proj(l + 1) : lm_proj();
-        ok &= close_chain(e, n, l);
+        ok &= close_chain(e, n);
       }
     } else {
       projection(e, e->h, n, d, L.wgu, 2 * F, EPI_SWIGLU, e->act);

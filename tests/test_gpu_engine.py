@@ -242,6 +242,7 @@ def test_decode_stamps_cover_every_projection_and_attention_launch():
     n_proj = sum(1 for c, _, _ in recs if c == B.KCLASS_PROJ)
     n_attn = sum(1 for c, _, _ in recs if c == B.KCLASS_ATTN)
     assert n_proj == TINY.n_layers + 1 and n_attn == 2 * TINY.n_layers
+    np.testing.assert_array_equal(lg0.cpu().numpy(), lg1.cpu().numpy())
     assert all(0 < b <= e for _, b, e in recs)
     span = max(e for _, _, e in recs) - min(b for _, b, _ in recs)
     assert span < 1e9  # one step, in nanoseconds
