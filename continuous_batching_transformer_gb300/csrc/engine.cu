@@ -157,13 +157,6 @@ struct cbt_engine {
   };
   std::map<std::tuple<int, const void*, const void*, const void*, bool>, Captured> graphs;
   // measurement stamps (cbt_engine_set_stamps): per stamped launch of a step, [begin, end]
-  // chained decode projections (O, gate/up, down, next QKV or lm_head in one launch): the
-  // phases being collected, their grid-barrier counters (zeroed at every step's start)
-  bool chain_open = false;
-  std::vector<CskChainPhase> chain;
-  double chain_bytes = 0.0;
-  int chain_t = -1;
-  unsigned long long* chain_bar = nullptr;
   bool stamps_on = false;
   unsigned long long* stamp_buf = nullptr;  // [kStampSlots][2]
   int stamp_n = 0;
@@ -209,7 +202,7 @@ static void free_scratch(cbt_engine* e) {
                   e->rows,    e->err,      e->act_h, e->act_o, e->act_u,  e->tc_part,
                   e->tc_cnt,  e->items,    e->item_meta, e->att_o, e->att_ml, e->stage,
                   e->qtile,   e->ss,       e->qb,     e->pf_units, e->q4_arena, e->pagetab,
-                  e->tok_pages, e->kv8_jobs, e->chain_bar};
+                  e->tok_pages, e->kv8_jobs};
   for (void* q : ptrs)
     if (q) cudaFree(q);
 }
@@ -434,7 +427,6 @@ extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_w
                 make_tmap_bf16(&e->q_map, e->qb, qd, 2 * e->qb_rows, 64, 128);
       if (rc == cudaSuccess) rc = cudaMemsetAsync(e->qtile, 0, qbytes, e->stream);
       e->ss_ld = std::max(32, p->max_batch);
-      chk(dmalloc(&e->chain_bar, (size_t)kMaxCskPhases, &tot));
       chk(dmalloc(&e->ss, (size_t)((c.d_model + 127) / 128) * e->ss_ld, &tot));
     }
     e->use_tc = maps_ok && c.d_ff % 64 == 0;
@@ -1151,16 +1143,8 @@ static bool tc_projection(cbt_engine* e, const CUtensorMap& wmap, const CUtensor
   p.part = e->tc_part;
   p.cnt = e->tc_cnt;
   p.err = e->err;
-  const int Mo = epi == EPI_SWIGLU ? M / 2 : M;
-  const double bytes = weight_bytes(e->cfg, M, K) + 4.0 * n * K + 4.0 * n * Mo * (epi == EPI_ADD ? 2 : 1);
-  if (e->chain_open) {  // a phase of the open chain (bf16 decode projections only)
-    if (!split || e->cfg.weight_format != CBT_WEIGHTS_BF16 || e->chain.size() >= (size_t)kMaxCskPhases)
-      return false;
-    e->chain.push_back(CskChainPhase{&wmap_kb, xm, p});
-    e->chain_bytes += bytes;
-    return true;
-  }
   if (n <= 32) p.stamp = next_stamp(e, CBT_KCLASS_PROJ);  // the decode projections
+  const int Mo = epi == EPI_SWIGLU ? M / 2 : M;
   int t = tbegin(e, CBT_KCLASS_PROJ);
   // decode rows: cluster split-K (partial sums meet in distributed shared memory); prefill
   // tokens: whole tiles per CTA
@@ -1173,25 +1157,7 @@ static bool tc_projection(cbt_engine* e, const CUtensorMap& wmap, const CUtensor
                : launch_tc_linear(wmap, *xm, p, split, BN, e->num_sms, e->tc_part_floats,
                                   e->stream);
   }
-  tend(e, t, bytes);
-  return ok;
-}
-
-// Chains: the projections queued between open_chain and close_chain run as one launch.
-static void open_chain(cbt_engine* e) {
-  e->chain.clear();
-  e->chain_bytes = 0.0;
-  e->chain_open = true;
-  e->chain_t = tbegin(e, CBT_KCLASS_PROJ);
-}
-
-static bool close_chain(cbt_engine* e, int n) {
-  e->chain_open = false;
-  const int BN = tc_split_bn(n);
-  const bool ok = launch_tc_csk_chain(e->chain.data(), (int)e->chain.size(), BN, e->num_sms,
-                                      e->chain_bar, next_stamp(e, CBT_KCLASS_PROJ), e->stream);
-  tend(e, e->chain_t, e->chain_bytes);
-  e->chain.clear();
+  tend(e, t, weight_bytes(e->cfg, M, K) + 4.0 * n * K + 4.0 * n * Mo * (epi == EPI_ADD ? 2 : 1));
   return ok;
 }
 
@@ -1216,26 +1182,10 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
   // decode on the tensor cores folds every RMSNorm into the projection that consumes it:
   // the residual-add epilogues and the embedding leave per-tile sums of squares in e->ss
   const bool fused = tcp && !gather && n <= 32;
-  // bf16 decode: after each layer's attention, O, gate/up, down and the next layer's QKV (the
-  // last layer: the lm_head) run as one chained launch; its grid barriers count from zero
-  const bool chained = fused && c.weight_format == CBT_WEIGHTS_BF16 && e->chain_bar;
   const int lo = tc_lo_rows(e, n), lo_out = tc_lo_rows(e, n_out);
   bool ok = true;
   e->stamp_n = 0;
   e->stamp_cls.clear();
-  if (chained &&
-      cudaMemsetAsync(e->chain_bar, 0, kMaxCskPhases * sizeof(unsigned long long), s) != cudaSuccess)
-    return cudaErrorLaunchFailure;
-  float* lg = logits ? logits : e->logits;
-  auto qkv_proj = [&](int l) {
-    return tc_projection(e, e->wmaps[l].qkv, e->wmaps_kb[l].qkv, e->q4w[l].qkv, e->act_h, n, d,
-                         qd + 2 * kvd, fused ? EPI_QKV : EPI_STORE, e->qkv, qd + 2 * kvd, nullptr, 0,
-                         fused, nullptr, l);
-  };
-  auto lm_proj = [&]() {
-    return tc_projection(e, e->lm_map, e->lm_map_kb, e->q4_lm, e->act_h, n_out, d, c.vocab,
-                         EPI_STORE, lg, c.vocab, nullptr, 0, fused);
-  };
   int t = tbegin(e, CBT_KCLASS_OTHER);
   launch_embed(tokens, n, static_cast<const uint16_t*>(e->w.embed), d, c.vocab, e->x, e->err,
                fused ? e->ss : nullptr, e->ss_ld,
@@ -1255,11 +1205,12 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
     }
     // decode on the tensor cores rotates q and k, appends K/V and lays out the attention's Q
     // operand in the QKV projection's epilogue; otherwise a separate kernel does it
-    if (tcp) {
-      if (!chained || l == 0) ok &= qkv_proj(l);  // chained: queued by the previous layer
-    } else {
+    if (tcp)
+      ok &= tc_projection(e, e->wmaps[l].qkv, e->wmaps_kb[l].qkv, e->q4w[l].qkv, e->act_h, n, d, qd + 2 * kvd,
+                          fused ? EPI_QKV : EPI_STORE, e->qkv, qd + 2 * kvd, nullptr, 0, fused,
+                          nullptr, l);
+    else
       projection(e, e->h, n, d, L.wqkv, qd + 2 * kvd, EPI_STORE, e->qkv);
-    }
     t = tbegin(e, CBT_KCLASS_ATTN);
     const bool tc_prefill = tcp && gather && e->pf_n > 0;
     if (!fused)
@@ -1346,7 +1297,6 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
       if (tcp) launch_f32_to_act(e->o, n, qd, e->act_o, lo, s);
     }
     tend(e, t, attn_bytes);
-    if (chained) open_chain(e);
     if (tcp)
       ok &= tc_projection(e, e->wmaps[l].o, e->wmaps_kb[l].o, e->q4w[l].o, e->act_o, n, qd, d, EPI_ADD, e->x, d, nullptr, 0,
                           false, fused ? fn : nullptr);
@@ -1367,10 +1317,6 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
                                    : static_cast<const uint16_t*>(e->w.final_norm);
       ok &= tc_projection(e, e->wmaps[l].d, e->wmaps_kb[l].d, e->q4w[l].d, e->act_u, n, F, d, EPI_ADD, e->x, d, nullptr, 0,
                           false, fused ? next_g : nullptr);
-      if (chained) {
-        ok &= l + 1 < c.n_layers ? qkv_proj(l + 1) : lm_proj();
-        ok &= close_chain(e, n);
-      }
     } else {
       projection(e, e->h, n, d, L.wgu, 2 * F, EPI_SWIGLU, e->act);
       projection(e, e->act, n, F, L.wd, d, EPI_ADD, e->x);
@@ -1390,8 +1336,11 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
     else launch_rmsnorm(xf, gn, n_out, d, c.rms_eps, hf, s);
     tend(e, t, 8.0 * n_out * d);
   }
+  float* lg = logits ? logits : e->logits;
   if (tcp) {
-    if (!chained && !lm_proj()) return cudaErrorNotSupported;  // chained: in the last chain
+    if (!tc_projection(e, e->lm_map, e->lm_map_kb, e->q4_lm, e->act_h, n_out, d, c.vocab, EPI_STORE, lg, c.vocab, nullptr,
+                       0, fused))
+      return cudaErrorNotSupported;
   } else {
     projection(e, hf, n_out, d, e->w.lm_head, c.vocab, EPI_STORE, lg);
   }

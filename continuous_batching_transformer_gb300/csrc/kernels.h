@@ -107,25 +107,12 @@ struct CskPlan {
   int nk;      // 64-column blocks per stage (one TMA box of weights, one of operand)
 };
 constexpr int kCskBlocks = 2;  // nk of the decode projections' tensor maps
-constexpr int kMaxCskPhases = 4;  // projections one chained launch runs
-// plan for the projections RB[k] x KS[k] (row tiles, 64-column blocks) run by one launch
-bool csk_plan(const int* RB, const int* KS, int n, int BN, int num_sms, CskPlan* out);
+bool csk_plan(int RB, int KS, int BN, int num_sms, CskPlan* out);
 // y = x W^T over n_act <= BN/2 decode rows (hi/lo operand), any TcParams epilogue.  tw: the
 // weights as make_tmap_kblocks(.., 128 rows (SwiGLU: 64 + 64), kCskBlocks, ..); tx: the operand
 // as make_tmap_kblocks(.., BN rows, kCskBlocks, 0).
 bool launch_tc_csk(const CUtensorMap& tw, const CUtensorMap& tx, TcParams p, int BN, int num_sms,
                    cudaStream_t s);
-// A chain: n <= kMaxCskPhases decode projections that follow each other (each one's operand and
-// epilogue inputs produced by the earlier ones, or before the launch) in one persistent launch,
-// the phases separated by grid barriers over the counters bar[0 .. n - 2] (device, zero when the
-// launch starts; NULL for n == 1).  stamp: the launch's measurement slot (or NULL).
-struct CskChainPhase {
-  const CUtensorMap* tw;  // as launch_tc_csk
-  const CUtensorMap* tx;
-  TcParams p;
-};
-bool launch_tc_csk_chain(const CskChainPhase* ph, int n, int BN, int num_sms,
-                         unsigned long long* bar, unsigned long long* stamp, cudaStream_t s);
 
 // ---- 4-bit affine decode projections (gemm_q4.cu: device layout; gemm_q4r.cu: kernel) ------
 // Native layout: per (128-row tile, 128-column superblock) one block of kQ4BlockBytes (codes
