@@ -19,7 +19,6 @@
 // previous kernel finishes, operand tiles after), an MMA warp (swap-AB: 128 weight rows x N
 // operand rows, bf16 hi/lo operand parts, fp32 accumulators in TMEM), four epilogue warps.
 #include <algorithm>
-#include <cstdlib>
 #include <map>
 #include <tuple>
 
@@ -37,16 +36,7 @@ constexpr int kThreads = 192;       // warp 0 TMA, warp 1 MMA (+TMEM alloc), war
 constexpr int kABytes = 128 * 128;  // 128 rows x 64 bf16
 constexpr int kMaxStages = 8;
 constexpr int kMaxSlots = 4;        // tiles one CTA owns in a launch
-constexpr int kSmemBudgetMax = 227 * 1024;
-// shared memory one CTA may take (experiment: CBT_CSK_SMEM_KB)
-static int smem_budget() {
-  static int v = [] {
-    const char* e = getenv("CBT_CSK_SMEM_KB");
-    const int kb = e ? atoi(e) : 227;
-    return (kb > 0 && kb <= 227 ? kb : 227) * 1024;
-  }();
-  return v;
-}
+constexpr int kSmemBudget = 227 * 1024;
 constexpr int kAcc = 4;             // accumulators per tile (see k_tc_csk)
 
 using csk::cluster_rank;
@@ -110,7 +100,7 @@ __device__ __forceinline__ Smem carve(uint8_t* smem, const CskPlan& q, bool qkv)
 }
 
 template <int BN>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     k_tc_csk(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tx,
              const TcParams p, const CskPlan q) {
   constexpr int H = BN / 2;  // operand rows: H hi parts, then H lo parts
@@ -439,7 +429,7 @@ bool csk_plan(int RB, int KS, int BN, int num_sms, CskPlan* out) {
     q.slots = C > 1 ? (tmax + C - 1) / C : 0;
     if (q.slots > kMaxSlots) continue;
     q.stages = 2;  // the shallowest pipeline a launch may get
-    if (csk_smem_bytes<64>(q, true) > (size_t)smem_budget()) continue;
+    if (csk_smem_bytes<64>(q, true) > (size_t)kSmemBudget) continue;
     const int fit = active_clusters<64>(C, csk_smem_bytes<64>(q, true));
     if (fit <= 0) continue;
     if (fit < q.NC) q.NC = fit;
@@ -459,8 +449,8 @@ bool csk_plan(int RB, int KS, int BN, int num_sms, CskPlan* out) {
     return BN == 16 ? csk_smem_bytes<16>(q, true)
                     : BN == 32 ? csk_smem_bytes<32>(q, true) : csk_smem_bytes<64>(q, true);
   };
-  while (bp.stages > 2 && smem(bp) > (size_t)smem_budget()) --bp.stages;
-  if (smem(bp) > (size_t)smem_budget()) return false;
+  while (bp.stages > 2 && smem(bp) > (size_t)kSmemBudget) --bp.stages;
+  if (smem(bp) > (size_t)kSmemBudget) return false;
   *out = bp;
   return true;
 }
