@@ -29,10 +29,9 @@
 // SwiGLU, RoPE + K/V append + the attention's Q operand).  C is chosen from the matrix shape
 // and the number of clusters of C CTAs that fit on the GPU at once.
 //
-// Batch rows are taken 16 at a time where the k-range's operand slice of 16 rows fits in shared
-// memory, else 8 at a time (gridDim.y passes, each over the same weights): a row's arithmetic
-// -- the k split, the group order, the fold -- depends on the matrix shape alone, so a row's
-// result does not depend on how many rows share the step.
+// Batch rows are taken 8 at a time (gridDim.y passes, each over the same weights): a row's
+// arithmetic -- the k split, the group order, the fold -- depends on the matrix shape alone,
+// so a row's result does not depend on how many rows share the step.
 //
 // The weights are the native block layout of gemm_q4.cu: per (128-row tile, 128-column
 // superblock) [4 chunks][128 rows][16 bytes] of codes (chunk c holds columns 32c .. 32c + 31 of
@@ -68,7 +67,6 @@ struct Q4rPlan {
   int NC;      // clusters
   int slots;   // inbox slots: most tiles one CTA owns
   int sb_max;  // most superblocks of one rank
-  int wide;    // 1: the plan fits 16-row passes (NB8 = 4), else 8-row passes
 };
 
 __host__ __device__ constexpr size_t align16(size_t v) { return (v + 15) & ~size_t(15); }
@@ -187,12 +185,12 @@ __device__ __forceinline__ void report_timeout(const TcParams& p, volatile int* 
   if (atomicCAS(p.err, 0, CBT_DEV_TIMEOUT) == 0) p.err[1] = 500 + role;
 }
 
-// The projection's parameters for batch rows [R pass, R pass + R) (R rows a pass): every
-// per-row pointer moves to the pass's first row; lo-part row offsets are absolute and stay.
-__device__ __forceinline__ TcParams pass_params(const TcParams& p0, int pass, int R) {
+// The projection's parameters for batch rows [8 pass, 8 pass + 8): every per-row pointer moves
+// to the pass's first row; lo-part row offsets are absolute and stay.
+__device__ __forceinline__ TcParams pass_params(const TcParams& p0, int pass) {
   TcParams p = p0;
-  const int r0 = R * pass;
-  p.n_act = min(R, p0.n_act - r0);
+  const int r0 = 8 * pass;
+  p.n_act = min(8, p0.n_act - r0);
   if (p.out) p.out += (size_t)r0 * p.ldo;
   if (p.next_act) p.next_act += (size_t)r0 * p.ldo;
   if (p.act) p.act += (size_t)r0 * p.act_ld;
@@ -230,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.flags);
 
   const int pass = blockIdx.y;
-  const TcParams p = pass_params(p0, pass, H);
+  const TcParams p = pass_params(p0, pass);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const int C = q.C;
@@ -307,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int n = warp; n < N; n += kWarps) {
       const int b = n % H;
       const bool valid = b < p.n_act;
-      const size_t row = n >= H ? (size_t)(x_lo + H * pass + b) : (size_t)(H * pass + b);
+      const size_t row = n >= H ? (size_t)(x_lo + 8 * pass + b) : (size_t)(8 * pass + b);
       const uint16_t* src = x + row * p.K + (size_t)sb0 * 128;
       const uint32_t dst = tc::smem_u32(xs + (size_t)n * pitch);
       for (int c = lane; c < per_row; c += 32)
@@ -541,8 +539,7 @@ int q4r_active_clusters(int C, size_t smem) {
 // streams, plus a little for each cluster hand-off.  How many clusters of C CTAs run at once is
 // asked of the occupancy calculator (clusters are placed within GPCs, so fewer than
 // num_sms / C may fit), at the widest operand's shared memory.
-template <int NB8>
-bool q4r_split_for(int RB, int SB, int num_sms, Q4rPlan* out) {
+bool q4r_split(int RB, int SB, int num_sms, Q4rPlan* out) {
   static const int kSizes[] = {1, 2, 3, 4, 6, 8};
   double best = 1e30;
   Q4rPlan bp{};
@@ -554,14 +551,14 @@ bool q4r_split_for(int RB, int SB, int num_sms, Q4rPlan* out) {
     if (q.sb_max > kMaxSbPerRank) continue;
     q.NC = std::min(RB, num_sms / C);
     q.slots = C > 1 ? ((RB + q.NC - 1) / q.NC + C - 1) / C : 0;
-    if (q.slots > kMaxSlots || q4r_smem<NB8>(q) > (size_t)kSmemBudget) continue;
-    const int fit = q4r_active_clusters<NB8>(C, q4r_smem<NB8>(q));
+    if (q.slots > kMaxSlots || q4r_smem<2>(q) > (size_t)kSmemBudget) continue;
+    const int fit = q4r_active_clusters<2>(C, q4r_smem<2>(q));
     if (fit <= 0) continue;
     if (fit < q.NC) {
       q.NC = fit;
       q.slots = C > 1 ? ((RB + q.NC - 1) / q.NC + C - 1) / C : 0;
-      if (q.slots > kMaxSlots || q4r_smem<NB8>(q) > (size_t)kSmemBudget ||
-          q4r_active_clusters<NB8>(C, q4r_smem<NB8>(q)) < q.NC)
+      if (q.slots > kMaxSlots || q4r_smem<2>(q) > (size_t)kSmemBudget ||
+          q4r_active_clusters<2>(C, q4r_smem<2>(q)) < q.NC)
         continue;
     }
     const int tmax = (RB + q.NC - 1) / q.NC;
@@ -572,15 +569,8 @@ bool q4r_split_for(int RB, int SB, int num_sms, Q4rPlan* out) {
     }
   }
   if (best >= 1e30) return false;
-  bp.wide = NB8 == 4;
   *out = bp;
   return true;
-}
-
-// The plan is sized for 16-row passes where some split of the k-range fits them, else for
-// 8-row passes; either way it depends on the matrix shape alone.
-bool q4r_split(int RB, int SB, int num_sms, Q4rPlan* out) {
-  return q4r_split_for<4>(RB, SB, num_sms, out) || q4r_split_for<2>(RB, SB, num_sms, out);
 }
 
 template <int NB8>
@@ -630,10 +620,7 @@ bool launch_q4_rd(TcParams p, const uint16_t* x, int x_lo, int num_sms, cudaStre
     if (!q4r_split(p.RB, p.K / 128, num_sms, &q)) return false;
     plans[key] = q;
   }
-  if (p.n_act <= 4) return q4r_launch<1>(p, x, x_lo, q, 1, s);
-  // 16 rows a pass where their operand slice fits beside the ring: the weights are then read
-  // once for every 16 rows instead of every 8
-  if (p.n_act > 8 && q.wide)
-    return q4r_launch<4>(p, x, x_lo, q, (p.n_act + 15) / 16, s);
-  return q4r_launch<2>(p, x, x_lo, q, (p.n_act + 7) / 8, s);
+  const int passes = (p.n_act + 7) / 8;
+  return p.n_act <= 4 ? q4r_launch<1>(p, x, x_lo, q, passes, s)
+                      : q4r_launch<2>(p, x, x_lo, q, passes, s);
 }
