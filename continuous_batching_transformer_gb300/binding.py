@@ -34,7 +34,8 @@ EXPORTS = ["cbt_status_str", "cbt_engine_create", "cbt_engine_destroy", "cbt_sla
            "cbt_kernel_launches", "cbt_quantize_affine4", "cbt_engine_set_timing",
            "cbt_engine_timing", "cbt_greedy_head_noalloc", "cbt_kv_slab_copy_prefix",
            "cbt_kv_slab_share_prefix", "cbt_slab_bytes_kv8", "cbt_quantize_kv8",
-           "cbt_slab_bytes_kvq", "cbt_quantize_kv", "cbt_engine_set_stamps", "cbt_engine_stamps"]
+           "cbt_slab_bytes_kvq", "cbt_quantize_kv", "cbt_engine_set_stamps", "cbt_engine_stamps",
+           "cbt_engine_test_stall"]
 KCLASS_PROJ, KCLASS_ATTN, KCLASS_OTHER = 0, 1, 2
 
 
@@ -127,6 +128,7 @@ def lib():
                                               c_void, c_void, c_void]
         L.cbt_engine_set_timing.argtypes = [c_void, c_int32]
         L.cbt_engine_set_stamps.argtypes = [c_void, c_int32]
+        L.cbt_engine_test_stall.argtypes = [c_void, c_int32]
         L.cbt_engine_stamps.argtypes = [c_void, c_int32, P(c_int32), c_void, c_void]
         L.cbt_engine_timing.argtypes = [c_void, c_int32, P(ctypes.c_double), P(ctypes.c_int64),
                                         P(ctypes.c_double)]
@@ -305,3 +307,7 @@ def engine_stamps(e: int, cap: int = 1024):
            "cbt_engine_stamps")
     k = min(cap, n.value)
     return [(int(cls[i]), int(t[2 * i]), int(t[2 * i + 1])) for i in range(k)]
+
+
+def engine_test_stall(e: int, spin_limit: int) -> None:
+    _check(lib().cbt_engine_test_stall(e, spin_limit), "cbt_engine_test_stall")

@@ -42,8 +42,9 @@ __device__ __forceinline__ bool wait_or_abort_sleep(uint64_t* bar, uint32_t pari
   return false;
 }
 
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  for (uint32_t i = 0; i < tc::kSpinLimit; ++i) {
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                              uint32_t limit = tc::kSpinLimit) {
+  for (uint32_t i = 0; i < limit; ++i) {
     if (tc::mbar_try_wait(bar, parity)) return true;
     if ((i & 1023) == 1023 && *abort) return false;
     if (i > 256) __nanosleep(32);
@@ -60,14 +61,15 @@ template <int H>
 __device__ __forceinline__ int combine_partials(const float (&vals)[H], float (&sum)[H],
                                                 float* inbox, uint64_t* inbox_full, int slot,
                                                 uint32_t rank, uint32_t owner, int C, int r,
-                                                volatile int* abort_flag) {
+                                                volatile int* abort_flag,
+                                                uint32_t limit = tc::kSpinLimit) {
   if (rank == owner) {
     if (C == 1) {
 #pragma unroll
       for (int n = 0; n < H; ++n) sum[n] = vals[n];
       return 1;
     }
-    if (!wait_or_abort(&inbox_full[slot], 0, abort_flag)) return -1;
+    if (!wait_or_abort(&inbox_full[slot], 0, abort_flag, limit)) return -1;
 #pragma unroll
     for (int n = 0; n < H; ++n) sum[n] = 0.f;
     for (int src = 0; src < C; ++src) {

@@ -157,6 +157,10 @@ struct cbt_engine {
   };
   std::map<std::tuple<int, const void*, const void*, const void*, bool>, Captured> graphs;
   // measurement stamps (cbt_engine_set_stamps): per stamped launch of a step, [begin, end]
+  // failure-detection test (cbt_engine_test_stall): the next decode step's lm_head projection
+  // requests nothing and its waits give up after stall_limit polls
+  uint32_t stall_limit = 0;
+  bool stall_now = false;
   bool stamps_on = false;
   unsigned long long* stamp_buf = nullptr;  // [kStampSlots][2]
   int stamp_n = 0;
@@ -1007,6 +1011,14 @@ extern "C" cbt_status cbt_engine_timing(cbt_engine* e, int32_t cls, double* ms, 
   return CBT_OK;
 }
 
+extern "C" cbt_status cbt_engine_test_stall(cbt_engine* e, int32_t spin_limit) {
+  if (!e) return CBT_ERR_NULL;
+  if (spin_limit <= 0) return CBT_ERR_INVALID;
+  if (!e->use_tc || e->cfg.weight_format != CBT_WEIGHTS_BF16) return CBT_ERR_UNSUPPORTED;
+  e->stall_limit = (uint32_t)spin_limit;
+  return CBT_OK;
+}
+
 extern "C" cbt_status cbt_engine_set_stamps(cbt_engine* e, int32_t enable) {
   if (!e) return CBT_ERR_NULL;
   if (cudaStreamSynchronize(e->stream) != cudaSuccess) return CBT_ERR_CUDA;
@@ -1144,6 +1156,11 @@ static bool tc_projection(cbt_engine* e, const CUtensorMap& wmap, const CUtensor
   p.cnt = e->tc_cnt;
   p.err = e->err;
   if (n <= 32) p.stamp = next_stamp(e, CBT_KCLASS_PROJ);  // the decode projections
+  if (e->stall_now) {
+    p.stall_loads = 1;
+    p.spin_limit = e->stall_limit;
+    e->stall_now = false;
+  }
   const int Mo = epi == EPI_SWIGLU ? M / 2 : M;
   int t = tbegin(e, CBT_KCLASS_PROJ);
   // decode rows: cluster split-K (partial sums meet in distributed shared memory); prefill
@@ -1337,6 +1354,7 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
     tend(e, t, 8.0 * n_out * d);
   }
   float* lg = logits ? logits : e->logits;
+  e->stall_now = e->stall_limit != 0 && fused && c.weight_format == CBT_WEIGHTS_BF16;
   if (tcp) {
     if (!tc_projection(e, e->lm_map, e->lm_map_kb, e->q4_lm, e->act_h, n_out, d, c.vocab, EPI_STORE, lg, c.vocab, nullptr,
                        0, fused))
@@ -1513,13 +1531,15 @@ extern "C" cbt_status cbt_decode_step_batch(cbt_engine* e, const int32_t* ids, i
       rc = cudaMemset2DAsync(e->stamp_buf + 1, 16, 0, 8, kStampSlots, e->stream);
   }
   if (rc == cudaSuccess) {
-    if (e->use_tc && e->timing_mask == 0 && e->stream != nullptr) {
+    if (e->use_tc && e->timing_mask == 0 && e->stream != nullptr && e->stall_limit == 0) {
       rc = run_decode_graph(e, B, last_tokens, max_keys, total_keys, logits, next_tokens);
     } else {
       rc = forward(e, B, last_tokens, max_keys, total_keys, false, B, logits, next_tokens);
       e->last_stamp_cls = e->stamp_cls;
     }
   }
+  e->stall_limit = 0;  // the stall is armed for one step
+  e->stall_now = false;
   if (rc != cudaSuccess) return rc == cudaErrorNotSupported ? CBT_ERR_UNSUPPORTED : CBT_ERR_CUDA;
   for (int b = 0; b < B; ++b) e->slabs[ids[b]].pos += 1;
   e->steps += 1;

@@ -122,6 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = C > 1 ? cluster_rank() : 0u;
+  const uint32_t lim = p.spin_limit ? p.spin_limit : tc::kSpinLimit;  // every wait's bound
   const int cid = blockIdx.x / C, NC = gridDim.x / C;
   const int Tc = cid < p.RB ? (p.RB - cid + NC - 1) / NC : 0;  // tiles cid, cid + NC, ...
   // this rank's stages: super-blocks of NK 64-column blocks [sb0, sb1) of each tile
@@ -178,10 +179,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                           pol_x);
         npend = 0;
       };
-      for (int j = 0; j < Tc && ok; ++j) {
+      for (int j = 0; j < Tc && ok && !p.stall_loads; ++j) {
         const int rb = cid + j * NC;
         for (int sb = sb0; sb < sb1; ++sb) {
-          if (!wait_or_abort(&sm.empty[stage], phase ^ 1, abort_flag)) {
+          if (!wait_or_abort(&sm.empty[stage], phase ^ 1, abort_flag, lim)) {
             report_timeout(p, abort_flag, 1);
             ok = false;
             break;
@@ -214,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           stage = S - 1;
           phase ^= 1;
         }
-        tc::mbar_wait(&sm.full[stage], phase);
+        tc::mbar_wait(&sm.full[stage], phase, lim);
       }
     }
   } else if (warp == 1) {
@@ -223,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int j = 0; j < Tc && ok; ++j) {
-        if (!wait_or_abort(&sm.acce[acc], acc_phase ^ 1, abort_flag)) {
+        if (!wait_or_abort(&sm.acce[acc], acc_phase ^ 1, abort_flag, lim)) {
           report_timeout(p, abort_flag, 2);
           break;
         }
@@ -231,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d0 = tmem + (uint32_t)(acc * kAcc * BN);
         for (int sb = sb0; sb < sb1; ++sb) {
           const uint32_t d = d0 + (uint32_t)(((sb - sb0) % kAcc) * BN);
-          if (!wait_or_abort(&sm.full[stage], phase, abort_flag)) {
+          if (!wait_or_abort(&sm.full[stage], phase, abort_flag, lim)) {
             report_timeout(p, abort_flag, 3);
             ok = false;
             break;
@@ -260,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // all MMAs of this thread complete before TMEM is released
       tc::mma_commit(sm.done);
-      tc::mbar_wait(sm.done, 0);
+      tc::mbar_wait(sm.done, 0, lim);
     }
   } else {  // ---- epilogue warps 2..5: TMEM lanes 32q .. 32q + 31 = tile rows
     pdl_wait();  // outputs and norm statistics are shared with the previous kernel
@@ -301,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         src.gn = tcepi::load_next_gain(p, rb, r);
         src.has_gn = true;
       }
-      if (!wait_or_abort(&sm.accf[acc], acc_phase, abort_flag)) {
+      if (!wait_or_abort(&sm.accf[acc], acc_phase, abort_flag, lim)) {
         report_timeout(p, abort_flag, 4);
         break;
       }
@@ -329,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float sum[H];
       const int got = csk::combine_partials<H>(vals, sum, sm.inbox, sm.inbox_full, slot, rank,
-                                               owner, C, r, abort_flag);
+                                               owner, C, r, abort_flag, lim);
       if (got < 0) {
         report_timeout(p, abort_flag, 5);
         break;
@@ -339,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // an owner leaves only after its inbox has been filled (bounded: a peer that gave up sends
     // nothing), so no st.async can land in a CTA that has exited
     if (C > 1 && threadIdx.x == 64)
-      for (int s = 0; s < owned; ++s) tc::mbar_wait(&sm.inbox_full[s], 0);
+      for (int s = 0; s < owned; ++s) tc::mbar_wait(&sm.inbox_full[s], 0, lim);
   }
   tc::tc_fence_before();
   __syncthreads();

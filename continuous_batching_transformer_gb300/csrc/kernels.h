@@ -78,6 +78,10 @@ struct TcParams {
   // 4-bit affine weights in the native block layout of gemm_q4.cu (launch_q4_rd only)
   const uint8_t* wq;
   unsigned long long* stamp;  // measurement stamp slot (common.cuh), or NULL
+  // failure detection test (launch_tc_csk only): the producer requests nothing, so every wait
+  // for a tile runs out after spin_limit polls (0: the default limit) and reports a timeout
+  int stall_loads;
+  uint32_t spin_limit;
 };
 
 

@@ -330,6 +330,18 @@ cbt_status cbt_engine_set_timing(cbt_engine* e, int32_t class_mask);
 cbt_status cbt_engine_timing(cbt_engine* e, int32_t kclass, double* total_ms, int64_t* intervals,
                              double* algorithmic_bytes);
 
+/* Failure-detection test of the bounded device waits.  Every wait in the library's kernels
+ * (on an mbarrier, a cluster peer or a flag) gives up after a bounded number of polls, records
+ * CBT_DEV_TIMEOUT in the device error word (info: the role that gave up) and lets its kernel
+ * end; nothing traps or hangs.  This call arms the next cbt_decode_step_batch of the engine so
+ * that its lm_head projection requests none of its weight tiles and every wait of that launch
+ * runs out after spin_limit polls.  That step then reports CBT_DEV_TIMEOUT through
+ * cbt_last_device_error; its logits and next tokens are unspecified, everything else it does
+ * (the K/V it appends, the positions it bumps) is as in a normal step, and later steps are
+ * unaffected.  Bf16 weights on the tensor-core path only (else CBT_ERR_UNSUPPORTED);
+ * spin_limit > 0 (else CBT_ERR_INVALID). */
+cbt_status cbt_engine_test_stall(cbt_engine* e, int32_t spin_limit);
+
 /* In-step stamps (measurement).  With enable != 0, every later decode step -- replayed steps
  * included -- records for each of its projection and attention launches (CBT_KCLASS_PROJ,
  * CBT_KCLASS_ATTN) the earliest time one of the launch's CTAs could start work that depends on

@@ -246,3 +246,42 @@ def test_decode_stamps_cover_every_projection_and_attention_launch():
     assert span < 1e9  # one step, in nanoseconds
     assert eng.device_error() == (0, 0)
     eng.close()
+
+
+def test_bounded_wait_reports_timeout_and_engine_stays_usable():
+    """Failure detection without a fault: the armed step's lm_head projection requests none of
+    its weight tiles, so its waits run out after a short limit; the step reports
+    CBT_DEV_TIMEOUT through the device error word, and the next step (fed the oracle's tokens)
+    matches the oracle -- the K/V the stalled step appended are intact."""
+    ensure_built()
+    import oracle
+    from continuous_batching_transformer_gb300 import binding as B
+    from tests.gpu_harness import TOL, check_logits
+    dev = torch.device("cuda:0")
+    w = DeviceWeights(TINY, dev)
+    om = oracle.OracleModel(TINY)
+    eng = Engine(w, arena_bytes=32 << 20, max_batch=4, max_prefill_tokens=64)
+    lens = [5, 9, 3]
+    slabs = [eng.kv_slab_alloc(64) for _ in lens]
+    caches = [oracle.KVCache(TINY, 64) for _ in lens]
+    toks = np.arange(sum(lens), dtype=np.int32) * 37 % TINY.vocab
+    lg = torch.empty((3, TINY.vocab), dtype=torch.float32, device=dev)
+    eng.prefill_segmented(slabs, lens, to_dev(toks, dev), lg)
+    ref = oracle.prefill_segmented(om, caches, lens, toks)
+    feed = np.array([oracle.argmax(r) for r in ref], np.int32)
+    B.engine_test_stall(eng.handle, 1 << 12)
+    eng.decode_step_batch(slabs, to_dev(feed, dev), lg)
+    ref = oracle.decode_step_batch(om, caches, feed)
+    code, info = eng.device_error()
+    assert code == 2 and 200 <= info < 300, (code, info)  # CBT_DEV_TIMEOUT from a projection role
+    assert [eng.position(s) for s in slabs] == [n + 1 for n in lens]
+    feed = np.array([oracle.argmax(r) for r in ref], np.int32)
+    for step in range(2):
+        eng.decode_step_batch(slabs, to_dev(feed, dev), lg)
+        ref = oracle.decode_step_batch(om, caches, feed)
+        check_logits(lg.cpu().numpy(), ref, TOL["bf16"], f"after the stall, step {step}")
+        feed = np.array([oracle.argmax(r) for r in ref], np.int32)
+    assert eng.device_error() == (0, 0)
+    with pytest.raises(B.CbtError):
+        B.engine_test_stall(eng.handle, 0)
+    eng.close()
