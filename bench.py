@@ -596,6 +596,99 @@ def trace_arm(args):
     return out
 
 
+PREFILL_METRIC = "segmented prefill tok/s (7B-shape, prompts packed into one call)"
+
+
+def prefill_flops(shape, seg_lens) -> float:
+    """Useful FLOPs of one segmented-prefill call: every prompt token through every linear
+    layer, lm_head for each segment's last token only, and causal attention inside each
+    segment (Q.K^T and P.V over the keys [0, j] of query j)."""
+    T = sum(seg_lens)
+    layer_params = shape.linear_params() - shape.vocab * shape.d_model
+    pairs = sum(n * (n + 1) // 2 for n in seg_lens)
+    attn = shape.n_layers * shape.n_heads * 4.0 * shape.head_dim * pairs
+    return 2.0 * layer_params * T + 2.0 * shape.vocab * shape.d_model * len(seg_lens) + attn
+
+
+def prefill_arm(args):
+    """Admission throughput: `7b-{bf16,affine4}-prefill` packs 4 prompts of 1024 seeded tokens
+    into one prefill_segmented call on fresh slabs, K timed calls after W warm-up calls, each
+    between CUDA events on the engine stream.  `roofline` is the tensor-core bound: useful
+    FLOPs per call over the call's time against the measured bf16 peak (the kernels run every
+    product on bf16 hi + lo operand parts, so the MMA work issued is about twice the useful
+    FLOPs)."""
+    import torch
+
+    import continuous_batching_transformer_gb300 as cbt
+    from continuous_batching_transformer_gb300 import binding as B
+    from continuous_batching_transformer_gb300.model import DeviceWeights, Engine
+    from synth.recipes import MISTRAL_7B, MISTRAL_7B_Q4
+
+    device = torch.device("cuda:0")
+    torch.cuda.set_device(device)
+    cbt.build()
+    shape = MISTRAL_7B_Q4 if args.workload.startswith("7b-affine4") else MISTRAL_7B
+    if args.layers:
+        from dataclasses import replace
+        shape = replace(shape, n_layers=args.layers, name=f"{shape.name}-{args.layers}-layers")
+    seg_lens = [1024] * 4
+    T = sum(seg_lens)
+    w = DeviceWeights(shape, device)
+    arena = (len(seg_lens) + 1) * B.slab_bytes(w.cfg, max(seg_lens))
+    eng = Engine(w, arena_bytes=arena, max_batch=8, max_prefill_tokens=T)
+    gen = torch.Generator().manual_seed(7)
+    toks = torch.randint(0, shape.vocab, (T,), generator=gen, dtype=torch.int32).to(device)
+    logits = torch.empty(len(seg_lens), shape.vocab, dtype=torch.float32, device=device)
+    nxt = torch.empty(len(seg_lens), dtype=torch.int32, device=device)
+    st = eng.stream
+    times = []
+    launches0 = None
+    clk = None
+    for i in range(args.warmup + args.steps):
+        if i == args.warmup:
+            torch.cuda.synchronize()
+            launches0 = B.kernel_launches()
+            clk = ClockSampler(None)
+        slabs = [eng.kv_slab_alloc(n) for n in seg_lens]
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        eng.prefill_segmented(slabs, seg_lens, toks, logits, nxt)
+        e1.record(st)
+        st.synchronize()
+        if i >= args.warmup:
+            times.append(e0.elapsed_time(e1) / 1e3)
+        for s in slabs:
+            eng.kv_slab_free(s)
+    clocks = clk.stop()
+    launches = B.kernel_launches() - launches0
+    code, info = eng.device_error()
+    if code != 0:
+        raise SystemExit(f"device error {code} ({info}) during prefill")
+    t = statistics.median(times)
+    flops = prefill_flops(shape, seg_lens)
+    peaks = measured_peaks() or {}
+    peak = peaks.get("bf16_tflops_sustained") or peaks.get("bf16_tflops")
+    achieved = flops / t / 1e12
+    out = {
+        "metric": PREFILL_METRIC, "value": T / t, "unit": "tok/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 (hi+lo operand parts)" if shape.weight_format == "bf16" else "affine4 weights",
+        "data": "synthetic (seeded weights and prompt tokens)",
+        "config": {"workload": f"prefill-{len(seg_lens)}x{seg_lens[0]}", "model": shape.name,
+                   "tokens_per_call": T, "parallelism": "1 gpu",
+                   "l2": "weights and activations stream from HBM; no flush between calls"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak if peak else None, "traffic": None,
+                     "of": "measured bf16 sustained", "useful_tflop_per_call": flops / 1e12},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+    }
+    eng.close()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -620,6 +713,8 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if args.impl == "gb300" and args.workload.startswith(("7b-bf16-trace", "7b-bf16-agents")):
         res = trace_arm(args)
+    elif args.impl == "gb300" and args.workload.endswith("-prefill"):
+        res = prefill_arm(args)
     elif args.impl == "reference":
         res = reference_arm(args, rank)
     else:

@@ -4,19 +4,20 @@
   back by every later step, over 32 layers);
 - the 4-bit affine weights at the batch sizes of the sweep not covered elsewhere (B = 1, 2, 8;
   B = 1 takes the one-column instantiation of the register-dequant projection);
-- a slice of the continuous-batching trace: the trace's own prompts (256 to 4096 tokens)
-  admitted by segmented prefill while other rows decode, rows joining and retiring.
+- a slice of the continuous-batching trace: the trace's own prompts (256 to 4096 tokens, their
+  earlier positions as seeded synthetic KV) admitted by segmented prefill while other rows
+  decode, rows joining and retiring.
 
 A full 7B prefill of thousands of tokens, or 128 separate oracle decode steps, is beyond the
-oracle's test budget.  Two exact devices keep it bounded:
+oracle's test budget.  Every input of the oracle comes from the seeded generators or from its
+own results:
 
-- teacher forcing: the logits of decode step i depend only on the tokens fed at steps <= i, so
-  the oracle replays the tokens the GPU fed a row in ONE causal pass over those positions;
-- hand-off: the K/V a prefill wrote (exported through the C ABI) become the oracle's cache.  At
-  sampled positions p the oracle recomputes token p from the GPU's K/V of positions [0, p):
-  its K/V at p in every layer must match what the GPU stored there, and at a segment's last
-  position its logits must match the prefill's logits.  Decode steps are then recomputed from
-  the exported cache.
+- greedy replay in one pass: the logits of decode step i depend only on the tokens fed at
+  steps <= i, so the oracle runs a row's steps as ONE causal pass over the tokens fed; each fed
+  token is checked to be the oracle's own argmax of the step before, so the pass is the
+  oracle's own greedy run;
+- long prompts: a prompt's earlier positions are the seeded synthetic KV on both sides, and
+  its last tokens are prefilled as a segment continuing that slab.
 """
 import gc
 
@@ -54,8 +55,9 @@ def release():
 def test_7b_bf16_b8_all_128_greedy_steps():
     """The 8-row workload with contexts 512..4096 for the 128 greedy steps it specifies, each
     step fed the previous step's device-side next tokens (no host round trip).  The row with the
-    shortest context is checked at every step against the oracle's teacher-forced replay of the
-    tokens the GPU fed it; the GPU's token register must hold the argmax of its own logits."""
+    shortest context is checked at every step against the oracle's greedy run of the same row
+    (one causal pass over the tokens fed, each of them the oracle's own argmax of the step
+    before); the GPU's token register must hold the argmax of its own logits."""
     ensure_built()
     dev = torch.device("cuda:0")
     wl = DECODE_7B_B8
@@ -94,6 +96,8 @@ def test_7b_bf16_b8_all_128_greedy_steps():
                          np.ones(steps, np.int32))
     errs = [check_logits(got[i:i + 1], ref[i:i + 1], TOL["bf16"], f"row {r} step {i}")
             for i in range(steps)]
+    for i in range(steps):  # token-identical: the GPU fed the oracle's greedy tokens
+        assert fed_h[i + 1] == oracle.argmax(ref[i]), f"step {i}: GPU token vs oracle argmax"
     print(f"128 steps, row {r} (ctx {ctx[r]}): max |logit - oracle| = {max(errs):.3e}")
 
 
@@ -157,41 +161,47 @@ def check_kv_at(shape, got_k, got_v, cache, p, what):
 
 
 def test_7b_trace_slice_joins_and_retires():
-    """The trace workload's first four requests (prompts of U[256, 4096] tokens, seed 1) on the
-    7B bf16 shape: requests 0 and 1 are admitted by one segmented prefill and decode two steps;
-    requests 2 and 3 join through a second segmented prefill and all four decode two steps;
-    request 0 retires and the other three decode one more step.  Checked by hand-off and
-    teacher forcing (module text)."""
+    """The trace's first four requests (seed 1: prompts of U[256, 4096] tokens) on the 7B bf16
+    shape through the public calls: requests 0 and 1 are admitted by one segmented prefill and
+    decode two steps; requests 2 and 3 join through a second segmented prefill and all four
+    decode two steps; request 0 retires and the other three decode one more step.
+
+    Each prompt's first n - 16 positions are the seeded synthetic KV (the same draws on both
+    sides) and its last 16 tokens are the prefilled segments, continuing that slab: the
+    admission attends over up to 4096 keys at the prompt's own positions, as the last query
+    block of a whole prompt does.  Every K/V the prefills and decode steps append, each
+    segment's logits and every decode step's logits are compared with the oracle's run of the
+    same calls, and the tokens the GPU fed are the oracle's greedy tokens at every step."""
     ensure_built()
     dev = torch.device("cuda:0")
     shape = MISTRAL_7B
-    V = shape.vocab
+    V, m_tok, seed = shape.vocab, 16, 11
     reqs = trace_requests(64, 2.0, 256, 4096, 256.0, 4096, seed=1)[:4]
     lens = [r.prompt_len for r in reqs]
-    prompts = [prompt_tokens(r, 1, V) for r in reqs]
+    pre = [n - m_tok for n in lens]
+    chunks = [prompt_tokens(r, 1, V)[p:] for r, p in zip(reqs, pre)]
     w = DeviceWeights(shape, dev)
     from continuous_batching_transformer_gb300 import binding as B
     caps = [n + 8 for n in lens]
     eng = Engine(w, arena_bytes=sum(B.slab_bytes(w.cfg, c) for c in caps), max_batch=8,
-                 max_prefill_tokens=max(lens[0] + lens[1], lens[2] + lens[3]))
+                 max_prefill_tokens=2 * m_tok)
     slabs = [eng.kv_slab_alloc(c) for c in caps]
+    for i in range(4):
+        eng.fill_synthetic_kv(slabs[i], i, pre[i], seed)
     pre_logits, exports = {}, {}
     dec_logits = {i: [] for i in range(4)}
     dec_fed = {i: [] for i in range(4)}
     tokbuf = torch.zeros(4, dtype=torch.int32, device=dev)
-    nxt = torch.zeros(4, dtype=torch.int32, device=dev)
 
     def admit(idx):
         lg = torch.empty((len(idx), V), dtype=torch.float32, device=dev)
         nx = torch.empty(len(idx), dtype=torch.int32, device=dev)
-        toks = np.concatenate([prompts[i] for i in idx])
-        eng.prefill_segmented([slabs[i] for i in idx], [lens[i] for i in idx], to_dev(toks, dev),
-                              lg, nx)
+        toks = np.concatenate([chunks[i] for i in idx])
+        eng.prefill_segmented([slabs[i] for i in idx], [m_tok] * len(idx), to_dev(toks, dev), lg, nx)
         host_lg, host_nx = lg.cpu().numpy(), nx.cpu().numpy()
         for j, i in enumerate(idx):
             pre_logits[i] = host_lg[j].copy()
             tokbuf[i] = int(host_nx[j])
-            exports[i] = exported_kv(eng, slabs[i], lens[i])
 
     def decode(live):
         lg = torch.empty((len(live), V), dtype=torch.float32, device=dev)
@@ -210,41 +220,43 @@ def test_7b_trace_slice_joins_and_retires():
     admit([2, 3])
     for _ in range(2):
         decode([0, 1, 2, 3])
+    exports[0] = exported_kv(eng, slabs[0], lens[0] + 4)
     eng.retire([slabs[0]])
     decode([1, 2, 3])
     assert eng.device_error() == (0, 0)
     assert [eng.position(s) for s in slabs[1:]] == [lens[1] + 5, lens[2] + 3, lens[3] + 3]
+    for i in range(1, 4):
+        exports[i] = exported_kv(eng, slabs[i], eng.position(slabs[i]))
     eng.close()
     del w
     release()
 
     m = oracle_model(shape)
+    caches = []
     for i in range(4):
-        n = lens[i]
+        c = oracle.KVCache(shape, caps[i])
+        c.fill_synthetic(i, pre[i], seed)
+        caches.append(c)
+    ref_pre = {}
+    for idx in ([0, 1], [2, 3]):
+        lg = oracle.prefill_continue(m, [caches[i] for i in idx], [m_tok] * len(idx),
+                                     np.concatenate([chunks[i] for i in idx]))
+        for j, i in enumerate(idx):
+            ref_pre[i] = lg[j]
+    for i in range(4):
         k, v = exports[i]
-        for p in sorted({0, 128, n // 2, n - 1}):
-            if p >= n:
-                continue
-            c = oracle.KVCache(shape, p + 1)
-            c.k[:, :, :p] = k[:, :, :p]
-            c.v[:, :, :p] = v[:, :, :p]
-            c.len = p
-            lg = oracle.forward(m, [c], np.zeros(1, np.int32), np.array([p], np.int32),
-                                prompts[i][p:p + 1], np.ones(1, np.int32))
-            check_kv_at(shape, k, v, c, p, f"request {i} (prompt {n})")
-            if p == n - 1:
-                check_logits(pre_logits[i][None], lg, TOL["bf16"], f"request {i} prefill logits")
-        # decode steps from the exported cache, teacher-forced on the tokens the GPU fed
+        check_logits(pre_logits[i][None], ref_pre[i][None], TOL["bf16"], f"request {i} prefill")
+        # the decode steps: the oracle's greedy tokens, one causal pass over them
         steps = len(dec_fed[i])
-        c = oracle.KVCache(shape, n + steps + 1)
-        c.k[:, :, :n] = k
-        c.v[:, :, :n] = v
-        c.len = n
-        ref = oracle.forward(m, [c], np.zeros(steps, np.int32),
+        assert dec_fed[i][0] == oracle.argmax(ref_pre[i]), f"request {i}: first token"
+        n = lens[i]
+        ref = oracle.forward(m, [caches[i]], np.zeros(steps, np.int32),
                              np.arange(n, n + steps, dtype=np.int32),
                              np.array(dec_fed[i], np.int32), np.ones(steps, np.int32))
         for s in range(steps):
             check_logits(dec_logits[i][s][None], ref[s:s + 1], TOL["bf16"],
                          f"request {i} decode step {s}")
-        # the first decode step fed the GPU's own greedy token of the prefill
-        assert dec_fed[i][0] == int(np.argmax(pre_logits[i])), f"request {i}: first token"
+            if s + 1 < steps:
+                assert dec_fed[i][s + 1] == oracle.argmax(ref[s]), f"request {i} step {s}: token"
+        for p in range(pre[i], n + steps):
+            check_kv_at(shape, k, v, caches[i], p, f"request {i} (prompt {n})")

@@ -96,12 +96,13 @@ def test_prefill_7b_shape_two_layers():
 def test_prefill_7b_full_depth_sampled():
     """The full 32-layer 7B shape: two segments (one spanning two query blocks) in one call.
     Each segment's last-token logits against the oracle; layer 0's K/V within one bf16 step
-    of the oracle's; then one decode step from the GPU's own slabs handed to the oracle.
+    of the oracle's; then one decode step, each side from its own slabs.
 
-    Deeper K/V are not compared element by element: both sides round K/V to bf16, so an
+    Deeper K/V are not compared element by element here: both sides round K/V to bf16, so an
     fp32-level difference flips single elements by one bf16 step and the flips compound over
     the layers (a plain fp32 CPU implementation differs from the oracle by 1.2e-2 on these
-    logits).  The decode step is therefore checked from the same K/V on both sides."""
+    logits).  The decode step after the prefill carries that drift; it stays within the logit
+    tolerance."""
     from synth.recipes import MISTRAL_7B
     ensure_built()
     dev = torch.device("cuda:0")
@@ -122,8 +123,6 @@ def test_prefill_7b_full_depth_sampled():
         k = torch.empty((shape.n_layers, shape.n_kv_heads, n, shape.head_dim), dtype=torch.bfloat16)
         v = torch.empty_like(k)
         eng.export_kv(slabs[r], k, v, n)
-        kb = k.view(torch.int16).numpy().astype(np.int32) & 0xFFFF
-        vb = v.view(torch.int16).numpy().astype(np.int32) & 0xFFFF
         for got, want in ((k[0].float().numpy(), caches[r].k[0, :, :n]),
                           (v[0].float().numpy(), caches[r].v[0, :, :n])):
             # layer 0 depends on no attention: at most one bf16 step apart (2^-7 relative),
@@ -132,16 +131,13 @@ def test_prefill_7b_full_depth_sampled():
             gap = np.abs(got - wf)
             assert (gap <= np.maximum(np.abs(wf) * 2.0 ** -7, 1e-4)).all(), \
                 f"layer-0 K/V beyond one bf16 step: {gap.max():.3e}"
-        # hand the GPU's K/V to the oracle for the decode step
-        caches[r].k[:, :, :n] = kb.astype(np.uint16)
-        caches[r].v[:, :, :n] = vb.astype(np.uint16)
     feed = np.asarray([oracle.argmax(x) for x in ref], np.int32)
     eng.decode_step_batch(slabs, to_dev(feed, dev), logits, nxt)
     ref2 = oracle.decode_step_batch(om, caches, feed)
     e2 = check_logits(logits.cpu().numpy(), ref2, TOL["bf16"], "7b decode after prefill")
     assert eng.device_error() == (0, 0)
     eng.close()
-    print(f"7b full depth: prefill {e1:.3e}, decode from the same K/V {e2:.3e}")
+    print(f"7b full depth: prefill {e1:.3e}, decode after it {e2:.3e}")
 
 
 @pytest.mark.parametrize("fmt", ["bf16", "affine4"])
