@@ -117,6 +117,12 @@ struct cbt_engine {
   std::vector<Q4Layer> q4w;
   uint8_t* q4_lm = nullptr;
   uint8_t* q4_arena = nullptr;
+  // 4-bit weights over more than 32 rows (prefill): one matrix at a time expanded into bf16 hi
+  // parts (q4x) and lo parts (q4x + q4x_elems), seen through one pair of maps per shape
+  enum { kQ4xQkv, kQ4xO, kQ4xGu, kQ4xDown, kQ4xLm, kQ4xShapes };
+  uint16_t* q4x = nullptr;
+  size_t q4x_elems = 0;
+  CUtensorMap q4x_maps[kQ4xShapes][2];
   int act_rows = 0;
   uint16_t *act_h = nullptr, *act_o = nullptr, *act_u = nullptr;
   std::map<std::pair<const void*, int>, CUtensorMap> xmaps;  // (operand buffer, N tile)
@@ -206,7 +212,7 @@ static void free_scratch(cbt_engine* e) {
                   e->rows,    e->err,      e->act_h, e->act_o, e->act_u,  e->tc_part,
                   e->tc_cnt,  e->items,    e->item_meta, e->att_o, e->att_ml, e->stage,
                   e->qtile,   e->ss,       e->qb,     e->pf_units, e->q4_arena, e->pagetab,
-                  e->tok_pages, e->kv8_jobs};
+                  e->tok_pages, e->kv8_jobs, e->q4x};
   for (void* q : ptrs)
     if (q) cudaFree(q);
 }
@@ -409,6 +415,21 @@ extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_w
                                    static_cast<const uint16_t*>(m.lin->biases), m.M, m.K, m.F,
                                    *m.dst, e->stream);
         off += q4_native_bytes(m.M, m.K, m.F);
+      }
+      if (T > 32 && maps_ok && rc == cudaSuccess) {
+        // projections over more than 32 rows run as dense tensor-core GEMMs over the expanded
+        // matrix (the head too when more than 32 rows may ask for logits)
+        const int shp[cbt_engine::kQ4xShapes][2] = {
+            {nqkv, c.d_model}, {c.d_model, qd}, {2 * c.d_ff, c.d_model}, {c.d_model, c.d_ff},
+            {c.vocab, c.d_model}};
+        const int nshape = p->max_batch > 32 ? cbt_engine::kQ4xShapes : cbt_engine::kQ4xLm;
+        size_t emax = 0;
+        for (int i = 0; i < nshape; ++i) emax = std::max(emax, (size_t)shp[i][0] * shp[i][1]);
+        chk(dmalloc(&e->q4x, 2 * emax, &tot));
+        e->q4x_elems = emax;
+        for (int i = 0; i < nshape && rc == cudaSuccess && maps_ok; ++i)
+          maps_ok = make_tmap_bf16(&e->q4x_maps[i][0], e->q4x, shp[i][1], shp[i][0], 64, 64) &&
+                    make_tmap_bf16(&e->q4x_maps[i][1], e->q4x + emax, shp[i][1], shp[i][0], 64, 64);
       }
     }
     // the whole arena seen as K rows (head_dim wide) and as V^T rows (64 keys wide)
@@ -1110,8 +1131,11 @@ static unsigned long long* next_stamp(cbt_engine* e, int cls) {
 // norm_in: the operand is x * g and each column is scaled by its RMSNorm factor, from the
 // sums of squares in e->ss.  next_gain (EPI_ADD): also write the updated rows' sums of squares
 // to e->ss and x * next_gain into e->act_h, the operand of the projection that follows.
+// 4-bit weights: q4w is the native copy (decode rows); q4lin the interchange-format matrix and
+// q4shape its entry in q4x_maps, for more than 32 rows (expanded, then a dense GEMM).
 static bool tc_projection(cbt_engine* e, const CUtensorMap& wmap, const CUtensorMap& wmap_kb,
-                          const uint8_t* q4w, const uint16_t* xbuf, int n, int K, int M, Epilogue epi, float* out,
+                          const uint8_t* q4w, const cbt_linear* q4lin, int q4shape,
+                          const uint16_t* xbuf, int n, int K, int M, Epilogue epi, float* out,
                           int ldo, uint16_t* act_out, int act_ld, bool norm_in = false,
                           const uint16_t* next_gain = nullptr, int layer = 0) {
   const bool split = n <= 32;
@@ -1166,9 +1190,18 @@ static bool tc_projection(cbt_engine* e, const CUtensorMap& wmap, const CUtensor
   // decode rows: cluster split-K (partial sums meet in distributed shared memory); prefill
   // tokens: whole tiles per CTA
   bool ok;
-  if (e->cfg.weight_format != CBT_WEIGHTS_BF16) {
+  if (e->cfg.weight_format != CBT_WEIGHTS_BF16 && split) {
     p.wq = q4w;
-    ok = split && launch_q4_rd(p, xbuf, tc_lo_rows(e, n), e->num_sms, e->stream);
+    ok = launch_q4_rd(p, xbuf, tc_lo_rows(e, n), e->num_sms, e->stream);
+  } else if (e->cfg.weight_format != CBT_WEIGHTS_BF16) {
+    uint16_t* hi = e->q4x;
+    ok = hi != nullptr && q4lin != nullptr && (size_t)M * K <= e->q4x_elems &&
+         launch_q4_expand(static_cast<const uint32_t*>(q4lin->w),
+                          static_cast<const uint16_t*>(q4lin->scales),
+                          static_cast<const uint16_t*>(q4lin->biases), M, K, hi, hi + e->q4x_elems,
+                          e->num_sms, e->stream) &&
+         launch_tc_linear(e->q4x_maps[q4shape][0], *xm, p, false, BN, e->num_sms,
+                          e->tc_part_floats, e->stream, &e->q4x_maps[q4shape][1]);
   } else {
     ok = split ? launch_tc_csk(wmap_kb, *xm, p, BN, e->num_sms, e->stream)
                : launch_tc_linear(wmap, *xm, p, split, BN, e->num_sms, e->tc_part_floats,
@@ -1194,8 +1227,11 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
   const double attn_bytes = 2.0 * kv_el * kvd * (double)total_keys
                             + 4.0 * n * (qd + 2 * kvd)              // q, k, v in
                             + 2.0 * 2.0 * n * kvd + 4.0 * n * qd;   // K/V appended, o out
-  // 4-bit weights go through the tensor cores for up to 32 rows (the decode projections)
-  const bool tcp = e->use_tc && (e->cfg.weight_format == CBT_WEIGHTS_BF16 || n <= 32);
+  // 4-bit weights go through the tensor cores for up to 32 rows (the decode projections), and
+  // for more rows when the engine holds the expansion scratch (dense GEMMs over bf16 hi + lo)
+  // (whose maps cover lm_head whenever more than 32 rows may ask for logits)
+  const bool tcp = e->use_tc && (e->cfg.weight_format == CBT_WEIGHTS_BF16 || n <= 32 ||
+                                 e->q4x != nullptr);
   // decode on the tensor cores folds every RMSNorm into the projection that consumes it:
   // the residual-add epilogues and the embedding leave per-tile sums of squares in e->ss
   const bool fused = tcp && !gather && n <= 32;
@@ -1223,7 +1259,8 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
     // decode on the tensor cores rotates q and k, appends K/V and lays out the attention's Q
     // operand in the QKV projection's epilogue; otherwise a separate kernel does it
     if (tcp)
-      ok &= tc_projection(e, e->wmaps[l].qkv, e->wmaps_kb[l].qkv, e->q4w[l].qkv, e->act_h, n, d, qd + 2 * kvd,
+      ok &= tc_projection(e, e->wmaps[l].qkv, e->wmaps_kb[l].qkv, e->q4w[l].qkv, &L.wqkv,
+                          cbt_engine::kQ4xQkv, e->act_h, n, d, qd + 2 * kvd,
                           fused ? EPI_QKV : EPI_STORE, e->qkv, qd + 2 * kvd, nullptr, 0, fused,
                           nullptr, l);
     else
@@ -1315,7 +1352,8 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
     }
     tend(e, t, attn_bytes);
     if (tcp)
-      ok &= tc_projection(e, e->wmaps[l].o, e->wmaps_kb[l].o, e->q4w[l].o, e->act_o, n, qd, d, EPI_ADD, e->x, d, nullptr, 0,
+      ok &= tc_projection(e, e->wmaps[l].o, e->wmaps_kb[l].o, e->q4w[l].o, &L.wo, cbt_engine::kQ4xO,
+                          e->act_o, n, qd, d, EPI_ADD, e->x, d, nullptr, 0,
                           false, fused ? fn : nullptr);
     else
       projection(e, e->o, n, qd, L.wo, d, EPI_ADD, e->x);
@@ -1326,13 +1364,15 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
       tend(e, t, 8.0 * n * d);
     }
     if (tcp) {
-      ok &= tc_projection(e, e->wmaps[l].gu, e->wmaps_kb[l].gu, e->q4w[l].gu, e->act_h, n, d, 2 * F, EPI_SWIGLU, nullptr, 0,
+      ok &= tc_projection(e, e->wmaps[l].gu, e->wmaps_kb[l].gu, e->q4w[l].gu, &L.wgu,
+                          cbt_engine::kQ4xGu, e->act_h, n, d, 2 * F, EPI_SWIGLU, nullptr, 0,
                           e->act_u, F, fused);
       // the down projection's epilogue prepares the next layer's (or the final) RMSNorm
       const uint16_t* next_g = l + 1 < c.n_layers
                                    ? static_cast<const uint16_t*>(e->layers[l + 1].attn_norm)
                                    : static_cast<const uint16_t*>(e->w.final_norm);
-      ok &= tc_projection(e, e->wmaps[l].d, e->wmaps_kb[l].d, e->q4w[l].d, e->act_u, n, F, d, EPI_ADD, e->x, d, nullptr, 0,
+      ok &= tc_projection(e, e->wmaps[l].d, e->wmaps_kb[l].d, e->q4w[l].d, &L.wd,
+                          cbt_engine::kQ4xDown, e->act_u, n, F, d, EPI_ADD, e->x, d, nullptr, 0,
                           false, fused ? next_g : nullptr);
     } else {
       projection(e, e->h, n, d, L.wgu, 2 * F, EPI_SWIGLU, e->act);
@@ -1356,7 +1396,8 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
   float* lg = logits ? logits : e->logits;
   e->stall_now = e->stall_limit != 0 && fused && c.weight_format == CBT_WEIGHTS_BF16;
   if (tcp) {
-    if (!tc_projection(e, e->lm_map, e->lm_map_kb, e->q4_lm, e->act_h, n_out, d, c.vocab, EPI_STORE, lg, c.vocab, nullptr,
+    if (!tc_projection(e, e->lm_map, e->lm_map_kb, e->q4_lm, &e->w.lm_head, cbt_engine::kQ4xLm,
+                       e->act_h, n_out, d, c.vocab, EPI_STORE, lg, c.vocab, nullptr,
                        0, fused))
       return cudaErrorNotSupported;
   } else {

@@ -13,6 +13,15 @@
 //   [128 rows][s0, b0, s1, b1]      bf16 scale and bias of the block's two groups.
 // SwiGLU tiles hold 64 gate rows and then the same 64 features' up rows, so one tile's
 // epilogue sees a feature's gate and up values together.
+//
+// Prefill projections (more than 32 tokens) are dense contractions: there a matrix is expanded
+// from the interchange format into bf16 hi and lo parts in engine scratch and the tensor-core
+// GEMM runs over both.  w = s * q + b is formed once in fp32 (s * q is exact: 8 significant
+// bits times 4; the sum rounds once), hi = bf16(w), lo = bf16(w - hi) (w - hi is exact), so
+// hi + lo carries w to about 2^-17 of its magnitude.
+#include <algorithm>
+
+#include "common.cuh"
 #include "kernels.h"
 
 namespace {
@@ -59,7 +68,48 @@ __global__ void k_q4_repack(const uint32_t* __restrict__ packed, const uint16_t*
   }
 }
 
+// One thread per word of eight codes (one row, eight consecutive columns inside one group);
+// the eight hi parts and the eight lo parts leave as one 16-byte store each.
+__global__ void k_q4_expand(const uint32_t* __restrict__ packed, const uint16_t* __restrict__ scales,
+                            const uint16_t* __restrict__ biases, long long words, int K,
+                            uint16_t* __restrict__ hi, uint16_t* __restrict__ lo) {
+  const int wpr = K / 8;  // words per row
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < words;
+       i += (long long)gridDim.x * blockDim.x) {
+    const uint32_t w = __ldcs(packed + i);
+    const long long row = i / wpr;
+    const int col = (int)(i - row * wpr) * 8;
+    const size_t gi = (size_t)row * (K / 64) + col / 64;
+    const float sc = bf16_to_f32(scales[gi]), bi = bf16_to_f32(biases[gi]);
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const float v0 = fmaf(sc, (float)((w >> (8 * t)) & 15u), bi);
+      const float v1 = fmaf(sc, (float)((w >> (8 * t + 4)) & 15u), bi);
+      const uint16_t h0 = f32_to_bf16(v0), h1 = f32_to_bf16(v1);
+      const uint16_t l0 = f32_to_bf16(v0 - bf16_to_f32(h0)), l1 = f32_to_bf16(v1 - bf16_to_f32(h1));
+      h[t] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+      l[t] = (uint32_t)l0 | ((uint32_t)l1 << 16);
+    }
+    *reinterpret_cast<uint4*>(hi + i * 8) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(lo + i * 8) = make_uint4(l[0], l[1], l[2], l[3]);
+  }
+}
+
 }  // namespace
+
+bool launch_q4_expand(const uint32_t* packed, const uint16_t* scales, const uint16_t* biases,
+                      int M, int K, uint16_t* hi, uint16_t* lo, int num_sms, cudaStream_t s) {
+  if (M <= 0 || K <= 0 || K % 64 || (reinterpret_cast<uintptr_t>(hi) & 15) ||
+      (reinterpret_cast<uintptr_t>(lo) & 15))
+    return false;
+  const long long words = (long long)M * (K / 8);
+  const long long want = (words + 255) / 256;
+  const int grid = (int)std::min<long long>(want, (long long)num_sms * 16);
+  k_q4_expand<<<grid, 256, 0, s>>>(packed, scales, biases, words, K, hi, lo);
+  count_launch();
+  return cudaGetLastError() == cudaSuccess;
+}
 
 size_t q4_native_bytes(int M, int K, int F) {
   if (K % 128) return 0;

@@ -24,9 +24,16 @@
 // tiles and the MMA chain runs over both.  The tensor core's fp32 accumulation rounds toward
 // zero (measured: a relative bias of -4e-6 over K = 4096, -1.5e-5 over K = 14336), and over a
 // deep prefill the bias reaches the logits through the bf16 rounding of every appended K/V;
-// so k-block k accumulates into accumulator k % kPrefillAcc and the epilogue adds the
-// accumulators in fp32 (round to nearest), which divides the bias by kPrefillAcc.  The
-// accumulators fill the tensor memory, so prefill tiles are single-buffered.
+// so every kDrainEvery k-blocks the MMAs start a fresh accumulator (kPrefillAcc of them in
+// rotation, which fill the tensor memory) and the epilogue warps add the finished one into fp32
+// sums with round to nearest while the next k-blocks run: only the MMAs of one group truncate.
+// Measured on a 4 x 1024-token 7B prefill: groups of 1, 2, 4 and 16 k-blocks take 260, 247,
+// 233 and 177 ms a call (the original 16-k-block interleave 142 ms); a 32-layer prefill then
+// decode stays within 1.6-1.7e-2 of the double-precision oracle for groups of up to 4 and
+// exceeds 2e-2 at 16.
+// Prefill over 4-bit weights (WLO): the matrix arrives expanded into bf16 hi and lo parts, each
+// stage carries both weight tiles, and the chain adds lo . x_hi to hi . x_hi + hi . x_lo (the
+// lo . x_lo term is below 2^-16 of the product).
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -45,7 +52,8 @@ constexpr int kABytes = 128 * 128;  // 128 rows x 64 bf16
 // Decode stages: 8 x (16 KB of weights + the operand tile) keeps 128 KB of weights in flight
 // per SM (5 stages, which would let a second CTA share the SM, measured slower).
 constexpr int kSplitStages = 8;
-constexpr int kPrefillAcc = 4;  // prefill accumulators per tile (k-blocks dealt round robin)
+constexpr int kPrefillAcc = 4;   // prefill accumulators in rotation
+constexpr int kDrainEvery = 4;   // k-blocks an accumulator takes before the epilogue adds it up
 
 struct Sched {
   long long u, u1;
@@ -100,27 +108,29 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 }
 
 
-template <int BN, int STAGES, bool SPLIT>
+template <int BN, int STAGES, bool SPLIT, bool WLO>
 __global__ void __launch_bounds__(kThreads, 1)
     k_tc_linear(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tx,
-                const TcParams p) {
+                const __grid_constant__ CUtensorMap twl, const TcParams p) {
+  static_assert(!(WLO && SPLIT), "weight lo parts are a prefill form");
   constexpr int kXTile = BN * 128;                     // one [BN rows][64] operand tile
   constexpr int kXBytes = SPLIT ? kXTile : 2 * kXTile;  // prefill stages: hi and lo tiles
+  constexpr int kAStage = WLO ? 2 * kABytes : kABytes;  // weight tile (+ its lo parts)
   constexpr uint32_t kTmemCols = SPLIT ? (2 * BN < 32 ? 32 : 2 * BN) : kPrefillAcc * BN;
   constexpr uint32_t kIdesc = tc::idesc_bf16(128, BN);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sX = smem + STAGES * kABytes;
+  uint8_t* sX = smem + STAGES * kAStage;
   uint64_t* full = reinterpret_cast<uint64_t*>(sX + STAGES * kXBytes);
   uint64_t* empty = full + STAGES;
-  uint64_t* accf = empty + STAGES;
-  uint64_t* acce = accf + 2;
-  uint64_t* done = acce + 2;
+  uint64_t* accf = empty + STAGES;  // per accumulator: MMAs done / drained by the epilogue
+  uint64_t* acce = accf + kPrefillAcc;
+  uint64_t* done = acce + kPrefillAcc;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* sflag = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [0] last, [1] abort
-  float* swx = reinterpret_cast<float*>(smem + STAGES * (kABytes + kXBytes) + 512);
+  float* swx = reinterpret_cast<float*>(smem + STAGES * (kAStage + kXBytes) + 512);
   float* rinv = swx + 128 * 33;  // [32] RMSNorm factor of each decode column
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -129,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < kPrefillAcc; ++a) {
       tc::mbar_init(&accf[a], 1);
       tc::mbar_init(&acce[a], 4);
     }
@@ -139,6 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mbar_fence_init();
     tc::tma_prefetch_desc(&tw);
     tc::tma_prefetch_desc(&tx);
+    if (WLO) tc::tma_prefetch_desc(&twl);
   }
   if (warp == 1) tc::tmem_alloc(tmem_slot, kTmemCols);
   tc::tc_fence_before();
@@ -184,9 +195,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          tc::mbar_expect_tx(&full[stage], kABytes + kXBytes);
-          tc::tma_load_2d(sA + stage * kABytes, &tw, &full[stage], k * 64, y0, pol_w);
-          tc::tma_load_2d(sA + stage * kABytes + 8192, &tw, &full[stage], k * 64, y1, pol_w);
+          tc::mbar_expect_tx(&full[stage], kAStage + kXBytes);
+          tc::tma_load_2d(sA + stage * kAStage, &tw, &full[stage], k * 64, y0, pol_w);
+          tc::tma_load_2d(sA + stage * kAStage + 8192, &tw, &full[stage], k * 64, y1, pol_w);
+          if (WLO) {
+            tc::tma_load_2d(sA + stage * kAStage + kABytes, &twl, &full[stage], k * 64, y0, pol_w);
+            tc::tma_load_2d(sA + stage * kAStage + kABytes + 8192, &twl, &full[stage], k * 64, y1,
+                            pol_w);
+          }
           if (dep_done) {
             tc::tma_load_2d(sX + stage * kXBytes, &tx, &full[stage], k * 64, nt * BN, pol_x);
             if (!SPLIT)
@@ -216,7 +232,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {  // ---- MMA issuer
+    if (lane == 0 && !SPLIT) {  // ---- MMA issuer, prefill: a fresh accumulator per k-block
+      int stage = 0, a = 0;
+      uint32_t phase = 0, aphase = 0;
+      bool ok = true;
+      while (ok && sch.next(p, tile, kb, ke)) {
+        for (int k = kb; k < ke; ++k) {
+          const bool first = (k - kb) % kDrainEvery == 0;
+          const bool last = (k - kb) % kDrainEvery == kDrainEvery - 1 || k == ke - 1;
+          if (first && !wait_or_abort(&acce[a], aphase ^ 1, sflag + 1)) {  // drained
+            report_timeout(p, sflag + 1, 2);
+            ok = false;
+            break;
+          }
+          if (!wait_or_abort(&full[stage], phase, sflag + 1)) {
+            report_timeout(p, sflag + 1, 3);
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint32_t d = tmem + (uint32_t)(a * BN);
+          const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sA + stage * kAStage));
+          const uint64_t xd = tc::sdesc_sw128(tc::smem_u32(sX + stage * kXBytes));
+          const uint64_t ld = tc::sdesc_sw128(tc::smem_u32(sX + stage * kXBytes + kXTile));
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)  // hi parts (the group's first MMA overwrites)
+            tc::mma_bf16(d, ad + 2 * kk, xd + 2 * kk, kIdesc, (kk > 0 || !first) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) tc::mma_bf16(d, ad + 2 * kk, ld + 2 * kk, kIdesc, 1u);
+          if (WLO) {  // the weights' lo parts against the operand's hi parts
+            const uint64_t al = tc::sdesc_sw128(tc::smem_u32(sA + stage * kAStage + kABytes));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) tc::mma_bf16(d, al + 2 * kk, xd + 2 * kk, kIdesc, 1u);
+          }
+          tc::mma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+          if (last) {
+            tc::mma_commit(&accf[a]);
+            if (++a == kPrefillAcc) {
+              a = 0;
+              aphase ^= 1;
+            }
+          }
+        }
+      }
+      tc::mma_commit(done);
+      tc::mbar_wait(done, 0);
+    } else if (lane == 0) {  // ---- MMA issuer, decode: one accumulator per tile, two buffers
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
@@ -226,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc::tc_fence_after();
-        const uint32_t d = tmem + acc * BN;  // decode; prefill: + (k - kb) % kPrefillAcc * BN
+        const uint32_t d = tmem + acc * BN;
         for (int k = kb; k < ke; ++k) {
           if (!wait_or_abort(&full[stage], phase, sflag + 1)) {
             report_timeout(p, sflag + 1, 3);
@@ -234,22 +299,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc::tc_fence_after();
-          const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sA + stage * kABytes));
+          const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sA + stage * kAStage));
           const uint64_t xd = tc::sdesc_sw128(tc::smem_u32(sX + stage * kXBytes));
-          if (SPLIT) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              tc::mma_bf16(d, ad + 2 * kk, xd + 2 * kk, kIdesc, (k > kb || kk > 0) ? 1u : 0u);
-          } else {  // hi parts, then lo parts, into accumulator (k - kb) % kPrefillAcc
-            const int j = (k - kb) % kPrefillAcc;
-            const uint32_t dj = tmem + (uint32_t)(j * BN);
-            const uint64_t ld = tc::sdesc_sw128(tc::smem_u32(sX + stage * kXBytes + kXTile));
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              tc::mma_bf16(dj, ad + 2 * kk, xd + 2 * kk, kIdesc, (k - kb >= kPrefillAcc || kk > 0) ? 1u : 0u);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) tc::mma_bf16(dj, ad + 2 * kk, ld + 2 * kk, kIdesc, 1u);
-          }
+          for (int kk = 0; kk < 4; ++kk)
+            tc::mma_bf16(d, ad + 2 * kk, xd + 2 * kk, kIdesc, (k > kb || kk > 0) ? 1u : 0u);
           tc::mma_commit(&empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
@@ -258,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         tc::mma_commit(&accf[acc]);
-        if (++acc == (SPLIT ? 2 : 1)) {
+        if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1;
         }
@@ -279,6 +333,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::named_bar_sync(1, 128);
     }
+    if (!SPLIT) {
+      // prefill: every k-block's accumulator is added into fp32 sums (round to nearest) as soon
+      // as its MMAs are done, then handed back; the tile's epilogue runs on the sums
+      int a = 0;
+      uint32_t aphase = 0;
+      bool ok = true;
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
+      while (ok && sch.next(p, tile, kb, ke)) {
+        const int rb = tile / p.NT, nt = tile % p.NT;
+        float sums[BN];
+#pragma unroll
+        for (int j = 0; j < BN; ++j) sums[j] = 0.f;
+        for (int k = kb; k < ke; k += kDrainEvery) {
+          if (!wait_or_abort(&accf[a], aphase, sflag + 1)) {
+            report_timeout(p, sflag + 1, 4);
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+#pragma unroll
+          for (int c0 = 0; c0 < BN; c0 += 64) {
+            uint32_t raw[64];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tc::tmem_ld16(tbase + (uint32_t)(a * BN + c0 + 16 * c), raw + 16 * c);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 64; ++j) sums[c0 + j] += __uint_as_float(raw[j]);
+          }
+          tc::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&acce[a]);
+          if (++a == kPrefillAcc) {
+            a = 0;
+            aphase ^= 1;
+          }
+        }
+        if (!ok) break;
+#pragma unroll
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          float res[32];
+          load_residual<32>(p, rb, r, nt * BN + c0, res);
+          finish<32>(p, rb, r, sums + c0, nt * BN + c0, swx, rinv, res, tcepi::epi_src_global(p));
+        }
+      }
+    } else {
     int acc = 0;
     uint32_t acc_phase = 0;
     while (sch.next(p, tile, kb, ke)) {
@@ -350,32 +449,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (threadIdx.x == 64) p.cnt[tile] = 0;
           }
         }
-      } else {
-        const int nacc = ke - kb < kPrefillAcc ? ke - kb : kPrefillAcc;
-#pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-          float vals[32], res[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) vals[j] = 0.f;
-          for (int a = 0; a < nacc; ++a) {  // accumulators added in a fixed order
-            uint32_t raw[32];
-            tc::tmem_ld16(taddr + (uint32_t)(a * BN) + c0, raw);
-            tc::tmem_ld16(taddr + (uint32_t)(a * BN) + c0 + 16, raw + 16);
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) vals[j] += __uint_as_float(raw[j]);
-          }
-          load_residual<32>(p, rb, r, nt * BN + c0, res);
-          finish<32>(p, rb, r, vals, nt * BN + c0, swx, rinv, res, tcepi::epi_src_global(p));
-        }
-        tc::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&acce[acc]);
       }
-      if (++acc == (SPLIT ? 2 : 1)) {
+      if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1;
       }
+    }
     }
   }
   tc::tc_fence_before();
@@ -386,16 +465,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, int STAGES, bool SPLIT>
+template <int BN, int STAGES, bool SPLIT, bool WLO = false>
 cudaError_t launch_inst(const CUtensorMap& tw, const CUtensorMap& tx, const TcParams& p, int grid,
-                        cudaStream_t s) {
-  constexpr size_t smem =
-      1024 + STAGES * (kABytes + BN * 128 * (SPLIT ? 1 : 2)) + 512 + 128 * 33 * 4 + 256;
+                        cudaStream_t s, const CUtensorMap* twl = nullptr) {
+  constexpr size_t smem = 1024 + STAGES * (kABytes * (WLO ? 2 : 1) + BN * 128 * (SPLIT ? 1 : 2)) +
+                          512 + 128 * 33 * 4 + 256;
   static_assert(smem <= 227 * 1024, "shared memory budget");
-  auto kern = k_tc_linear<BN, STAGES, SPLIT>;
+  auto kern = k_tc_linear<BN, STAGES, SPLIT, WLO>;
   cudaError_t rc = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (rc != cudaSuccess) return rc;
-  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, tw, tx, p);
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, tw, tx, WLO ? *twl : tw, p);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -457,7 +536,8 @@ int tc_plain_bn(int n) { return n <= 64 ? 64 : 128; }
 // Plan and launch one projection.  p carries shapes, epilogue and outputs; this fills the
 // schedule.  Returns false if the shape is outside what the kernel supports.
 bool launch_tc_linear(const CUtensorMap& tw, const CUtensorMap& tx, TcParams p, bool split, int BN,
-                      int num_sms, size_t part_floats, cudaStream_t s) {
+                      int num_sms, size_t part_floats, cudaStream_t s, const CUtensorMap* twl) {
+  if (twl && split) return false;
   if (p.K % 64 || p.K <= 0 || p.n_act <= 0) return false;
   if (p.epi == EPI_SWIGLU && (p.F % 64 || p.M != 2 * p.F)) return false;
   if (!split && p.ss_in) return false;  // the per-column RMSNorm factors exist for decode rows only
@@ -499,7 +579,11 @@ bool launch_tc_linear(const CUtensorMap& tw, const CUtensorMap& tx, TcParams p, 
   const int tiles = p.RB * p.NT;
   const int G = std::min(tiles, num_sms);
   cudaError_t rc;
-  if (BN == 64) rc = launch_inst<64, 6, false>(tw, tx, p, G, s);
+  if (twl) {  // weights as hi + lo parts: a third tile per stage
+    if (BN == 64) rc = launch_inst<64, 4, false, true>(tw, tx, p, G, s, twl);
+    else if (BN == 128) rc = launch_inst<128, 3, false, true>(tw, tx, p, G, s, twl);
+    else return false;
+  } else if (BN == 64) rc = launch_inst<64, 6, false>(tw, tx, p, G, s);
   else if (BN == 128) rc = launch_inst<128, 4, false>(tw, tx, p, G, s);
   else return false;
   return rc == cudaSuccess;

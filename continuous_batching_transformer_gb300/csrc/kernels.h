@@ -96,8 +96,11 @@ bool make_tmap_kblocks(CUtensorMap* m, const void* base, uint64_t K, uint64_t ro
 // N tile for hi/lo (split) activations of n rows, and for plain bf16 activations
 int tc_split_bn(int n);
 int tc_plain_bn(int n);
+// twl (prefill only): the lo parts of weights given as bf16 hi + lo matrices (both maps 64 x 64
+// boxes over [M][K]); the product is hi.x_hi + hi.x_lo + lo.x_hi.
 bool launch_tc_linear(const CUtensorMap& tw, const CUtensorMap& tx, TcParams p, bool split,
-                      int BN, int num_sms, size_t part_floats, cudaStream_t s);
+                      int BN, int num_sms, size_t part_floats, cudaStream_t s,
+                      const CUtensorMap* twl = nullptr);
 
 // ---- cluster split-K decode projections (gemm_csk.cu) -----------------------------------------
 // Clusters of C CTAs; cluster c takes row tiles c, c + NC, ...; rank r streams k-blocks
@@ -129,6 +132,10 @@ size_t q4_native_bytes(int M, int K, int F);
 // scales and biases [M][K/64])
 bool launch_q4_repack(const uint32_t* packed, const uint16_t* scales, const uint16_t* biases,
                       int M, int K, int F, uint8_t* out, cudaStream_t s);
+// expand an interchange-format matrix into bf16 hi and lo parts [M][K] (16-byte aligned):
+// w = fp32(s * q + b), hi = bf16(w), lo = bf16(w - hi); for the tensor-core prefill projections
+bool launch_q4_expand(const uint32_t* packed, const uint16_t* scales, const uint16_t* biases,
+                      int M, int K, uint16_t* hi, uint16_t* lo, int num_sms, cudaStream_t s);
 // y = x W^T over n_act <= 32 decode rows with W = p.wq in the native layout, the codes
 // dequantised in registers; x is the operand buffer (bf16 rows of K columns: hi parts at rows b,
 // lo parts at rows x_lo + b), the rows taken 8 at a time.  Any TcParams epilogue.

@@ -272,7 +272,10 @@ __global__ void __launch_bounds__(kAttnThreads)
     for (int k = 0; k < HD / 16; ++k) {
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        const int d = 16 * k + 2 * tq + 8 * half;
+        // contraction slots 2 tq, 2 tq + 1 (half 0) and 2 tq + 8, 2 tq + 9 (half 1) of k-step k
+        // hold dims 16 k + 4 tq + 2 half + {0, 1}: a thread's four dims are consecutive, so one
+        // load gives its key codes (the same order on the K side below)
+        const int d = 16 * k + 4 * tq + 2 * half;
         const uint32_t hi = *reinterpret_cast<const uint32_t*>(st.q + sw128_offset(gq, d, 2048));
         const uint32_t lo = *reinterpret_cast<const uint32_t*>(st.q + sw128_offset(8 + gq, d, 2048));
         const float q0 = bf16_lo(hi) + bf16_lo(lo), q1 = bf16_hi(hi) + bf16_hi(lo);
@@ -306,13 +309,14 @@ __global__ void __launch_bounds__(kAttnThreads)
         for (int nt = 0; nt < 4; ++nt) {
           const uint8_t* row = st.kc + (32 * warp + 8 * nt + gq) * kPitch;
           uint32_t b0, b1;
-          if (BITS == 8) {
-            b0 = codes8_to_half2(*reinterpret_cast<const uint16_t*>(row + 16 * k + 2 * tq));
-            b1 = codes8_to_half2(*reinterpret_cast<const uint16_t*>(row + 16 * k + 2 * tq + 8));
+          if (BITS == 8) {  // codes of dims 16 k + 4 tq .. + 3
+            const uint32_t c = *reinterpret_cast<const uint32_t*>(row + 16 * k + 4 * tq);
+            b0 = codes8_to_half2(c);
+            b1 = codes8_to_half2(c >> 16);
           } else {
-            const uint32_t x0 = row[8 * k + tq], x1 = row[8 * k + tq + 4];
-            b0 = codes4_to_half2((x0 & 0xFu) | ((x0 & 0xF0u) << 12));
-            b1 = codes4_to_half2((x1 & 0xFu) | ((x1 & 0xF0u) << 12));
+            const uint32_t c = *reinterpret_cast<const uint16_t*>(row + 8 * k + 2 * tq);
+            b0 = codes4_to_half2((c & 0xFu) | ((c & 0xF0u) << 12));
+            b1 = codes4_to_half2(((c >> 8) & 0xFu) | ((c & 0xF000u) << 4));
           }
           mma_f16(acc[nt], qa[k], b0, b1);
         }
@@ -379,32 +383,61 @@ __global__ void __launch_bounds__(kAttnThreads)
       bsum += __shfl_xor_sync(0xffffffffu, bsum, 1);
       bsum += __shfl_xor_sync(0xffffffffu, bsum, 2);
       if (tq == 0) sm.redb[warp][gq][gr] = bsum;
+      // V codes: output tile t's column n is dim 64 gr + 8 n + t, so this thread's B column
+      // (n = gq) in tiles 0..7 is the 8 consecutive dims from 64 gr + 8 gq: one load per key
+      // row gives all eight tiles' codes
+      float o[8][4];
 #pragma unroll
-      for (int d8 = 0; d8 < 8; ++d8) {
-        const int dim = 64 * gr + 8 * d8 + gq;  // B column of this thread
-        float o[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int t = 0; t < 8; ++t)
 #pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-          const int key0 = 32 * warp + 16 * ks + 2 * tq;
-          uint32_t b0, b1;
+        for (int i = 0; i < 4; ++i) o[t][i] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {
+        const int key0 = 32 * warp + 16 * ks + 2 * tq;
+        const int rows[4] = {key0, key0 + 1, key0 + 8, key0 + 9};
+        uint32_t w[4][2];  // per row: codes of the 8 dims (8 bits: two words; 4 bits: one)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
           if (BITS == 8) {
-            const uint8_t* col = st.vc + dim;
-            b0 = codes8_to_half2((uint32_t)col[key0 * kPitch] | ((uint32_t)col[(key0 + 1) * kPitch] << 8));
-            b1 = codes8_to_half2((uint32_t)col[(key0 + 8) * kPitch] |
-                                 ((uint32_t)col[(key0 + 9) * kPitch] << 8));
+            const uint2 v = *reinterpret_cast<const uint2*>(st.vc + rows[r] * kPitch + 64 * gr + 8 * gq);
+            w[r][0] = v.x;
+            w[r][1] = v.y;
           } else {
-            const uint8_t* col = st.vc + (dim >> 1);
-            const int sh = 4 * (dim & 1);
-            b0 = codes4_to_half2(((col[key0 * kPitch] >> sh) & 0xFu) |
-                                 (((uint32_t)(col[(key0 + 1) * kPitch] >> sh) & 0xFu) << 16));
-            b1 = codes4_to_half2(((col[(key0 + 8) * kPitch] >> sh) & 0xFu) |
-                                 (((uint32_t)(col[(key0 + 9) * kPitch] >> sh) & 0xFu) << 16));
+            w[r][0] = *reinterpret_cast<const uint32_t*>(st.vc + rows[r] * kPitch + 32 * gr + 4 * gq);
+            w[r][1] = 0u;
           }
-          mma_f16(o, pa[ks], b0, b1);
         }
-        if (gq < G) {  // rows gq (high parts) + gq + 8 (remainders): head gq, dims 2 tq, 2 tq + 1
-          const int d0 = 64 * gr + 8 * d8 + 2 * tq;
-          *reinterpret_cast<float2*>(&sm.ored[warp][gq][d0]) = make_float2(o[0] + o[2], o[1] + o[3]);
+#pragma unroll
+        for (int t = 0; t < 8; t += 2) {
+          // b0 of tile t: (key0, key0 + 1) codes of dim t; b1: (key0 + 8, key0 + 9)
+          uint32_t b[2][2];  // [tile t, t + 1][b0, b1]
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb) {
+            const uint32_t x = w[2 * hb][0], y = w[2 * hb + 1][0];
+            if (BITS == 8) {
+              const uint32_t xs = t < 4 ? x : w[2 * hb][1], ys = t < 4 ? y : w[2 * hb + 1][1];
+              const int by = t & 3;  // bytes by and by + 1 of the rows' word
+              const uint32_t u = __byte_perm(xs, ys, (uint32_t)(by | ((4 + by) << 4) | ((by + 1) << 8) |
+                                                                ((5 + by) << 12)));
+              b[0][hb] = codes8_to_half2(u);        // (x_t, y_t)
+              b[1][hb] = codes8_to_half2(u >> 16);  // (x_t+1, y_t+1)
+            } else {
+              const int by = t >> 1;  // byte by holds dims t (low nibble) and t + 1 (high)
+              const uint32_t u = __byte_perm(x, y, (uint32_t)(by | ((4 + by) << 8)));  // x.by in 0, y.by in 2
+              b[0][hb] = codes4_to_half2(u & 0x000F000Fu);
+              b[1][hb] = codes4_to_half2((u >> 4) & 0x000F000Fu);
+            }
+          }
+          mma_f16(o[t], pa[ks], b[0][0], b[0][1]);
+          mma_f16(o[t + 1], pa[ks], b[1][0], b[1][1]);
+        }
+      }
+      if (gq < G) {  // rows gq (high parts) + gq + 8 (remainders): head gq
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const int d0 = 64 * gr + 16 * tq + t;  // columns 2 tq and 2 tq + 1 of tile t
+          sm.ored[warp][gq][d0] = o[t][0] + o[t][2];
+          sm.ored[warp][gq][d0 + 8] = o[t][1] + o[t][3];
         }
       }
     }

@@ -2,7 +2,9 @@
 tensor-core flash attention walks several key blocks, ragged tails and grouped-query heads.
 Each case packs several segments into one call, then extends two of them with a second call
 whose segments start mid-block (positions not a multiple of 128), then takes one decode step;
-logits are checked element by element against the CPU oracle (bf16 tolerance 2e-2)."""
+logits are checked element by element against the CPU oracle (tolerance 2e-2 for bf16
+weights, 5e-2 for 4-bit affine weights, which prefill expands into bf16 hi + lo parts for the
+tensor cores)."""
 import numpy as np
 import pytest
 import torch
@@ -30,8 +32,12 @@ def seeded_tokens(n: int, seed: int, vocab: int) -> np.ndarray:
     return np.asarray(np.random.default_rng(seed).integers(0, vocab, n), np.int32)
 
 
-def run_case(shape: ModelShape, lens, ext, cap: int):
+def run_case(shape: ModelShape, lens, ext, cap: int, fmt: str = "bf16"):
     ensure_built()
+    if fmt != "bf16":
+        from dataclasses import replace
+        shape = replace(shape, weight_format=fmt, name=f"{shape.name}-{fmt}")
+    tol = TOL[fmt]
     dev = torch.device("cuda:0")
     w = DeviceWeights(shape, dev)
     om = oracle.OracleModel(shape)
@@ -44,7 +50,7 @@ def run_case(shape: ModelShape, lens, ext, cap: int):
     nxt = torch.empty(len(lens), dtype=torch.int32, device=dev)
     eng.prefill_segmented(slabs, lens, to_dev(np.concatenate(toks), dev), logits, nxt)
     ref = oracle.prefill_segmented(om, caches, lens, np.concatenate(toks))
-    errs = [check_logits(logits.cpu().numpy(), ref, TOL["bf16"], f"{shape.name} prefill")]
+    errs = [check_logits(logits.cpu().numpy(), ref, tol, f"{shape.name} prefill")]
 
     # second call: segments that start part-way into a key block
     rows = sorted(ext)
@@ -61,7 +67,7 @@ def run_case(shape: ModelShape, lens, ext, cap: int):
         want[-1] = 1
         ref2.append(oracle.forward(om, [caches[r]], np.zeros(n, np.int32),
                                    np.arange(start, start + n, dtype=np.int32), t, want)[0])
-    errs.append(check_logits(lg2.cpu().numpy(), np.stack(ref2), TOL["bf16"],
+    errs.append(check_logits(lg2.cpu().numpy(), np.stack(ref2), tol,
                              f"{shape.name} extension"))
     for r in rows:
         assert eng.position(slabs[r]) == lens[r] + ext[r]
@@ -73,24 +79,27 @@ def run_case(shape: ModelShape, lens, ext, cap: int):
     feed = np.asarray(feed, np.int32)
     eng.decode_step_batch(slabs, to_dev(feed, dev), logits, nxt)
     ref3 = oracle.decode_step_batch(om, caches, feed)
-    errs.append(check_logits(logits.cpu().numpy(), ref3, TOL["bf16"], f"{shape.name} decode"))
+    errs.append(check_logits(logits.cpu().numpy(), ref3, tol, f"{shape.name} decode"))
     assert eng.device_error() == (0, 0)
     eng.close()
     return max(errs)
 
 
+@pytest.mark.parametrize("fmt", ["bf16", "affine4"])
 @pytest.mark.parametrize("name", sorted(SHAPES))
-def test_prefill_multi_block(name):
-    err = run_case(SHAPES[name], LENS, EXT, cap=512)
-    print(f"{name}: max |logit - oracle| = {err:.3e}")
+def test_prefill_multi_block(name, fmt):
+    err = run_case(SHAPES[name], LENS, EXT, cap=512, fmt=fmt)
+    print(f"{name} {fmt}: max |logit - oracle| = {err:.3e}")
 
 
-def test_prefill_7b_shape_two_layers():
+@pytest.mark.parametrize("fmt", ["bf16", "affine4"])
+def test_prefill_7b_shape_two_layers(fmt):
     """The 7B widths (d_model 4096, 32 q / 8 kv heads, head_dim 128, SwiGLU 14336, vocab
-    32000) at two layers, so the oracle finishes in seconds."""
+    32000) at two layers, so the oracle finishes in seconds; 4-bit weights take the expanded
+    tensor-core path at 300-token segments."""
     shape = ModelShape("mistral-7b-shape-2L", 2, 4096, 32, 8, 128, 14336, 32000, 1e-5, 1e6)
-    err = run_case(shape, [300, 129, 40], {0: 100, 1: 27}, cap=512)
-    print(f"7b-shape 2 layers: max |logit - oracle| = {err:.3e}")
+    err = run_case(shape, [300, 129, 40], {0: 100, 1: 27}, cap=512, fmt=fmt)
+    print(f"7b-shape 2 layers {fmt}: max |logit - oracle| = {err:.3e}")
 
 
 def test_prefill_7b_full_depth_sampled():
