@@ -32,12 +32,17 @@ namespace {
 using tcepi::finish;
 using tcepi::load_residual;
 
-constexpr int kThreads = 192;       // warp 0 TMA, warp 1 MMA (+TMEM alloc), warps 2..5 epilogue
+// warp 0 TMA, warps 1 and 6 MMA (warp 1 also allocates TMEM), warps 2..5 epilogue
+constexpr int kThreads = 224;
 constexpr int kABytes = 128 * 128;  // 128 rows x 64 bf16
 constexpr int kMaxStages = 8;
 constexpr int kMaxSlots = 4;        // tiles one CTA owns in a launch
 constexpr int kSmemBudget = 227 * 1024;
-constexpr int kAcc = 4;             // accumulators per tile (see k_tc_csk)
+// One thread issues a tcgen05.mma about every 60 ns whatever its shape, so at N = 16..64 one
+// issuer caps an SM near 65 GB/s of weights (8 MMAs a 32 KB stage); two issuers, each taking
+// one of a stage's two 64-column blocks into accumulators of its own, lift that cap.
+constexpr int kIssuers = 2;
+constexpr int kAcc = 2;             // accumulators per issuer and tile (see k_tc_csk)
 
 using csk::cluster_rank;
 using csk::cluster_sync;
@@ -105,11 +110,12 @@ __global__ void __launch_bounds__(kThreads, 1)
              const TcParams p, const CskPlan q) {
   constexpr int H = BN / 2;  // operand rows: H hi parts, then H lo parts
   constexpr int kXBytes = BN * 128;  // operand tile of one 64-column block
-  // two buffers (tiles in flight) of kAcc accumulators: super-block sb accumulates into
-  // accumulator (sb - sb0) % kAcc, and the epilogue adds them in fp32 (round to nearest) --
-  // the tensor core's own fp32 accumulation rounds toward zero, and the split divides that
-  // bias by kAcc
-  constexpr uint32_t kTmemCols = 2 * kAcc * BN < 32 ? 32 : 2 * kAcc * BN;
+  // two buffers (tiles in flight) of kIssuers x kAcc accumulators: issuer i's block of
+  // super-block sb accumulates into its accumulator (sb - sb0) % kAcc, and the epilogue adds
+  // all of them in fp32 (round to nearest) -- the tensor core's own fp32 accumulation rounds
+  // toward zero, and the split divides that bias by kIssuers x kAcc
+  static_assert(kCskBlocks == kIssuers, "one 64-column block of a stage per issuer");
+  constexpr uint32_t kTmemCols = 2 * kIssuers * kAcc * BN < 32 ? 32 : 2 * kIssuers * kAcc * BN;
   constexpr uint32_t kIdesc = tc::idesc_bf16(128, BN);
   constexpr uint32_t kPartBytes = 128 * H * 4;  // one CTA's partial sums of one tile
   extern __shared__ uint8_t smem_raw[];
@@ -134,13 +140,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       tc::mbar_init(&sm.full[s], 1);
-      tc::mbar_init(&sm.empty[s], 1);
+      tc::mbar_init(&sm.empty[s], kIssuers);  // every issuer's MMAs have read the stage
     }
     for (int a = 0; a < 2; ++a) {
-      tc::mbar_init(&sm.accf[a], 1);
+      tc::mbar_init(&sm.accf[a], kIssuers);
       tc::mbar_init(&sm.acce[a], 4);
     }
-    tc::mbar_init(sm.done, 1);
+    tc::mbar_init(sm.done, kIssuers);
     for (int s = 0; s < kMaxSlots; ++s) tc::mbar_init(&sm.inbox_full[s], 1);
     // each tile this CTA owns receives the partial sums of the C - 1 other ranks
     if (C > 1)
@@ -218,8 +224,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_wait(&sm.full[stage], phase, lim);
       }
     }
-  } else if (warp == 1) {
-    if (lane == 0) {  // ---- MMA issuer
+  } else if (warp == 1 || warp == 6) {
+    if (lane == 0) {  // ---- MMA issuers: issuer iss takes block iss of every stage
+      const int iss = warp == 1 ? 0 : 1;
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
@@ -229,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc::tc_fence_after();
-        const uint32_t d0 = tmem + (uint32_t)(acc * kAcc * BN);
+        const uint32_t d0 = tmem + (uint32_t)((acc * kIssuers + iss) * kAcc * BN);
         for (int sb = sb0; sb < sb1; ++sb) {
           const uint32_t d = d0 + (uint32_t)(((sb - sb0) % kAcc) * BN);
           if (!wait_or_abort(&sm.full[stage], phase, abort_flag, lim)) {
@@ -238,13 +245,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc::tc_fence_after();
-          for (int jj = 0; jj < NK; ++jj) {
+          for (int jj = iss; jj < NK; jj += kIssuers) {
             const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sm.a + stage * stage_a + jj * kABytes));
             const uint64_t xd = tc::sdesc_sw128(tc::smem_u32(sm.x + stage * stage_x + jj * kXBytes));
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               tc::mma_bf16(d, ad + 2 * kk, xd + 2 * kk, kIdesc,
-                           (sb - sb0 >= kAcc || jj > 0 || kk > 0) ? 1u : 0u);
+                           (sb - sb0 >= kAcc || jj > iss || kk > 0) ? 1u : 0u);
           }
           tc::mma_commit(&sm.empty[stage]);
           if (++stage == S) {
@@ -310,9 +317,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       float vals[H];
 #pragma unroll
       for (int n = 0; n < H; ++n) vals[n] = 0.f;
-      const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(acc * kAcc * BN);
-      const int nacc = sb1 - sb0 < kAcc ? sb1 - sb0 : kAcc;
-      for (int a = 0; a < nacc; ++a) {  // accumulators in a fixed order; hi + lo per column
+      const uint32_t taddr =
+          tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(acc * kIssuers * kAcc * BN);
+      const int nacc = sb1 - sb0 < kAcc ? sb1 - sb0 : kAcc;  // per issuer
+      const int niss = NK < kIssuers ? NK : kIssuers;        // issuers that had a block
+      for (int a = 0; a < niss * kAcc; ++a) {  // issuer-major, a fixed order; hi + lo per column
+        if (a % kAcc >= nacc) continue;
         uint32_t raw[BN];
 #pragma unroll
         for (int c = 0; c < BN / 16; ++c)
