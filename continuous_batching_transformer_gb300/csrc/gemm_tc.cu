@@ -1,39 +1,29 @@
-// gemm_tc.cu -- projections y = x W^T on the 5th-generation tensor cores (sm_103a).
+// gemm_tc.cu -- prefill projections y = x W^T on the 5th-generation tensor cores (sm_103a).
 //
-// Swap-AB: the weight rows are the MMA's M side (128 per tile), the activation rows its N
-// side, so a decode step with B rows is one 128 x N x 64 MMA chain per weight tile and every
-// weight byte crosses HBM once.  Per CTA: one TMA producer thread streams 128x64 bf16 weight
-// tiles and Nx64 activation tiles into a ring of 128-byte-swizzled shared-memory stages;
-// one thread issues tcgen05.mma into a double-buffered TMEM accumulator; four epilogue warps
-// read the accumulator back (tcgen05.ld) and apply the epilogue (store, residual add, or
-// SwiGLU into the next projection's bf16 operand).
+// Swap-AB: the weight rows are the MMA's M side (128 per tile), N tiles of 64 or 128 tokens
+// its N side, whole tiles per CTA over a persistent grid.  Per CTA: one TMA producer thread
+// streams 128x64 bf16 weight tiles and the tokens' 64-column operand tiles into a ring of
+// 128-byte-swizzled shared-memory stages; two threads issue tcgen05.mma into TMEM; four
+// epilogue warps read the accumulators back (tcgen05.ld) and apply the epilogue (store,
+// residual add, or SwiGLU into the next projection's bf16 operand).
 //
-// Decode (SPLIT): activations enter as bf16 hi/lo pairs (x = hi + lo), rows [0, BN/2) hi and
-// [BN/2, BN) lo, summed in the epilogue -- fp32-grade operands at no cost, since the N side
-// is padded anyway.  Work is split stream-K: the (row block, k-step) units are divided evenly
-// over the grid, so every CTA streams the same number of weight bytes; a row block cut
-// between CTAs is finished by whichever CTA completes it last, summing the partial sums in
-// a fixed order, so results do not depend on timing.
+// The activations are bf16 hi/lo pairs (x = hi + lo: lo parts at row act_lo + t), so the
+// operand carries fp32-grade precision; a stage holds both operand tiles.  One thread issues a
+// tcgen05.mma only about every 60 ns whatever its shape, so the products are split over two
+// issuers, each into accumulators of its own: issuer 0 takes hi(W) . x_hi, issuer 1 takes
+// hi(W) . x_lo (and, for 4-bit weights expanded into bf16 hi + lo parts (WLO), lo(W) . x_hi;
+// the lo . lo term is below 2^-16 of the product).
 //
-// RMSNorm without a kernel of its own (decode): RMSNorm(x) W^T = rsqrt(mean(x^2) + eps) *
-// ((x * g) W^T), so the residual-add epilogue that produces x also writes x * g (the next
-// projection's operand, hi/lo) and x's sums of squares over its 128-row tile; the consuming
-// projection scales each accumulated column by the row's rsqrt(mean(x^2) + eps).
-// Prefill (!SPLIT): N tiles of up to 128 tokens, whole tiles per CTA.  The activations are
-// bf16 hi/lo pairs here too (lo parts at row act_lo + t): each stage carries both operand
-// tiles and the MMA chain runs over both.  The tensor core's fp32 accumulation rounds toward
-// zero (measured: a relative bias of -4e-6 over K = 4096, -1.5e-5 over K = 14336), and over a
-// deep prefill the bias reaches the logits through the bf16 rounding of every appended K/V;
-// so every kDrainEvery k-blocks the MMAs start a fresh accumulator (kPrefillAcc of them in
-// rotation, which fill the tensor memory) and the epilogue warps add the finished one into fp32
-// sums with round to nearest while the next k-blocks run: only the MMAs of one group truncate.
-// Measured on a 4 x 1024-token 7B prefill: groups of 1, 2, 4 and 16 k-blocks take 260, 247,
-// 233 and 177 ms a call (the original 16-k-block interleave 142 ms); a 32-layer prefill then
-// decode stays within 1.6-1.7e-2 of the double-precision oracle for groups of up to 4 and
-// exceeds 2e-2 at 16.
-// Prefill over 4-bit weights (WLO): the matrix arrives expanded into bf16 hi and lo parts, each
-// stage carries both weight tiles, and the chain adds lo . x_hi to hi . x_hi + hi . x_lo (the
-// lo . x_lo term is below 2^-16 of the product).
+// The tensor core's fp32 accumulation rounds toward zero (measured: a relative bias of -4e-6
+// over K = 4096, -1.5e-5 over K = 14336), and over a deep prefill the bias reaches the logits
+// through the bf16 rounding of every appended K/V.  So every kDrainEvery k-blocks the issuers
+// start fresh accumulators (two groups in flight, each a pair of accumulators, which fills the
+// tensor memory at N = 128) and the epilogue warps add the finished pair into fp32 sums with
+// round to nearest while the next group runs: the large accumulator takes only the hi . hi
+// MMAs of one group.  Measured on a 4 x 1024-token 7B prefill (bf16): groups of 4, 8 and 16
+// k-blocks take 226, 217 and 203 ms a call, against 142 ms for accumulators that run the whole
+// K range and are read once per tile; a 32-layer prefill then decode stays within 1.6-1.8e-2
+// of the double-precision oracle up to 8 k-blocks a group and exceeds 2e-2 at 16 and beyond.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -47,51 +37,10 @@ namespace {
 using tcepi::finish;
 using tcepi::load_residual;
 
-constexpr int kThreads = 192;       // warp 0 TMA, warp 1 MMA (+TMEM alloc), warps 2..5 epilogue
+// warp 0 TMA, warps 1 and 6 MMA (warp 1 also allocates TMEM), warps 2..5 epilogue
+constexpr int kThreads = 224;
 constexpr int kABytes = 128 * 128;  // 128 rows x 64 bf16
-// Decode stages: 8 x (16 KB of weights + the operand tile) keeps 128 KB of weights in flight
-// per SM (5 stages, which would let a second CTA share the SM, measured slower).
-constexpr int kSplitStages = 8;
-constexpr int kPrefillAcc = 4;   // prefill accumulators in rotation
-constexpr int kDrainEvery = 4;   // k-blocks an accumulator takes before the epilogue adds it up
-
-struct Sched {
-  long long u, u1;
-  int t;
-  __device__ void init(const TcParams& p) {
-    if (p.streamk) {
-      u = (long long)blockIdx.x * p.U / gridDim.x;
-      u1 = (long long)(blockIdx.x + 1) * p.U / gridDim.x;
-    } else {
-      t = blockIdx.x;
-    }
-  }
-  __device__ bool next(const TcParams& p, int& tile, int& kb, int& ke) {
-    if (p.streamk) {
-      if (u >= u1) return false;
-      tile = (int)(u / p.KS);
-      kb = (int)(u % p.KS);
-      long long rem = u1 - u;
-      ke = (int)((long long)p.KS < kb + rem ? (long long)p.KS : kb + rem);
-      u += ke - kb;
-      return true;
-    }
-    if (t >= p.RB * p.NT) return false;
-    tile = t;
-    kb = 0;
-    ke = p.KS;
-    t += gridDim.x;
-    return true;
-  }
-};
-
-// CTA whose stream-K range holds unit u (ranges are [c*U/G, (c+1)*U/G))
-__host__ __device__ inline int cta_of_unit(long long U, long long G, long long u) {
-  long long c = u * G / U;
-  while (c + 1 < G && (c + 1) * U / G <= u) ++c;
-  while (c > 0 && c * U / G > u) --c;
-  return (int)c;
-}
+constexpr int kDrainEvery = 8;      // k-blocks a group of accumulators takes
 
 __device__ __forceinline__ void report_timeout(const TcParams& p, volatile int* abort, int role) {
   *abort = 1;
@@ -107,16 +56,14 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   return false;
 }
 
-
-template <int BN, int STAGES, bool SPLIT, bool WLO>
+template <int BN, int STAGES, bool WLO>
 __global__ void __launch_bounds__(kThreads, 1)
     k_tc_linear(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tx,
                 const __grid_constant__ CUtensorMap twl, const TcParams p) {
-  static_assert(!(WLO && SPLIT), "weight lo parts are a prefill form");
-  constexpr int kXTile = BN * 128;                     // one [BN rows][64] operand tile
-  constexpr int kXBytes = SPLIT ? kXTile : 2 * kXTile;  // prefill stages: hi and lo tiles
+  constexpr int kXTile = BN * 128;                      // one [BN tokens][64] operand tile
+  constexpr int kXBytes = 2 * kXTile;                   // its hi and lo tiles
   constexpr int kAStage = WLO ? 2 * kABytes : kABytes;  // weight tile (+ its lo parts)
-  constexpr uint32_t kTmemCols = SPLIT ? (2 * BN < 32 ? 32 : 2 * BN) : kPrefillAcc * BN;
+  constexpr uint32_t kTmemCols = 4 * BN;                // 2 groups x (issuer 0, issuer 1)
   constexpr uint32_t kIdesc = tc::idesc_bf16(128, BN);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -125,25 +72,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sX = smem + STAGES * kAStage;
   uint64_t* full = reinterpret_cast<uint64_t*>(sX + STAGES * kXBytes);
   uint64_t* empty = full + STAGES;
-  uint64_t* accf = empty + STAGES;  // per accumulator: MMAs done / drained by the epilogue
-  uint64_t* acce = accf + kPrefillAcc;
-  uint64_t* done = acce + kPrefillAcc;
+  uint64_t* accf = empty + STAGES;  // per group buffer: both issuers' MMAs done
+  uint64_t* acce = accf + 2;        // per group buffer: added up by the epilogue
+  uint64_t* done = acce + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
-  volatile int* sflag = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [0] last, [1] abort
+  volatile int* sflag = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [1] abort
   float* swx = reinterpret_cast<float*>(smem + STAGES * (kAStage + kXBytes) + 512);
-  float* rinv = swx + 128 * 33;  // [32] RMSNorm factor of each decode column
+  float* rinv = swx + 128 * 33;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       tc::mbar_init(&full[s], 1);
-      tc::mbar_init(&empty[s], 1);
+      tc::mbar_init(&empty[s], 2);  // both issuers' MMAs have read the stage
     }
-    for (int a = 0; a < kPrefillAcc; ++a) {
-      tc::mbar_init(&accf[a], 1);
-      tc::mbar_init(&acce[a], 4);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&accf[b], 2);
+      tc::mbar_init(&acce[b], 4);
     }
-    tc::mbar_init(done, 1);
+    tc::mbar_init(done, 2);
     sflag[0] = 0;
     sflag[1] = 0;
     tc::mbar_fence_init();
@@ -156,11 +103,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-
   pdl_launch();
-  Sched sch;
-  sch.init(p);
-  int tile, kb, ke;
+  const int tiles = p.RB * p.NT;
+
   if (warp == 0) {
     if (lane == 0) {  // ---- TMA producer
       const uint64_t pol_w = tc::policy_evict_first(), pol_x = tc::policy_evict_last();
@@ -173,23 +118,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       int pend_k[STAGES], pend_nt[STAGES], pend_st[STAGES];
       int npend = 0;
       bool dep_done = false;
+      auto load_x = [&](int st, int k, int nt) {
+        tc::tma_load_2d(sX + st * kXBytes, &tx, &full[st], k * 64, nt * BN, pol_x);
+        tc::tma_load_2d(sX + st * kXBytes + kXTile, &tx, &full[st], k * 64, p.act_lo + nt * BN,
+                        pol_x);
+      };
       auto flush_pending = [&]() {
         pdl_wait();
         dep_done = true;
-        for (int i = 0; i < npend; ++i) {
-          tc::tma_load_2d(sX + pend_st[i] * kXBytes, &tx, &full[pend_st[i]], pend_k[i] * 64,
-                          pend_nt[i] * BN, pol_x);
-          if (!SPLIT)
-            tc::tma_load_2d(sX + pend_st[i] * kXBytes + kXTile, &tx, &full[pend_st[i]],
-                            pend_k[i] * 64, p.act_lo + pend_nt[i] * BN, pol_x);
-        }
+        for (int i = 0; i < npend; ++i) load_x(pend_st[i], pend_k[i], pend_nt[i]);
         npend = 0;
       };
-      while (ok && sch.next(p, tile, kb, ke)) {
+      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
         const int rb = tile / p.NT, nt = tile % p.NT;
         const int y0 = p.epi == EPI_SWIGLU ? rb * 64 : rb * 128;
         const int y1 = p.epi == EPI_SWIGLU ? p.F + rb * 64 : rb * 128 + 64;
-        for (int k = kb; k < ke; ++k) {
+        for (int k = 0; k < p.KS; ++k) {
           if (!wait_or_abort(&empty[stage], phase ^ 1, sflag + 1)) {
             report_timeout(p, sflag + 1, 1);
             ok = false;
@@ -204,10 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             pol_w);
           }
           if (dep_done) {
-            tc::tma_load_2d(sX + stage * kXBytes, &tx, &full[stage], k * 64, nt * BN, pol_x);
-            if (!SPLIT)
-              tc::tma_load_2d(sX + stage * kXBytes + kXTile, &tx, &full[stage], k * 64,
-                              p.act_lo + nt * BN, pol_x);
+            load_x(stage, k, nt);
           } else {
             pend_k[npend] = k;
             pend_nt[npend] = nt;
@@ -231,16 +172,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_wait(&full[stage], phase);
       }
     }
-  } else if (warp == 1) {
-    if (lane == 0 && !SPLIT) {  // ---- MMA issuer, prefill: a fresh accumulator per k-block
-      int stage = 0, a = 0;
-      uint32_t phase = 0, aphase = 0;
+  } else if (warp == 1 || warp == 6) {
+    if (lane == 0) {  // ---- MMA issuers
+      const int iss = warp == 1 ? 0 : 1;
+      int stage = 0, b = 0;
+      uint32_t phase = 0, bphase = 0;
       bool ok = true;
-      while (ok && sch.next(p, tile, kb, ke)) {
-        for (int k = kb; k < ke; ++k) {
-          const bool first = (k - kb) % kDrainEvery == 0;
-          const bool last = (k - kb) % kDrainEvery == kDrainEvery - 1 || k == ke - 1;
-          if (first && !wait_or_abort(&acce[a], aphase ^ 1, sflag + 1)) {  // drained
+      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+        for (int k = 0; k < p.KS; ++k) {
+          const bool first = k % kDrainEvery == 0;
+          const bool last = k % kDrainEvery == kDrainEvery - 1 || k == p.KS - 1;
+          if (first && !wait_or_abort(&acce[b], bphase ^ 1, sflag + 1)) {  // added up
             report_timeout(p, sflag + 1, 2);
             ok = false;
             break;
@@ -251,19 +193,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc::tc_fence_after();
-          const uint32_t d = tmem + (uint32_t)(a * BN);
+          const uint32_t d = tmem + (uint32_t)((2 * b + iss) * BN);
           const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sA + stage * kAStage));
-          const uint64_t xd = tc::sdesc_sw128(tc::smem_u32(sX + stage * kXBytes));
-          const uint64_t ld = tc::sdesc_sw128(tc::smem_u32(sX + stage * kXBytes + kXTile));
+          const uint64_t xd = tc::sdesc_sw128(tc::smem_u32(sX + stage * kXBytes + iss * kXTile));
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)  // hi parts (the group's first MMA overwrites)
+          for (int kk = 0; kk < 4; ++kk)  // a group's first MMA overwrites the accumulator
             tc::mma_bf16(d, ad + 2 * kk, xd + 2 * kk, kIdesc, (kk > 0 || !first) ? 1u : 0u);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) tc::mma_bf16(d, ad + 2 * kk, ld + 2 * kk, kIdesc, 1u);
-          if (WLO) {  // the weights' lo parts against the operand's hi parts
+          if (WLO && iss == 1) {  // the weights' lo parts against the operand's hi parts
             const uint64_t al = tc::sdesc_sw128(tc::smem_u32(sA + stage * kAStage + kABytes));
+            const uint64_t xh = tc::sdesc_sw128(tc::smem_u32(sX + stage * kXBytes));
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) tc::mma_bf16(d, al + 2 * kk, xd + 2 * kk, kIdesc, 1u);
+            for (int kk = 0; kk < 4; ++kk) tc::mma_bf16(d, al + 2 * kk, xh + 2 * kk, kIdesc, 1u);
           }
           tc::mma_commit(&empty[stage]);
           if (++stage == STAGES) {
@@ -271,190 +211,60 @@ __global__ void __launch_bounds__(kThreads, 1)
             phase ^= 1;
           }
           if (last) {
-            tc::mma_commit(&accf[a]);
-            if (++a == kPrefillAcc) {
-              a = 0;
-              aphase ^= 1;
-            }
+            tc::mma_commit(&accf[b]);
+            b ^= 1;
+            if (b == 0) bphase ^= 1;
           }
         }
       }
-      tc::mma_commit(done);
-      tc::mbar_wait(done, 0);
-    } else if (lane == 0) {  // ---- MMA issuer, decode: one accumulator per tile, two buffers
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      bool ok = true;
-      while (ok && sch.next(p, tile, kb, ke)) {
-        if (!wait_or_abort(&acce[acc], acc_phase ^ 1, sflag + 1)) {
-          report_timeout(p, sflag + 1, 2);
-          break;
-        }
-        tc::tc_fence_after();
-        const uint32_t d = tmem + acc * BN;
-        for (int k = kb; k < ke; ++k) {
-          if (!wait_or_abort(&full[stage], phase, sflag + 1)) {
-            report_timeout(p, sflag + 1, 3);
-            ok = false;
-            break;
-          }
-          tc::tc_fence_after();
-          const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sA + stage * kAStage));
-          const uint64_t xd = tc::sdesc_sw128(tc::smem_u32(sX + stage * kXBytes));
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc::mma_bf16(d, ad + 2 * kk, xd + 2 * kk, kIdesc, (k > kb || kk > 0) ? 1u : 0u);
-          tc::mma_commit(&empty[stage]);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
-        if (!ok) break;
-        tc::mma_commit(&accf[acc]);
-        if (++acc == 2) {
-          acc = 0;
-          acc_phase ^= 1;
-        }
-      }
-      // all MMAs of this thread complete before TMEM is released
+      // all MMAs of both issuers complete before TMEM is released
       tc::mma_commit(done);
       tc::mbar_wait(done, 0);
     }
   } else {  // ---- epilogue warps 2..5
-    pdl_wait();  // outputs and the stream-K scratch are shared with the previous kernel
+    pdl_wait();  // outputs are shared with the previous kernel
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;
-    if (SPLIT && p.ss_in) {  // RMSNorm factor of each decode row, from the per-tile sums
-      if (r < p.n_act) {
-        float s = 0.f;
-        for (int t = 0; t < p.ss_tiles; ++t) s += p.ss_in[(size_t)t * p.ss_ld + r];
-        rinv[r] = rsqrtf(s / (float)p.K + p.eps);
-      }
-      tc::named_bar_sync(1, 128);
-    }
-    if (!SPLIT) {
-      // prefill: every k-block's accumulator is added into fp32 sums (round to nearest) as soon
-      // as its MMAs are done, then handed back; the tile's epilogue runs on the sums
-      int a = 0;
-      uint32_t aphase = 0;
-      bool ok = true;
-      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
-      while (ok && sch.next(p, tile, kb, ke)) {
-        const int rb = tile / p.NT, nt = tile % p.NT;
-        float sums[BN];
+    const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
+    int b = 0;
+    uint32_t bphase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+      const int rb = tile / p.NT, nt = tile % p.NT;
+      float sums[BN];
 #pragma unroll
-        for (int j = 0; j < BN; ++j) sums[j] = 0.f;
-        for (int k = kb; k < ke; k += kDrainEvery) {
-          if (!wait_or_abort(&accf[a], aphase, sflag + 1)) {
-            report_timeout(p, sflag + 1, 4);
-            ok = false;
-            break;
-          }
-          tc::tc_fence_after();
-#pragma unroll
-          for (int c0 = 0; c0 < BN; c0 += 64) {
-            uint32_t raw[64];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tc::tmem_ld16(tbase + (uint32_t)(a * BN + c0 + 16 * c), raw + 16 * c);
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 64; ++j) sums[c0 + j] += __uint_as_float(raw[j]);
-          }
-          tc::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&acce[a]);
-          if (++a == kPrefillAcc) {
-            a = 0;
-            aphase ^= 1;
-          }
+      for (int j = 0; j < BN; ++j) sums[j] = 0.f;
+      for (int k = 0; k < p.KS; k += kDrainEvery) {
+        if (!wait_or_abort(&accf[b], bphase, sflag + 1)) {
+          report_timeout(p, sflag + 1, 4);
+          ok = false;
+          break;
         }
-        if (!ok) break;
+        tc::tc_fence_after();
 #pragma unroll
         for (int c0 = 0; c0 < BN; c0 += 32) {
-          float res[32];
-          load_residual<32>(p, rb, r, nt * BN + c0, res);
-          finish<32>(p, rb, r, sums + c0, nt * BN + c0, swx, rinv, res, tcepi::epi_src_global(p));
-        }
-      }
-    } else {
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    while (sch.next(p, tile, kb, ke)) {
-      if (!wait_or_abort(&accf[acc], acc_phase, sflag + 1)) {
-        report_timeout(p, sflag + 1, 4);
-        break;
-      }
-      tc::tc_fence_after();
-      const int rb = tile / p.NT, nt = tile % p.NT;
-      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-      if (SPLIT) {
-        constexpr int H = BN / 2;
-        uint32_t raw[BN];
+          uint32_t hi[32], lo[32];
+          tc::tmem_ld16(tbase + (uint32_t)(2 * b * BN + c0), hi);
+          tc::tmem_ld16(tbase + (uint32_t)(2 * b * BN + c0 + 16), hi + 16);
+          tc::tmem_ld16(tbase + (uint32_t)((2 * b + 1) * BN + c0), lo);
+          tc::tmem_ld16(tbase + (uint32_t)((2 * b + 1) * BN + c0 + 16), lo + 16);
+          tc::tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < BN / 16; ++c) tc::tmem_ld16(taddr + 16 * c, raw + 16 * c);
-        tc::tmem_ld_wait();
+          for (int j = 0; j < 32; ++j) sums[c0 + j] += __uint_as_float(hi[j]) + __uint_as_float(lo[j]);
+        }
         tc::tc_fence_before();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&acce[acc]);
-        float vals[H];
-#pragma unroll
-        for (int n = 0; n < H; ++n) vals[n] = __uint_as_float(raw[n]) + __uint_as_float(raw[n + H]);
-        if (kb == 0 && ke == p.KS) {
-          float res[H];
-          load_residual<H>(p, rb, r, 0, res);
-          finish<H>(p, rb, r, vals, 0, swx, rinv, res, tcepi::epi_src_global(p));
-        } else {
-          const int first = cta_of_unit(p.U, gridDim.x, (long long)tile * p.KS);
-          const int slot = blockIdx.x - first;
-          float* pp = p.part + ((size_t)tile * p.slots + slot) * H * 128;
-#pragma unroll
-          for (int n = 0; n < H; ++n)
-            if (n < p.n_act) pp[n * 128 + r] = vals[n];
-          __threadfence();
-          tc::named_bar_sync(1, 128);
-          if (threadIdx.x == 64) {
-            const int old = atomicAdd(p.cnt + tile, ke - kb);
-            sflag[0] = (old + (ke - kb) == p.KS) ? 1 : 0;
-          }
-          tc::named_bar_sync(1, 128);
-          if (sflag[0]) {
-            __threadfence();
-            const int last = cta_of_unit(p.U, gridDim.x, (long long)tile * p.KS + p.KS - 1);
-            float res[H], sum[H];
-            load_residual<H>(p, rb, r, 0, res);
-#pragma unroll
-            for (int n = 0; n < H; ++n) sum[n] = 0.f;
-            // partial slots in order (a fixed summation order keeps results reproducible),
-            // the loads of kChunk slots in flight together
-            constexpr int kChunk = H <= 16 ? 4 : 2;
-            const int nslots = last - first + 1;
-            for (int s0 = 0; s0 < nslots; s0 += kChunk) {
-              float ld[kChunk][H];
-#pragma unroll
-              for (int i = 0; i < kChunk; ++i) {
-                const float* ps = p.part + ((size_t)tile * p.slots + s0 + i) * H * 128;
-#pragma unroll
-                for (int n = 0; n < H; ++n)
-                  ld[i][n] = (s0 + i < nslots && n < p.n_act) ? __ldcg(ps + n * 128 + r) : 0.f;
-              }
-#pragma unroll
-              for (int i = 0; i < kChunk; ++i)
-                if (s0 + i < nslots) {
-#pragma unroll
-                  for (int n = 0; n < H; ++n) sum[n] += ld[i][n];
-                }
-            }
-            finish<H>(p, rb, r, sum, 0, swx, rinv, res, tcepi::epi_src_global(p));
-            if (threadIdx.x == 64) p.cnt[tile] = 0;
-          }
-        }
+        if (lane == 0) tc::mbar_arrive(&acce[b]);
+        b ^= 1;
+        if (b == 0) bphase ^= 1;
       }
-      if (++acc == 2) {
-        acc = 0;
-        acc_phase ^= 1;
+      if (!ok) break;
+#pragma unroll
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        float res[32];
+        load_residual<32>(p, rb, r, nt * BN + c0, res);
+        finish<32>(p, rb, r, sums + c0, nt * BN + c0, swx, rinv, res, tcepi::epi_src_global(p));
       }
-    }
     }
   }
   tc::tc_fence_before();
@@ -465,13 +275,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, int STAGES, bool SPLIT, bool WLO = false>
+template <int BN, int STAGES, bool WLO>
 cudaError_t launch_inst(const CUtensorMap& tw, const CUtensorMap& tx, const TcParams& p, int grid,
-                        cudaStream_t s, const CUtensorMap* twl = nullptr) {
-  constexpr size_t smem = 1024 + STAGES * (kABytes * (WLO ? 2 : 1) + BN * 128 * (SPLIT ? 1 : 2)) +
-                          512 + 128 * 33 * 4 + 256;
+                        cudaStream_t s, const CUtensorMap* twl) {
+  constexpr size_t smem =
+      1024 + STAGES * (kABytes * (WLO ? 2 : 1) + 2 * BN * 128) + 512 + 128 * 33 * 4 + 256;
   static_assert(smem <= 227 * 1024, "shared memory budget");
-  auto kern = k_tc_linear<BN, STAGES, SPLIT, WLO>;
+  auto kern = k_tc_linear<BN, STAGES, WLO>;
   cudaError_t rc = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (rc != cudaSuccess) return rc;
   return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, tw, tx, WLO ? *twl : tw, p);
@@ -533,58 +343,35 @@ bool make_tmap_kblocks(CUtensorMap* m, const void* base, uint64_t K, uint64_t ro
 int tc_split_bn(int n) { return n <= 8 ? 16 : (n <= 16 ? 32 : 64); }
 int tc_plain_bn(int n) { return n <= 64 ? 64 : 128; }
 
-// Plan and launch one projection.  p carries shapes, epilogue and outputs; this fills the
-// schedule.  Returns false if the shape is outside what the kernel supports.
+// Plan and launch one prefill projection: N tiles of BN (64 or 128) tokens, whole tiles per CTA
+// over min(tiles, SMs) CTAs.  p carries shapes, epilogue and outputs.  Returns false if the
+// shape is outside what the kernel supports (decode rows go to launch_tc_csk / launch_q4_rd).
 bool launch_tc_linear(const CUtensorMap& tw, const CUtensorMap& tx, TcParams p, bool split, int BN,
                       int num_sms, size_t part_floats, cudaStream_t s, const CUtensorMap* twl) {
-  if (twl && split) return false;
+  (void)part_floats;
+  if (split) return false;
   if (p.K % 64 || p.K <= 0 || p.n_act <= 0) return false;
   if (p.epi == EPI_SWIGLU && (p.F % 64 || p.M != 2 * p.F)) return false;
-  if (!split && p.ss_in) return false;  // the per-column RMSNorm factors exist for decode rows only
-  if (!split && p.act_lo < p.n_act) return false;  // prefill operands carry their lo parts
+  if (p.ss_in) return false;               // the folded RMSNorm is a decode form
+  if (p.act_lo < p.n_act) return false;    // the operand carries its lo parts
   p.RB = p.epi == EPI_SWIGLU ? p.F / 64 : (p.M + 127) / 128;
   p.KS = p.K / 64;
-  if (split) {
-    if (2 * p.n_act > BN) return false;
-    p.NT = 1;
-    p.streamk = 1;
-    p.U = (long long)p.RB * p.KS;
-    int G = (int)std::min<long long>(num_sms, p.U);
-    // partial slots per tile: most CTAs whose ranges meet one tile
-    for (;;) {
-      int slots = 1;
-      for (int t = 0; t < p.RB; ++t) {
-        int f = cta_of_unit(p.U, G, (long long)t * p.KS);
-        int l = cta_of_unit(p.U, G, (long long)t * p.KS + p.KS - 1);
-        slots = std::max(slots, l - f + 1);
-      }
-      if ((size_t)p.RB * slots * (BN / 2) * 128 <= part_floats || G == 1) {
-        p.slots = slots;
-        break;
-      }
-      G = std::max(1, G / 2);
-    }
-    if ((size_t)p.RB * p.slots * (BN / 2) * 128 > part_floats) return false;
-    cudaError_t rc;
-    if (BN == 16) rc = launch_inst<16, kSplitStages, true>(tw, tx, p, G, s);
-    else if (BN == 32) rc = launch_inst<32, kSplitStages, true>(tw, tx, p, G, s);
-    else if (BN == 64) rc = launch_inst<64, kSplitStages, true>(tw, tx, p, G, s);
-    else return false;
-    return rc == cudaSuccess;
-  }
   p.NT = (p.n_act + BN - 1) / BN;
   p.streamk = 0;
   p.U = (long long)p.RB * p.NT * p.KS;
   p.slots = 0;
-  const int tiles = p.RB * p.NT;
-  const int G = std::min(tiles, num_sms);
+  const int G = std::min(p.RB * p.NT, num_sms);
   cudaError_t rc;
   if (twl) {  // weights as hi + lo parts: a third tile per stage
-    if (BN == 64) rc = launch_inst<64, 4, false, true>(tw, tx, p, G, s, twl);
-    else if (BN == 128) rc = launch_inst<128, 3, false, true>(tw, tx, p, G, s, twl);
+    if (BN == 64) rc = launch_inst<64, 4, true>(tw, tx, p, G, s, twl);
+    else if (BN == 128) rc = launch_inst<128, 3, true>(tw, tx, p, G, s, twl);
     else return false;
-  } else if (BN == 64) rc = launch_inst<64, 6, false>(tw, tx, p, G, s);
-  else if (BN == 128) rc = launch_inst<128, 4, false>(tw, tx, p, G, s);
-  else return false;
+  } else if (BN == 64) {
+    rc = launch_inst<64, 6, false>(tw, tx, p, G, s, nullptr);
+  } else if (BN == 128) {
+    rc = launch_inst<128, 4, false>(tw, tx, p, G, s, nullptr);
+  } else {
+    return false;
+  }
   return rc == cudaSuccess;
 }
