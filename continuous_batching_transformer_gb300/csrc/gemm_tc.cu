@@ -259,11 +259,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (b == 0) bphase ^= 1;
       }
       if (!ok) break;
+      // one copy of the (large) epilogue code: each 16-column chunk is moved out of the sums
+      // by constant indices (so they stay in registers) and finished in a loop that is not
+      // unrolled -- four inlined copies crowd the issuing warps out of the instruction cache
+#pragma unroll 1
+      for (int c = 0; c < BN / 16; ++c) {
+        float v[16], res[16];
 #pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        float res[32];
-        load_residual<32>(p, rb, r, nt * BN + c0, res);
-        finish<32>(p, rb, r, sums + c0, nt * BN + c0, swx, rinv, res, tcepi::epi_src_global(p));
+        for (int cc = 0; cc < BN / 16; ++cc)
+          if (cc == c) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = sums[16 * cc + j];
+          }
+        load_residual<16>(p, rb, r, nt * BN + 16 * c, res);
+        finish<16>(p, rb, r, v, nt * BN + 16 * c, swx, rinv, res, tcepi::epi_src_global(p));
       }
     }
   }

@@ -24,7 +24,11 @@
 namespace {
 
 constexpr int kItemKeys = 128;  // keys per attention item (one 128-key sub-chunk)
-constexpr int kAttnThreads = 128;
+constexpr int kAttnWarps = 8;                        // each takes 16 keys of an item
+constexpr int kAttnThreads = 32 * kAttnWarps;
+constexpr int kKeysPerWarp = kItemKeys / kAttnWarps;
+constexpr int kNt = kKeysPerWarp / 8;                // score tiles (n8) per warp
+constexpr int kKs = kKeysPerWarp / 16;               // P.V k16 steps per warp
 
 // One warp quantises one group of 64 values; lane j holds values 2j and 2j + 1.  With
 // L = 2^BITS - 1: scale = bf16((max - min) / L), bias = bf16(min), code = clamp(rint((x - bias) /
@@ -183,13 +187,13 @@ struct QAttnSmem {
     alignas(16) uint8_t q[16 * HD * 2];  // the Q operand image (bf16 hi rows 0..7, lo 8..15)
   };
   Stage st[2];
-  float ored[4][G][HD];  // per warp: its keys' share of P.V
-  float redm[4][8], redl[4][8];
-  float redb[4][8][NG];
+  float ored[kAttnWarps][G][HD];  // per warp: its keys' share of P.V
+  float redm[kAttnWarps][8], redl[kAttnWarps][8];
+  float redb[kAttnWarps][8][NG];
 };
 
-// One item (row b, kv head g, 128-key sub-chunk s0) per iteration; warp w takes keys
-// [32 w, 32 w + 32) of it.  Scores S[h][key] = sum over 64-dim groups of
+// One item (row b, kv head g, 128-key sub-chunk s0) per iteration; each of the 8 warps takes
+// 16 of its keys (16 w .. 16 w + 15), so a short chain per warp and 16 warps per SM.  Scores S[h][key] = sum over 64-dim groups of
 // scale * (q . codes) + bias * sum(q): an m16n8k16 MMA per 16 dims and 8 keys, the A rows being
 // the group's q heads as fp16 high parts (rows 0..7) and remainders (rows 8..15), the codes
 // converted exactly to fp16, one accumulator per group folded with its key's scale and bias.
@@ -291,23 +295,23 @@ __global__ void __launch_bounds__(kAttnThreads)
       qsum[gr] += __shfl_xor_sync(0xffffffffu, qsum[gr], 1);
       qsum[gr] += __shfl_xor_sync(0xffffffffu, qsum[gr], 2);
     }
-    // ---- scores of this warp's 32 keys: s[nt][j] is key 32 w + 8 nt + 2 tq + j, head gq
-    float s[4][2];
+    // ---- scores of this warp's 16 keys: s[nt][j] is key 16 w + 8 nt + 2 tq + j, head gq
+    float s[kNt][2];
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) s[nt][0] = s[nt][1] = 0.f;
+    for (int nt = 0; nt < kNt; ++nt) s[nt][0] = s[nt][1] = 0.f;
 #pragma unroll
     for (int gr = 0; gr < NG; ++gr) {
-      float acc[4][4];
+      float acc[kNt][4];
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
+      for (int nt = 0; nt < kNt; ++nt)
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         const int k = 4 * gr + kk;
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-          const uint8_t* row = st.kc + (32 * warp + 8 * nt + gq) * kPitch;
+        for (int nt = 0; nt < kNt; ++nt) {
+          const uint8_t* row = st.kc + (kKeysPerWarp * warp + 8 * nt + gq) * kPitch;
           uint32_t b0, b1;
           if (BITS == 8) {  // codes of dims 16 k + 4 tq .. + 3
             const uint32_t c = *reinterpret_cast<const uint32_t*>(row + 16 * k + 4 * tq);
@@ -322,10 +326,10 @@ __global__ void __launch_bounds__(kAttnThreads)
         }
       }
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
+      for (int nt = 0; nt < kNt; ++nt)
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          const int key = 32 * warp + 8 * nt + 2 * tq + j;
+          const int key = kKeysPerWarp * warp + 8 * nt + 2 * tq + j;
           const float sc = bf16_to_f32(st.ks[key * NG + gr]), bi = bf16_to_f32(st.kb[key * NG + gr]);
           s[nt][j] += sc * (acc[nt][j] + acc[nt][j + 2]) + bi * qsum[gr];
         }
@@ -333,10 +337,10 @@ __global__ void __launch_bounds__(kAttnThreads)
     // ---- softmax of head gq over the item's keys
     float mx = -INFINITY;
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < kNt; ++nt)
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const int key = 32 * warp + 8 * nt + 2 * tq + j;
+        const int key = kKeysPerWarp * warp + 8 * nt + 2 * tq + j;
         if (key >= nk) s[nt][j] = -INFINITY;
         mx = fmaxf(mx, s[nt][j]);
       }
@@ -344,11 +348,13 @@ __global__ void __launch_bounds__(kAttnThreads)
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
     if (tq == 0) sm.redm[warp][gq] = mx;
     __syncthreads();
-    const float m = fmaxf(fmaxf(sm.redm[0][gq], sm.redm[1][gq]), fmaxf(sm.redm[2][gq], sm.redm[3][gq]));
-    float l = 0.f;
-    float p[4][2];
+    float m = sm.redm[0][gq];
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int w = 1; w < kAttnWarps; ++w) m = fmaxf(m, sm.redm[w][gq]);
+    float l = 0.f;
+    float p[kNt][2];
+#pragma unroll
+    for (int nt = 0; nt < kNt; ++nt)
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         p[nt][j] = s[nt][j] == -INFINITY ? 0.f : __expf(s[nt][j] - m);
@@ -360,17 +366,17 @@ __global__ void __launch_bounds__(kAttnThreads)
     // ---- P.V over this warp's keys, group by group
 #pragma unroll
     for (int gr = 0; gr < NG; ++gr) {
-      uint32_t pa[2][4];
+      uint32_t pa[kKs][4];
       float bsum = 0.f;
 #pragma unroll
-      for (int ks = 0; ks < 2; ++ks)
+      for (int ks = 0; ks < kKs; ++ks)
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           const int nt = 2 * ks + half;
           float pv[2];
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
-            const int key = 32 * warp + 8 * nt + 2 * tq + j;
+            const int key = kKeysPerWarp * warp + 8 * nt + 2 * tq + j;
             const bool ok = key < nk;  // masked keys may hold stale scales and biases
             pv[j] = ok ? p[nt][j] * bf16_to_f32(st.vs[key * NG + gr]) : 0.f;
             bsum += ok ? p[nt][j] * bf16_to_f32(st.vb[key * NG + gr]) : 0.f;
@@ -392,8 +398,8 @@ __global__ void __launch_bounds__(kAttnThreads)
 #pragma unroll
         for (int i = 0; i < 4; ++i) o[t][i] = 0.f;
 #pragma unroll
-      for (int ks = 0; ks < 2; ++ks) {
-        const int key0 = 32 * warp + 16 * ks + 2 * tq;
+      for (int ks = 0; ks < kKs; ++ks) {
+        const int key0 = kKeysPerWarp * warp + 16 * ks + 2 * tq;
         const int rows[4] = {key0, key0 + 1, key0 + 8, key0 + 9};
         uint32_t w[4][2];  // per row: codes of the 8 dims (8 bits: two words; 4 bits: one)
 #pragma unroll
@@ -442,17 +448,25 @@ __global__ void __launch_bounds__(kAttnThreads)
       }
     }
     __syncthreads();
-    // ---- this item's partial output per q head: the four warps' shares in warp order
+    // ---- this item's partial output per q head: the warps' shares in warp order
     for (int i = tid; i < G * HD; i += kAttnThreads) {
       const int h = i / HD, d = i % HD, gr = d / 64;
-      const float o = sm.ored[0][h][d] + sm.ored[1][h][d] + sm.ored[2][h][d] + sm.ored[3][h][d] +
-                      (sm.redb[0][h][gr] + sm.redb[1][h][gr] + sm.redb[2][h][gr] + sm.redb[3][h][gr]);
+      float o = 0.f, bsum = 0.f;
+#pragma unroll
+      for (int w = 0; w < kAttnWarps; ++w) {  // the warps' shares in warp order
+        o += sm.ored[w][h][d];
+        bsum += sm.redb[w][h][gr];
+      }
+      o += bsum;
       a.part_o[((long long)it * G + h) * HD + d] = o;
     }
     if (tid < G) {
-      const float mm = fmaxf(fmaxf(sm.redm[0][tid], sm.redm[1][tid]), fmaxf(sm.redm[2][tid], sm.redm[3][tid]));
-      a.part_ml[(long long)it * G + tid] =
-          make_float2(mm, sm.redl[0][tid] + sm.redl[1][tid] + sm.redl[2][tid] + sm.redl[3][tid]);
+      float mm = sm.redm[0][tid], ll = 0.f;
+#pragma unroll
+      for (int w = 1; w < kAttnWarps; ++w) mm = fmaxf(mm, sm.redm[w][tid]);
+#pragma unroll
+      for (int w = 0; w < kAttnWarps; ++w) ll += sm.redl[w][tid];
+      a.part_ml[(long long)it * G + tid] = make_float2(mm, ll);
     }
   }
   cp_async_wait_all();  // no copy in flight at exit
