@@ -15,9 +15,10 @@
 // Layout of the work: tile t of the matrix belongs to cluster t % NC (clusters take tiles
 // cid, cid + NC, ...), rank r of the cluster streams k-blocks [r*KS/C, (r+1)*KS/C) of each of
 // its cluster's tiles, and tile j of a cluster (in that order) is owned by rank j % C.  Per CTA
-// the pipeline is the one of gemm_tc.cu: a TMA producer warp (weights requested before the
-// previous kernel finishes, operand tiles after), an MMA warp (swap-AB: 128 weight rows x N
-// operand rows, bf16 hi/lo operand parts, fp32 accumulators in TMEM), four epilogue warps.
+// the pipeline: a TMA producer warp for the weights (which stream from the kernel's start, before
+// the previous kernel finishes), a TMA producer warp for the operand tiles (after it), two MMA
+// warps (swap-AB: 128 weight rows x N operand rows, bf16 hi/lo operand parts, fp32
+// accumulators in TMEM), four epilogue warps.
 #include <algorithm>
 #include <map>
 #include <tuple>
@@ -32,8 +33,9 @@ namespace {
 using tcepi::finish;
 using tcepi::load_residual;
 
-// warp 0 TMA, warps 1 and 6 MMA (warp 1 also allocates TMEM), warps 2..5 epilogue
-constexpr int kThreads = 224;
+// warp 0 TMA (weights), warp 7 TMA (operand), warps 1 and 6 MMA (warp 1 also allocates TMEM),
+// warps 2..5 epilogue
+constexpr int kThreads = 256;
 constexpr int kABytes = 128 * 128;  // 128 rows x 64 bf16
 constexpr int kMaxStages = 8;
 constexpr int kMaxSlots = 4;        // tiles one CTA owns in a launch
@@ -166,25 +168,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_launch();
 
   if (warp == 0) {
-    if (lane == 0) {  // ---- TMA producer
-      const uint64_t pol_w = tc::policy_evict_first(), pol_x = tc::policy_evict_last();
+    if (lane == 0) {  // ---- TMA producer of the weight tiles
+      // The weights never depend on the previous kernel: they stream from the start, while the
+      // operand producer (warp 7) waits for it.  Each stage's barrier expects both halves.
+      const uint64_t pol_w = tc::policy_evict_first();
       int stage = 0;
       uint32_t phase = 0;
       long long issued = 0;
       bool ok = true;
-      // the weights never depend on the previous kernel: the first stages' weight tiles are
-      // requested before waiting for it, their operand tiles once it has finished
-      int pend_k[kMaxStages], pend_st[kMaxStages];
-      int npend = 0;
-      bool dep_done = false;
-      auto flush_pending = [&]() {
-        pdl_wait();
-        dep_done = true;
-        for (int i = 0; i < npend; ++i)
-          tc::tma_load_3d(sm.x + pend_st[i] * stage_x, &tx, &sm.full[pend_st[i]], 0, 0, pend_k[i] * NK,
-                          pol_x);
-        npend = 0;
-      };
       for (int j = 0; j < Tc && ok && !p.stall_loads; ++j) {
         const int rb = cid + j * NC;
         for (int sb = sb0; sb < sb1; ++sb) {
@@ -200,13 +191,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::tma_load_4d(sm.a + stage * stage_a, &tw, &sm.full[stage], 0, rb * 64, 0, sb * NK, pol_w);
           else
             tc::tma_load_3d(sm.a + stage * stage_a, &tw, &sm.full[stage], 0, rb * 128, sb * NK, pol_w);
-          if (dep_done) {
-            tc::tma_load_3d(sm.x + stage * stage_x, &tx, &sm.full[stage], 0, 0, sb * NK, pol_x);
-          } else {
-            pend_k[npend] = sb;
-            pend_st[npend] = stage;
-            if (++npend == S) flush_pending();
-          }
           ++issued;
           if (++stage == S) {
             stage = 0;
@@ -214,14 +198,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (!dep_done) flush_pending();
-      // never leave with copies in flight: wait for the last loads issued to each stage
+      // never leave with copies in flight: wait for the last loads issued to each stage (weights
+      // and operands complete the same barrier)
       for (int i = 0; i < S && i < issued; ++i) {
         if (--stage < 0) {
           stage = S - 1;
           phase ^= 1;
         }
         tc::mbar_wait(&sm.full[stage], phase, lim);
+      }
+    }
+  } else if (warp == 7) {
+    if (lane == 0) {  // ---- TMA producer of the operand tiles, once the previous kernel is done
+      // A stage's operand may land before the weight producer's expect-tx: the barrier's
+      // transaction count goes below zero until then, and the phase cannot complete without
+      // that arrival.  Waiting on the same empty phases keeps this thread within one ring pass.
+      const uint64_t pol_x = tc::policy_evict_last();
+      pdl_wait();
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int j = 0; j < Tc && ok && !p.stall_loads; ++j) {
+        for (int sb = sb0; sb < sb1; ++sb) {
+          if (!wait_or_abort(&sm.empty[stage], phase ^ 1, abort_flag, lim)) {
+            report_timeout(p, abort_flag, 6);
+            ok = false;
+            break;
+          }
+          tc::tma_load_3d(sm.x + stage * stage_x, &tx, &sm.full[stage], 0, 0, sb * NK, pol_x);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
       }
     }
   } else if (warp == 1 || warp == 6) {
