@@ -50,7 +50,23 @@ __device__ __forceinline__ void flag_timeout(int* err, volatile int* abort_flag,
   if (atomicCAS(err, 0, CBT_DEV_TIMEOUT) == 0) err[1] = where;
 }
 
-template <int HD>
+// the maxima (MAX) or sums of N values of every lane, across the warp: the N reductions
+// interleaved level by level, so their shuffle latencies overlap
+template <int N, bool MAX>
+__device__ __forceinline__ void warp_reduce_n(float (&v)[N]) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float t[N];
+#pragma unroll
+    for (int h = 0; h < N; ++h) t[h] = __shfl_xor_sync(0xffffffffu, v[h], o);
+#pragma unroll
+    for (int h = 0; h < N; ++h) v[h] = MAX ? fmaxf(v[h], t[h]) : v[h] + t[h];
+  }
+}
+
+// G q heads per kv head, GT = G rounded up to 1, 2, 4 or 8: the softmax and the output
+// accumulation run over GT heads (the MMAs' unused head rows are zero), masked to G
+template <int HD, int GT>
 __global__ void __launch_bounds__(160, kCtasPerSm)
     k_attn_decode(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                   const uint8_t* __restrict__ qtile, const QueryRow* __restrict__ rows,
@@ -165,6 +181,8 @@ __global__ void __launch_bounds__(160, kCtasPerSm)
     }
   } else {
     // ---- compute warps: MMA issue (thread 0), softmax (thread = key), accumulate (thread = dim)
+    // P rows of the heads past GT (and their lo rows) are never written: zero once
+    for (int i = tid; i < 2 * 2048 / 4; i += kCompute) reinterpret_cast<uint32_t*>(sP)[i] = 0u;
     pdl_wait();  // Q, the new K/V and the partial buffers are shared with earlier kernels
     if (tid == 0) stamp_begin(stamp);
     uint32_t qn = 0, kn = 0, vn = 0, sn = 0;
@@ -176,9 +194,9 @@ __global__ void __launch_bounds__(160, kCtasPerSm)
         m_run[tid] = -INFINITY;
         l_run[tid] = 0.f;
       }
-      float oacc[8];
+      float oacc[GT];
 #pragma unroll
-      for (int h = 0; h < 8; ++h) oacc[h] = 0.f;
+      for (int h = 0; h < GT; ++h) oacc[h] = 0.f;
       tc::named_bar_sync(1, kCompute);
 
       for (int sub = w.s0; sub < w.s1; ++sub, ++sn) {
@@ -214,15 +232,19 @@ __global__ void __launch_bounds__(160, kCtasPerSm)
         tc::tmem_ld_wait();
         const int key = sub * kSub + tid;
         const bool valid = key < n;
-        float s[8];
+        float s[GT], mx[GT];
 #pragma unroll
-        for (int h = 0; h < 8; ++h) {
+        for (int h = 0; h < GT; ++h) {
           s[h] = valid ? __uint_as_float(raw[h]) + __uint_as_float(raw[8 + h]) : -INFINITY;
-          const float mx = warp_max(s[h]);
-          if (lane == 0) red[warp * 8 + h] = mx;
+          mx[h] = s[h];
+        }
+        warp_reduce_n<GT, true>(mx);
+        if (lane == 0) {
+#pragma unroll
+          for (int h = 0; h < GT; ++h) red[warp * 8 + h] = mx[h];
         }
         tc::named_bar_sync(1, kCompute);
-        if (tid < 8) {
+        if (tid < GT) {
           const float mloc = fmaxf(fmaxf(red[tid], red[8 + tid]), fmaxf(red[16 + tid], red[24 + tid]));
           const float mo = m_run[tid];
           const float mn = fmaxf(mo, mloc);
@@ -230,14 +252,19 @@ __global__ void __launch_bounds__(160, kCtasPerSm)
           m_run[tid] = mn;
         }
         tc::named_bar_sync(1, kCompute);
+        float ps[GT];
 #pragma unroll
-        for (int h = 0; h < 8; ++h) {
+        for (int h = 0; h < GT; ++h) {  // P rows of heads >= GT stay zero (set at the start)
           const float p = (valid && h < G) ? __expf(s[h] - m_run[h]) : 0.f;
           const uint16_t hi = f32_to_bf16(p);
           st_bf16(sP, sw128_offset(h, tid, 2048), hi);
           st_bf16(sP, sw128_offset(8 + h, tid, 2048), f32_to_bf16(p - bf16_to_f32(hi)));
-          const float ps = warp_sum(p);
-          if (lane == 0) red2[warp * 8 + h] = ps;
+          ps[h] = p;
+        }
+        warp_reduce_n<GT, false>(ps);
+        if (lane == 0) {
+#pragma unroll
+          for (int h = 0; h < GT; ++h) red2[warp * 8 + h] = ps[h];
         }
         if (sub * kSub + kSub > n) {
           // keys past t_s: their V^T columns may hold stale values, so once V has landed
@@ -256,7 +283,7 @@ __global__ void __launch_bounds__(160, kCtasPerSm)
         fence_proxy_async();
         tc::tc_fence_before();
         tc::named_bar_sync(1, kCompute);
-        if (tid < 8)
+        if (tid < GT)
           l_run[tid] = l_run[tid] * scl[tid] + red2[tid] + red2[8 + tid] + red2[16 + tid] + red2[24 + tid];
         if (tid == 0) {
           if (!tc::mbar_wait(vfull, vn & 1)) {
@@ -283,7 +310,7 @@ __global__ void __launch_bounds__(160, kCtasPerSm)
         tc::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + 16, raw);
         tc::tmem_ld_wait();
 #pragma unroll
-        for (int h = 0; h < 8; ++h)
+        for (int h = 0; h < GT; ++h)
           oacc[h] = oacc[h] * scl[h] + __uint_as_float(raw[h]) + __uint_as_float(raw[8 + h]);
         tc::tc_fence_before();
       }
@@ -380,16 +407,16 @@ __global__ void __launch_bounds__(128)
   }
 }
 
-template <int HD>
+template <int HD, int GT>
 cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const AttnDecodeArgs& a,
                           int grid, cudaStream_t s) {
   constexpr int nKh = HD / 64;
   constexpr size_t smem = 1024 + (nKh + 2) * kBox + nKh * 2048 + 2 * 2048 + 512;
   static_assert(smem * kCtasPerSm <= 228 * 1024, "shared memory budget");
-  cudaError_t rc = cudaFuncSetAttribute(k_attn_decode<HD>,
+  cudaError_t rc = cudaFuncSetAttribute(k_attn_decode<HD, GT>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (rc != cudaSuccess) return rc;
-  return launch_pdl(k_attn_decode<HD>, dim3(grid), dim3(160), smem, s, tk, tv, a.qtile, a.rows,
+  return launch_pdl(k_attn_decode<HD, GT>, dim3(grid), dim3(160), smem, s, tk, tv, a.qtile, a.rows,
                     a.items, a.n_items, a.layer, a.n_kv_heads, a.n_heads / a.n_kv_heads, a.part_o,
                     a.part_ml, a.err, a.stamp);
 }
@@ -401,8 +428,18 @@ bool launch_attn_decode_tc(const CUtensorMap& tk, const CUtensorMap& tv, const A
   if (a.n_heads % a.n_kv_heads || a.n_heads / a.n_kv_heads > 8) return false;
   const int grid = kCtasPerSm * num_sms;  // persistent; the item count is read on the device
   cudaError_t rc;
-  if (a.head_dim == 128) rc = launch_decode<128>(tk, tv, a, grid, s);
-  else if (a.head_dim == 64) rc = launch_decode<64>(tk, tv, a, grid, s);
+  const int G = a.n_heads / a.n_kv_heads;
+  const int gt = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8;
+  if (a.head_dim == 128)
+    rc = gt == 1 ? launch_decode<128, 1>(tk, tv, a, grid, s)
+         : gt == 2 ? launch_decode<128, 2>(tk, tv, a, grid, s)
+         : gt == 4 ? launch_decode<128, 4>(tk, tv, a, grid, s)
+                   : launch_decode<128, 8>(tk, tv, a, grid, s);
+  else if (a.head_dim == 64)
+    rc = gt == 1 ? launch_decode<64, 1>(tk, tv, a, grid, s)
+         : gt == 2 ? launch_decode<64, 2>(tk, tv, a, grid, s)
+         : gt == 4 ? launch_decode<64, 4>(tk, tv, a, grid, s)
+                   : launch_decode<64, 8>(tk, tv, a, grid, s);
   else return false;
   if (rc != cudaSuccess) return false;
   return launch_attn_merge(a, s);
