@@ -357,9 +357,34 @@ __global__ void k_argmax(const float* logits, int vocab, int32_t* out) {
   const float* r = logits + (size_t)blockIdx.x * vocab;
   float best = -INFINITY;
   int idx = 0x7fffffff;
-  for (int i = threadIdx.x; i < vocab; i += blockDim.x) {
-    float v = r[i];
-    if (v > best) { best = v; idx = i; }  // strided scan: earlier index kept on ties
+  if ((vocab & 3) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0) {
+    // 16-byte loads, kU of them in flight per thread (one load per iteration leaves the
+    // scan a chain of memory latencies); each thread still visits its indices in increasing
+    // order, so the earlier index is kept on ties
+    constexpr int kU = 8;
+    const float4* r4 = reinterpret_cast<const float4*>(r);
+    const int n4 = vocab >> 2;
+    for (int base = threadIdx.x; base < n4; base += blockDim.x * kU) {
+      float4 v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = base + u * (int)blockDim.x;
+        v[u] = i < n4 ? __ldcg(r4 + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = 4 * (base + u * (int)blockDim.x);
+        if (v[u].x > best) { best = v[u].x; idx = i; }
+        if (v[u].y > best) { best = v[u].y; idx = i + 1; }
+        if (v[u].z > best) { best = v[u].z; idx = i + 2; }
+        if (v[u].w > best) { best = v[u].w; idx = i + 3; }
+      }
+    }
+  } else {
+    for (int i = threadIdx.x; i < vocab; i += blockDim.x) {
+      float v = r[i];
+      if (v > best) { best = v; idx = i; }  // strided scan: earlier index kept on ties
+    }
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
