@@ -125,12 +125,20 @@ __device__ __forceinline__ void finish(const TcParams& p, int rb, int r, float* 
       }
     }
     if (p.ss_out) {
-      // sums of squares of the updated rows over this tile's 128 rows, for the next RMSNorm
+      // sums of squares of the updated rows over this tile's 128 rows, for the next RMSNorm;
+      // the CNT warp reductions interleaved level by level, so their shuffles overlap
       const int w = r >> 5, lane = r & 31;
 #pragma unroll
-      for (int j = 0; j < CNT; ++j) {
-        const float s = warp_sum(sq[j]);
-        if (lane == 0) swx[w * 32 + j] = s;
+      for (int o = 16; o > 0; o >>= 1) {
+        float t[CNT];
+#pragma unroll
+        for (int j = 0; j < CNT; ++j) t[j] = __shfl_xor_sync(0xffffffffu, sq[j], o);
+#pragma unroll
+        for (int j = 0; j < CNT; ++j) sq[j] += t[j];
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int j = 0; j < CNT; ++j) swx[w * 32 + j] = sq[j];
       }
       tc::named_bar_sync(1, 128);
       if (r < CNT && tok0 + r < p.n_act)
