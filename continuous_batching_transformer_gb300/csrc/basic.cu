@@ -10,17 +10,90 @@
 // With ss, also what the first RMSNorm needs when it is folded into the QKV projection: the
 // row's sums of squares over each 128-element tile, ss[tile * ss_ld + i], and the operand
 // x * gain as bf16 hi (row i of act) and lo (row lo_rows + i) parts.
-__global__ void k_embed(const int32_t* tokens, int d, int vocab, const uint16_t* table, float* x,
-                        int* err, float* ss, int ss_ld, const uint16_t* gain, uint16_t* act,
-                        int lo_rows) {
+// Embedding rows (one block of 256 threads per token) and, in the blocks after them, the RoPE
+// cos/sin table of the call's positions (fp32 [n][head_dim / 2] each, angles in double): one
+// launch for the step's two independent prologue kernels.  A token's row is read with 16-byte
+// loads, eight columns a thread, all in flight together; the same values give the first
+// RMSNorm's per-128-column sums of squares (16 threads per tile).
+__global__ void k_embed_rope(const int32_t* tokens, int n, int d, int vocab,
+                             const uint16_t* table, float* x, int* err, float* ss, int ss_ld,
+                             const uint16_t* gain, uint16_t* act, int lo_rows,
+                             const QueryRow* rows, int half, int head_dim, double theta,
+                             float* cosv, float* sinv) {
   pdl_wait();
   pdl_launch();
-  int i = blockIdx.x;
-  int t = tokens[i];
+  if ((int)blockIdx.x >= n) {  // RoPE table
+    const int idx = (blockIdx.x - n) * blockDim.x + threadIdx.x;
+    if (idx >= n * half) return;
+    const int t = idx / half, i = idx % half;
+    const double freq = pow(theta, -2.0 * (double)i / (double)head_dim);
+    const double ang = (double)rows[t].pos * freq;
+    double sv, cv;
+    sincos(ang, &sv, &cv);
+    cosv[idx] = (float)cv;
+    sinv[idx] = (float)sv;
+    return;
+  }
+  const int i = blockIdx.x;
+  const int t = tokens[i];
   float* xr = x + (size_t)i * d;
   const bool bad = t < 0 || t >= vocab;
   if (bad && threadIdx.x == 0) set_device_error(err, CBT_DEV_TOKEN_RANGE, i);
   const uint16_t* er = table + (size_t)(bad ? 0 : t) * d;
+  if ((d & 127) == 0 && (reinterpret_cast<uintptr_t>(table) & 15) == 0 &&
+      (!act || (reinterpret_cast<uintptr_t>(gain) & 15) == 0)) {
+    constexpr int kU = 4;  // 8-column chunks per thread in flight
+    const int nch = d >> 3;
+    for (int c0 = threadIdx.x; c0 < nch; c0 += blockDim.x * kU) {
+      uint4 e[kU], g[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int c = c0 + u * (int)blockDim.x;
+        e[u] = (c < nch && !bad) ? __ldg(reinterpret_cast<const uint4*>(er) + c) : make_uint4(0, 0, 0, 0);
+        g[u] = (c < nch && act) ? __ldg(reinterpret_cast<const uint4*>(gain) + c) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int c = c0 + u * (int)blockDim.x;
+        const uint32_t ew[4] = {e[u].x, e[u].y, e[u].z, e[u].w};
+        const uint32_t gw[4] = {g[u].x, g[u].y, g[u].z, g[u].w};
+        float v[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          v[2 * k] = bf16_lo(ew[k]);
+          v[2 * k + 1] = bf16_hi(ew[k]);
+        }
+        float sq = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) sq = fmaf(v[k], v[k], sq);
+        if (c < nch) {
+          *reinterpret_cast<float4*>(xr + 8 * c) = make_float4(v[0], v[1], v[2], v[3]);
+          *reinterpret_cast<float4*>(xr + 8 * c + 4) = make_float4(v[4], v[5], v[6], v[7]);
+          if (act) {
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float a0 = v[2 * k] * bf16_lo(gw[k]), a1 = v[2 * k + 1] * bf16_hi(gw[k]);
+              const uint16_t h0 = f32_to_bf16(a0), h1 = f32_to_bf16(a1);
+              hw[k] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+              lw[k] = (uint32_t)f32_to_bf16(a0 - bf16_to_f32(h0)) |
+                      ((uint32_t)f32_to_bf16(a1 - bf16_to_f32(h1)) << 16);
+            }
+            *reinterpret_cast<uint4*>(act + (size_t)i * d + 8 * c) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            if (lo_rows > 0)
+              *reinterpret_cast<uint4*>(act + (size_t)(lo_rows + i) * d + 8 * c) =
+                  make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          }
+        }
+        if (ss) {  // the 16 chunks of a 128-column tile sit in 16 consecutive lanes
+#pragma unroll
+          for (int o = 8; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+          if ((threadIdx.x & 15) == 0 && c < nch) ss[(size_t)(c >> 4) * ss_ld + i] = sq;
+        }
+      }
+    }
+    return;
+  }
   for (int j = threadIdx.x; j < d; j += blockDim.x) {
     const float v = bad ? 0.f : bf16_to_f32(er[j]);
     xr[j] = v;
@@ -34,23 +107,26 @@ __global__ void k_embed(const int32_t* tokens, int d, int vocab, const uint16_t*
   if (ss) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
     for (int tile = warp; tile * 128 < d; tile += nw) {
-      float s = 0.f;
+      float sum = 0.f;
       for (int j = tile * 128 + lane; j < d && j < tile * 128 + 128; j += 32) {
         const float v = bad ? 0.f : bf16_to_f32(er[j]);
-        s = fmaf(v, v, s);
+        sum = fmaf(v, v, sum);
       }
-      s = warp_sum(s);
-      if (lane == 0) ss[(size_t)tile * ss_ld + i] = s;
+      sum = warp_sum(sum);
+      if (lane == 0) ss[(size_t)tile * ss_ld + i] = sum;
     }
   }
 }
 
-void launch_embed(const int32_t* tokens, int n, const uint16_t* table, int d, int vocab, float* x,
-                  int* err, float* ss, int ss_ld, const uint16_t* gain, uint16_t* act,
-                  int lo_rows, cudaStream_t s) {
+void launch_embed_rope(const int32_t* tokens, int n, const uint16_t* table, int d, int vocab,
+                       float* x, int* err, float* ss, int ss_ld, const uint16_t* gain,
+                       uint16_t* act, int lo_rows, const QueryRow* rows, int head_dim,
+                       double theta, float* cosv, float* sinv, cudaStream_t s) {
   if (n <= 0) return;
-  launch_pdl(k_embed, dim3(n), dim3(256), 0, s, tokens, d, vocab, table, x, err, ss, ss_ld, gain,
-             act, lo_rows);
+  const int half = head_dim / 2;
+  const int rope_blocks = (n * half + 255) / 256;
+  launch_pdl(k_embed_rope, dim3(n + rope_blocks), dim3(256), 0, s, tokens, n, d, vocab, table, x,
+             err, ss, ss_ld, gain, act, lo_rows, rows, half, head_dim, theta, cosv, sinv);
 }
 
 // ---- RMSNorm: h = x / sqrt(mean(x^2) + eps) * g -----------------------------------------
@@ -130,29 +206,6 @@ void launch_f32_to_act(const float* src, int n, int K, uint16_t* act, int lo_row
 }
 
 // ---- RoPE angles once per call: cos/sin of pos * theta^(-2i/hd), evaluated in double -------
-__global__ void k_rope_table(const QueryRow* rows, int n, int half, int head_dim, double theta,
-                             float* cosv, float* sinv) {
-  pdl_wait();
-  pdl_launch();
-  int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= n * half) return;
-  int t = idx / half, i = idx % half;
-  double freq = pow(theta, -2.0 * (double)i / (double)head_dim);
-  double ang = (double)rows[t].pos * freq;
-  double sv, cv;
-  sincos(ang, &sv, &cv);
-  cosv[idx] = (float)cv;
-  sinv[idx] = (float)sv;
-}
-
-void launch_rope_table(const QueryRow* rows, int n, int head_dim, double theta, float* cosv,
-                       float* sinv, cudaStream_t s) {
-  int half = head_dim / 2;
-  int tot = n * half;
-  if (tot <= 0) return;
-  launch_pdl(k_rope_table, dim3((tot + 255) / 256), dim3(256), 0, s, rows, n, half, head_dim, theta, cosv, sinv);
-}
-
 // ---- RoPE q, k in place at the token's position; append k, v to its own slab at pos ------
 __global__ void k_rope_append(float* qkv, const QueryRow* rows, int layer, int n_heads,
                               int n_kv_heads, int head_dim, const float* cosv, const float* sinv,

@@ -1240,11 +1240,10 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
   e->stamp_n = 0;
   e->stamp_cls.clear();
   int t = tbegin(e, CBT_KCLASS_OTHER);
-  launch_embed(tokens, n, static_cast<const uint16_t*>(e->w.embed), d, c.vocab, e->x, e->err,
-               fused ? e->ss : nullptr, e->ss_ld,
-               static_cast<const uint16_t*>(e->layers[0].attn_norm), fused ? e->act_h : nullptr,
-               lo, s);
-  launch_rope_table(e->rows, n, c.head_dim, c.rope_theta, e->cosv, e->sinv, s);
+  launch_embed_rope(tokens, n, static_cast<const uint16_t*>(e->w.embed), d, c.vocab, e->x, e->err,
+                    fused ? e->ss : nullptr, e->ss_ld,
+                    static_cast<const uint16_t*>(e->layers[0].attn_norm), fused ? e->act_h : nullptr,
+                    lo, e->rows, c.head_dim, c.rope_theta, e->cosv, e->sinv, s);
   tend(e, t, 2.0 * n * d + 4.0 * n * d);
   for (int l = 0; l < c.n_layers && ok; ++l) {
     const cbt_layer_weights& L = e->layers[l];

@@ -226,16 +226,16 @@ void launch_rmsnorm_act(const float* x, const uint16_t* gain, int n, int d, floa
 // fp32 rows into a bf16 operand (hi/lo as above)
 void launch_f32_to_act(const float* src, int n, int K, uint16_t* act, int lo_rows, cudaStream_t s);
 
-// embed + token range check
-void launch_embed(const int32_t* tokens, int n, const uint16_t* table, int d, int vocab, float* x,
-                  int* err, float* ss, int ss_ld, const uint16_t* gain, uint16_t* act,
-                  int lo_rows, cudaStream_t s);
+// embed + token range check (and, decode, the first RMSNorm's statistics and operand), with the
+// RoPE cos/sin table of the rows' positions (fp32 [n][head_dim / 2], angles in double) built by
+// extra blocks of the same launch
+void launch_embed_rope(const int32_t* tokens, int n, const uint16_t* table, int d, int vocab,
+                       float* x, int* err, float* ss, int ss_ld, const uint16_t* gain,
+                       uint16_t* act, int lo_rows, const QueryRow* rows, int head_dim,
+                       double theta, float* cosv, float* sinv, cudaStream_t s);
 // RMSNorm rows of x into h
 cudaError_t launch_rmsnorm(const float* x, const uint16_t* gain, int n, int d, float eps,
                            float* h, cudaStream_t s);
-// per-token RoPE cos/sin for the positions in rows (fp32 [n][hd/2] each), in double
-void launch_rope_table(const QueryRow* rows, int n, int head_dim, double theta, float* cosv,
-                       float* sinv, cudaStream_t s);
 // RoPE q and k in place at each token's position; append k, v (bf16) to its slab; with
 // qtile, also write each row's Q operand images for the decode attention ([n][Hkv][16][hd])
 void launch_rope_append(float* qkv, const QueryRow* rows, int n, int layer, int n_heads,
