@@ -187,6 +187,8 @@ struct QAttnSmem {
     alignas(16) uint8_t q[16 * HD * 2];  // the Q operand image (bf16 hi rows 0..7, lo 8..15)
   };
   Stage st[2];
+  alignas(16) uint32_t qfrag[(HD / 16) * 32 * 4];  // the item's Q fragments, [k-step][lane][4]
+  float qks[HD / 16][8];                           // sum of q over each k-step's dims, per head
   float ored[kAttnWarps][G][HD];  // per warp: its keys' share of P.V
   float redm[kAttnWarps][8], redl[kAttnWarps][8];
   float redb[kAttnWarps][8][NG];
@@ -266,35 +268,47 @@ __global__ void __launch_bounds__(kAttnThreads)
       if (tid == 0) set_device_error(a.err, CBT_DEV_WORK_ITEM, it);
       continue;
     }
-    // ---- Q fragments (head gq: high parts in A rows gq, remainders in rows gq + 8) and the
-    // group sums of q
-    uint32_t qa[HD / 16][4];
-    float qsum[NG];
-#pragma unroll
-    for (int gr = 0; gr < NG; ++gr) qsum[gr] = 0.f;
-#pragma unroll
-    for (int k = 0; k < HD / 16; ++k) {
+    // ---- Q fragments (head gq: high parts in A rows gq, remainders in rows gq + 8), built once
+    // per item by the whole CTA: thread (k, l) converts fragment k of lane l and the k-step's
+    // sum of q for head l / 4; contraction slots 2 tq, 2 tq + 1 (half 0) and 2 tq + 8, 2 tq + 9
+    // (half 1) of k-step k hold dims 16 k + 4 tq + 2 half + {0, 1}: a thread's four dims are
+    // consecutive, so one load gives its key codes (the same order on the K side below)
+    if (tid < (HD / 16) * 32) {
+      const int k = tid >> 5, fgq = lane >> 2, ftq = lane & 3;
+      uint32_t f[4];
+      float fs = 0.f;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        // contraction slots 2 tq, 2 tq + 1 (half 0) and 2 tq + 8, 2 tq + 9 (half 1) of k-step k
-        // hold dims 16 k + 4 tq + 2 half + {0, 1}: a thread's four dims are consecutive, so one
-        // load gives its key codes (the same order on the K side below)
-        const int d = 16 * k + 4 * tq + 2 * half;
-        const uint32_t hi = *reinterpret_cast<const uint32_t*>(st.q + sw128_offset(gq, d, 2048));
-        const uint32_t lo = *reinterpret_cast<const uint32_t*>(st.q + sw128_offset(8 + gq, d, 2048));
+        const int d = 16 * k + 4 * ftq + 2 * half;
+        const uint32_t hi = *reinterpret_cast<const uint32_t*>(st.q + sw128_offset(fgq, d, 2048));
+        const uint32_t lo = *reinterpret_cast<const uint32_t*>(st.q + sw128_offset(8 + fgq, d, 2048));
         const float q0 = bf16_lo(hi) + bf16_lo(lo), q1 = bf16_hi(hi) + bf16_hi(lo);
         const __half2 h = __floats2half2_rn(q0, q1);
         const float2 hf = __half22float2(h);
-        qa[k][2 * half] = *reinterpret_cast<const uint32_t*>(&h);
-        qa[k][2 * half + 1] = pack_half2(q0 - hf.x, q1 - hf.y);
-        qsum[k / 4] += q0 + q1;
+        f[2 * half] = *reinterpret_cast<const uint32_t*>(&h);
+        f[2 * half + 1] = pack_half2(q0 - hf.x, q1 - hf.y);
+        fs += q0 + q1;
       }
+      reinterpret_cast<uint4*>(sm.qfrag)[tid] = make_uint4(f[0], f[1], f[2], f[3]);
+      fs += __shfl_xor_sync(0xffffffffu, fs, 1);
+      fs += __shfl_xor_sync(0xffffffffu, fs, 2);
+      if (ftq == 0) sm.qks[k][fgq] = fs;  // sum over the k-step's 16 dims of head fgq
+    }
+    __syncthreads();
+    uint32_t qa[HD / 16][4];
+    float qsum[NG];
+#pragma unroll
+    for (int k = 0; k < HD / 16; ++k) {
+      const uint4 f = reinterpret_cast<const uint4*>(sm.qfrag)[k * 32 + lane];
+      qa[k][0] = f.x;
+      qa[k][1] = f.y;
+      qa[k][2] = f.z;
+      qa[k][3] = f.w;
     }
 #pragma unroll
-    for (int gr = 0; gr < NG; ++gr) {
-      qsum[gr] += __shfl_xor_sync(0xffffffffu, qsum[gr], 1);
-      qsum[gr] += __shfl_xor_sync(0xffffffffu, qsum[gr], 2);
-    }
+    for (int gr = 0; gr < NG; ++gr)  // the group's four k-steps, in order
+      qsum[gr] = ((sm.qks[4 * gr][gq] + sm.qks[4 * gr + 1][gq]) + sm.qks[4 * gr + 2][gq]) +
+                 sm.qks[4 * gr + 3][gq];
     // ---- scores of this warp's 16 keys: s[nt][j] is key 16 w + 8 nt + 2 tq + j, head gq
     float s[kNt][2];
 #pragma unroll
