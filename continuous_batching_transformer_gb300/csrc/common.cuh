@@ -65,6 +65,7 @@ struct AttnItem {
   long long kbase;
   int cap, p0;  // quantised KV: kbase is the byte offset of the slab or page, cap its layout
                 // capacity, p0 its first position
+  int n;        // the row's keys (its position + 1), so an item needs no second load
 };
 
 // Device error word: the first error wins (code, info).
@@ -112,4 +113,5 @@ enum Epilogue : int {
   EPI_ADD = 1,     // out[n][m] += y (residual)
   EPI_SWIGLU = 2,  // W = [gate; up] (2F rows): out[n][j] = silu(y_gate[j]) * y_up[j], j < F
   EPI_QKV = 3,     // W = [Wq; Wk; Wv]: RoPE, KV append and the attention's Q operand (decode)
+  EPI_QKVQ = 4,    // EPI_QKV on a quantised-KV engine: the new K/V quantised into the slabs
 };

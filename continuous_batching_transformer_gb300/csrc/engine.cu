@@ -1149,7 +1149,7 @@ static bool tc_projection(cbt_engine* e, const CUtensorMap& wmap, const CUtensor
     p.ss_tiles = (e->cfg.d_model + 127) / 128;
     p.eps = e->cfg.rms_eps;
   }
-  if (epi == EPI_QKV) {  // RoPE + KV append + the attention's Q operand, in the epilogue
+  if (epi == EPI_QKV || epi == EPI_QKVQ) {  // RoPE + KV append + the attention's Q operand
     p.rows = e->rows;
     p.layer = layer;
     p.n_heads = e->cfg.n_heads;
@@ -1159,6 +1159,10 @@ static bool tc_projection(cbt_engine* e, const CUtensorMap& wmap, const CUtensor
     p.sinv = e->sinv;
     p.arena = static_cast<uint16_t*>(e->p.kv_arena);
     p.qtile = e->qtile;
+    if (epi == EPI_QKVQ) {  // the new K/V quantised in the epilogue, into each row's slab
+      p.kvq_jobs = e->kv8_jobs;
+      p.kvq_bits = e->kv_bits;
+    }
   }
   if (next_gain) {
     p.ss_out = e->ss;
@@ -1260,7 +1264,7 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
     if (tcp)
       ok &= tc_projection(e, e->wmaps[l].qkv, e->wmaps_kb[l].qkv, e->q4w[l].qkv, &L.wqkv,
                           cbt_engine::kQ4xQkv, e->act_h, n, d, qd + 2 * kvd,
-                          fused ? EPI_QKV : EPI_STORE, e->qkv, qd + 2 * kvd, nullptr, 0, fused,
+                          fused ? (quant ? EPI_QKVQ : EPI_QKV) : EPI_STORE, e->qkv, qd + 2 * kvd, nullptr, 0, fused,
                           nullptr, l);
     else
       projection(e, e->h, n, d, L.wqkv, qd + 2 * kvd, EPI_STORE, e->qkv);
@@ -1272,11 +1276,13 @@ static cudaError_t forward(cbt_engine* e, int n, const int32_t* tokens, int max_
                          tc_prefill ? e->qb : nullptr, e->qb_rows, s);
     uint8_t* arena8 = static_cast<uint8_t*>(e->p.kv_arena);
     if (quant && !gather) {
-      // quantised KV decode: each row's new K/V went to its staging page (the QKV epilogue, or
-      // the RoPE kernel above); quantise them into the row's slab, then split attention over
-      // the codes on the tensor cores and the merge into the O projection's operand
-      ok &= launch_kvq_convert(e->kv8_jobs, n, 1, l, 1, c.n_kv_heads, c.head_dim, e->kv_bits,
-                               arena8, s);
+      // quantised KV decode: the fused QKV epilogue quantised each row's new K/V into its slab;
+      // otherwise they went to the row's staging page (the RoPE kernel above) and are
+      // quantised here.  Then split attention over the codes on the tensor cores and the merge
+      // into the O projection's operand
+      if (!fused)
+        ok &= launch_kvq_convert(e->kv8_jobs, n, 1, l, 1, c.n_kv_heads, c.head_dim, e->kv_bits,
+                                 arena8, s);
       KvqAttnArgs qa{};
       qa.qtile = e->qtile;
       qa.rows = e->rows;
@@ -1428,7 +1434,8 @@ static cudaError_t plan_decode_attention(cbt_engine* e, int B) {
     for (int g = 0; g < Hkv; ++g)
       for (int sp = 0; sp < splits; ++sp) {
         AttnItem it{b, g, sp * kSubsPerItem, std::min(nsub, (sp + 1) * kSubsPerItem),
-                    row_base(e, *e->hslab[b], sp * kSubsPerItem * 128), 0, 0};
+                    row_base(e, *e->hslab[b], sp * kSubsPerItem * 128), 0, 0,
+                    e->hrows[b].pos + 1};
         if (e->quant()) {  // the quantised slab or page: byte offset, capacity, first position
           const QLoc q = qloc(e, *e->hslab[b], sp * kSubsPerItem * 128);
           it.kbase = q.off;

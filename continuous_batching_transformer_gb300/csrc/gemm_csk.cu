@@ -106,7 +106,9 @@ __device__ __forceinline__ Smem carve(uint8_t* smem, const CskPlan& q, bool qkv)
   return s;
 }
 
-template <int BN>
+// EPI: the launch's epilogue (p.epi), a template parameter so that each launch carries only
+// its own epilogue code (all four inlined together crowd the instruction cache)
+template <int BN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     k_tc_csk(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tx,
              const TcParams p, const CskPlan q) {
@@ -123,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  const Smem sm = carve<BN>(base, q, p.epi == EPI_QKV);
+  const Smem sm = carve<BN>(base, q, EPI == EPI_QKV || EPI == EPI_QKVQ);
   const int S = q.stages, C = q.C, NK = q.nk;
   const int stage_a = NK * kABytes, stage_x = NK * kXBytes;  // bytes per stage
   volatile int* abort_flag = sm.sflag + 1;
@@ -187,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mbar_expect_tx(&sm.full[stage], stage_a + stage_x);
           // NK blocks of the tile's 128 weight rows (SwiGLU: 64 gate rows, then the same 64
           // features' up rows) in one box, each block a swizzled [128][64] tile
-          if (p.epi == EPI_SWIGLU)
+          if (EPI == EPI_SWIGLU)
             tc::tma_load_4d(sm.a + stage * stage_a, &tw, &sm.full[stage], 0, rb * 64, 0, sb * NK, pol_w);
           else
             tc::tma_load_3d(sm.a + stage * stage_a, &tw, &sm.full[stage], 0, rb * 128, sb * NK, pol_w);
@@ -292,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     tcepi::EpiSrc src = tcepi::epi_src_global(p);
-    if (p.epi == EPI_QKV) {
+    if (EPI == EPI_QKV || EPI == EPI_QKVQ) {
       // the row table and the RoPE tables in shared memory, loaded while the weights stream
       const int half = p.head_dim >> 1;
       for (int i = r; i < p.n_act * half; i += 128) {
@@ -314,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the owner's global inputs of this tile, requested before its accumulator is ready
       float res[H];
       if (rank == owner) {
-        load_residual<H>(p, rb, r, 0, res);
+        load_residual<H, EPI>(p, rb, r, 0, res);
         src.gn = tcepi::load_next_gain(p, rb, r);
         src.has_gn = true;
       }
@@ -354,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         report_timeout(p, abort_flag, 5);
         break;
       }
-      if (got > 0) finish<H>(p, rb, r, sum, 0, sm.swx, sm.rinv, res, src);
+      if (got > 0) finish<H, EPI>(p, rb, r, sum, 0, sm.swx, sm.rinv, res, src);
     }
     // an owner leaves only after its inbox has been filled (bounded: a peer that gave up sends
     // nothing), so no st.async can land in a CTA that has exited
@@ -372,11 +374,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // cluster dims and PDL on one launch
-template <int BN>
+template <int BN, int EPI>
 cudaError_t launch_csk(const CUtensorMap& tw, const CUtensorMap& tx, const TcParams& p,
                        const CskPlan& q, cudaStream_t s) {
-  const size_t smem = csk_smem_bytes<BN>(q, p.epi == EPI_QKV);
-  auto kern = k_tc_csk<BN>;
+  const size_t smem = csk_smem_bytes<BN>(q, EPI == EPI_QKV || EPI == EPI_QKVQ);
+  auto kern = k_tc_csk<BN, EPI>;
   cudaError_t rc = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (rc != cudaSuccess) return rc;
   cudaLaunchConfig_t cfg = {};
@@ -397,6 +399,19 @@ cudaError_t launch_csk(const CUtensorMap& tw, const CUtensorMap& tx, const TcPar
   return cudaLaunchKernelEx(&cfg, kern, tw, tx, p, q);
 }
 
+template <int BN>
+cudaError_t launch_csk_epi(const CUtensorMap& tw, const CUtensorMap& tx, const TcParams& p,
+                           const CskPlan& q, cudaStream_t s) {
+  switch (p.epi) {
+    case EPI_STORE: return launch_csk<BN, EPI_STORE>(tw, tx, p, q, s);
+    case EPI_ADD: return launch_csk<BN, EPI_ADD>(tw, tx, p, q, s);
+    case EPI_SWIGLU: return launch_csk<BN, EPI_SWIGLU>(tw, tx, p, q, s);
+    case EPI_QKV: return launch_csk<BN, EPI_QKV>(tw, tx, p, q, s);
+    case EPI_QKVQ: return launch_csk<BN, EPI_QKVQ>(tw, tx, p, q, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
 // most clusters of C CTAs (each with `smem` bytes) resident at once, cached per configuration
 template <int BN>
 int active_clusters(int C, size_t smem) {
@@ -404,7 +419,7 @@ int active_clusters(int C, size_t smem) {
   auto key = std::make_pair(C, smem);
   auto it = cache.find(key);
   if (it != cache.end()) return it->second;
-  auto kern = k_tc_csk<BN>;
+  auto kern = k_tc_csk<BN, EPI_ADD>;  // every epilogue's instance has the same shape
   int n = 0;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
       cudaSuccess) {
@@ -493,9 +508,9 @@ bool launch_tc_csk(const CUtensorMap& tw, const CUtensorMap& tx, TcParams p, int
     plans[key] = q;
   }
   cudaError_t rc;
-  if (BN == 16) rc = launch_csk<16>(tw, tx, p, q, s);
-  else if (BN == 32) rc = launch_csk<32>(tw, tx, p, q, s);
-  else if (BN == 64) rc = launch_csk<64>(tw, tx, p, q, s);
+  if (BN == 16) rc = launch_csk_epi<16>(tw, tx, p, q, s);
+  else if (BN == 32) rc = launch_csk_epi<32>(tw, tx, p, q, s);
+  else if (BN == 64) rc = launch_csk_epi<64>(tw, tx, p, q, s);
   else return false;
   return rc == cudaSuccess;
 }

@@ -200,6 +200,7 @@ __device__ __forceinline__ TcParams pass_params(const TcParams& p0, int pass) {
   if (p.cosv) p.cosv += (size_t)r0 * (p.head_dim / 2);
   if (p.sinv) p.sinv += (size_t)r0 * (p.head_dim / 2);
   if (p.qtile) p.qtile += (size_t)r0 * p.n_kv_heads * 16 * p.head_dim * 2;
+  if (p.kvq_jobs) p.kvq_jobs += r0;
   return p;
 }
 
@@ -321,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ssq[i] = __ldcg(p.ss_in + (size_t)tt * p.ss_ld + b);
     }
   tcepi::EpiSrc src = tcepi::epi_src_global(p);
-  if (p.epi == EPI_QKV) {
+  if (p.epi == EPI_QKV || p.epi == EPI_QKVQ) {
     const int half = p.head_dim >> 1;
     for (int i = threadIdx.x; i < p.n_act * half; i += kThreads) {
       scos[i] = p.cosv[i];
@@ -605,7 +606,7 @@ bool q4r_launch(const TcParams& p, const uint16_t* x, int x_lo, const Q4rPlan& q
 bool launch_q4_rd(TcParams p, const uint16_t* x, int x_lo, int num_sms, cudaStream_t s) {
   if (!p.wq || !x || p.K % 128 || p.K <= 0 || p.n_act <= 0 || p.n_act > 32) return false;
   if (p.epi == EPI_SWIGLU && (p.F % 64 || p.M != 2 * p.F)) return false;
-  if (p.epi == EPI_QKV && (p.head_dim > 128 || p.head_dim % 2)) return false;
+  if ((p.epi == EPI_QKV || p.epi == EPI_QKVQ) && (p.head_dim > 128 || p.head_dim % 2)) return false;
   if (p.ss_in && p.ss_tiles > kMaxSsTiles) return false;
   p.RB = p.epi == EPI_SWIGLU ? p.F / 64 : (p.M + 127) / 128;
   p.KS = p.K / 64;

@@ -38,6 +38,8 @@ struct LinearW {
 };
 
 // ---- tensor-core projections (gemm_tc.cu) --------------------------------------------------
+struct Kv8Job;
+
 struct TcParams {
   int M, K;          // W is [M][K] bf16; for EPI_SWIGLU M = 2F (gate rows, then up rows)
   int F;             // EPI_SWIGLU: features per output row
@@ -75,6 +77,11 @@ struct TcParams {
   const float* sinv;
   uint16_t* arena;
   uint8_t* qtile;
+  // EPI_QKVQ (EPI_QKV on a quantised-KV engine): the new K/V are quantised in the epilogue (groups of 64
+  // dims, kvq_bits bits) straight into each row's quantised slab, described by kvq_jobs[row]
+  // (dst, dst_cap, dst_p0); arena is then the arena's bytes and nothing is written in bf16
+  const Kv8Job* kvq_jobs;
+  int kvq_bits;
   // 4-bit affine weights in the native block layout of gemm_q4.cu (launch_q4_rd only)
   const uint8_t* wq;
   unsigned long long* stamp;  // measurement stamp slot (common.cuh), or NULL
@@ -169,6 +176,12 @@ bool launch_attn_decode_tc(const CUtensorMap& tk, const CUtensorMap& tv, const A
 // scales and bf16 biases [cap][head_dim / 64]
 CBT_HD long long kvq_block_bytes(int cap, int head_dim, int bits) {
   return (long long)cap * (head_dim * bits / 8 + head_dim / 16);
+}
+// byte offset of block (layer, K|V, kv head) of the quantised slab or page at byte offset off
+CBT_HD long long kvq_block(long long off, int cap, int layer, int kv, int head, int n_kv_heads,
+                           int head_dim, int bits) {
+  return off + (((long long)layer * 2 + kv) * n_kv_heads + head) *
+                   kvq_block_bytes(cap, head_dim, bits);
 }
 // Positions [t0, t0 + n) of a bf16 slab (or a staging page: a QueryRow base and capacity) to
 // be quantised into the quantised slab or page at byte offset dst (layout capacity dst_cap),

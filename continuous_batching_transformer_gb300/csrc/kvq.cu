@@ -82,13 +82,6 @@ __global__ void k_quantize_kv(const uint16_t* x, int rows, int cols, uint8_t* co
                        scales + grp, biases + grp, lane);
 }
 
-// block (layer, kv, head) of a quantised slab or page at byte offset `off`, capacity `cap`
-CBT_D long long kvq_block(long long off, int cap, int layer, int kv, int head, int n_kv_heads,
-                          int head_dim, int bits) {
-  return off + (((long long)layer * 2 + kv) * n_kv_heads + head) *
-                   kvq_block_bytes(cap, head_dim, bits);
-}
-
 // One warp per (job, position, layer, K|V, kv head, group of 64 dims).  Job j converts positions
 // [t0, t0 + n) of layers [l0, l0 + nl) from its bf16 source into its quantised destination,
 // whose position p sits at local index p - dst_p0.
@@ -212,17 +205,13 @@ __global__ void __launch_bounds__(kAttnThreads)
   S& sm = *reinterpret_cast<S*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;  // fragment row group and thread in group
-  pdl_wait();
-  pdl_launch();
-  if (tid == 0) stamp_begin(a.stamp);
-  const int total = *a.n_items;
+  const int total = *a.n_items;  // step inputs (the work list): readable before the wait
 
   // stage an item: codes of its keys (rows past the row's position zero-filled), their scales
-  // and biases (whole 16-byte chunks up to the last valid key; the rest masked later), Q image
-  auto prefetch = [&](int it, int si) {
-    const AttnItem w = a.items[it];
-    const int n = a.rows[w.b].pos + 1;
-    const int nk = min(kItemKeys, n - w.s0 * kItemKeys);
+  // and biases (whole 16-byte chunks up to the last valid key; the rest masked later) -- and
+  // its Q image (prefetch_q)
+  auto prefetch_codes = [&](const AttnItem& w, int si) {
+    const int nk = min(kItemKeys, w.n - w.s0 * kItemKeys);
     const long long loc = (long long)w.s0 * kItemKeys - w.p0;
     typename S::Stage& st = sm.st[si];
     const uint8_t* kblk = a.arena + kvq_block(w.kbase, w.cap, a.layer, 0, w.g, a.n_kv_heads, HD, BITS);
@@ -247,25 +236,54 @@ __global__ void __launch_bounds__(kAttnThreads)
       uint16_t* dst = which == 0 ? st.ks : which == 1 ? st.kb : which == 2 ? st.vs : st.vb;
       cp_async16(reinterpret_cast<uint8_t*>(dst) + c * 16, blk + (ok ? off : 0), ok ? 16u : 0u);
     }
+  };
+  auto prefetch_q = [&](const AttnItem& w, int si) {
     const uint8_t* qsrc = a.qtile + ((size_t)w.b * a.n_kv_heads + w.g) * (16 * HD * 2);
     for (int i = tid; i < 16 * HD * 2 / 16; i += kAttnThreads)
-      cp_async16(st.q + i * 16, qsrc + i * 16, 16u);
+      cp_async16(sm.st[si].q + i * 16, qsrc + i * 16, 16u);
   };
 
+  // The first item's codes are requested before waiting for the previous kernel when they were
+  // written by earlier steps (the item does not hold the row's new position); its Q image, and
+  // the codes of an item that holds the new position, after it.
   int si = 0;
-  if ((int)blockIdx.x < total) prefetch(blockIdx.x, 0);
+  AttnItem wc{};
+  bool codes_early = false;
+  if ((int)blockIdx.x < total) {
+    wc = a.items[blockIdx.x];
+    if ((wc.s0 + 1) * kItemKeys < wc.n) {
+      prefetch_codes(wc, 0);
+      codes_early = true;
+    }
+  }
+  pdl_wait();
+  pdl_launch();
+  if (tid == 0) stamp_begin(a.stamp);
+  if ((int)blockIdx.x < total) {
+    if (!codes_early) prefetch_codes(wc, 0);
+    prefetch_q(wc, 0);
+  }
   cp_async_commit();
   for (int it = blockIdx.x; it < total; it += gridDim.x, si ^= 1) {
     cp_async_wait_all();
     __syncthreads();  // stage si holds item it; every warp is done with the previous item
-    if (it + (int)gridDim.x < total) prefetch(it + gridDim.x, si ^ 1);
-    cp_async_commit();
+    // the next item's descriptor, requested now and used once this item's scores are done
+    // (its copies then go out without a load round trip on the path)
+    const int itn = it + (int)gridDim.x;
+    AttnItem wn{};
+    if (itn < total) wn = a.items[itn];
     typename S::Stage& st = sm.st[si];
-    const AttnItem w = a.items[it];
-    const int n = a.rows[w.b].pos + 1;
+    const AttnItem w = wc;
+    const int n = w.n;
     const int nk = min(kItemKeys, n - w.s0 * kItemKeys);
     if (w.s1 != w.s0 + 1 || nk <= 0) {  // the work list is built one sub-chunk per item
       if (tid == 0) set_device_error(a.err, CBT_DEV_WORK_ITEM, it);
+      if (itn < total) {
+        prefetch_codes(wn, si ^ 1);
+        prefetch_q(wn, si ^ 1);
+      }
+      cp_async_commit();
+      wc = wn;
       continue;
     }
     // ---- Q fragments (head gq: high parts in A rows gq, remainders in rows gq + 8), built once
@@ -348,6 +366,12 @@ __global__ void __launch_bounds__(kAttnThreads)
           s[nt][j] += sc * (acc[nt][j] + acc[nt][j + 2]) + bi * qsum[gr];
         }
     }
+    if (itn < total) {  // the next item into the other stage (every warp is past its data)
+      prefetch_codes(wn, si ^ 1);
+      prefetch_q(wn, si ^ 1);
+    }
+    cp_async_commit();
+    wc = wn;
     // ---- softmax of head gq over the item's keys
     float mx = -INFINITY;
 #pragma unroll

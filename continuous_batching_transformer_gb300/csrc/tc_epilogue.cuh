@@ -9,16 +9,18 @@
 namespace tcepi {
 
 // Residual values out[tok0 + j][m] of tile row r for an EPI_ADD epilogue, all loads issued
-// before any is used (the epilogue's latency is a chain of global round trips otherwise)
-template <int CNT>
+// before any is used (the epilogue's latency is a chain of global round trips otherwise).
+// EPI_T >= 0: the epilogue fixed at compile time (only its code is generated), else p.epi.
+template <int CNT, int EPI_T = -1>
 __device__ __forceinline__ void load_residual(const TcParams& p, int rb, int r, int tok0,
                                               float* res) {
+  const int epi = EPI_T >= 0 ? EPI_T : p.epi;
   const int m = rb * 128 + r;
 #pragma unroll
   for (int j = 0; j < CNT; ++j) {
     const int t = tok0 + j;
-    res[j] = (p.epi == EPI_ADD && m < p.M && t < p.n_act) ? __ldcg(p.out + (size_t)t * p.ldo + m)
-                                                          : 0.f;
+    res[j] = (epi == EPI_ADD && m < p.M && t < p.n_act) ? __ldcg(p.out + (size_t)t * p.ldo + m)
+                                                        : 0.f;
   }
 }
 
@@ -44,18 +46,110 @@ __device__ __forceinline__ float load_next_gain(const TcParams& p, int rb, int r
   return (p.next_act && m < p.M) ? bf16_to_f32(p.next_gain[m]) : 0.f;
 }
 
+// The new K/V of a quantised-KV engine, quantised where they are produced: tile row r holds dim
+// i of a K or V head for the CNT decode rows (x[j], already rounded to bf16).  Per row j and
+// 64-dim group: L = 2^bits - 1, scale = bf16((max - min) / L), bias = bf16(min), code =
+// clamp(rint((x - bias) / scale), 0, L) with the quotient the correctly rounded double one
+// (q0 = d / s through the group's reciprocal, then one exact-residual correction: the
+// reciprocal is computed once per (row, group) and the division of every element is three
+// double operations instead of one).  The codes, scale and bias go to the row's quantised slab
+// or page (kvq_jobs[j]); nothing is written in bf16.
+template <int CNT>
+__device__ __forceinline__ void kvq_append(const TcParams& p, int rb, int r, const float (&x)[CNT],
+                                           float* swx, const EpiSrc& src) {
+  const int hd = p.head_dim, bits = p.kvq_bits;
+  const int row = rb * 128 + r, head = row / hd, i = row % hd;
+  const bool isv = head >= p.n_heads + p.n_kv_heads;
+  const int g = head - p.n_heads - (isv ? p.n_kv_heads : 0);
+  const int lane = r & 31, wq = r >> 5, grp = r >> 6;  // 64-row groups of the tile
+  const int L = (1 << bits) - 1;
+  float mn[CNT], mx[CNT];
+#pragma unroll
+  for (int j = 0; j < CNT; ++j) mn[j] = mx[j] = x[j];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float a[CNT], b[CNT];
+#pragma unroll
+    for (int j = 0; j < CNT; ++j) {
+      a[j] = __shfl_xor_sync(0xffffffffu, mn[j], o);
+      b[j] = __shfl_xor_sync(0xffffffffu, mx[j], o);
+    }
+#pragma unroll
+    for (int j = 0; j < CNT; ++j) {
+      mn[j] = fminf(mn[j], a[j]);
+      mx[j] = fmaxf(mx[j], b[j]);
+    }
+  }
+  float* wmm = swx;                                   // [4 warps][CNT][min, max]
+  float* gsb = swx + 8 * CNT;                         // [2 groups][CNT][scale, bias]
+  double* ginv = reinterpret_cast<double*>(
+      (reinterpret_cast<uintptr_t>(swx + 12 * CNT) + 7) & ~uintptr_t(7));  // [2 groups][CNT]
+  tc::named_bar_sync(1, 128);  // the exchange buffer is free again
+  if (lane == 0) {
+#pragma unroll
+    for (int j = 0; j < CNT; ++j) {
+      wmm[(wq * CNT + j) * 2] = mn[j];
+      wmm[(wq * CNT + j) * 2 + 1] = mx[j];
+    }
+  }
+  tc::named_bar_sync(1, 128);
+  const int jj = r & 63;  // thread jj of a group prepares row jj's scale, bias and reciprocal
+  if (jj < CNT && jj < p.n_act) {
+    const int w0 = 2 * grp, w1 = 2 * grp + 1;
+    const float gmn = fminf(wmm[(w0 * CNT + jj) * 2], wmm[(w1 * CNT + jj) * 2]);
+    const float gmx = fmaxf(wmm[(w0 * CNT + jj) * 2 + 1], wmm[(w1 * CNT + jj) * 2 + 1]);
+    const uint16_t sb = f32_to_bf16((float)(((double)gmx - (double)gmn) / (double)L));
+    const float sc = bf16_to_f32(sb);
+    gsb[(grp * CNT + jj) * 2] = sc;
+    gsb[(grp * CNT + jj) * 2 + 1] = bf16_to_f32(f32_to_bf16(gmn));
+    ginv[grp * CNT + jj] = sc != 0.f ? 1.0 / (double)sc : 0.0;
+  }
+  tc::named_bar_sync(1, 128);
+  uint8_t* arena8 = reinterpret_cast<uint8_t*>(p.arena);
+  const int ng = hd / 64, gr = i / 64, row_bytes = hd * bits / 8;
+#pragma unroll
+  for (int j = 0; j < CNT; ++j) {
+    if (j >= p.n_act) break;
+    const float sc = gsb[(grp * CNT + j) * 2], bi = gsb[(grp * CNT + j) * 2 + 1];
+    uint32_t code = 0u;
+    if (sc != 0.f) {
+      const double s = sc, d = (double)x[j] - (double)bi, inv = ginv[grp * CNT + j];
+      const double q0 = d * inv;
+      const double q1 = fma(fma(-q0, s, d), inv, q0);  // the correctly rounded d / s
+      const double t = rint(q1);
+      code = t < 0.0 ? 0u : (t > (double)L ? (uint32_t)L : (uint32_t)t);
+    }
+    const Kv8Job jb = p.kvq_jobs[j];
+    const long long loc = (long long)src.rows[j].pos - jb.dst_p0;
+    const long long blk = kvq_block(jb.dst, jb.dst_cap, p.layer, isv ? 1 : 0, g, p.n_kv_heads, hd,
+                                    bits);
+    if (bits == 8) {
+      arena8[blk + loc * row_bytes + i] = (uint8_t)code;
+    } else {  // dims 2k (low nibble) and 2k + 1 are adjacent lanes
+      const uint32_t hi = __shfl_down_sync(0xffffffffu, code, 1);
+      if ((i & 1) == 0) arena8[blk + loc * row_bytes + (i >> 1)] = (uint8_t)(code | (hi << 4));
+    }
+    if ((i & 63) == 0) {
+      uint16_t* sp = reinterpret_cast<uint16_t*>(arena8 + blk + (long long)jb.dst_cap * row_bytes);
+      sp[loc * ng + gr] = f32_to_bf16(sc);
+      sp[(long long)jb.dst_cap * ng + loc * ng + gr] = f32_to_bf16(bi);
+    }
+  }
+}
+
 // Final epilogue of CNT (<= 32) columns (tokens tok0 .. tok0+CNT-1) of tile row r of row
 // block rb.  All 128 epilogue threads call it together.  rinv (when p.ss_in) holds each
 // column's RMSNorm factor; res the residual values from load_residual (EPI_ADD).
-template <int CNT>
+template <int CNT, int EPI_T = -1>
 __device__ __forceinline__ void finish(const TcParams& p, int rb, int r, float* vals, int tok0,
                                        float* swx, const float* rinv, const float* res,
                                        const EpiSrc& src) {
+  const int epi = EPI_T >= 0 ? EPI_T : p.epi;
   if (p.ss_in) {
 #pragma unroll
     for (int j = 0; j < CNT; ++j) vals[j] *= rinv[j];
   }
-  if (p.epi == EPI_QKV) {
+  if (epi == EPI_QKV || epi == EPI_QKVQ) {
     // Row r of the tile is dim i of head `head` of q|k|v (heads are head_dim-aligned in the
     // tile); its RoPE partner is dim i ^ half of the same head, held by tile row r ^ half.
     const int hd = p.head_dim, half = hd >> 1;
@@ -74,6 +168,12 @@ __device__ __forceinline__ void finish(const TcParams& p, int rb, int r, float* 
     tc::named_bar_sync(1, 128);
     const int pr = r ^ half;
     const int G = p.n_heads / p.n_kv_heads;
+    // a tile of K/V heads on a quantised-KV engine (uniform over the tile: the q rows end on a
+    // 256-row boundary) quantises its rows once they are all rotated
+    const bool kvq = epi == EPI_QKVQ && rb * 128 >= p.n_heads * hd;
+    float xq[CNT];
+#pragma unroll
+    for (int j = 0; j < CNT; ++j) xq[j] = 0.f;
 #pragma unroll
     for (int j = 0; j < CNT; ++j) {
       if (j >= p.n_act || row >= p.M) break;
@@ -82,7 +182,9 @@ __device__ __forceinline__ void finish(const TcParams& p, int rb, int r, float* 
         const float w = swx[pr * (CNT + 1) + j];
         v = i < half ? v * cs[j] - w * sn[j] : w * sn[j] + v * cs[j];
       }
-      if (head < p.n_heads) {
+      if (kvq) {
+        xq[j] = bf16_to_f32(f32_to_bf16(v));
+      } else if (head < p.n_heads) {
         // Q operand image of row j, kv head head / G: hi part in tile row head % G, lo part
         // in row 8 + head % G, scaled by 1/sqrt(head_dim)
         uint8_t* tile = p.qtile + ((size_t)j * p.n_kv_heads + head / G) * (16 * hd * 2);
@@ -101,9 +203,10 @@ __device__ __forceinline__ void finish(const TcParams& p, int rb, int r, float* 
                           hd)] = f32_to_bf16(v);
       }
     }
+    if (kvq) kvq_append<CNT>(p, rb, r, xq, swx, src);
     return;
   }
-  if (p.epi != EPI_SWIGLU) {
+  if (epi != EPI_SWIGLU) {
     const int m = rb * 128 + r;
     const float gn = src.has_gn ? src.gn : load_next_gain(p, rb, r);
     float sq[CNT];
@@ -112,7 +215,7 @@ __device__ __forceinline__ void finish(const TcParams& p, int rb, int r, float* 
       const int t = tok0 + j;
       sq[j] = 0.f;
       if (m < p.M && t < p.n_act) {
-        const float v = p.epi == EPI_ADD ? vals[j] + res[j] : vals[j];
+        const float v = epi == EPI_ADD ? vals[j] + res[j] : vals[j];
         p.out[(size_t)t * p.ldo + m] = v;
         sq[j] = v * v;
         if (p.next_act) {  // the next projection's operand x * g, as hi/lo parts
