@@ -348,9 +348,9 @@ def gpu_arm(args, rank: int, world: int):
         step_ms = ms_max / K
         if wl.shape.weight_format == "bf16":
             traffic = measured_traffic("projection")
-        else:  # the 4-bit projections stream their weights once per 8 rows
+        else:  # the 4-bit projections stream their weights once up to 16 rows, then per 16
             traffic = measured_traffic("projection_affine4")
-            traffic = traffic * ((Bsz + 7) // 8) if traffic is not None else None
+            traffic = traffic * ((Bsz + 15) // 16) if traffic is not None else None
         result = {
             "metric": METRIC,
             "value": replicas_throughput(Bsz, K, world, ms_max / 1e3),

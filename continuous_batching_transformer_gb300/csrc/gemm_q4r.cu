@@ -29,9 +29,14 @@
 // SwiGLU, RoPE + K/V append + the attention's Q operand).  C is chosen from the matrix shape
 // and the number of clusters of C CTAs that fit on the GPU at once.
 //
-// Batch rows are taken 8 at a time (gridDim.y passes, each over the same weights): a row's
-// arithmetic -- the k split, the group order, the fold -- depends on the matrix shape alone,
-// so a row's result does not depend on how many rows share the step.
+// Up to 8 batch rows (k_q4_rd): the operand slice of the CTA's whole k-range is staged in
+// shared memory once, with its group sums.  9 to 32 rows (k_q4_rs): 16 rows (32 operand
+// columns) per pass over the weights (gridDim.y passes); the slice no longer fits, so the
+// operand streams superblock by superblock through a ring shared by the four warps of a set,
+// whose 128 threads also add up that superblock's group sums (two barriers per superblock).
+// A row's arithmetic -- the k split, the group order, the fold, the order in which its group
+// sums are added -- depends on the matrix shape alone (MMA columns do not mix), so a row's
+// result does not depend on how many rows share the step, nor on which kernel takes it.
 //
 // The weights are the native block layout of gemm_q4.cu: per (128-row tile, 128-column
 // superblock) [4 chunks][128 rows][16 bytes] of codes (chunk c holds columns 32c .. 32c + 31 of
@@ -180,17 +185,36 @@ __device__ __forceinline__ uint32_t unpack_pair(uint32_t w, int p, uint32_t m, u
   return and_or(w >> (4 * p), m, c);
 }
 
+// sum of 32 consecutive bf16 operand values (four 16-byte pieces) in index order; a group's
+// sum over its 64 columns is (first 32) + (last 32) in both kernels
+__device__ __forceinline__ float sum32(const uint4* v) {
+  float s = 0.f;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 u = v[c];
+    s += bf16_lo(u.x);
+    s += bf16_hi(u.x);
+    s += bf16_lo(u.y);
+    s += bf16_hi(u.y);
+    s += bf16_lo(u.z);
+    s += bf16_hi(u.z);
+    s += bf16_lo(u.w);
+    s += bf16_hi(u.w);
+  }
+  return s;
+}
+
 __device__ __forceinline__ void report_timeout(const TcParams& p, volatile int* abort, int role) {
   *abort = 1;
   if (atomicCAS(p.err, 0, CBT_DEV_TIMEOUT) == 0) p.err[1] = 500 + role;
 }
 
-// The projection's parameters for batch rows [8 pass, 8 pass + 8): every per-row pointer moves
+// The projection's parameters for batch rows [R pass, R pass + R): every per-row pointer moves
 // to the pass's first row; lo-part row offsets are absolute and stay.
-__device__ __forceinline__ TcParams pass_params(const TcParams& p0, int pass) {
+__device__ __forceinline__ TcParams pass_params(const TcParams& p0, int pass, int R) {
   TcParams p = p0;
-  const int r0 = 8 * pass;
-  p.n_act = min(8, p0.n_act - r0);
+  const int r0 = R * pass;
+  p.n_act = min(R, p0.n_act - r0);
   if (p.out) p.out += (size_t)r0 * p.ldo;
   if (p.next_act) p.next_act += (size_t)r0 * p.ldo;
   if (p.act) p.act += (size_t)r0 * p.act_ld;
@@ -204,6 +228,7 @@ __device__ __forceinline__ TcParams pass_params(const TcParams& p0, int pass) {
   return p;
 }
 
+// ---- k_q4_rd: up to 8 rows, the operand slice staged once ------------------------------------
 // One CTA: k-range [sb0, sb1) of tiles cid, cid + NC, ... for batch rows [8 y, 8 y + 8).
 // NB8 n8 blocks of operand columns: NB8 = 1 takes up to 4 rows (hi parts in columns 0-3, lo
 // parts in 4-7), NB8 = 2 up to 8 rows (hi block, then lo block).
@@ -229,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.flags);
 
   const int pass = blockIdx.y;
-  const TcParams p = pass_params(p0, pass);
+  const TcParams p = pass_params(p0, pass, 8);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const int C = q.C;
@@ -344,20 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int idx = threadIdx.x; idx < 2 * nsb * N; idx += kThreads) {
     const int gl = idx / N, n = idx - gl * N;
     const uint4* v = reinterpret_cast<const uint4*>(xs + (size_t)n * pitch + gl * 128);
-    float s = 0.f;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint4 u = v[c];
-      s += bf16_lo(u.x);
-      s += bf16_hi(u.x);
-      s += bf16_lo(u.y);
-      s += bf16_hi(u.y);
-      s += bf16_lo(u.z);
-      s += bf16_hi(u.z);
-      s += bf16_lo(u.w);
-      s += bf16_hi(u.w);
-    }
-    xsum[gl * N + n] = s;
+    xsum[gl * N + n] = sum32(v) + sum32(v + 4);
   }
   __syncthreads();
 
@@ -503,18 +515,372 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (C > 1) csk::cluster_sync();
 }
 
+// ---- k_q4_rs: 9 to 32 rows, 16 per pass, the operand streamed ------------------------------
+constexpr int kRsN = 32;                 // operand columns of a pass: 16 rows, hi and lo parts
+constexpr int kRsH = kRsN / 2;
+constexpr int kRsDepth = 3;              // ring slots per warp (weights) and per set (operand)
+constexpr int kXPitch = 272;             // bytes per operand row of a ring slot (128 bf16 + 16:
+                                         // conflict-free 16-byte fragment loads)
+constexpr int kXSlot = kRsN * kXPitch;   // one operand ring slot: 32 rows of one superblock
+
+struct LayoutRs {
+  size_t ring, xr, xsb, sacc, inbox, swx, rinv, cosv, sinv, rows, ssq, bars, flags, total;
+};
+
+__host__ __device__ inline LayoutRs layout_rs(const Q4rPlan& q) {
+  constexpr int N = kRsN, H = kRsH;
+  LayoutRs L;
+  size_t o = 0;
+  L.ring = o;
+  o += (size_t)kWarps * kRsDepth * kStage;
+  L.xr = o;  // [warp set][slot][N rows][kXPitch]
+  o = align16(o + (size_t)2 * kRsDepth * kXSlot);
+  L.xsb = o;  // [warp set][parity][group][N]: group sums of two consecutive superblocks
+  o = align16(o + (size_t)2 * 2 * 2 * N * 4);
+  L.sacc = o;
+  o = align16(o + (size_t)2 * 2 * 128 * H * 4);  // [tile parity][warp set][128 rows][H]
+  L.inbox = o;
+  o = align16(o + (size_t)q.slots * (q.C > 1 ? q.C - 1 : 0) * 128 * H * 4);
+  L.swx = o;
+  o = align16(o + (size_t)(128 * (H + 1) + 32) * 4);
+  L.rinv = o;
+  o = align16(o + 32 * 4);
+  L.cosv = o;
+  o = align16(o + (size_t)H * 64 * 4);
+  L.sinv = o;
+  o = align16(o + (size_t)H * 64 * 4);
+  L.rows = o;
+  o = align16(o + (size_t)H * sizeof(QueryRow));
+  L.ssq = o;
+  o = align16(o + (size_t)kMaxSsTiles * H * 4);
+  L.bars = o;
+  o = align16(o + kMaxSlots * 8);
+  L.flags = o;
+  o += 16;
+  L.total = o;
+  return L;
+}
+
+// One CTA: k-range [sb0, sb1) of tiles cid, cid + NC, ... for batch rows [16 y, 16 y + 16).
+// The work split, the weight ring, the MMAs and the fold are those of k_q4_rd at four n8
+// blocks (hi parts of the 16 rows, then their lo parts); per superblock the set's threads wait
+// for their copies of this superblock and the next, meet at the set's barrier (both have
+// landed, the slots of the superblock before are free), issue the copies kRsDepth - 1
+// superblocks ahead, add up the next superblock's 64 group sums (a pair of threads per sum;
+// this superblock's were added in the previous iteration), then multiply.
+__global__ void __launch_bounds__(kThreads, 1)
+    k_q4_rs(const __grid_constant__ TcParams p0, const uint16_t* __restrict__ x, int x_lo,
+            const Q4rPlan q) {
+  constexpr int NB8 = 4, N = kRsN, H = kRsH;
+  constexpr int kXPieces = N * 16 / 128;  // 16-byte operand pieces per thread of a set
+  extern __shared__ __align__(16) uint8_t smem[];
+  const LayoutRs L = layout_rs(q);
+  uint8_t* ring = smem + L.ring;
+  float* sacc = reinterpret_cast<float*>(smem + L.sacc);
+  float* inbox = reinterpret_cast<float*>(smem + L.inbox);
+  float* swx = reinterpret_cast<float*>(smem + L.swx);
+  float* rinv = reinterpret_cast<float*>(smem + L.rinv);
+  float* scos = reinterpret_cast<float*>(smem + L.cosv);
+  float* ssin = reinterpret_cast<float*>(smem + L.sinv);
+  QueryRow* srows = reinterpret_cast<QueryRow*>(smem + L.rows);
+  float* ssq = reinterpret_cast<float*>(smem + L.ssq);
+  uint64_t* inbox_full = reinterpret_cast<uint64_t*>(smem + L.bars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.flags);
+
+  const int pass = blockIdx.y;
+  const TcParams p = pass_params(p0, pass, H);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int C = q.C;
+  const uint32_t rank = C > 1 ? csk::cluster_rank() : 0u;
+  const int cid = blockIdx.x / C, NC = gridDim.x / C;
+  const int Tc = cid < p.RB ? (p.RB - cid + NC - 1) / NC : 0;
+  const int SB = p.K / 128;
+  const int sb0 = (int)((long long)rank * SB / C);
+  const int sb1 = (int)((long long)(rank + 1) * SB / C);
+  const int nsb = sb1 - sb0;
+  const int owned = Tc > (int)rank ? (Tc - (int)rank + C - 1) / C : 0;
+  // warp set h takes local superblocks [kbase, kbase + nh) of every tile; warp w of a set holds
+  // tile rows 32 w .. 32 w + 31
+  const int h = warp >> 2, rw = kRows * (warp & 3);
+  const int n0 = (nsb + 1) >> 1;
+  const int nh = h ? nsb - n0 : n0, kbase = h ? n0 : 0;
+  const int nst = Tc * nh;
+  uint8_t* xr = smem + L.xr + (size_t)h * kRsDepth * kXSlot;  // this set's operand ring
+  float* xsb = reinterpret_cast<float*>(smem + L.xsb) + h * 2 * 2 * N;
+  const int bar = 3 + h;  // the set's named barrier
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kMaxSlots; ++s) tc::mbar_init(&inbox_full[s], 1);
+    if (C > 1)
+      for (int s = 0; s < owned; ++s)
+        tc::mbar_expect_tx(&inbox_full[s], (uint32_t)((C - 1) * 128 * H * 4));
+    abort_flag[0] = 0;
+    tc::mbar_fence_init();
+  }
+  // operand rows past the pass's rows are zero in every slot (no copy ever writes them)
+  for (int i = threadIdx.x; i < 2 * kRsDepth * N * (kXPitch / 16); i += kThreads) {
+    const int n = (i / (kXPitch / 16)) % N;
+    if (n % H >= p.n_act)
+      reinterpret_cast<uint4*>(smem + L.xr)[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  __syncthreads();
+  if (C > 1) csk::cluster_sync();
+  pdl_launch();
+
+  // ---- weight blocks: this warp's 32 rows, kRsDepth - 1 blocks ahead (weights only: these may
+  // be requested before the previous kernel has finished)
+  const uint32_t wring = tc::smem_u32(ring) + (uint32_t)(warp * kRsDepth * kStage);
+  const uint8_t* blk0 = p.wq + ((size_t)cid * SB + sb0 + kbase) * kQ4BlockBytes;
+  const uint8_t* pcode = blk0 + (rw + lane) * 16;
+  const uint8_t* pscale = blk0 + kCodeBytes + rw * 8 + (lane & 15) * 16;
+  const size_t tile_skip = ((size_t)NC * SB - nh) * kQ4BlockBytes;  // last block -> next tile
+  const uint64_t pol_w = tc::policy_evict_first();
+  int is_n = 0, is_k = 0;
+  uint32_t is_dst = wring + lane * 16;
+  const uint32_t ring_end = wring + kRsDepth * kStage;
+  auto issue_w = [&]() {
+    if (is_n < nst) {
+      cp_async16s(is_dst, pcode, pol_w);
+      cp_async16s(is_dst + kChunkPitch, pcode + 2048, pol_w);
+      cp_async16s(is_dst + 2 * kChunkPitch, pcode + 2 * 2048, pol_w);
+      cp_async16s(is_dst + 3 * kChunkPitch, pcode + 3 * 2048, pol_w);
+      if (lane < 16) cp_async16s(is_dst + kScaleOff, pscale, pol_w);
+      pcode += kQ4BlockBytes;
+      pscale += kQ4BlockBytes;
+      if (++is_k == nh) {
+        is_k = 0;
+        pcode += tile_skip;
+        pscale += tile_skip;
+      }
+      ++is_n;
+      is_dst += kStage;
+      if (is_dst >= ring_end) is_dst -= kRsDepth * kStage;
+    }
+  };
+  // operand pieces of this thread (the set's 128 threads copy a superblock's N rows x 256
+  // bytes): piece m is row n = (sti + 128 m) / 16, 16-byte column c = (sti + 128 m) % 16
+  const int sti = (warp & 3) * 32 + lane;
+  const uint16_t* xsrc[kXPieces];
+  uint32_t xdst[kXPieces];
+  bool xval[kXPieces];
+#pragma unroll
+  for (int m = 0; m < kXPieces; ++m) {
+    const int pi = sti + 128 * m, n = pi >> 4, c = pi & 15;
+    const int b = n % H;
+    xval[m] = b < p.n_act;
+    const size_t row = n >= H ? (size_t)(x_lo + H * pass + b) : (size_t)(H * pass + b);
+    xsrc[m] = x + row * p.K + (size_t)(sb0 + kbase) * 128 + c * 8;
+    xdst[m] = (uint32_t)(n * kXPitch + c * 16);
+  }
+  const uint32_t xr_u32 = tc::smem_u32(xr);
+  // the operand of iteration io (superblock kbase + io % nh of the k-range) into slot
+  // io % kRsDepth
+  auto issue_x = [&](int io) {
+    if (io < nst) {
+      const size_t col = (size_t)(io % nh) * 128;
+      const uint32_t slot = xr_u32 + (uint32_t)((io % kRsDepth) * kXSlot);
+#pragma unroll
+      for (int m = 0; m < kXPieces; ++m)
+        if (xval[m]) cp_async16_zfill_s(slot + xdst[m], xsrc[m] + col, 16u);
+    }
+  };
+  for (int s = 0; s < kRsDepth - 1; ++s) {
+    issue_w();
+    cp_async_commit();
+  }
+
+  pdl_wait();
+  if (threadIdx.x == 0) stamp_begin(p.stamp);
+  for (int s = 0; s < kRsDepth - 1; ++s) issue_x(s);
+  cp_async_commit();
+  // the folded RMSNorm's per-tile sums of squares: every value requested at once (one per
+  // thread), added up in tile order after the barrier
+  if (p.ss_in)
+    for (int i = threadIdx.x; i < p.ss_tiles * p.n_act; i += kThreads) {
+      const int tt = i / p.n_act, b = i - tt * p.n_act;
+      ssq[i] = __ldcg(p.ss_in + (size_t)tt * p.ss_ld + b);
+    }
+  tcepi::EpiSrc src = tcepi::epi_src_global(p);
+  if (p.epi == EPI_QKV || p.epi == EPI_QKVQ) {
+    const int half = p.head_dim >> 1;
+    for (int i = threadIdx.x; i < p.n_act * half; i += kThreads) {
+      scos[i] = p.cosv[i];
+      ssin[i] = p.sinv[i];
+    }
+    if (threadIdx.x < p.n_act) srows[threadIdx.x] = p.rows[threadIdx.x];
+    src.rows = srows;
+    src.cosv = scos;
+    src.sinv = ssin;
+  }
+  // group sums of iteration io (slot io % kRsDepth) into parity io & 1: this thread pair takes
+  // group gs, column ns; half hs of the 64 values each, then (first 32) + (last 32)
+  const int gs = (sti >> 1) / N, ns = (sti >> 1) % N, hs = sti & 1;
+  auto group_sums = [&](int io) {
+    const uint4* v = reinterpret_cast<const uint4*>(xr + (io % kRsDepth) * kXSlot + ns * kXPitch +
+                                                    gs * 128 + hs * 64);
+    const float sh = sum32(v);
+    const float o = __shfl_xor_sync(0xffffffffu, sh, 1);
+    if (hs == 0) xsb[(io & 1) * 2 * N + gs * N + ns] = sh + o;
+  };
+  cp_async_wait<0>();  // the first superblocks' operand (and the weight blocks before it)
+  __syncthreads();
+  if (p.ss_in && threadIdx.x < p.n_act) {
+    float s = 0.f;
+    for (int tt = 0; tt < p.ss_tiles; ++tt) s += ssq[tt * p.n_act + threadIdx.x];
+    rinv[threadIdx.x] = rsqrtf(s / (float)p.K + p.eps);
+  }
+  if (nst > 0) group_sums(0);  // (read after the first iteration's barrier)
+
+  float y[2][NB8][4];  // [row block u][n8 block][fragment]
+#pragma unroll
+  for (int u = 0; u < 2; ++u)
+#pragma unroll
+    for (int nb = 0; nb < NB8; ++nb)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) y[u][nb][c] = 0.f;
+  // per-lane views: code words of rows 16u + g / 16u + g + 8 (chunk 2G + t/2, half t&1),
+  // scales, operand column g of each n8 block
+  const uint32_t lane_w = (t >> 1) * kChunkPitch + g * 16 + 8 * (t & 1);
+  const uint32_t xlane = xr_u32 + (uint32_t)(g * kXPitch + 32 * t);
+  const uint32_t xsl = tc::smem_u32(xsb) + (uint32_t)(2 * t * 4);
+  uint32_t st = wring;  // the ring slot consumed next
+  const uint32_t km = opaque_const(0x000F000Fu), kc = opaque_const(0x43004300u);
+  int it = 0;  // iteration (tile, superblock) of this warp set
+  for (int j = 0; j < Tc; ++j) {
+    float res[H];
+    const uint32_t owner = (uint32_t)(j % C);
+    if (warp < 4 && rank == owner) {  // epilogue inputs of this tile, requested early
+      const int rb = cid + j * NC;
+      tcepi::load_residual<H>(p, rb, threadIdx.x, 0, res);
+      src.gn = tcepi::load_next_gain(p, rb, threadIdx.x);
+      src.has_gn = true;
+    }
+    for (int k = 0; k < nh; ++k, ++it) {
+      cp_async_wait<0>();            // this thread's copies of iterations it, it + 1 ...
+      tc::named_bar_sync(bar, 128);  // ... and the set's; the slots of it - 1 are free, the
+                                     // sums of it are in
+      issue_w();
+      issue_x(it + kRsDepth - 1);
+      cp_async_commit();
+      if (it + 1 < nst) group_sums(it + 1);
+      const uint32_t xo = (uint32_t)((it % kRsDepth) * kXSlot);
+      const uint32_t xsp = xsl + (uint32_t)((it & 1) * 2 * N * 4);
+      uint2 sv[2][2];                // [u][row g, row g + 8]: (s0, b0), (s1, b1)
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        sv[u][0] = lds64(st + kScaleOff + (16 * u + g) * 8);
+        sv[u][1] = lds64(st + kScaleOff + (16 * u + g + 8) * 8);
+      }
+#pragma unroll
+      for (int G = 0; G < 2; ++G) {
+        // operand fragments of group G (both row blocks use them): column nb * 8 + g, the
+        // sixteen k 64 G + 16 t .. + 15 as bf16 pairs, 8 per MMA pair jp
+        const uint32_t xg = xlane + xo + G * 128;
+        uint4 xv[2][NB8];
+        float2 X[NB8];
+#pragma unroll
+        for (int nb = 0; nb < NB8; ++nb) {
+          xv[0][nb] = lds128(xg + nb * 8 * kXPitch);
+          xv[1][nb] = lds128(xg + nb * 8 * kXPitch + 16);
+          const uint2 Xw = lds64(xsp + (G * N + nb * 8) * 4);
+          X[nb] = make_float2(__uint_as_float(Xw.x), __uint_as_float(Xw.y));
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          // lane (g, t): columns 64 G + 16 t .. + 15 of rows 16u + g and 16u + g + 8
+          const uint32_t wa = st + lane_w + G * 2 * kChunkPitch + u * 256;
+          const uint2 wA = lds64(wa), wB = lds64(wa + 128);
+          float acc[NB8][4];
+#pragma unroll
+          for (int jp = 0; jp < 2; ++jp) {
+            const uint32_t a = jp ? wA.y : wA.x, b = jp ? wB.y : wB.x;
+            const uint32_t A0[4] = {unpack_pair(a, 0, km, kc), unpack_pair(b, 0, km, kc),
+                                    unpack_pair(a, 1, km, kc), unpack_pair(b, 1, km, kc)};
+            const uint32_t A1[4] = {unpack_pair(a, 2, km, kc), unpack_pair(b, 2, km, kc),
+                                    unpack_pair(a, 3, km, kc), unpack_pair(b, 3, km, kc)};
+#pragma unroll
+            for (int nb = 0; nb < NB8; ++nb) {
+              if (jp == 0) mma16816_z(acc[nb], A0, xv[0][nb].x, xv[0][nb].y);
+              else mma16816(acc[nb], A0, xv[jp][nb].x, xv[jp][nb].y);
+              mma16816(acc[nb], A1, xv[jp][nb].z, xv[jp][nb].w);
+            }
+          }
+          const uint32_t swa = G ? sv[u][0].y : sv[u][0].x, swb = G ? sv[u][1].y : sv[u][1].x;
+          const float s_a = bf16_lo(swa), s_b = bf16_lo(swb);
+          const float c_a = fmaf(-128.f, s_a, bf16_hi(swa));
+          const float c_b = fmaf(-128.f, s_b, bf16_hi(swb));
+#pragma unroll
+          for (int nb = 0; nb < NB8; ++nb) {
+            y[u][nb][0] = fmaf(s_a, acc[nb][0], fmaf(c_a, X[nb].x, y[u][nb][0]));
+            y[u][nb][1] = fmaf(s_a, acc[nb][1], fmaf(c_a, X[nb].y, y[u][nb][1]));
+            y[u][nb][2] = fmaf(s_b, acc[nb][2], fmaf(c_b, X[nb].x, y[u][nb][2]));
+            y[u][nb][3] = fmaf(s_b, acc[nb][3], fmaf(c_b, X[nb].y, y[u][nb][3]));
+          }
+        }
+      }
+      st += kStage;
+      if (st >= ring_end) st = wring;
+    }
+
+    // ---- end of tile j: hi + lo parts into the warp set's half of the hand-off buffer
+    float* sa = sacc + (size_t)((j & 1) * 2 + h) * 128 * H;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int r0 = rw + 16 * u + g;
+#pragma unroll
+      for (int nb = 0; nb < NB8 / 2; ++nb) {
+        const float* lo = y[u][nb + NB8 / 2];
+        *reinterpret_cast<float2*>(sa + r0 * H + nb * 8 + 2 * t) =
+            make_float2(y[u][nb][0] + lo[0], y[u][nb][1] + lo[1]);
+        *reinterpret_cast<float2*>(sa + (r0 + 8) * H + nb * 8 + 2 * t) =
+            make_float2(y[u][nb][2] + lo[2], y[u][nb][3] + lo[3]);
+      }
+#pragma unroll
+      for (int nb = 0; nb < NB8; ++nb)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) y[u][nb][c] = 0.f;
+    }
+    tc::named_bar_sync(2, kThreads);
+    if (warp < 4) {
+      // ---- tile row r: both halves, then the cluster's partials, then the epilogue
+      const int r = threadIdx.x;
+      const float* s0 = sacc + (size_t)((j & 1) * 2) * 128 * H + r * H;
+      const float* s1 = s0 + 128 * H;
+      float vals[H];
+#pragma unroll
+      for (int b = 0; b < H; ++b) vals[b] = s0[b] + s1[b];
+      const int rb = cid + j * NC;
+      float sum[H];
+      const int got = csk::combine_partials<H>(vals, sum, inbox, inbox_full, j / C, rank, owner,
+                                               C, r, abort_flag);
+      if (got < 0) report_timeout(p, abort_flag, 1);
+      tc::named_bar_sync(1, 128);  // the same decision in all 128 threads
+      if (got > 0 && *abort_flag == 0) tcepi::finish<H>(p, rb, r, sum, 0, swx, rinv, res, src);
+    }
+  }
+  cp_async_wait<0>();  // (only empty groups remain: every issued block was consumed)
+  if (threadIdx.x == 0) stamp_end(p.stamp);
+  if (C > 1 && threadIdx.x == 0)
+    for (int s = 0; s < owned; ++s) tc::mbar_wait(&inbox_full[s], 0);
+  if (C > 1) csk::cluster_sync();
+}
+
 template <int NB8>
 size_t q4r_smem(const Q4rPlan& q) {
   return layout(8 * NB8, q).total;
 }
 
-template <int NB8>
-int q4r_active_clusters(int C, size_t smem) {
-  static std::map<std::pair<int, size_t>, int> cache;
-  const auto key = std::make_pair(C, smem);
+size_t q4rs_smem(const Q4rPlan& q) { return layout_rs(q).total; }
+
+using Q4Kernel = void (*)(TcParams, const uint16_t*, int, Q4rPlan);
+
+// most clusters of C CTAs of kern (each with `smem` bytes) resident at once, cached
+int q4_active_clusters(Q4Kernel kern, int C, size_t smem) {
+  static std::map<std::tuple<const void*, int, size_t>, int> cache;
+  const auto key = std::make_tuple(reinterpret_cast<const void*>(kern), C, smem);
   auto it = cache.find(key);
   if (it != cache.end()) return it->second;
-  auto kern = k_q4_rd<NB8>;
   int n = 0;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
       cudaSuccess) {
@@ -535,11 +901,20 @@ int q4r_active_clusters(int C, size_t smem) {
   return cache[key] = n;
 }
 
+// clusters of the plan's C that both kernels can keep resident (0: a kernel does not fit)
+int q4_plan_fit(const Q4rPlan& q) {
+  if (q.slots > kMaxSlots || q4r_smem<2>(q) > (size_t)kSmemBudget ||
+      q4rs_smem(q) > (size_t)kSmemBudget)
+    return 0;
+  return std::min(q4_active_clusters(k_q4_rd<2>, q.C, q4r_smem<2>(q)),
+                  q4_active_clusters(k_q4_rs, q.C, q4rs_smem(q)));
+}
+
 // The split of the k-range (C) follows from the matrix shape alone -- so a row's arithmetic
 // does not depend on the number of rows -- by the cost of the busiest CTA: superblocks it
 // streams, plus a little for each cluster hand-off.  How many clusters of C CTAs run at once is
 // asked of the occupancy calculator (clusters are placed within GPCs, so fewer than
-// num_sms / C may fit), at the widest operand's shared memory.
+// num_sms / C may fit), for both kernels at their widest operand.
 bool q4r_split(int RB, int SB, int num_sms, Q4rPlan* out) {
   static const int kSizes[] = {1, 2, 3, 4, 6, 8};
   double best = 1e30;
@@ -552,15 +927,12 @@ bool q4r_split(int RB, int SB, int num_sms, Q4rPlan* out) {
     if (q.sb_max > kMaxSbPerRank) continue;
     q.NC = std::min(RB, num_sms / C);
     q.slots = C > 1 ? ((RB + q.NC - 1) / q.NC + C - 1) / C : 0;
-    if (q.slots > kMaxSlots || q4r_smem<2>(q) > (size_t)kSmemBudget) continue;
-    const int fit = q4r_active_clusters<2>(C, q4r_smem<2>(q));
+    const int fit = q4_plan_fit(q);
     if (fit <= 0) continue;
     if (fit < q.NC) {
       q.NC = fit;
       q.slots = C > 1 ? ((RB + q.NC - 1) / q.NC + C - 1) / C : 0;
-      if (q.slots > kMaxSlots || q4r_smem<2>(q) > (size_t)kSmemBudget ||
-          q4r_active_clusters<2>(C, q4r_smem<2>(q)) < q.NC)
-        continue;
+      if (q4_plan_fit(q) < q.NC) continue;
     }
     const int tmax = (RB + q.NC - 1) / q.NC;
     const double cost = (double)tmax * q.sb_max + (C > 1 ? 1.0 : 0.0) + 0.01 * C;
@@ -574,12 +946,9 @@ bool q4r_split(int RB, int SB, int num_sms, Q4rPlan* out) {
   return true;
 }
 
-template <int NB8>
-bool q4r_launch(const TcParams& p, const uint16_t* x, int x_lo, const Q4rPlan& q, int passes,
-                cudaStream_t s) {
-  // the plan's clusters fit at the widest operand's shared memory, so at this one too
-  const size_t smem = q4r_smem<NB8>(q);
-  auto kern = k_q4_rd<NB8>;
+bool q4_launch(Q4Kernel kern, size_t smem, const TcParams& p, const uint16_t* x, int x_lo,
+               const Q4rPlan& q, int passes, cudaStream_t s) {
+  // the plan's clusters fit at both kernels' widest operand, so at this one too
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return false;
@@ -621,7 +990,7 @@ bool launch_q4_rd(TcParams p, const uint16_t* x, int x_lo, int num_sms, cudaStre
     if (!q4r_split(p.RB, p.K / 128, num_sms, &q)) return false;
     plans[key] = q;
   }
-  const int passes = (p.n_act + 7) / 8;
-  return p.n_act <= 4 ? q4r_launch<1>(p, x, x_lo, q, passes, s)
-                      : q4r_launch<2>(p, x, x_lo, q, passes, s);
+  if (p.n_act <= 4) return q4_launch(k_q4_rd<1>, q4r_smem<1>(q), p, x, x_lo, q, 1, s);
+  if (p.n_act <= 8) return q4_launch(k_q4_rd<2>, q4r_smem<2>(q), p, x, x_lo, q, 1, s);
+  return q4_launch(k_q4_rs, q4rs_smem(q), p, x, x_lo, q, (p.n_act + kRsH - 1) / kRsH, s);
 }

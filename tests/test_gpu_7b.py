@@ -64,10 +64,16 @@ def test_7b_bf16_b32_long_contexts():
     run_sampled(LONG_7B_B32, [int(np.argmax(ctx)), int(np.argmin(ctx))], TOL["bf16"])
 
 
-def test_7b_affine4_b16_two_passes():
-    """4-bit weights at B = 16: the projections take the rows in two passes of 8 over the
-    same weights; rows from both passes."""
+def test_7b_affine4_b16_one_pass():
+    """4-bit weights at B = 16: the projections take all 16 rows (32 operand columns) in one
+    pass over the weights; rows from both halves of the operand."""
     run_sampled(decode_7b_fixed(16, 2048, "affine4"), [0, 9, 15], TOL["affine4"])
+
+
+def test_7b_affine4_b32_two_passes():
+    """4-bit weights at B = 32: two passes of 16 rows over the same weights; rows from both
+    passes."""
+    run_sampled(decode_7b_fixed(32, 2048, "affine4"), [0, 17, 31], TOL["affine4"])
 
 
 def test_7b_bf16_b8_paged_kv():
