@@ -352,8 +352,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       float sum[H];
       const int got = csk::combine_partials<H>(vals, sum, sm.inbox, sm.inbox_full, slot, rank,
                                                owner, C, r, abort_flag, lim);
-      if (got < 0) {
-        report_timeout(p, abort_flag, 5);
+      // one decision for the 128 threads (the epilogue synchronises them)
+      if (tc::named_bar_any(1, 128, got < 0)) {
+        if (got < 0) report_timeout(p, abort_flag, 5);
         break;
       }
       if (got > 0) finish<H, EPI>(p, rb, r, sum, 0, sm.swx, sm.rinv, res, src);

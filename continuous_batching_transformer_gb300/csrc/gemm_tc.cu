@@ -258,7 +258,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         b ^= 1;
         if (b == 0) bphase ^= 1;
       }
-      if (!ok) break;
+      if (tc::named_bar_any(1, 128, !ok)) {  // one decision for the 128 threads
+        ok = false;
+        break;
+      }
       // one copy of the (large) epilogue code: each 16-column chunk is moved out of the sums
       // by constant indices (so they stay in registers) and finished in a loop that is not
       // unrolled -- four inlined copies crowd the issuing warps out of the instruction cache

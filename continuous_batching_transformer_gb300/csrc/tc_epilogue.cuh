@@ -138,139 +138,142 @@ __device__ __forceinline__ void kvq_append(const TcParams& p, int rb, int r, con
 }
 
 // Final epilogue of CNT (<= 32) columns (tokens tok0 .. tok0+CNT-1) of tile row r of row
-// block rb.  All 128 epilogue threads call it together.  rinv (when p.ss_in) holds each
-// column's RMSNorm factor; res the residual values from load_residual (EPI_ADD).
+// block rb.  All 128 epilogue threads call it together (it synchronises them on named barrier
+// 1).  rinv (when p.ss_in) holds each column's RMSNorm factor; res the residual values from
+// load_residual (EPI_ADD).  The tile's values are staged in swx ([row][CNT + 1]) and every
+// per-column step below is a rolled loop over them: unrolled over 32 columns, the three store
+// paths of a launch grow past the instruction cache and the epilogue waits on instruction
+// fetches.
 template <int CNT, int EPI_T = -1>
 __device__ __forceinline__ void finish(const TcParams& p, int rb, int r, float* vals, int tok0,
                                        float* swx, const float* rinv, const float* res,
                                        const EpiSrc& src) {
   const int epi = EPI_T >= 0 ? EPI_T : p.epi;
+  constexpr int LD = CNT + 1;  // staged row pitch: a column's 32 rows sit in 32 banks
   if (p.ss_in) {
 #pragma unroll
     for (int j = 0; j < CNT; ++j) vals[j] *= rinv[j];
   }
+  const int n = min(CNT, p.n_act - tok0);  // columns that are tokens
+  tc::named_bar_sync(1, 128);              // swx is free
   if (epi == EPI_QKV || epi == EPI_QKVQ) {
     // Row r of the tile is dim i of head `head` of q|k|v (heads are head_dim-aligned in the
     // tile); its RoPE partner is dim i ^ half of the same head, held by tile row r ^ half.
     const int hd = p.head_dim, half = hd >> 1;
     const int row = rb * 128 + r, head = row / hd, i = row % hd;
     const bool rope = head < p.n_heads + p.n_kv_heads;
-    float cs[CNT], sn[CNT];
 #pragma unroll
-    for (int j = 0; j < CNT; ++j) {
-      const bool ok = rope && j < p.n_act;
-      cs[j] = ok ? src.cosv[j * half + (i & (half - 1))] : 1.f;
-      sn[j] = ok ? src.sinv[j * half + (i & (half - 1))] : 0.f;
-    }
+    for (int j = 0; j < CNT; ++j) swx[r * LD + j] = vals[j];
     tc::named_bar_sync(1, 128);
-#pragma unroll
-    for (int j = 0; j < CNT; ++j) swx[r * (CNT + 1) + j] = vals[j];
-    tc::named_bar_sync(1, 128);
-    const int pr = r ^ half;
+    const int pr = r ^ half, ci = i & (half - 1);
     const int G = p.n_heads / p.n_kv_heads;
-    // a tile of K/V heads on a quantised-KV engine (uniform over the tile: the q rows end on a
-    // 256-row boundary) quantises its rows once they are all rotated
-    const bool kvq = epi == EPI_QKVQ && rb * 128 >= p.n_heads * hd;
-    float xq[CNT];
-#pragma unroll
-    for (int j = 0; j < CNT; ++j) xq[j] = 0.f;
-#pragma unroll
-    for (int j = 0; j < CNT; ++j) {
-      if (j >= p.n_act || row >= p.M) break;
-      float v = vals[j];
-      if (rope) {  // q and k turn by pos * theta^(-2(i%half)/hd)
-        const float w = swx[pr * (CNT + 1) + j];
-        v = i < half ? v * cs[j] - w * sn[j] : w * sn[j] + v * cs[j];
+    // q and k turn by pos * theta^(-2(i%half)/hd)
+    auto rotated = [&](int j) {
+      float v = swx[r * LD + j];
+      if (rope) {
+        const float w = swx[pr * LD + j];
+        const float c = src.cosv[j * half + ci], sn = src.sinv[j * half + ci];
+        v = i < half ? v * c - w * sn : w * sn + v * c;
       }
-      if (kvq) {
-        xq[j] = bf16_to_f32(f32_to_bf16(v));
-      } else if (head < p.n_heads) {
-        // Q operand image of row j, kv head head / G: hi part in tile row head % G, lo part
-        // in row 8 + head % G, scaled by 1/sqrt(head_dim)
-        uint8_t* tile = p.qtile + ((size_t)j * p.n_kv_heads + head / G) * (16 * hd * 2);
-        const float qv = v * rsqrtf((float)hd);
+      return v;
+    };
+    if (epi == EPI_QKVQ && rb * 128 >= p.n_heads * hd) {
+      // a tile of K/V heads on a quantised-KV engine (uniform over the tile: the q rows end on
+      // a 256-row boundary) quantises its rows once they are all rotated
+      float xq[CNT];
+#pragma unroll
+      for (int j = 0; j < CNT; ++j) xq[j] = (j < n && row < p.M) ? bf16_to_f32(f32_to_bf16(rotated(j))) : 0.f;
+      kvq_append<CNT>(p, rb, r, xq, swx, src);
+      return;
+    }
+    if (row >= p.M) return;
+    if (head < p.n_heads) {
+      // Q operand image of row j, kv head head / G: hi part in tile row head % G, lo part in
+      // row 8 + head % G, scaled by 1/sqrt(head_dim)
+      const size_t img = (size_t)16 * hd * 2;
+      uint8_t* tile = p.qtile + (size_t)(head / G) * img;
+      const uint32_t ohi = sw128_offset(head % G, i, 2048), olo = sw128_offset(8 + head % G, i, 2048);
+      const float qs = rsqrtf((float)hd);
+#pragma unroll 2
+      for (int j = 0; j < n; ++j) {
+        const float qv = rotated(j) * qs;
         const uint16_t hi = f32_to_bf16(qv);
-        *reinterpret_cast<uint16_t*>(tile + sw128_offset(head % G, i, 2048)) = hi;
-        *reinterpret_cast<uint16_t*>(tile + sw128_offset(8 + head % G, i, 2048)) =
-            f32_to_bf16(qv - bf16_to_f32(hi));
-      } else {
+        uint8_t* t = tile + (size_t)j * p.n_kv_heads * img;
+        *reinterpret_cast<uint16_t*>(t + ohi) = hi;
+        *reinterpret_cast<uint16_t*>(t + olo) = f32_to_bf16(qv - bf16_to_f32(hi));
+      }
+    } else if (rope) {
+#pragma unroll 2
+      for (int j = 0; j < n; ++j) {
         const QueryRow qr = src.rows[j];
-        if (head < p.n_heads + p.n_kv_heads)
-          p.arena[k_index(qr, p.layer, head - p.n_heads, qr.pos, i, p.n_kv_heads, hd)] =
-              f32_to_bf16(v);
-        else
-          p.arena[v_index(qr, p.layer, head - p.n_heads - p.n_kv_heads, qr.pos, i, p.n_kv_heads,
-                          hd)] = f32_to_bf16(v);
+        p.arena[k_index(qr, p.layer, head - p.n_heads, qr.pos, i, p.n_kv_heads, hd)] =
+            f32_to_bf16(rotated(j));
+      }
+    } else {
+#pragma unroll 2
+      for (int j = 0; j < n; ++j) {
+        const QueryRow qr = src.rows[j];
+        p.arena[v_index(qr, p.layer, head - p.n_heads - p.n_kv_heads, qr.pos, i, p.n_kv_heads,
+                        hd)] = f32_to_bf16(swx[r * LD + j]);
       }
     }
-    if (kvq) kvq_append<CNT>(p, rb, r, xq, swx, src);
     return;
   }
   if (epi != EPI_SWIGLU) {
     const int m = rb * 128 + r;
     const float gn = src.has_gn ? src.gn : load_next_gain(p, rb, r);
-    float sq[CNT];
 #pragma unroll
-    for (int j = 0; j < CNT; ++j) {
-      const int t = tok0 + j;
-      sq[j] = 0.f;
-      if (m < p.M && t < p.n_act) {
-        const float v = epi == EPI_ADD ? vals[j] + res[j] : vals[j];
-        p.out[(size_t)t * p.ldo + m] = v;
-        sq[j] = v * v;
+    for (int j = 0; j < CNT; ++j)
+      swx[r * LD + j] = m < p.M ? (epi == EPI_ADD ? vals[j] + res[j] : vals[j]) : 0.f;
+    if (m < p.M) {
+#pragma unroll 2
+      for (int j = 0; j < n; ++j) {
+        const size_t t = (size_t)(tok0 + j);
+        const float v = swx[r * LD + j];
+        p.out[t * p.ldo + m] = v;
         if (p.next_act) {  // the next projection's operand x * g, as hi/lo parts
           const float a = v * gn;
           const uint16_t hi = f32_to_bf16(a);
-          p.next_act[(size_t)t * p.ldo + m] = hi;
-          if (p.next_lo)
-            p.next_act[(size_t)(p.next_lo + t) * p.ldo + m] = f32_to_bf16(a - bf16_to_f32(hi));
+          p.next_act[t * p.ldo + m] = hi;
+          if (p.next_lo) p.next_act[(p.next_lo + t) * p.ldo + m] = f32_to_bf16(a - bf16_to_f32(hi));
         }
       }
     }
     if (p.ss_out) {
-      // sums of squares of the updated rows over this tile's 128 rows, for the next RMSNorm;
-      // the CNT warp reductions interleaved level by level, so their shuffles overlap
-      const int w = r >> 5, lane = r & 31;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        float t[CNT];
-#pragma unroll
-        for (int j = 0; j < CNT; ++j) t[j] = __shfl_xor_sync(0xffffffffu, sq[j], o);
-#pragma unroll
-        for (int j = 0; j < CNT; ++j) sq[j] += t[j];
-      }
-      if (lane == 0) {
-#pragma unroll
-        for (int j = 0; j < CNT; ++j) swx[w * 32 + j] = sq[j];
-      }
+      // sums of squares of the updated rows over this tile's 128 rows, for the next RMSNorm:
+      // column j = r / 4; thread w = r % 4 adds rows 32 w .. 32 w + 31 (from row 32 w + w,
+      // wrapping, so the four threads of a column read four banks), then (w0 + w1) + (w2 + w3)
       tc::named_bar_sync(1, 128);
-      if (r < CNT && tok0 + r < p.n_act)
-        p.ss_out[(size_t)rb * p.ss_ld + tok0 + r] = swx[r] + swx[32 + r] + swx[64 + r] + swx[96 + r];
-      tc::named_bar_sync(1, 128);
+      const int j = r >> 2, w = r & 3;
+      float sq = 0.f;
+      if (j < n) {
+#pragma unroll 8
+        for (int k = 0; k < 32; ++k) {
+          const float v = swx[(32 * w + ((k + w) & 31)) * LD + j];
+          sq += v * v;
+        }
+      }
+      sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+      sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+      if (w == 0 && j < n) p.ss_out[(size_t)rb * p.ss_ld + tok0 + j] = sq;
     }
     return;
   }
-  // SwiGLU: tile rows 0..63 are gate rows, 64..127 the up rows of the same 64 features
-  tc::named_bar_sync(1, 128);
-  if (r >= 64) {
+  // SwiGLU: tile rows 0..63 are gate rows, 64..127 the up rows of the same 64 features; two
+  // threads per feature take alternate columns
 #pragma unroll
-    for (int j = 0; j < CNT; ++j) swx[(r - 64) * (CNT + 1) + j] = vals[j];
-  }
+  for (int j = 0; j < CNT; ++j) swx[r * LD + j] = vals[j];
   tc::named_bar_sync(1, 128);
-  if (r < 64) {
-    const int f = rb * 64 + r;
-    if (f < p.F) {
-#pragma unroll
-      for (int j = 0; j < CNT; ++j) {
-        const int t = tok0 + j;
-        if (t < p.n_act) {
-          const float g = vals[j], u = swx[r * (CNT + 1) + j];
-          const float a = g / (1.f + expf(-g)) * u;
-          const uint16_t hi = f32_to_bf16(a);
-          p.act[(size_t)t * p.act_ld + f] = hi;
-          if (p.act_lo) p.act[(size_t)(p.act_lo + t) * p.act_ld + f] = f32_to_bf16(a - bf16_to_f32(hi));
-        }
-      }
+  const int fr = r & 63, f = rb * 64 + fr;
+  if (f < p.F) {
+#pragma unroll 2
+    for (int j = r >> 6; j < n; j += 2) {
+      const size_t t = (size_t)(tok0 + j);
+      const float g = swx[fr * LD + j], u = swx[(64 + fr) * LD + j];
+      const float a = g / (1.f + expf(-g)) * u;
+      const uint16_t hi = f32_to_bf16(a);
+      p.act[t * p.act_ld + f] = hi;
+      if (p.act_lo) p.act[(p.act_lo + t) * p.act_ld + f] = f32_to_bf16(a - bf16_to_f32(hi));
     }
   }
 }
