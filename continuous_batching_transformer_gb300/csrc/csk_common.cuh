@@ -1,7 +1,7 @@
 // csk_common.cuh -- pieces shared by the cluster split-K decode projections (bf16 weights in
 // gemm_csk.cu, 4-bit affine weights in gemm_q4.cu): cluster rank and distributed-shared-memory
-// addressing, the cluster barrier, st.async into a peer's inbox, bounded mbarrier waits, and the
-// hand-off of a tile's partial sums to its owner.
+// addressing, the cluster barrier, st.async into a peer's inbox, bounded mbarrier waits, the
+// hand-off of a tile's partial sums to its owner and their reduce-scatter over the cluster.
 #pragma once
 #include "tc_common.cuh"
 
@@ -100,6 +100,71 @@ __device__ __forceinline__ int combine_partials(const float (&vals)[H], float (&
   for (int c = 0; c < H / 4; ++c)
     st_async_f4(dst + 16 * c, vals[4 * c], vals[4 * c + 1], vals[4 * c + 2], vals[4 * c + 3], bar);
   return 0;
+}
+
+// Tokens [t0, t1) of a tile's H columns that rank `rank` of a C-CTA cluster finishes when the
+// tile's partial sums are reduce-scattered over the cluster: chunks of a multiple of 4 columns
+// (one st.async of 16 bytes each), possibly none for the last ranks.
+__host__ __device__ __forceinline__ int rs_chunk(int H, int C) { return 4 * ((H + 4 * C - 1) / (4 * C)); }
+
+// Reduce-scatter of one tile's partial sums over the C CTAs of a cluster: each CTA sends every
+// peer that peer's columns of its `vals` (row r of the tile) into the peer's inbox for tile
+// `tile` (sender index skipping the receiver), then waits for the C - 1 partials of its own
+// columns [t0, t1) and adds all C in rank order -- the fixed order of a single owner -- into
+// sum[t0 .. t1).  Returns 1 when it holds columns to finish, 0 when it has none, -1 if the wait
+// timed out.  The inbox holds 128 x chunk floats per (tile, sender).
+template <int H>
+__device__ __forceinline__ int reduce_scatter(const float (&vals)[H], float (&sum)[H],
+                                              float* inbox, uint64_t* inbox_full, int tile,
+                                              uint32_t rank, int C, int r,
+                                              volatile int* abort_flag,
+                                              uint32_t limit = tc::kSpinLimit) {
+  const int chunk = rs_chunk(H, C);
+  for (int k = 0; k < C; ++k) {
+    if (k == (int)rank) continue;
+    const int k0 = min(H, k * chunk), k1 = min(H, k0 + chunk);
+    if (k1 <= k0) continue;
+    const int from = (int)rank - ((int)rank > k);
+    const uint32_t dst = peer_addr(
+        tc::smem_u32(inbox + ((size_t)(tile * (C - 1) + from) * 128 + r) * chunk), (uint32_t)k);
+    const uint32_t bar = peer_addr(tc::smem_u32(&inbox_full[tile]), (uint32_t)k);
+#pragma unroll
+    for (int c = 0; c < H / 4; ++c)
+      if (4 * c >= k0 && 4 * c < k1)
+        st_async_f4(dst + 4 * (4 * c - k0), vals[4 * c], vals[4 * c + 1], vals[4 * c + 2],
+                    vals[4 * c + 3], bar);
+  }
+  const int t0 = min(H, (int)rank * chunk), t1 = min(H, t0 + chunk);
+  if (t1 <= t0) return 0;
+  if (C == 1) {
+#pragma unroll
+    for (int n = 0; n < H; ++n) sum[n] = vals[n];
+    return 1;
+  }
+#pragma unroll
+  for (int n = 0; n < H; ++n) sum[n] = 0.f;
+  if (!wait_or_abort(&inbox_full[tile], 0, abort_flag, limit)) return -1;
+  for (int src = 0; src < C; ++src) {
+    if (src == (int)rank) {
+#pragma unroll
+      for (int n = 0; n < H; ++n)
+        if (n >= t0 && n < t1) sum[n] += vals[n];
+    } else {
+      const int from = src - (src > (int)rank);
+      const float4* in = reinterpret_cast<const float4*>(
+          inbox + ((size_t)(tile * (C - 1) + from) * 128 + r) * chunk);
+#pragma unroll
+      for (int c = 0; c < H / 4; ++c)
+        if (4 * c >= t0 && 4 * c < t1) {
+          const float4 v = in[(4 * c - t0) / 4];
+          sum[4 * c] += v.x;
+          sum[4 * c + 1] += v.y;
+          sum[4 * c + 2] += v.z;
+          sum[4 * c + 3] += v.w;
+        }
+    }
+  }
+  return 1;
 }
 
 }  // namespace csk

@@ -6,15 +6,18 @@
 // dimension has to be split too, and the partial sums of a tile meet somewhere.  Through global
 // memory that hand-off is slow on a streaming SM: a store, or any release fence, waits behind
 // the ~128 KB of weight tiles the SM keeps in flight (microseconds).  Here the CTAs that split a
-// tile form a thread-block cluster and hand their partial sums to the tile's owner through
-// distributed shared memory: each sender writes its 128 rows x N/2 fp32 sums into the owner's
-// inbox with st.async, which signals the owner's mbarrier with the byte count; the owner adds
-// the partials in rank order (a fixed order, so results do not depend on timing) and runs the
-// epilogue.  No partial sum touches global memory and no fence is executed.
+// tile form a thread-block cluster and reduce-scatter their partial sums through distributed
+// shared memory: the tile's N/2 output columns (tokens) are cut into one chunk per rank, each
+// CTA writes every peer's columns of its 128-row partial sums into that peer's inbox with
+// st.async (which signals the peer's mbarrier with the byte count), and each CTA adds the C
+// partials of its own columns in rank order (a fixed order, so results do not depend on timing
+// or on which CTA adds them) and runs the epilogue for those columns.  No partial sum touches
+// global memory, no fence is executed, and the combine and epilogue are spread over the
+// cluster instead of falling on one CTA per tile.
 //
 // Layout of the work: tile t of the matrix belongs to cluster t % NC (clusters take tiles
 // cid, cid + NC, ...), rank r of the cluster streams k-blocks [r*KS/C, (r+1)*KS/C) of each of
-// its cluster's tiles, and tile j of a cluster (in that order) is owned by rank j % C.  Per CTA
+// its cluster's tiles and finishes columns [r*chunk, (r+1)*chunk) of each.  Per CTA
 // the pipeline: a TMA producer warp for the weights (which stream from the kernel's start, before
 // the previous kernel finishes), a TMA producer warp for the operand tiles (after it), two MMA
 // warps (swap-AB: 128 weight rows x N operand rows, bf16 hi/lo operand parts, fp32
@@ -38,7 +41,7 @@ using tcepi::load_residual;
 constexpr int kThreads = 256;
 constexpr int kABytes = 128 * 128;  // 128 rows x 64 bf16
 constexpr int kMaxStages = 8;
-constexpr int kMaxSlots = 4;        // tiles one CTA owns in a launch
+constexpr int kMaxSlots = 16;       // tiles of one cluster in a launch (an inbox barrier each)
 constexpr int kSmemBudget = 227 * 1024;
 // One thread issues a tcgen05.mma about every 60 ns whatever its shape, so at N = 16..64 one
 // issuer caps an SM near 65 GB/s of weights (8 MMAs a 32 KB stage); two issuers, each taking
@@ -65,10 +68,10 @@ struct Smem {
   volatile int* sflag;
 };
 
-// inbox of a CTA: per owned tile, the partial sums of the C - 1 other ranks
+// inbox of a CTA: per tile of its cluster, the C - 1 other ranks' partial sums of its columns
 template <int BN>
-__host__ __device__ constexpr size_t inbox_floats(int C, int slots) {
-  return (size_t)slots * (C - 1) * 128 * (BN / 2);
+__host__ __device__ inline size_t inbox_floats(int C, int slots) {
+  return C > 1 ? (size_t)slots * (C - 1) * 128 * csk::rs_chunk(BN / 2, C) : 0;
 }
 
 // shared copies of the RoPE tables: BN/2 rows x up to 64 pairs, cos and sin
@@ -121,7 +124,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(kCskBlocks == kIssuers, "one 64-column block of a stage per issuer");
   constexpr uint32_t kTmemCols = 2 * kIssuers * kAcc * BN < 32 ? 32 : 2 * kIssuers * kAcc * BN;
   constexpr uint32_t kIdesc = tc::idesc_bf16(128, BN);
-  constexpr uint32_t kPartBytes = 128 * H * 4;  // one CTA's partial sums of one tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -139,7 +141,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int SB = p.KS / NK;
   const int sb0 = (int)((long long)rank * SB / C);
   const int sb1 = (int)((long long)(rank + 1) * SB / C);
-  const int owned = Tc > (int)rank ? (Tc - (int)rank + C - 1) / C : 0;
+  // this rank's columns of every tile (reduce-scatter), none for the last ranks of a wide split
+  const int t0 = min(H, (int)rank * csk::rs_chunk(H, C)), t1 = min(H, t0 + csk::rs_chunk(H, C));
+  const int owned = t1 > t0 ? Tc : 0;  // tiles whose inbox this CTA waits for
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -152,9 +156,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::mbar_init(sm.done, kIssuers);
     for (int s = 0; s < kMaxSlots; ++s) tc::mbar_init(&sm.inbox_full[s], 1);
-    // each tile this CTA owns receives the partial sums of the C - 1 other ranks
+    // each tile's inbox receives the C - 1 other ranks' partial sums of this CTA's columns
     if (C > 1)
-      for (int s = 0; s < owned; ++s) tc::mbar_expect_tx(&sm.inbox_full[s], (C - 1) * kPartBytes);
+      for (int s = 0; s < owned; ++s)
+        tc::mbar_expect_tx(&sm.inbox_full[s], (uint32_t)((C - 1) * 128 * (t1 - t0) * 4));
     sm.sflag[0] = 0;
     sm.sflag[1] = 0;
     tc::mbar_fence_init();
@@ -311,12 +316,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     for (int j = 0; j < Tc; ++j) {
       const int rb = cid + j * NC;
-      const uint32_t owner = (uint32_t)(j % C);
-      const int slot = j / C;
-      // the owner's global inputs of this tile, requested before its accumulator is ready
+      // the global inputs of this CTA's columns of the tile, requested before its accumulator
+      // is ready
       float res[H];
-      if (rank == owner) {
-        load_residual<H, EPI>(p, rb, r, 0, res);
+      if (owned) {
+        load_residual<H, EPI>(p, rb, r, 0, res, t0, t1);
         src.gn = tcepi::load_next_gain(p, rb, r);
         src.has_gn = true;
       }
@@ -350,16 +354,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc_phase ^= 1;
       }
       float sum[H];
-      const int got = csk::combine_partials<H>(vals, sum, sm.inbox, sm.inbox_full, slot, rank,
-                                               owner, C, r, abort_flag, lim);
+      const int got = csk::reduce_scatter<H>(vals, sum, sm.inbox, sm.inbox_full, j, rank, C, r,
+                                             abort_flag, lim);
       // one decision for the 128 threads (the epilogue synchronises them)
       if (tc::named_bar_any(1, 128, got < 0)) {
         if (got < 0) report_timeout(p, abort_flag, 5);
         break;
       }
-      if (got > 0) finish<H, EPI>(p, rb, r, sum, 0, sm.swx, sm.rinv, res, src);
+      if (got > 0) finish<H, EPI>(p, rb, r, sum, 0, sm.swx, sm.rinv, res, src, t0, t1);
     }
-    // an owner leaves only after its inbox has been filled (bounded: a peer that gave up sends
+    // a CTA leaves only after its inboxes have been filled (bounded: a peer that gave up sends
     // nothing), so no st.async can land in a CTA that has exited
     if (C > 1 && threadIdx.x == 64)
       for (int s = 0; s < owned; ++s) tc::mbar_wait(&sm.inbox_full[s], 0, lim);
@@ -462,7 +466,7 @@ bool csk_plan(int RB, int KS, int BN, int num_sms, CskPlan* out) {
     q.C = C;
     q.NC = std::min(RB, num_sms / C);
     const int tmax = (RB + q.NC - 1) / q.NC;
-    q.slots = C > 1 ? (tmax + C - 1) / C : 0;
+    q.slots = C > 1 ? tmax : 0;
     if (q.slots > kMaxSlots) continue;
     q.stages = 2;  // the shallowest pipeline a launch may get
     if (csk_smem_bytes<64>(q, true) > (size_t)kSmemBudget) continue;
@@ -470,7 +474,7 @@ bool csk_plan(int RB, int KS, int BN, int num_sms, CskPlan* out) {
     if (fit <= 0) continue;
     if (fit < q.NC) q.NC = fit;
     const int tmax2 = (RB + q.NC - 1) / q.NC;
-    q.slots = C > 1 ? (tmax2 + C - 1) / C : 0;
+    q.slots = C > 1 ? tmax2 : 0;
     if (q.slots > kMaxSlots) continue;
     const double cost = (double)tmax2 * ((SB + C - 1) / C) * kCskBlocks + (C > 1 ? 2.0 : 0.0) + 0.01 * C;
     if (cost < best) {

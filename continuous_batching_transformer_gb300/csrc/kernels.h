@@ -117,7 +117,7 @@ struct CskPlan {
   int C;       // CTAs per cluster (split of K)
   int NC;      // clusters
   int stages;  // pipeline depth
-  int slots;   // inbox slots: most tiles one CTA owns
+  int slots;   // inbox slots: most tiles of one cluster (C > 1)
   int nk;      // 64-column blocks per stage (one TMA box of weights, one of operand)
 };
 constexpr int kCskBlocks = 2;  // nk of the decode projections' tensor maps

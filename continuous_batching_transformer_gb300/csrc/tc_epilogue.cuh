@@ -8,19 +8,21 @@
 
 namespace tcepi {
 
-// Residual values out[tok0 + j][m] of tile row r for an EPI_ADD epilogue, all loads issued
-// before any is used (the epilogue's latency is a chain of global round trips otherwise).
-// EPI_T >= 0: the epilogue fixed at compile time (only its code is generated), else p.epi.
+// Residual values out[tok0 + j][m] of tile row r for an EPI_ADD epilogue (columns jlo <= j <
+// jhi), all loads issued before any is used (the epilogue's latency is a chain of global round
+// trips otherwise).  EPI_T >= 0: the epilogue fixed at compile time (only its code is
+// generated), else p.epi.
 template <int CNT, int EPI_T = -1>
 __device__ __forceinline__ void load_residual(const TcParams& p, int rb, int r, int tok0,
-                                              float* res) {
+                                              float* res, int jlo = 0, int jhi = CNT) {
   const int epi = EPI_T >= 0 ? EPI_T : p.epi;
   const int m = rb * 128 + r;
 #pragma unroll
   for (int j = 0; j < CNT; ++j) {
     const int t = tok0 + j;
-    res[j] = (epi == EPI_ADD && m < p.M && t < p.n_act) ? __ldcg(p.out + (size_t)t * p.ldo + m)
-                                                        : 0.f;
+    res[j] = (epi == EPI_ADD && m < p.M && t < p.n_act && j >= jlo && j < jhi)
+                 ? __ldcg(p.out + (size_t)t * p.ldo + m)
+                 : 0.f;
   }
 }
 
@@ -56,7 +58,7 @@ __device__ __forceinline__ float load_next_gain(const TcParams& p, int rb, int r
 // or page (kvq_jobs[j]); nothing is written in bf16.
 template <int CNT>
 __device__ __forceinline__ void kvq_append(const TcParams& p, int rb, int r, const float (&x)[CNT],
-                                           float* swx, const EpiSrc& src) {
+                                           float* swx, const EpiSrc& src, int jlo, int jhi) {
   const int hd = p.head_dim, bits = p.kvq_bits;
   const int row = rb * 128 + r, head = row / hd, i = row % hd;
   const bool isv = head >= p.n_heads + p.n_kv_heads;
@@ -94,7 +96,7 @@ __device__ __forceinline__ void kvq_append(const TcParams& p, int rb, int r, con
   }
   tc::named_bar_sync(1, 128);
   const int jj = r & 63;  // thread jj of a group prepares row jj's scale, bias and reciprocal
-  if (jj < CNT && jj < p.n_act) {
+  if (jj < CNT && jj >= jlo && jj < jhi) {
     const int w0 = 2 * grp, w1 = 2 * grp + 1;
     const float gmn = fminf(wmm[(w0 * CNT + jj) * 2], wmm[(w1 * CNT + jj) * 2]);
     const float gmx = fmaxf(wmm[(w0 * CNT + jj) * 2 + 1], wmm[(w1 * CNT + jj) * 2 + 1]);
@@ -109,7 +111,7 @@ __device__ __forceinline__ void kvq_append(const TcParams& p, int rb, int r, con
   const int ng = hd / 64, gr = i / 64, row_bytes = hd * bits / 8;
 #pragma unroll
   for (int j = 0; j < CNT; ++j) {
-    if (j >= p.n_act) break;
+    if (j < jlo || j >= jhi) continue;
     const float sc = gsb[(grp * CNT + j) * 2], bi = gsb[(grp * CNT + j) * 2 + 1];
     uint32_t code = 0u;
     if (sc != 0.f) {
@@ -138,8 +140,8 @@ __device__ __forceinline__ void kvq_append(const TcParams& p, int rb, int r, con
 }
 
 // Final epilogue of CNT (<= 32) columns (tokens tok0 .. tok0+CNT-1) of tile row r of row
-// block rb.  All 128 epilogue threads call it together (it synchronises them on named barrier
-// 1).  rinv (when p.ss_in) holds each column's RMSNorm factor; res the residual values from
+// block rb, of which columns jlo <= j < jhi are written.  All 128 epilogue threads call it
+// together (it synchronises them on named barrier 1).  rinv (when p.ss_in) holds each column's RMSNorm factor; res the residual values from
 // load_residual (EPI_ADD).  The tile's values are staged in swx ([row][CNT + 1]) and every
 // per-column step below is a rolled loop over them: unrolled over 32 columns, the three store
 // paths of a launch grow past the instruction cache and the epilogue waits on instruction
@@ -147,14 +149,14 @@ __device__ __forceinline__ void kvq_append(const TcParams& p, int rb, int r, con
 template <int CNT, int EPI_T = -1>
 __device__ __forceinline__ void finish(const TcParams& p, int rb, int r, float* vals, int tok0,
                                        float* swx, const float* rinv, const float* res,
-                                       const EpiSrc& src) {
+                                       const EpiSrc& src, int jlo = 0, int jhi = CNT) {
   const int epi = EPI_T >= 0 ? EPI_T : p.epi;
   constexpr int LD = CNT + 1;  // staged row pitch: a column's 32 rows sit in 32 banks
   if (p.ss_in) {
 #pragma unroll
     for (int j = 0; j < CNT; ++j) vals[j] *= rinv[j];
   }
-  const int n = min(CNT, p.n_act - tok0);  // columns that are tokens
+  const int n = min(jhi, p.n_act - tok0);  // columns [jlo, n) are tokens to write
   tc::named_bar_sync(1, 128);              // swx is free
   if (epi == EPI_QKV || epi == EPI_QKVQ) {
     // Row r of the tile is dim i of head `head` of q|k|v (heads are head_dim-aligned in the
@@ -182,8 +184,9 @@ __device__ __forceinline__ void finish(const TcParams& p, int rb, int r, float* 
       // a 256-row boundary) quantises its rows once they are all rotated
       float xq[CNT];
 #pragma unroll
-      for (int j = 0; j < CNT; ++j) xq[j] = (j < n && row < p.M) ? bf16_to_f32(f32_to_bf16(rotated(j))) : 0.f;
-      kvq_append<CNT>(p, rb, r, xq, swx, src);
+      for (int j = 0; j < CNT; ++j)
+        xq[j] = (j >= jlo && j < n && row < p.M) ? bf16_to_f32(f32_to_bf16(rotated(j))) : 0.f;
+      kvq_append<CNT>(p, rb, r, xq, swx, src, jlo, n);
       return;
     }
     if (row >= p.M) return;
@@ -195,7 +198,7 @@ __device__ __forceinline__ void finish(const TcParams& p, int rb, int r, float* 
       const uint32_t ohi = sw128_offset(head % G, i, 2048), olo = sw128_offset(8 + head % G, i, 2048);
       const float qs = rsqrtf((float)hd);
 #pragma unroll 2
-      for (int j = 0; j < n; ++j) {
+      for (int j = jlo; j < n; ++j) {
         const float qv = rotated(j) * qs;
         const uint16_t hi = f32_to_bf16(qv);
         uint8_t* t = tile + (size_t)j * p.n_kv_heads * img;
@@ -204,14 +207,14 @@ __device__ __forceinline__ void finish(const TcParams& p, int rb, int r, float* 
       }
     } else if (rope) {
 #pragma unroll 2
-      for (int j = 0; j < n; ++j) {
+      for (int j = jlo; j < n; ++j) {
         const QueryRow qr = src.rows[j];
         p.arena[k_index(qr, p.layer, head - p.n_heads, qr.pos, i, p.n_kv_heads, hd)] =
             f32_to_bf16(rotated(j));
       }
     } else {
 #pragma unroll 2
-      for (int j = 0; j < n; ++j) {
+      for (int j = jlo; j < n; ++j) {
         const QueryRow qr = src.rows[j];
         p.arena[v_index(qr, p.layer, head - p.n_heads - p.n_kv_heads, qr.pos, i, p.n_kv_heads,
                         hd)] = f32_to_bf16(swx[r * LD + j]);
@@ -227,7 +230,7 @@ __device__ __forceinline__ void finish(const TcParams& p, int rb, int r, float* 
       swx[r * LD + j] = m < p.M ? (epi == EPI_ADD ? vals[j] + res[j] : vals[j]) : 0.f;
     if (m < p.M) {
 #pragma unroll 2
-      for (int j = 0; j < n; ++j) {
+      for (int j = jlo; j < n; ++j) {
         const size_t t = (size_t)(tok0 + j);
         const float v = swx[r * LD + j];
         p.out[t * p.ldo + m] = v;
@@ -246,7 +249,7 @@ __device__ __forceinline__ void finish(const TcParams& p, int rb, int r, float* 
       tc::named_bar_sync(1, 128);
       const int j = r >> 2, w = r & 3;
       float sq = 0.f;
-      if (j < n) {
+      if (j >= jlo && j < n) {
 #pragma unroll 8
         for (int k = 0; k < 32; ++k) {
           const float v = swx[(32 * w + ((k + w) & 31)) * LD + j];
@@ -255,25 +258,27 @@ __device__ __forceinline__ void finish(const TcParams& p, int rb, int r, float* 
       }
       sq += __shfl_xor_sync(0xffffffffu, sq, 1);
       sq += __shfl_xor_sync(0xffffffffu, sq, 2);
-      if (w == 0 && j < n) p.ss_out[(size_t)rb * p.ss_ld + tok0 + j] = sq;
+      if (w == 0 && j >= jlo && j < n) p.ss_out[(size_t)rb * p.ss_ld + tok0 + j] = sq;
     }
     return;
   }
-  // SwiGLU: tile rows 0..63 are gate rows, 64..127 the up rows of the same 64 features; two
-  // threads per feature take alternate columns
+  if (epi == EPI_SWIGLU) {
+    // SwiGLU: tile rows 0..63 are gate rows, 64..127 the up rows of the same 64 features; two
+    // threads per feature take alternate columns
 #pragma unroll
-  for (int j = 0; j < CNT; ++j) swx[r * LD + j] = vals[j];
-  tc::named_bar_sync(1, 128);
-  const int fr = r & 63, f = rb * 64 + fr;
-  if (f < p.F) {
+    for (int j = 0; j < CNT; ++j) swx[r * LD + j] = vals[j];
+    tc::named_bar_sync(1, 128);
+    const int fr = r & 63, f = rb * 64 + fr;
+    if (f < p.F) {
 #pragma unroll 2
-    for (int j = r >> 6; j < n; j += 2) {
-      const size_t t = (size_t)(tok0 + j);
-      const float g = swx[fr * LD + j], u = swx[(64 + fr) * LD + j];
-      const float a = g / (1.f + expf(-g)) * u;
-      const uint16_t hi = f32_to_bf16(a);
-      p.act[t * p.act_ld + f] = hi;
-      if (p.act_lo) p.act[(p.act_lo + t) * p.act_ld + f] = f32_to_bf16(a - bf16_to_f32(hi));
+      for (int j = jlo + (r >> 6); j < n; j += 2) {
+        const size_t t = (size_t)(tok0 + j);
+        const float g = swx[fr * LD + j], u = swx[(64 + fr) * LD + j];
+        const float a = g / (1.f + expf(-g)) * u;
+        const uint16_t hi = f32_to_bf16(a);
+        p.act[t * p.act_ld + f] = hi;
+        if (p.act_lo) p.act[(p.act_lo + t) * p.act_ld + f] = f32_to_bf16(a - bf16_to_f32(hi));
+      }
     }
   }
 }
