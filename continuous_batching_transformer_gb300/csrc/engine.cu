@@ -1418,26 +1418,34 @@ static void drop_graphs(cbt_engine* e);
 static cudaError_t upload_page_tables(cbt_engine* e);
 
 // Work list of the tensor-core decode attention for the rows in e->hrows[0..B): per row and kv
-// head, runs of kSubsPerItem 128-key sub-chunks over positions [0, pos].  Grows the item and
-// partial buffers when needed and copies the list to the device on the engine stream.
-static constexpr int kSubsPerItem = 1;
+// head, runs of 128-key sub-chunks over positions [0, pos].  Grows the item and partial
+// buffers when needed and copies the list to the device on the engine stream.
+//
+// Sub-chunks per item: one, or two for a row whose own context reaches kLongSubs sub-chunks
+// (half the partial outputs and merge work of a long row, with items still plentiful enough
+// to balance the grid).  The choice depends on the row's own length, so a row's result does
+// not depend on the other rows of the step.  Paged slabs keep one (an item lies in one page,
+// and pages may be 128 positions); so does quantised KV (its kernel takes one per item).
+static constexpr int kLongSubs = 64;
+static int subs_per_item(const cbt_engine* e, const Slab& sl, int nsub) {
+  return (nsub >= kLongSubs && !e->quant() && !paged(e, sl)) ? 2 : 1;
+}
 
 static cudaError_t plan_decode_attention(cbt_engine* e, int B) {
   const int Hkv = e->cfg.n_kv_heads, G = e->cfg.n_heads / Hkv, hd = e->cfg.head_dim;
   e->hitems.clear();
   for (int b = 0; b < B; ++b) {
     const int nsub = (e->hrows[b].pos + 1 + 127) / 128;
-    const int splits = (nsub + kSubsPerItem - 1) / kSubsPerItem;
+    const int per = subs_per_item(e, *e->hslab[b], nsub);
+    const int splits = (nsub + per - 1) / per;
     e->hitem_base[b] = (int)e->hitems.size();
     e->hitem_count[b] = splits;
-    // an item's sub-chunks lie in one page (pages are multiples of 128 * kSubsPerItem keys)
     for (int g = 0; g < Hkv; ++g)
       for (int sp = 0; sp < splits; ++sp) {
-        AttnItem it{b, g, sp * kSubsPerItem, std::min(nsub, (sp + 1) * kSubsPerItem),
-                    row_base(e, *e->hslab[b], sp * kSubsPerItem * 128), 0, 0,
-                    e->hrows[b].pos + 1};
+        AttnItem it{b, g, sp * per, std::min(nsub, (sp + 1) * per),
+                    row_base(e, *e->hslab[b], sp * per * 128), 0, 0, e->hrows[b].pos + 1};
         if (e->quant()) {  // the quantised slab or page: byte offset, capacity, first position
-          const QLoc q = qloc(e, *e->hslab[b], sp * kSubsPerItem * 128);
+          const QLoc q = qloc(e, *e->hslab[b], sp * per * 128);
           it.kbase = q.off;
           it.cap = q.cap;
           it.p0 = q.p0;

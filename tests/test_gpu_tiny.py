@@ -163,3 +163,50 @@ def test_affine4_decode_operand_widths(B):
         solo.decode_step_batch(s1, to_dev(feeds[step][B - 1:], dev), lg1)
         np.testing.assert_array_equal(lg1.cpu().numpy()[0], outs[step][B - 1])
     solo.close()
+
+
+def test_long_rows_take_two_subchunk_items():
+    """Rows whose context reaches 8192 keys are split into attention items of two 128-key
+    sub-chunks (the others into items of one): rows of 8300 (an odd count of sub-chunks, so its
+    last item has one), 8191 and 300 positions of seeded synthetic KV, two decode steps fed the
+    oracle's own greedy tokens, against the oracle, and the long row's logits equal, bit for
+    bit, to those of the row decoded alone (the item split depends on the row's own length)."""
+    ensure_built()
+    shape = ModelShape("long-items", 2, 512, 4, 2, 128, 1024, 2048, 1e-5, 1e6, gain_sigma=0.1)
+    dev = torch.device("cuda:0")
+    ctx = [8300, 8191, 300]
+    seed = 5
+    om = oracle.OracleModel(shape)
+    caches = []
+    for r, n in enumerate(ctx):
+        c = oracle.KVCache(shape, n + 8)
+        c.fill_synthetic(r, n, seed)
+        caches.append(c)
+    feeds = [np.asarray(np.random.default_rng(9).integers(0, shape.vocab, len(ctx)), np.int32)]
+    refs = []
+    for step in range(2):
+        refs.append(oracle.decode_step_batch(om, caches, feeds[-1]))
+        feeds.append(np.array([oracle.argmax(o) for o in refs[-1]], dtype=np.int32))
+    w = DeviceWeights(shape, dev)
+
+    def run(rows):
+        eng = Engine(w, arena_bytes=96 << 20, max_batch=4, max_prefill_tokens=64)
+        slabs = []
+        for r in rows:
+            slabs.append(eng.kv_slab_alloc(ctx[r] + 8))
+            eng.fill_synthetic_kv(slabs[-1], r, ctx[r], seed)
+        logits = torch.empty((len(rows), shape.vocab), dtype=torch.float32, device=dev)
+        outs = []
+        for step in range(2):
+            eng.decode_step_batch(slabs, to_dev(feeds[step][rows], dev), logits)
+            outs.append(logits.cpu().numpy().copy())
+        assert eng.device_error() == (0, 0)
+        eng.close()
+        return outs
+
+    batched = run([0, 1, 2])
+    for step in range(2):
+        check_logits(batched[step], refs[step], TOL["bf16"], f"long rows step {step}")
+    solo = run([0])
+    for step in range(2):
+        assert np.array_equal(solo[step][0], batched[step][0]), f"step {step}: batched != solo"
