@@ -23,6 +23,11 @@ constexpr int kSub = 128;      // keys per sub-chunk (MMA M)
 constexpr int kBox = 16384;    // one 128 x 128-byte tile
 constexpr int kCompute = 128;  // threads of warps 0..3; warp 4 is the producer
 constexpr int kCtasPerSm = 3;
+// Two threads issue each contraction's MMAs (threads 0 and 32, half of the k-steps each, into
+// accumulators of their own, added when read): one thread issues a tcgen05.mma only about
+// every 60 ns, which made the eight MMAs of S and of P.V a long step of every sub-chunk.
+constexpr int kIssuers = 2;
+constexpr uint32_t kTmemCols = 64;  // issuer i: S^T in columns 32 i .. +15, O^T in 32 i + 16 .. +15
 
 __device__ __forceinline__ void st_bf16(uint8_t* base, uint32_t off, uint16_t v) {
   *reinterpret_cast<uint16_t*>(base + off) = v;
@@ -99,17 +104,18 @@ __global__ void __launch_bounds__(160, kCtasPerSm)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    for (int i = 0; i < 8; ++i) tc::mbar_init(&bars[i], 1);
+    // full barriers: the producer's arrival; empty and MMA barriers: both issuers' commits
+    for (int i = 0; i < 8; ++i) tc::mbar_init(&bars[i], i < 3 ? 1 : kIssuers);
     *abort_flag = 0;
     tc::mbar_fence_init();
     tc::tma_prefetch_desc(&tk);
     tc::tma_prefetch_desc(&tv);
   }
-  if (warp == 0) tc::tmem_alloc(tmem_slot, 32);
+  if (warp == 0) tc::tmem_alloc(tmem_slot, kTmemCols);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  const uint32_t tmem = *tmem_slot;  // columns 0..15: S^T, 16..31: O^T
+  const uint32_t tmem = *tmem_slot;
   pdl_launch();
   // the work list and the row table are step inputs copied before the step's first kernel, so
   // they may be read before waiting for the previous kernel
@@ -200,7 +206,8 @@ __global__ void __launch_bounds__(160, kCtasPerSm)
       tc::named_bar_sync(1, kCompute);
 
       for (int sub = w.s0; sub < w.s1; ++sub, ++sn) {
-        if (tid == 0) {
+        if (tid == 0 || tid == 32) {  // issuer i: k-steps [i HD/32, (i + 1) HD/32)
+          const int iss = tid >> 5;
           bool good = true;
           if (sub == w.s0) good = tc::mbar_wait(qfull, qn & 1);
           good = good && tc::mbar_wait(kfull, kn & 1);
@@ -208,11 +215,13 @@ __global__ void __launch_bounds__(160, kCtasPerSm)
             flag_timeout(err, abort_flag, 24);
           } else {
             tc::tc_fence_after();
+            constexpr int kSteps = HD / 16 / kIssuers;
 #pragma unroll
-            for (int kk = 0; kk < HD / 16; ++kk) {
+            for (int k = 0; k < kSteps; ++k) {
+              const int kk = iss * kSteps + k;
               const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sK + (kk >> 2) * kBox)) + 2 * (kk & 3);
               const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sQ + (kk >> 2) * 2048)) + 2 * (kk & 3);
-              tc::mma_bf16(tmem, ad, bd, kIdesc, kk > 0 ? 1u : 0u);
+              tc::mma_bf16(tmem + 32 * iss, ad, bd, kIdesc, k > 0 ? 1u : 0u);
             }
             tc::mma_commit(bar_s);
             tc::mma_commit(kempty);                 // K buffer free once the MMA has read it
@@ -227,15 +236,18 @@ __global__ void __launch_bounds__(160, kCtasPerSm)
         }
         tc::tc_fence_after();
         // scores of this thread's key: S^T lane = key, columns j (hi) + 8 + j (lo)
-        uint32_t raw[16];
+        uint32_t raw[16], raw2[16];
         tc::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16), raw);
+        tc::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + 32, raw2);
         tc::tmem_ld_wait();
         const int key = sub * kSub + tid;
         const bool valid = key < n;
         float s[GT], mx[GT];
 #pragma unroll
         for (int h = 0; h < GT; ++h) {
-          s[h] = valid ? __uint_as_float(raw[h]) + __uint_as_float(raw[8 + h]) : -INFINITY;
+          s[h] = valid ? (__uint_as_float(raw[h]) + __uint_as_float(raw[8 + h])) +
+                             (__uint_as_float(raw2[h]) + __uint_as_float(raw2[8 + h]))
+                       : -INFINITY;
           mx[h] = s[h];
         }
         warp_reduce_n<GT, true>(mx);
@@ -285,16 +297,19 @@ __global__ void __launch_bounds__(160, kCtasPerSm)
         tc::named_bar_sync(1, kCompute);
         if (tid < GT)
           l_run[tid] = l_run[tid] * scl[tid] + red2[tid] + red2[8 + tid] + red2[16 + tid] + red2[24 + tid];
-        if (tid == 0) {
+        if (tid == 0 || tid == 32) {  // issuer i: keys [64 i, 64 i + 64)
+          const int iss = tid >> 5;
           if (!tc::mbar_wait(vfull, vn & 1)) {
             flag_timeout(err, abort_flag, 26);
           } else {
             tc::tc_fence_after();
+            constexpr int kSteps = kSub / 16 / kIssuers;
 #pragma unroll
-            for (int kk = 0; kk < kSub / 16; ++kk) {
+            for (int k = 0; k < kSteps; ++k) {
+              const int kk = iss * kSteps + k;
               const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sV + (kk >> 2) * kBox)) + 2 * (kk & 3);
               const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sP + (kk >> 2) * 2048)) + 2 * (kk & 3);
-              tc::mma_bf16(tmem + 16, ad, bd, kIdesc, kk > 0 ? 1u : 0u);
+              tc::mma_bf16(tmem + 32 * iss + 16, ad, bd, kIdesc, k > 0 ? 1u : 0u);
             }
             tc::mma_commit(bar_o);
             tc::mma_commit(vempty);
@@ -308,10 +323,12 @@ __global__ void __launch_bounds__(160, kCtasPerSm)
         }
         tc::tc_fence_after();
         tc::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + 16, raw);
+        tc::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + 48, raw2);
         tc::tmem_ld_wait();
 #pragma unroll
         for (int h = 0; h < GT; ++h)
-          oacc[h] = oacc[h] * scl[h] + __uint_as_float(raw[h]) + __uint_as_float(raw[8 + h]);
+          oacc[h] = oacc[h] * scl[h] + ((__uint_as_float(raw[h]) + __uint_as_float(raw[8 + h])) +
+                                        (__uint_as_float(raw2[h]) + __uint_as_float(raw2[8 + h])));
         tc::tc_fence_before();
       }
       ++qn;
@@ -328,7 +345,7 @@ __global__ void __launch_bounds__(160, kCtasPerSm)
   __syncthreads();
   if (warp == 0) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, 32);
+    tc::tmem_dealloc(tmem, kTmemCols);
   }
   if (tid == 0) stamp_end(stamp);
 }
