@@ -111,8 +111,9 @@ bool launch_tc_linear(const CUtensorMap& tw, const CUtensorMap& tx, TcParams p, 
 
 // ---- cluster split-K decode projections (gemm_csk.cu) -----------------------------------------
 // Clusters of C CTAs; cluster c takes row tiles c, c + NC, ...; rank r streams k-blocks
-// [r*KS/C, (r+1)*KS/C) of each and hands its partial sums to the tile's owner through
-// distributed shared memory.
+// [r*KS/C, (r+1)*KS/C) of each, and the tile's partial sums are reduce-scattered over the
+// cluster through distributed shared memory (rank r adds and finishes its chunk of the
+// columns).
 struct CskPlan {
   int C;       // CTAs per cluster (split of K)
   int NC;      // clusters
