@@ -98,9 +98,7 @@ __global__ void __launch_bounds__(160, kCtasPerSm)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* red = reinterpret_cast<float*>(tmem_slot + 4);  // [4 warps][8 heads]
   float* red2 = red + 32;                                // [4 warps][8 heads]
-  float* m_run = red2 + 32;                              // [8]
-  float* l_run = m_run + 8;
-  float* scl = l_run + 8;
+  float* l_run = red2 + 32;                              // [8]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -196,10 +194,12 @@ __global__ void __launch_bounds__(160, kCtasPerSm)
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
       const AttnItem w = items[it];
       const int n = rows[w.b].pos + 1;
-      if (tid < 8) {
-        m_run[tid] = -INFINITY;
-        l_run[tid] = 0.f;
-      }
+      if (tid < 8) l_run[tid] = 0.f;
+      // the running max of every head, kept by every thread: each computes it from the same
+      // inputs in the same order, so no exchange is needed between the max and the weights
+      float m_run[GT];
+#pragma unroll
+      for (int h = 0; h < GT; ++h) m_run[h] = -INFINITY;
       float oacc[GT];
 #pragma unroll
       for (int h = 0; h < GT; ++h) oacc[h] = 0.f;
@@ -256,14 +256,15 @@ __global__ void __launch_bounds__(160, kCtasPerSm)
           for (int h = 0; h < GT; ++h) red[warp * 8 + h] = mx[h];
         }
         tc::named_bar_sync(1, kCompute);
-        if (tid < GT) {
-          const float mloc = fmaxf(fmaxf(red[tid], red[8 + tid]), fmaxf(red[16 + tid], red[24 + tid]));
-          const float mo = m_run[tid];
+        float scl[GT];
+#pragma unroll
+        for (int h = 0; h < GT; ++h) {
+          const float mloc = fmaxf(fmaxf(red[h], red[8 + h]), fmaxf(red[16 + h], red[24 + h]));
+          const float mo = m_run[h];
           const float mn = fmaxf(mo, mloc);
-          scl[tid] = mo == -INFINITY ? 0.f : __expf(mo - mn);
-          m_run[tid] = mn;
+          scl[h] = mo == -INFINITY ? 0.f : __expf(mo - mn);
+          m_run[h] = mn;
         }
-        tc::named_bar_sync(1, kCompute);
         float ps[GT];
 #pragma unroll
         for (int h = 0; h < GT; ++h) {  // P rows of heads >= GT stay zero (set at the start)
@@ -295,8 +296,13 @@ __global__ void __launch_bounds__(160, kCtasPerSm)
         fence_proxy_async();
         tc::tc_fence_before();
         tc::named_bar_sync(1, kCompute);
-        if (tid < GT)
-          l_run[tid] = l_run[tid] * scl[tid] + red2[tid] + red2[8 + tid] + red2[16 + tid] + red2[24 + tid];
+        if (tid < GT) {
+          float sc = scl[0];
+#pragma unroll
+          for (int h = 1; h < GT; ++h)
+            if (h == tid) sc = scl[h];
+          l_run[tid] = l_run[tid] * sc + red2[tid] + red2[8 + tid] + red2[16 + tid] + red2[24 + tid];
+        }
         if (tid == 0 || tid == 32) {  // issuer i: keys [64 i, 64 i + 64)
           const int iss = tid >> 5;
           if (!tc::mbar_wait(vfull, vn & 1)) {
@@ -337,7 +343,13 @@ __global__ void __launch_bounds__(160, kCtasPerSm)
       if (tid < HD) {
         for (int h = 0; h < G; ++h) part_o[((size_t)it * G + h) * HD + tid] = oacc[h];
       }
-      if (tid < G) part_ml[(size_t)it * G + tid] = make_float2(m_run[tid], l_run[tid]);
+      if (tid < G) {
+        float mm = m_run[0];
+#pragma unroll
+        for (int h = 1; h < GT; ++h)
+          if (h == tid) mm = m_run[h];
+        part_ml[(size_t)it * G + tid] = make_float2(mm, l_run[tid]);
+      }
       tc::named_bar_sync(1, kCompute);
     }
   }
