@@ -100,8 +100,8 @@ struct cbt_engine {
   std::vector<int32_t> hidx;
   int64_t steps = 0, prefill_tokens = 0;
 
-  // tensor-core path (bf16 weights): TMA descriptors of every weight matrix (64x64 boxes),
-  // bf16 operand buffers of the projections and the stream-K scratch
+  // tensor-core path (bf16 weights): TMA descriptors of every weight matrix (64x64 boxes)
+  // and bf16 operand buffers of the projections
   bool use_tc = false;
   int num_sms = 0;
   struct LayerMaps {
@@ -127,9 +127,6 @@ struct cbt_engine {
   uint16_t *act_h = nullptr, *act_o = nullptr, *act_u = nullptr;
   std::map<std::pair<const void*, int>, CUtensorMap> xmaps;  // (operand buffer, N tile)
   std::map<std::pair<const void*, int>, CUtensorMap> xmaps_kb;
-  float* tc_part = nullptr;
-  size_t tc_part_floats = 0;
-  int* tc_cnt = nullptr;
   // tensor-core decode attention: TMA descriptors over the whole KV arena, the per-step work
   // list and the split-K partials (grown on demand)
   CUtensorMap kv_kmap, kv_vmap;
@@ -209,8 +206,8 @@ extern "C" const char* cbt_status_str(cbt_status s) {
 static void free_scratch(cbt_engine* e) {
   void* ptrs[] = {e->x,       e->h,        e->qkv,  e->o,     e->act,    e->part,
                   e->xg,      e->logits,   e->cosv, e->sinv,  e->next_tok, e->last_idx,
-                  e->rows,    e->err,      e->act_h, e->act_o, e->act_u,  e->tc_part,
-                  e->tc_cnt,  e->items,    e->item_meta, e->att_o, e->att_ml, e->stage,
+                  e->rows,    e->err,      e->act_h, e->act_o, e->act_u,
+                  e->items,    e->item_meta, e->att_o, e->att_ml, e->stage,
                   e->qtile,   e->ss,       e->qb,     e->pf_units, e->q4_arena, e->pagetab,
                   e->tok_pages, e->kv8_jobs, e->q4x};
   for (void* q : ptrs)
@@ -344,7 +341,7 @@ extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_w
   const bool bf16w = c.weight_format == CBT_WEIGHTS_BF16;
   if (rc == cudaSuccess && (bf16w || (c.d_model % 128 == 0 && qd % 128 == 0 && c.d_ff % 128 == 0))) {
     // tensor-core path: weight descriptors (bf16) or native 4-bit blocks, bf16 operand
-    // buffers, stream-K scratch
+    // buffers
     int dev = 0;
     chk(cudaGetDevice(&dev));
     chk(cudaDeviceGetAttribute(&e->num_sms, cudaDevAttrMultiProcessorCount, dev));
@@ -352,12 +349,6 @@ extern "C" cbt_status cbt_engine_create(const cbt_model_config* cfg, const cbt_w
     chk(dmalloc(&e->act_h, (size_t)e->act_rows * std::max(c.d_model, qd), &tot));
     chk(dmalloc(&e->act_o, (size_t)e->act_rows * qd, &tot));
     chk(dmalloc(&e->act_u, (size_t)e->act_rows * c.d_ff, &tot));
-    e->tc_part_floats = (size_t)4 << 20;
-    chk(dmalloc(&e->tc_part, e->tc_part_floats, &tot));
-    const int max_tiles = std::max({(nqkv + 127) / 128, (c.d_model + 127) / 128, c.d_ff / 64,
-                                    (c.vocab + 127) / 128});
-    chk(dmalloc(&e->tc_cnt, (size_t)max_tiles, &tot));
-    if (rc == cudaSuccess) rc = cudaMemsetAsync(e->tc_cnt, 0, sizeof(int) * max_tiles, e->stream);
     if (rc == cudaSuccess) {
       const size_t arows = e->act_rows;
       for (uint16_t* a : {e->act_h, e->act_o, e->act_u}) {
@@ -1180,8 +1171,6 @@ static bool tc_projection(cbt_engine* e, const CUtensorMap& wmap, const CUtensor
   p.act = act_out;
   p.act_ld = act_ld;
   p.act_lo = tc_lo_rows(e, n);
-  p.part = e->tc_part;
-  p.cnt = e->tc_cnt;
   p.err = e->err;
   if (n <= 32) p.stamp = next_stamp(e, CBT_KCLASS_PROJ);  // the decode projections
   if (e->stall_now) {
@@ -1204,12 +1193,11 @@ static bool tc_projection(cbt_engine* e, const CUtensorMap& wmap, const CUtensor
                           static_cast<const uint16_t*>(q4lin->scales),
                           static_cast<const uint16_t*>(q4lin->biases), M, K, hi, hi + e->q4x_elems,
                           e->num_sms, e->stream) &&
-         launch_tc_linear(e->q4x_maps[q4shape][0], *xm, p, false, BN, e->num_sms,
-                          e->tc_part_floats, e->stream, &e->q4x_maps[q4shape][1]);
+         launch_tc_linear(e->q4x_maps[q4shape][0], *xm, p, false, BN, e->num_sms, e->stream,
+                          &e->q4x_maps[q4shape][1]);
   } else {
     ok = split ? launch_tc_csk(wmap_kb, *xm, p, BN, e->num_sms, e->stream)
-               : launch_tc_linear(wmap, *xm, p, split, BN, e->num_sms, e->tc_part_floats,
-                                  e->stream);
+               : launch_tc_linear(wmap, *xm, p, split, BN, e->num_sms, e->stream);
   }
   tend(e, t, weight_bytes(e->cfg, M, K) + 4.0 * n * K + 4.0 * n * Mo * (epi == EPI_ADD ? 2 : 1));
   return ok;

@@ -359,8 +359,7 @@ int tc_plain_bn(int n) { return n <= 64 ? 64 : 128; }
 // over min(tiles, SMs) CTAs.  p carries shapes, epilogue and outputs.  Returns false if the
 // shape is outside what the kernel supports (decode rows go to launch_tc_csk / launch_q4_rd).
 bool launch_tc_linear(const CUtensorMap& tw, const CUtensorMap& tx, TcParams p, bool split, int BN,
-                      int num_sms, size_t part_floats, cudaStream_t s, const CUtensorMap* twl) {
-  (void)part_floats;
+                      int num_sms, cudaStream_t s, const CUtensorMap* twl) {
   if (split) return false;
   if (p.K % 64 || p.K <= 0 || p.n_act <= 0) return false;
   if (p.epi == EPI_SWIGLU && (p.F % 64 || p.M != 2 * p.F)) return false;
@@ -369,9 +368,6 @@ bool launch_tc_linear(const CUtensorMap& tw, const CUtensorMap& tx, TcParams p, 
   p.RB = p.epi == EPI_SWIGLU ? p.F / 64 : (p.M + 127) / 128;
   p.KS = p.K / 64;
   p.NT = (p.n_act + BN - 1) / BN;
-  p.streamk = 0;
-  p.U = (long long)p.RB * p.NT * p.KS;
-  p.slots = 0;
   const int G = std::min(p.RB * p.NT, num_sms);
   cudaError_t rc;
   if (twl) {  // weights as hi + lo parts: a third tile per stage

@@ -50,12 +50,8 @@ struct TcParams {
   uint16_t* act;     // EPI_SWIGLU: bf16 operand of the next projection, [rows][act_ld]
   int act_ld;
   int act_lo;        // row offset of the lo parts (0: plain bf16, no lo part)
-  // schedule, filled by launch_tc_linear
+  // schedule, filled by the launcher: row tiles, token tiles, 64-column k-blocks
   int RB, NT, KS;
-  long long U;
-  int streamk, slots;
-  float* part;       // stream-K partial sums
-  int* cnt;          // per-tile completion counters, zero between launches
   int* err;          // device error word
   // RMSNorm folded into the projections (decode rows only).  Consumer side: the operand is
   // x * g, and column b of the result is scaled by rsqrt(sum_t ss_in[t][b] / K + eps).
@@ -106,8 +102,7 @@ int tc_plain_bn(int n);
 // twl (prefill only): the lo parts of weights given as bf16 hi + lo matrices (both maps 64 x 64
 // boxes over [M][K]); the product is hi.x_hi + hi.x_lo + lo.x_hi.
 bool launch_tc_linear(const CUtensorMap& tw, const CUtensorMap& tx, TcParams p, bool split,
-                      int BN, int num_sms, size_t part_floats, cudaStream_t s,
-                      const CUtensorMap* twl = nullptr);
+                      int BN, int num_sms, cudaStream_t s, const CUtensorMap* twl = nullptr);
 
 // ---- cluster split-K decode projections (gemm_csk.cu) -----------------------------------------
 // Clusters of C CTAs; cluster c takes row tiles c, c + NC, ...; rank r streams k-blocks

@@ -1,5 +1,6 @@
-// tc_epilogue.cuh -- epilogues of the tensor-core projections (decode and prefill), shared by
-// the stream-K kernel (gemm_tc.cu) and the cluster split-K kernel (gemm_csk.cu): RMSNorm scale,
+// tc_epilogue.cuh -- epilogues of the projections (decode and prefill), shared by the prefill
+// GEMM (gemm_tc.cu), the cluster split-K decode kernel (gemm_csk.cu) and the 4-bit decode
+// kernels (gemm_q4r.cu): RMSNorm scale,
 // residual add with the next RMSNorm's statistics and operand, SwiGLU, and for QKV the RoPE
 // rotation, the K/V append and the decode attention's Q operand image.
 #pragma once
