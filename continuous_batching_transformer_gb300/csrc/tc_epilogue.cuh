@@ -1,8 +1,8 @@
 // tc_epilogue.cuh -- epilogues of the projections (decode and prefill), shared by the prefill
 // GEMM (gemm_tc.cu), the cluster split-K decode kernel (gemm_csk.cu) and the 4-bit decode
-// kernels (gemm_q4r.cu): RMSNorm scale,
-// residual add with the next RMSNorm's statistics and operand, SwiGLU, and for QKV the RoPE
-// rotation, the K/V append and the decode attention's Q operand image.
+// kernels (gemm_q4r.cu): RMSNorm scale, residual add with the next RMSNorm's statistics and
+// operand, SwiGLU, and for QKV the RoPE rotation, the K/V append (or its quantisation) and the
+// decode attention's Q operand image.
 #pragma once
 #include "kernels.h"
 #include "tc_common.cuh"
@@ -50,7 +50,8 @@ __device__ __forceinline__ float load_next_gain(const TcParams& p, int rb, int r
 }
 
 // The new K/V of a quantised-KV engine, quantised where they are produced: tile row r holds dim
-// i of a K or V head for the CNT decode rows (x[j], already rounded to bf16).  Per row j and
+// i of a K or V head for the CNT decode rows (x[j], already rounded to bf16; rows jlo <= j <
+// jhi are written).  Per row j and
 // 64-dim group: L = 2^bits - 1, scale = bf16((max - min) / L), bias = bf16(min), code =
 // clamp(rint((x - bias) / scale), 0, L) with the quotient the correctly rounded double one
 // (q0 = d / s through the group's reciprocal, then one exact-residual correction: the
