@@ -51,13 +51,12 @@ __device__ __forceinline__ float load_next_gain(const TcParams& p, int rb, int r
 
 // The new K/V of a quantised-KV engine, quantised where they are produced: tile row r holds dim
 // i of a K or V head for the CNT decode rows (x[j], already rounded to bf16; rows jlo <= j <
-// jhi are written).  Per row j and
-// 64-dim group: L = 2^bits - 1, scale = bf16((max - min) / L), bias = bf16(min), code =
-// clamp(rint((x - bias) / scale), 0, L) with the quotient the correctly rounded double one
-// (q0 = d / s through the group's reciprocal, then one exact-residual correction: the
-// reciprocal is computed once per (row, group) and the division of every element is three
-// double operations instead of one).  The codes, scale and bias go to the row's quantised slab
-// or page (kvq_jobs[j]); nothing is written in bf16.
+// jhi are written).  Per row j and 64-dim group: L = 2^bits - 1, scale = bf16((max - min) / L),
+// bias = bf16(min), code = clamp(rint((x - bias) / scale), 0, L) with the quotient the
+// correctly rounded double one (q0 = d / s through the group's reciprocal, then one
+// exact-residual correction: the reciprocal is computed once per (row, group) and the division
+// of every element is three double operations instead of one).  The codes, scale and bias go
+// to the row's quantised slab or page (kvq_jobs[j]); nothing is written in bf16.
 template <int CNT>
 __device__ __forceinline__ void kvq_append(const TcParams& p, int rb, int r, const float (&x)[CNT],
                                            float* swx, const EpiSrc& src, int jlo, int jhi) {
