@@ -365,7 +365,7 @@ def gpu_arm(args, rank: int, world: int):
             "dtype": ("bf16" if wl.shape.weight_format == "bf16" else "affine4-w/bf16")
                      + (f"/kv-affine{args.kv_bits}" if args.kv_bits in (4, 8) else ""),
             "data": "synthetic (seeded N(0,0.02) weights, seeded KV slabs and tokens)",
-            "config": {"workload": wl.name, "model": wl.shape.name, "batch_per_gpu": Bsz,
+            "config": {"workload": wl.name, "shape": wl.shape.name, "batch_per_gpu": Bsz,
                        "kv_page_tokens": args.page_tokens, "kv_bits": args.kv_bits,
                        "ctx_lengths": ctx, "parallelism": f"replicas x{world}" if world > 1 else "1 gpu",
                        "l2": "inputs larger than L2 (weights alone are %.1f GB per step)"
@@ -502,7 +502,7 @@ def reference_arm(args, rank: int):
     return {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "tok/s",
             "n_gpus": 0, "steps": done, "warmup": 0, "ms_per_step": 1e3 * t_total / done,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": wl.name, "model": wl.shape.name,
+            "data": "synthetic", "config": {"workload": wl.name, "shape": wl.shape.name,
                                             "batch_per_gpu": len(wl.context_lengths()),
                                             "kv_bits": args.kv_bits},
             "cpu_baseline": cb,
@@ -576,7 +576,7 @@ def trace_arm(args):
                                 "trace-64req-poisson2-" + ("realtime" if realtime else "t0"))
                                + ("-chunk2048" if chunk else "") + ("-prefix-share" if reuse == "share" else
                                   "-prefix-reuse" if reuse else ""),
-                   "model": shape.name, "live_cap": live_cap, "admission_chunk": chunk,
+                   "shape": shape.name, "live_cap": live_cap, "admission_chunk": chunk,
                    "kv_page_tokens": page,
                    "parallelism": "1 gpu"},
         "trace": {"requests": len(reqs), "generated_tokens": res.generated,
@@ -676,7 +676,7 @@ def prefill_arm(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16 (hi+lo operand parts)" if shape.weight_format == "bf16" else "affine4 weights",
         "data": "synthetic (seeded weights and prompt tokens)",
-        "config": {"workload": f"prefill-{len(seg_lens)}x{seg_lens[0]}", "model": shape.name,
+        "config": {"workload": f"prefill-{len(seg_lens)}x{seg_lens[0]}", "shape": shape.name,
                    "tokens_per_call": T, "parallelism": "1 gpu",
                    "l2": "weights and activations stream from HBM; no flush between calls"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
