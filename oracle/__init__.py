@@ -1,7 +1,7 @@
 """CPU oracle of the continuous-batching decode step -- TEST INFRASTRUCTURE ONLY.
 
-Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
-``bench.py`` may import this package.  It shares no code with the CUDA path
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg and
+reference arm of ``bench.py`` may import this package.  It shares no code with the CUDA path
 (``continuous_batching_transformer_gb300``); the two meet only in the seeded
 input generator ``synth``.
 
@@ -12,7 +12,12 @@ the oracle's own format and marshals calls through ctypes.
 What it computes follows the gnosis page "Continuous Decode Batching -- the
 transformer capture" (sections on forward_batch_segmented and
 decode_step_batch) and the mlx-bun batching design (greedy argmax, lowest id
-on ties).  Pins: ``tests/test_oracle_pins.py``.
+on ties).  Pins: ``tests/test_oracle_pins.py`` -- every component (RMSNorm,
+RoPE, attention, SwiGLU, the projections, the quantisers, argmax) against closed
+forms, hand examples and library routines, and the whole model against an fp64
+composition of library routines and the pages' invariants.  The pages print no
+worked example with values, so the end-to-end logits of the full model are
+parity unpinned beyond those pins and invariants.
 """
 from __future__ import annotations
 
